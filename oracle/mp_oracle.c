@@ -1,0 +1,265 @@
+/*
+ * mp_oracle.c -- plain, slow, single-threaded CPU oracle for the MoE
+ * expert-parallel layout / dispatch / combine path and the variable-size
+ * reduce-scatterv / all-gatherv packing.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls
+ * it.  Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared.
+ * (-ffp-contract=off keeps every float add a separate IEEE binary32 add.)
+ *
+ * Sources followed (cited by page title and section):
+ *  [EP]  "MSCCLPP EP implementation" (microsoft/mscclpp pull request #852):
+ *        the port description (get_dispatch_layout computes counts and
+ *        token-in-rank; intranode_dispatch / intranode_combine), the
+ *        commit note on the bench byte accounting (the receive buffer holds
+ *        one row per (token, source rank) pair) and the commit note that
+ *        combine runs in the reverse direction of dispatch.
+ *  [AGV] "Add pynccl all-gatherv and reducescatterv" (vllm-project/vllm pull
+ *        request #20154): the all_gather / reduce_scatter code under review
+ *        (per-root split along dim 0, offsets are running sums of sizes).
+ *
+ * Where the pages leave a step open, the readings below are used (each is
+ * listed again in the design notes of the repository):
+ *  - receive rows are ordered by destination rank, then source rank
+ *    ascending, then token ascending; a token appears once per destination
+ *    rank that owns at least one of its experts;
+ *  - expert e lives on rank e / (E/R); topk_idx == -1 is a masked entry;
+ *  - recv_topk_idx holds the local expert id (e - d*E/R) or -1 when the
+ *    expert is not on the destination; recv_topk_weights holds the weight
+ *    or 0.0f;
+ *  - combine is the unweighted sum of a token's returned rows, accumulated
+ *    in fp32 from +0.0f in ascending destination-rank order and rounded to
+ *    bf16 once, round-to-nearest-even;
+ *  - reduce-scatterv sums the R inputs in fp32 in ascending rank order and
+ *    rounds once; all-gatherv concatenates the shards in rank order.
+ *
+ * Status bits returned (same meaning as the library's):
+ *   8 = expert id outside [-1, E);  4 = receive capacity exceeded;
+ *   1 = invalid argument.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BAD_ARG 1
+#define ORC_CAPACITY 4
+#define ORC_BAD_EXPERT 8
+
+/* ------------------------------------------------------------------ */
+/* bf16 <-> binary32, from the IEEE-754 formats.                        */
+/* bf16 is the top half of a binary32: widening is a 16-bit shift.      */
+/* ------------------------------------------------------------------ */
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Narrowing keeps the top 16 bits and rounds on the 16 dropped bits:
+ * above half -> up, below half -> down, exactly half -> to the even
+ * (low bit 0) neighbour.  A carry out of the mantissa moves into the
+ * exponent, which is what IEEE rounding wants (and reaches infinity from
+ * the largest finite values).  NaN stays NaN: sign and payload top bits
+ * kept, quiet bit forced so truncation cannot turn it into infinity. */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t exp_bits = u & 0x7f800000u, man_bits = u & 0x007fffffu;
+  if (exp_bits == 0x7f800000u && man_bits != 0u)
+    return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t kept = u >> 16;
+  uint32_t dropped = u & 0xffffu;
+  const uint32_t half = 0x8000u;
+  if (dropped > half || (dropped == half && (kept & 1u))) kept += 1u;
+  return (uint16_t)kept;
+}
+
+/* ------------------------------------------------------------------ */
+/* Layout [EP, get_dispatch_layout: "counts + token-in-rank"].          */
+/*   num_tokens_per_expert[s][e] = #(t,k) with topk_idx[s][t][k] == e   */
+/*   is_token_in_rank[s][t]      = bit d set iff some k has its expert  */
+/*                                 on rank d                            */
+/*   num_tokens_per_rank[s][d]   = #t with bit d set                    */
+/* ------------------------------------------------------------------ */
+int oracle_layout(int R, int N, int K, int E, const int32_t *topk_idx,
+                  int32_t *num_tokens_per_rank, int32_t *num_tokens_per_expert,
+                  uint32_t *is_token_in_rank) {
+  if (R < 1 || R > 32 || N < 0 || K < 1 || E < R || E % R != 0) return ORC_BAD_ARG;
+  const int El = E / R;
+  int status = 0;
+  for (int64_t i = 0; i < (int64_t)R * R; ++i) num_tokens_per_rank[i] = 0;
+  for (int64_t i = 0; i < (int64_t)R * E; ++i) num_tokens_per_expert[i] = 0;
+  for (int s = 0; s < R; ++s) {
+    for (int t = 0; t < N; ++t) {
+      uint32_t mask = 0u;
+      for (int k = 0; k < K; ++k) {
+        int32_t e = topk_idx[((int64_t)s * N + t) * K + k];
+        if (e == -1) continue; /* masked entry */
+        if (e < -1 || e >= E) { status |= ORC_BAD_EXPERT; continue; }
+        num_tokens_per_expert[(int64_t)s * E + e] += 1;
+        mask |= 1u << (e / El);
+      }
+      is_token_in_rank[(int64_t)s * N + t] = mask;
+      for (int d = 0; d < R; ++d)
+        if ((mask >> d) & 1u) num_tokens_per_rank[(int64_t)s * R + d] += 1;
+    }
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------ */
+/* Dispatch [EP, intranode_dispatch; receive rows "one row per (token,  */
+/* source rank) pair"].  Rows are appended in the literal loop order    */
+/* for d, for s, for t -- that loop *is* the ordering definition.       */
+/* Outputs besides the rows:                                            */
+/*   dest_offsets[d]   first row of destination d; dest_offsets[R] =    */
+/*                     total rows                                       */
+/*   rank_prefix[s][d] rows that destination d received from ranks < s  */
+/*   num_recv_tokens_per_expert[d][j] = #(s,t,k) with expert d*El+j     */
+/*   send_row[s][t][d] row of (s,t) at d, or -1 (not sent / no room)    */
+/* row_bytes is the payload size of one token row (bf16: 2H, e4m3: H);  */
+/* scales_per_row floats of x_scales travel with each row (0 = none).   */
+/* ------------------------------------------------------------------ */
+int oracle_dispatch(int R, int N, int K, int E, int64_t row_bytes, int scales_per_row,
+                    const uint8_t *x, const float *x_scales, const int32_t *topk_idx,
+                    const float *topk_weights, const uint32_t *is_token_in_rank,
+                    int64_t recv_capacity, uint8_t *recv_x, float *recv_scales,
+                    int32_t *recv_src_rank, int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                    float *recv_topk_weights, int32_t *dest_offsets, int32_t *rank_prefix,
+                    int32_t *num_recv_tokens_per_expert, int32_t *send_row) {
+  if (R < 1 || R > 32 || N < 0 || K < 1 || E < R || E % R != 0 || row_bytes < 0 ||
+      scales_per_row < 0 || recv_capacity < 0)
+    return ORC_BAD_ARG;
+  const int El = E / R;
+  int status = 0;
+  for (int64_t i = 0; i < (int64_t)R * N * R; ++i) send_row[i] = -1;
+
+  int64_t row = 0;
+  for (int d = 0; d < R; ++d) {
+    dest_offsets[d] = (int32_t)row;
+    for (int s = 0; s < R; ++s) {
+      rank_prefix[(int64_t)s * R + d] = (int32_t)(row - dest_offsets[d]);
+      for (int t = 0; t < N; ++t) {
+        const int64_t tok = (int64_t)s * N + t;
+        if (!((is_token_in_rank[tok] >> d) & 1u)) continue;
+        if (row >= recv_capacity) { status |= ORC_CAPACITY; row += 1; continue; }
+        memcpy(recv_x + row * row_bytes, x + tok * row_bytes, (size_t)row_bytes);
+        for (int c = 0; c < scales_per_row; ++c)
+          recv_scales[row * scales_per_row + c] = x_scales[tok * scales_per_row + c];
+        recv_src_rank[row] = s;
+        recv_src_idx[row] = t;
+        for (int k = 0; k < K; ++k) {
+          int32_t e = topk_idx[tok * K + k];
+          int local = (e >= d * El && e < (d + 1) * El);
+          recv_topk_idx[row * K + k] = local ? e - d * El : -1;
+          recv_topk_weights[row * K + k] = local ? topk_weights[tok * K + k] : 0.0f;
+        }
+        send_row[tok * R + d] = (int32_t)row;
+        row += 1;
+      }
+    }
+  }
+  dest_offsets[R] = (int32_t)row;
+
+  for (int64_t i = 0; i < (int64_t)E; ++i) num_recv_tokens_per_expert[i] = 0;
+  for (int64_t i = 0; i < (int64_t)R * N * K; ++i) {
+    int32_t e = topk_idx[i];
+    if (e >= 0 && e < E) num_recv_tokens_per_expert[e] += 1; /* [d][j] = e */
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------ */
+/* Combine [EP, intranode_combine: the reverse of dispatch].            */
+/*   out[s][t][h] = bf16( sum over d = 0..R-1 ascending, send_row >= 0, */
+/*                        of float(y[send_row[s][t][d]][h]) )           */
+/* accumulated in binary32 starting at +0.0f, rounded once.             */
+/* ------------------------------------------------------------------ */
+int oracle_combine(int R, int N, int H, const uint16_t *y, int64_t y_rows,
+                   const int32_t *send_row, uint16_t *out) {
+  if (R < 1 || R > 32 || N < 0 || H < 0 || y_rows < 0) return ORC_BAD_ARG;
+  int status = 0;
+  float *acc = (float *)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+  if (!acc) return ORC_BAD_ARG;
+  for (int s = 0; s < R; ++s) {
+    for (int t = 0; t < N; ++t) {
+      const int64_t tok = (int64_t)s * N + t;
+      for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+      for (int d = 0; d < R; ++d) {
+        int32_t r = send_row[tok * R + d];
+        if (r < 0) continue;
+        if ((int64_t)r >= y_rows) { status |= ORC_CAPACITY; continue; }
+        const uint16_t *src = y + (int64_t)r * H;
+        for (int h = 0; h < H; ++h) acc[h] = acc[h] + oracle_bf16_to_f32(src[h]);
+      }
+      uint16_t *dst = out + tok * H;
+      for (int h = 0; h < H; ++h) dst[h] = oracle_f32_to_bf16(acc[h]);
+    }
+  }
+  free(acc);
+  return status;
+}
+
+/* ------------------------------------------------------------------ */
+/* Reduce-scatterv [AGV, reduce_scatter with sizes: one reduce per      */
+/* root r over rows [off_r, off_r + sizes[r]) of every rank's input].   */
+/*   in  bf16 [R][S][H] (rank q's full input at q*S*H), S = sum(sizes)  */
+/*   out bf16 [S][H]; rank r's shard is rows [off_r, off_r + sizes[r])  */
+/*   out = bf16( sum over q ascending of float(in[q]) ), from +0.0f     */
+/* ------------------------------------------------------------------ */
+int oracle_reducescatterv(int R, int H, const int64_t *sizes, const uint16_t *in,
+                          uint16_t *out) {
+  if (R < 1 || H < 0) return ORC_BAD_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return ORC_BAD_ARG;
+    S += sizes[r];
+  }
+  int64_t off = 0;
+  for (int r = 0; r < R; ++r) {
+    for (int64_t i = off; i < off + sizes[r]; ++i) {
+      for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int q = 0; q < R; ++q)
+          acc = acc + oracle_bf16_to_f32(in[((int64_t)q * S + i) * H + h]);
+        out[i * H + h] = oracle_f32_to_bf16(acc);
+      }
+    }
+    off += sizes[r];
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* All-gatherv [AGV, all_gather with sizes: one broadcast per root r of */
+/* its sizes[r] rows into rows [off_r, off_r + sizes[r]) of everyone's  */
+/* output].                                                             */
+/*   in  [S][row_bytes] -- shard r at rows [off_r, off_r + sizes[r])    */
+/*   out [R][S][row_bytes] -- logical rank q's gathered copy at q*S     */
+/* ------------------------------------------------------------------ */
+int oracle_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const uint8_t *in,
+                      uint8_t *out) {
+  if (R < 1 || row_bytes < 0) return ORC_BAD_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return ORC_BAD_ARG;
+    S += sizes[r];
+  }
+  for (int q = 0; q < R; ++q) {
+    int64_t off = 0;
+    for (int r = 0; r < R; ++r) {
+      for (int64_t i = off; i < off + sizes[r]; ++i)
+        memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes, (size_t)row_bytes);
+      off += sizes[r];
+    }
+  }
+  return 0;
+}
+
+/* Element-wise binary32 -> bf16 narrowing over an array (used by pins). */
+void oracle_f32_to_bf16_array(int64_t n, const float *in, uint16_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
+}

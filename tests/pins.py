@@ -1,0 +1,347 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function takes one compiled oracle (``oracle.OracleLib``) and
+raises AssertionError when the oracle disagrees with what the pages and the
+mathematics fix: the hand-worked fixtures under ``tests/golden/``, brute
+force over tiny inputs written with sets and sorting (not the oracle's
+append loop), closed forms, special cases and library routines (torch's own
+float -> bf16 rounding).  ``test_oracle_pins.py`` runs them on the oracle;
+``test_oracle_mutants.py`` runs them on copies of the oracle with a planted
+mistake and checks that at least one pin fails for every mistake.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+from collections import Counter
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from combine_mp_layout_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _bits(a) -> np.ndarray:
+    """float values -> bf16 bit patterns through torch's conversion (a library routine)."""
+    return wl.bf16_bits(torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def _f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def load(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# bf16 conversions against torch's conversion routines
+# --------------------------------------------------------------------------
+def pin_bf16_rounding(orc) -> None:
+    rng = np.random.default_rng(11)
+    # random binary32 bit patterns over the whole finite range
+    u = rng.integers(0, 2**32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    f = u.view(np.float32)
+    f = f[np.isfinite(f)]
+    # exact ties with odd and even kept halves, values next to ties, subnormals,
+    # zeros, the largest finite values and the overflow boundary
+    kept = rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint32)
+    ties = ((kept << 16) | 0x8000).view(np.float32)
+    near = np.concatenate([((kept << 16) | 0x7fff), ((kept << 16) | 0x8001)]).view(np.float32)
+    special = np.array([0.0, -0.0, 1.0, -1.0, 1.00390625, 1.01171875, 3.4028235e38,
+                        -3.4028235e38, 3.3961775e38, 1e-40, -1e-40, 1.4e-45, 2.0**-126,
+                        65504.0, 0.1, 1.0 / 3.0], np.float32)
+    allv = np.concatenate([f, ties[np.isfinite(ties)], near[np.isfinite(near)], special])
+    got = orc.f32_to_bf16_array(allv)
+    want = _bits(allv)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, "bf16 narrowing differs from torch at %r" % (allv[bad[:5]],)
+    # NaN stays NaN
+    nan_bits = orc.f32_to_bf16_array(np.array([np.nan, -np.nan], np.float32))
+    assert all(((int(b) & 0x7f80) == 0x7f80 and (int(b) & 0x7f) != 0) for b in nan_bits)
+    # widening is exact: compare with torch's bf16 -> fp32
+    b = rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint16)
+    tw = torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    ow = np.array([orc.bf16_to_f32(int(v)) for v in b], np.float32)
+    fin = np.isfinite(tw)
+    assert np.array_equal(ow[fin].view(np.uint32), tw[fin].view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# layout / dispatch: hand-worked fixture and brute force
+# --------------------------------------------------------------------------
+def pin_ep_hand_fixture(orc) -> None:
+    g = load("ep_hand_r2.json")
+    E, ex = g["E"], g["expect"]
+    idx = np.array(g["topk_idx"], np.int32)
+    w = np.array(g["topk_weights"], np.float32)
+    x = _bits(g["x"])
+    ntpr, ntpe, mask, st = orc.layout(idx, E)
+    assert st == 0
+    assert ntpr.tolist() == ex["num_tokens_per_rank"]
+    assert ntpe.tolist() == ex["num_tokens_per_expert"]
+    assert mask.tolist() == ex["is_token_in_rank"]
+    out, st = orc.dispatch(x, idx, w, mask, E)
+    assert st == 0
+    for key in ("dest_offsets", "rank_prefix", "num_recv_tokens_per_expert", "send_row",
+                "recv_src_rank", "recv_src_idx", "recv_topk_idx"):
+        assert out[key].tolist() == ex[key], key
+    assert out["recv_topk_weights"].tolist() == ex["recv_topk_weights"]
+    assert np.array_equal(out["recv_x"], _bits(ex["recv_x"]))
+    comb, st = orc.combine(out["recv_x"], out["send_row"])
+    assert st == 0 and np.array_equal(comb, _bits(ex["combine_of_recv_x"]))
+    comb, st = orc.combine(_bits(ex["y"]), out["send_row"])
+    assert st == 0 and np.array_equal(comb, _bits(ex["combine_of_y"]))
+
+
+def brute_force_ep(topk_idx: np.ndarray, topk_weights: np.ndarray, E: int):
+    """Independent formulation: experts as sets, rows as a sorted list of
+    (dest, src, token) triples, counts with Counter."""
+    R, N, K = topk_idx.shape
+    El = E // R
+    owner = {e: e // El for e in range(E)}
+    triples, ntpe, ntpr, masks = [], {}, {}, {}
+    for s in range(R):
+        ce = Counter(int(e) for e in topk_idx[s].reshape(-1) if 0 <= e < E)
+        ntpe[s] = [ce.get(e, 0) for e in range(E)]
+        cr = Counter()
+        for t in range(N):
+            ranks = {owner[int(e)] for e in topk_idx[s, t] if 0 <= e < E}
+            masks[(s, t)] = ranks
+            cr.update(ranks)
+            triples.extend((d, s, t) for d in ranks)
+        ntpr[s] = [cr.get(d, 0) for d in range(R)]
+    triples.sort()
+    pos = {tr: i for i, tr in enumerate(triples)}
+    return triples, pos, ntpe, ntpr, masks
+
+
+def check_ep_against_brute(orc, topk_idx, topk_weights, E, x=None) -> None:
+    R, N, K = topk_idx.shape
+    El = E // R
+    triples, pos, ntpe, ntpr, masks = brute_force_ep(topk_idx, topk_weights, E)
+    o_ntpr, o_ntpe, o_mask, st = orc.layout(topk_idx, E)
+    assert st == 0
+    assert o_ntpe.tolist() == [ntpe[s] for s in range(R)]
+    assert o_ntpr.tolist() == [ntpr[s] for s in range(R)]
+    for (s, t), ranks in masks.items():
+        assert {d for d in range(R) if (int(o_mask[s, t]) >> d) & 1} == ranks
+    if x is None:
+        x = np.arange(R * N * 8, dtype=np.uint16).reshape(R, N, 8)
+    out, st = orc.dispatch(x, topk_idx, topk_weights, o_mask, E)
+    assert st == 0
+    T = len(triples)
+    assert out["num_recv"] == T and out["dest_offsets"][R] == T
+    for d in range(R):
+        first = next((i for i, tr in enumerate(triples) if tr[0] >= d), T)
+        assert out["dest_offsets"][d] == first
+        for s in range(R):
+            before = sum(1 for tr in triples if tr[0] == d and tr[1] < s)
+            assert out["rank_prefix"][s, d] == before
+    for i, (d, s, t) in enumerate(triples):
+        assert out["recv_src_rank"][i] == s and out["recv_src_idx"][i] == t
+        assert np.array_equal(out["recv_x"][i], x[s, t])
+        for k in range(K):
+            e = int(topk_idx[s, t, k])
+            on_d = e in set(range(d * El, (d + 1) * El))
+            assert out["recv_topk_idx"][i, k] == (e - d * El if on_d else -1)
+            assert out["recv_topk_weights"][i, k] == (topk_weights[s, t, k] if on_d else 0.0)
+    for s, t, d in itertools.product(range(R), range(N), range(R)):
+        assert out["send_row"][s, t, d] == pos.get((d, s, t), -1)
+    allc = Counter(int(e) for e in topk_idx.reshape(-1) if 0 <= e < E)
+    assert out["num_recv_tokens_per_expert"].reshape(-1).tolist() == [allc.get(e, 0) for e in range(E)]
+
+
+def pin_ep_brute_force(orc) -> None:
+    rng = np.random.default_rng(3)
+    for R, N, El, K in [(1, 5, 3, 2), (2, 7, 2, 3), (3, 6, 2, 4), (4, 9, 1, 3), (4, 4, 3, 12),
+                        (3, 8, 4, 1)]:
+        E = R * El
+        idx = wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)
+        # mask some entries (-1), including whole tokens
+        m = rng.random(idx.shape) < 0.15
+        idx = np.where(m, -1, idx).astype(np.int32)
+        if N > 2:
+            idx[0, 1, :] = -1
+        w = rng.random(idx.shape).astype(np.float32)
+        check_ep_against_brute(orc, idx, w, E)
+
+
+def pin_ep_invariants(orc) -> None:
+    """Invariants on a moderate random case (uniform and skewed routing)."""
+    for name, over in [("tiny", {}), ("skew", dict(N=64, H=8)), ("dsv3", dict(N=32, H=8))]:
+        inp = wl.make_ep(name, seed=5, **over)
+        R, N, K, E = inp.R, inp.N, inp.K, inp.E
+        idx = inp.topk_idx.copy()
+        idx[:, ::7, 0] = -1
+        ntpr, ntpe, mask, st = orc.layout(idx, E)
+        assert st == 0
+        masked = int((idx == -1).sum())
+        assert int(ntpe.sum()) == R * N * K - masked
+        pop = np.unpackbits(mask.view(np.uint8)).sum()
+        assert int(ntpr.sum()) == int(pop)
+        x = np.arange(R * N * 4, dtype=np.int32).reshape(R, N, 4)
+        out, st = orc.dispatch(x, idx, inp.topk_weights, mask, E)
+        assert st == 0
+        T = out["num_recv"]
+        assert int(out["dest_offsets"][-1]) == T == int(ntpr.sum())
+        assert np.all(np.diff(out["dest_offsets"]) == ntpr.sum(axis=0))
+        keys = list(zip(out["recv_src_rank"].tolist(), out["recv_src_idx"].tolist()))
+        dest = np.searchsorted(out["dest_offsets"], np.arange(T), side="right") - 1
+        trip = list(zip(dest.tolist(), *zip(*keys))) if T else []
+        assert trip == sorted(trip) and len(set(trip)) == T
+        assert np.array_equal(out["recv_x"], x[out["recv_src_rank"], out["recv_src_idx"]])
+        El = E // R
+        assert out["num_recv_tokens_per_expert"].sum() == int(ntpe.sum())
+        assert np.array_equal(out["num_recv_tokens_per_expert"].reshape(-1), ntpe.sum(axis=0))
+        # every local topk entry of a row points at a real expert of that destination
+        loc = out["recv_topk_idx"]
+        assert np.all((loc == -1) | ((loc >= 0) & (loc < El)))
+
+
+def pin_ep_special_cases(orc) -> None:
+    rng = np.random.default_rng(9)
+    # R = 1: dispatch is the identity on tokens with an expert; combine gives them back
+    idx = wl.topk_uniform(rng, 10, 4, 2).reshape(1, 10, 2)
+    idx[0, 3] = -1
+    w = rng.random(idx.shape).astype(np.float32)
+    x = _bits(rng.standard_normal((1, 10, 8)))
+    _, _, mask, _ = orc.layout(idx, 4)
+    out, st = orc.dispatch(x, idx, w, mask, 4)
+    keep = [t for t in range(10) if t != 3]
+    assert st == 0 and np.array_equal(out["recv_x"], x[0, keep])
+    comb, _ = orc.combine(out["recv_x"], out["send_row"])
+    assert np.array_equal(comb[0, keep], x[0, keep]) and not comb[0, 3].any()
+    # K = E: every token goes to every rank, R*N*R rows
+    R, N, E = 3, 4, 6
+    idx = np.tile(np.arange(E, dtype=np.int32), (R, N, 1))
+    _, ntpe, mask, _ = orc.layout(idx, E)
+    assert np.all(mask == (1 << R) - 1) and np.all(ntpe == N)
+    out, _ = orc.dispatch(np.zeros((R, N, 8), np.uint16), idx, np.ones(idx.shape, np.float32),
+                          mask, E)
+    assert out["num_recv"] == R * N * R
+    # everything masked: no rows, zero counts, combine gives +0 rows
+    idx = np.full((2, 5, 3), -1, np.int32)
+    ntpr, ntpe, mask, st = orc.layout(idx, 4)
+    assert st == 0 and not ntpr.any() and not ntpe.any() and not mask.any()
+    out, st = orc.dispatch(np.ones((2, 5, 8), np.uint16), idx, np.ones(idx.shape, np.float32),
+                           mask, 4)
+    assert st == 0 and out["num_recv"] == 0 and np.all(out["send_row"] == -1)
+    comb, _ = orc.combine(np.zeros((1, 8), np.uint16), out["send_row"])
+    assert not comb.any()
+    # bad expert ids are flagged and ignored
+    idx = np.array([[[0, 9], [-3, 1]]], np.int32)
+    ntpr, ntpe, mask, st = orc.layout(idx, 2)
+    assert st & 8 and mask.tolist() == [[1, 1]] and ntpe.tolist() == [[1, 1]]
+    # receive capacity: rows past it are not written and their send_row is -1
+    idx = np.array([[[0], [1], [0]], [[1], [0], [1]]], np.int32)
+    _, _, mask, _ = orc.layout(idx, 2)
+    x = np.arange(2 * 3 * 8, dtype=np.uint16).reshape(2, 3, 8)
+    out, st = orc.dispatch(x, idx, np.ones(idx.shape, np.float32), mask, 2, recv_capacity=4)
+    assert st & 4 and out["num_recv"] == 6
+    assert int((out["send_row"] >= 0).sum()) == 4 and out["send_row"].max() == 3
+
+
+# --------------------------------------------------------------------------
+# combine / reduce-scatterv sums
+# --------------------------------------------------------------------------
+def pin_sum_order_fixture(orc) -> None:
+    g = load("sum_order_r3.json")
+    rows = _bits(g["rows_in_rank_order"])          # [3][8]
+    want = np.array([int(h, 16) for h in g["expect_bf16_bits"]], np.uint16)
+    # as a combine: one token of source rank 0 sent to ranks 0, 1, 2 (rows 0, 1, 2)
+    send_row = np.full((3, 1, 3), -1, np.int32)
+    send_row[0, 0] = [0, 1, 2]
+    out, st = orc.combine(rows, send_row)
+    assert st == 0 and np.array_equal(out[0, 0], want), out[0, 0]
+    assert not out[1:].any()
+    # as a reduce-scatterv: rank q's one-row input is row q; the row is rank 1's shard
+    out, st = orc.reducescatterv(rows.reshape(3, 1, 8), [0, 1, 0])
+    assert st == 0 and np.array_equal(out[0], want)
+
+
+def pin_combine_closed_forms(orc) -> None:
+    rng = np.random.default_rng(21)
+    inp = wl.make_ep("dsv3", seed=2, N=48, H=64)
+    R, N, E = inp.R, inp.N, inp.E
+    idx = inp.topk_idx.copy()
+    idx[1, 5] = -1
+    _, _, mask, _ = orc.layout(idx, E)
+    x = wl.bf16_bits(inp.x)
+    out, _ = orc.dispatch(x, idx, inp.topk_weights, mask, E)
+    # combine of an un-modified dispatch is bf16(c * x), c = number of destination
+    # ranks (c*x is exact in fp32 for bf16 x and c <= 32; one rounding by torch)
+    c = np.unpackbits(mask.view(np.uint8).reshape(R, N, 4), axis=-1).sum(-1).astype(np.float32)
+    want = _bits(_f32(x) * c[..., None])
+    want[c == 0] = 0  # no destination: the +0.0 start value, not 0 * x (which may be -0)
+    comb, st = orc.combine(out["recv_x"], out["send_row"])
+    assert st == 0 and np.array_equal(comb, want)
+    # small-integer rows: every fp32 partial sum is exact, so the result is the
+    # exact integer sum (|sum| <= 8*16 fits bf16's 8 significant bits)
+    T = out["num_recv"]
+    yi = rng.integers(-16, 17, size=(T, 64)).astype(np.float32)
+    comb, _ = orc.combine(_bits(yi), out["send_row"])
+    exact = np.zeros((R, N, 64), np.float64)
+    for s, t, d in itertools.product(range(R), range(N), range(R)):
+        r = out["send_row"][s, t, d]
+        if r >= 0:
+            exact[s, t] += yi[r]
+    assert np.array_equal(_f32(comb), exact.astype(np.float32))
+    # random rows: within the fp32 recursive-summation bound of the exact sum
+    # plus half a bf16 ulp of the final rounding
+    yr = rng.standard_normal((T, 64)).astype(np.float32)
+    yb = _bits(yr)
+    yv = _f32(yb).astype(np.float64)
+    comb, _ = orc.combine(yb, out["send_row"])
+    got = _f32(comb).astype(np.float64)
+    for s, t in itertools.product(range(R), range(N)):
+        rows = [r for r in out["send_row"][s, t] if r >= 0]
+        if not rows:
+            assert not comb[s, t].any()
+            continue
+        for h in range(0, 64, 7):
+            vals = [Fraction(float(yv[r, h])) for r in rows]
+            ex = float(sum(vals, Fraction(0)))
+            absum = float(sum(abs(v) for v in vals))
+            bound = (len(rows) - 1) * 2.0**-24 * absum * 1.01 + 2.0**-8 * abs(ex) * 1.01 + 1e-30
+            assert abs(got[s, t, h] - ex) <= bound, (s, t, h, got[s, t, h], ex)
+
+
+def pin_rsv_agv(orc) -> None:
+    rng = np.random.default_rng(33)
+    R, H = 8, 16
+    sizes = [3, 0, 5, 1, 0, 2, 4, 1]
+    S = sum(sizes)
+    shard = _bits(rng.standard_normal((S, H)))
+    # all-gatherv: every logical rank's output is the shards concatenated in rank order
+    ag, st = orc.allgatherv(shard, sizes, R)
+    assert st == 0 and ag.shape == (R, S, H)
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    for q, r in itertools.product(range(R), range(R)):
+        assert np.array_equal(ag[q, off[r]:off[r + 1]], shard[off[r]:off[r + 1]])
+    # round trip: reduce-scatterv of the gathered copies is bf16(R * shard), exact for R = 8
+    rs, st = orc.reducescatterv(ag, sizes)
+    assert st == 0 and np.array_equal(rs, _bits(_f32(shard) * np.float32(R)))
+    # small integers: exact sums
+    xi = rng.integers(-16, 17, size=(R, S, H)).astype(np.float32)
+    rs, _ = orc.reducescatterv(_bits(xi), sizes)
+    assert np.array_equal(_f32(rs), xi.sum(0, dtype=np.float64).astype(np.float32))
+    # random: within the summation bound
+    xr = _f32(_bits(rng.standard_normal((R, S, H)))).astype(np.float64)
+    rs, _ = orc.reducescatterv(_bits(xr), sizes)
+    ex = np.array([[math.fsum(xr[:, i, h]) for h in range(H)] for i in range(S)])
+    bound = (R - 1) * 2.0**-24 * np.abs(xr).sum(0) * 1.01 + 2.0**-8 * np.abs(ex) * 1.01 + 1e-30
+    assert np.all(np.abs(_f32(rs) - ex) <= bound)
+    # empty shards everywhere: nothing to do
+    rs, st = orc.reducescatterv(np.zeros((3, 0, 8), np.uint16), [0, 0, 0])
+    assert st == 0 and rs.shape == (0, 8)
+
+
+ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
+            pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv]

@@ -1,0 +1,71 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check
+that the pins catch every one of them: a dropped term, a wrong index or
+sign, a reversed loop, a wrong start value, a different rounding.
+
+Each mutant is one textual replacement in a temporary copy of
+``oracle/mp_oracle.c``; the copy is compiled with the oracle's own flags and
+loaded next to the real one.  Mutants are chosen so that none of them
+writes outside its buffers.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import pins
+
+MUTANTS = {
+    "round_half_up": ("if (dropped > half ||", "if (dropped >= half ||"),
+    "ties_to_odd": ("(dropped == half && (kept & 1u))", "(dropped == half && !(kept & 1u))"),
+    "widen_wrong_shift": ("((uint32_t)b) << 16", "((uint32_t)b) << 15"),
+    "owner_round_robin": ("mask |= 1u << (e / El);", "mask |= 1u << (e % R);"),
+    "expert_count_mirrored": ("num_tokens_per_expert[(int64_t)s * E + e] += 1;",
+                              "num_tokens_per_expert[(int64_t)s * E + (E - 1 - e)] += 1;"),
+    "masked_counts_as_rank0": ("if (e == -1) continue; /* masked entry */",
+                               "if (e == -1) { mask |= 1u; continue; }"),
+    "tokens_descending": ("for (int t = 0; t < N; ++t) {\n        const int64_t tok = (int64_t)s * N + t;\n        if (!((is_token_in_rank",
+                          "for (int t = N - 1; t >= 0; --t) {\n        const int64_t tok = (int64_t)s * N + t;\n        if (!((is_token_in_rank"),
+    "global_expert_ids": ("local ? e - d * El : -1", "local ? e : -1"),
+    "nonlocal_weight_kept": ("local ? topk_weights[tok * K + k] : 0.0f", "topk_weights[tok * K + k]"),
+    "rank_prefix_absolute": ("(int32_t)(row - dest_offsets[d])", "(int32_t)(row)"),
+    "src_idx_off_by_one": ("recv_src_idx[row] = t;", "recv_src_idx[row] = t + 1;"),
+    "recv_expert_count_shifted": ("if (e >= 0 && e < E) num_recv_tokens_per_expert[e] += 1;",
+                                  "if (e >= 0 && e < E) num_recv_tokens_per_expert[(e + 1) % E] += 1;"),
+    "combine_descending": ("for (int d = 0; d < R; ++d) {\n        int32_t r = send_row",
+                           "for (int d = R - 1; d >= 0; --d) {\n        int32_t r = send_row"),
+    "combine_negative_zero_start": ("for (int h = 0; h < H; ++h) acc[h] = 0.0f;",
+                                    "for (int h = 0; h < H; ++h) acc[h] = -0.0f;"),
+    "combine_drops_first_rank": ("if (r < 0) continue;", "if (r < 0 || d == 0) continue;"),
+    "combine_in_double": ("float *acc = (float *)malloc(sizeof(float)",
+                          "double *acc = (double *)malloc(sizeof(double)"),
+    "rsv_descending": ("for (int q = 0; q < R; ++q)\n          acc = acc",
+                       "for (int q = R - 1; q >= 0; --q)\n          acc = acc"),
+    "rsv_in_double": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
+                      "        double acc = 0.0;\n        for (int q = 0; q < R; ++q)"),
+    "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
+                        "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
+}
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    with open(os.path.join(os.path.dirname(oracle.__file__), "mp_oracle.c")) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, src_text, tmp_path):
+    old, new = MUTANTS[name]
+    assert src_text.count(old) == 1, "mutation site not unique: %s" % name
+    src = tmp_path / ("mut_%s.c" % name)
+    src.write_text(src_text.replace(old, new))
+    lib = oracle.compile_oracle(str(src), str(tmp_path / ("libmut_%s.so" % name)))
+    orc = oracle.OracleLib(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+            break
+    assert caught, "no pin caught the planted mistake %r" % name
