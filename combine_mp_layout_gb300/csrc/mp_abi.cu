@@ -1,0 +1,153 @@
+// mp_abi.cu -- the C ABI declared in include/mp_layout.h: argument checks,
+// workspace sizing and the launch sequence of each call.  No allocation,
+// no synchronisation, no state kept between calls.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mp_layout.h"
+#include "mp_common.cuh"
+#include "mp_internal.h"
+
+namespace mp {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+static bool ep_shape_ok(int R, int N, int K, int E) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || K < 1 || K > MP_MAX_TOPK) return false;
+  if (E < R || E > MP_MAX_EXPERTS || E % R != 0) return false;
+  if (int64_t(R) * N * K >= (int64_t(1) << 31)) return false;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MP_OK : MP_ERR_CUDA; }
+
+}  // namespace mp
+
+using namespace mp;
+
+extern "C" {
+
+const char* mp_status_string(int status) {
+  if (status == MP_OK) return "ok";
+  if (status & MP_ERR_INVALID_ARG) return "invalid argument";
+  if (status & MP_ERR_CUDA) return "CUDA launch failed";
+  if (status & MP_ERR_CAPACITY) return "receive capacity exceeded";
+  if (status & MP_ERR_BAD_EXPERT) return "expert id outside [-1, E)";
+  if (status & MP_ERR_TIMEOUT) return "device-side wait timed out";
+  return "unknown status";
+}
+
+size_t mp_workspace_size(int R, int N, int E) {
+  if (!ep_shape_ok(R, N, 1, E)) return 0;
+  return size_t(ws_total_bytes(R, N, E));
+}
+
+int mp_layout(int R, int N, int K, int E, const int32_t* topk_idx, int32_t* num_tokens_per_rank,
+              int32_t* num_tokens_per_expert, uint32_t* is_token_in_rank, int32_t* dev_err,
+              void* workspace, mp_stream_t stream) {
+  if (!ep_shape_ok(R, N, K, E)) return MP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !dev_err || !workspace)
+    return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !is_token_in_rank)) return MP_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_rank) || !aligned4(num_tokens_per_expert) ||
+      !aligned4(is_token_in_rank) || !aligned4(dev_err) || !aligned16(workspace))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_layout(R, N, K, E, topk_idx, num_tokens_per_rank,
+                                   num_tokens_per_expert, is_token_in_rank, dev_err,
+                                   static_cast<unsigned char*>(workspace),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void* x, const float* x_scales,
+                const int32_t* topk_idx, const float* topk_weights,
+                const uint32_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
+                const int32_t* num_tokens_per_expert, int64_t recv_capacity, void* recv_x,
+                float* recv_scales, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
+                int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert, int32_t* send_row,
+                int32_t* dev_err, void* workspace, mp_stream_t stream) {
+  if (!ep_shape_ok(R, N, K, E) || H <= 0 || recv_capacity < 0) return MP_ERR_INVALID_ARG;
+  if (dtype != MP_BF16 && dtype != MP_E4M3) return MP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == MP_E4M3;
+  if (fp8 ? (H % MP_SCALE_BLOCK != 0) : (H % 8 != 0)) return MP_ERR_INVALID_ARG;
+  if (fp8 != (x_scales != nullptr) || fp8 != (recv_scales != nullptr)) return MP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !dest_offsets || !rank_prefix ||
+      !num_recv_tokens_per_expert || !dev_err || !workspace)
+    return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !topk_idx || !topk_weights || !is_token_in_rank || !send_row))
+    return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && (!recv_x || !recv_src_rank || !recv_src_idx || !recv_topk_idx ||
+                            !recv_topk_weights))
+    return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || !aligned4(x_scales) ||
+      !aligned4(recv_scales) || !aligned4(topk_idx) || !aligned4(topk_weights) ||
+      !aligned4(is_token_in_rank) || !aligned4(send_row) || !aligned4(recv_src_rank) ||
+      !aligned4(recv_src_idx) || !aligned4(recv_topk_idx) || !aligned4(recv_topk_weights))
+    return MP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                              num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                              recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                              dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                              dev_err, static_cast<unsigned char*>(workspace), st);
+  if (e != cudaSuccess) return MP_ERR_CUDA;
+  const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
+  e = launch_dispatch_copy(R, int64_t(R) * N, row_bytes, x, recv_x, recv_capacity, send_row,
+                           fp8 ? H / MP_SCALE_BLOCK : 0, x_scales, recv_scales, st);
+  return cuda_status(e);
+}
+
+int mp_combine(int R, int N, int H, const void* y, int64_t y_rows, const int32_t* send_row,
+               void* out, int32_t* dev_err, mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || H % 8 != 0 || y_rows < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (!dev_err) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!send_row || !out || (y_rows > 0 && !y))) return MP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || !aligned4(send_row) || !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(R, int64_t(R) * N, H, y, y_rows, send_row, out, dev_err,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_reducescatterv(int R, int H, const int64_t* sizes, const void* in, void* out,
+                      mp_stream_t stream) {
+  if (R < 1 || H <= 0 || H % 8 != 0 || !sizes) return MP_ERR_INVALID_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return MP_ERR_INVALID_ARG;
+    S += sizes[r];
+  }
+  if (S > 0 && (!in || !out || !aligned16(in) || !aligned16(out))) return MP_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_reducescatterv(R, S, H, in, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_allgatherv(int R, int64_t row_bytes, const int64_t* sizes, const void* in, void* out,
+                  mp_stream_t stream) {
+  if (R < 1 || row_bytes <= 0 || row_bytes % 16 != 0 || !sizes) return MP_ERR_INVALID_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return MP_ERR_INVALID_ARG;
+    S += sizes[r];
+  }
+  if (S > 0 && (!in || !out || !aligned16(in) || !aligned16(out))) return MP_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_allgatherv(R, S, row_bytes, in, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// mp_internal.h -- launchers shared between the kernel files and the C ABI.
+// Arguments are validated by the C ABI before any launcher is called.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mp {
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_layout(int R, int N, int K, int E, const int32_t* topk_idx,
+                          int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                          uint32_t* is_token_in_rank, int32_t* dev_err, unsigned char* ws,
+                          cudaStream_t stream);
+
+cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
+                        const float* topk_weights, const uint32_t* is_token_in_rank,
+                        const int32_t* num_tokens_per_rank, const int32_t* num_tokens_per_expert,
+                        int64_t recv_capacity, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
+                        int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                        int32_t* send_row, int32_t* dev_err, unsigned char* ws,
+                        cudaStream_t stream);
+
+// Copies token rows (row_bytes each, a multiple of 16) to every receive row
+// listed in send_row; scales_per_row fp32 scales travel with each row.
+cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                 void* recv_x, int64_t recv_capacity, const int32_t* send_row,
+                                 int scales_per_row,
+                                 const float* x_scales, float* recv_scales, cudaStream_t stream);
+
+cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
+                           const int32_t* send_row, void* out, int32_t* dev_err,
+                           cudaStream_t stream);
+
+cudaError_t launch_reducescatterv(int R, int64_t S, int H, const void* in, void* out,
+                                  cudaStream_t stream);
+
+cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
+                              cudaStream_t stream);
+
+}  // namespace mp

@@ -160,3 +160,11 @@ def make_rsv(name_or_cfg="rsv", seed: int = 0, **overrides) -> RSVInputs:
     x = torch.randn((R, S, H), generator=g, dtype=torch.float32).to(torch.bfloat16)
     shards = torch.randn((S, H), generator=g, dtype=torch.float32).to(torch.bfloat16)
     return RSVInputs(R, H, sizes, x, shards)
+
+
+def gathered_bf16(rows: int, H: int, seed: int, table_rows: int = 1024) -> torch.Tensor:
+    """[rows][H] bf16 synthetic expert outputs made cheaply at large sizes: each row is
+    a row of a standard-normal table picked uniformly at random (CPU)."""
+    table = random_bf16((table_rows, H), seed)
+    pick = torch.from_numpy(np.random.default_rng(seed + 17).integers(0, table_rows, rows))
+    return table.index_select(0, pick)

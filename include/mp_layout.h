@@ -1,0 +1,207 @@
+/*
+ * mp_layout.h -- C ABI of the GB300 (sm_103a) MoE expert-parallel
+ * layout / dispatch / combine path and the variable-size
+ * reduce-scatterv / all-gatherv packing.
+ *
+ * Problem statement.  R logical ranks each hold N tokens of hidden size H
+ * (x[R][N][H]) routed to K of E experts (topk_idx[R][N][K], topk_weights
+ * [R][N][K]); the E experts are split evenly, expert e living on rank
+ * e / (E/R).  All R ranks' buffers live in the memory of ONE GPU, so every
+ * step below is a single-device permutation or reduction done by this
+ * library's own CUDA kernels.
+ *
+ * Conventions shared by every entry point.
+ *  - Every pointer argument except `sizes` (host) is a DEVICE pointer.
+ *    The caller owns every buffer, including the workspace; the library
+ *    allocates nothing and keeps no state between calls.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and is asynchronous: outputs are valid once the stream
+ *    has reached the point after the call.
+ *  - The return value reports what the host can see before the launch:
+ *    MP_ERR_INVALID_ARG for an argument that fails the checks listed with
+ *    each call (nothing is launched), MP_ERR_CUDA when a launch fails.
+ *  - Errors that depend on device data are OR-ed (atomicOr) into the
+ *    caller's device word `dev_err` (int32, zero it before the first call,
+ *    read it after synchronising).  Writes are clamped so that bad data never
+ *    makes a kernel touch memory outside the buffers described here.
+ *  - Arrays are dense row-major with the shapes given in brackets.
+ *  - bf16 values are passed as their 16-bit patterns (uint16 storage),
+ *    e4m3 values as bytes (OCP FP8 E4M3 "fn" encoding; only copied).
+ *  - Kernels read their inputs with 16-byte vector loads: every payload
+ *    pointer (x, recv_x, y, out, in) must be 16-byte aligned; the index
+ *    arrays must be 4-byte aligned.
+ *
+ * Source pages, by title and section:
+ *  [EP]  "MSCCLPP EP implementation", microsoft/mscclpp pull request #852:
+ *        port scope (get_dispatch_layout, intranode_dispatch,
+ *        intranode_combine), the intranode multirank validation note, the
+ *        internode combine note (combine runs in the reverse direction of
+ *        dispatch), the bench byte-accounting notes (one receive row per
+ *        (token, source rank) pair; combine moves as many bytes as
+ *        dispatch) and the FP8 E4M3 payload with FP32 scales.
+ *  [AGV] "Add pynccl all-gatherv and reducescatterv", vllm-project/vllm pull
+ *        request #20154: all_gatherv / reduce_scatterv along dim 0 with
+ *        per-rank sizes (one broadcast / reduce per root inside an NCCL
+ *        group).
+ * Where the pages leave a choice open, the plainest reading is used; each
+ * is named at the call it affects.
+ */
+#ifndef MP_LAYOUT_H
+#define MP_LAYOUT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *mp_stream_t;
+
+/* Status bits: returned by the calls (host-visible errors) and OR-ed into
+ * the caller's device error word (data-dependent errors). */
+enum {
+  MP_OK = 0,
+  MP_ERR_INVALID_ARG = 1, /* argument check failed; nothing launched            */
+  MP_ERR_CUDA = 2,        /* a CUDA launch or attribute call failed               */
+  MP_ERR_CAPACITY = 4,    /* more receive rows than recv_capacity / y_rows        */
+  MP_ERR_BAD_EXPERT = 8,  /* topk_idx entry outside [-1, E)                       */
+  MP_ERR_TIMEOUT = 16     /* a bounded device-side wait gave up (about a second)  */
+};
+
+/* Payload element types of mp_dispatch. */
+enum { MP_BF16 = 0, MP_E4M3 = 1 };
+
+#define MP_MAX_RANKS 32     /* is_token_in_rank is one 32-bit mask per token  */
+#define MP_MAX_TOPK 32
+#define MP_MAX_EXPERTS 8192
+#define MP_SCALE_BLOCK 128  /* channels per fp32 scale of an e4m3 payload     */
+
+/* Human-readable text for one status bit (or the lowest bit set). */
+const char *mp_status_string(int status);
+
+/* Bytes of workspace that mp_layout and mp_dispatch need for R ranks, N
+ * tokens per rank and E experts (their counters, per-block partial counts
+ * and scan tile states).  The caller allocates it (device memory), fills it
+ * with zeros ONCE before the first call, and then passes the same buffer
+ * to every call of the same (R, N, E): each call leaves it zero-filled
+ * again for the next one.  Calls that share a workspace must be ordered on
+ * one stream.  Returns 0 for arguments mp_layout would reject. */
+size_t mp_workspace_size(int R, int N, int E);
+
+/*
+ * mp_layout -- [EP] get_dispatch_layout ("counts + token-in-rank").
+ *   in   topk_idx              int32 [R][N][K]; -1 marks a masked entry
+ *   out  num_tokens_per_rank   int32 [R][R]  [s][d] = #tokens of s sent to d
+ *   out  num_tokens_per_expert int32 [R][E]  [s][e] = #(t,k) of s with expert e
+ *   out  is_token_in_rank      uint32 [R][N] bit d set iff token (s,t) has an
+ *                                            expert on rank d
+ * Checks: 1 <= R <= 32, N >= 0, 1 <= K <= 32, R <= E <= 8192, E % R == 0,
+ *   R*N*K < 2^31, non-NULL pointers (topk_idx may be NULL when N == 0).
+ * Device errors: MP_ERR_BAD_EXPERT (entry < -1 or >= E; the entry is
+ *   ignored).
+ */
+int mp_layout(int R, int N, int K, int E, const int32_t *topk_idx,
+              int32_t *num_tokens_per_rank, int32_t *num_tokens_per_expert,
+              uint32_t *is_token_in_rank, int32_t *dev_err, void *workspace,
+              mp_stream_t stream);
+
+/*
+ * mp_dispatch -- [EP] intranode_dispatch: the receive offsets (a single-pass
+ * decoupled-lookback scan) and the row copy.
+ * Receive layout (reading of the pages, which fix no order): one row per
+ * (token, destination rank that owns at least one of the token's experts),
+ * ordered by destination rank, then source rank, then token, ascending.
+ *   in   x                 [R][N][H] payload, bf16 (dtype MP_BF16) or e4m3
+ *                          (MP_E4M3)
+ *   in   x_scales          fp32 [R][N][H/128] for MP_E4M3, NULL for MP_BF16
+ *   in   topk_idx, topk_weights            as given to mp_layout
+ *   in   is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert
+ *                          the outputs of mp_layout for the same topk_idx
+ *   in   recv_capacity     rows available in the receive buffers
+ *   out  recv_x            [recv_capacity][H] payload rows
+ *   out  recv_scales       fp32 [recv_capacity][H/128] (MP_E4M3; else NULL)
+ *   out  recv_src_rank, recv_src_idx   int32 [recv_capacity]: source (s, t)
+ *   out  recv_topk_idx     int32 [recv_capacity][K]: local expert id
+ *                          (e - d*E/R) when expert e is on the row's
+ *                          destination d, else -1
+ *   out  recv_topk_weights fp32 [recv_capacity][K]: the weight for a local
+ *                          expert, else 0.0f
+ *   out  dest_offsets      int32 [R+1]: first row of destination d;
+ *                          dest_offsets[R] = total rows T_recv
+ *   out  rank_prefix       int32 [R][R]: [s][d] = rows of destination d
+ *                          that come from source ranks < s
+ *   out  num_recv_tokens_per_expert int32 [R][E/R]
+ *   out  send_row          int32 [R][N][R]: [s][t][d] = receive row of token
+ *                          (s,t) at destination d, or -1 (not sent, or past
+ *                          recv_capacity); this is the handle mp_combine needs
+ * Rows past recv_capacity are not written (MP_ERR_CAPACITY).  A capacity of
+ * R*N*min(R,K) can never overflow; the exact need is dest_offsets[R]
+ * (= the sum of num_tokens_per_rank).
+ * Checks: as mp_layout, plus H > 0, H % 8 == 0 (bf16) or H % 128 == 0
+ *   (e4m3), x_scales/recv_scales non-NULL exactly for MP_E4M3,
+ *   recv_capacity >= 0, 16-byte aligned payload pointers.
+ * Device errors: MP_ERR_CAPACITY, MP_ERR_TIMEOUT (scan wait gave up),
+ *   MP_ERR_INVALID_ARG (the workspace was not zero-filled before first use).
+ */
+int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void *x,
+                const float *x_scales, const int32_t *topk_idx, const float *topk_weights,
+                const uint32_t *is_token_in_rank, const int32_t *num_tokens_per_rank,
+                const int32_t *num_tokens_per_expert, int64_t recv_capacity, void *recv_x,
+                float *recv_scales, int32_t *recv_src_rank, int32_t *recv_src_idx,
+                int32_t *recv_topk_idx, float *recv_topk_weights, int32_t *dest_offsets,
+                int32_t *rank_prefix, int32_t *num_recv_tokens_per_expert, int32_t *send_row,
+                int32_t *dev_err, void *workspace, mp_stream_t stream);
+
+/*
+ * mp_combine -- [EP] intranode_combine, the reverse of dispatch.
+ *   in   y        bf16 [y_rows][H]: one row per receive row (for example the
+ *                 expert outputs, or recv_x itself)
+ *   in   send_row int32 [R][N][R] from mp_dispatch
+ *   out  out      bf16 [R][N][H]:
+ *        out[s][t] = bf16( sum over d = 0..R-1 ascending with
+ *                          send_row[s][t][d] >= 0 of float(y[send_row[s][t][d]]) )
+ *        accumulated in fp32 starting from +0.0f, rounded once to bf16 with
+ *        round-to-nearest-even (reading of the pages, which fix neither the
+ *        order nor the precision).  The sum is unweighted; a token with no
+ *        destination gets +0.0.
+ * Checks: 1 <= R <= 32, N >= 0, H > 0, H % 8 == 0, y_rows >= 0, aligned
+ *   non-NULL pointers.
+ * Device errors: MP_ERR_CAPACITY for a send_row entry >= y_rows (skipped).
+ */
+int mp_combine(int R, int N, int H, const void *y, int64_t y_rows, const int32_t *send_row,
+               void *out, int32_t *dev_err, mp_stream_t stream);
+
+/*
+ * mp_reducescatterv -- [AGV] reduce_scatterv along dim 0 with per-rank sizes.
+ *   sizes  HOST int64 [R]: rows of rank r's shard (>= 0); S = sum(sizes),
+ *          off_r = sizes[0] + ... + sizes[r-1]
+ *   in     bf16 [R][S][H]: logical rank q's full input at in + q*S*H
+ *   out    bf16 [S][H]: rank r's shard is rows [off_r, off_r + sizes[r]),
+ *          out[i] = bf16( sum over q = 0..R-1 ascending of float(in[q][i]) ),
+ *          fp32 from +0.0f, rounded once (round-to-nearest-even).
+ * Checks: R >= 1, H > 0, H % 8 == 0, sizes non-NULL with every entry >= 0,
+ *   16-byte aligned non-NULL in/out when S > 0.
+ */
+int mp_reducescatterv(int R, int H, const int64_t *sizes, const void *in, void *out,
+                      mp_stream_t stream);
+
+/*
+ * mp_allgatherv -- [AGV] all_gatherv along dim 0 with per-rank sizes.
+ *   sizes      HOST int64 [R] as above
+ *   row_bytes  bytes of one row (any element type; a multiple of 16)
+ *   in         [S][row_bytes]: the R shards back to back, shard r at row off_r
+ *   out        [R][S][row_bytes]: logical rank q's gathered copy at
+ *              out + q*S*row_bytes; every copy is the shards in rank order.
+ * Checks: R >= 1, row_bytes > 0, row_bytes % 16 == 0, sizes entries >= 0,
+ *   16-byte aligned non-NULL in/out when S > 0.
+ */
+int mp_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const void *in, void *out,
+                  mp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MP_LAYOUT_H */

@@ -1,0 +1,310 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: bit-exact for counts, masks, offsets, send_row, receive metadata and
+copied payload bytes (bf16 and e4m3); combine / reduce-scatterv within
+1 bf16 ulp of the oracle's fp32 ascending-order sum rounded once (both sides
+use the same order and rounding, so 0 ulp is what is expected; the bar is
+the stated tolerance).  Sizes span several scan tiles / layout blocks with
+ragged tails, ragged hidden sizes, R from 1 to 32, masked entries, empty
+inputs, capacity overflow and bad expert ids; the full-size workloads run
+in the launch configuration the benchmark times.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_mp_layout_gb300 import binding as B
+from combine_mp_layout_gb300 import workloads as wl
+from combine_mp_layout_gb300.pipeline import EPPlan, RSVPlan
+from tests import pins
+
+pytestmark = pytest.mark.gpu
+
+ULP_TOL = 1  # combine / reduce-scatterv: at most 1 bf16 ulp from the oracle
+
+
+def ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in bf16 ulps between two arrays of bf16 bit patterns (ordered-integer map)."""
+    def ordered(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, 0x8000 - (b & 0x7fff), 0x8000 + b)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def assert_bf16_close(got_bits, want_bits, what):
+    d = ulp_distance(np.asarray(got_bits), np.asarray(want_bits))
+    assert d.size == 0 or int(d.max()) <= ULP_TOL, "%s: max %d ulp at %r" % (
+        what, int(d.max()), np.unravel_index(int(d.argmax()), d.shape))
+
+
+def run_gpu(inp: wl.EPInputs, recv_capacity=None, y: torch.Tensor | None = None,
+            repeat: int = 1) -> EPPlan:
+    plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H, inp.dtype, recv_capacity)
+    plan.load(inp)
+    for _ in range(repeat):
+        plan.dev_err.zero_()
+        B.check(plan.layout(), "mp_layout")
+        B.check(plan.dispatch(), "mp_dispatch")
+        B.check(plan.combine(y), "mp_combine")
+    torch.cuda.synchronize()
+    return plan
+
+
+def x_host(inp: wl.EPInputs) -> np.ndarray:
+    return wl.bf16_bits(inp.x) if inp.dtype == "bf16" else wl.u8_bits(inp.x)
+
+
+def compare_ep(inp: wl.EPInputs, plan: EPPlan, recv_capacity=None, y_bits=None,
+               expect_err: int = 0):
+    R, N, E = inp.R, inp.N, inp.E
+    ntpr, ntpe, mask, st = oracle.layout(inp.topk_idx, E)
+    xs = inp.x_scales.numpy() if inp.x_scales is not None else None
+    out, st2 = oracle.dispatch(x_host(inp), inp.topk_idx, inp.topk_weights, mask, E,
+                               x_scales=xs, recv_capacity=recv_capacity)
+    assert (st | st2) == expect_err == plan.device_error(), (st, st2, plan.device_error())
+    assert np.array_equal(plan.num_tokens_per_rank.cpu().numpy(), ntpr)
+    assert np.array_equal(plan.num_tokens_per_expert.cpu().numpy(), ntpe)
+    assert np.array_equal(plan.is_token_in_rank.cpu().numpy().view(np.uint32), mask)
+    for key in ("dest_offsets", "rank_prefix", "num_recv_tokens_per_expert", "send_row"):
+        assert np.array_equal(getattr(plan, key).cpu().numpy(), out[key]), key
+    n = min(out["num_recv"], plan.cap)
+    assert np.array_equal(plan.recv_src_rank[:n].cpu().numpy(), out["recv_src_rank"])
+    assert np.array_equal(plan.recv_src_idx[:n].cpu().numpy(), out["recv_src_idx"])
+    assert np.array_equal(plan.recv_topk_idx[:n].cpu().numpy(), out["recv_topk_idx"])
+    assert np.array_equal(plan.recv_topk_weights[:n].cpu().numpy().view(np.uint32),
+                          out["recv_topk_weights"].view(np.uint32))
+    got_x = wl.bf16_bits(plan.recv_x[:n]) if inp.dtype == "bf16" else wl.u8_bits(plan.recv_x[:n])
+    assert np.array_equal(got_x, out["recv_x"]), "recv_x bytes"
+    if xs is not None:
+        assert np.array_equal(plan.recv_scales[:n].cpu().numpy().view(np.uint32),
+                              out["recv_scales"].view(np.uint32))
+    if inp.dtype == "bf16" or y_bits is not None:
+        yb = out["recv_x"] if y_bits is None else y_bits
+        comb, st3 = oracle.combine(yb, out["send_row"])
+        assert st3 == 0
+        assert_bf16_close(wl.bf16_bits(plan.out), comb, "combine")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# small and fuzzed shapes
+# ---------------------------------------------------------------------------
+def test_tiny_config():
+    inp = wl.make_ep("tiny", seed=0)
+    compare_ep(inp, run_gpu(inp))
+
+
+def test_hand_fixture_on_gpu():
+    g = pins.load("ep_hand_r2.json")
+    ex = g["expect"]
+    R, N, E, K = g["R"], g["N"], g["E"], g["K"]
+    x = torch.zeros((R, N, 8), dtype=torch.float32)
+    x[..., :2] = torch.tensor(g["x"])
+    inp = wl.EPInputs(R, N, 8, E, K, "bf16", np.array(g["topk_idx"], np.int32),
+                      np.array(g["topk_weights"], np.float32), x.to(torch.bfloat16))
+    plan = run_gpu(inp)
+    assert plan.num_tokens_per_rank.cpu().tolist() == ex["num_tokens_per_rank"]
+    assert plan.num_tokens_per_expert.cpu().tolist() == ex["num_tokens_per_expert"]
+    assert plan.is_token_in_rank.cpu().tolist() == ex["is_token_in_rank"]
+    for key in ("dest_offsets", "rank_prefix", "num_recv_tokens_per_expert", "send_row"):
+        assert getattr(plan, key).cpu().tolist() == ex[key], key
+    T = ex["dest_offsets"][-1]
+    assert plan.recv_src_rank[:T].cpu().tolist() == ex["recv_src_rank"]
+    assert plan.recv_src_idx[:T].cpu().tolist() == ex["recv_src_idx"]
+    assert plan.recv_topk_idx[:T].cpu().tolist() == ex["recv_topk_idx"]
+    assert plan.recv_topk_weights[:T].cpu().tolist() == ex["recv_topk_weights"]
+    assert plan.recv_x[:T, :2].float().cpu().tolist() == ex["recv_x"]
+    assert plan.out[..., :2].float().cpu().tolist() == ex["combine_of_recv_x"]
+    y = torch.zeros((T, 8), dtype=torch.bfloat16, device="cuda")
+    y[:, :2] = torch.tensor(ex["y"], dtype=torch.bfloat16)
+    B.check(plan.combine(y))
+    torch.cuda.synchronize()
+    assert plan.out[..., :2].float().cpu().tolist() == ex["combine_of_y"]
+
+
+def test_sum_order_fixture_on_gpu():
+    g = pins.load("sum_order_r3.json")
+    rows = torch.tensor(g["rows_in_rank_order"], dtype=torch.float32).to(torch.bfloat16).cuda()
+    want = [int(h, 16) for h in g["expect_bf16_bits"]]
+    send_row = torch.full((3, 1, 3), -1, dtype=torch.int32, device="cuda")
+    send_row[0, 0] = torch.tensor([0, 1, 2], dtype=torch.int32)
+    out = torch.full((3, 1, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.check(B.mp_combine(3, 1, 8, rows, 3, send_row, out, err))
+    rs_out = torch.full((1, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    B.check(B.mp_reducescatterv(3, 8, [0, 1, 0], rows.reshape(3, 1, 8).contiguous(), rs_out))
+    torch.cuda.synchronize()
+    assert wl.bf16_bits(out[0, 0]).tolist() == want
+    assert not wl.bf16_bits(out[1:]).any()
+    assert wl.bf16_bits(rs_out[0]).tolist() == want
+    assert int(err.item()) == 0
+
+
+FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
+    (1, 100, 4, 2, 64),
+    (2, 257, 8, 2, 136),
+    (3, 300, 12, 3, 264),
+    (4, 513, 16, 4, 8),
+    (5, 257, 20, 6, 1032),
+    (8, 1000, 64, 8, 520),
+    (16, 130, 32, 3, 96),
+    (32, 40, 64, 8, 16),
+    (7, 777, 28, 28, 24),   # K = E: every token to every rank
+]
+
+
+@pytest.mark.parametrize("shape", FUZZ, ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
+def test_fuzz_shapes(shape):
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"),
+                     seed=R * 1000 + N)
+    if K < E:  # mask some entries and a few whole tokens
+        rng = np.random.default_rng(N)
+        idx = inp.topk_idx.copy()
+        idx[rng.random(idx.shape) < 0.1] = -1
+        idx[:, ::17, :] = -1
+        inp.topk_idx = idx
+    y = wl.random_bf16((R * N * min(R, K), H), seed=N)
+    plan = run_gpu(inp, y=y.cuda())
+    compare_ep(inp, plan, y_bits=wl.bf16_bits(y))
+
+
+def test_zipf_small():
+    inp = wl.make_ep("skew", seed=3, N=300, H=64)
+    compare_ep(inp, run_gpu(inp))
+
+
+def test_fp8_small():
+    inp = wl.make_ep("fp8", seed=4, N=333, H=384)
+    y = wl.random_bf16((inp.R * inp.N * 8, inp.H), seed=4)
+    plan = run_gpu(inp, y=y.cuda())
+    compare_ep(inp, plan, y_bits=wl.bf16_bits(y))
+
+
+def test_repeated_calls_reuse_workspace():
+    """The scan's tile states are tagged per launch: back-to-back calls on one
+    workspace (and a changed routing in between) stay exact."""
+    inp = wl.make_ep("dsv3", seed=6, N=700, H=64)
+    plan = run_gpu(inp, repeat=3)
+    compare_ep(inp, plan)
+    inp2 = wl.make_ep("dsv3", seed=7, N=700, H=64)
+    plan.load(inp2)
+    for _ in range(2):
+        plan.dev_err.zero_()
+        plan.step()
+    torch.cuda.synchronize()
+    compare_ep(inp2, plan)
+
+
+def test_empty_tokens():
+    inp = wl.make_ep(dict(R=4, N=0, E=16, K=2, H=64, routing="uniform", dtype="bf16"))
+    plan = run_gpu(inp)
+    assert plan.num_tokens_per_rank.abs().sum().item() == 0
+    assert plan.dest_offsets.abs().sum().item() == 0
+
+
+def test_all_masked():
+    inp = wl.make_ep(dict(R=3, N=50, E=6, K=2, H=64, routing="uniform", dtype="bf16"))
+    inp.topk_idx[:] = -1
+    plan = run_gpu(inp)
+    compare_ep(inp, plan)
+    assert not wl.bf16_bits(plan.out).any()
+
+
+def test_capacity_overflow():
+    inp = wl.make_ep(dict(R=4, N=300, E=16, K=4, H=64, routing="uniform", dtype="bf16"), seed=2)
+    _, _, mask, _ = oracle.layout(inp.topk_idx, inp.E)
+    total = int(np.unpackbits(mask.view(np.uint8)).sum())
+    cap = total // 2
+    plan = run_gpu(inp, recv_capacity=cap)
+    compare_ep(inp, plan, recv_capacity=cap, expect_err=B.MP_ERR_CAPACITY)
+
+
+def test_bad_expert_ids():
+    inp = wl.make_ep(dict(R=2, N=64, E=8, K=2, H=64, routing="uniform", dtype="bf16"), seed=8)
+    inp.topk_idx[0, 3, 0] = 8
+    inp.topk_idx[1, 9, 1] = -5
+    plan = run_gpu(inp)
+    compare_ep(inp, plan, expect_err=B.MP_ERR_BAD_EXPERT)
+
+
+def test_combine_rejects_rows_past_y():
+    send_row = torch.tensor([[[0, 5]]], dtype=torch.int32, device="cuda").expand(2, 1, 2).contiguous()
+    y = torch.ones((4, 8), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((2, 1, 8), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.check(B.mp_combine(2, 1, 8, y, 4, send_row, out, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.MP_ERR_CAPACITY
+    assert out.float().cpu().eq(1.0).all()  # only row 0 was summed
+
+
+@pytest.mark.parametrize("R,H,sizes", [(8, 64, [3, 0, 5, 1, 0, 2, 4, 1]), (3, 8, [0, 0, 0]),
+                                       (5, 1032, [100, 0, 257, 3, 64]), (1, 72, [9])])
+def test_rsv_agv_small(R, H, sizes):
+    inp = wl.make_rsv(dict(R=R, H=H, sizes=sizes), seed=R + H)
+    plan = RSVPlan(R, H, sizes)
+    plan.x.copy_(inp.x)
+    plan.shards.copy_(inp.shards)
+    B.check(plan.reducescatterv())
+    B.check(plan.allgatherv())
+    torch.cuda.synchronize()
+    rs, st = oracle.reducescatterv(wl.bf16_bits(inp.x), sizes)
+    ag, st2 = oracle.allgatherv(wl.bf16_bits(inp.shards), sizes, R)
+    assert st == st2 == 0
+    assert_bf16_close(wl.bf16_bits(plan.rs_out), rs, "reducescatterv")
+    assert np.array_equal(wl.bf16_bits(plan.ag_out), ag)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads (the benchmark's launch configuration)
+# ---------------------------------------------------------------------------
+def test_dsv3_full():
+    inp = wl.make_ep("dsv3", seed=0)
+    plan = run_gpu(inp)
+    out = compare_ep(inp, plan)
+    # order-sensitive combine at full size: random expert outputs
+    y = wl.gathered_bf16(out["num_recv"], inp.H, seed=5)
+    B.check(plan.combine(y.cuda()))
+    torch.cuda.synchronize()
+    comb, st = oracle.combine(wl.bf16_bits(y), out["send_row"])
+    assert st == 0 and plan.device_error() == 0
+    assert_bf16_close(wl.bf16_bits(plan.out), comb, "dsv3 combine(y)")
+
+
+def test_skew_full():
+    inp = wl.make_ep("skew", seed=0)
+    compare_ep(inp, run_gpu(inp))
+
+
+def test_fp8_full():
+    inp = wl.make_ep("fp8", seed=0)
+    _, _, mask, _ = oracle.layout(inp.topk_idx, inp.E)
+    total = int(np.unpackbits(mask.view(np.uint8)).sum())
+    y = wl.gathered_bf16(total, inp.H, seed=99)
+    plan = run_gpu(inp, y=y.cuda())
+    compare_ep(inp, plan, y_bits=wl.bf16_bits(y))
+
+
+def test_rsv_full_sampled():
+    inp = wl.make_rsv("rsv", seed=0)
+    R, H, sizes, S = inp.R, inp.H, inp.sizes.tolist(), inp.S
+    plan = RSVPlan(R, H, sizes)
+    plan.x.copy_(inp.x)
+    plan.shards.copy_(inp.shards)
+    B.check(plan.reducescatterv())
+    B.check(plan.allgatherv())
+    torch.cuda.synchronize()
+    # the oracle on a sample of rows: the sampled rows of every input, as one shard
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(S, size=min(S, 3000), replace=False))
+    xs = wl.bf16_bits(inp.x[:, torch.as_tensor(rows)])
+    rs, st = oracle.reducescatterv(xs, [len(rows)] + [0] * (R - 1))
+    assert st == 0
+    assert_bf16_close(wl.bf16_bits(plan.rs_out[torch.as_tensor(rows).cuda()]), rs, "rsv sample")
+    # all-gatherv is a copy: every logical rank's output equals the shards exactly
+    for q in range(R):
+        assert torch.equal(plan.ag_out[q].view(torch.int16), plan.shards.view(torch.int16))
