@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmp_layout.so")
-UNITS = ["mp_abi", "mp_layout_kernels", "mp_copy_kernels"]
+UNITS = ["mp_abi", "mp_layout_kernels", "mp_copy_kernels", "mp_noalloc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

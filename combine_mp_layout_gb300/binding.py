@@ -143,3 +143,30 @@ def mp_reducescatterv(R, H, sizes, inp, out, stream=None) -> int:
 def mp_allgatherv(R, row_bytes, sizes, inp, out, stream=None) -> int:
     return lib().mp_allgatherv(R, int(row_bytes), _host_sizes(sizes), _dev(inp, "in"),
                                _dev(out, "out"), _stream(stream))
+
+
+def mp_dispatch_noalloc(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weights,
+                        is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert,
+                        recv_capacity, recv_x, recv_scales, recv_src_rank, recv_src_idx,
+                        recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
+                        num_recv_tokens_per_expert, send_row, dev_err, stream=None) -> int:
+    """mp_dispatch without a workspace, for callers that cannot allocate device memory
+    (the scan's scratch is a fixed array inside the library; see the C header)."""
+    L = lib()
+    f = L.mp_dispatch_noalloc
+    if f.argtypes is None:
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        f.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i64,
+                      P, P, P, P, P, P, P, P, P, P, P, P]
+        f.restype = ctypes.c_int
+    return f(R, N, K, E, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
+             _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"),
+             _dev(is_token_in_rank, "is_token_in_rank"),
+             _dev(num_tokens_per_rank, "num_tokens_per_rank"),
+             _dev(num_tokens_per_expert, "num_tokens_per_expert"), int(recv_capacity),
+             _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
+             _dev(recv_src_rank, "recv_src_rank"), _dev(recv_src_idx, "recv_src_idx"),
+             _dev(recv_topk_idx, "recv_topk_idx"), _dev(recv_topk_weights, "recv_topk_weights"),
+             _dev(dest_offsets, "dest_offsets"), _dev(rank_prefix, "rank_prefix"),
+             _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
+             _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _stream(stream))

@@ -200,6 +200,43 @@ int mp_reducescatterv(int R, int H, const int64_t *sizes, const void *in, void *
 int mp_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const void *in, void *out,
                   mp_stream_t stream);
 
+/*
+ * mp_dispatch_noalloc -- mp_dispatch for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: this is a convenience of this
+ * library.)
+ * Some callers cannot call cudaMalloc for the workspace mp_dispatch needs:
+ * a host application that reserves (nearly) all device memory for its own
+ * pool at start-up, a plugin whose host framework owns every device
+ * allocation, or a latency-critical loop in which cudaMalloc / cudaFree would
+ * synchronise the device.  This call takes the same arguments as mp_dispatch
+ * except the workspace, and computes the same outputs; it allocates nothing.
+ * The scan's scratch lives instead in a fixed array of
+ * MP_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
+ * GPU that loads the library holds until the process exits.
+ *  - Limit: problems whose mp_workspace_size(R, N, E) exceeds
+ *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with R=8 and E=256 that allows up to
+ *    29,824 tokens per rank) are rejected with MP_ERR_INVALID_ARG before
+ *    anything is launched; use mp_dispatch with a workspace for those.
+ *  - Set-up: the first call on each device (with that device current) finds
+ *    the array's device address and zero-fills it with a synchronous
+ *    cudaMemset.  Make that first call before any stream capture.
+ *  - Every call on a device shares the one array and starts by clearing its
+ *    counters on `stream`, so calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race and give wrong results: order them on
+ *    one stream.
+ * The caller still owns every input and output buffer, as for mp_dispatch.
+ */
+#define MP_NOALLOC_SCRATCH_BYTES (1u << 20)
+int mp_dispatch_noalloc(int R, int N, int K, int E, int H, int dtype, const void *x,
+                        const float *x_scales, const int32_t *topk_idx,
+                        const float *topk_weights, const uint32_t *is_token_in_rank,
+                        const int32_t *num_tokens_per_rank, const int32_t *num_tokens_per_expert,
+                        int64_t recv_capacity, void *recv_x, float *recv_scales,
+                        int32_t *recv_src_rank, int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                        float *recv_topk_weights, int32_t *dest_offsets, int32_t *rank_prefix,
+                        int32_t *num_recv_tokens_per_expert, int32_t *send_row,
+                        int32_t *dev_err, mp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
