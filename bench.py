@@ -42,10 +42,31 @@ def parse():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default="dsv3", choices=["dsv3", "skew", "fp8", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override N (tokens per rank), e.g. for small profiler captures")
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-rows", action="store_true",
+                    help="skip timing the e4m3 dispatch and reduce-scatterv / all-gatherv rows")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the slowest replica sets the time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of N independent replicas: every rank's units over the
+    slowest rank's time."""
+    return units_per_rank * world * steps / (ms_max / 1e3)
 
 
 def peaks():
@@ -59,12 +80,16 @@ def peaks():
 
 
 def algorithmic_bytes(R, N, K, E, H, T, elt=2, scales_per_row=0):
-    """Bytes each phase must move (read + write), not padded or dense equivalents."""
+    """Bytes each phase must move (read + write), not padded or dense equivalents.
+    offsets: mask + topk ids/weights read, send_row + per-row metadata written;
+    rows: each token row read once and written once per destination (+ its scales);
+    combine: every receive row read once, each token row written once."""
     layout = R * N * K * 4 + R * N * 4 + R * E * 4 + R * R * 4
-    meta = R * N * K * 8 + R * N * 4 + T * (8 + 8 * K) + R * N * R * 4 + R * R * 4
-    dispatch = R * N * H * elt + T * H * elt + (R * N + T) * scales_per_row * 4 + meta
+    offsets = R * N * K * 8 + R * N * 4 + T * (8 + 8 * K) + R * N * R * 4 + R * R * 4
+    rows = R * N * H * elt + T * H * elt + (R * N + T) * scales_per_row * 4 + R * N * R * 4
     combine = T * H * 2 + R * N * H * 2 + R * N * R * 4
-    return dict(layout=layout, dispatch=dispatch, combine=combine)
+    return dict(layout=layout, offsets=offsets, rows=rows, dispatch=offsets + rows,
+                combine=combine)
 
 
 # ---------------------------------------------------------------------------
@@ -208,6 +233,102 @@ def config_block(name, inp):
 
 
 # ---------------------------------------------------------------------------
+# the other rows of the path on their own workloads (device-timed)
+# ---------------------------------------------------------------------------
+def measure_other_rows(steps: int, peak: float):
+    """e4m3 dispatch (R=8, N=8192, H=7168, per-128-channel fp32 scales, top-8 of 256)
+    with its bf16 combine, and reduce-scatterv / all-gatherv (R=8, H=4096, per-rank
+    rows U{0..16384}).  Inputs are synthetic (drawn on the device: only the timing
+    is used here; parity on these workloads is in the tests)."""
+    import numpy as np
+    import torch
+
+    from combine_mp_layout_gb300 import binding as B
+    from combine_mp_layout_gb300 import workloads as wl
+    from combine_mp_layout_gb300.pipeline import EPPlan, RSVPlan
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def row(ms, nbytes):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"ms": ms, "algorithmic_bytes": int(nbytes), "GB/s": gbs, "frac_of_peak": gbs / peak}
+
+    out = {}
+    # in-kernel e4m3 quantisation on dispatch, on the dsv3 workload
+    cfg = wl.CONFIGS["dsv3"]
+    R, N, H, E, K = cfg["R"], cfg["N"], cfg["H"], cfg["E"], cfg["K"]
+    rng = np.random.default_rng(0)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    plan = EPPlan(R, N, K, E, H, "bf16")
+    plan.topk_idx.copy_(torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)))
+    plan.topk_weights.copy_(torch.from_numpy(wl.softmax_weights(rng, R, N, K)))
+    plan.x.copy_(torch.randn((R, N, H), generator=g, device="cuda").to(torch.bfloat16))
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    torch.cuda.synchronize()
+    T = plan.num_recv()
+    rq = torch.empty((plan.cap, H), dtype=torch.uint8, device="cuda")
+    rs = torch.empty((plan.cap, H // 128), dtype=torch.float32, device="cuda")
+    ms_q = timed(lambda: B.check(B.mp_dispatch_rows_e4m3(R, N, H, plan.x, plan.send_row, plan.cap,
+                                                          rq, rs)), steps)
+    out["dispatch_rows_quantise_e4m3"] = dict(
+        row(ms_q, R * N * H * 2 + T * (H + H // 128 * 4) + R * N * R * 4),
+        workload="dsv3 rows quantised in-kernel: bf16 in, e4m3 + fp32 scale per 128 channels out")
+    del plan, rq, rs
+    torch.cuda.empty_cache()
+
+    cfg = wl.CONFIGS["fp8"]
+    R, N, H, E, K = cfg["R"], cfg["N"], cfg["H"], cfg["E"], cfg["K"]
+    rng = np.random.default_rng(0)
+    plan = EPPlan(R, N, K, E, H, "e4m3")
+    plan.topk_idx.copy_(torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)))
+    plan.topk_weights.copy_(torch.from_numpy(wl.softmax_weights(rng, R, N, K)))
+    g = torch.Generator(device="cuda").manual_seed(0)
+    plan.x.copy_(torch.randn((R, N, H), generator=g, device="cuda").to(torch.float8_e4m3fn))
+    plan.x_scales.copy_(torch.rand(plan.x_scales.shape, generator=g, device="cuda") * 1.5 + 0.5)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    torch.cuda.synchronize()
+    T = plan.num_recv()
+    y = torch.randn((T, H), generator=g, device="cuda").to(torch.bfloat16)
+    spr = H // 128
+    ms_rows = timed(lambda: B.check(plan.dispatch_rows()), steps)
+    ms_comb = timed(lambda: B.check(plan.combine(y)), steps)
+    assert plan.device_error() == 0
+    out["fp8_dispatch_rows"] = dict(row(ms_rows, R * N * H + T * H + (R * N + T) * spr * 4
+                                        + R * N * R * 4), workload="fp8: R=8, N=8192, H=7168 e4m3 "
+                                   "+ fp32 scale per 128 channels, E=256, top-8", receive_rows=T)
+    out["fp8_combine_bf16"] = row(ms_comb, T * H * 2 + R * N * H * 2 + R * N * R * 4)
+    del plan, y
+    torch.cuda.empty_cache()
+
+    cfg = wl.CONFIGS["rsv"]
+    sizes = np.random.default_rng(0).integers(0, cfg["max_rows"] + 1, cfg["R"]).tolist()
+    rp = RSVPlan(cfg["R"], cfg["H"], sizes)
+    rp.x.normal_(generator=g)
+    rp.shards.normal_(generator=g)
+    S, Rr, Hh = rp.S, cfg["R"], cfg["H"]
+    ms_rs = timed(lambda: B.check(rp.reducescatterv()), max(5, steps // 4))
+    ms_ag = timed(lambda: B.check(rp.allgatherv()), max(5, steps // 4))
+    out["reducescatterv"] = dict(row(ms_rs, Rr * S * Hh * 2 + S * Hh * 2),
+                                 workload="rsv: R=8, H=4096 bf16, rows per rank U{0..16384}, S=%d" % S)
+    out["allgatherv"] = row(ms_ag, S * Hh * 2 + Rr * S * Hh * 2)
+    del rp
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
 # the CUDA arm
 # ---------------------------------------------------------------------------
 def main():
@@ -236,7 +357,8 @@ def main():
         torch.cuda.synchronize()
 
     B.lib()  # fail loudly if the library is missing
-    inp = wl.make_ep(args.config, seed=args.seed)
+    over = {"N": args.tokens} if args.tokens > 0 else {}
+    inp = wl.make_ep(args.config, seed=args.seed, **over)
     R, N, K, E, H = inp.R, inp.N, inp.K, inp.E, inp.H
     plan = EPPlan(R, N, K, E, H, inp.dtype)
     plan.load(inp)
@@ -259,7 +381,7 @@ def main():
                            scales_per_row=0 if inp.dtype == "bf16" else H // 128)
 
     # timed region: K steps, per-phase CUDA events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -272,79 +394,111 @@ def main():
         e[0].record(stream)
         B.check(plan.layout())
         e[1].record(stream)
-        B.check(plan.dispatch())
+        B.check(plan.dispatch_offsets())
         e[2].record(stream)
-        B.check(plan.combine(y))
+        B.check(plan.dispatch_rows())
         e[3].record(stream)
+        B.check(plan.combine(y))
+        e[4].record(stream)
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    ph = {"layout": 0.0, "dispatch": 0.0, "combine": 0.0}
+    ph = {"layout": 0.0, "offsets": 0.0, "rows": 0.0, "combine": 0.0}
     for e in ev:
         ph["layout"] += e[0].elapsed_time(e[1])
-        ph["dispatch"] += e[1].elapsed_time(e[2])
-        ph["combine"] += e[2].elapsed_time(e[3])
+        ph["offsets"] += e[1].elapsed_time(e[2])
+        ph["rows"] += e[2].elapsed_time(e[3])
+        ph["combine"] += e[3].elapsed_time(e[4])
     ph = {k: v / args.steps for k, v in ph.items()}
+    ph["dispatch"] = ph["offsets"] + ph["rows"]
     assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
 
-    t_max = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
+    total_ms = max_over_ranks(total_ms, world, device="cuda")
     ms_step = total_ms / args.steps
     tokens = R * N * world
-    value = tokens * args.steps / (total_ms / 1e3)
-    step_bytes = nb["layout"] + nb["dispatch"] + nb["combine"]
+    value = replica_throughput(R * N, args.steps, world, total_ms)
+    step_bytes = nb["layout"] + nb["offsets"] + nb["rows"] + nb["combine"]
     eff_gbs = step_bytes * world / (ms_step / 1e3) / 1e9
 
-    # end to end through the public API with host buffers (pinned)
+    # End to end through the public API with host buffers (pinned): every step
+    # copies its inputs host->device, runs layout -> dispatch -> combine and
+    # copies its result device->host.  Steps are pipelined the way a serving
+    # loop would run them: two buffer sets, the copies of step i+1 / i-1 on
+    # their own streams overlapping the kernels of step i.
     e2e = None
     if args.e2e_steps > 0:
         h_topk = torch.from_numpy(inp.topk_idx).pin_memory()
         h_w = torch.from_numpy(inp.topk_weights).pin_memory()
         h_x = inp.x.pin_memory()
         h_xs = inp.x_scales.pin_memory() if inp.x_scales is not None else None
-        h_out = torch.empty(plan.out.shape, dtype=plan.out.dtype).pin_memory()
+        plans = [plan, EPPlan(R, N, K, E, H, inp.dtype)]
+        h_out = [torch.empty(plan.out.shape, dtype=plan.out.dtype).pin_memory() for _ in plans]
         h2d = h_topk.nbytes + h_w.nbytes + h_x.nbytes + (h_xs.nbytes if h_xs is not None else 0)
-        d2h = h_out.nbytes
+        d2h = h_out[0].nbytes
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        s_run = stream
+        ev_in = [torch.cuda.Event() for _ in plans]
+        ev_run = [torch.cuda.Event() for _ in plans]
+        ev_out = [torch.cuda.Event() for _ in plans]
 
-        def e2e_step():
-            plan.topk_idx.copy_(h_topk, non_blocking=True)
-            plan.topk_weights.copy_(h_w, non_blocking=True)
-            plan.x.copy_(h_x, non_blocking=True)
-            if h_xs is not None:
-                plan.x_scales.copy_(h_xs, non_blocking=True)
-            plan.step(y)
-            h_out.copy_(plan.out, non_blocking=True)
+        def e2e_steps(n):
+            for i in range(n):
+                j = i % 2
+                p = plans[j]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_run[j])  # step i-2 has consumed p's inputs
+                    p.topk_idx.copy_(h_topk, non_blocking=True)
+                    p.topk_weights.copy_(h_w, non_blocking=True)
+                    p.x.copy_(h_x, non_blocking=True)
+                    if h_xs is not None:
+                        p.x_scales.copy_(h_xs, non_blocking=True)
+                    ev_in[j].record(s_in)
+                s_run.wait_event(ev_in[j])
+                if i >= 2:
+                    s_run.wait_event(ev_out[j])  # step i-2's result has left p.out
+                p.step(y, stream=s_run)
+                ev_run[j].record(s_run)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_run[j])
+                    h_out[j].copy_(p.out, non_blocking=True)
+                    ev_out[j].record(s_out)
 
-        for _ in range(3):
-            e2e_step()
+        e2e_steps(4)
+        torch.cuda.synchronize()
         barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record(stream)
+        a.record(s_in)
+        e2e_steps(args.e2e_steps)
+        s_in.wait_stream(s_out)
+        b.record(s_in)
+        torch.cuda.synchronize()
         barrier()
-        e_ms = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-        e2e = {"value": tokens * args.e2e_steps / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+        for p in plans:
+            assert p.device_error() == 0, B.mp_status_string(p.device_error())
+        e_ms = max_over_ranks(a.elapsed_time(b), world, device="cuda")
+        e2e = {"value": replica_throughput(R * N, args.e2e_steps, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": float(e_ms.item()) / args.e2e_steps}
+               "ms_per_step": e_ms / args.e2e_steps,
+               "pipelining": "two buffer sets; H2D, kernels and D2H on separate streams"}
+        del plans[1]
 
-    # roofline of the dominant kernel (the larger of dispatch and combine)
+    # roofline of the dominant kernel (the larger of the row copy and combine)
     peak, peak_kind = peaks()
-    dom = "dispatch" if ph["dispatch"] >= ph["combine"] else "combine"
+    dom = "rows" if ph["rows"] >= ph["combine"] else "combine"
     achieved = nb[dom] / (ph[dom] / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": {"dispatch": "mp_dispatch (scan + row copy)",
+    roofline = {"bound": "hbm", "kernel": {"rows": "mp_k_dispatch (dispatch row copy)",
                                            "combine": "mp_k_combine"}[dom],
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": peak_kind, "traffic": None,
                 "all_phases": {k: {"ms": ph[k], "algorithmic_bytes": nb[k],
-                                   "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in ph}}
+                                   "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in nb}}
+
+    other = None
+    if not args.no_other_rows and args.config == "dsv3" and args.tokens == 0:
+        other = measure_other_rows(max(10, min(args.steps, 100)), peaks()[0])
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -363,8 +517,8 @@ def main():
             "effective_hbm_gbs": eff_gbs, "frac_of_8tbs": eff_gbs / world / NOMINAL_HBM_GBS,
             "frac_of_measured_copy_peak": eff_gbs / world / peak,
             "receive_rows": T, "phases_ms": ph,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clk,
+            "roofline": roofline, "other_rows": other, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps if N > 0 else 0, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

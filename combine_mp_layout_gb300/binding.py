@@ -56,11 +56,15 @@ def lib() -> ctypes.CDLL:
         L.mp_layout.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.mp_dispatch.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i64,
                                   P, P, P, P, P, P, P, P, P, P, P, P, P]
+        L.mp_dispatch_offsets.argtypes = [i32, i32, i32, i32, P, P, P, P, P, i64,
+                                          P, P, P, P, P, P, P, P, P, P, P]
+        L.mp_dispatch_rows.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P]
+        L.mp_dispatch_rows_e4m3.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
         L.mp_combine.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
         L.mp_reducescatterv.argtypes = [i32, i32, P, P, P, P]
         L.mp_allgatherv.argtypes = [i32, i64, P, P, P, P]
-        for f in ("mp_layout", "mp_dispatch", "mp_combine", "mp_reducescatterv",
-                  "mp_allgatherv"):
+        for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
+                  "mp_dispatch_rows_e4m3", "mp_combine", "mp_reducescatterv", "mp_allgatherv"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -123,6 +127,39 @@ def mp_dispatch(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weights, is_to
         _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
         _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _dev(workspace, "workspace"),
         _stream(stream))
+
+
+def mp_dispatch_offsets(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                        num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                        recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                        dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
+                        workspace, stream=None) -> int:
+    return lib().mp_dispatch_offsets(
+        R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"),
+        _dev(is_token_in_rank, "is_token_in_rank"),
+        _dev(num_tokens_per_rank, "num_tokens_per_rank"),
+        _dev(num_tokens_per_expert, "num_tokens_per_expert"), int(recv_capacity),
+        _dev(recv_src_rank, "recv_src_rank"), _dev(recv_src_idx, "recv_src_idx"),
+        _dev(recv_topk_idx, "recv_topk_idx"), _dev(recv_topk_weights, "recv_topk_weights"),
+        _dev(dest_offsets, "dest_offsets"), _dev(rank_prefix, "rank_prefix"),
+        _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
+        _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _dev(workspace, "workspace"),
+        _stream(stream))
+
+
+def mp_dispatch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x, recv_scales,
+                     stream=None) -> int:
+    return lib().mp_dispatch_rows(R, N, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
+                                  _dev(send_row, "send_row"), int(recv_capacity),
+                                  _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
+                                  _stream(stream))
+
+
+def mp_dispatch_rows_e4m3(R, N, H, x, send_row, recv_capacity, recv_x, recv_scales,
+                          stream=None) -> int:
+    return lib().mp_dispatch_rows_e4m3(R, N, H, _dev(x, "x"), _dev(send_row, "send_row"),
+                                       int(recv_capacity), _dev(recv_x, "recv_x"),
+                                       _dev(recv_scales, "recv_scales"), _stream(stream))
 
 
 def mp_combine(R, N, H, y, y_rows, send_row, out, dev_err, stream=None) -> int:

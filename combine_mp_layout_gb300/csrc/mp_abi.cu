@@ -72,6 +72,120 @@ int mp_layout(int R, int N, int K, int E, const int32_t* topk_idx, int32_t* num_
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace mp {
+
+// Checks shared by mp_dispatch and mp_dispatch_offsets.
+static int check_offsets_args(int R, int N, int K, int E, const int32_t* topk_idx,
+                              const float* topk_weights, const uint32_t* is_token_in_rank,
+                              const int32_t* num_tokens_per_rank,
+                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                              const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                              const int32_t* recv_topk_idx, const float* recv_topk_weights,
+                              const int32_t* dest_offsets, const int32_t* rank_prefix,
+                              const int32_t* num_recv_tokens_per_expert, const int32_t* send_row,
+                              const int32_t* dev_err, const void* workspace) {
+  if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !dest_offsets || !rank_prefix ||
+      !num_recv_tokens_per_expert || !dev_err || !workspace)
+    return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !topk_weights || !is_token_in_rank || !send_row))
+    return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 &&
+      (!recv_src_rank || !recv_src_idx || !recv_topk_idx || !recv_topk_weights))
+    return MP_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned4(topk_idx) || !aligned4(topk_weights) ||
+      !aligned4(is_token_in_rank) || !aligned4(send_row) || !aligned4(recv_src_rank) ||
+      !aligned4(recv_src_idx) || !aligned4(recv_topk_idx) || !aligned4(recv_topk_weights) ||
+      !aligned4(num_tokens_per_rank) || !aligned4(num_tokens_per_expert) ||
+      !aligned4(dest_offsets) || !aligned4(rank_prefix) ||
+      !aligned4(num_recv_tokens_per_expert) || !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return MP_OK;
+}
+
+// Checks shared by mp_dispatch and mp_dispatch_rows.
+static int check_rows_args(int R, int N, int H, int dtype, const void* x, const float* x_scales,
+                           const int32_t* send_row, int64_t recv_capacity, const void* recv_x,
+                           const float* recv_scales) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || recv_capacity < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (dtype != MP_BF16 && dtype != MP_E4M3) return MP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == MP_E4M3;
+  if (fp8 ? (H % MP_SCALE_BLOCK != 0) : (H % 8 != 0)) return MP_ERR_INVALID_ARG;
+  if (fp8 != (x_scales != nullptr) || fp8 != (recv_scales != nullptr)) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !send_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && !recv_x) return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned4(x_scales) || !aligned4(recv_scales) ||
+      !aligned4(send_row))
+    return MP_ERR_INVALID_ARG;
+  return MP_OK;
+}
+
+static cudaError_t launch_rows(int R, int N, int H, int dtype, const void* x,
+                               const float* x_scales, const int32_t* send_row,
+                               int64_t recv_capacity, void* recv_x, float* recv_scales,
+                               cudaStream_t st) {
+  const bool fp8 = dtype == MP_E4M3;
+  const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
+  return launch_dispatch_copy(R, int64_t(R) * N, row_bytes, x, recv_x, recv_capacity, send_row,
+                              fp8 ? H / MP_SCALE_BLOCK : 0, x_scales, recv_scales, st);
+}
+
+}  // namespace mp
+
+extern "C" {
+
+int mp_dispatch_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+                        const float* topk_weights, const uint32_t* is_token_in_rank,
+                        const int32_t* num_tokens_per_rank, const int32_t* num_tokens_per_expert,
+                        int64_t recv_capacity, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
+                        int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                        int32_t* send_row, int32_t* dev_err, void* workspace,
+                        mp_stream_t stream) {
+  const int st = check_offsets_args(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                                    num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                                    recv_src_rank, recv_src_idx, recv_topk_idx,
+                                    recv_topk_weights, dest_offsets, rank_prefix,
+                                    num_recv_tokens_per_expert, send_row, dev_err, workspace);
+  if (st != MP_OK) return st;
+  return cuda_status(launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                                 num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                                 recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                                 dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                                 dev_err, static_cast<unsigned char*>(workspace),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_rows(int R, int N, int H, int dtype, const void* x, const float* x_scales,
+                     const int32_t* send_row, int64_t recv_capacity, void* recv_x,
+                     float* recv_scales, mp_stream_t stream) {
+  const int st = check_rows_args(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                                 recv_scales);
+  if (st != MP_OK) return st;
+  return cuda_status(launch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                                 recv_scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_rows_e4m3(int R, int N, int H, const void* x, const int32_t* send_row,
+                          int64_t recv_capacity, void* recv_x, float* recv_scales,
+                          mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || H % MP_SCALE_BLOCK != 0 ||
+      recv_capacity < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !send_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && (!recv_x || !recv_scales)) return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned4(recv_scales) || !aligned4(send_row))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch_quant(R, int64_t(R) * N, H, x, recv_x, recv_scales,
+                                           recv_capacity, send_row,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void* x, const float* x_scales,
                 const int32_t* topk_idx, const float* topk_weights,
                 const uint32_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
@@ -80,35 +194,24 @@ int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void* x, con
                 int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
                 int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert, int32_t* send_row,
                 int32_t* dev_err, void* workspace, mp_stream_t stream) {
-  if (!ep_shape_ok(R, N, K, E) || H <= 0 || recv_capacity < 0) return MP_ERR_INVALID_ARG;
-  if (dtype != MP_BF16 && dtype != MP_E4M3) return MP_ERR_INVALID_ARG;
-  const bool fp8 = dtype == MP_E4M3;
-  if (fp8 ? (H % MP_SCALE_BLOCK != 0) : (H % 8 != 0)) return MP_ERR_INVALID_ARG;
-  if (fp8 != (x_scales != nullptr) || fp8 != (recv_scales != nullptr)) return MP_ERR_INVALID_ARG;
-  if (!num_tokens_per_rank || !num_tokens_per_expert || !dest_offsets || !rank_prefix ||
-      !num_recv_tokens_per_expert || !dev_err || !workspace)
-    return MP_ERR_INVALID_ARG;
-  if (N > 0 && (!x || !topk_idx || !topk_weights || !is_token_in_rank || !send_row))
-    return MP_ERR_INVALID_ARG;
-  if (recv_capacity > 0 && (!recv_x || !recv_src_rank || !recv_src_idx || !recv_topk_idx ||
-                            !recv_topk_weights))
-    return MP_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || !aligned4(x_scales) ||
-      !aligned4(recv_scales) || !aligned4(topk_idx) || !aligned4(topk_weights) ||
-      !aligned4(is_token_in_rank) || !aligned4(send_row) || !aligned4(recv_src_rank) ||
-      !aligned4(recv_src_idx) || !aligned4(recv_topk_idx) || !aligned4(recv_topk_weights))
-    return MP_ERR_INVALID_ARG;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int st = check_offsets_args(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                              num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                              recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                              dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                              dev_err, workspace);
+  if (st == MP_OK)
+    st = check_rows_args(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                         recv_scales);
+  if (st != MP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
                               num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
                               recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
                               dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
-                              dev_err, static_cast<unsigned char*>(workspace), st);
+                              dev_err, static_cast<unsigned char*>(workspace), cs);
   if (e != cudaSuccess) return MP_ERR_CUDA;
-  const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
-  e = launch_dispatch_copy(R, int64_t(R) * N, row_bytes, x, recv_x, recv_capacity, send_row,
-                           fp8 ? H / MP_SCALE_BLOCK : 0, x_scales, recv_scales, st);
-  return cuda_status(e);
+  return cuda_status(launch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                                 recv_scales, cs));
 }
 
 int mp_combine(int R, int N, int H, const void* y, int64_t y_rows, const int32_t* send_row,

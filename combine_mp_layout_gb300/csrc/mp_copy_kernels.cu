@@ -3,60 +3,93 @@
 // all-gatherv (one read, R writes).
 //
 // All four are streaming kernels: nothing is reused, so they are bound by
-// HBM bandwidth and the design goal is bytes in flight.  Each runs a
-// persistent grid (SM count x resident blocks) and splits the work into
-// small units handed out round-robin to warps:
-//   dispatch / combine : (token, slab) with a slab of 32 lanes x U 16-byte
-//                        vectors of the token's row, so consecutive warps
-//                        stream consecutive slabs of the same row and the
-//                        per-SM load evens out across rows of unequal fan-out;
-//   reduce-scatterv / all-gatherv : 16-byte vectors of the flat arrays.
-// Payload moves as 16-byte vectors with L1-bypassing streaming loads.
+// HBM bandwidth and the design goal is bytes in flight with few
+// instructions.  Each runs a persistent grid (SM count x resident blocks) and
+// splits the work into small units handed out round-robin to warps:
+//   dispatch / combine : (token, slab) with a slab of 32 lanes x U vectors of
+//                        the token's row, so consecutive warps stream
+//                        consecutive slabs of the same row and the per-SM
+//                        load evens out across rows of unequal fan-out;
+//   reduce-scatterv / all-gatherv : vectors of the flat arrays.
+// Payload moves as 32-byte vectors (the 256-bit global loads and stores of
+// sm_100-class GPUs) when the row size and the pointers allow, else as
+// 16-byte vectors; loads bypass L1 and are marked evict-first in L2.
 #include <cstdint>
 
 #include "mp_common.cuh"
 #include "mp_internal.h"
 
+// Compile-time tuning (vector words: 8 = 32-byte, 4 = 16-byte accesses).
+#ifndef MP_DISPATCH_NW
+#define MP_DISPATCH_NW 8
+#endif
+#ifndef MP_DISPATCH_U
+#define MP_DISPATCH_U 2
+#endif
+#ifndef MP_COMBINE_NW
+#define MP_COMBINE_NW 8
+#endif
+#ifndef MP_COMBINE_U
+#define MP_COMBINE_U 1
+#endif
+#ifndef MP_COMBINE_RB
+#define MP_COMBINE_RB 4
+#endif
+#ifndef MP_COMBINE_MINB
+#define MP_COMBINE_MINB 3
+#endif
+
+#ifndef MP_DISPATCH_TMA
+#define MP_DISPATCH_TMA 0
+#endif
+#ifndef MP_TMA_STAGES
+#define MP_TMA_STAGES 6
+#endif
+#ifndef MP_TMA_CHUNK
+#define MP_TMA_CHUNK 8
+#endif
+
 namespace mp {
 
 constexpr int kCopyThreads = 256;
+constexpr int kWarpsPerBlock = kCopyThreads / kWarp;
 
 // ---------------------------------------------------------------------------
 // Dispatch copy ("MSCCLPP EP implementation", microsoft/mscclpp PR #852:
-// intranode_dispatch moves each token row, as 16-byte vectors, to every rank
-// that owns one of its experts).  One read of x, one write per receive row.
+// intranode_dispatch moves each token row, as vectors, to every rank that
+// owns one of its experts).  One read of x, one write per receive row.
 // ---------------------------------------------------------------------------
-template <int U>
+template <int NW, int U>
 __global__ void __launch_bounds__(kCopyThreads)
-mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ x,
-              int4* __restrict__ recv_x, int64_t recv_capacity,
-              const int32_t* __restrict__ send_row, int spr,
-              const float* __restrict__ x_scales, float* __restrict__ recv_scales) {
+mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ x,
+              Words<NW>* __restrict__ recv_x, int64_t recv_capacity,
+              const int32_t* __restrict__ send_row, int spr, const float* __restrict__ x_scales,
+              float* __restrict__ recv_scales) {
   const int lane = threadIdx.x & 31;
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
   const int64_t units = tokens * slabs;
-  const int64_t nw = int64_t(gridDim.x) * (kCopyThreads / kWarp);
-  for (int64_t unit = int64_t(blockIdx.x) * (kCopyThreads / kWarp) + (threadIdx.x >> 5);
-       unit < units; unit += nw) {
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
+       unit += nw) {
     const int64_t tok = unit / slabs;
     const int64_t slab = unit - tok * slabs;
     const int my = lane < R ? __ldg(send_row + tok * R + lane) : -1;
     unsigned vm = __ballot_sync(kFull, my >= 0 && int64_t(my) < recv_capacity);
     if (vm == 0) continue;
     const int64_t i0 = slab * slab_vec + lane;
-    int4 v[U];
+    Words<NW> v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < vpr) v[u] = ld_stream(x + tok * vpr + i0 + u * kWarp);
+      if (i0 + u * kWarp < vpr) v[u] = ld_stream_w<NW>(x + tok * vpr + i0 + u * kWarp);
     while (vm) {
       const int d = __ffs(vm) - 1;
       vm &= vm - 1;
       const int64_t row = __shfl_sync(kFull, my, d);
-      int4* dst = recv_x + row * vpr;
+      Words<NW>* dst = recv_x + row * vpr;
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (i0 + u * kWarp < vpr) st_stream(dst + i0 + u * kWarp, v[u]);
+        if (i0 + u * kWarp < vpr) st_stream_w<NW>(dst + i0 + u * kWarp, v[u]);
       if (spr > 0 && slab == 0)
         for (int c = lane; c < spr; c += kWarp)
           recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
@@ -65,23 +98,222 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ x,
 }
 
 // ---------------------------------------------------------------------------
+// Dispatch copy with the bulk-copy (TMA) engine.  One warp per block; lane 0
+// streams the block's token rows through a ring of NS shared-memory stages:
+// a global->shared bulk load per row piece (completing on the stage's
+// mbarrier), then one contiguous shared->global bulk store per destination.
+// A stage is refilled once the stores issued LAG items earlier have finished
+// reading it.  Blocks take chunks of kTmaChunk tokens round-robin; the
+// chunk's send_row entries are staged in shared memory by the whole warp.
+// ---------------------------------------------------------------------------
+constexpr int kTmaStages = MP_TMA_STAGES;
+constexpr int kTmaLag = 2;
+constexpr int kTmaChunk = MP_TMA_CHUNK;
+constexpr uint32_t kTmaPiece = 16384;  // bytes per bulk copy (rows are cut into pieces)
+static_assert(kTmaLag < kTmaStages, "lag below the stage count");
+
+__host__ __device__ inline size_t tma_smem_bytes(uint32_t piece_bytes) {
+  return size_t(kTmaStages) * piece_bytes + size_t(kTmaChunk) * MP_MAX_RANKS * 4 +
+         size_t(kTmaStages) * 8;
+}
+
+__global__ void __launch_bounds__(kWarp)
+mp_k_dispatch_tma(int R, int64_t tokens, int64_t row_bytes, uint32_t piece_bytes, int pieces,
+                  const unsigned char* __restrict__ x, unsigned char* __restrict__ recv_x,
+                  int64_t recv_capacity, const int32_t* __restrict__ send_row, int spr,
+                  const float* __restrict__ x_scales, float* __restrict__ recv_scales,
+                  int32_t* __restrict__ dev_err) {
+  extern __shared__ __align__(128) unsigned char sm_tma[];
+  unsigned char* stages = sm_tma;
+  int32_t* table = reinterpret_cast<int32_t*>(sm_tma + size_t(kTmaStages) * piece_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(table + kTmaChunk * MP_MAX_RANKS);
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    for (int i = 0; i < kTmaStages; ++i) mbar_init(&bars[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  const int64_t chunks = (tokens + kTmaChunk - 1) / kTmaChunk;
+  uint32_t g = 0;  // items this block has processed before the current chunk
+  bool failed = false;
+  for (int64_t ch = blockIdx.x; ch < chunks; ch += gridDim.x) {
+    const int64_t tok0 = ch * kTmaChunk;
+    const int nt = int(tokens - tok0 < kTmaChunk ? tokens - tok0 : kTmaChunk);
+    for (int i = lane; i < nt * R; i += kWarp) table[i] = __ldg(send_row + tok0 * R + i);
+    __syncwarp();
+    if (lane == 0 && !failed) {
+      const int nitems = nt * pieces;
+      auto issue_load = [&](int item) {
+        const uint32_t st = (g + uint32_t(item)) % kTmaStages;
+        const int t = item / pieces, pc = item - t * pieces;
+        const int64_t off = int64_t(pc) * piece_bytes;
+        const uint32_t bytes = uint32_t(row_bytes - off < piece_bytes ? row_bytes - off : piece_bytes);
+        mbar_arrive_expect_tx(&bars[st], bytes);
+        bulk_g2s(stages + size_t(st) * piece_bytes, x + (tok0 + t) * row_bytes + off, bytes,
+                 &bars[st]);
+      };
+      const int pro = nitems < kTmaStages ? nitems : kTmaStages;
+      for (int i = 0; i < pro; ++i) issue_load(i);
+      int issued = pro;  // items whose load is in flight or done
+      for (int i = 0; i < nitems; ++i) {
+        const uint32_t gi = g + uint32_t(i);
+        const uint32_t st = gi % kTmaStages, parity = (gi / kTmaStages) & 1u;
+        uint32_t spins = 0;
+        bool ok = true;
+        while (!mbar_try_wait(&bars[st], parity)) {
+          if (++spins > kSpinLimit) { ok = false; break; }
+        }
+        if (!ok) {
+          // give up: report, then wait (bounded) for this block's loads in flight
+          failed = true;
+          raise_error(dev_err, MP_ERR_TIMEOUT);
+          for (int k = i + 1; k < issued; ++k) {
+            const uint32_t gk = g + uint32_t(k);
+            uint32_t n = 0;
+            while (!mbar_try_wait(&bars[gk % kTmaStages], (gk / kTmaStages) & 1u) &&
+                   ++n < kSpinLimit) {
+            }
+          }
+          break;
+        }
+        const int t = i / pieces, pc = i - t * pieces;
+        const int64_t off = int64_t(pc) * piece_bytes;
+        const uint32_t bytes = uint32_t(row_bytes - off < piece_bytes ? row_bytes - off : piece_bytes);
+        const unsigned char* src = stages + size_t(st) * piece_bytes;
+        for (int d = 0; d < R; ++d) {
+          const int row = table[t * R + d];
+          if (row >= 0 && int64_t(row) < recv_capacity)
+            bulk_s2g(recv_x + int64_t(row) * row_bytes + off, src, bytes);
+        }
+        bulk_commit();
+        const int j = i - kTmaLag;  // refill the stage of item j with item j + NS
+        if (j >= 0 && j + kTmaStages < nitems) {
+          bulk_wait_read<kTmaLag>();
+          issue_load(j + kTmaStages);
+          ++issued;
+        }
+      }
+      bulk_wait_read<0>();  // every stage free again before the next chunk
+      g += uint32_t(nitems);
+    }
+    __syncwarp();
+    if (spr > 0) {  // e4m3 scales travel with the rows (plain copies by the warp)
+      for (int t = 0; t < nt; ++t)
+        for (int d = 0; d < R; ++d) {
+          const int row = table[t * R + d];
+          if (row >= 0 && int64_t(row) < recv_capacity)
+            for (int c = lane; c < spr; c += kWarp)
+              recv_scales[int64_t(row) * spr + c] = __ldg(x_scales + (tok0 + t) * spr + c);
+        }
+    }
+    __syncwarp();
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch with in-kernel FP8 quantisation (same page: E4M3 payloads with
+// FP32 scales).  Each 128-channel block of a bf16 token row gets
+// scale = amax / 448 (1 when the block is all zero) and codes
+// e4m3_rn_satfinite(x / scale); the e4m3 row and its scales are written to
+// every destination row.  Reading x once as bf16 and writing 1 byte per
+// channel per destination roughly halves the traffic of a bf16 dispatch.
+// A lane holds 8 channels (one 16-byte load); 16 lanes make a block.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int U>
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
+                 unsigned char* __restrict__ recv_x, float* __restrict__ recv_scales,
+                 int64_t recv_capacity, const int32_t* __restrict__ send_row) {
+  const int lane = threadIdx.x & 31;
+  const int64_t vpr = H / 8;  // 8-channel vectors per row
+  const int nb = H / 128;     // scale blocks per row
+  const int64_t slab_vec = int64_t(kWarp) * U;
+  const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
+  const int64_t units = tokens * slabs;
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
+       unit += nw) {
+    const int64_t tok = unit / slabs;
+    const int64_t slab = unit - tok * slabs;
+    const int my = lane < R ? __ldg(send_row + tok * R + lane) : -1;
+    unsigned vm = __ballot_sync(kFull, my >= 0 && int64_t(my) < recv_capacity);
+    if (vm == 0) continue;
+    const int64_t i0 = slab * slab_vec + lane;
+    uint2 q[U];
+    float scale[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * kWarp;
+      const bool valid = i < vpr;  // whole 16-lane blocks are valid or not (H % 128 == 0)
+      Words<4> v;
+      float f[8];
+      float amax = 0.0f;
+      if (valid) {
+        v = ld_stream_w<4>(x + tok * vpr + i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[2 * j] = __uint_as_float(v.w[j] << 16);
+          f[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      scale[u] = sc;
+      if (valid) {
+        uint32_t b[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = cvt_e4m3x2(__fdiv_rn(f[2 * j + 1], sc), __fdiv_rn(f[2 * j], sc));
+        q[u] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+      }
+    }
+    while (vm) {
+      const int d = __ffs(vm) - 1;
+      vm &= vm - 1;
+      const int64_t row = __shfl_sync(kFull, my, d);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + u * kWarp;
+        if (i < vpr) {
+          unsigned char* dst = recv_x + row * H + i * 8;
+          asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(q[u].x),
+                       "r"(q[u].y)
+                       : "memory");
+          if ((lane & 15) == 0) recv_scales[row * nb + i / 16] = scale[u];
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Combine (same page: intranode_combine runs in the reverse direction of
 // dispatch).  out[s][t] = bf16_rn( sum_{d ascending} float(y[send_row[s][t][d]]) )
-// from +0.0f.  Up to 8 source rows are loaded at once (memory-level
+// from +0.0f.  Up to RB source rows are loaded at once (memory-level
 // parallelism) and then added strictly in ascending d.
 // ---------------------------------------------------------------------------
-template <int U>
-__global__ void __launch_bounds__(kCopyThreads, 2)
-mp_k_combine(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ y, int64_t y_rows,
-             const int32_t* __restrict__ send_row, int4* __restrict__ out,
+template <int NW, int U, int RB>
+__global__ void __launch_bounds__(kCopyThreads, MP_COMBINE_MINB)
+mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y, int64_t y_rows,
+             const int32_t* __restrict__ send_row, Words<NW>* __restrict__ out,
              int32_t* __restrict__ dev_err) {
   const int lane = threadIdx.x & 31;
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
   const int64_t units = tokens * slabs;
-  const int64_t nw = int64_t(gridDim.x) * (kCopyThreads / kWarp);
-  for (int64_t unit = int64_t(blockIdx.x) * (kCopyThreads / kWarp) + (threadIdx.x >> 5);
-       unit < units; unit += nw) {
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
+       unit += nw) {
     const int64_t tok = unit / slabs;
     const int64_t slab = unit - tok * slabs;
     int my = lane < R ? __ldg(send_row + tok * R + lane) : -1;
@@ -91,15 +323,15 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ y, int
     }
     unsigned vm = __ballot_sync(kFull, my >= 0);
     const int64_t i0 = slab * slab_vec + lane;
-    float acc[U][8];
+    float acc[U][2 * NW];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+      for (int j = 0; j < 2 * NW; ++j) acc[u][j] = 0.0f;
     while (vm) {
-      int64_t rows[8];
+      int64_t rows[RB];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < RB; ++j) {
         rows[j] = -1;
         if (vm) {
           const int d = __ffs(vm) - 1;
@@ -107,22 +339,23 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ y, int
           rows[j] = __shfl_sync(kFull, my, d);
         }
       }
-      int4 v[8][U];
+      Words<NW> v[RB][U];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < RB; ++j)
 #pragma unroll
         for (int u = 0; u < U; ++u)
           if (rows[j] >= 0 && i0 + u * kWarp < vpr)
-            v[j][u] = ld_stream(y + rows[j] * vpr + i0 + u * kWarp);
+            v[j][u] = ld_stream_w<NW>(y + rows[j] * vpr + i0 + u * kWarp);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < RB; ++j)
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (rows[j] >= 0 && i0 + u * kWarp < vpr) add_bf16x8(acc[u], v[j][u]);
+          if (rows[j] >= 0 && i0 + u * kWarp < vpr) add_bf16<NW>(acc[u], v[j][u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < vpr) st_stream(out + tok * vpr + i0 + u * kWarp, pack_bf16x8(acc[u]));
+      if (i0 + u * kWarp < vpr)
+        st_stream_w<NW>(out + tok * vpr + i0 + u * kWarp, pack_bf16<NW>(acc[u]));
   }
 }
 
@@ -133,51 +366,53 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const int4* __restrict__ y, int
 // element-wise fp32 sum over q ascending, rounded once; rank r's shard is a
 // row range of the output.
 // ---------------------------------------------------------------------------
+template <int NW>
 __global__ void __launch_bounds__(kCopyThreads)
-mp_k_rsv(int R, int64_t nvec, const int4* __restrict__ in, int4* __restrict__ out) {
+mp_k_rsv(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __restrict__ out) {
   const int64_t stride = int64_t(gridDim.x) * kCopyThreads;
   for (int64_t i = int64_t(blockIdx.x) * kCopyThreads + threadIdx.x; i < nvec; i += stride) {
-    float acc[8];
+    float acc[2 * NW];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < 2 * NW; ++j) acc[j] = 0.0f;
     for (int q0 = 0; q0 < R; q0 += 8) {
-      int4 v[8];
+      Words<NW> v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (q0 + j < R) v[j] = ld_stream(in + int64_t(q0 + j) * nvec + i);
+        if (q0 + j < R) v[j] = ld_stream_w<NW>(in + int64_t(q0 + j) * nvec + i);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (q0 + j < R) add_bf16x8(acc, v[j]);
+        if (q0 + j < R) add_bf16<NW>(acc, v[j]);
     }
-    st_stream(out + i, pack_bf16x8(acc));
+    st_stream_w<NW>(out + i, pack_bf16<NW>(acc));
   }
 }
 
 // ---------------------------------------------------------------------------
 // All-gatherv (same page: one broadcast per root of its rows into every
 // rank's output).  Every logical rank's copy is the concatenated shards, so
-// each 16-byte vector is read once and written R times.
+// each vector is read once and written R times.
 // ---------------------------------------------------------------------------
+template <int NW, int U>
 __global__ void __launch_bounds__(kCopyThreads)
-mp_k_agv(int R, int64_t nvec, const int4* __restrict__ in, int4* __restrict__ out) {
-  constexpr int U = 4;
+mp_k_agv(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __restrict__ out) {
   const int64_t stride = int64_t(gridDim.x) * kCopyThreads * U;
   for (int64_t i0 = int64_t(blockIdx.x) * kCopyThreads * U + threadIdx.x; i0 < nvec;
        i0 += stride) {
-    int4 v[U];
+    Words<NW> v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (i0 + u * kCopyThreads < nvec) v[u] = ld_stream(in + i0 + u * kCopyThreads);
+      if (i0 + u * kCopyThreads < nvec) v[u] = ld_stream_w<NW>(in + i0 + u * kCopyThreads);
     for (int q = 0; q < R; ++q)
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (i0 + u * kCopyThreads < nvec) st_stream(out + int64_t(q) * nvec + i0 + u * kCopyThreads, v[u]);
+        if (i0 + u * kCopyThreads < nvec)
+          st_stream_w<NW>(out + int64_t(q) * nvec + i0 + u * kCopyThreads, v[u]);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Launchers: a persistent grid of (SMs x resident blocks) blocks, trimmed to
-// the work available.
+// the work available; 32-byte vectors when sizes and pointers allow.
 // ---------------------------------------------------------------------------
 template <typename Kernel>
 static int resident_blocks(Kernel k) {
@@ -187,28 +422,106 @@ static int resident_blocks(Kernel k) {
   return n;
 }
 
-static unsigned grid_for(int per_sm, int64_t work_items_per_block_unit, int64_t items) {
+static unsigned grid_for(int per_sm, int64_t items_per_block, int64_t items) {
   const int64_t full = int64_t(sm_count()) * per_sm;
-  const int64_t need = (items + work_items_per_block_unit - 1) / work_items_per_block_unit;
+  const int64_t need = (items + items_per_block - 1) / items_per_block;
   return unsigned(need < 1 ? 1 : (need < full ? need : full));
 }
 
-constexpr int kDispatchU = 4;
-constexpr int kCombineU = 2;
+static bool aligned(const void* p, int bytes) {
+  return (reinterpret_cast<uintptr_t>(p) % uintptr_t(bytes)) == 0;
+}
+
+template <int NW, int U>
+static cudaError_t dispatch_copy_nw(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                    void* recv_x, int64_t recv_capacity, const int32_t* send_row,
+                                    int spr, const float* x_scales, float* recv_scales,
+                                    cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_dispatch<NW, U>);
+  const int64_t vpr = row_bytes / (4 * NW);
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+  mp_k_dispatch<NW, U><<<grid, kCopyThreads, 0, stream>>>(
+      R, tokens, vpr, static_cast<const Words<NW>*>(x), static_cast<Words<NW>*>(recv_x),
+      recv_capacity, send_row, spr, x_scales, recv_scales);
+  return cudaGetLastError();
+}
+
+static cudaError_t dispatch_copy_tma(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                     void* recv_x, int64_t recv_capacity,
+                                     const int32_t* send_row, int spr, const float* x_scales,
+                                     float* recv_scales, int32_t* dev_err, cudaStream_t stream) {
+  const uint32_t piece = uint32_t(row_bytes < kTmaPiece ? row_bytes : kTmaPiece);
+  const int pieces = int((row_bytes + piece - 1) / piece);
+  const size_t smem = tma_smem_bytes(piece);
+  static thread_local int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < int(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(mp_k_dispatch_tma,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = int(smem);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mp_k_dispatch_tma, kWarp, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t chunks = (tokens + kTmaChunk - 1) / kTmaChunk;
+  const unsigned grid = grid_for(per_sm, 1, chunks);
+  mp_k_dispatch_tma<<<grid, kWarp, smem, stream>>>(
+      R, tokens, row_bytes, piece, pieces, static_cast<const unsigned char*>(x),
+      static_cast<unsigned char*>(recv_x), recv_capacity, send_row, spr, x_scales, recv_scales,
+      dev_err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const void* x,
                                  void* recv_x, int64_t recv_capacity, const int32_t* send_row,
-                                 int scales_per_row,
-                                 const float* x_scales, float* recv_scales, cudaStream_t stream) {
+                                 int scales_per_row, const float* x_scales, float* recv_scales,
+                                 cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  static int per_sm = resident_blocks(mp_k_dispatch<kDispatchU>);
-  const int64_t vpr = row_bytes / 16;
-  const int64_t slabs = (vpr + kWarp * kDispatchU - 1) / (kWarp * kDispatchU);
-  const unsigned grid = grid_for(per_sm, kCopyThreads / kWarp, tokens * slabs);
-  mp_k_dispatch<kDispatchU><<<grid, kCopyThreads, 0, stream>>>(
-      R, tokens, vpr, static_cast<const int4*>(x), static_cast<int4*>(recv_x), recv_capacity,
-      send_row,
-      scales_per_row, x_scales, recv_scales);
+  if (MP_DISPATCH_TMA)
+    return dispatch_copy_tma(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
+                             scales_per_row, x_scales, recv_scales, nullptr, stream);
+  if (MP_DISPATCH_NW == 8 && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
+    return dispatch_copy_nw<MP_DISPATCH_NW, MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x,
+                                                           recv_capacity, send_row,
+                                                           scales_per_row, x_scales, recv_scales,
+                                                           stream);
+  return dispatch_copy_nw<4, 2 * MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
+                                                send_row, scales_per_row, x_scales, recv_scales,
+                                                stream);
+}
+
+cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
+                                  float* recv_scales, int64_t recv_capacity,
+                                  const int32_t* send_row, cudaStream_t stream) {
+  if (tokens == 0) return cudaSuccess;
+  constexpr int U = 4;
+  static const int per_sm = resident_blocks(mp_k_dispatch_q8<U>);
+  const int64_t vpr = H / 8;
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+  mp_k_dispatch_q8<U><<<grid, kCopyThreads, 0, stream>>>(
+      R, tokens, H, static_cast<const Words<4>*>(x), static_cast<unsigned char*>(recv_x),
+      recv_scales, recv_capacity, send_row);
+  return cudaGetLastError();
+}
+
+template <int NW, int U, int RB>
+static cudaError_t combine_nw(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
+                              const int32_t* send_row, void* out, int32_t* dev_err,
+                              cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_combine<NW, U, RB>);
+  const int64_t vpr = int64_t(H) * 2 / (4 * NW);
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+  mp_k_combine<NW, U, RB><<<grid, kCopyThreads, 0, stream>>>(
+      R, tokens, vpr, static_cast<const Words<NW>*>(y), y_rows, send_row,
+      static_cast<Words<NW>*>(out), dev_err);
   return cudaGetLastError();
 }
 
@@ -216,36 +529,50 @@ cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t 
                            const int32_t* send_row, void* out, int32_t* dev_err,
                            cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  static int per_sm = resident_blocks(mp_k_combine<kCombineU>);
-  const int64_t vpr = int64_t(H) / 8;
-  const int64_t slabs = (vpr + kWarp * kCombineU - 1) / (kWarp * kCombineU);
-  const unsigned grid = grid_for(per_sm, kCopyThreads / kWarp, tokens * slabs);
-  mp_k_combine<kCombineU><<<grid, kCopyThreads, 0, stream>>>(
-      R, tokens, vpr, static_cast<const int4*>(y), y_rows, send_row, static_cast<int4*>(out),
-      dev_err);
+  if (MP_COMBINE_NW == 8 && (int64_t(H) * 2) % 32 == 0 && aligned(y, 32) && aligned(out, 32))
+    return combine_nw<MP_COMBINE_NW, MP_COMBINE_U, MP_COMBINE_RB>(R, tokens, H, y, y_rows,
+                                                                  send_row, out, dev_err, stream);
+  return combine_nw<4, 2 * MP_COMBINE_U, MP_COMBINE_RB>(R, tokens, H, y, y_rows, send_row, out,
+                                                       dev_err, stream);
+}
+
+template <int NW>
+static cudaError_t rsv_nw(int R, int64_t bytes_per_rank, const void* in, void* out,
+                          cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_rsv<NW>);
+  const int64_t nvec = bytes_per_rank / (4 * NW);
+  const unsigned grid = grid_for(per_sm, kCopyThreads, nvec);
+  mp_k_rsv<NW><<<grid, kCopyThreads, 0, stream>>>(R, nvec, static_cast<const Words<NW>*>(in),
+                                                   static_cast<Words<NW>*>(out));
   return cudaGetLastError();
 }
 
 cudaError_t launch_reducescatterv(int R, int64_t S, int H, const void* in, void* out,
                                   cudaStream_t stream) {
-  const int64_t nvec = S * H / 8;
-  if (nvec == 0) return cudaSuccess;
-  static int per_sm = resident_blocks(mp_k_rsv);
-  const unsigned grid = grid_for(per_sm, kCopyThreads, nvec);
-  mp_k_rsv<<<grid, kCopyThreads, 0, stream>>>(R, nvec, static_cast<const int4*>(in),
-                                               static_cast<int4*>(out));
+  const int64_t bytes = S * H * 2;
+  if (bytes == 0) return cudaSuccess;
+  if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32))
+    return rsv_nw<8>(R, bytes, in, out, stream);
+  return rsv_nw<4>(R, bytes, in, out, stream);
+}
+
+template <int NW, int U>
+static cudaError_t agv_nw(int R, int64_t bytes, const void* in, void* out, cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_agv<NW, U>);
+  const int64_t nvec = bytes / (4 * NW);
+  const unsigned grid = grid_for(per_sm, int64_t(kCopyThreads) * U, nvec);
+  mp_k_agv<NW, U><<<grid, kCopyThreads, 0, stream>>>(R, nvec, static_cast<const Words<NW>*>(in),
+                                                      static_cast<Words<NW>*>(out));
   return cudaGetLastError();
 }
 
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream) {
-  const int64_t nvec = S * row_bytes / 16;
-  if (nvec == 0) return cudaSuccess;
-  static int per_sm = resident_blocks(mp_k_agv);
-  const unsigned grid = grid_for(per_sm, kCopyThreads * 4, nvec);
-  mp_k_agv<<<grid, kCopyThreads, 0, stream>>>(R, nvec, static_cast<const int4*>(in),
-                                               static_cast<int4*>(out));
-  return cudaGetLastError();
+  const int64_t bytes = S * row_bytes;
+  if (bytes == 0) return cudaSuccess;
+  if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32))
+    return agv_nw<8, 2>(R, bytes, in, out, stream);
+  return agv_nw<4, 4>(R, bytes, in, out, stream);
 }
 
 }  // namespace mp

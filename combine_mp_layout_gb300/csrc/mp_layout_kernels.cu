@@ -3,19 +3,22 @@
 // Layout ("MSCCLPP EP implementation", microsoft/mscclpp PR #852, port
 // scope: get_dispatch_layout computes counts and token-in-rank).  One block
 // per (source rank, 256-token slice); warp ballots build the per-rank
-// counts, a shared-memory histogram the per-expert counts.  The last block
-// of each source rank to finish adds the per-block partials in block order.
+// counts, a shared-memory histogram the per-expert counts.  Blocks add their
+// counts into a per-rank accumulator (integer adds: order-free, exact) and
+// the last block of each rank copies the totals out.
 //
 // Scan (the counterpart of the notify/prefix-matrix step of the same port,
 // here a single-pass decoupled lookback).  The receive row of token (s,t)
 // at destination d is
-//     dest_base[d] + #{(s',t') < (s,t) in flattened order with bit d},
-// dest_base[d] = rows of all destinations < d.  The flattened (s,t) axis is
-// cut into 256-token tiles; each tile publishes its R-wide count vector,
-// looks back over its predecessors for the exclusive prefix, publishes the
-// inclusive prefix and writes the rows' metadata.  Tiles are handed out in
-// launch order through an atomic counter, so every tile a block waits on
-// belongs to a block that is already running.
+//     dest_base[d] + rank_prefix[s][d] + #{t' < t : bit d of token (s,t')},
+// dest_base[d] = rows of all destinations < d, rank_prefix[s][d] = rows of d
+// from source ranks < s (both sums of num_tokens_per_rank).  Each source
+// rank's tokens are cut into 128-token tiles; each tile publishes its R-wide
+// count vector, looks back over the earlier tiles of its rank for the
+// exclusive prefix, publishes the inclusive prefix and writes the rows'
+// metadata.  Tiles are handed out in launch order through an atomic
+// counter, so every tile a block waits on belongs to a block that is
+// already running.
 #include <cstdint>
 
 #include "mp_common.cuh"
@@ -32,8 +35,8 @@ mp_k_layout(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
             uint32_t* __restrict__ is_token_in_rank, int32_t* __restrict__ dev_err,
             unsigned char* __restrict__ ws) {
   extern __shared__ int32_t sm_layout[];
-  int32_t* hist = sm_layout;            // [E]
-  int32_t* rcount = sm_layout + E;      // [R]
+  int32_t* hist = sm_layout;               // [E]
+  int32_t* rcount = sm_layout + E;         // [MP_MAX_RANKS]
   int32_t* idx_s = rcount + MP_MAX_RANKS;  // [kLayoutTokens * K]
   __shared__ int last_block;
 
@@ -49,7 +52,11 @@ mp_k_layout(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
   if (tid < MP_MAX_RANKS) rcount[tid] = 0;
   // stage this slice's topk_idx with coalesced loads
   const int32_t* src = topk_idx + (int64_t(s) * N + t0) * K;
-  for (int i = tid; i < ntok * K; i += blockDim.x) idx_s[i] = src[i];
+  {
+    const int n = ntok * K;
+#pragma unroll 4
+    for (int i = tid; i < n; i += kLayoutTokens) idx_s[i] = __ldg(src + i);
+  }
   __syncthreads();
 
   uint32_t mask = 0;
@@ -77,37 +84,45 @@ mp_k_layout(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
     return;
   }
 
+  // Several blocks per source rank: add this block's counts into the rank's
+  // accumulator (integer adds, so the order of the blocks does not matter);
+  // the last block to finish copies the totals out and zeroes the
+  // accumulator for the next call.
   Control* ctl = reinterpret_cast<Control*>(ws);
-  int32_t* part = reinterpret_cast<int32_t*>(ws + ws_partials_offset()) +
-                  (int64_t(s) * C + c) * (E + R);
-  for (int i = tid; i < E; i += blockDim.x) part[i] = hist[i];
-  if (tid < R) part[E + tid] = rcount[tid];
+  int32_t* acc = reinterpret_cast<int32_t*>(ws + ws_acc_offset()) + int64_t(s) * (E + R);
+  for (int i = tid; i < E; i += blockDim.x)
+    if (hist[i]) atomicAdd(&acc[i], hist[i]);
+  if (tid < R && rcount[tid]) atomicAdd(&acc[E + tid], rcount[tid]);
   __threadfence();
   __syncthreads();
   if (tid == 0) last_block = (atomicAdd(&ctl->layout_done[s], 1u) == unsigned(C - 1));
   __syncthreads();
   if (!last_block) return;
   __threadfence();
-  const int32_t* base = reinterpret_cast<const int32_t*>(ws + ws_partials_offset()) +
-                        int64_t(s) * C * (E + R);
   for (int i = tid; i < E + R; i += blockDim.x) {
-    int sum = 0;
-    for (int b = 0; b < C; ++b) sum += ld_cg_i32(base + int64_t(b) * (E + R) + i);
-    if (i < E) num_tokens_per_expert[int64_t(s) * E + i] = sum;
-    else num_tokens_per_rank[s * R + (i - E)] = sum;
+    const int v = __ldcg(acc + i);
+    acc[i] = 0;
+    if (i < E) num_tokens_per_expert[int64_t(s) * E + i] = v;
+    else num_tokens_per_rank[s * R + (i - E)] = v;
   }
-  if (tid == 0) ctl->layout_done[s] = 0;  // leave the workspace zeroed for the next call
+  if (tid == 0) ctl->layout_done[s] = 0;
 }
 
 // ---------------------------------------------------------------------------
 // Receive-offset scan (decoupled lookback) + row metadata
 // ---------------------------------------------------------------------------
-// Tile state word: [63:62] flag (1 = aggregate only, 2 = inclusive prefix),
-// [61:32] launch epoch (30 bits), [31:0] count.
-constexpr uint64_t kFlagAggregate = 1ull << 62;
-constexpr uint64_t kFlagInclusive = 2ull << 62;
-__device__ __forceinline__ uint64_t make_state(uint64_t flag, uint32_t epoch, uint32_t v) {
-  return flag | (uint64_t(epoch & 0x3fffffffu) << 32) | v;
+// Tile record: flag word (epoch << 2 | status, status 1 = aggregate counts
+// published, 2 = inclusive prefix published), then R aggregate counts and R
+// inclusive prefixes.  A single thread writes a record's counts and then
+// releases its flag, so a reader that acquires the flag sees the counts.
+// The scan is segmented by source rank: the rows of source rank s start, at
+// destination d, at dest_base[d] + rank_prefix[s][d] (both sums of
+// num_tokens_per_rank), so a tile only looks back over the earlier tiles of
+// its own rank and the first tile of each rank is inclusive at once.
+constexpr uint32_t kStatusAggregate = 1u;
+constexpr uint32_t kStatusInclusive = 2u;
+__device__ __forceinline__ uint32_t make_flag(uint32_t epoch, uint32_t status) {
+  return (epoch << 2) | status;
 }
 
 struct ScanArgs {
@@ -132,48 +147,65 @@ struct ScanArgs {
 
 constexpr int kScanWarps = kScanTokens / kWarp;
 
+// Warp-wide sum; every lane gets the total.
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
 __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
   extern __shared__ int32_t sm_scan[];
-  int32_t* idx_s = sm_scan;                               // [kScanTokens * K]
+  int32_t* idx_s = sm_scan;                                             // [kScanTokens * K]
   float* w_s = reinterpret_cast<float*>(sm_scan + kScanTokens * a.K);  // [kScanTokens * K]
-  __shared__ uint32_t wball[kScanWarps][MP_MAX_RANKS];    // per-warp ballots
-  __shared__ int32_t woff[kScanWarps][MP_MAX_RANKS];      // per-warp exclusive offsets
-  __shared__ int64_t row_base[MP_MAX_RANKS];              // dest_base[d] + tile prefix
-  __shared__ int32_t tot[MP_MAX_RANKS];
+  int32_t* sr_s = sm_scan + 2 * kScanTokens * a.K;                      // [kScanTokens * R]
+  __shared__ int32_t ntpr_s[MP_MAX_RANKS * MP_MAX_RANKS];  // num_tokens_per_rank
+  __shared__ uint32_t wball[kScanWarps][MP_MAX_RANKS];     // per-warp ballots
+  __shared__ int32_t woff[kScanWarps][MP_MAX_RANKS];       // per-warp exclusive offsets
+  __shared__ uint32_t tcount[MP_MAX_RANKS];                // tile counts, then inclusive prefix
+  __shared__ uint32_t tcnt[MP_MAX_RANKS];                  // tile counts
+  __shared__ int64_t row_base[MP_MAX_RANKS];               // first receive row of the tile at d
+  __shared__ uint8_t tok_of[MP_MAX_RANKS][kScanTokens];    // [d][rank within d] -> token
   __shared__ uint32_t sh_tile, sh_epoch;
   __shared__ int sh_last;
 
   const int R = a.R, N = a.N, K = a.K, E = a.E;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Control* ctl = reinterpret_cast<Control*>(a.ws);
-  uint64_t* state = reinterpret_cast<uint64_t*>(a.ws + ws_status_offset(R, N, E));
-  const int64_t T = int64_t(R) * N;
+  uint32_t* flags = reinterpret_cast<uint32_t*>(a.ws + ws_flags_offset(R, E));
+  uint32_t* agg = reinterpret_cast<uint32_t*>(a.ws + ws_agg_offset(R, N, E));
+  uint32_t* incl = reinterpret_cast<uint32_t*>(a.ws + ws_incl_offset(R, N, E));
+  const int C = int(scan_tiles_per_rank(N));
 
   if (tid == 0) {
-    sh_epoch = ld_relaxed_u32(&ctl->scan_epoch);
+    sh_epoch = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
     sh_tile = atomicAdd(&ctl->scan_tile_counter, 1u);
   }
-  // totals per destination (independent of the tile)
-  if (tid < R) {
-    int sum = 0;
-    for (int s = 0; s < R; ++s) sum += a.num_tokens_per_rank[s * R + tid];
-    tot[tid] = sum;
-  }
+  for (int i = tid; i < R * R; i += blockDim.x) ntpr_s[i] = __ldg(a.num_tokens_per_rank + i);
   __syncthreads();
   const uint32_t tile = sh_tile, epoch = sh_epoch;
   if (tile >= gridDim.x) {  // only possible if the workspace was not zero-filled
     if (tid == 0) raise_error(a.dev_err, MP_ERR_INVALID_ARG);
     return;
   }
-  const int64_t g0 = int64_t(tile) * kScanTokens;
-  const int ntok = int(T - g0 < kScanTokens ? T - g0 : kScanTokens);
+  const int src_rank = int(tile / uint32_t(C));
+  const int c = int(tile - uint32_t(src_rank) * uint32_t(C));  // tile index within the rank
+  const int t0 = c * kScanTokens;
+  const int ntok = min(kScanTokens, N - t0);
+  const int64_t g0 = int64_t(src_rank) * N + t0;  // first token, flattened (s, t)
 
-  // stage this tile's topk rows (contiguous along the flattened axis)
-  for (int i = tid; i < ntok * K; i += blockDim.x) {
-    idx_s[i] = a.topk_idx[g0 * K + i];
-    w_s[i] = a.topk_weights[g0 * K + i];
+  // the mask first (the aggregate depends on it), the topk rows alongside
+  const uint32_t mask = tid < ntok ? __ldg(a.is_token_in_rank + g0 + tid) : 0u;
+  {
+    const int n = ntok * K;
+    const int32_t* gi = a.topk_idx + g0 * K;
+    const float* gw = a.topk_weights + g0 * K;
+#pragma unroll 4
+    for (int i = tid; i < n; i += kScanTokens) {
+      idx_s[i] = __ldg(gi + i);
+      w_s[i] = __ldg(gw + i);
+    }
   }
-  const uint32_t mask = tid < ntok ? a.is_token_in_rank[g0 + tid] : 0u;
   for (int d = 0; d < R; ++d) {
     const unsigned b = __ballot_sync(kFull, (mask >> d) & 1u);
     if (lane == 0) wball[warp][d] = b;
@@ -181,106 +213,162 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
   __syncthreads();
 
   if (warp == 0) {
-    // lane d: the tile's count for destination d and per-warp offsets
-    int cnt = 0;
+    // lane d: the tile's count for destination d and the per-warp offsets
+    uint32_t cnt = 0;
     if (lane < R) {
       for (int w = 0; w < kScanWarps; ++w) {
-        woff[w][lane] = cnt;
+        woff[w][lane] = int32_t(cnt);
         cnt += __popc(wball[w][lane]);
       }
+      tcount[lane] = cnt;
+      tcnt[lane] = cnt;
     }
-    // destination bases: exclusive scan of the totals over d
-    int incl = lane < R ? tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int dest_base = incl - (lane < R ? tot[lane] : 0);
-    const int total_rows = __shfl_sync(kFull, incl, R - 1);
-
-    int64_t excl = 0;
-    if (lane < R) {
-      uint64_t* my = state + int64_t(tile) * R + lane;
-      if (tile == 0) {
-        st_release_u64(my, make_state(kFlagInclusive, epoch, uint32_t(cnt)));
-      } else {
-        st_release_u64(my, make_state(kFlagAggregate, epoch, uint32_t(cnt)));
-        // walk back until a predecessor with an inclusive prefix
-        int64_t j = int64_t(tile) - 1;
-        bool timed_out = false;
-        while (j >= 0) {
-          const uint64_t* p = state + j * R + lane;
-          uint64_t v = ld_acquire_u64(p);
+    __syncwarp();
+    const int64_t rec = int64_t(tile) * R;
+    uint32_t excl = 0;  // lane d: rows of destination d in this rank's earlier tiles
+    if (c == 0) {
+      if (lane == 0) {
+        for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
+        st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
+      }
+    } else {
+      if (lane == 0) {
+        for (int d = 0; d < R; ++d) agg[rec + d] = tcount[d];
+        st_release_u32(&flags[tile], make_flag(epoch, kStatusAggregate));
+      }
+      // Look back over up to 32 earlier tiles of this rank at a time (lane j
+      // looks at tile base - j), stopping at the nearest one whose inclusive
+      // prefix is out.  Every wait is bounded (MP_ERR_TIMEOUT).
+      const int64_t first = int64_t(src_rank) * C;
+      bool timed_out = false;
+      for (int64_t base = int64_t(tile) - 1; base >= first; base -= 32) {
+        const int64_t p = base - lane;
+        uint32_t status = 0;
+        if (p >= first) {
+          uint32_t f = ld_acquire_u32(&flags[p]);
           uint32_t spins = 0, nap = 32;
-          while (((v >> 32) & 0x3fffffffu) != (epoch & 0x3fffffffu) || (v >> 62) == 0) {
+          while ((f >> 2) != epoch || (f & 3u) == 0) {
             if (++spins > kSpinLimit) { timed_out = true; break; }
             __nanosleep(nap);
             if (nap < 1024) nap <<= 1;
-            v = ld_acquire_u64(p);
+            f = ld_acquire_u32(&flags[p]);
           }
-          if (timed_out) break;
-          excl += uint32_t(v);
-          if ((v >> 62) == 2) break;
-          --j;
+          status = timed_out ? kStatusInclusive : (f & 3u);
         }
-        if (timed_out) raise_error(a.dev_err, MP_ERR_TIMEOUT);
-        st_release_u64(my, make_state(kFlagInclusive, epoch, uint32_t(excl + cnt)));
+        const unsigned inclusive = __ballot_sync(kFull, p >= first && status == kStatusInclusive);
+        const int stop = inclusive ? __ffs(inclusive) - 1 : 31;
+        const bool use = p >= first && lane <= stop && !timed_out;
+        const uint32_t* src = status == kStatusInclusive ? incl : agg;
+        uint32_t v[MP_MAX_RANKS];
+#pragma unroll
+        for (int d = 0; d < MP_MAX_RANKS; ++d)
+          v[d] = (use && d < R) ? __ldcg(src + p * R + d) : 0u;
+#pragma unroll
+        for (int d = 0; d < MP_MAX_RANKS; ++d) {
+          if (d < R) {
+            const uint32_t sum = warp_sum(v[d]);
+            if (lane == d) excl += sum;
+          }
+        }
+        if (__any_sync(kFull, timed_out) || inclusive) break;
       }
-      row_base[lane] = int64_t(dest_base) + excl;
+      if (__any_sync(kFull, timed_out) && lane == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
+      if (lane < R) tcount[lane] += excl;  // inclusive prefix through this tile
+      __syncwarp();
+      if (lane == 0) {
+        for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
+        st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
+      }
     }
-    // the first tile also writes the small per-destination tables
-    if (tile == 0) {
-      if (lane < R) a.dest_offsets[lane] = dest_base;
-      if (lane == 0) a.dest_offsets[R] = total_rows;
+    // first row of this tile at d: rows of destinations < d (an exclusive
+    // warp scan of the per-destination totals), rows of d from source ranks
+    // < src_rank, rows of d from this rank's earlier tiles
+    int64_t tot = 0, pre = 0;
+    if (lane < R) {
+      for (int s = 0; s < R; ++s) {
+        const int v = ntpr_s[s * R + lane];
+        tot += v;
+        if (s < src_rank) pre += v;
+      }
+    }
+    int64_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane < R) row_base[lane] = (inc - tot) + pre + excl;
+  } else if (tile == 0) {
+    // warps 1..: the small per-destination tables, while warp 0 publishes
+    const int t = tid - kWarp, nt = kScanTokens - kWarp;
+    for (int i = t; i < R * R; i += nt) {  // rank_prefix[s][d]
+      const int s = i / R, d = i - s * R;
+      int sum = 0;
+      for (int q = 0; q < s; ++q) sum += ntpr_s[q * R + d];
+      a.rank_prefix[i] = sum;
+    }
+    for (int d = t; d <= R; d += nt) {  // dest_offsets
+      int sum = 0;
+      for (int q = 0; q < R * R; ++q)
+        if ((q - (q / R) * R) < d) sum += ntpr_s[q];
+      a.dest_offsets[d] = sum;
+    }
+    for (int e = t; e < E; e += nt) {  // num_recv_tokens_per_expert[d][j], e = d*E/R + j
+      int sum = 0;
+#pragma unroll 8
+      for (int s = 0; s < R; ++s) sum += __ldg(a.num_tokens_per_expert + int64_t(s) * E + e);
+      a.num_recv_tokens_per_expert[e] = sum;
     }
   }
   __syncthreads();
 
-  // rows of this thread's token
+  // Each token's row at each destination: staged in shared memory (send_row)
+  // and as a per-destination token list, so that the stores below run along
+  // contiguous rows (a tile's rows for one destination are consecutive).
   if (tid < ntok) {
-    const int64_t g = g0 + tid;
-    const int s = int(g / N), t = int(g - int64_t(s) * N);
-    const int El = E / R;
-    int32_t* sr = a.send_row + g * R;
-    bool overflow = false;
     for (int d = 0; d < R; ++d) {
       int32_t out = -1;
       if ((mask >> d) & 1u) {
-        const int64_t row = row_base[d] + woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
-        if (row < a.recv_capacity) {
-          out = int32_t(row);
-          a.recv_src_rank[row] = s;
-          a.recv_src_idx[row] = t;
-          const int lo = d * El, hi = lo + El;
-          for (int k = 0; k < K; ++k) {
-            const int e = idx_s[tid * K + k];
-            const bool local = e >= lo && e < hi;
-            a.recv_topk_idx[row * K + k] = local ? e - lo : -1;
-            a.recv_topk_weights[row * K + k] = local ? w_s[tid * K + k] : 0.0f;
-          }
-        } else {
-          overflow = true;
-        }
+        const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
+        tok_of[d][rank] = uint8_t(tid);
+        const int64_t row = row_base[d] + rank;
+        if (row < a.recv_capacity) out = int32_t(row);
       }
-      sr[d] = out;
+      sr_s[tid * R + d] = out;
     }
-    if (overflow) raise_error(a.dev_err, MP_ERR_CAPACITY);
   }
-
-  if (tile == 0) {
-    // rank_prefix[s][d] = rows of d from sources < s; per-expert receive counts
-    for (int i = tid; i < R * R; i += blockDim.x) {
-      const int s = i / R, d = i - s * R;
-      int sum = 0;
-      for (int q = 0; q < s; ++q) sum += a.num_tokens_per_rank[q * R + d];
-      a.rank_prefix[i] = sum;
+  __syncthreads();
+  for (int i = tid; i < ntok * R; i += kScanTokens) a.send_row[g0 * R + i] = sr_s[i];
+  {
+    const int El = E / R;
+    const int step_r = kScanTokens / K, step_k = kScanTokens - step_r * K;
+    bool overflow = false;
+    for (int d = 0; d < R; ++d) {
+      const int64_t base = row_base[d];
+      const int cnt = int(tcnt[d]);
+      const int64_t room = a.recv_capacity - base;
+      const int n_ok = room <= 0 ? 0 : (room < cnt ? int(room) : cnt);
+      overflow |= n_ok < cnt;
+      for (int i = tid; i < n_ok; i += kScanTokens) {
+        a.recv_src_rank[base + i] = src_rank;
+        a.recv_src_idx[base + i] = t0 + tok_of[d][i];
+      }
+      const int lo = d * El, hi = lo + El;
+      // element i = r*K + k of this destination's rows; (r, k) advance by
+      // (kScanTokens / K, kScanTokens % K) per step, avoiding a division
+      int r = tid / K, k = tid - (tid / K) * K;
+      for (int i = tid; i < n_ok * K; i += kScanTokens) {
+        const int tk = tok_of[d][r];
+        const int e = idx_s[tk * K + k];
+        const bool local = e >= lo && e < hi;
+        a.recv_topk_idx[base * K + i] = local ? e - lo : -1;
+        a.recv_topk_weights[base * K + i] = local ? w_s[tk * K + k] : 0.0f;
+        r += step_r;
+        k += step_k;
+        if (k >= K) { k -= K; ++r; }
+      }
     }
-    for (int e = tid; e < E; e += blockDim.x) {
-      int sum = 0;
-      for (int s = 0; s < R; ++s) sum += a.num_tokens_per_expert[int64_t(s) * E + e];
-      a.num_recv_tokens_per_expert[e] = sum;
-    }
+    if (overflow && tid == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
   }
 
   // the last block out resets the counters and moves to the next epoch
@@ -352,11 +440,11 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
              num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx, recv_topk_idx,
              recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
              dev_err, ws};
-  const size_t smem = 2 * sizeof(int32_t) * size_t(kScanTokens) * K;
+  const size_t smem = sizeof(int32_t) * size_t(kScanTokens) * (2 * size_t(K) + R);
   static thread_local int configured_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && configured_smem[dev] < int(smem) && smem > 40 * 1024) {
+  if (dev < 64 && configured_smem[dev] < int(smem) && smem > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(mp_k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;

@@ -80,6 +80,24 @@ class EPPlan:
             self.dest_offsets, self.rank_prefix, self.num_recv_tokens_per_expert, self.send_row,
             self.dev_err, self.workspace, stream)
 
+    def dispatch_offsets(self, stream=None) -> int:
+        return B.mp_dispatch_offsets(
+            self.R, self.N, self.K, self.E, self.topk_idx, self.topk_weights,
+            self.is_token_in_rank, self.num_tokens_per_rank, self.num_tokens_per_expert,
+            self.cap, self.recv_src_rank, self.recv_src_idx, self.recv_topk_idx,
+            self.recv_topk_weights, self.dest_offsets, self.rank_prefix,
+            self.num_recv_tokens_per_expert, self.send_row, self.dev_err, self.workspace, stream)
+
+    def dispatch_rows(self, x: torch.Tensor | None = None, x_scales=None, recv_x=None,
+                      recv_scales=None, stream=None) -> int:
+        """Copy rows with the current send_row (default: this plan's own x / recv_x)."""
+        x = self.x if x is None else x
+        return B.mp_dispatch_rows(
+            self.R, self.N, self.H, B.MP_BF16 if self.dtype == "bf16" else B.MP_E4M3, x,
+            self.x_scales if x_scales is None else x_scales, self.send_row, self.cap,
+            self.recv_x if recv_x is None else recv_x,
+            self.recv_scales if recv_scales is None else recv_scales, stream)
+
     def combine(self, y: torch.Tensor | None = None, stream=None) -> int:
         """Combine y (default: recv_x, i.e. identity experts) back into self.out."""
         y = self.recv_x if y is None else y

@@ -82,9 +82,11 @@ enum { MP_BF16 = 0, MP_E4M3 = 1 };
 const char *mp_status_string(int status);
 
 /* Bytes of workspace that mp_layout and mp_dispatch need for R ranks, N
- * tokens per rank and E experts (their counters, per-block partial counts
- * and scan tile states).  The caller allocates it (device memory), fills it
- * with zeros ONCE before the first call, and then passes the same buffer
+ * tokens per rank and E experts (their counters, the per-rank count
+ * accumulators and the scan's tile records: R*(E+R)*4 bytes plus about
+ * (4 + 8R) bytes per 128 tokens of each rank, 26 KB for R=8, N=4096,
+ * E=256).  The caller allocates it (device memory), fills it with zeros
+ * ONCE before the first call, and then passes the same buffer
  * to every call of the same (R, N, E): each call leaves it zero-filled
  * again for the next one.  Calls that share a workspace must be ordered on
  * one stream.  Returns 0 for arguments mp_layout would reject. */
@@ -155,6 +157,53 @@ int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void *x,
                 int32_t *dev_err, void *workspace, mp_stream_t stream);
 
 /*
+ * mp_dispatch_offsets and mp_dispatch_rows -- the two steps of mp_dispatch as
+ * separate calls, with the same argument meanings.  mp_dispatch is exactly
+ * mp_dispatch_offsets followed by mp_dispatch_rows on the same stream.
+ *
+ * mp_dispatch_offsets: the receive-offset scan.  Writes dest_offsets,
+ *   rank_prefix, num_recv_tokens_per_expert, send_row and the per-row
+ *   metadata (recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights).
+ *   Checks and device errors as mp_dispatch, minus those about the payload.
+ * mp_dispatch_rows: the row copy.  recv_x[send_row[s][t][d]] = x[s][t] (and
+ *   the row's scales for MP_E4M3) for every entry >= 0 and < recv_capacity.
+ *   It reads only send_row, so one set of offsets can dispatch several
+ *   payloads routed the same way (the offsets are computed once).
+ *   Checks: 1 <= R <= 32, N >= 0, H and dtype as mp_dispatch, R*N*R < 2^31,
+ *   16-byte aligned x / recv_x, x_scales/recv_scales non-NULL exactly for
+ *   MP_E4M3.  No device errors.
+ */
+int mp_dispatch_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
+                        const float *topk_weights, const uint32_t *is_token_in_rank,
+                        const int32_t *num_tokens_per_rank, const int32_t *num_tokens_per_expert,
+                        int64_t recv_capacity, int32_t *recv_src_rank, int32_t *recv_src_idx,
+                        int32_t *recv_topk_idx, float *recv_topk_weights, int32_t *dest_offsets,
+                        int32_t *rank_prefix, int32_t *num_recv_tokens_per_expert,
+                        int32_t *send_row, int32_t *dev_err, void *workspace,
+                        mp_stream_t stream);
+int mp_dispatch_rows(int R, int N, int H, int dtype, const void *x, const float *x_scales,
+                     const int32_t *send_row, int64_t recv_capacity, void *recv_x,
+                     float *recv_scales, mp_stream_t stream);
+
+/*
+ * mp_dispatch_rows_e4m3 -- the row copy with in-kernel FP8 quantisation
+ * ([EP] FP8 E4M3 payload with FP32 scales; the pages give no recipe, the
+ * reading used: per block of 128 channels of a token row, amax = max |x|,
+ * scale = amax / 448 in fp32 (1 when amax is 0), code = e4m3(x / scale) with
+ * an fp32 division and round-to-nearest-even, saturating at +-448).
+ *   in   x          bf16 [R][N][H], H % 128 == 0
+ *   in   send_row   int32 [R][N][R] from mp_dispatch_offsets (or mp_dispatch)
+ *   out  recv_x     e4m3 [recv_capacity][H]: the quantised row at every
+ *                   destination row of the token
+ *   out  recv_scales fp32 [recv_capacity][H/128]
+ * Dequantised x is code * scale.  Checks: 1 <= R <= 32, N >= 0, H > 0,
+ * H % 128 == 0, R*N*R < 2^31, 16-byte aligned x / recv_x.  No device errors.
+ */
+int mp_dispatch_rows_e4m3(int R, int N, int H, const void *x, const int32_t *send_row,
+                          int64_t recv_capacity, void *recv_x, float *recv_scales,
+                          mp_stream_t stream);
+
+/*
  * mp_combine -- [EP] intranode_combine, the reverse of dispatch.
  *   in   y        bf16 [y_rows][H]: one row per receive row (for example the
  *                 expert outputs, or recv_x itself)
@@ -214,9 +263,10 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const void *in
  * MP_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
  * GPU that loads the library holds until the process exits.
  *  - Limit: problems whose mp_workspace_size(R, N, E) exceeds
- *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with R=8 and E=256 that allows up to
- *    29,824 tokens per rank) are rejected with MP_ERR_INVALID_ARG before
- *    anything is launched; use mp_dispatch with a workspace for those.
+ *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with E=256 that allows up to 244,608
+ *    tokens per rank at R=8 and 15,488 at R=32) are rejected with
+ *    MP_ERR_INVALID_ARG before anything is launched; use mp_dispatch with a
+ *    workspace for those.
  *  - Set-up: the first call on each device (with that device current) finds
  *    the array's device address and zero-fills it with a synchronous
  *    cudaMemset.  Make that first call before any stream capture.

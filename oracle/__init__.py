@@ -63,6 +63,12 @@ class OracleLib:
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
         L.oracle_f32_to_bf16_array.argtypes = [i64, P, P]
         L.oracle_f32_to_bf16_array.restype = None
+        L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f32.restype = ctypes.c_float
+        L.oracle_quantize_e4m3.argtypes = [i64, i32, P, P, P]
+        L.oracle_quantize_e4m3.restype = ctypes.c_int
         for f in ("oracle_layout", "oracle_dispatch", "oracle_combine",
                   "oracle_reducescatterv", "oracle_allgatherv"):
             getattr(L, f).restype = ctypes.c_int
@@ -162,6 +168,23 @@ class OracleLib:
     def f32_to_bf16(self, f: float) -> int:
         return self.L.oracle_f32_to_bf16(f)
 
+    def f32_to_e4m3(self, f: float) -> int:
+        return self.L.oracle_f32_to_e4m3(f)
+
+    def e4m3_to_f32(self, b: int) -> float:
+        return self.L.oracle_e4m3_to_f32(b)
+
+    def quantize_e4m3(self, x_bits: np.ndarray):
+        """x_bits uint16 (bf16 patterns) [..., H] -> (q uint8 [..., H], scales fp32
+        [..., H/128], status)."""
+        x_bits = _c(x_bits, np.uint16)
+        H = x_bits.shape[-1]
+        T = x_bits.size // H if H else 0
+        q = np.zeros(x_bits.shape, np.uint8)
+        sc = np.zeros(x_bits.shape[:-1] + (max(H // 128, 1),), np.float32)
+        st = self.L.oracle_quantize_e4m3(T, H, _p(x_bits), _p(q), _p(sc))
+        return q, sc, st
+
     def f32_to_bf16_array(self, a: np.ndarray) -> np.ndarray:
         """Element-wise oracle narrowing of a binary32 array to bf16 bit patterns."""
         a = np.ascontiguousarray(a, np.float32)
@@ -211,3 +234,7 @@ def allgatherv(*a, **k):
 
 def f32_to_bf16_array(a):
     return default().f32_to_bf16_array(a)
+
+
+def quantize_e4m3(x_bits):
+    return default().quantize_e4m3(x_bits)

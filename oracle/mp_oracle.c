@@ -42,6 +42,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #define ORC_BAD_ARG 1
 #define ORC_CAPACITY 4
@@ -262,4 +263,79 @@ int oracle_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const uint
 /* Element-wise binary32 -> bf16 narrowing over an array (used by pins). */
 void oracle_f32_to_bf16_array(int64_t n, const float *in, uint16_t *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* FP8 E4M3 ("fn": no infinities, S.1111.111 is NaN, largest finite   */
+/* 448 = 1.75 * 2^8, smallest normal 2^-6, subnormals k * 2^-9).      */
+/* Narrowing from binary32 rounds to nearest, ties to even, on the    */
+/* value's exact binary expansion, and saturates to +-448 (values at  */
+/* or above 448 in magnitude give 448).  Written from the format,     */
+/* with integer arithmetic on the binary32 fields.                    */
+/* ------------------------------------------------------------------ */
+static uint32_t rne_shift(uint32_t v, int sh) { /* round v / 2^sh to nearest, ties even */
+  if (sh <= 0) return v << (-sh);
+  if (sh >= 32) return 0u;
+  uint32_t q = v >> sh, rem = v & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  if (rem > half || (rem == half && (q & 1u))) q += 1u;
+  return q;
+}
+
+uint8_t oracle_f32_to_e4m3(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+  uint32_t ebits = (u >> 23) & 0xffu, mbits = u & 0x7fffffu;
+  if (ebits == 0xffu && mbits) return (uint8_t)(sign | 0x7fu); /* NaN */
+  if (ebits == 0xffu) return (uint8_t)(sign | 0x7eu);           /* +-inf saturate */
+  if (ebits == 0u) return sign;  /* binary32 subnormals are far below 2^-10 */
+  int e = (int)ebits - 127;      /* value = 1.m * 2^e */
+  uint32_t sig = (1u << 23) | mbits; /* 24-bit significand */
+  if (e >= -6) {
+    /* normal range of the target: keep 3 fraction bits */
+    uint32_t q = rne_shift(sig, 20); /* in [8, 16] */
+    if (q == 16u) { q = 8u; e += 1; }
+    if (e > 8 || (e == 8 && q > 14u)) return (uint8_t)(sign | 0x7eu); /* saturate to 448 */
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)(q - 8u));
+  }
+  /* below the normal range: units of 2^-9, value / 2^-9 = sig * 2^(e + 9 - 23) */
+  uint32_t k = rne_shift(sig, 23 - (e + 9)); /* in [0, 8] */
+  if (k >= 8u) return (uint8_t)(sign | 0x08u); /* rounds up to the smallest normal */
+  return (uint8_t)(sign | (uint8_t)k);
+}
+
+float oracle_e4m3_to_f32(uint8_t b) {
+  float s = (b & 0x80u) ? -1.0f : 1.0f;
+  int e = (b >> 3) & 0xf, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) return s * (float)m * 0.001953125f; /* m * 2^-9 */
+  return s * ldexpf(1.0f + (float)m / 8.0f, e - 7);
+}
+
+/* Per-block quantisation of bf16 rows to e4m3 (reading of the pages, which
+ * name an FP8 E4M3 payload with FP32 scales but give no recipe): for each
+ * token row and each block of 128 channels, amax = max |x|, scale =
+ * amax / 448 (binary32 division; 1 when amax is 0), q = e4m3(x / scale)
+ * (binary32 division, then the narrowing above).  Dequantised x ~ q * scale.
+ *   x      bf16 [T][H], H a multiple of 128
+ *   q      e4m3 [T][H]
+ *   scales fp32 [T][H/128] */
+int oracle_quantize_e4m3(int64_t T, int H, const uint16_t *x, uint8_t *q, float *scales) {
+  if (T < 0 || H <= 0 || H % 128 != 0) return ORC_BAD_ARG;
+  const int nb = H / 128;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t *xb = x + t * H + (int64_t)b * 128;
+      float amax = 0.0f;
+      for (int h = 0; h < 128; ++h) {
+        float v = fabsf(oracle_bf16_to_f32(xb[h]));
+        if (v > amax) amax = v;
+      }
+      const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      scales[t * nb + b] = scale;
+      for (int h = 0; h < 128; ++h)
+        q[t * H + (int64_t)b * 128 + h] = oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / scale);
+    }
+  }
+  return 0;
 }

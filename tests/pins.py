@@ -343,5 +343,71 @@ def pin_rsv_agv(orc) -> None:
     assert st == 0 and rs.shape == (0, 8)
 
 
+# --------------------------------------------------------------------------
+# FP8 E4M3 narrowing and per-128-channel block quantisation
+# --------------------------------------------------------------------------
+def _torch_e4m3(vals: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(vals, np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def pin_e4m3_conversions(orc) -> None:
+    rng = np.random.default_rng(41)
+    # every finite code decodes like torch's float8_e4m3fn
+    codes = np.array([c for c in range(256) if (c & 0x7f) != 0x7f], np.uint8)
+    tdec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    odec = np.array([orc.e4m3_to_f32(int(c)) for c in codes], np.float32)
+    assert np.array_equal(odec, tdec)
+    # narrowing: random binary32 values inside the finite range, every code value,
+    # every midpoint between neighbouring codes (ties) and values just either side
+    mags = np.sort(np.unique(np.abs(tdec)))
+    mids = (mags[:-1].astype(np.float64) + mags[1:]) / 2
+    near = np.concatenate([np.nextafter(mids.astype(np.float32), np.float32(0)),
+                           np.nextafter(mids.astype(np.float32), np.float32(1000))])
+    rnd = (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 9, 20000))).astype(np.float32)
+    allv = np.concatenate([mags, mids.astype(np.float32), near, rnd]).astype(np.float32)
+    allv = allv[np.abs(allv) <= 448]
+    allv = np.concatenate([allv, -allv])
+    ours = np.array([orc.f32_to_e4m3(float(v)) for v in allv], np.uint8)
+    theirs = _torch_e4m3(allv)
+    bad = np.nonzero(ours != theirs)[0]
+    assert bad.size == 0, allv[bad[:5]]
+    # saturation to +-448 above the range (satfinite), NaN stays NaN
+    for v in (449.0, 464.0, 500.0, 1e6, float("inf")):
+        assert orc.f32_to_e4m3(v) == 0x7e and orc.f32_to_e4m3(-v) == 0xfe
+    assert orc.f32_to_e4m3(float("nan")) & 0x7f == 0x7f
+
+
+def pin_block_quantisation(orc) -> None:
+    rng = np.random.default_rng(43)
+    x = (rng.standard_normal((40, 512)) * np.exp2(rng.integers(-6, 6, (40, 1)))).astype(np.float32)
+    x[3, :128] = 0.0                     # an all-zero block: scale 1, codes 0
+    x[4, 128:256] = 2.5                  # a constant block: every code is 448
+    x[5, 256:384] = -x[5, 256:384]
+    xb = _bits(x)
+    xf = _f32(xb).astype(np.float64)
+    q, sc, st = orc.quantize_e4m3(xb)
+    assert st == 0 and q.shape == x.shape and sc.shape == (40, 4)
+    blocks = xf.reshape(40, 4, 128)
+    amax = np.abs(blocks).max(-1)
+    want_scale = np.where(amax > 0, (amax.astype(np.float32) / np.float32(448)), 1.0)
+    assert np.array_equal(sc, want_scale.astype(np.float32))
+    assert sc[3, 0] == 1.0 and not q[3, :128].any()
+    assert np.all(q[4, 128:256] == 0x7e)
+    # the largest element of every non-zero block lands on the largest code
+    qb = q.reshape(40, 4, 128)
+    for t, b in zip(*np.nonzero(amax > 0)):
+        j = int(np.abs(blocks[t, b]).argmax())
+        assert qb[t, b, j] & 0x7f == 0x7e
+    # dequantised values are within half an e4m3 step of x (relative 2^-4 for
+    # normals, 2^-10 * scale below the normal range), the sign is kept
+    deq = torch.from_numpy(q.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    deq = (deq.reshape(40, 4, 128) * sc[..., None]).reshape(40, 512)
+    tol = np.maximum(np.abs(xf) * 2.0**-4, np.repeat(sc, 128, axis=1) * 2.0**-10) * 1.0001
+    assert np.all(np.abs(deq - xf) <= tol)
+    assert np.all((deq == 0) | (np.sign(deq) == np.sign(xf)))
+
+
 ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
-            pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv]
+            pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
+            pin_e4m3_conversions, pin_block_quantisation]

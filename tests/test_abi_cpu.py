@@ -47,11 +47,12 @@ def test_status_strings(L):
 
 
 def test_workspace_size(L):
-    # control block + per-block partial counts + 8-byte tile states
+    # control block + per-rank count accumulators + tile records (flag + 2R counts)
+    # for tiles of 128 tokens that never straddle two source ranks
     s = B.mp_workspace_size(8, 4096, 256)
-    blocks = (4096 + 255) // 256
-    tiles = (8 * 4096 + 255) // 256
-    assert s >= 512 + 8 * blocks * (256 + 8) * 4 + tiles * 8 * 8
+    tiles = 8 * ((4096 + 127) // 128)
+    assert s >= 512 + 8 * (256 + 8) * 4 + tiles * (4 + 2 * 8 * 4)
+    assert s < 512 + 8 * (256 + 8) * 4 + tiles * (4 + 2 * 8 * 4) + 4 * 256
     assert s % 256 == 0
     assert B.mp_workspace_size(2, 0, 8) > 0
     assert B.mp_workspace_size(0, 10, 8) == 0      # R < 1

@@ -42,6 +42,15 @@ MUTANTS = {
                        "for (int q = R - 1; q >= 0; --q)\n          acc = acc"),
     "rsv_in_double": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
                       "        double acc = 0.0;\n        for (int q = 0; q < R; ++q)"),
+    "e4m3_ties_away": ("if (rem > half || (rem == half && (q & 1u))) q += 1u;",
+                       "if (rem >= half) q += 1u;"),
+    "e4m3_bias_off": ("(uint8_t)((e + 7) << 3)", "(uint8_t)((e + 8) << 3)"),
+    "e4m3_no_subnormals": ("uint32_t k = rne_shift(sig, 23 - (e + 9)); /* in [0, 8] */",
+                           "uint32_t k = 0u; (void)rne_shift; /* flushed */"),
+    "quant_divisor_240": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    "quant_multiplies": ("oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / scale)",
+                         "oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) * scale)"),
+    "quant_zero_scale": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 448.0f : 0.0f"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
 }

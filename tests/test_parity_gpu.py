@@ -199,6 +199,76 @@ def test_repeated_calls_reuse_workspace():
     compare_ep(inp2, plan)
 
 
+def test_split_dispatch_and_cached_rows():
+    """mp_dispatch_offsets + mp_dispatch_rows equal mp_dispatch, and one set of offsets
+    dispatches a second payload routed the same way (e4m3 with scales too)."""
+    for dtype, H in (("bf16", 264), ("e4m3", 256)):
+        inp = wl.make_ep(dict(R=6, N=500, E=24, K=4, H=H, routing="uniform", dtype=dtype), seed=9)
+        plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H, dtype)
+        plan.load(inp)
+        B.check(plan.layout())
+        B.check(plan.dispatch_offsets())
+        B.check(plan.dispatch_rows())
+        B.check(plan.combine(wl.random_bf16((plan.cap, H), 1).cuda()) if dtype != "bf16"
+                else plan.combine())
+        torch.cuda.synchronize()
+        compare_ep(inp, plan, y_bits=wl.bf16_bits(wl.random_bf16((plan.cap, H), 1))
+                   if dtype != "bf16" else None)
+        # a second payload, same routing: only the row copy runs
+        inp2 = wl.make_ep(dict(R=6, N=500, E=24, K=4, H=H, routing="uniform", dtype=dtype),
+                          seed=9)
+        g = torch.Generator().manual_seed(123)
+        x2 = torch.randn((inp.R, inp.N, H), generator=g)
+        inp2.x = x2.to(torch.bfloat16) if dtype == "bf16" else x2.to(torch.float8_e4m3fn)
+        if dtype != "bf16":
+            inp2.x_scales = torch.rand((inp.R, inp.N, H // 128), generator=g) + 0.5
+        recv2 = torch.zeros_like(plan.recv_x)
+        rs2 = torch.zeros_like(plan.recv_scales) if dtype != "bf16" else None
+        B.check(plan.dispatch_rows(x=inp2.x.cuda(),
+                                   x_scales=inp2.x_scales.cuda() if dtype != "bf16" else None,
+                                   recv_x=recv2, recv_scales=rs2))
+        torch.cuda.synchronize()
+        _, _, mask, _ = oracle.layout(inp2.topk_idx, inp2.E)
+        xs = inp2.x_scales.numpy() if dtype != "bf16" else None
+        out, st = oracle.dispatch(x_host(inp2), inp2.topk_idx, inp2.topk_weights, mask, inp2.E,
+                                  x_scales=xs)
+        n = out["num_recv"]
+        got = wl.bf16_bits(recv2[:n]) if dtype == "bf16" else wl.u8_bits(recv2[:n])
+        assert st == 0 and np.array_equal(got, out["recv_x"])
+        if xs is not None:
+            assert np.array_equal(rs2[:n].cpu().numpy().view(np.uint32),
+                                  out["recv_scales"].view(np.uint32))
+
+
+@pytest.mark.parametrize("shape", [(4, 300, 16, 4, 384), (3, 129, 12, 2, 128),
+                                   (8, 4096, 256, 8, 7168)],
+                         ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
+def test_dispatch_rows_e4m3_quantises_like_the_oracle(shape):
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=H)
+    x = inp.x.float()
+    x[0, 0, :128] = 0.0                      # an all-zero block
+    x[0, 1, :] = 3.0                         # constant blocks
+    x[R - 1, N - 1, -128:] *= 1e-3           # a block of small values (subnormal codes)
+    inp.x = x.to(torch.bfloat16)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    rq = torch.zeros((plan.cap, H), dtype=torch.uint8, device="cuda")
+    rs = torch.zeros((plan.cap, H // 128), dtype=torch.float32, device="cuda")
+    B.check(B.mp_dispatch_rows_e4m3(R, N, H, plan.x, plan.send_row, plan.cap, rq, rs))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    q, sc, st = oracle.quantize_e4m3(wl.bf16_bits(inp.x))
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    out, st2 = oracle.dispatch(q, inp.topk_idx, inp.topk_weights, mask, E, x_scales=sc)
+    assert st == st2 == 0
+    n = out["num_recv"]
+    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"])
+    assert np.array_equal(rs[:n].cpu().numpy().view(np.uint32), out["recv_scales"].view(np.uint32))
+
+
 def test_empty_tokens():
     inp = wl.make_ep(dict(R=4, N=0, E=16, K=2, H=64, routing="uniform", dtype="bf16"))
     plan = run_gpu(inp)

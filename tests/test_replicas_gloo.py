@@ -1,0 +1,47 @@
+"""The multi-GPU path is N independent replicas (the hot path has no exchange
+between GPUs): the benchmark's only cross-rank logic is the max over ranks
+of the timed region and the whole-job throughput.  Checked here with two
+gloo ranks on the CPU."""
+import os
+import socket
+
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = [7.5, 9.25][rank]  # rank 1 is the slow replica
+        m = bench.max_over_ranks(ms, world, device="cpu")
+        out[rank] = (m, bench.replica_throughput(32768, 10, world, m))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_throughput():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 9.25
+    assert abs(res[0][1] - 32768 * 2 * 10 / 9.25e-3) < 1e-6 * res[0][1]
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.0, 1) == 3.0
+    assert bench.replica_throughput(100, 4, 1, 2.0) == 100 * 4 / 2e-3

@@ -66,14 +66,14 @@ def test_noalloc_matches_dispatch_on_two_calls_in_a_row():
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch():
-    # mp_workspace_size(8, 40000, 256) is above the fixed 1 MiB; the call must be
+    # mp_workspace_size(32, 100000, 256) is above the fixed 1 MiB; the call must be
     # refused before anything is launched (all pointers NULL, so nothing could run).
-    assert B.mp_workspace_size(8, 40000, 256) > (1 << 20)
+    assert B.mp_workspace_size(32, 100000, 256) > (1 << 20)
     f = B.lib().mp_dispatch_noalloc
     import ctypes
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     f.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i64,
                   P, P, P, P, P, P, P, P, P, P, P, P]
     f.restype = ctypes.c_int
-    st = f(8, 40000, 8, 256, 7168, B.MP_BF16, *([None] * 7), 10, *([None] * 12))
+    st = f(32, 100000, 8, 256, 7168, B.MP_BF16, *([None] * 7), 10, *([None] * 12))
     assert st == B.MP_ERR_INVALID_ARG
