@@ -60,11 +60,19 @@ def lib() -> ctypes.CDLL:
                                           P, P, P, P, P, P, P, P, P, P, P]
         L.mp_dispatch_rows.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P]
         L.mp_dispatch_rows_e4m3.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
+        L.mp_dispatch_offsets_global.argtypes = [i32, i32, i32, i32, P, P, P, P, P, i64,
+                                                 ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P]
+        L.mp_combine_weights.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
+        L.mp_dispatch_ll_offsets.argtypes = [i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P]
+        L.mp_dispatch_ll_rows.argtypes = [i32, i32, i32, i32, i32, P, P, P, i64, P, P, P]
+        L.mp_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, P]
         L.mp_combine.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
         L.mp_reducescatterv.argtypes = [i32, i32, P, P, P, P]
         L.mp_allgatherv.argtypes = [i32, i64, P, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
-                  "mp_dispatch_rows_e4m3", "mp_combine", "mp_reducescatterv", "mp_allgatherv"):
+                  "mp_dispatch_rows_e4m3", "mp_dispatch_offsets_global", "mp_combine_weights",
+                  "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
+                  "mp_combine", "mp_reducescatterv", "mp_allgatherv"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -155,6 +163,32 @@ def mp_dispatch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_
                                   _stream(stream))
 
 
+def mp_dispatch_offsets_global(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                               num_tokens_per_rank, num_tokens_per_expert, recv_capacity, sentinel,
+                               recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                               dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                               dev_err, workspace, stream=None) -> int:
+    return lib().mp_dispatch_offsets_global(
+        R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"),
+        _dev(is_token_in_rank, "is_token_in_rank"),
+        _dev(num_tokens_per_rank, "num_tokens_per_rank"),
+        _dev(num_tokens_per_expert, "num_tokens_per_expert"), int(recv_capacity), int(sentinel),
+        _dev(recv_src_rank, "recv_src_rank"), _dev(recv_src_idx, "recv_src_idx"),
+        _dev(recv_topk_idx, "recv_topk_idx"), _dev(recv_topk_weights, "recv_topk_weights"),
+        _dev(dest_offsets, "dest_offsets"), _dev(rank_prefix, "rank_prefix"),
+        _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
+        _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _dev(workspace, "workspace"),
+        _stream(stream))
+
+
+def mp_combine_weights(R, N, K, recv_topk_weights, recv_rows, send_row, combined, dev_err,
+                       stream=None) -> int:
+    return lib().mp_combine_weights(R, N, K, _dev(recv_topk_weights, "recv_topk_weights"),
+                                    int(recv_rows), _dev(send_row, "send_row"),
+                                    _dev(combined, "combined_topk_weights"),
+                                    _dev(dev_err, "dev_err"), _stream(stream))
+
+
 def mp_dispatch_rows_e4m3(R, N, H, x, send_row, recv_capacity, recv_x, recv_scales,
                           stream=None) -> int:
     return lib().mp_dispatch_rows_e4m3(R, N, H, _dev(x, "x"), _dev(send_row, "send_row"),
@@ -207,3 +241,44 @@ def mp_dispatch_noalloc(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weight
              _dev(dest_offsets, "dest_offsets"), _dev(rank_prefix, "rank_prefix"),
              _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
              _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _stream(stream))
+
+
+def mp_allgatherv_multi(R, row_bytes, sizes, inputs, outputs, stream=None) -> int:
+    """All-gatherv of several tensors with the same per-rank row counts, one launch."""
+    L = lib()
+    f = L.mp_allgatherv_multi
+    if f.argtypes is None:
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
+        f.restype = ctypes.c_int
+    n = len(inputs)
+    if len(outputs) != n or len(row_bytes) != n:
+        raise ValueError("one row size and one output per input")
+    rb = (ctypes.c_int64 * n)(*[int(b) for b in row_bytes])
+    ins = (ctypes.c_void_p * n)(*[_dev(t, "in").value for t in inputs])
+    outs = (ctypes.c_void_p * n)(*[_dev(t, "out").value for t in outputs])
+    return f(R, n, rb, _host_sizes(sizes), ins, outs, _stream(stream))
+
+
+def mp_dispatch_ll_offsets(R, N, K, E, topk_idx, num_tokens_per_expert, recv_capacity,
+                           expert_offsets, expert_src_offsets, recv_src_token, slot_row, dev_err,
+                           stream=None) -> int:
+    return lib().mp_dispatch_ll_offsets(
+        R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(num_tokens_per_expert, "num_tokens_per_expert"),
+        int(recv_capacity), _dev(expert_offsets, "expert_offsets"),
+        _dev(expert_src_offsets, "expert_src_offsets"), _dev(recv_src_token, "recv_src_token"),
+        _dev(slot_row, "slot_row"), _dev(dev_err, "dev_err"), _stream(stream))
+
+
+def mp_dispatch_ll_rows(R, N, K, H, dtype, x, x_scales, slot_row, recv_capacity, recv_x,
+                        recv_scales, stream=None) -> int:
+    return lib().mp_dispatch_ll_rows(R, N, K, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
+                                     _dev(slot_row, "slot_row"), int(recv_capacity),
+                                     _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
+                                     _stream(stream))
+
+
+def mp_combine_ll(R, N, K, H, y, y_rows, slot_row, topk_weights, out, dev_err, stream=None) -> int:
+    return lib().mp_combine_ll(R, N, K, H, _dev(y, "y"), int(y_rows), _dev(slot_row, "slot_row"),
+                               _dev(topk_weights, "topk_weights"), _dev(out, "out"),
+                               _dev(dev_err, "dev_err"), _stream(stream))

@@ -160,6 +160,47 @@ int mp_dispatch_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int mp_dispatch_offsets_global(int R, int N, int K, int E, const int32_t* topk_idx,
+                               const float* topk_weights, const uint32_t* is_token_in_rank,
+                               const int32_t* num_tokens_per_rank,
+                               const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                               int32_t sentinel, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                               int32_t* recv_topk_idx, float* recv_topk_weights,
+                               int32_t* dest_offsets, int32_t* rank_prefix,
+                               int32_t* num_recv_tokens_per_expert, int32_t* send_row,
+                               int32_t* dev_err, void* workspace, mp_stream_t stream) {
+  const int st = check_offsets_args(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                                    num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                                    recv_src_rank, recv_src_idx, recv_topk_idx,
+                                    recv_topk_weights, dest_offsets, rank_prefix,
+                                    num_recv_tokens_per_expert, send_row, dev_err, workspace);
+  if (st != MP_OK) return st;
+  return cuda_status(launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                                 num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                                 recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                                 dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                                 dev_err, static_cast<unsigned char*>(workspace),
+                                 reinterpret_cast<cudaStream_t>(stream), 1, sentinel));
+}
+
+int mp_combine_weights(int R, int N, int K, const float* recv_topk_weights, int64_t recv_rows,
+                       const int32_t* send_row, float* combined_topk_weights, int32_t* dev_err,
+                       mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || K < 1 || K > MP_MAX_TOPK || recv_rows < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31) || int64_t(R) * N * K >= (int64_t(1) << 31))
+    return MP_ERR_INVALID_ARG;
+  if (!dev_err || (N > 0 && (!send_row || !combined_topk_weights)) ||
+      (recv_rows > 0 && !recv_topk_weights))
+    return MP_ERR_INVALID_ARG;
+  if (!aligned4(recv_topk_weights) || !aligned4(send_row) || !aligned4(combined_topk_weights) ||
+      !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_weights(R, int64_t(R) * N, K, recv_topk_weights, recv_rows,
+                                            send_row, combined_topk_weights, dev_err,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mp_dispatch_rows(int R, int N, int H, int dtype, const void* x, const float* x_scales,
                      const int32_t* send_row, int64_t recv_capacity, void* recv_x,
                      float* recv_scales, mp_stream_t stream) {
@@ -251,6 +292,78 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t* sizes, const void* in
   if (S > 0 && (!in || !out || !aligned16(in) || !aligned16(out))) return MP_ERR_INVALID_ARG;
   return cuda_status(
       launch_allgatherv(R, S, row_bytes, in, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_allgatherv_multi(int R, int ntensors, const int64_t* row_bytes, const int64_t* sizes,
+                        const void* const* in, void* const* out, mp_stream_t stream) {
+  if (R < 1 || ntensors < 1 || ntensors > MP_MAX_TENSORS || !row_bytes || !sizes || !in || !out)
+    return MP_ERR_INVALID_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return MP_ERR_INVALID_ARG;
+    S += sizes[r];
+  }
+  for (int j = 0; j < ntensors; ++j) {
+    if (row_bytes[j] <= 0 || row_bytes[j] % 16 != 0) return MP_ERR_INVALID_ARG;
+    if (S > 0 && (!in[j] || !out[j] || !aligned16(in[j]) || !aligned16(out[j])))
+      return MP_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_allgatherv_multi(R, ntensors, row_bytes, S, in, out,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+                           const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                           int32_t* expert_offsets, int32_t* expert_src_offsets,
+                           int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
+                           mp_stream_t stream) {
+  if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
+  if (int64_t(N) * K * 4 > 200 * 1024) return MP_ERR_INVALID_ARG;  // the rank's slab in smem
+  if (!num_tokens_per_expert || !expert_offsets || !expert_src_offsets || !dev_err)
+    return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(expert_offsets) ||
+      !aligned4(expert_src_offsets) || !aligned4(recv_src_token) || !aligned4(slot_row) ||
+      !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_ll_offsets(R, N, K, E, topk_idx, num_tokens_per_expert,
+                                       recv_capacity, expert_offsets, expert_src_offsets,
+                                       recv_src_token, slot_row, dev_err,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_ll_rows(int R, int N, int K, int H, int dtype, const void* x,
+                        const float* x_scales, const int32_t* slot_row, int64_t recv_capacity,
+                        void* recv_x, float* recv_scales, mp_stream_t stream) {
+  if (K < 1 || K > MP_MAX_TOPK || R < 1 || R > MP_MAX_RANKS) return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * K >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  // the row copy with the K top-k slots of a token in place of its R destinations
+  const int st = check_rows_args(1, N, H, dtype, x, x_scales, slot_row, recv_capacity, recv_x,
+                                 recv_scales);
+  if (st != MP_OK) return st;
+  const bool fp8 = dtype == MP_E4M3;
+  const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
+  return cuda_status(launch_dispatch_copy(K, int64_t(R) * N, row_bytes, x, recv_x, recv_capacity,
+                                          slot_row, fp8 ? H / MP_SCALE_BLOCK : 0, x_scales,
+                                          recv_scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_combine_ll(int R, int N, int K, int H, const void* y, int64_t y_rows,
+                  const int32_t* slot_row, const float* topk_weights, void* out,
+                  int32_t* dev_err, mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || K < 1 || K > MP_MAX_TOPK || H <= 0 || H % 8 != 0 ||
+      y_rows < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * K >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (!dev_err || (N > 0 && (!slot_row || !topk_weights || !out || (y_rows > 0 && !y))))
+    return MP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || !aligned4(slot_row) || !aligned4(topk_weights) ||
+      !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_weighted(K, int64_t(R) * N, H, y, y_rows, slot_row,
+                                             topk_weights, out, dev_err,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -110,6 +110,24 @@ struct alignas(NW * 4) Words {
   uint32_t w[NW];
 };
 
+// Like ld_stream_w, but leaves the line in L2 with normal priority (for data
+// that other warps re-read shortly after).
+template <int NW>
+__device__ __forceinline__ Words<NW> ld_shared_l2_w(const Words<NW>* p) {
+  Words<NW> v;
+  if constexpr (NW == 8) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                   "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+  }
+  return v;
+}
+
 template <int NW>
 __device__ __forceinline__ Words<NW> ld_stream_w(const Words<NW>* p) {
   Words<NW> v;
@@ -149,6 +167,17 @@ __device__ __forceinline__ void add_bf16(float* acc, const Words<NW>& v) {
   for (int i = 0; i < NW; ++i) {
     acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(v.w[i] << 16));
     acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(v.w[i] & 0xffff0000u));
+  }
+}
+
+// acc += w * v for the 2*NW bf16 of v: a binary32 product, then a binary32
+// add (two roundings, never fused).
+template <int NW>
+__device__ __forceinline__ void add_bf16_weighted(float* acc, const Words<NW>& v, float w) {
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, __uint_as_float(v.w[i] << 16)));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, __uint_as_float(v.w[i] & 0xffff0000u)));
   }
 }
 

@@ -42,6 +42,14 @@
 #ifndef MP_DISPATCH_TMA
 #define MP_DISPATCH_TMA 0
 #endif
+// 1: one warp unit per (token, slab, destination) instead of (token, slab)
+#ifndef MP_DISPATCH_PER_DEST
+#define MP_DISPATCH_PER_DEST 0
+#endif
+// 1: one unit per (chunk, copy) in all-gatherv instead of (chunk, all copies)
+#ifndef MP_AGV_PER_COPY
+#define MP_AGV_PER_COPY 0
+#endif
 #ifndef MP_TMA_STAGES
 #define MP_TMA_STAGES 6
 #endif
@@ -94,6 +102,46 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ 
         for (int c = lane; c < spr; c += kWarp)
           recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch copy, one warp unit per (token, slab, destination): the warps that
+// run side by side copy the same slab of one token to its destinations, so
+// the rows being written at any moment form a narrow band (the re-reads of
+// the slab hit L2; DRAM still reads each token row once).
+// ---------------------------------------------------------------------------
+template <int NW, int U>
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_dispatch_pd(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ x,
+                 Words<NW>* __restrict__ recv_x, int64_t recv_capacity,
+                 const int32_t* __restrict__ send_row, int spr,
+                 const float* __restrict__ x_scales, float* __restrict__ recv_scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t slab_vec = int64_t(kWarp) * U;
+  const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
+  const int64_t units = tokens * slabs * R;
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
+       unit += nw) {
+    const int64_t ts = unit / R;
+    const int d = int(unit - ts * R);
+    const int64_t tok = ts / slabs;
+    const int64_t slab = ts - tok * slabs;
+    const int64_t row = __ldg(send_row + tok * R + d);
+    if (row < 0 || row >= recv_capacity) continue;
+    const int64_t i0 = slab * slab_vec + lane;
+    Words<NW> v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * kWarp < vpr) v[u] = ld_shared_l2_w<NW>(x + tok * vpr + i0 + u * kWarp);
+    Words<NW>* dst = recv_x + row * vpr;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * kWarp < vpr) st_stream_w<NW>(dst + i0 + u * kWarp, v[u]);
+    if (spr > 0 && slab == 0)
+      for (int c = lane; c < spr; c += kWarp)
+        recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
   }
 }
 
@@ -302,11 +350,13 @@ mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
 // from +0.0f.  Up to RB source rows are loaded at once (memory-level
 // parallelism) and then added strictly in ascending d.
 // ---------------------------------------------------------------------------
-template <int NW, int U, int RB>
+// With a weight array (the low-latency combine) the R "ranks" are the K top-k
+// slots of the token and each row is scaled by its slot's weight first.
+template <int NW, int U, int RB, bool WEIGHTED>
 __global__ void __launch_bounds__(kCopyThreads, MP_COMBINE_MINB)
 mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y, int64_t y_rows,
-             const int32_t* __restrict__ send_row, Words<NW>* __restrict__ out,
-             int32_t* __restrict__ dev_err) {
+             const int32_t* __restrict__ send_row, const float* __restrict__ weights,
+             Words<NW>* __restrict__ out, int32_t* __restrict__ dev_err) {
   const int lane = threadIdx.x & 31;
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
@@ -321,6 +371,8 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y
       if (slab == 0) raise_error(dev_err, MP_ERR_CAPACITY);
       my = -1;
     }
+    float myw = 0.0f;
+    if (WEIGHTED && lane < R) myw = __ldg(weights + tok * R + lane);
     unsigned vm = __ballot_sync(kFull, my >= 0);
     const int64_t i0 = slab * slab_vec + lane;
     float acc[U][2 * NW];
@@ -330,13 +382,16 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y
       for (int j = 0; j < 2 * NW; ++j) acc[u][j] = 0.0f;
     while (vm) {
       int64_t rows[RB];
+      float wts[RB];
 #pragma unroll
       for (int j = 0; j < RB; ++j) {
         rows[j] = -1;
+        wts[j] = 0.0f;
         if (vm) {
           const int d = __ffs(vm) - 1;
           vm &= vm - 1;
           rows[j] = __shfl_sync(kFull, my, d);
+          if (WEIGHTED) wts[j] = __shfl_sync(kFull, myw, d);
         }
       }
       Words<NW> v[RB][U];
@@ -350,7 +405,10 @@ mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y
       for (int j = 0; j < RB; ++j)
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (rows[j] >= 0 && i0 + u * kWarp < vpr) add_bf16<NW>(acc[u], v[j][u]);
+          if (rows[j] >= 0 && i0 + u * kWarp < vpr) {
+            if (WEIGHTED) add_bf16_weighted<NW>(acc[u], v[j][u], wts[j]);
+            else add_bf16<NW>(acc[u], v[j][u]);
+          }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -410,6 +468,58 @@ mp_k_agv(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __res
   }
 }
 
+// All-gatherv with one warp unit per (2-vector-per-lane chunk, copy): warps
+// running together write the same chunk to the R copies (chunk re-reads hit L2).
+template <int NW>
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_agv_pc(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __restrict__ out) {
+  constexpr int U = 2;
+  const int lane = threadIdx.x & 31;
+  const int64_t chunks = (nvec + kWarp * U - 1) / (kWarp * U);
+  const int64_t units = chunks * R;
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
+       unit += nw) {
+    const int64_t c = unit / R;
+    const int q = int(unit - c * R);
+    const int64_t i0 = c * kWarp * U + lane;
+    Words<NW> v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * kWarp < nvec) v[u] = ld_shared_l2_w<NW>(in + i0 + u * kWarp);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * kWarp < nvec) st_stream_w<NW>(out + int64_t(q) * nvec + i0 + u * kWarp, v[u]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Multi-tensor all-gatherv (same page: all-gathering a list of tensors lets
+// quantised data and its scales travel together).  Up to MP_MAX_TENSORS
+// tensors share the per-rank row counts; one launch walks the concatenation
+// of their 16-byte vectors, each read once and written R times.
+// ---------------------------------------------------------------------------
+struct AgvList {
+  const int4* in[MP_MAX_TENSORS];
+  int4* out[MP_MAX_TENSORS];
+  int64_t nvec[MP_MAX_TENSORS];   // vectors of one gathered copy of tensor j
+  int64_t first[MP_MAX_TENSORS];  // index of tensor j's first vector in the walk
+  int n;
+};
+
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_agv_multi(int R, int64_t total, AgvList l) {
+  const int64_t stride = int64_t(gridDim.x) * kCopyThreads;
+  for (int64_t g = int64_t(blockIdx.x) * kCopyThreads + threadIdx.x; g < total; g += stride) {
+    int j = 0;
+    while (j + 1 < l.n && g >= l.first[j + 1]) ++j;
+    const int64_t i = g - l.first[j];
+    const Words<4> v = ld_stream_w<4>(reinterpret_cast<const Words<4>*>(l.in[j]) + i);
+    Words<4>* out = reinterpret_cast<Words<4>*>(l.out[j]);
+    for (int q = 0; q < R; ++q) st_stream_w<4>(out + int64_t(q) * l.nvec[j] + i, v);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Launchers: a persistent grid of (SMs x resident blocks) blocks, trimmed to
 // the work available; 32-byte vectors when sizes and pointers allow.
@@ -430,6 +540,21 @@ static unsigned grid_for(int per_sm, int64_t items_per_block, int64_t items) {
 
 static bool aligned(const void* p, int bytes) {
   return (reinterpret_cast<uintptr_t>(p) % uintptr_t(bytes)) == 0;
+}
+
+template <int NW, int U>
+static cudaError_t dispatch_copy_pd(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                    void* recv_x, int64_t recv_capacity, const int32_t* send_row,
+                                    int spr, const float* x_scales, float* recv_scales,
+                                    cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_dispatch_pd<NW, U>);
+  const int64_t vpr = row_bytes / (4 * NW);
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs * R);
+  mp_k_dispatch_pd<NW, U><<<grid, kCopyThreads, 0, stream>>>(
+      R, tokens, vpr, static_cast<const Words<NW>*>(x), static_cast<Words<NW>*>(recv_x),
+      recv_capacity, send_row, spr, x_scales, recv_scales);
+  return cudaGetLastError();
 }
 
 template <int NW, int U>
@@ -486,6 +611,15 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
   if (MP_DISPATCH_TMA)
     return dispatch_copy_tma(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
                              scales_per_row, x_scales, recv_scales, nullptr, stream);
+  if (MP_DISPATCH_PER_DEST) {
+    if (row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
+      return dispatch_copy_pd<8, MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
+                                                send_row, scales_per_row, x_scales, recv_scales,
+                                                stream);
+    return dispatch_copy_pd<4, 2 * MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
+                                                  send_row, scales_per_row, x_scales,
+                                                  recv_scales, stream);
+  }
   if (MP_DISPATCH_NW == 8 && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
     return dispatch_copy_nw<MP_DISPATCH_NW, MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x,
                                                            recv_capacity, send_row,
@@ -511,29 +645,42 @@ cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, v
   return cudaGetLastError();
 }
 
-template <int NW, int U, int RB>
+template <int NW, int U, int RB, bool W>
 static cudaError_t combine_nw(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
-                              const int32_t* send_row, void* out, int32_t* dev_err,
-                              cudaStream_t stream) {
-  static const int per_sm = resident_blocks(mp_k_combine<NW, U, RB>);
+                              const int32_t* send_row, const float* weights, void* out,
+                              int32_t* dev_err, cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_combine<NW, U, RB, W>);
   const int64_t vpr = int64_t(H) * 2 / (4 * NW);
   const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
   const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
-  mp_k_combine<NW, U, RB><<<grid, kCopyThreads, 0, stream>>>(
-      R, tokens, vpr, static_cast<const Words<NW>*>(y), y_rows, send_row,
+  mp_k_combine<NW, U, RB, W><<<grid, kCopyThreads, 0, stream>>>(
+      R, tokens, vpr, static_cast<const Words<NW>*>(y), y_rows, send_row, weights,
       static_cast<Words<NW>*>(out), dev_err);
   return cudaGetLastError();
+}
+
+template <bool W>
+static cudaError_t combine_any(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
+                               const int32_t* send_row, const float* weights, void* out,
+                               int32_t* dev_err, cudaStream_t stream) {
+  if (tokens == 0) return cudaSuccess;
+  if (MP_COMBINE_NW == 8 && (int64_t(H) * 2) % 32 == 0 && aligned(y, 32) && aligned(out, 32))
+    return combine_nw<MP_COMBINE_NW, MP_COMBINE_U, MP_COMBINE_RB, W>(
+        R, tokens, H, y, y_rows, send_row, weights, out, dev_err, stream);
+  return combine_nw<4, 2 * MP_COMBINE_U, MP_COMBINE_RB, W>(R, tokens, H, y, y_rows, send_row,
+                                                          weights, out, dev_err, stream);
 }
 
 cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
                            const int32_t* send_row, void* out, int32_t* dev_err,
                            cudaStream_t stream) {
-  if (tokens == 0) return cudaSuccess;
-  if (MP_COMBINE_NW == 8 && (int64_t(H) * 2) % 32 == 0 && aligned(y, 32) && aligned(out, 32))
-    return combine_nw<MP_COMBINE_NW, MP_COMBINE_U, MP_COMBINE_RB>(R, tokens, H, y, y_rows,
-                                                                  send_row, out, dev_err, stream);
-  return combine_nw<4, 2 * MP_COMBINE_U, MP_COMBINE_RB>(R, tokens, H, y, y_rows, send_row, out,
-                                                       dev_err, stream);
+  return combine_any<false>(R, tokens, H, y, y_rows, send_row, nullptr, out, dev_err, stream);
+}
+
+cudaError_t launch_combine_weighted(int K, int64_t tokens, int H, const void* y, int64_t y_rows,
+                                    const int32_t* slot_row, const float* weights, void* out,
+                                    int32_t* dev_err, cudaStream_t stream) {
+  return combine_any<true>(K, tokens, H, y, y_rows, slot_row, weights, out, dev_err, stream);
 }
 
 template <int NW>
@@ -566,13 +713,93 @@ static cudaError_t agv_nw(int R, int64_t bytes, const void* in, void* out, cudaS
   return cudaGetLastError();
 }
 
+template <int NW>
+static cudaError_t agv_pc(int R, int64_t bytes, const void* in, void* out, cudaStream_t stream) {
+  static const int per_sm = resident_blocks(mp_k_agv_pc<NW>);
+  const int64_t nvec = bytes / (4 * NW);
+  const int64_t chunks = (nvec + kWarp * 2 - 1) / (kWarp * 2);
+  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, chunks * R);
+  mp_k_agv_pc<NW><<<grid, kCopyThreads, 0, stream>>>(R, nvec, static_cast<const Words<NW>*>(in),
+                                                      static_cast<Words<NW>*>(out));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream) {
   const int64_t bytes = S * row_bytes;
   if (bytes == 0) return cudaSuccess;
+  if (MP_AGV_PER_COPY) {
+    if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32)) return agv_pc<8>(R, bytes, in, out, stream);
+    return agv_pc<4>(R, bytes, in, out, stream);
+  }
   if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32))
     return agv_nw<8, 2>(R, bytes, in, out, stream);
   return agv_nw<4, 4>(R, bytes, in, out, stream);
+}
+
+}  // namespace mp
+
+namespace mp {
+
+cudaError_t launch_allgatherv_multi(int R, int n, const int64_t* S_row_bytes, int64_t S,
+                                    const void* const* in, void* const* out,
+                                    cudaStream_t stream) {
+  AgvList l{};
+  l.n = n;
+  int64_t total = 0;
+  for (int j = 0; j < n; ++j) {
+    l.in[j] = static_cast<const int4*>(in[j]);
+    l.out[j] = static_cast<int4*>(out[j]);
+    l.nvec[j] = S * S_row_bytes[j] / 16;
+    l.first[j] = total;
+    total += l.nvec[j];
+  }
+  if (total == 0) return cudaSuccess;
+  static const int per_sm = resident_blocks(mp_k_agv_multi);
+  const unsigned grid = grid_for(per_sm, kCopyThreads, total);
+  mp_k_agv_multi<<<grid, kCopyThreads, 0, stream>>>(R, total, l);
+  return cudaGetLastError();
+}
+
+}  // namespace mp
+
+namespace mp {
+
+// Combined top-k weights ("MSCCLPP EP implementation": intranode_combine returns
+// the combined weights with the rows): one thread per (token, slot), fp32 sum
+// over the token's destinations in ascending order from +0.0f.
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_combine_weights(int R, int64_t tokens, int K, const float* __restrict__ w, int64_t rows,
+                     const int32_t* __restrict__ send_row, float* __restrict__ out,
+                     int32_t* __restrict__ dev_err) {
+  const int64_t n = tokens * K;
+  const int64_t stride = int64_t(gridDim.x) * kCopyThreads;
+  for (int64_t i = int64_t(blockIdx.x) * kCopyThreads + threadIdx.x; i < n; i += stride) {
+    const int64_t tok = i / K;
+    const int k = int(i - tok * K);
+    float acc = 0.0f;
+    bool bad = false;
+    for (int d = 0; d < R; ++d) {
+      const int r = __ldg(send_row + tok * R + d);
+      if (r < 0) continue;
+      if (int64_t(r) >= rows) { bad = true; continue; }
+      acc = __fadd_rn(acc, __ldg(w + int64_t(r) * K + k));
+    }
+    out[i] = acc;
+    if (bad) raise_error(dev_err, MP_ERR_CAPACITY);
+  }
+}
+
+cudaError_t launch_combine_weights(int R, int64_t tokens, int K, const float* recv_topk_weights,
+                                   int64_t recv_rows, const int32_t* send_row, float* combined,
+                                   int32_t* dev_err, cudaStream_t stream) {
+  const int64_t n = tokens * K;
+  if (n == 0) return cudaSuccess;
+  static const int per_sm = resident_blocks(mp_k_combine_weights);
+  const unsigned grid = grid_for(per_sm, kCopyThreads, n);
+  mp_k_combine_weights<<<grid, kCopyThreads, 0, stream>>>(R, tokens, K, recv_topk_weights,
+                                                          recv_rows, send_row, combined, dev_err);
+  return cudaGetLastError();
 }
 
 }  // namespace mp

@@ -22,7 +22,24 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                         int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
                         int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
                         int32_t* send_row, int32_t* dev_err, unsigned char* ws,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int global_ids = 0, int32_t sentinel = -1);
+
+// Low-latency expert-major offsets (one block per source rank).
+cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                              int32_t* expert_offsets, int32_t* expert_src_offsets,
+                              int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
+                              cudaStream_t stream);
+
+// out[t] = bf16( sum over k ascending of weights[t][k] * y[slot_row[t][k]] )
+cudaError_t launch_combine_weighted(int K, int64_t tokens, int H, const void* y, int64_t y_rows,
+                                    const int32_t* slot_row, const float* weights, void* out,
+                                    int32_t* dev_err, cudaStream_t stream);
+
+// combined[t][k] = sum over d ascending of recv_topk_weights[send_row[t][d]][k]
+cudaError_t launch_combine_weights(int R, int64_t tokens, int K, const float* recv_topk_weights,
+                                   int64_t recv_rows, const int32_t* send_row, float* combined,
+                                   int32_t* dev_err, cudaStream_t stream);
 
 // Copies token rows (row_bytes each, a multiple of 16) to every receive row
 // listed in send_row; scales_per_row fp32 scales travel with each row.
@@ -46,5 +63,10 @@ cudaError_t launch_reducescatterv(int R, int64_t S, int H, const void* in, void*
 
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream);
+
+// All-gatherv of n tensors (row_bytes[j] bytes per row, multiples of 16) with
+// the same S gathered rows, in one launch.
+cudaError_t launch_allgatherv_multi(int R, int n, const int64_t* row_bytes, int64_t S,
+                                    const void* const* in, void* const* out, cudaStream_t stream);
 
 }  // namespace mp

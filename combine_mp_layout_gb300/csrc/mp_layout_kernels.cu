@@ -143,6 +143,8 @@ struct ScanArgs {
   int32_t* send_row;
   int32_t* dev_err;
   unsigned char* ws;
+  int global_ids;    // recv_topk_idx: 0 = local ids / -1, 1 = global ids / sentinel
+  int32_t sentinel;  // value for non-local entries when global_ids
 };
 
 constexpr int kScanWarps = kScanTokens / kWarp;
@@ -361,7 +363,8 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
         const int tk = tok_of[d][r];
         const int e = idx_s[tk * K + k];
         const bool local = e >= lo && e < hi;
-        a.recv_topk_idx[base * K + i] = local ? e - lo : -1;
+        a.recv_topk_idx[base * K + i] =
+            a.global_ids ? (local ? e : a.sentinel) : (local ? e - lo : -1);
         a.recv_topk_weights[base * K + i] = local ? w_s[tk * K + k] : 0.0f;
         r += step_r;
         k += step_k;
@@ -385,6 +388,91 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
     __threadfence();
     atomicAdd(&ctl->scan_epoch, 1u);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Low-latency expert-major offsets ("MSCCLPP EP implementation", the
+// low-latency dispatch/combine: per-expert receive buffers).  One row per
+// (token, top-k slot with a valid expert); expert e's rows are contiguous,
+// blocks in ascending e, rows inside a block ordered by source rank then
+// token.  One block per source rank; each thread owns a contiguous run of
+// experts, gets its first row from a block-wide scan of the per-expert totals
+// (the layout's num_tokens_per_expert), and walks the rank's top-k slab in
+// token order, so the row order is deterministic.  Meant for the small
+// batches of the low-latency mode (cost per thread ~ N*K per owned expert).
+// ---------------------------------------------------------------------------
+constexpr int kLLThreads = 1024;
+
+__global__ void __launch_bounds__(kLLThreads)
+mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
+                const int32_t* __restrict__ num_tokens_per_expert, int64_t recv_capacity,
+                int32_t* __restrict__ expert_offsets, int32_t* __restrict__ expert_src_offsets,
+                int32_t* __restrict__ recv_src_token, int32_t* __restrict__ slot_row,
+                int32_t* __restrict__ dev_err) {
+  extern __shared__ int32_t ll_topk[];  // [N * K] of this source rank
+  __shared__ int64_t warp_sums[kLLThreads / kWarp];
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nk = int64_t(N) * K;
+  const int32_t* src = topk_idx + int64_t(s) * nk;
+  int32_t* slots = slot_row + int64_t(s) * nk;
+  for (int64_t i = tid; i < nk; i += kLLThreads) {
+    const int e = __ldg(src + i);
+    ll_topk[i] = e;
+    if (e < 0 || e >= E) slots[i] = -1;  // masked or invalid: no row
+  }
+  // this thread's experts [e0, e1) and their totals over every source rank
+  const int cpt = (E + kLLThreads - 1) / kLLThreads;
+  const int e0 = min(E, tid * cpt), e1 = min(E, e0 + cpt);
+  int64_t chunk = 0;
+  for (int e = e0; e < e1; ++e)
+    for (int q = 0; q < R; ++q) chunk += __ldg(num_tokens_per_expert + int64_t(q) * E + e);
+  // block-wide exclusive scan of the chunk totals
+  int64_t inc = chunk;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < kLLThreads / kWarp ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += v;
+    }
+    if (lane < kLLThreads / kWarp) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  int64_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + inc - chunk;
+  bool overflow = false;
+  for (int e = e0; e < e1; ++e) {
+    int64_t tot = 0, pre = 0;
+    for (int q = 0; q < R; ++q) {
+      const int c = __ldg(num_tokens_per_expert + int64_t(q) * E + e);
+      tot += c;
+      if (q < s) pre += c;
+    }
+    if (s == 0) expert_offsets[e] = int32_t(base);
+    expert_src_offsets[int64_t(e) * R + s] = int32_t(pre);
+    int64_t row = base + pre;
+    for (int64_t i = 0; i < nk; ++i) {
+      if (ll_topk[i] != e) continue;
+      if (row < recv_capacity) {
+        slots[i] = int32_t(row);
+        recv_src_token[row] = int32_t(int64_t(s) * N + i / K);
+      } else {
+        slots[i] = -1;
+        overflow = true;
+      }
+      ++row;
+    }
+    base += tot;
+  }
+  if (s == 0 && e0 < E && e1 == E) expert_offsets[E] = int32_t(base);
+  if (overflow) raise_error(dev_err, MP_ERR_CAPACITY);
 }
 
 }  // namespace mp
@@ -428,7 +516,7 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                         int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* dest_offsets,
                         int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
                         int32_t* send_row, int32_t* dev_err, unsigned char* ws,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int global_ids, int32_t sentinel) {
   if (N == 0) {  // no tokens, no rows
     cudaError_t e = cudaMemsetAsync(dest_offsets, 0, sizeof(int32_t) * (R + 1), stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(rank_prefix, 0, sizeof(int32_t) * R * R, stream);
@@ -439,7 +527,7 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
   ScanArgs a{R, N, K, E, topk_idx, topk_weights, is_token_in_rank, num_tokens_per_rank,
              num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx, recv_topk_idx,
              recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
-             dev_err, ws};
+             dev_err, ws, global_ids, sentinel};
   const size_t smem = sizeof(int32_t) * size_t(kScanTokens) * (2 * size_t(K) + R);
   static thread_local int configured_smem[64] = {0};
   int dev = 0;
@@ -451,6 +539,33 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
     configured_smem[dev] = int(smem);
   }
   mp_k_scan<<<unsigned(scan_tiles(R, N)), kScanTokens, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mp
+
+namespace mp {
+
+cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                              int32_t* expert_offsets, int32_t* expert_src_offsets,
+                              int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
+                              cudaStream_t stream) {
+  const size_t smem = sizeof(int32_t) * size_t(N) * K;
+  static thread_local int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && configured[dev] < int(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(mp_k_ll_offsets,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = int(smem);
+  }
+  mp_k_ll_offsets<<<unsigned(R), kLLThreads, smem, stream>>>(R, N, K, E, topk_idx,
+                                                            num_tokens_per_expert, recv_capacity,
+                                                            expert_offsets, expert_src_offsets,
+                                                            recv_src_token, slot_row, dev_err);
   return cudaGetLastError();
 }
 

@@ -186,6 +186,41 @@ int mp_dispatch_rows(int R, int N, int H, int dtype, const void *x, const float 
                      float *recv_scales, mp_stream_t stream);
 
 /*
+ * mp_dispatch_offsets_global -- mp_dispatch_offsets with the receive rows'
+ * expert ids in global numbering ([EP] the later variant that returns
+ * global token-major expert ids with a configurable invalid-expert
+ * sentinel): recv_topk_idx[row][k] = e when topk expert e lives on the row's
+ * destination, else `sentinel` (e.g. E).  Everything else as
+ * mp_dispatch_offsets.
+ */
+int mp_dispatch_offsets_global(int R, int N, int K, int E, const int32_t *topk_idx,
+                               const float *topk_weights, const uint32_t *is_token_in_rank,
+                               const int32_t *num_tokens_per_rank,
+                               const int32_t *num_tokens_per_expert, int64_t recv_capacity,
+                               int32_t sentinel, int32_t *recv_src_rank, int32_t *recv_src_idx,
+                               int32_t *recv_topk_idx, float *recv_topk_weights,
+                               int32_t *dest_offsets, int32_t *rank_prefix,
+                               int32_t *num_recv_tokens_per_expert, int32_t *send_row,
+                               int32_t *dev_err, void *workspace, mp_stream_t stream);
+
+/*
+ * mp_combine_weights -- the combined top-k weights that accompany combine
+ * ([EP] intranode_combine returns the combined weights with the rows).
+ *   in   recv_topk_weights fp32 [recv_rows][K] (as written by dispatch, or
+ *        updated by the experts)
+ *   in   send_row int32 [R][N][R]
+ *   out  combined_topk_weights fp32 [R][N][K]:
+ *        [s][t][k] = sum over d = 0..R-1 ascending with send_row[s][t][d] >= 0
+ *        of recv_topk_weights[send_row[s][t][d]][k], fp32 from +0.0f
+ *        (for an un-modified dispatch: each valid slot's weight, +0 for masked)
+ * Checks: 1 <= R <= 32, N >= 0, 1 <= K <= 32, recv_rows >= 0.
+ * Device errors: MP_ERR_CAPACITY for a send_row entry >= recv_rows (skipped).
+ */
+int mp_combine_weights(int R, int N, int K, const float *recv_topk_weights, int64_t recv_rows,
+                       const int32_t *send_row, float *combined_topk_weights, int32_t *dev_err,
+                       mp_stream_t stream);
+
+/*
  * mp_dispatch_rows_e4m3 -- the row copy with in-kernel FP8 quantisation
  * ([EP] FP8 E4M3 payload with FP32 scales; the pages give no recipe, the
  * reading used: per block of 128 channels of a token row, amax = max |x|,
@@ -286,6 +321,63 @@ int mp_dispatch_noalloc(int R, int N, int K, int E, int H, int dtype, const void
                         float *recv_topk_weights, int32_t *dest_offsets, int32_t *rank_prefix,
                         int32_t *num_recv_tokens_per_expert, int32_t *send_row,
                         int32_t *dev_err, mp_stream_t stream);
+
+/*
+ * mp_allgatherv_multi -- [AGV] all-gatherv of a list of tensors in one launch
+ * (the page's motivation: gathering quantised data and its scales together).
+ * Tensor j has row_bytes[j] bytes per row (a multiple of 16) and the same
+ * per-rank row counts `sizes`; the result for each tensor is exactly
+ * mp_allgatherv(R, row_bytes[j], sizes, in[j], out[j]).
+ *   row_bytes  HOST int64 [ntensors]
+ *   sizes      HOST int64 [R]
+ *   in, out    HOST arrays of ntensors DEVICE pointers (in[j]: [S][row_bytes[j]],
+ *              out[j]: [R][S][row_bytes[j]])
+ * Checks: R >= 1, 1 <= ntensors <= MP_MAX_TENSORS, row_bytes as above,
+ *   sizes >= 0, 16-byte aligned non-NULL pointers when S > 0.
+ */
+#define MP_MAX_TENSORS 8
+int mp_allgatherv_multi(int R, int ntensors, const int64_t *row_bytes, const int64_t *sizes,
+                        const void *const *in, void *const *out, mp_stream_t stream);
+
+/*
+ * Low-latency expert-major layout ([EP] the low-latency dispatch/combine:
+ * per-expert receive buffers, one entry per (token, expert) pair, combine
+ * reducing a token's expert outputs with its top-k weights).  Reading used
+ * (the pages fix no order): expert e's rows are contiguous, blocks in
+ * ascending e; inside a block rows are ordered by source rank, then token.
+ * Meant for the small batches of the low-latency mode: the offsets kernel
+ * runs one block per source rank (N*K*4 bytes of that rank's top-k ids must
+ * fit in 200 KB of shared memory).
+ *
+ * mp_dispatch_ll_offsets
+ *   in   topk_idx               int32 [R][N][K] (-1 = masked)
+ *   in   num_tokens_per_expert  int32 [R][E] from mp_layout (same topk_idx)
+ *   out  expert_offsets         int32 [E+1]: first row of expert e; [E] = total
+ *   out  expert_src_offsets     int32 [E][R]: rows of e from source ranks < s
+ *   out  recv_src_token         int32 [recv_capacity]: flattened s*N + t
+ *   out  slot_row               int32 [R][N][K]: row of (s,t) at expert
+ *                               topk_idx[s][t][k], or -1 (masked / no room)
+ *   Device errors: MP_ERR_CAPACITY (rows past recv_capacity are dropped).
+ * mp_dispatch_ll_rows: recv_x[slot_row[s][t][k]] = x[s][t] (and its scales
+ *   for MP_E4M3), every entry >= 0 and < recv_capacity; x / recv_x / dtype /
+ *   H as mp_dispatch_rows.
+ * mp_combine_ll: out[s][t] = bf16( sum over k = 0..K-1 ascending with
+ *   slot_row[s][t][k] >= 0 of topk_weights[s][t][k] * float(y[row]) ), each
+ *   product and each sum a separate fp32 operation from +0.0f, rounded once
+ *   to bf16 (round-to-nearest-even).  y: bf16 [y_rows][H].
+ *   Device errors: MP_ERR_CAPACITY for a slot_row entry >= y_rows (skipped).
+ */
+int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
+                           const int32_t *num_tokens_per_expert, int64_t recv_capacity,
+                           int32_t *expert_offsets, int32_t *expert_src_offsets,
+                           int32_t *recv_src_token, int32_t *slot_row, int32_t *dev_err,
+                           mp_stream_t stream);
+int mp_dispatch_ll_rows(int R, int N, int K, int H, int dtype, const void *x,
+                        const float *x_scales, const int32_t *slot_row, int64_t recv_capacity,
+                        void *recv_x, float *recv_scales, mp_stream_t stream);
+int mp_combine_ll(int R, int N, int K, int H, const void *y, int64_t y_rows,
+                  const int32_t *slot_row, const float *topk_weights, void *out,
+                  int32_t *dev_err, mp_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -69,6 +69,14 @@ class OracleLib:
         L.oracle_e4m3_to_f32.restype = ctypes.c_float
         L.oracle_quantize_e4m3.argtypes = [i64, i32, P, P, P]
         L.oracle_quantize_e4m3.restype = ctypes.c_int
+        L.oracle_recv_topk_global.argtypes = [i32, i32, i32, i32, P, P, P, P, ctypes.c_int32, P]
+        L.oracle_recv_topk_global.restype = ctypes.c_int
+        L.oracle_combine_weights.argtypes = [i32, i32, i32, P, i64, P, P]
+        L.oracle_combine_weights.restype = ctypes.c_int
+        L.oracle_dispatch_ll.argtypes = [i32, i32, i32, i32, i64, P, P, i64, P, P, P, P, P]
+        L.oracle_dispatch_ll.restype = ctypes.c_int
+        L.oracle_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P]
+        L.oracle_combine_ll.restype = ctypes.c_int
         for f in ("oracle_layout", "oracle_dispatch", "oracle_combine",
                   "oracle_reducescatterv", "oracle_allgatherv"):
             getattr(L, f).restype = ctypes.c_int
@@ -185,6 +193,62 @@ class OracleLib:
         st = self.L.oracle_quantize_e4m3(T, H, _p(x_bits), _p(q), _p(sc))
         return q, sc, st
 
+    def recv_topk_global(self, topk_idx, E, disp: dict, sentinel: int):
+        """Global expert ids of the receive rows of an oracle dispatch result."""
+        topk_idx = _c(topk_idx, np.int32)
+        R, N, K = topk_idx.shape
+        T = int(disp["num_recv"])
+        out = np.full((max(T, 1), K), -7, np.int32)
+        src_rank = _c(disp["recv_src_rank"], np.int32)
+        src_idx = _c(disp["recv_src_idx"], np.int32)
+        offs = _c(disp["dest_offsets"], np.int32)
+        st = self.L.oracle_recv_topk_global(R, N, K, E, _p(topk_idx), _p(src_rank), _p(src_idx),
+                                            _p(offs), sentinel, _p(out))
+        return out[:T], st
+
+    def combine_weights(self, recv_topk_weights: np.ndarray, send_row: np.ndarray):
+        """recv_topk_weights fp32 [rows][K], send_row [R][N][R] -> (fp32 [R][N][K], status)."""
+        w = _c(recv_topk_weights, np.float32)
+        send_row = _c(send_row, np.int32)
+        R, N, _ = send_row.shape
+        K = w.shape[1]
+        out = np.zeros((R, N, K), np.float32)
+        st = self.L.oracle_combine_weights(R, N, K, _p(w), w.shape[0], _p(send_row), _p(out))
+        return out, st
+
+    def dispatch_ll(self, x: np.ndarray, topk_idx: np.ndarray, E: int,
+                    recv_capacity: int | None = None):
+        """Expert-major low-latency dispatch of x [R][N][...] (bytes copied)."""
+        x = np.ascontiguousarray(x)
+        topk_idx = _c(topk_idx, np.int32)
+        R, N, K = topk_idx.shape
+        row_shape = x.shape[2:]
+        row_bytes = x.itemsize * int(np.prod(row_shape))
+        total = int(((topk_idx >= 0) & (topk_idx < E)).sum())
+        cap = total if recv_capacity is None else int(recv_capacity)
+        n1 = max(cap, 1)
+        recv_x = np.zeros((n1,) + row_shape, x.dtype)
+        src = np.full(n1, -7, np.int32)
+        eoff = np.zeros(E + 1, np.int32)
+        esoff = np.zeros((E, R), np.int32)
+        slot = np.zeros((R, N, K), np.int32)
+        st = self.L.oracle_dispatch_ll(R, N, K, E, row_bytes, _p(x), _p(topk_idx), cap,
+                                       _p(recv_x), _p(src), _p(eoff), _p(esoff), _p(slot))
+        n = min(cap, total)
+        return dict(recv_x=recv_x[:n], recv_src_token=src[:n], expert_offsets=eoff,
+                    expert_src_offsets=esoff, slot_row=slot, num_recv=total), st
+
+    def combine_ll(self, y_bits: np.ndarray, slot_row: np.ndarray, topk_weights: np.ndarray):
+        y_bits = _c(y_bits, np.uint16)
+        slot_row = _c(slot_row, np.int32)
+        w = _c(topk_weights, np.float32)
+        R, N, K = slot_row.shape
+        H = y_bits.shape[1]
+        out = np.zeros((R, N, H), np.uint16)
+        st = self.L.oracle_combine_ll(R, N, K, H, _p(y_bits), y_bits.shape[0], _p(slot_row),
+                                      _p(w), _p(out))
+        return out, st
+
     def f32_to_bf16_array(self, a: np.ndarray) -> np.ndarray:
         """Element-wise oracle narrowing of a binary32 array to bf16 bit patterns."""
         a = np.ascontiguousarray(a, np.float32)
@@ -238,3 +302,19 @@ def f32_to_bf16_array(a):
 
 def quantize_e4m3(x_bits):
     return default().quantize_e4m3(x_bits)
+
+
+def recv_topk_global(topk_idx, E, disp, sentinel):
+    return default().recv_topk_global(topk_idx, E, disp, sentinel)
+
+
+def combine_weights(recv_topk_weights, send_row):
+    return default().combine_weights(recv_topk_weights, send_row)
+
+
+def dispatch_ll(x, topk_idx, E, recv_capacity=None):
+    return default().dispatch_ll(x, topk_idx, E, recv_capacity)
+
+
+def combine_ll(y_bits, slot_row, topk_weights):
+    return default().combine_ll(y_bits, slot_row, topk_weights)

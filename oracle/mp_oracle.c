@@ -339,3 +339,126 @@ int oracle_quantize_e4m3(int64_t T, int H, const uint16_t *x, uint8_t *q, float 
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Receive-row expert ids in global numbering [EP, the later variant */
+/* that returns global token-major expert ids with a configurable     */
+/* invalid-expert sentinel]: for receive row r at destination d (the  */
+/* d with dest_offsets[d] <= r < dest_offsets[d+1]) holding token     */
+/* (s, t): out[r][k] = e when e = topk_idx[s][t][k] lives on d, else  */
+/* `sentinel`.                                                        */
+/* ------------------------------------------------------------------ */
+int oracle_recv_topk_global(int R, int N, int K, int E, const int32_t *topk_idx,
+                            const int32_t *recv_src_rank, const int32_t *recv_src_idx,
+                            const int32_t *dest_offsets, int32_t sentinel, int32_t *out) {
+  if (R < 1 || N < 0 || K < 1 || E < R || E % R != 0) return ORC_BAD_ARG;
+  const int El = E / R;
+  for (int d = 0; d < R; ++d) {
+    for (int64_t r = dest_offsets[d]; r < dest_offsets[d + 1]; ++r) {
+      const int64_t tok = (int64_t)recv_src_rank[r] * N + recv_src_idx[r];
+      for (int k = 0; k < K; ++k) {
+        const int32_t e = topk_idx[tok * K + k];
+        out[r * K + k] = (e >= d * El && e < (d + 1) * El) ? e : sentinel;
+      }
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Combined top-k weights [EP, intranode_combine returns the combined */
+/* weights alongside the combined rows]: for token (s,t) and slot k,  */
+/* the binary32 sum from +0.0f, over d = 0..R-1 ascending with        */
+/* send_row[s][t][d] >= 0, of recv_topk_weights[send_row][k].         */
+/* ------------------------------------------------------------------ */
+int oracle_combine_weights(int R, int N, int K, const float *recv_topk_weights,
+                           int64_t recv_rows, const int32_t *send_row, float *out) {
+  if (R < 1 || N < 0 || K < 1 || recv_rows < 0) return ORC_BAD_ARG;
+  int status = 0;
+  for (int64_t tok = 0; tok < (int64_t)R * N; ++tok) {
+    for (int k = 0; k < K; ++k) {
+      float acc = 0.0f;
+      for (int d = 0; d < R; ++d) {
+        const int32_t r = send_row[tok * R + d];
+        if (r < 0) continue;
+        if ((int64_t)r >= recv_rows) { status |= ORC_CAPACITY; continue; }
+        acc = acc + recv_topk_weights[(int64_t)r * K + k];
+      }
+      out[tok * K + k] = acc;
+    }
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------ */
+/* Low-latency expert-major layout [EP, low-latency dispatch/combine: */
+/* per-expert receive buffers, one entry per (token, expert) pair].   */
+/* Reading (the pages fix no order): expert e's rows are contiguous,  */
+/* blocks in ascending e; inside a block rows are ordered by source   */
+/* rank, then token, ascending.  A masked slot (-1) or an id outside  */
+/* [0, E) gets no row.                                                */
+/*   expert_offsets[e]    first row of expert e; [E] = total rows     */
+/*   expert_src_offsets[e][s] rows of e from source ranks < s         */
+/*   recv_src_token[row]  flattened source token s*N + t              */
+/*   slot_row[s][t][k]    row of (s,t) at expert topk_idx[s][t][k], -1 */
+/*   recv_x[row]          x[s][t] (row_bytes bytes)                   */
+/* ------------------------------------------------------------------ */
+int oracle_dispatch_ll(int R, int N, int K, int E, int64_t row_bytes, const uint8_t *x,
+                       const int32_t *topk_idx, int64_t recv_capacity, uint8_t *recv_x,
+                       int32_t *recv_src_token, int32_t *expert_offsets,
+                       int32_t *expert_src_offsets, int32_t *slot_row) {
+  if (R < 1 || N < 0 || K < 1 || E < 1 || row_bytes < 0 || recv_capacity < 0) return ORC_BAD_ARG;
+  int status = 0;
+  for (int64_t i = 0; i < (int64_t)R * N * K; ++i) slot_row[i] = -1;
+  int64_t row = 0;
+  for (int e = 0; e < E; ++e) {
+    expert_offsets[e] = (int32_t)row;
+    for (int s = 0; s < R; ++s) {
+      expert_src_offsets[(int64_t)e * R + s] = (int32_t)(row - expert_offsets[e]);
+      for (int t = 0; t < N; ++t) {
+        const int64_t tok = (int64_t)s * N + t;
+        for (int k = 0; k < K; ++k) {
+          if (topk_idx[tok * K + k] != e) continue;
+          if (row < recv_capacity) {
+            memcpy(recv_x + row * row_bytes, x + tok * row_bytes, (size_t)row_bytes);
+            recv_src_token[row] = (int32_t)tok;
+            slot_row[tok * K + k] = (int32_t)row;
+          } else {
+            status |= ORC_CAPACITY;
+          }
+          row += 1;
+        }
+      }
+    }
+  }
+  expert_offsets[E] = (int32_t)row;
+  return status;
+}
+
+/* Low-latency combine [EP, low-latency combine: the expert outputs of a   */
+/* token are reduced with its top-k weights]: out[s][t] = bf16( sum over   */
+/* k = 0..K-1 ascending with slot_row >= 0 of w[s][t][k] * float(y[row]) ), */
+/* each product and each sum a separate binary32 operation, from +0.0f.    */
+int oracle_combine_ll(int R, int N, int K, int H, const uint16_t *y, int64_t y_rows,
+                      const int32_t *slot_row, const float *topk_weights, uint16_t *out) {
+  if (R < 1 || N < 0 || K < 1 || H < 0 || y_rows < 0) return ORC_BAD_ARG;
+  int status = 0;
+  float *acc = (float *)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+  if (!acc) return ORC_BAD_ARG;
+  for (int64_t tok = 0; tok < (int64_t)R * N; ++tok) {
+    for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const int32_t r = slot_row[tok * K + k];
+      if (r < 0) continue;
+      if ((int64_t)r >= y_rows) { status |= ORC_CAPACITY; continue; }
+      const float w = topk_weights[tok * K + k];
+      for (int h = 0; h < H; ++h) {
+        const float p = w * oracle_bf16_to_f32(y[(int64_t)r * H + h]);
+        acc[h] = acc[h] + p;
+      }
+    }
+    for (int h = 0; h < H; ++h) out[tok * H + h] = oracle_f32_to_bf16(acc[h]);
+  }
+  free(acc);
+  return status;
+}

@@ -98,6 +98,19 @@ def pin_ep_hand_fixture(orc) -> None:
     assert st == 0 and np.array_equal(comb, _bits(ex["combine_of_recv_x"]))
     comb, st = orc.combine(_bits(ex["y"]), out["send_row"])
     assert st == 0 and np.array_equal(comb, _bits(ex["combine_of_y"]))
+    gid, st = orc.recv_topk_global(idx, E, out, 4)
+    assert st == 0 and gid.tolist() == ex["recv_topk_idx_global_sentinel_4"]
+    cw, st = orc.combine_weights(out["recv_topk_weights"], out["send_row"])
+    assert st == 0 and cw.tolist() == ex["combined_topk_weights"]
+    ll, st = orc.dispatch_ll(x, idx, E)
+    assert st == 0
+    assert ll["expert_offsets"].tolist() == ex["ll_expert_offsets"]
+    assert ll["expert_src_offsets"].tolist() == ex["ll_expert_src_offsets"]
+    assert ll["recv_src_token"].tolist() == ex["ll_recv_src_token"]
+    assert ll["slot_row"].tolist() == ex["ll_slot_row"]
+    assert np.array_equal(ll["recv_x"], x.reshape(-1, x.shape[-1])[ll["recv_src_token"]])
+    comb, st = orc.combine_ll(ll["recv_x"], ll["slot_row"], w)
+    assert st == 0 and np.array_equal(comb, _bits(ex["ll_combine_of_recv_x"]))
 
 
 def brute_force_ep(topk_idx: np.ndarray, topk_weights: np.ndarray, E: int):
@@ -203,6 +216,68 @@ def pin_ep_invariants(orc) -> None:
         # every local topk entry of a row points at a real expert of that destination
         loc = out["recv_topk_idx"]
         assert np.all((loc == -1) | ((loc >= 0) & (loc < El)))
+
+
+def pin_global_ids_and_combined_weights(orc) -> None:
+    """Global ids are the local ids shifted back by d*E/R (sentinel where the local id
+    is -1); combined weights of an un-modified dispatch give back each valid slot's
+    weight exactly (the other destinations add +0) and +0 for masked slots."""
+    inp = wl.make_ep("skew", seed=8, N=96, H=8)
+    R, N, K, E = inp.R, inp.N, inp.K, inp.E
+    idx = inp.topk_idx.copy()
+    idx[:, ::5, 1] = -1
+    _, _, mask, _ = orc.layout(idx, E)
+    out, _ = orc.dispatch(np.zeros((R, N, 8), np.uint16), idx, inp.topk_weights, mask, E)
+    El = E // R
+    for sentinel in (E, -1, 12345):
+        gid, st = orc.recv_topk_global(idx, E, out, sentinel)
+        assert st == 0
+        dest = np.searchsorted(out["dest_offsets"], np.arange(out["num_recv"]), side="right") - 1
+        loc = out["recv_topk_idx"]
+        want = np.where(loc >= 0, loc + (dest * El)[:, None], sentinel)
+        assert np.array_equal(gid, want)
+    cw, st = orc.combine_weights(out["recv_topk_weights"], out["send_row"])
+    assert st == 0
+    valid = (idx >= 0) & (idx < E)
+    assert np.array_equal(cw.view(np.uint32),
+                          np.where(valid, inp.topk_weights, np.float32(0)).view(np.uint32))
+
+
+def pin_low_latency_layout(orc) -> None:
+    """Expert-major rows against a sorted enumeration of (expert, source, token) triples;
+    the weighted combine against exact sums where every step is exact."""
+    rng = np.random.default_rng(17)
+    for R, N, E, K in [(2, 9, 6, 3), (3, 16, 12, 4), (4, 5, 4, 4), (1, 7, 3, 2)]:
+        idx = wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)
+        idx[rng.random(idx.shape) < 0.2] = -1
+        x = rng.integers(0, 60000, (R, N, 8)).astype(np.uint16)
+        ll, st = orc.dispatch_ll(x, idx, E)
+        assert st == 0
+        triples = sorted((int(idx[s, t, k]), s, t, k) for s in range(R) for t in range(N)
+                         for k in range(K) if idx[s, t, k] >= 0)
+        assert ll["num_recv"] == len(triples) == ll["expert_offsets"][E]
+        for r, (e, s, t, k) in enumerate(triples):
+            assert ll["slot_row"][s, t, k] == r and ll["recv_src_token"][r] == s * N + t
+            assert ll["expert_offsets"][e] <= r < ll["expert_offsets"][e + 1]
+            assert np.array_equal(ll["recv_x"][r], x[s, t])
+        for e in range(E):
+            for s in range(R):
+                before = sum(1 for tr in triples if tr[0] == e and tr[1] < s)
+                assert ll["expert_src_offsets"][e, s] == before
+        assert np.all(ll["slot_row"][idx < 0] == -1)
+        # weights that are powers of two and small-integer rows: every product and
+        # partial sum is exact, so the result is the exact weighted sum
+        wts = np.exp2(-rng.integers(0, 4, idx.shape)).astype(np.float32)
+        y = rng.integers(-8, 9, (ll["num_recv"], 8)).astype(np.float32)
+        comb, st = orc.combine_ll(_bits(y), ll["slot_row"], wts)
+        exact = np.zeros((R, N, 8))
+        for s in range(R):
+            for t in range(N):
+                for k in range(K):
+                    r = ll["slot_row"][s, t, k]
+                    if r >= 0:
+                        exact[s, t] += float(wts[s, t, k]) * y[r]
+        assert st == 0 and np.array_equal(_f32(comb), exact.astype(np.float32))
 
 
 def pin_ep_special_cases(orc) -> None:
@@ -410,4 +485,5 @@ def pin_block_quantisation(orc) -> None:
 
 ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
-            pin_e4m3_conversions, pin_block_quantisation]
+            pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
+            pin_low_latency_layout]

@@ -33,11 +33,12 @@ MUTANTS = {
                                   "if (e >= 0 && e < E) num_recv_tokens_per_expert[(e + 1) % E] += 1;"),
     "combine_descending": ("for (int d = 0; d < R; ++d) {\n        int32_t r = send_row",
                            "for (int d = R - 1; d >= 0; --d) {\n        int32_t r = send_row"),
-    "combine_negative_zero_start": ("for (int h = 0; h < H; ++h) acc[h] = 0.0f;",
-                                    "for (int h = 0; h < H; ++h) acc[h] = -0.0f;"),
-    "combine_drops_first_rank": ("if (r < 0) continue;", "if (r < 0 || d == 0) continue;"),
-    "combine_in_double": ("float *acc = (float *)malloc(sizeof(float)",
-                          "double *acc = (double *)malloc(sizeof(double)"),
+    "combine_negative_zero_start": ("const int64_t tok = (int64_t)s * N + t;\n      for (int h = 0; h < H; ++h) acc[h] = 0.0f;",
+                                    "const int64_t tok = (int64_t)s * N + t;\n      for (int h = 0; h < H; ++h) acc[h] = -0.0f;"),
+    "combine_drops_first_rank": ("if (r < 0) continue;\n        if ((int64_t)r >= y_rows)",
+                                 "if (r < 0 || d == 0) continue;\n        if ((int64_t)r >= y_rows)"),
+    "combine_in_double": ("R > 32 || N < 0 || H < 0 || y_rows < 0) return ORC_BAD_ARG;\n  int status = 0;\n  float *acc = (float *)malloc(sizeof(float)",
+                          "R > 32 || N < 0 || H < 0 || y_rows < 0) return ORC_BAD_ARG;\n  int status = 0;\n  double *acc = (double *)malloc(sizeof(double)"),
     "rsv_descending": ("for (int q = 0; q < R; ++q)\n          acc = acc",
                        "for (int q = R - 1; q >= 0; --q)\n          acc = acc"),
     "rsv_in_double": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
@@ -51,6 +52,18 @@ MUTANTS = {
     "quant_multiplies": ("oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / scale)",
                          "oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) * scale)"),
     "quant_zero_scale": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 448.0f : 0.0f"),
+    "global_ids_sentinel_ignored": ("(e >= d * El && e < (d + 1) * El) ? e : sentinel;",
+                                    "(e >= d * El && e < (d + 1) * El) ? e : -1;"),
+    "global_ids_off_by_rank": ("for (int d = 0; d < R; ++d) {\n    for (int64_t r = dest_offsets[d]; r < dest_offsets[d + 1]; ++r) {",
+                               "for (int d = 0; d < R; ++d) {\n    for (int64_t r = dest_offsets[d]; r < dest_offsets[d + 1] - (d == 0); ++r) {"),
+    "combined_weights_skip_last": ("        acc = acc + recv_topk_weights[(int64_t)r * K + k];",
+                                   "        if (d < R - 1) acc = acc + recv_topk_weights[(int64_t)r * K + k];"),
+    "ll_source_major": ("  for (int e = 0; e < E; ++e) {\n    expert_offsets[e] = (int32_t)row;\n    for (int s = 0; s < R; ++s) {",
+                        "  for (int e = E - 1; e >= 0; --e) {\n    expert_offsets[e] = (int32_t)row;\n    for (int s = 0; s < R; ++s) {"),
+    "ll_unweighted": ("const float p = w * oracle_bf16_to_f32(y[(int64_t)r * H + h]);",
+                      "const float p = oracle_bf16_to_f32(y[(int64_t)r * H + h]);"),
+    "ll_keeps_masked": ("if (topk_idx[tok * K + k] != e) continue;",
+                        "if (topk_idx[tok * K + k] != e && !(e == 0 && topk_idx[tok * K + k] == -1)) continue;"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
 }

@@ -329,6 +329,92 @@ def test_rsv_agv_small(R, H, sizes):
     assert np.array_equal(wl.bf16_bits(plan.ag_out), ag)
 
 
+def test_global_ids_and_combined_weights():
+    inp = wl.make_ep("skew", seed=12, N=700, H=64)
+    R, N, K, E = inp.R, inp.N, inp.K, inp.E
+    inp.topk_idx[:, ::9, 2] = -1
+    plan = EPPlan(R, N, K, E, inp.H)
+    plan.load(inp)
+    B.check(plan.layout())
+    gids = torch.full_like(plan.recv_topk_idx, -3)
+    B.check(B.mp_dispatch_offsets_global(
+        R, N, K, E, plan.topk_idx, plan.topk_weights, plan.is_token_in_rank,
+        plan.num_tokens_per_rank, plan.num_tokens_per_expert, plan.cap, E, plan.recv_src_rank,
+        plan.recv_src_idx, gids, plan.recv_topk_weights, plan.dest_offsets, plan.rank_prefix,
+        plan.num_recv_tokens_per_expert, plan.send_row, plan.dev_err, plan.workspace))
+    cw = torch.full((R, N, K), -3.0, device="cuda")
+    B.check(B.mp_combine_weights(R, N, K, plan.recv_topk_weights, plan.cap, plan.send_row, cw,
+                                 plan.dev_err))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    out, st = oracle.dispatch(np.zeros((R, N, 8), np.uint16), inp.topk_idx, inp.topk_weights,
+                              mask, E)
+    want_gid, st2 = oracle.recv_topk_global(inp.topk_idx, E, out, E)
+    want_cw, st3 = oracle.combine_weights(out["recv_topk_weights"], out["send_row"])
+    assert st == st2 == st3 == 0
+    n = out["num_recv"]
+    assert np.array_equal(gids[:n].cpu().numpy(), want_gid)
+    assert np.array_equal(plan.send_row.cpu().numpy(), out["send_row"])
+    assert np.array_equal(cw.cpu().numpy().view(np.uint32), want_cw.view(np.uint32))
+
+
+@pytest.mark.parametrize("cfg", [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
+                                 dict(R=5, N=77, E=20, K=6, H=264), dict(R=3, N=300, E=9, K=9, H=64)],
+                         ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c)
+def test_low_latency_layout_matches_oracle(cfg):
+    inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=cfg["N"])
+    R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
+    inp.topk_idx[:, ::7, 1] = -1
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    cap = R * N * K
+    dev = "cuda"
+    eoff = torch.full((E + 1,), -3, dtype=torch.int32, device=dev)
+    esoff = torch.full((E, R), -3, dtype=torch.int32, device=dev)
+    src = torch.full((cap,), -3, dtype=torch.int32, device=dev)
+    slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+    B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, plan.num_tokens_per_expert, cap,
+                                     eoff, esoff, src, slot, plan.dev_err))
+    B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
+    y = wl.random_bf16((cap, H), seed=N).cuda()
+    out = torch.zeros((R, N, H), dtype=torch.bfloat16, device=dev)
+    B.check(B.mp_combine_ll(R, N, K, H, y, cap, slot, plan.topk_weights, out, plan.dev_err))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    ll, st = oracle.dispatch_ll(wl.bf16_bits(inp.x), inp.topk_idx, E)
+    assert st == 0
+    n = ll["num_recv"]
+    assert np.array_equal(eoff.cpu().numpy(), ll["expert_offsets"])
+    assert np.array_equal(esoff.cpu().numpy(), ll["expert_src_offsets"])
+    assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+    assert np.array_equal(src[:n].cpu().numpy(), ll["recv_src_token"])
+    assert np.array_equal(wl.bf16_bits(rx[:n]), ll["recv_x"])
+    comb, st = oracle.combine_ll(wl.bf16_bits(y), ll["slot_row"], inp.topk_weights)
+    assert st == 0
+    assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll")
+
+
+def test_allgatherv_multi_matches_per_tensor_oracle():
+    R, sizes = 5, [7, 0, 130, 1, 33]
+    S = sum(sizes)
+    g = torch.Generator().manual_seed(5)
+    data = torch.randint(0, 256, (S, 2048), generator=g, dtype=torch.uint8)      # e.g. packed fp4
+    scales = torch.randint(0, 256, (S, 16 * 8), generator=g, dtype=torch.uint8)  # 128-byte rows
+    hid = torch.randn((S, 72), generator=g).to(torch.bfloat16)                    # 144-byte rows
+    ins = [data, scales, hid]
+    outs = [torch.zeros((R,) + tuple(t.shape), dtype=t.dtype, device="cuda") for t in ins]
+    row_bytes = [t[0].nbytes for t in ins]
+    B.check(B.mp_allgatherv_multi(R, row_bytes, sizes, [t.cuda() for t in ins], outs))
+    torch.cuda.synchronize()
+    for t, o in zip(ins, outs):
+        want, st = oracle.allgatherv(t.view(torch.uint8).numpy(), sizes, R)
+        assert st == 0
+        assert np.array_equal(o.cpu().view(torch.uint8).numpy(), want)
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads (the benchmark's launch configuration)
 # ---------------------------------------------------------------------------
