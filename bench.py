@@ -69,6 +69,25 @@ def replica_throughput(units_per_rank: int, steps: int, world: int, ms_max: floa
     return units_per_rank * world * steps / (ms_max / 1e3)
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or when the kernel's
+    source files have changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        h = hashlib.sha256()
+        for p in rec["source_files"]:
+            with open(os.path.join(ROOT, p), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        return int(rec["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -489,10 +508,14 @@ def main():
     peak, peak_kind = peaks()
     dom = "rows" if ph["rows"] >= ph["combine"] else "combine"
     achieved = nb[dom] / (ph[dom] / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": {"rows": "mp_k_dispatch (dispatch row copy)",
-                                           "combine": "mp_k_combine"}[dom],
-                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_kind": peak_kind, "traffic": None,
+    kname = {"rows": "mp_k_dispatch<8,2>", "combine": "mp_k_combine<8,1,4,0>"}[dom]
+    traffic = recorded_traffic(kname) if (args.config == "dsv3" and args.tokens == 0) else None
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": traffic,
+                "traffic_note": "ncu dram read+write per launch, scaled by tokens from an "
+                                "N=1536 capture summarised under profiles/; null if the "
+                                "kernel source changed since",
                 "all_phases": {k: {"ms": ph[k], "algorithmic_bytes": nb[k],
                                    "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in nb}}
 

@@ -45,3 +45,20 @@ def test_max_over_ranks_and_whole_job_throughput():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(3.0, 1) == 3.0
     assert bench.replica_throughput(100, 4, 1, 2.0) == 100 * 4 / 2e-3
+
+
+def test_recorded_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+    import json
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    import hashlib
+    rec = {"k": {"traffic_bytes_per_launch": 123, "source_files": ["k.cu"],
+                 "source_sha256": hashlib.sha256(b"kernel v1").hexdigest()}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k") == 123
+    src.write_text("kernel v2")  # the kernel changed since the counters were taken
+    assert bench.recorded_traffic("k") is None
+    assert bench.recorded_traffic("other") is None
