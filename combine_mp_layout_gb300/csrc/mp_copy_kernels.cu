@@ -26,6 +26,10 @@
 #ifndef MP_DISPATCH_U
 #define MP_DISPATCH_U 2
 #endif
+// dispatch grid = resident blocks x this (more than one wave when > 1)
+#ifndef MP_DISPATCH_GRID_MULT
+#define MP_DISPATCH_GRID_MULT 1
+#endif
 #ifndef MP_COMBINE_NW
 #define MP_COMBINE_NW 8
 #endif
@@ -562,7 +566,7 @@ static cudaError_t dispatch_copy_nw(int R, int64_t tokens, int64_t row_bytes, co
                                     void* recv_x, int64_t recv_capacity, const int32_t* send_row,
                                     int spr, const float* x_scales, float* recv_scales,
                                     cudaStream_t stream) {
-  static const int per_sm = resident_blocks(mp_k_dispatch<NW, U>);
+  static const int per_sm = resident_blocks(mp_k_dispatch<NW, U>) * MP_DISPATCH_GRID_MULT;
   const int64_t vpr = row_bytes / (4 * NW);
   const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
   const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
