@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/mp_layout.h"
@@ -228,6 +229,14 @@ __device__ __forceinline__ int4 pack_bf16x8(const float* acc) {
   r.z = int(pack_bf16x2_rn(acc[4], acc[5]));
   r.w = int(pack_bf16x2_rn(acc[6], acc[7]));
   return r;
+}
+
+// Kernel launch used by every launcher (one place to change launch attributes).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                        size_t smem, cudaStream_t stream, Args&&... args) {
+  kernel<<<grid, block, smem, stream>>>(std::forward<Args>(args)...);
+  return cudaGetLastError();
 }
 
 // Bounded spin for the decoupled lookback: about a second at most (2^20

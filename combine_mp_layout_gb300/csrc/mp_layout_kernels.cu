@@ -147,7 +147,8 @@ struct ScanArgs {
   int32_t sentinel;  // value for non-local entries when global_ids
 };
 
-constexpr int kScanWarps = kScanTokens / kWarp;
+constexpr int kScanThreads = 256;  // two threads per token of a tile
+constexpr int kScanWarps = kScanThreads / kWarp;
 
 // Warp-wide sum; every lane gets the total.
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
@@ -156,7 +157,7 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
   return v;
 }
 
-__global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
+__global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   extern __shared__ int32_t sm_scan[];
   int32_t* idx_s = sm_scan;                                             // [kScanTokens * K]
   float* w_s = reinterpret_cast<float*>(sm_scan + kScanTokens * a.K);  // [kScanTokens * K]
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
     const int32_t* gi = a.topk_idx + g0 * K;
     const float* gw = a.topk_weights + g0 * K;
 #pragma unroll 4
-    for (int i = tid; i < n; i += kScanTokens) {
+    for (int i = tid; i < n; i += kScanThreads) {
       idx_s[i] = __ldg(gi + i);
       w_s[i] = __ldg(gw + i);
     }
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
     if (lane < R) row_base[lane] = (inc - tot) + pre + excl;
   } else if (tile == 0) {
     // warps 1..: the small per-destination tables, while warp 0 publishes
-    const int t = tid - kWarp, nt = kScanTokens - kWarp;
+    const int t = tid - kWarp, nt = kScanThreads - kWarp;
     for (int i = t; i < R * R; i += nt) {  // rank_prefix[s][d]
       const int s = i / R, d = i - s * R;
       int sum = 0;
@@ -340,10 +341,11 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
     }
   }
   __syncthreads();
-  for (int i = tid; i < ntok * R; i += kScanTokens) a.send_row[g0 * R + i] = sr_s[i];
+#pragma unroll 4
+  for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sr_s[i];
   {
     const int El = E / R;
-    const int step_r = kScanTokens / K, step_k = kScanTokens - step_r * K;
+    const int step_r = kScanThreads / K, step_k = kScanThreads - step_r * K;
     bool overflow = false;
     for (int d = 0; d < R; ++d) {
       const int64_t base = row_base[d];
@@ -351,15 +353,17 @@ __global__ void __launch_bounds__(kScanTokens) mp_k_scan(ScanArgs a) {
       const int64_t room = a.recv_capacity - base;
       const int n_ok = room <= 0 ? 0 : (room < cnt ? int(room) : cnt);
       overflow |= n_ok < cnt;
-      for (int i = tid; i < n_ok; i += kScanTokens) {
+#pragma unroll 4
+      for (int i = tid; i < n_ok; i += kScanThreads) {
         a.recv_src_rank[base + i] = src_rank;
         a.recv_src_idx[base + i] = t0 + tok_of[d][i];
       }
       const int lo = d * El, hi = lo + El;
       // element i = r*K + k of this destination's rows; (r, k) advance by
-      // (kScanTokens / K, kScanTokens % K) per step, avoiding a division
+      // (kScanThreads / K, kScanThreads % K) per step, avoiding a division
       int r = tid / K, k = tid - (tid / K) * K;
-      for (int i = tid; i < n_ok * K; i += kScanTokens) {
+#pragma unroll 4
+      for (int i = tid; i < n_ok * K; i += kScanThreads) {
         const int tk = tok_of[d][r];
         const int e = idx_s[tk * K + k];
         const bool local = e >= lo && e < hi;
@@ -503,10 +507,9 @@ cudaError_t launch_layout(int R, int N, int K, int E, const int32_t* topk_idx,
     configured_smem[dev] = int(smem);
   }
   dim3 grid(unsigned(layout_blocks_per_rank(N)), unsigned(R));
-  mp_k_layout<<<grid, kLayoutTokens, smem, stream>>>(R, N, K, E, topk_idx, num_tokens_per_rank,
-                                                      num_tokens_per_expert, is_token_in_rank,
-                                                      dev_err, ws);
-  return cudaGetLastError();
+  return launch_kernel(mp_k_layout, dim3(grid), dim3(kLayoutTokens), smem, stream, R, N, K, E,
+                       topk_idx, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                       dev_err, ws);
 }
 
 cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
@@ -538,8 +541,8 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
     if (e != cudaSuccess) return e;
     configured_smem[dev] = int(smem);
   }
-  mp_k_scan<<<unsigned(scan_tiles(R, N)), kScanTokens, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(mp_k_scan, dim3(unsigned(scan_tiles(R, N))), dim3(kScanThreads), smem,
+                       stream, a);
 }
 
 }  // namespace mp
@@ -562,11 +565,9 @@ cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_id
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  mp_k_ll_offsets<<<unsigned(R), kLLThreads, smem, stream>>>(R, N, K, E, topk_idx,
-                                                            num_tokens_per_expert, recv_capacity,
-                                                            expert_offsets, expert_src_offsets,
-                                                            recv_src_token, slot_row, dev_err);
-  return cudaGetLastError();
+  return launch_kernel(mp_k_ll_offsets, dim3(unsigned(R)), dim3(kLLThreads), smem, stream, R, N, K,
+                       E, topk_idx, num_tokens_per_expert, recv_capacity, expert_offsets,
+                       expert_src_offsets, recv_src_token, slot_row, dev_err);
 }
 
 }  // namespace mp

@@ -73,6 +73,8 @@ class OracleLib:
         L.oracle_recv_topk_global.restype = ctypes.c_int
         L.oracle_combine_weights.argtypes = [i32, i32, i32, P, i64, P, P]
         L.oracle_combine_weights.restype = ctypes.c_int
+        L.oracle_quantize_mxfp8.argtypes = [i64, i32, P, P, P]
+        L.oracle_quantize_mxfp8.restype = ctypes.c_int
         L.oracle_dispatch_ll.argtypes = [i32, i32, i32, i32, i64, P, P, i64, P, P, P, P, P]
         L.oracle_dispatch_ll.restype = ctypes.c_int
         L.oracle_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P]
@@ -193,6 +195,17 @@ class OracleLib:
         st = self.L.oracle_quantize_e4m3(T, H, _p(x_bits), _p(q), _p(sc))
         return q, sc, st
 
+    def quantize_mxfp8(self, x_bits: np.ndarray):
+        """x_bits uint16 (bf16 patterns) [..., H] -> (q uint8 [..., H], UE8M0 codes uint8
+        [..., H/32], status)."""
+        x_bits = _c(x_bits, np.uint16)
+        H = x_bits.shape[-1]
+        T = x_bits.size // H if H else 0
+        q = np.zeros(x_bits.shape, np.uint8)
+        codes = np.zeros(x_bits.shape[:-1] + (max(H // 32, 1),), np.uint8)
+        st = self.L.oracle_quantize_mxfp8(T, H, _p(x_bits), _p(q), _p(codes))
+        return q, codes, st
+
     def recv_topk_global(self, topk_idx, E, disp: dict, sentinel: int):
         """Global expert ids of the receive rows of an oracle dispatch result."""
         topk_idx = _c(topk_idx, np.int32)
@@ -306,6 +319,10 @@ def quantize_e4m3(x_bits):
 
 def recv_topk_global(topk_idx, E, disp, sentinel):
     return default().recv_topk_global(topk_idx, E, disp, sentinel)
+
+
+def quantize_mxfp8(x_bits):
+    return default().quantize_mxfp8(x_bits)
 
 
 def combine_weights(recv_topk_weights, send_row):

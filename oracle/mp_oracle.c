@@ -462,3 +462,52 @@ int oracle_combine_ll(int R, int N, int K, int H, const uint16_t *y, int64_t y_r
   free(acc);
   return status;
 }
+
+/* ------------------------------------------------------------------ */
+/* MXFP8 block quantisation [EP, the later FP8 commits: E4M3 payloads */
+/* with UE8M0 scale bytes per 32 elements, tiny non-zero blocks kept  */
+/* at UE8M0 code zero].  Written from the microscaling definition:    */
+/* per block of 32 channels, amax = max |x|, the shared scale is      */
+/* X = 2^(floor(log2(amax)) - 8) (8 = exponent of E4M3's largest      */
+/* normal), stored as the byte code = log2(X) + 127; codes below 0    */
+/* are clamped to 0 (X = 2^-127) so a tiny non-zero block is still    */
+/* encoded, and an all-zero block gets code 0.  Elements are          */
+/* e4m3(x / X) with the narrowing above (saturating at +-448).        */
+/*   x bf16 [T][H] (H % 32 == 0), q e4m3 [T][H], codes uint8 [T][H/32] */
+/* ------------------------------------------------------------------ */
+static int floor_log2_f32(float a) { /* a > 0, finite */
+  uint32_t u;
+  memcpy(&u, &a, sizeof u);
+  int e = (int)((u >> 23) & 0xffu);
+  if (e != 0) return e - 127;
+  uint32_t m = u & 0x7fffffu; /* subnormal: m * 2^-149 */
+  int p = 31;
+  while (!((m >> p) & 1u)) --p;
+  return p - 149;
+}
+
+int oracle_quantize_mxfp8(int64_t T, int H, const uint16_t *x, uint8_t *q, uint8_t *codes) {
+  if (T < 0 || H <= 0 || H % 32 != 0) return ORC_BAD_ARG;
+  const int nb = H / 32;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t *xb = x + t * H + (int64_t)b * 32;
+      float amax = 0.0f;
+      for (int h = 0; h < 32; ++h) {
+        float v = fabsf(oracle_bf16_to_f32(xb[h]));
+        if (v > amax) amax = v;
+      }
+      int code = 0;
+      if (amax > 0.0f) {
+        code = floor_log2_f32(amax) - 8 + 127;
+        if (code < 0) code = 0;
+        if (code > 254) code = 254;
+      }
+      codes[t * nb + b] = (uint8_t)code;
+      const float X = ldexpf(1.0f, code - 127);
+      for (int h = 0; h < 32; ++h)
+        q[t * H + (int64_t)b * 32 + h] = oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / X);
+    }
+  }
+  return 0;
+}

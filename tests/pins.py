@@ -483,7 +483,42 @@ def pin_block_quantisation(orc) -> None:
     assert np.all((deq == 0) | (np.sign(deq) == np.sign(xf)))
 
 
+def pin_mxfp8_quantisation(orc) -> None:
+    """Scale codes against numpy's frexp (an independent exponent extraction); the
+    block maximum lands in the top binade of e4m3; decoded values within half an e4m3
+    step of x; all-zero blocks code 0; tiny non-zero blocks kept at code 0."""
+    rng = np.random.default_rng(47)
+    x = (rng.standard_normal((30, 256)) * np.exp2(rng.integers(-20, 20, (30, 8)).repeat(32, 1)))
+    x = x.astype(np.float32)
+    x[2, :32] = 0.0                                   # all-zero block
+    x[3, 32:64] = np.float32(2.0**-130) * rng.integers(1, 8, 32)  # tiny non-zero block
+    xb = _bits(x)
+    xf = _f32(xb).astype(np.float64)
+    q, codes, st = orc.quantize_mxfp8(xb)
+    assert st == 0 and codes.shape == (30, 8)
+    amax = np.abs(xf.reshape(30, 8, 32)).max(-1)
+    mant, ex = np.frexp(amax)                         # amax = mant * 2^ex, mant in [0.5, 1)
+    want = np.where(amax > 0, np.clip(ex - 1 - 8 + 127, 0, 254), 0)
+    assert np.array_equal(codes.astype(np.int64), want)
+    assert codes[2, 0] == 0 and not q[2, :32].any()
+    assert codes[3, 1] == 0 and q[3, 32:64].any()
+    deq = torch.from_numpy(q.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    X = np.exp2(codes.astype(np.float64) - 127)
+    deq = (deq.reshape(30, 8, 32) * X[..., None]).reshape(30, 256)
+    tol = np.maximum(np.abs(xf) * 2.0**-4, np.repeat(X, 32, axis=1) * 2.0**-10) * 1.0001
+    normal = codes.repeat(32, 1) > 0
+    Xe = np.repeat(X, 32, axis=1)
+    sat = np.abs(xf) >= 448 * Xe   # x / X above E4M3's largest finite value: clamped
+    assert np.all(np.abs(deq - xf)[normal & ~sat] <= tol[normal & ~sat])
+    assert np.all(np.abs(deq)[sat] == (448 * Xe)[sat])
+    qb = q.reshape(30, 8, 32)
+    for t, b in zip(*np.nonzero((amax > 0) & (codes > 0))):
+        j = int(np.abs(xf.reshape(30, 8, 32)[t, b]).argmax())
+        mag = torch.tensor([int(qb[t, b, j]) & 0x7f], dtype=torch.uint8).view(torch.float8_e4m3fn).float().item()
+        assert 256.0 <= mag <= 448.0
+
+
 ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
             pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
-            pin_low_latency_layout]
+            pin_low_latency_layout, pin_mxfp8_quantisation]

@@ -64,6 +64,8 @@ MUTANTS = {
                       "const float p = oracle_bf16_to_f32(y[(int64_t)r * H + h]);"),
     "ll_keeps_masked": ("if (topk_idx[tok * K + k] != e) continue;",
                         "if (topk_idx[tok * K + k] != e && !(e == 0 && topk_idx[tok * K + k] == -1)) continue;"),
+    "mxfp8_emax_7": ("code = floor_log2_f32(amax) - 8 + 127;", "code = floor_log2_f32(amax) - 7 + 127;"),
+    "mxfp8_flush_tiny": ("        if (code < 0) code = 0;\n", "        if (code < 0) code = 0, amax = 0.0f;\n        if (amax == 0.0f) { for (int h = 0; h < 32; ++h) q[t * H + (int64_t)b * 32 + h] = 0; codes[t * nb + b] = 0; continue; }\n"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
 }

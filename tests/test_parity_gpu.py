@@ -153,6 +153,7 @@ FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
     (16, 130, 32, 3, 96),
     (32, 40, 64, 8, 16),
     (7, 777, 28, 28, 24),   # K = E: every token to every rank
+    (2, 9000, 8, 3, 16),    # more than 8192 tokens per rank: multi-block layout
 ]
 
 
