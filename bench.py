@@ -303,7 +303,14 @@ def measure_other_rows(steps: int, peak: float):
     out["dispatch_rows_quantise_e4m3"] = dict(
         row(ms_q, R * N * H * 2 + T * (H + H // 128 * 4) + R * N * R * 4),
         workload="dsv3 rows quantised in-kernel: bf16 in, e4m3 + fp32 scale per 128 channels out")
-    del plan, rq, rs
+    rc = torch.empty((plan.cap, H // 32), dtype=torch.uint8, device="cuda")
+    ms_mx = timed(lambda: B.check(B.mp_dispatch_rows_mxfp8(R, N, H, plan.x, plan.send_row,
+                                                           plan.cap, rq, rc)), steps)
+    out["dispatch_rows_quantise_mxfp8"] = dict(
+        row(ms_mx, R * N * H * 2 + T * (H + H // 32) + R * N * R * 4),
+        workload="dsv3 rows quantised in-kernel: bf16 in, MXFP8 (e4m3 + UE8M0 byte per 32 "
+                 "channels) out")
+    del plan, rq, rs, rc
     torch.cuda.empty_cache()
 
     cfg = wl.CONFIGS["fp8"]

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
                                           P, P, P, P, P, P, P, P, P, P, P]
         L.mp_dispatch_rows.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P]
         L.mp_dispatch_rows_e4m3.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
+        L.mp_dispatch_rows_mxfp8.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
         L.mp_dispatch_offsets_global.argtypes = [i32, i32, i32, i32, P, P, P, P, P, i64,
                                                  ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P]
         L.mp_combine_weights.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
@@ -70,7 +71,8 @@ def lib() -> ctypes.CDLL:
         L.mp_reducescatterv.argtypes = [i32, i32, P, P, P, P]
         L.mp_allgatherv.argtypes = [i32, i64, P, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
-                  "mp_dispatch_rows_e4m3", "mp_dispatch_offsets_global", "mp_combine_weights",
+                  "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
+                  "mp_combine_weights",
                   "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv"):
             getattr(L, f).restype = ctypes.c_int
@@ -194,6 +196,13 @@ def mp_dispatch_rows_e4m3(R, N, H, x, send_row, recv_capacity, recv_x, recv_scal
     return lib().mp_dispatch_rows_e4m3(R, N, H, _dev(x, "x"), _dev(send_row, "send_row"),
                                        int(recv_capacity), _dev(recv_x, "recv_x"),
                                        _dev(recv_scales, "recv_scales"), _stream(stream))
+
+
+def mp_dispatch_rows_mxfp8(R, N, H, x, send_row, recv_capacity, recv_x, recv_scales,
+                           stream=None) -> int:
+    return lib().mp_dispatch_rows_mxfp8(R, N, H, _dev(x, "x"), _dev(send_row, "send_row"),
+                                        int(recv_capacity), _dev(recv_x, "recv_x"),
+                                        _dev(recv_scales, "recv_scales"), _stream(stream))
 
 
 def mp_combine(R, N, H, y, y_rows, send_row, out, dev_err, stream=None) -> int:

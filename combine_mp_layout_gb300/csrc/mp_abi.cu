@@ -222,7 +222,21 @@ int mp_dispatch_rows_e4m3(int R, int N, int H, const void* x, const int32_t* sen
   if (recv_capacity > 0 && (!recv_x || !recv_scales)) return MP_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(recv_x) || !aligned4(recv_scales) || !aligned4(send_row))
     return MP_ERR_INVALID_ARG;
-  return cuda_status(launch_dispatch_quant(R, int64_t(R) * N, H, x, recv_x, recv_scales,
+  return cuda_status(launch_dispatch_quant(R, int64_t(R) * N, H, x, recv_x, recv_scales, 0,
+                                           recv_capacity, send_row,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_rows_mxfp8(int R, int N, int H, const void* x, const int32_t* send_row,
+                           int64_t recv_capacity, void* recv_x, uint8_t* recv_scales,
+                           mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || H % 32 != 0 || recv_capacity < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !send_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && (!recv_x || !recv_scales)) return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned4(send_row)) return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch_quant(R, int64_t(R) * N, H, x, recv_x, recv_scales, 1,
                                            recv_capacity, send_row,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }

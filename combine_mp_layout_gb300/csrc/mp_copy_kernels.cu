@@ -278,14 +278,27 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   return r;
 }
 
-template <int U>
+// MXFP8 (MX = true; the same page's later commits: E4M3 with one UE8M0 scale
+// byte per 32 channels, tiny non-zero blocks kept at code zero): 4 lanes make
+// a block; code = clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an
+// all-zero block), X = 2^(code - 127), element codes e4m3(x / X).
+__device__ __forceinline__ int floor_log2_pos(float a) {  // a > 0, finite
+  const uint32_t u = __float_as_uint(a);
+  const int e = int((u >> 23) & 0xffu);
+  if (e != 0) return e - 127;
+  return (31 - __clz(u & 0x7fffffu)) - 149;  // binary32 subnormal: m * 2^-149
+}
+
+template <int U, bool MX>
 __global__ void __launch_bounds__(kCopyThreads)
 mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
-                 unsigned char* __restrict__ recv_x, float* __restrict__ recv_scales,
+                 unsigned char* __restrict__ recv_x, void* __restrict__ recv_scales,
                  int64_t recv_capacity, const int32_t* __restrict__ send_row) {
+  constexpr int kBlock = MX ? 32 : 128;       // channels per scale
+  constexpr int kLanes = kBlock / 8;          // lanes per scale block
   const int lane = threadIdx.x & 31;
   const int64_t vpr = H / 8;  // 8-channel vectors per row
-  const int nb = H / 128;     // scale blocks per row
+  const int nb = H / kBlock;  // scales per row
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
   const int64_t units = tokens * slabs;
@@ -300,10 +313,11 @@ mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
     const int64_t i0 = slab * slab_vec + lane;
     uint2 q[U];
     float scale[U];
+    uint32_t code[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * kWarp;
-      const bool valid = i < vpr;  // whole 16-lane blocks are valid or not (H % 128 == 0)
+      const bool valid = i < vpr;  // whole scale blocks are valid or not (H % kBlock == 0)
       Words<4> v;
       float f[8];
       float amax = 0.0f;
@@ -318,8 +332,17 @@ mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
         for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      for (int o = kLanes / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      float sc;
+      if (MX) {
+        int c = 0;
+        if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - 8 + 127));
+        code[u] = uint32_t(c);
+        sc = c > 0 ? __uint_as_float(uint32_t(c) << 23) : __uint_as_float(0x00400000u);
+      } else {
+        sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        code[u] = 0;
+      }
       scale[u] = sc;
       if (valid) {
         uint32_t b[4];
@@ -341,7 +364,12 @@ mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
           asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(q[u].x),
                        "r"(q[u].y)
                        : "memory");
-          if ((lane & 15) == 0) recv_scales[row * nb + i / 16] = scale[u];
+          if ((lane & (kLanes - 1)) == 0) {
+            if (MX)
+              static_cast<unsigned char*>(recv_scales)[row * nb + i / kLanes] = uint8_t(code[u]);
+            else
+              static_cast<float*>(recv_scales)[row * nb + i / kLanes] = scale[u];
+          }
         }
       }
     }
@@ -641,17 +669,25 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
 }
 
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
-                                  float* recv_scales, int64_t recv_capacity,
+                                  void* recv_scales, int mx, int64_t recv_capacity,
                                   const int32_t* send_row, cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
   constexpr int U = 4;
-  static const int per_sm = resident_blocks(mp_k_dispatch_q8<U>);
   const int64_t vpr = H / 8;
   const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  if (mx) {
+    static const int per_sm = resident_blocks(mp_k_dispatch_q8<U, true>);
+    const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+    return launch_kernel(mp_k_dispatch_q8<U, true>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
+                         tokens, H, static_cast<const Words<4>*>(x),
+                         static_cast<unsigned char*>(recv_x), recv_scales, recv_capacity,
+                         send_row);
+  }
+  static const int per_sm = resident_blocks(mp_k_dispatch_q8<U, false>);
   const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
-  return launch_kernel(mp_k_dispatch_q8<U>, dim3(grid), dim3(kCopyThreads), 0, stream, R, tokens, H,
-                       static_cast<const Words<4>*>(x), static_cast<unsigned char*>(recv_x),
-                       recv_scales, recv_capacity, send_row);
+  return launch_kernel(mp_k_dispatch_q8<U, false>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
+                       tokens, H, static_cast<const Words<4>*>(x),
+                       static_cast<unsigned char*>(recv_x), recv_scales, recv_capacity, send_row);
 }
 
 template <int NW, int U, int RB, bool W>

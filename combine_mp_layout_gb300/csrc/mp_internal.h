@@ -48,10 +48,11 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                  int scales_per_row,
                                  const float* x_scales, float* recv_scales, cudaStream_t stream);
 
-// Quantises bf16 token rows to e4m3 with one fp32 scale per 128 channels and
-// copies them to every receive row listed in send_row.
+// Quantises bf16 token rows to e4m3 -- one fp32 scale per 128 channels (mx = 0)
+// or one UE8M0 byte per 32 channels (mx = 1) -- and copies them to every
+// receive row listed in send_row.
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
-                                  float* recv_scales, int64_t recv_capacity,
+                                  void* recv_scales, int mx, int64_t recv_capacity,
                                   const int32_t* send_row, cudaStream_t stream);
 
 cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,

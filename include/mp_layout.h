@@ -239,6 +239,24 @@ int mp_dispatch_rows_e4m3(int R, int N, int H, const void *x, const int32_t *sen
                           mp_stream_t stream);
 
 /*
+ * mp_dispatch_rows_mxfp8 -- the row copy with in-kernel MXFP8 quantisation
+ * ([EP] the later FP8 commits: E4M3 payloads with UE8M0 scale bytes per 32
+ * elements, tiny non-zero blocks kept at UE8M0 code zero; read with the
+ * microscaling definition): per block of 32 channels, amax = max |x|,
+ * code = clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an all-zero
+ * block), X = 2^(code - 127), element codes e4m3(x / X) with round-to-
+ * nearest-even, saturating at +-448 (values of x / X in (448, 512) clamp).
+ *   in   x           bf16 [R][N][H], H % 32 == 0
+ *   out  recv_x      e4m3 [recv_capacity][H]
+ *   out  recv_scales uint8 [recv_capacity][H/32]: the UE8M0 codes
+ * Dequantised x is element * 2^(code - 127).  Checks as mp_dispatch_rows_e4m3
+ * with H % 32 == 0.  No device errors.
+ */
+int mp_dispatch_rows_mxfp8(int R, int N, int H, const void *x, const int32_t *send_row,
+                           int64_t recv_capacity, void *recv_x, uint8_t *recv_scales,
+                           mp_stream_t stream);
+
+/*
  * mp_combine -- [EP] intranode_combine, the reverse of dispatch.
  *   in   y        bf16 [y_rows][H]: one row per receive row (for example the
  *                 expert outputs, or recv_x itself)

@@ -142,3 +142,38 @@ def test_binding_refuses_cpu_tensors(L):
     t = torch.zeros(16, dtype=torch.int32)
     with pytest.raises(TypeError):
         B.mp_combine(2, 4, 64, t, 1, t, t, t)
+
+
+@no_gpu
+def test_newer_entry_points_reject(L):
+    """Host checks of the NEXT-row entry points (every argument set below is invalid)."""
+    P, N0 = _p(), _p(0)
+    L.mp_dispatch_rows_e4m3.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int64] + [ctypes.c_void_p] * 3
+    assert L.mp_dispatch_rows_e4m3(2, 8, 100, P, P, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # H % 128
+    assert L.mp_dispatch_rows_e4m3(2, 8, 128, _p(FAKE + 8), P, 16, P, P, N0) == B.MP_ERR_INVALID_ARG
+    L.mp_dispatch_rows_mxfp8.argtypes = L.mp_dispatch_rows_e4m3.argtypes
+    assert L.mp_dispatch_rows_mxfp8(2, 8, 48, P, P, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # H % 32
+    assert L.mp_dispatch_rows_mxfp8(2, 8, 64, P, P, 16, P, N0, N0) == B.MP_ERR_INVALID_ARG  # scales
+    L.mp_combine_weights.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int64] + \
+        [ctypes.c_void_p] * 4
+    assert L.mp_combine_weights(2, 8, 0, P, 4, P, P, P, N0) == B.MP_ERR_INVALID_ARG      # K < 1
+    assert L.mp_combine_weights(2, 8, 2, P, 4, P, P, N0, N0) == B.MP_ERR_INVALID_ARG     # dev_err
+    L.mp_dispatch_ll_offsets.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int64] + [ctypes.c_void_p] * 6
+    assert L.mp_dispatch_ll_offsets(2, 8, 2, 7, P, P, 16, P, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG
+    assert L.mp_dispatch_ll_offsets(2, 60000, 8, 8, P, P, 16, P, P, P, P, P, N0) == \
+        B.MP_ERR_INVALID_ARG  # the rank's top-k slab does not fit in shared memory
+    L.mp_combine_ll.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_int64] + \
+        [ctypes.c_void_p] * 5
+    assert L.mp_combine_ll(2, 8, 2, 60, P, 4, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG   # H % 8
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    sizes = (ctypes.c_int64 * 2)(3, 4)
+    rb = (ctypes.c_int64 * 2)(64, 40)
+    L.mp_allgatherv_multi.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
+    assert L.mp_allgatherv_multi(2, 2, rb, sizes, arr, arr, N0) == B.MP_ERR_INVALID_ARG   # 40 % 16
+    assert L.mp_allgatherv_multi(2, 9, rb, sizes, arr, arr, N0) == B.MP_ERR_INVALID_ARG   # > 8 tensors
+    L.mp_dispatch_noalloc.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + \
+        [ctypes.c_void_p] * 12
+    assert L.mp_dispatch_noalloc(32, 100000, 8, 256, 64, B.MP_BF16, *([P] * 7), 16,
+                                 *([P] * 11), N0) == B.MP_ERR_INVALID_ARG                # > 1 MiB scratch

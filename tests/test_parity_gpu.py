@@ -270,6 +270,37 @@ def test_dispatch_rows_e4m3_quantises_like_the_oracle(shape):
     assert np.array_equal(rs[:n].cpu().numpy().view(np.uint32), out["recv_scales"].view(np.uint32))
 
 
+@pytest.mark.parametrize("shape", [(4, 300, 16, 4, 96), (8, 4096, 256, 8, 7168)],
+                         ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
+def test_dispatch_rows_mxfp8_quantises_like_the_oracle(shape):
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=H + 1)
+    x = inp.x.float()
+    x[0, 0, :32] = 0.0                          # all-zero block: code 0
+    x[0, 1, 32:64] = 2.0**-130                  # tiny non-zero block: code 0, kept
+    x[R - 1, 2, :] *= 300.0                     # large values: saturation above 448 * X
+    x[1, 3, :32] *= torch.exp2(torch.arange(32, dtype=torch.float32) - 16)  # wide range
+    inp.x = x.to(torch.bfloat16)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    rq = torch.zeros((plan.cap, H), dtype=torch.uint8, device="cuda")
+    rc = torch.zeros((plan.cap, H // 32), dtype=torch.uint8, device="cuda")
+    B.check(B.mp_dispatch_rows_mxfp8(R, N, H, plan.x, plan.send_row, plan.cap, rq, rc))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    q, codes, st = oracle.quantize_mxfp8(wl.bf16_bits(inp.x))
+    assert st == 0
+    payload = np.concatenate([q, codes], axis=-1)  # dispatch codes and elements as one byte row
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    out, st2 = oracle.dispatch(payload, inp.topk_idx, inp.topk_weights, mask, E)
+    assert st2 == 0
+    n = out["num_recv"]
+    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"][:, :H])
+    assert np.array_equal(rc[:n].cpu().numpy(), out["recv_x"][:, H:])
+
+
 def test_empty_tokens():
     inp = wl.make_ep(dict(R=4, N=0, E=16, K=2, H=64, routing="uniform", dtype="bf16"))
     plan = run_gpu(inp)
