@@ -69,19 +69,31 @@ def replica_throughput(units_per_rank: int, steps: int, world: int, ms_max: floa
     return units_per_rank * world * steps / (ms_max / 1e3)
 
 
+def _source_digest(slices) -> str:
+    """sha256 over the given pieces of source: whole files, or the text of a file
+    from a `begin` marker up to (not including) an `end` marker."""
+    import hashlib
+    h = hashlib.sha256()
+    for sl in slices:
+        with open(os.path.join(ROOT, sl["file"]), "rb") as f:
+            text = f.read()
+        if "begin" in sl:
+            b = text.index(sl["begin"].encode())
+            e = text.index(sl["end"].encode(), b)
+            text = text[b:e]
+        h.update(text)
+    return h.hexdigest()
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/traffic.json), or None when there is none or when the kernel's
-    source files have changed since the counters were taken."""
-    import hashlib
+    source (its own text, its launcher and the shared device helpers) has
+    changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel]
-        h = hashlib.sha256()
-        for p in rec["source_files"]:
-            with open(os.path.join(ROOT, p), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest() != rec["source_sha256"]:
+        if _source_digest(rec["source"]) != rec["source_sha256"]:
             return None
         return int(rec["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):

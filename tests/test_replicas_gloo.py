@@ -52,13 +52,15 @@ def test_recorded_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     src = tmp_path / "k.cu"
-    src.write_text("kernel v1")
-    import hashlib
-    rec = {"k": {"traffic_bytes_per_launch": 123, "source_files": ["k.cu"],
-                 "source_sha256": hashlib.sha256(b"kernel v1").hexdigest()}}
-    (prof / "traffic.json").write_text(json.dumps(rec))
+    src.write_text("head // K-BEGIN kernel v1 // K-END tail")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sl = [{"file": "k.cu", "begin": "// K-BEGIN", "end": "// K-END"}]
+    rec = {"k": {"traffic_bytes_per_launch": 123, "source": sl,
+                 "source_sha256": bench._source_digest(sl)}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
     assert bench.recorded_traffic("k") == 123
-    src.write_text("kernel v2")  # the kernel changed since the counters were taken
+    src.write_text("other head // K-BEGIN kernel v1 // K-END other tail")  # unrelated edit
+    assert bench.recorded_traffic("k") == 123
+    src.write_text("head // K-BEGIN kernel v2 // K-END tail")  # the kernel itself changed
     assert bench.recorded_traffic("k") is None
     assert bench.recorded_traffic("other") is None
