@@ -267,10 +267,12 @@ def config_block(name, inp):
 # the other rows of the path on their own workloads (device-timed)
 # ---------------------------------------------------------------------------
 def measure_other_rows(steps: int, peak: float):
-    """e4m3 dispatch (R=8, N=8192, H=7168, per-128-channel fp32 scales, top-8 of 256)
-    with its bf16 combine, and reduce-scatterv / all-gatherv (R=8, H=4096, per-rank
-    rows U{0..16384}).  Inputs are synthetic (drawn on the device: only the timing
-    is used here; parity on these workloads is in the tests)."""
+    """The rows besides the dsv3 step: in-kernel quantise-dispatch (e4m3 and MXFP8) of
+    the dsv3 rows; e4m3 dispatch (R=8, N=8192, H=7168, per-128-channel fp32 scales,
+    top-8 of 256) with its bf16 combine; reduce-scatterv / all-gatherv (R=8, H=4096,
+    per-rank rows U{0..16384}) and the all-gatherv with quantisation fused in; the
+    skewed step (R=16, Zipf routing).  Inputs are synthetic (mostly drawn on the
+    device: only the timing is used here; parity on these workloads is in the tests)."""
     import numpy as np
     import torch
 
@@ -361,7 +363,52 @@ def measure_other_rows(steps: int, peak: float):
     out["reducescatterv"] = dict(row(ms_rs, Rr * S * Hh * 2 + S * Hh * 2),
                                  workload="rsv: R=8, H=4096 bf16, rows per rank U{0..16384}, S=%d" % S)
     out["allgatherv"] = row(ms_ag, S * Hh * 2 + Rr * S * Hh * 2)
-    del rp
+    # all-gatherv with the quantisation fused in: rows quantised once, codes and
+    # scales written to every rank's copy
+    qx = torch.empty((Rr, S, Hh), dtype=torch.uint8, device="cuda")
+    qs = torch.empty((Rr, S, Hh // 128), dtype=torch.float32, device="cuda")
+    ms_agq = timed(lambda: B.check(B.mp_allgatherv_e4m3(Rr, Hh, sizes, rp.shards, qx, qs)),
+                   max(5, steps // 4))
+    out["allgatherv_quantise_e4m3"] = dict(
+        row(ms_agq, S * Hh * 2 + Rr * S * (Hh + Hh // 128 * 4)),
+        workload="rsv shards quantised once (fp32 scale per 128 channels), gathered to 8 ranks")
+    del qs
+    qc = torch.empty((Rr, S, Hh // 32), dtype=torch.uint8, device="cuda")
+    ms_agm = timed(lambda: B.check(B.mp_allgatherv_mxfp8(Rr, Hh, sizes, rp.shards, qx, qc)),
+                   max(5, steps // 4))
+    out["allgatherv_quantise_mxfp8"] = dict(
+        row(ms_agm, S * Hh * 2 + Rr * S * (Hh + Hh // 32)),
+        workload="rsv shards quantised once (MXFP8, UE8M0 byte per 32 channels), gathered "
+                 "to 8 ranks")
+    del rp, qx, qc
+    torch.cuda.empty_cache()
+
+    # the skewed workload: Zipf(1.2) routing, rank 0 hot
+    inp = wl.make_ep("skew", seed=0)
+    R, N, H, E, K = inp.R, inp.N, inp.H, inp.E, inp.K
+    plan = EPPlan(R, N, K, E, H, "bf16")
+    plan.load(inp)
+    del inp
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    torch.cuda.synchronize()
+    T = plan.num_recv()
+    y = torch.randn((T, H), generator=g, device="cuda").to(torch.bfloat16)
+
+    def skew_step():
+        B.check(plan.layout())
+        B.check(plan.dispatch())
+        B.check(plan.combine(y))
+
+    ms_sk = timed(skew_step, steps)
+    assert plan.device_error() == 0
+    ab = algorithmic_bytes(R, N, K, E, H, T)
+    nbytes = ab["layout"] + ab["dispatch"] + ab["combine"]
+    out["skew_step"] = dict(row(ms_sk, nbytes), tokens_per_s=R * N / (ms_sk / 1e3),
+                            receive_rows=T,
+                            workload="skew: R=16, N=2048, H=4096 bf16, E=64, top-6 Zipf(1.2); "
+                                     "layout + dispatch + combine")
+    del plan, y
     torch.cuda.empty_cache()
     return out
 

@@ -70,11 +70,14 @@ def lib() -> ctypes.CDLL:
         L.mp_combine.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
         L.mp_reducescatterv.argtypes = [i32, i32, P, P, P, P]
         L.mp_allgatherv.argtypes = [i32, i64, P, P, P, P]
+        L.mp_allgatherv_e4m3.argtypes = [i32, i32, P, P, P, P, P]
+        L.mp_allgatherv_mxfp8.argtypes = [i32, i32, P, P, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
                   "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
-                  "mp_combine", "mp_reducescatterv", "mp_allgatherv"):
+                  "mp_combine", "mp_reducescatterv", "mp_allgatherv",
+                  "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -223,6 +226,16 @@ def mp_reducescatterv(R, H, sizes, inp, out, stream=None) -> int:
 def mp_allgatherv(R, row_bytes, sizes, inp, out, stream=None) -> int:
     return lib().mp_allgatherv(R, int(row_bytes), _host_sizes(sizes), _dev(inp, "in"),
                                _dev(out, "out"), _stream(stream))
+
+
+def mp_allgatherv_e4m3(R, H, sizes, inp, out, out_scales, stream=None) -> int:
+    return lib().mp_allgatherv_e4m3(R, H, _host_sizes(sizes), _dev(inp, "in"), _dev(out, "out"),
+                                    _dev(out_scales, "out_scales"), _stream(stream))
+
+
+def mp_allgatherv_mxfp8(R, H, sizes, inp, out, out_scales, stream=None) -> int:
+    return lib().mp_allgatherv_mxfp8(R, H, _host_sizes(sizes), _dev(inp, "in"), _dev(out, "out"),
+                                     _dev(out_scales, "out_scales"), _stream(stream))
 
 
 def mp_dispatch_noalloc(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weights,

@@ -308,6 +308,31 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t* sizes, const void* in
       launch_allgatherv(R, S, row_bytes, in, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int allgatherv_quant(int R, int H, int block, const int64_t* sizes, const void* in,
+                            void* out, void* out_scales, int mx, mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || H <= 0 || H % block != 0 || !sizes) return MP_ERR_INVALID_ARG;
+  int64_t S = 0;
+  for (int r = 0; r < R; ++r) {
+    if (sizes[r] < 0) return MP_ERR_INVALID_ARG;
+    S += sizes[r];
+  }
+  if (S > 0 && (!in || !out || !out_scales || !aligned16(in) || !aligned16(out) ||
+                (!mx && !aligned4(out_scales))))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_allgatherv_quant(R, S, H, in, out, out_scales, mx,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_allgatherv_e4m3(int R, int H, const int64_t* sizes, const void* in, void* out,
+                       float* out_scales, mp_stream_t stream) {
+  return allgatherv_quant(R, H, MP_SCALE_BLOCK, sizes, in, out, out_scales, 0, stream);
+}
+
+int mp_allgatherv_mxfp8(int R, int H, const int64_t* sizes, const void* in, void* out,
+                        uint8_t* out_scales, mp_stream_t stream) {
+  return allgatherv_quant(R, H, 32, sizes, in, out, out_scales, 1, stream);
+}
+
 int mp_allgatherv_multi(int R, int ntensors, const int64_t* row_bytes, const int64_t* sizes,
                         const void* const* in, void* const* out, mp_stream_t stream) {
   if (R < 1 || ntensors < 1 || ntensors > MP_MAX_TENSORS || !row_bytes || !sizes || !in || !out)

@@ -264,13 +264,30 @@ mp_k_dispatch_tma(int R, int64_t tokens, int64_t row_bytes, uint32_t piece_bytes
 }
 
 // ---------------------------------------------------------------------------
-// Dispatch with in-kernel FP8 quantisation (same page: E4M3 payloads with
-// FP32 scales).  Each 128-channel block of a bf16 token row gets
-// scale = amax / 448 (1 when the block is all zero) and codes
-// e4m3_rn_satfinite(x / scale); the e4m3 row and its scales are written to
-// every destination row.  Reading x once as bf16 and writing 1 byte per
-// channel per destination roughly halves the traffic of a bf16 dispatch.
-// A lane holds 8 channels (one 16-byte load); 16 lanes make a block.
+// Row copies with in-kernel FP8 quantisation.
+//
+// [EP] (the FP8 commits of "MSCCLPP EP implementation"): E4M3 payloads with
+// FP32 scales.  Each 128-channel block of a bf16 row gets scale = amax / 448
+// (1 when the block is all zero) and codes e4m3_rn_satfinite(x / scale).
+// MXFP8 (MX = true; the same page's later commits: E4M3 with one UE8M0 scale
+// byte per 32 channels, tiny non-zero blocks kept at code zero): code =
+// clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an all-zero block),
+// X = 2^(code - 127), element codes e4m3(x / X).  Dividing by a power of two
+// and multiplying by its (exactly representable) reciprocal round the same
+// real number once, so MX multiplies by 2^(127 - code).
+//
+// Destinations.  Dispatch (GATHER = false): token `tok`'s destinations are
+// send_row[tok][d] for d < R, skipped when negative or >= `limit` (the receive
+// capacity).  Gather (GATHER = true; [AGV] "Add pynccl all-gatherv and
+// reducescatterv", the note that gathering a list of tensors lets a caller
+// quantise before the all-gather): `limit` = S and logical rank q receives
+// row tok at q * S + tok, so one launch quantises each row once and writes
+// codes and scales R times.
+//
+// A lane holds CPL channels (CPL = 8: one 16-byte load; 16: one 32-byte load)
+// and stores CPL code bytes per destination; kBlock / CPL lanes share a scale.
+// Each row is read once as bf16 and written as 1 byte per channel per
+// destination, roughly half the traffic of a bf16 copy.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;
@@ -278,10 +295,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   return r;
 }
 
-// MXFP8 (MX = true; the same page's later commits: E4M3 with one UE8M0 scale
-// byte per 32 channels, tiny non-zero blocks kept at code zero): 4 lanes make
-// a block; code = clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an
-// all-zero block), X = 2^(code - 127), element codes e4m3(x / X).
 __device__ __forceinline__ int floor_log2_pos(float a) {  // a > 0, finite
   const uint32_t u = __float_as_uint(a);
   const int e = int((u >> 23) & 0xffu);
@@ -289,86 +302,116 @@ __device__ __forceinline__ int floor_log2_pos(float a) {  // a > 0, finite
   return (31 - __clz(u & 0x7fffffu)) - 149;  // binary32 subnormal: m * 2^-149
 }
 
-template <int U, bool MX>
+template <int NB>
+__device__ __forceinline__ void st_codes(unsigned char* p, const uint32_t (&w)[NB]) {
+  if constexpr (NB == 4) {
+    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+  } else {
+    static_assert(NB == 2, "8 or 16 code bytes per lane");
+    asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+                 : "memory");
+  }
+}
+
+template <int CPL, int U, bool MX, bool GATHER>
 __global__ void __launch_bounds__(kCopyThreads)
-mp_k_dispatch_q8(int R, int64_t tokens, int H, const Words<4>* __restrict__ x,
-                 unsigned char* __restrict__ recv_x, void* __restrict__ recv_scales,
-                 int64_t recv_capacity, const int32_t* __restrict__ send_row) {
-  constexpr int kBlock = MX ? 32 : 128;       // channels per scale
-  constexpr int kLanes = kBlock / 8;          // lanes per scale block
+mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
+                unsigned char* __restrict__ out, void* __restrict__ out_scales, int64_t limit,
+                const int32_t* __restrict__ send_row) {
+  constexpr int kBlock = MX ? 32 : 128;  // channels per scale
+  constexpr int kLanes = kBlock / CPL;   // lanes per scale block
+  constexpr int NW = CPL / 2;            // 32-bit words of bf16 per lane
+  constexpr int NB = CPL / 4;            // 32-bit words of codes per lane
+  static_assert(kLanes >= 1 && kLanes <= 32, "scale block spans whole lanes");
   const int lane = threadIdx.x & 31;
-  const int64_t vpr = H / 8;  // 8-channel vectors per row
-  const int nb = H / kBlock;  // scales per row
+  const int64_t vpr = H / CPL;  // lane vectors per row
+  const int nb = H / kBlock;    // scales per row
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
   const int64_t units = tokens * slabs;
   const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  const Words<NW>* xv = reinterpret_cast<const Words<NW>*>(x);
   for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
        unit += nw) {
     const int64_t tok = unit / slabs;
     const int64_t slab = unit - tok * slabs;
-    const int my = lane < R ? __ldg(send_row + tok * R + lane) : -1;
-    unsigned vm = __ballot_sync(kFull, my >= 0 && int64_t(my) < recv_capacity);
-    if (vm == 0) continue;
+    int64_t my;
+    unsigned vm;
+    if constexpr (GATHER) {
+      my = int64_t(lane) * limit + tok;
+      vm = R >= 32 ? kFull : ((1u << R) - 1u);
+    } else {
+      const int r = lane < R ? __ldg(send_row + tok * R + lane) : -1;
+      my = r;
+      vm = __ballot_sync(kFull, r >= 0 && int64_t(r) < limit);
+      if (vm == 0) continue;
+    }
     const int64_t i0 = slab * slab_vec + lane;
-    uint2 q[U];
-    float scale[U];
-    uint32_t code[U];
+    uint32_t q[U][NB];
+    uint32_t sbits[U];  // fp32 scale bits, or the UE8M0 code
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * kWarp;
       const bool valid = i < vpr;  // whole scale blocks are valid or not (H % kBlock == 0)
-      Words<4> v;
-      float f[8];
+      float f[CPL];
       float amax = 0.0f;
       if (valid) {
-        v = ld_stream_w<4>(x + tok * vpr + i);
+        const Words<NW> v = ld_stream_w<NW>(xv + tok * vpr + i);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NW; ++j) {
           f[2 * j] = __uint_as_float(v.w[j] << 16);
           f[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        for (int j = 0; j < CPL; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
 #pragma unroll
       for (int o = kLanes / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      float sc;
-      if (MX) {
+      if constexpr (MX) {
         int c = 0;
         if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - 8 + 127));
-        code[u] = uint32_t(c);
-        sc = c > 0 ? __uint_as_float(uint32_t(c) << 23) : __uint_as_float(0x00400000u);
-      } else {
-        sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        code[u] = 0;
-      }
-      scale[u] = sc;
-      if (valid) {
-        uint32_t b[4];
+        sbits[u] = uint32_t(c);
+        // 2^(127 - c): biased exponent 254 - c, or the subnormal 2^-127 at c = 254
+        const float inv = c < 254 ? __uint_as_float(uint32_t(254 - c) << 23)
+                                  : __uint_as_float(0x00400000u);
+        if (valid) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          b[j] = cvt_e4m3x2(__fdiv_rn(f[2 * j + 1], sc), __fdiv_rn(f[2 * j], sc));
-        q[u] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+          for (int j = 0; j < NB; ++j) {
+            const uint32_t lo = cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
+            const uint32_t hi =
+                cvt_e4m3x2(__fmul_rn(f[4 * j + 3], inv), __fmul_rn(f[4 * j + 2], inv));
+            q[u][j] = lo | (hi << 16);
+          }
+        }
+      } else {
+        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        sbits[u] = __float_as_uint(sc);
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(f[4 * j + 1], sc), __fdiv_rn(f[4 * j], sc));
+            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(f[4 * j + 3], sc), __fdiv_rn(f[4 * j + 2], sc));
+            q[u][j] = lo | (hi << 16);
+          }
+        }
       }
     }
     while (vm) {
       const int d = __ffs(vm) - 1;
       vm &= vm - 1;
-      const int64_t row = __shfl_sync(kFull, my, d);
+      const int64_t row = GATHER ? int64_t(d) * limit + tok : __shfl_sync(kFull, my, d);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t i = i0 + u * kWarp;
         if (i < vpr) {
-          unsigned char* dst = recv_x + row * H + i * 8;
-          asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(q[u].x),
-                       "r"(q[u].y)
-                       : "memory");
+          st_codes<NB>(out + row * H + i * CPL, q[u]);
           if ((lane & (kLanes - 1)) == 0) {
-            if (MX)
-              static_cast<unsigned char*>(recv_scales)[row * nb + i / kLanes] = uint8_t(code[u]);
+            if constexpr (MX)
+              static_cast<unsigned char*>(out_scales)[row * nb + i / kLanes] = uint8_t(sbits[u]);
             else
-              static_cast<float*>(recv_scales)[row * nb + i / kLanes] = scale[u];
+              static_cast<uint32_t*>(out_scales)[row * nb + i / kLanes] = sbits[u];
           }
         }
       }
@@ -668,26 +711,69 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                                 stream);
 }
 
+// Quantising copies.  Launch shapes measured on GB300 (dsv3 dispatch rows,
+// R=8, N=4096, H=7168; rsv all-gatherv, R=8, S=65,463, H=4096):
+//  - 16 channels per lane (32-byte loads, 16-byte code stores) beat 8 by
+//    10-15%; a source that is not 32-byte aligned takes the 8-channel form;
+//  - 2 vectors per lane and unit, except 1 for the e4m3 gather (276 vs
+//    285 us);
+//  - one short block per kWarpsPerBlock units (the write-heavy policy above)
+//    for MXFP8 dispatch (260 vs 296 us) and both gathers (276-285 vs 321 us),
+//    but a persistent grid for the e4m3 dispatch, whose fp32 division per
+//    element makes it the most compute-heavy (279 vs 296 us).
+// MP_QUANT_CPL = 8 and MP_QUANT_FULL_MASK (bit (GATHER ? 2 : 0) + (MX ? 1 : 0)
+// set = short blocks) reproduce the other shapes for measurement.
+#ifndef MP_QUANT_CPL
+#define MP_QUANT_CPL 16
+#endif
+#ifndef MP_QUANT_FULL_MASK
+#define MP_QUANT_FULL_MASK 14
+#endif
+
+template <int CPL, int U, bool MX, bool GATHER>
+static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void* out,
+                              void* out_scales, int64_t limit, const int32_t* send_row,
+                              cudaStream_t stream) {
+  auto kernel = mp_k_quant_rows<CPL, U, MX, GATHER>;
+  static const int per_sm = resident_blocks(kernel);
+  const int64_t vpr = H / CPL;
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  constexpr bool full = (MP_QUANT_FULL_MASK >> ((GATHER ? 2 : 0) + (MX ? 1 : 0))) & 1;
+  const unsigned grid = full ? grid_full(kWarpsPerBlock, tokens * slabs)
+                             : grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+  return launch_kernel(kernel, dim3(grid), dim3(kCopyThreads), 0, stream, R, tokens, H,
+                       static_cast<const uint16_t*>(x), static_cast<unsigned char*>(out),
+                       out_scales, limit, send_row);
+}
+
+template <bool MX, bool GATHER>
+static cudaError_t quant_rows_any(int R, int64_t tokens, int H, const void* x, void* out,
+                                  void* out_scales, int64_t limit, const int32_t* send_row,
+                                  cudaStream_t stream) {
+  if (tokens == 0) return cudaSuccess;
+  constexpr int U = (GATHER && !MX) ? 1 : 2;  // vectors per lane at 16 channels per lane
+  if constexpr (MP_QUANT_CPL == 16) {
+    if (aligned(x, 32))
+      return quant_rows<16, U, MX, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
+                                           stream);
+  }
+  return quant_rows<8, 2 * U, MX, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
+                                          stream);
+}
+
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
                                   void* recv_scales, int mx, int64_t recv_capacity,
                                   const int32_t* send_row, cudaStream_t stream) {
-  if (tokens == 0) return cudaSuccess;
-  constexpr int U = 4;
-  const int64_t vpr = H / 8;
-  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
-  if (mx) {
-    static const int per_sm = resident_blocks(mp_k_dispatch_q8<U, true>);
-    const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
-    return launch_kernel(mp_k_dispatch_q8<U, true>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
-                         tokens, H, static_cast<const Words<4>*>(x),
-                         static_cast<unsigned char*>(recv_x), recv_scales, recv_capacity,
-                         send_row);
-  }
-  static const int per_sm = resident_blocks(mp_k_dispatch_q8<U, false>);
-  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
-  return launch_kernel(mp_k_dispatch_q8<U, false>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
-                       tokens, H, static_cast<const Words<4>*>(x),
-                       static_cast<unsigned char*>(recv_x), recv_scales, recv_capacity, send_row);
+  return mx ? quant_rows_any<true, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
+                                          send_row, stream)
+            : quant_rows_any<false, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
+                                           send_row, stream);
+}
+
+cudaError_t launch_allgatherv_quant(int R, int64_t S, int H, const void* in, void* out,
+                                    void* out_scales, int mx, cudaStream_t stream) {
+  return mx ? quant_rows_any<true, true>(R, S, H, in, out, out_scales, S, nullptr, stream)
+            : quant_rows_any<false, true>(R, S, H, in, out, out_scales, S, nullptr, stream);
 }
 
 template <int NW, int U, int RB, bool W>

@@ -62,6 +62,11 @@ cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t 
 cudaError_t launch_reducescatterv(int R, int64_t S, int H, const void* in, void* out,
                                   cudaStream_t stream);
 
+// Quantises each of the S bf16 rows of `in` once (scales as in
+// launch_dispatch_quant) and writes codes and scales to all R logical ranks'
+// copies: out[q][i] and out_scales[q][i] for q < R.
+cudaError_t launch_allgatherv_quant(int R, int64_t S, int H, const void* in, void* out,
+                                    void* out_scales, int mx, cudaStream_t stream);
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream);
 

@@ -341,6 +341,30 @@ int mp_dispatch_noalloc(int R, int N, int K, int E, int H, int dtype, const void
                         int32_t *dev_err, mp_stream_t stream);
 
 /*
+ * mp_allgatherv_e4m3 / mp_allgatherv_mxfp8 -- [AGV] all-gatherv with the
+ * quantisation fused in (the page's note that gathering a list of tensors
+ * lets a caller quantise before the all-gather; here data and scales leave
+ * one launch together).  Each bf16 row of `in` is quantised once, exactly as
+ * mp_dispatch_rows_e4m3 (one fp32 scale per 128 channels) or
+ * mp_dispatch_rows_mxfp8 (one UE8M0 byte per 32 channels) quantise a token
+ * row, and every logical rank q receives all S rows in order:
+ *   sizes       HOST int64 [R], S = sum(sizes) (only S matters: every
+ *               rank's gathered copy is the shards in rank order)
+ *   in          bf16 [S][H]
+ *   out         e4m3 [R][S][H]
+ *   out_scales  fp32 [R][S][H/128] (e4m3) or uint8 [R][S][H/32] (mxfp8)
+ * The result equals quantising `in` and then calling mp_allgatherv on the
+ * codes and on the scales.
+ * Checks: 1 <= R <= MP_MAX_RANKS, H > 0 and a multiple of the scale block,
+ *   sizes >= 0, non-NULL in/out/out_scales when S > 0, in and out 16-byte
+ *   aligned, fp32 scales 4-byte aligned.  No device errors.
+ */
+int mp_allgatherv_e4m3(int R, int H, const int64_t *sizes, const void *in, void *out,
+                       float *out_scales, mp_stream_t stream);
+int mp_allgatherv_mxfp8(int R, int H, const int64_t *sizes, const void *in, void *out,
+                        uint8_t *out_scales, mp_stream_t stream);
+
+/*
  * mp_allgatherv_multi -- [AGV] all-gatherv of a list of tensors in one launch
  * (the page's motivation: gathering quantised data and its scales together).
  * Tensor j has row_bytes[j] bytes per row (a multiple of 16) and the same

@@ -23,7 +23,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mp_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mp_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_five_calls():
@@ -173,6 +173,15 @@ def test_newer_entry_points_reject(L):
     L.mp_allgatherv_multi.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
     assert L.mp_allgatherv_multi(2, 2, rb, sizes, arr, arr, N0) == B.MP_ERR_INVALID_ARG   # 40 % 16
     assert L.mp_allgatherv_multi(2, 9, rb, sizes, arr, arr, N0) == B.MP_ERR_INVALID_ARG   # > 8 tensors
+    L.mp_allgatherv_e4m3.argtypes = [ctypes.c_int] * 2 + [ctypes.c_void_p] * 5
+    L.mp_allgatherv_mxfp8.argtypes = L.mp_allgatherv_e4m3.argtypes
+    assert L.mp_allgatherv_e4m3(2, 96, sizes, P, P, P, N0) == B.MP_ERR_INVALID_ARG     # H % 128
+    assert L.mp_allgatherv_e4m3(33, 128, sizes, P, P, P, N0) == B.MP_ERR_INVALID_ARG   # R > 32
+    assert L.mp_allgatherv_e4m3(2, 128, sizes, P, P, _p(FAKE + 2), N0) == B.MP_ERR_INVALID_ARG
+    assert L.mp_allgatherv_mxfp8(2, 48, sizes, P, P, P, N0) == B.MP_ERR_INVALID_ARG    # H % 32
+    assert L.mp_allgatherv_mxfp8(2, 64, sizes, P, N0, P, N0) == B.MP_ERR_INVALID_ARG   # out NULL
+    neg = (ctypes.c_int64 * 2)(3, -1)
+    assert L.mp_allgatherv_mxfp8(2, 64, neg, P, P, P, N0) == B.MP_ERR_INVALID_ARG      # size < 0
     L.mp_dispatch_noalloc.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + \
         [ctypes.c_void_p] * 12
     assert L.mp_dispatch_noalloc(32, 100000, 8, 256, 64, B.MP_BF16, *([P] * 7), 16,

@@ -447,6 +447,129 @@ def test_allgatherv_multi_matches_per_tensor_oracle():
         assert np.array_equal(o.cpu().view(torch.uint8).numpy(), want)
 
 
+def _special_blocks(x: torch.Tensor, block: int) -> torch.Tensor:
+    """Plant an all-zero, a tiny, a large and a wide-range scale block in a [S][H] tensor."""
+    x = x.float()
+    S, H = x.shape
+    x[0, :block] = 0.0
+    if S > 1:
+        x[1, block:2 * block] = 2.0**-130
+    x[S - 1, :] *= 300.0
+    x[S // 2, :32] *= torch.exp2(torch.arange(32, dtype=torch.float32) - 16)
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+@pytest.mark.parametrize("R,H,sizes", [(5, 256, [7, 0, 130, 1, 33]), (1, 128, [3]),
+                                       (32, 128, [1] * 32), (3, 384, [0, 0, 0])],
+                         ids=["R5_ragged", "R1", "R32", "empty"])
+def test_allgatherv_quantised_equals_quantise_then_gather(fmt, R, H, sizes):
+    S = sum(sizes)
+    blk = 128 if fmt == "e4m3" else 32
+    x = wl.random_bf16((max(S, 1), H), seed=R * H)[:S]
+    if S:
+        x = _special_blocks(x, blk)
+    out = torch.full((R, S, H), 0x5A, dtype=torch.uint8, device="cuda")
+    if fmt == "e4m3":
+        osc = torch.full((R, S, H // 128), -1.0, dtype=torch.float32, device="cuda")
+        B.check(B.mp_allgatherv_e4m3(R, H, sizes, x.cuda(), out, osc))
+        q, sc, st = oracle.quantize_e4m3(wl.bf16_bits(x))
+        sc = sc.view(np.uint8)
+    else:
+        osc = torch.full((R, S, H // 32), 0x5A, dtype=torch.uint8, device="cuda")
+        B.check(B.mp_allgatherv_mxfp8(R, H, sizes, x.cuda(), out, osc))
+        q, sc, st = oracle.quantize_mxfp8(wl.bf16_bits(x))
+    torch.cuda.synchronize()
+    assert st == 0
+    want_q, st1 = oracle.allgatherv(q, sizes, R)
+    want_s, st2 = oracle.allgatherv(sc, sizes, R)
+    assert st1 == st2 == 0
+    assert np.array_equal(out.cpu().numpy(), want_q)
+    got_s = osc.cpu().view(torch.uint8).numpy()
+    assert np.array_equal(got_s, want_s.reshape(got_s.shape))
+
+
+def _offset_16(t: torch.Tensor) -> torch.Tensor:
+    """A CUDA copy of t whose data starts 16 bytes past a 32-byte boundary."""
+    buf = torch.zeros(t.numel() * t.element_size() + 48, dtype=torch.uint8, device="cuda")
+    base = (-buf.data_ptr()) % 32 + 16
+    out = buf[base:base + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+    out.copy_(t)
+    assert out.data_ptr() % 32 == 16
+    return out
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+def test_quantising_copies_from_a_16_byte_aligned_source(fmt):
+    """Sources that are 16- but not 32-byte aligned take the 8-channels-per-lane form."""
+    R, N, E, K, H = 4, 300, 16, 4, 384
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=77)
+    inp.x = _special_blocks(inp.x.reshape(R * N, H), 128 if fmt == "e4m3" else 32).reshape(R, N, H)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    xo = _offset_16(plan.x)
+    nsc = H // 128 if fmt == "e4m3" else H // 32
+    sdt = torch.float32 if fmt == "e4m3" else torch.uint8
+    rq = torch.zeros((plan.cap, H), dtype=torch.uint8, device="cuda")
+    rs = torch.zeros((plan.cap, nsc), dtype=sdt, device="cuda")
+    f = B.mp_dispatch_rows_e4m3 if fmt == "e4m3" else B.mp_dispatch_rows_mxfp8
+    B.check(f(R, N, H, xo, plan.send_row, plan.cap, rq, rs))
+    sizes = [5, 0, 17]
+    S = sum(sizes)
+    sh = _offset_16(plan.x.reshape(R * N, H)[:S])
+    gq = torch.zeros((3, S, H), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((3, S, nsc), dtype=sdt, device="cuda")
+    g = B.mp_allgatherv_e4m3 if fmt == "e4m3" else B.mp_allgatherv_mxfp8
+    B.check(g(3, H, sizes, sh, gq, gs))
+    torch.cuda.synchronize()
+    quant = oracle.quantize_e4m3 if fmt == "e4m3" else oracle.quantize_mxfp8
+    q, sc, st = quant(wl.bf16_bits(inp.x))
+    assert st == 0
+    payload = np.concatenate([q, sc.view(np.uint8)], axis=-1)
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    out, st2 = oracle.dispatch(payload, inp.topk_idx, inp.topk_weights, mask, E)
+    assert st2 == 0
+    n = out["num_recv"]
+    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"][:, :H])
+    assert np.array_equal(rs[:n].cpu().view(torch.uint8).numpy(), out["recv_x"][:, H:])
+    flat_q, flat_s = q.reshape(R * N, H)[:S], sc.view(np.uint8).reshape(R * N, -1)[:S]
+    for r in range(3):
+        assert np.array_equal(gq[r].cpu().numpy(), flat_q)
+        assert np.array_equal(gs[r].cpu().view(torch.uint8).numpy(), flat_s)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+def test_allgatherv_quantised_full_size(fmt):
+    """The rsv shape (R=8, H=4096, sizes ~ U{0..16384}): every rank's copy equals the
+    oracle's quantisation of the gathered rows."""
+    rsv = wl.CONFIGS["rsv"]
+    R, H = rsv["R"], rsv["H"]
+    sizes = np.random.default_rng(0).integers(0, rsv["max_rows"] + 1, size=R).tolist()
+    S = sum(sizes)
+    blk = 128 if fmt == "e4m3" else 32
+    x = _special_blocks(wl.gathered_bf16(S, H, seed=3), blk)
+    out = torch.zeros((R, S, H), dtype=torch.uint8, device="cuda")
+    if fmt == "e4m3":
+        osc = torch.zeros((R, S, H // 128), dtype=torch.float32, device="cuda")
+        B.check(B.mp_allgatherv_e4m3(R, H, sizes, x.cuda(), out, osc))
+        q, sc, st = oracle.quantize_e4m3(wl.bf16_bits(x))
+        sc = torch.from_numpy(sc.view(np.int32)).cuda()
+        osc = osc.view(torch.int32)
+    else:
+        osc = torch.zeros((R, S, H // 32), dtype=torch.uint8, device="cuda")
+        B.check(B.mp_allgatherv_mxfp8(R, H, sizes, x.cuda(), out, osc))
+        q, sc, st = oracle.quantize_mxfp8(wl.bf16_bits(x))
+        sc = torch.from_numpy(sc).cuda()
+    torch.cuda.synchronize()
+    assert st == 0
+    q = torch.from_numpy(q).cuda()
+    for r in range(R):
+        assert torch.equal(out[r], q), "rank %d codes" % r
+        assert torch.equal(osc[r], sc), "rank %d scales" % r
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads (the benchmark's launch configuration)
 # ---------------------------------------------------------------------------
