@@ -324,7 +324,23 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_mx, R * N * H * 2 + T * (H + H // 32) + R * N * R * 4),
         workload="dsv3 rows quantised in-kernel: bf16 in, MXFP8 (e4m3 + UE8M0 byte per 32 "
                  "channels) out")
-    del plan, rq, rs, rc
+    # global expert ids with a sentinel (the same scan) and the combined top-k weights
+    gids = torch.empty_like(plan.recv_topk_idx)
+    ms_g = timed(lambda: B.check(B.mp_dispatch_offsets_global(
+        R, N, K, E, plan.topk_idx, plan.topk_weights, plan.is_token_in_rank,
+        plan.num_tokens_per_rank, plan.num_tokens_per_expert, plan.cap, E, plan.recv_src_rank,
+        plan.recv_src_idx, gids, plan.recv_topk_weights, plan.dest_offsets, plan.rank_prefix,
+        plan.num_recv_tokens_per_expert, plan.send_row, plan.dev_err, plan.workspace)), steps)
+    cw = torch.empty((R, N, K), dtype=torch.float32, device="cuda")
+    ms_cw = timed(lambda: B.check(B.mp_combine_weights(R, N, K, plan.recv_topk_weights, plan.cap,
+                                                       plan.send_row, cw, plan.dev_err)), steps)
+    assert plan.device_error() == 0
+    out["dispatch_offsets_global_ids"] = dict(
+        row(ms_g, algorithmic_bytes(R, N, K, E, H, T)["offsets"]),
+        workload="dsv3 receive offsets with global expert ids (sentinel E)")
+    out["combine_topk_weights"] = dict(row(ms_cw, T * K * 4 + R * N * R * 4 + R * N * K * 4),
+                                       workload="dsv3 combined top-k weights")
+    del plan, rq, rs, rc, gids, cw
     torch.cuda.empty_cache()
 
     cfg = wl.CONFIGS["fp8"]
@@ -380,7 +396,85 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_agm, S * Hh * 2 + Rr * S * (Hh + Hh // 32)),
         workload="rsv shards quantised once (MXFP8, UE8M0 byte per 32 channels), gathered "
                  "to 8 ranks")
-    del rp, qx, qc
+    # multi-tensor all-gatherv: e4m3 data and its fp32 scales in one launch
+    del qc
+    qd = torch.randint(0, 256, (S, Hh), generator=g, device="cuda", dtype=torch.uint8)
+    qs = torch.rand((S, Hh // 128), generator=g, device="cuda")
+    qso = torch.empty((Rr, S, Hh // 128), dtype=torch.float32, device="cuda")
+    ms_mt = timed(lambda: B.check(B.mp_allgatherv_multi(Rr, [Hh, Hh // 128 * 4], sizes, [qd, qs],
+                                                        [qx, qso])), max(5, steps // 4))
+    out["allgatherv_multi_e4m3_and_scales"] = dict(
+        row(ms_mt, (S + Rr * S) * (Hh + Hh // 128 * 4)),
+        workload="rsv rows as e4m3 data + fp32 scale per 128 channels, two tensors, one launch")
+    del rp, qx, qd, qs, qso
+    torch.cuda.empty_cache()
+
+    # low-latency expert-major layout at the pages' small-batch shape (R=8, N=128,
+    # H=7168, top-8 of 256): layout -> LL offsets -> LL rows -> weighted LL combine,
+    # launched one by one and replayed as one CUDA graph
+    R, N, H, E, K = 8, 128, 7168, 256, 8
+    rng = np.random.default_rng(1)
+    plan = EPPlan(R, N, K, E, H, "bf16")
+    plan.topk_idx.copy_(torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)))
+    plan.topk_weights.copy_(torch.from_numpy(wl.softmax_weights(rng, R, N, K)))
+    plan.x.copy_(torch.randn((R, N, H), generator=g, device="cuda").to(torch.bfloat16))
+    cap = R * N * K
+    eoff = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    esoff = torch.empty((E, R), dtype=torch.int32, device="cuda")
+    src = torch.empty(cap, dtype=torch.int32, device="cuda")
+    slot = torch.empty((R, N, K), dtype=torch.int32, device="cuda")
+    rx = torch.empty((cap, H), dtype=torch.bfloat16, device="cuda")
+    yl = torch.randn((cap, H), generator=g, device="cuda").to(torch.bfloat16)
+    lo = torch.empty((R, N, H), dtype=torch.bfloat16, device="cuda")
+
+    def ll_step():
+        B.check(plan.layout())
+        B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, plan.num_tokens_per_expert,
+                                         cap, eoff, esoff, src, slot, plan.dev_err))
+        B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
+        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
+
+    ms_ll = timed(ll_step, steps)
+    ll_calls = [
+        lambda: B.check(plan.layout()),
+        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx,
+                                                 plan.num_tokens_per_expert, cap, eoff, esoff,
+                                                 src, slot, plan.dev_err)),
+        lambda: B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap,
+                                              rx, None)),
+        lambda: B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo,
+                                        plan.dev_err))]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ll_calls) + 1)]
+           for _ in range(steps)]
+    for ev in evs:
+        ev[0].record()
+        for c, call in enumerate(ll_calls):
+            call()
+            ev[c + 1].record()
+    torch.cuda.synchronize()
+    ll_phase_us = {name: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / steps * 1e3
+                   for c, name in enumerate(("layout", "ll_offsets", "ll_rows", "combine_ll"))}
+    s_cap = torch.cuda.Stream()
+    s_cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_cap):
+        ll_step()
+    torch.cuda.current_stream().wait_stream(s_cap)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ll_step()
+    ms_llg = timed(graph.replay, steps)
+    assert plan.device_error() == 0
+    ll_bytes = (algorithmic_bytes(R, N, K, E, H, 0)["layout"]
+                + R * N * K * 8 + cap * 4 + (E + 1) * 4 + E * R * 4   # LL offsets
+                + R * N * H * 2 + cap * H * 2 + R * N * K * 4           # LL rows
+                + cap * H * 2 + R * N * K * 8 + R * N * H * 2)          # weighted LL combine
+    out["low_latency_step_n128"] = dict(
+        row(ms_ll, ll_bytes), us_per_step=ms_ll * 1e3, us_per_step_cuda_graph=ms_llg * 1e3,
+        phases_us=ll_phase_us, receive_rows=int(cap),
+        GBs_cuda_graph=ll_bytes / (ms_llg / 1e3) / 1e9,
+        workload="R=8, N=128, H=7168 bf16, E=256, top-8: layout + LL offsets + LL rows + "
+                 "weighted LL combine (4 launches)")
+    del plan, rx, yl, lo, graph
     torch.cuda.empty_cache()
 
     # the skewed workload: Zipf(1.2) routing, rank 0 hot

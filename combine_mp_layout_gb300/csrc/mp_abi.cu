@@ -357,7 +357,6 @@ int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                            int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                            mp_stream_t stream) {
   if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
-  if (int64_t(N) * K * 4 > 200 * 1024) return MP_ERR_INVALID_ARG;  // the rank's slab in smem
   if (!num_tokens_per_expert || !expert_offsets || !expert_src_offsets || !dev_err)
     return MP_ERR_INVALID_ARG;
   if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;

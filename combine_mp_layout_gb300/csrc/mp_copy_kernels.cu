@@ -39,6 +39,13 @@
 #ifndef MP_COMBINE_MINB
 #define MP_COMBINE_MINB 3
 #endif
+// Small dispatches (fewer warp units at the default shape than the GPU holds
+// warps, e.g. the low-latency batches of 128 tokens per rank) use 1 vector per
+// lane and unit instead, for 4x the units: measured 29 -> 25 us for the rows
+// of R=8, N=128, top-8, H=7168 (MP_SMALL_DISPATCH = 0 turns this off).
+#ifndef MP_SMALL_DISPATCH
+#define MP_SMALL_DISPATCH 1
+#endif
 
 #ifndef MP_DISPATCH_TMA
 #define MP_DISPATCH_TMA 0
@@ -701,6 +708,13 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                                   send_row, scales_per_row, x_scales,
                                                   recv_scales, stream);
   }
+  if (MP_SMALL_DISPATCH && MP_DISPATCH_NW == 8 && row_bytes % 32 == 0 && aligned(x, 32) &&
+      aligned(recv_x, 32)) {
+    const int64_t slabs = (row_bytes / 32 + kWarp * MP_DISPATCH_U - 1) / (kWarp * MP_DISPATCH_U);
+    if (tokens * slabs < int64_t(sm_count()) * (2048 / kWarp))
+      return dispatch_copy_nw<8, 1>(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
+                                    scales_per_row, x_scales, recv_scales, stream);
+  }
   if (MP_DISPATCH_NW == 8 && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
     return dispatch_copy_nw<MP_DISPATCH_NW, MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x,
                                                            recv_capacity, send_row,
@@ -712,7 +726,7 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
 }
 
 // Quantising copies.  Launch shapes measured on GB300 (dsv3 dispatch rows,
-// R=8, N=4096, H=7168; rsv all-gatherv, R=8, S=65,463, H=4096):
+// R=8, N=4096, H=7168; rsv all-gatherv, R=8, S=44,383, H=4096):
 //  - 16 channels per lane (32-byte loads, 16-byte code stores) beat 8 by
 //    10-15%; a source that is not 32-byte aligned takes the 8-channel form;
 //  - 2 vectors per lane and unit, except 1 for the e4m3 gather (276 vs

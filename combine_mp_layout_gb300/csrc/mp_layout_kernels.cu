@@ -398,14 +398,28 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 // Low-latency expert-major offsets ("MSCCLPP EP implementation", the
 // low-latency dispatch/combine: per-expert receive buffers).  One row per
 // (token, top-k slot with a valid expert); expert e's rows are contiguous,
-// blocks in ascending e, rows inside a block ordered by source rank then
-// token.  One block per source rank; each thread owns a contiguous run of
-// experts, gets its first row from a block-wide scan of the per-expert totals
-// (the layout's num_tokens_per_expert), and walks the rank's top-k slab in
-// token order, so the row order is deterministic.  Meant for the small
-// batches of the low-latency mode (cost per thread ~ N*K per owned expert).
+// blocks in ascending e, rows inside a block ordered by source rank, then
+// token, then top-k slot.
+//
+// One block per source rank s, a stable counting sort of its N*K entries:
+//  1. the rank's entries are cut into nseg contiguous segments, one per warp,
+//     and each warp counts its segment's entries per expert in shared memory;
+//  2. every expert's first row (a block-wide scan of the per-expert totals
+//     over all source ranks, from the layout's num_tokens_per_expert, plus
+//     the rows of e from ranks < s) and, per expert, the exclusive prefix of
+//     the segment counts;
+//  3. each warp walks its segment 32 entries at a time in order; lanes with
+//     the same expert find each other with __match_any_sync and take
+//     consecutive rows, so the order is deterministic.
+// Shared memory: (nseg + 1) * E int32, nseg = min(32, 16384 / E) (>= 1).
 // ---------------------------------------------------------------------------
 constexpr int kLLThreads = 1024;
+constexpr int kLLHistInts = 16384;
+
+__host__ __device__ inline int ll_segments(int E) {
+  const int n = kLLHistInts / (E > 0 ? E : 1);
+  return n < 1 ? 1 : (n > kLLThreads / kWarp ? kLLThreads / kWarp : n);
+}
 
 __global__ void __launch_bounds__(kLLThreads)
 mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
@@ -413,33 +427,40 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
                 int32_t* __restrict__ expert_offsets, int32_t* __restrict__ expert_src_offsets,
                 int32_t* __restrict__ recv_src_token, int32_t* __restrict__ slot_row,
                 int32_t* __restrict__ dev_err) {
-  extern __shared__ int32_t ll_topk[];  // [N * K] of this source rank
+  extern __shared__ int32_t ll_smem[];
   __shared__ int64_t warp_sums[kLLThreads / kWarp];
+  const int nseg = ll_segments(E);
+  int32_t* hist = ll_smem;             // [nseg][E]: counts, then running offsets
+  int32_t* rowbase = ll_smem + nseg * E;  // [E]: first row of (expert, this rank)
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nk = int64_t(N) * K;
   const int32_t* src = topk_idx + int64_t(s) * nk;
   int32_t* slots = slot_row + int64_t(s) * nk;
-  for (int64_t i = tid; i < nk; i += kLLThreads) {
-    const int e = __ldg(src + i);
-    ll_topk[i] = e;
-    if (e < 0 || e >= E) slots[i] = -1;  // masked or invalid: no row
-  }
-  // this thread's experts [e0, e1) and their totals over every source rank
+  const int64_t seg_len = (nk + nseg - 1) / nseg;
+  const int64_t g0 = min(nk, int64_t(warp) * seg_len), g1 = min(nk, g0 + seg_len);
+  for (int i = tid; i < nseg * E; i += kLLThreads) hist[i] = 0;
+  __syncthreads();
+  // 1. counts per (segment, expert)
+  if (warp < nseg)
+    for (int64_t i = g0 + lane; i < g1; i += kWarp) {
+      const int e = __ldg(src + i);
+      if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+    }
+  // 2a. this thread's experts [e0, e1) and their totals over every source rank
   const int cpt = (E + kLLThreads - 1) / kLLThreads;
   const int e0 = min(E, tid * cpt), e1 = min(E, e0 + cpt);
   int64_t chunk = 0;
   for (int e = e0; e < e1; ++e)
     for (int q = 0; q < R; ++q) chunk += __ldg(num_tokens_per_expert + int64_t(q) * E + e);
-  // block-wide exclusive scan of the chunk totals
-  int64_t inc = chunk;
+  int64_t inc = chunk;  // block-wide exclusive scan of the chunk totals
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t v = __shfl_up_sync(kFull, inc, o);
     if (lane >= o) inc += v;
   }
   if (lane == 31) warp_sums[warp] = inc;
-  __syncthreads();
+  __syncthreads();  // also orders the segment counts before 2b
   if (warp == 0) {
     int64_t w = lane < kLLThreads / kWarp ? warp_sums[lane] : 0;
 #pragma unroll
@@ -451,7 +472,7 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   }
   __syncthreads();
   int64_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + inc - chunk;
-  bool overflow = false;
+  // 2b. per expert: outputs, first row of this rank, exclusive prefix over segments
   for (int e = e0; e < e1; ++e) {
     int64_t tot = 0, pre = 0;
     for (int q = 0; q < R; ++q) {
@@ -461,21 +482,43 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
     }
     if (s == 0) expert_offsets[e] = int32_t(base);
     expert_src_offsets[int64_t(e) * R + s] = int32_t(pre);
-    int64_t row = base + pre;
-    for (int64_t i = 0; i < nk; ++i) {
-      if (ll_topk[i] != e) continue;
-      if (row < recv_capacity) {
-        slots[i] = int32_t(row);
-        recv_src_token[row] = int32_t(int64_t(s) * N + i / K);
-      } else {
-        slots[i] = -1;
-        overflow = true;
-      }
-      ++row;
+    rowbase[e] = int32_t(base + pre);
+    int run = 0;
+    for (int g = 0; g < nseg; ++g) {
+      const int c = hist[g * E + e];
+      hist[g * E + e] = run;
+      run += c;
     }
     base += tot;
   }
   if (s == 0 && e0 < E && e1 == E) expert_offsets[E] = int32_t(base);
+  __syncthreads();
+  // 3. rows, segment by segment in entry order
+  bool overflow = false;
+  if (warp < nseg) {
+    for (int64_t i0 = g0; i0 < g1; i0 += kWarp) {
+      const int64_t i = i0 + lane;
+      const int e = i < g1 ? __ldg(src + i) : -1;
+      const bool ok = e >= 0 && e < E;
+      const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
+      const int run = ok ? hist[warp * E + e] : 0;
+      __syncwarp();
+      if (ok) {
+        const int64_t row = int64_t(rowbase[e]) + run + __popc(peers & lanemask_lt());
+        if (row < recv_capacity) {
+          slots[i] = int32_t(row);
+          recv_src_token[row] = int32_t(int64_t(s) * N + i / K);
+        } else {
+          slots[i] = -1;
+          overflow = true;
+        }
+        if ((peers >> lane) == 1u) hist[warp * E + e] = run + __popc(peers);  // highest peer
+      } else if (i < g1) {
+        slots[i] = -1;  // masked or invalid: no row
+      }
+      __syncwarp();
+    }
+  }
   if (overflow) raise_error(dev_err, MP_ERR_CAPACITY);
 }
 
@@ -554,7 +597,7 @@ cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_id
                               int32_t* expert_offsets, int32_t* expert_src_offsets,
                               int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                               cudaStream_t stream) {
-  const size_t smem = sizeof(int32_t) * size_t(N) * K;
+  const size_t smem = sizeof(int32_t) * size_t(ll_segments(E) + 1) * size_t(E);
   static thread_local int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);

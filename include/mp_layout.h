@@ -388,8 +388,8 @@ int mp_allgatherv_multi(int R, int ntensors, const int64_t *row_bytes, const int
  * (the pages fix no order): expert e's rows are contiguous, blocks in
  * ascending e; inside a block rows are ordered by source rank, then token.
  * Meant for the small batches of the low-latency mode: the offsets kernel
- * runs one block per source rank (N*K*4 bytes of that rank's top-k ids must
- * fit in 200 KB of shared memory).
+ * runs one block per source rank (a stable counting sort of that rank's N*K
+ * entries), so its time grows with N*K.
  *
  * mp_dispatch_ll_offsets
  *   in   topk_idx               int32 [R][N][K] (-1 = masked)

@@ -162,8 +162,8 @@ def test_newer_entry_points_reject(L):
     L.mp_dispatch_ll_offsets.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2 + \
         [ctypes.c_int64] + [ctypes.c_void_p] * 6
     assert L.mp_dispatch_ll_offsets(2, 8, 2, 7, P, P, 16, P, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG
-    assert L.mp_dispatch_ll_offsets(2, 60000, 8, 8, P, P, 16, P, P, P, P, P, N0) == \
-        B.MP_ERR_INVALID_ARG  # the rank's top-k slab does not fit in shared memory
+    assert L.mp_dispatch_ll_offsets(2, 8, 33, 8, P, P, 16, P, P, P, P, P, N0) == \
+        B.MP_ERR_INVALID_ARG  # K > MP_MAX_TOPK
     L.mp_combine_ll.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_int64] + \
         [ctypes.c_void_p] * 5
     assert L.mp_combine_ll(2, 8, 2, 60, P, 4, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG   # H % 8

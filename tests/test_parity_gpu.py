@@ -392,16 +392,23 @@ def test_global_ids_and_combined_weights():
 
 
 @pytest.mark.parametrize("cfg", [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
-                                 dict(R=5, N=77, E=20, K=6, H=264), dict(R=3, N=300, E=9, K=9, H=64)],
-                         ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c)
+                                 dict(R=5, N=77, E=20, K=6, H=264), dict(R=3, N=300, E=9, K=9, H=64),
+                                 dict(R=4, N=3000, E=64, K=6, H=64),
+                                 dict(R=8, N=64, E=8192, K=8, H=64),
+                                 dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5),
+                                 dict(R=1, N=40, E=3, K=3, H=64)],
+                         ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
+                         + ("_cap" if "cap_frac" in c else ""))
 def test_low_latency_layout_matches_oracle(cfg):
+    cfg = dict(cfg)
+    cap_frac = cfg.pop("cap_frac", None)
     inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=cfg["N"])
     R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
     inp.topk_idx[:, ::7, 1] = -1
     plan = EPPlan(R, N, K, E, H)
     plan.load(inp)
     B.check(plan.layout())
-    cap = R * N * K
+    cap = R * N * K if cap_frac is None else int(R * N * K * cap_frac)
     dev = "cuda"
     eoff = torch.full((E + 1,), -3, dtype=torch.int32, device=dev)
     esoff = torch.full((E, R), -3, dtype=torch.int32, device=dev)
@@ -415,10 +422,10 @@ def test_low_latency_layout_matches_oracle(cfg):
     out = torch.zeros((R, N, H), dtype=torch.bfloat16, device=dev)
     B.check(B.mp_combine_ll(R, N, K, H, y, cap, slot, plan.topk_weights, out, plan.dev_err))
     torch.cuda.synchronize()
-    assert plan.device_error() == 0
-    ll, st = oracle.dispatch_ll(wl.bf16_bits(inp.x), inp.topk_idx, E)
-    assert st == 0
-    n = ll["num_recv"]
+    ll, st = oracle.dispatch_ll(wl.bf16_bits(inp.x), inp.topk_idx, E, recv_capacity=cap)
+    assert plan.device_error() == st
+    assert (st == 0) == (cap_frac is None)
+    n = min(ll["num_recv"], cap)
     assert np.array_equal(eoff.cpu().numpy(), ll["expert_offsets"])
     assert np.array_equal(esoff.cpu().numpy(), ll["expert_src_offsets"])
     assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
