@@ -582,23 +582,45 @@ mp_k_agv_pc(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __
 // of their 16-byte vectors, each read once and written R times.
 // ---------------------------------------------------------------------------
 struct AgvList {
-  const int4* in[MP_MAX_TENSORS];
-  int4* out[MP_MAX_TENSORS];
+  const void* in[MP_MAX_TENSORS];
+  void* out[MP_MAX_TENSORS];
   int64_t nvec[MP_MAX_TENSORS];   // vectors of one gathered copy of tensor j
   int64_t first[MP_MAX_TENSORS];  // index of tensor j's first vector in the walk
   int n;
 };
 
+// Multi-tensor all-gatherv: the tensors' vectors are walked as one sequence;
+// each thread reads U vectors once and stores each of them R times, like
+// mp_k_agv (one short block per kCopyThreads * U vectors).
+template <int NW, int U>
 __global__ void __launch_bounds__(kCopyThreads)
 mp_k_agv_multi(int R, int64_t total, AgvList l) {
-  const int64_t stride = int64_t(gridDim.x) * kCopyThreads;
-  for (int64_t g = int64_t(blockIdx.x) * kCopyThreads + threadIdx.x; g < total; g += stride) {
-    int j = 0;
-    while (j + 1 < l.n && g >= l.first[j + 1]) ++j;
-    const int64_t i = g - l.first[j];
-    const Words<4> v = ld_stream_w<4>(reinterpret_cast<const Words<4>*>(l.in[j]) + i);
-    Words<4>* out = reinterpret_cast<Words<4>*>(l.out[j]);
-    for (int q = 0; q < R; ++q) st_stream_w<4>(out + int64_t(q) * l.nvec[j] + i, v);
+  const int64_t stride = int64_t(gridDim.x) * kCopyThreads * U;
+  for (int64_t i0 = int64_t(blockIdx.x) * kCopyThreads * U + threadIdx.x; i0 < total;
+       i0 += stride) {
+    Words<NW> v[U];
+    int jj[U];
+    int64_t ii[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = i0 + u * kCopyThreads;
+      jj[u] = -1;
+      ii[u] = 0;
+      if (g < total) {
+        int j = 0;
+        while (j + 1 < l.n && g >= l.first[j + 1]) ++j;
+        jj[u] = j;
+        ii[u] = g - l.first[j];
+        v[u] = ld_stream_w<NW>(static_cast<const Words<NW>*>(l.in[j]) + ii[u]);
+      }
+    }
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (jj[u] >= 0)
+          st_stream_w<NW>(static_cast<Words<NW>*>(l.out[jj[u]]) + int64_t(q) * l.nvec[jj[u]] +
+                              ii[u],
+                          v[u]);
   }
 }
 
@@ -881,23 +903,33 @@ cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* i
 
 namespace mp {
 
-cudaError_t launch_allgatherv_multi(int R, int n, const int64_t* S_row_bytes, int64_t S,
-                                    const void* const* in, void* const* out,
-                                    cudaStream_t stream) {
+template <int NW, int U>
+static cudaError_t agv_multi_nw(int R, int n, const int64_t* row_bytes, int64_t S,
+                                const void* const* in, void* const* out, cudaStream_t stream) {
   AgvList l{};
   l.n = n;
   int64_t total = 0;
   for (int j = 0; j < n; ++j) {
-    l.in[j] = static_cast<const int4*>(in[j]);
-    l.out[j] = static_cast<int4*>(out[j]);
-    l.nvec[j] = S * S_row_bytes[j] / 16;
+    l.in[j] = in[j];
+    l.out[j] = out[j];
+    l.nvec[j] = S * row_bytes[j] / (4 * NW);
     l.first[j] = total;
     total += l.nvec[j];
   }
   if (total == 0) return cudaSuccess;
-  static const int per_sm = resident_blocks(mp_k_agv_multi);
-  const unsigned grid = grid_for(per_sm, kCopyThreads, total);
-  return launch_kernel(mp_k_agv_multi, dim3(grid), dim3(kCopyThreads), 0, stream, R, total, l);
+  const unsigned grid = grid_full(int64_t(kCopyThreads) * U, total);
+  return launch_kernel(mp_k_agv_multi<NW, U>, dim3(grid), dim3(kCopyThreads), 0, stream, R, total,
+                       l);
+}
+
+cudaError_t launch_allgatherv_multi(int R, int n, const int64_t* row_bytes, int64_t S,
+                                    const void* const* in, void* const* out,
+                                    cudaStream_t stream) {
+  bool wide = true;  // 32-byte vectors when every tensor allows them
+  for (int j = 0; j < n; ++j)
+    wide = wide && (S * row_bytes[j]) % 32 == 0 && aligned(in[j], 32) && aligned(out[j], 32);
+  if (wide) return agv_multi_nw<8, 2>(R, n, row_bytes, S, in, out, stream);
+  return agv_multi_nw<4, 4>(R, n, row_bytes, S, in, out, stream);
 }
 
 }  // namespace mp

@@ -436,14 +436,17 @@ def test_low_latency_layout_matches_oracle(cfg):
     assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll")
 
 
-def test_allgatherv_multi_matches_per_tensor_oracle():
+@pytest.mark.parametrize("wide", [False, True], ids=["16B", "32B"])
+def test_allgatherv_multi_matches_per_tensor_oracle(wide):
+    """Tensors whose bytes all split into 32-byte vectors take the wide path; a
+    144-byte-row tensor with an odd row count forces 16-byte vectors."""
     R, sizes = 5, [7, 0, 130, 1, 33]
     S = sum(sizes)
     g = torch.Generator().manual_seed(5)
     data = torch.randint(0, 256, (S, 2048), generator=g, dtype=torch.uint8)      # e.g. packed fp4
     scales = torch.randint(0, 256, (S, 16 * 8), generator=g, dtype=torch.uint8)  # 128-byte rows
     hid = torch.randn((S, 72), generator=g).to(torch.bfloat16)                    # 144-byte rows
-    ins = [data, scales, hid]
+    ins = [data, scales] if wide else [data, scales, hid]
     outs = [torch.zeros((R,) + tuple(t.shape), dtype=t.dtype, device="cuda") for t in ins]
     row_bytes = [t[0].nbytes for t in ins]
     B.check(B.mp_allgatherv_multi(R, row_bytes, sizes, [t.cuda() for t in ins], outs))
