@@ -75,6 +75,12 @@ class OracleLib:
         L.oracle_combine_weights.restype = ctypes.c_int
         L.oracle_quantize_mxfp8.argtypes = [i64, i32, P, P, P]
         L.oracle_quantize_mxfp8.restype = ctypes.c_int
+        L.oracle_quantize_mxfp4.argtypes = [i64, i32, P, P, P]
+        L.oracle_quantize_mxfp4.restype = ctypes.c_int
+        L.oracle_f32_to_e2m1.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e2m1.restype = ctypes.c_uint8
+        L.oracle_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_to_f32.restype = ctypes.c_float
         L.oracle_dispatch_ll.argtypes = [i32, i32, i32, i32, i64, P, P, i64, P, P, P, P, P]
         L.oracle_dispatch_ll.restype = ctypes.c_int
         L.oracle_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P]
@@ -206,6 +212,23 @@ class OracleLib:
         st = self.L.oracle_quantize_mxfp8(T, H, _p(x_bits), _p(q), _p(codes))
         return q, codes, st
 
+    def quantize_mxfp4(self, x_bits: np.ndarray):
+        """x_bits uint16 (bf16 patterns) [..., H] -> (q uint8 [..., H/2] (two E2M1 codes
+        per byte, even channel in the low nibble), UE8M0 codes uint8 [..., H/32], status)."""
+        x_bits = _c(x_bits, np.uint16)
+        H = x_bits.shape[-1]
+        T = x_bits.size // H if H else 0
+        q = np.zeros(x_bits.shape[:-1] + (max(H // 2, 1),), np.uint8)
+        codes = np.zeros(x_bits.shape[:-1] + (max(H // 32, 1),), np.uint8)
+        st = self.L.oracle_quantize_mxfp4(T, H, _p(x_bits), _p(q), _p(codes))
+        return q, codes, st
+
+    def f32_to_e2m1(self, f: float) -> int:
+        return self.L.oracle_f32_to_e2m1(f)
+
+    def e2m1_to_f32(self, c: int) -> float:
+        return self.L.oracle_e2m1_to_f32(c)
+
     def recv_topk_global(self, topk_idx, E, disp: dict, sentinel: int):
         """Global expert ids of the receive rows of an oracle dispatch result."""
         topk_idx = _c(topk_idx, np.int32)
@@ -323,6 +346,10 @@ def recv_topk_global(topk_idx, E, disp, sentinel):
 
 def quantize_mxfp8(x_bits):
     return default().quantize_mxfp8(x_bits)
+
+
+def quantize_mxfp4(x_bits):
+    return default().quantize_mxfp4(x_bits)
 
 
 def combine_weights(recv_topk_weights, send_row):

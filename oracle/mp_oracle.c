@@ -511,3 +511,67 @@ int oracle_quantize_mxfp8(int64_t T, int H, const uint16_t *x, uint8_t *q, uint8
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 block quantisation [AGV, the review note that gathering a    */
+/* list of tensors lets the caller quantise to fp4 before the         */
+/* all-gather; the pages name no fp4 format, so the microscaling one  */
+/* of the EP page's MXFP8 scheme is used with E2M1 elements].         */
+/* E2M1 (OCP FP4): sign bit 3, magnitude codes 0..7 stand for         */
+/* 0, 0.5, 1, 1.5, 2, 3, 4, 6.  Narrowing picks the nearest magnitude,*/
+/* a tie goes to the even code, magnitudes >= 6 saturate to 6, and    */
+/* the sign is kept (a negative value that rounds to zero is -0).     */
+/* Per block of 32 channels: code = clamp(floor(log2 amax) - 2 + 127, */
+/* 0, 254) (2 = exponent of E2M1's largest normal, 6 = 1.5 * 2^2),    */
+/* 0 for an all-zero block; X = 2^(code - 127); element e2m1(x / X).  */
+/* Two elements per byte: channel 2j in bits 0-3, 2j+1 in bits 4-7.   */
+/*   x bf16 [T][H] (H % 32 == 0), q uint8 [T][H/2], codes [T][H/32]   */
+/* ------------------------------------------------------------------ */
+static const float e2m1_mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+uint8_t oracle_f32_to_e2m1(float x) {
+  const uint8_t sign = signbit(x) ? 8u : 0u;
+  const double a = fabs((double)x);
+  if (!(a < 6.0)) return (uint8_t)(sign | 7u); /* saturate (NaN never occurs in inputs) */
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = fabs(a - e2m1_mag[c]), db = fabs(a - e2m1_mag[best]);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  return (uint8_t)(sign | (uint8_t)best);
+}
+
+float oracle_e2m1_to_f32(uint8_t c) {
+  const float m = e2m1_mag[c & 7u];
+  return (c & 8u) ? -m : m;
+}
+
+int oracle_quantize_mxfp4(int64_t T, int H, const uint16_t *x, uint8_t *q, uint8_t *codes) {
+  if (T < 0 || H <= 0 || H % 32 != 0) return ORC_BAD_ARG;
+  const int nb = H / 32;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t *xb = x + t * H + (int64_t)b * 32;
+      float amax = 0.0f;
+      for (int h = 0; h < 32; ++h) {
+        float v = fabsf(oracle_bf16_to_f32(xb[h]));
+        if (v > amax) amax = v;
+      }
+      int code = 0;
+      if (amax > 0.0f) {
+        code = floor_log2_f32(amax) - 2 + 127;
+        if (code < 0) code = 0;
+        if (code > 254) code = 254;
+      }
+      codes[t * nb + b] = (uint8_t)code;
+      const float X = ldexpf(1.0f, code - 127);
+      uint8_t *qb = q + t * (H / 2) + (int64_t)b * 16;
+      for (int h = 0; h < 32; h += 2) {
+        const uint8_t lo = oracle_f32_to_e2m1(oracle_bf16_to_f32(xb[h]) / X);
+        const uint8_t hi = oracle_f32_to_e2m1(oracle_bf16_to_f32(xb[h + 1]) / X);
+        qb[h / 2] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+  return 0;
+}

@@ -518,7 +518,65 @@ def pin_mxfp8_quantisation(orc) -> None:
         assert 256.0 <= mag <= 448.0
 
 
+def _e2m1_by_binade(v: np.ndarray) -> np.ndarray:
+    """E2M1 narrowing written independently of the oracle: scale each binade so that
+    the format's step becomes 1, round with numpy's round-half-to-even, scale back,
+    saturate at 6; the code is the position of the magnitude in the value grid."""
+    a = np.abs(v.astype(np.float64))
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    r = np.minimum(np.round(a / step) * step, 6.0)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    code = np.searchsorted(grid, r).astype(np.uint8)
+    assert np.array_equal(grid[code], r)
+    return code | np.where(np.signbit(v), 8, 0).astype(np.uint8)
+
+
+def pin_mxfp4_quantisation(orc) -> None:
+    """E2M1 decoding against the bit layout (bias 1); narrowing against a binade-scaled
+    numpy round-half-to-even; scale codes against numpy's frexp; nibble order; decoded
+    values within half an E2M1 step of x / X; zero and tiny blocks."""
+    for c in range(16):  # sign, 2 exponent bits (bias 1), 1 mantissa bit
+        e, m = (c >> 1) & 3, c & 1
+        mag = m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1)
+        assert orc.e2m1_to_f32(c) == (-mag if c & 8 else mag)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (grid[:-1] + grid[1:]) / 2
+    rng = np.random.default_rng(53)
+    vals = np.concatenate([grid, mids, np.nextafter(mids, 0), np.nextafter(mids, 10), [6.5, 7.0, 8.0, 1e30],
+                           rng.standard_normal(4000) * 3]).astype(np.float32)
+    vals = np.concatenate([vals, -vals])
+    ours = np.array([orc.f32_to_e2m1(float(v)) for v in vals], np.uint8)
+    assert np.array_equal(ours, _e2m1_by_binade(vals))
+    x = (rng.standard_normal((24, 128)) * np.exp2(rng.integers(-20, 20, (24, 4)).repeat(32, 1)))
+    x = x.astype(np.float32)
+    x[2, :32] = 0.0                                            # all-zero block
+    x[3, 32:64] = np.float32(2.0**-130) * rng.integers(1, 8, 32)  # tiny non-zero block
+    x[4, 64:96] = np.tile([1.0, 6.0], 16) * 2.0**5             # even channels 1*X, odd 6*X
+    xb = _bits(x)
+    xf = _f32(xb).astype(np.float64)
+    q, codes, st = orc.quantize_mxfp4(xb)
+    assert st == 0 and q.shape == (24, 64) and codes.shape == (24, 4)
+    amax = np.abs(xf.reshape(24, 4, 32)).max(-1)
+    _, ex = np.frexp(amax)
+    want = np.where(amax > 0, np.clip(ex - 1 - 2 + 127, 0, 254), 0)
+    assert np.array_equal(codes.astype(np.int64), want)
+    assert codes[2, 0] == 0 and not q[2, :16].any()
+    assert codes[3, 1] == 0 and q[3, 16:32].any()
+    # amax 6 * 2^5 = 192: floor(log2) 7, code 127 + 7 - 2, X = 2^5; 1*X -> code 2, 6*X -> 7
+    assert codes[4, 2] == 127 + 5 and np.all(q[4, 32:48] == 0x72)
+    lo, hi = q & 0x0F, q >> 4
+    el = np.stack([lo, hi], axis=-1).reshape(24, 128)
+    sign = np.where(el & 8, -1.0, 1.0)
+    deq = sign * grid[el & 7] * np.repeat(np.exp2(codes.astype(np.float64) - 127), 32, axis=1)
+    Xe = np.repeat(np.exp2(codes.astype(np.float64) - 127), 32, axis=1)
+    sat = np.abs(xf) >= 6 * Xe
+    tol = np.maximum(np.abs(xf) / 4, 0.25 * Xe) * 1.0001
+    assert np.all(np.abs(deq - xf)[~sat] <= tol[~sat])
+    assert np.all(np.abs(deq)[sat] == (6 * Xe)[sat])
+    assert np.all(np.signbit(deq) == np.signbit(xf))
+
+
 ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
             pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
-            pin_low_latency_layout, pin_mxfp8_quantisation]
+            pin_low_latency_layout, pin_mxfp8_quantisation, pin_mxfp4_quantisation]

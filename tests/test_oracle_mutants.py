@@ -65,7 +65,14 @@ MUTANTS = {
     "ll_keeps_masked": ("if (topk_idx[tok * K + k] != e) continue;",
                         "if (topk_idx[tok * K + k] != e && !(e == 0 && topk_idx[tok * K + k] == -1)) continue;"),
     "mxfp8_emax_7": ("code = floor_log2_f32(amax) - 8 + 127;", "code = floor_log2_f32(amax) - 7 + 127;"),
-    "mxfp8_flush_tiny": ("        if (code < 0) code = 0;\n", "        if (code < 0) code = 0, amax = 0.0f;\n        if (amax == 0.0f) { for (int h = 0; h < 32; ++h) q[t * H + (int64_t)b * 32 + h] = 0; codes[t * nb + b] = 0; continue; }\n"),
+    "mxfp8_flush_tiny": ("- 8 + 127;\n        if (code < 0) code = 0;\n", "- 8 + 127;\n        if (code < 0) code = 0, amax = 0.0f;\n        if (amax == 0.0f) { for (int h = 0; h < 32; ++h) q[t * H + (int64_t)b * 32 + h] = 0; codes[t * nb + b] = 0; continue; }\n"),
+    "e2m1_ties_up": ("if (dc < db || (dc == db && (c & 1) == 0)) best = c;",
+                     "if (dc <= db) best = c;"),
+    "e2m1_sign_dropped": ("const uint8_t sign = signbit(x) ? 8u : 0u;",
+                          "const uint8_t sign = 0u;"),
+    "mxfp4_emax_8": ("code = floor_log2_f32(amax) - 2 + 127;", "code = floor_log2_f32(amax) - 8 + 127;"),
+    "mxfp4_nibbles_swapped": ("qb[h / 2] = (uint8_t)(lo | (hi << 4));", "qb[h / 2] = (uint8_t)(hi | (lo << 4));"),
+    "e2m1_saturates_to_4": ("if (!(a < 6.0)) return (uint8_t)(sign | 7u);", "if (!(a < 6.0)) return (uint8_t)(sign | 6u);"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
 }
