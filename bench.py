@@ -267,7 +267,7 @@ def config_block(name, inp):
 # the other rows of the path on their own workloads (device-timed)
 # ---------------------------------------------------------------------------
 def measure_other_rows(steps: int, peak: float):
-    """The rows besides the dsv3 step: in-kernel quantise-dispatch (e4m3 and MXFP8) of
+    """The rows besides the dsv3 step: in-kernel quantise-dispatch (e4m3, MXFP8, MXFP4) of
     the dsv3 rows; e4m3 dispatch (R=8, N=8192, H=7168, per-128-channel fp32 scales,
     top-8 of 256) with its bf16 combine; reduce-scatterv / all-gatherv (R=8, H=4096,
     per-rank rows U{0..16384}) and the all-gatherv with quantisation fused in; the
@@ -324,6 +324,14 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_mx, R * N * H * 2 + T * (H + H // 32) + R * N * R * 4),
         workload="dsv3 rows quantised in-kernel: bf16 in, MXFP8 (e4m3 + UE8M0 byte per 32 "
                  "channels) out")
+    rq4 = torch.empty((plan.cap, H // 2), dtype=torch.uint8, device="cuda")
+    ms_m4 = timed(lambda: B.check(B.mp_dispatch_rows_mxfp4(R, N, H, plan.x, plan.send_row,
+                                                           plan.cap, rq4, rc)), steps)
+    out["dispatch_rows_quantise_mxfp4"] = dict(
+        row(ms_m4, R * N * H * 2 + T * (H // 2 + H // 32) + R * N * R * 4),
+        workload="dsv3 rows quantised in-kernel: bf16 in, MXFP4 (two e2m1 codes per byte + "
+                 "UE8M0 byte per 32 channels) out")
+    del rq4
     # global expert ids with a sentinel (the same scan) and the combined top-k weights
     gids = torch.empty_like(plan.recv_topk_idx)
     ms_g = timed(lambda: B.check(B.mp_dispatch_offsets_global(
@@ -396,6 +404,13 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_agm, S * Hh * 2 + Rr * S * (Hh + Hh // 32)),
         workload="rsv shards quantised once (MXFP8, UE8M0 byte per 32 channels), gathered "
                  "to 8 ranks")
+    qx4 = torch.empty((Rr, S, Hh // 2), dtype=torch.uint8, device="cuda")
+    ms_ag4 = timed(lambda: B.check(B.mp_allgatherv_mxfp4(Rr, Hh, sizes, rp.shards, qx4, qc)),
+                   max(5, steps // 4))
+    out["allgatherv_quantise_mxfp4"] = dict(
+        row(ms_ag4, S * Hh * 2 + Rr * S * (Hh // 2 + Hh // 32)),
+        workload="rsv shards quantised once (MXFP4), gathered to 8 ranks")
+    del qx4
     # multi-tensor all-gatherv: e4m3 data and its fp32 scales in one launch
     del qc
     qd = torch.randint(0, 256, (S, Hh), generator=g, device="cuda", dtype=torch.uint8)

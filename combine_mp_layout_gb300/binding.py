@@ -72,12 +72,15 @@ def lib() -> ctypes.CDLL:
         L.mp_allgatherv.argtypes = [i32, i64, P, P, P, P]
         L.mp_allgatherv_e4m3.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_allgatherv_mxfp8.argtypes = [i32, i32, P, P, P, P, P]
+        L.mp_allgatherv_mxfp4.argtypes = [i32, i32, P, P, P, P, P]
+        L.mp_dispatch_rows_mxfp4.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
                   "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
-                  "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8"):
+                  "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
+                  "mp_dispatch_rows_mxfp4"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -208,6 +211,13 @@ def mp_dispatch_rows_mxfp8(R, N, H, x, send_row, recv_capacity, recv_x, recv_sca
                                         _dev(recv_scales, "recv_scales"), _stream(stream))
 
 
+def mp_dispatch_rows_mxfp4(R, N, H, x, send_row, recv_capacity, recv_x, recv_scales,
+                           stream=None) -> int:
+    return lib().mp_dispatch_rows_mxfp4(R, N, H, _dev(x, "x"), _dev(send_row, "send_row"),
+                                        int(recv_capacity), _dev(recv_x, "recv_x"),
+                                        _dev(recv_scales, "recv_scales"), _stream(stream))
+
+
 def mp_combine(R, N, H, y, y_rows, send_row, out, dev_err, stream=None) -> int:
     return lib().mp_combine(R, N, H, _dev(y, "y"), int(y_rows), _dev(send_row, "send_row"),
                             _dev(out, "out"), _dev(dev_err, "dev_err"), _stream(stream))
@@ -235,6 +245,11 @@ def mp_allgatherv_e4m3(R, H, sizes, inp, out, out_scales, stream=None) -> int:
 
 def mp_allgatherv_mxfp8(R, H, sizes, inp, out, out_scales, stream=None) -> int:
     return lib().mp_allgatherv_mxfp8(R, H, _host_sizes(sizes), _dev(inp, "in"), _dev(out, "out"),
+                                     _dev(out_scales, "out_scales"), _stream(stream))
+
+
+def mp_allgatherv_mxfp4(R, H, sizes, inp, out, out_scales, stream=None) -> int:
+    return lib().mp_allgatherv_mxfp4(R, H, _host_sizes(sizes), _dev(inp, "in"), _dev(out, "out"),
                                      _dev(out_scales, "out_scales"), _stream(stream))
 
 

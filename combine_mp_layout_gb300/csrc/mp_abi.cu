@@ -241,6 +241,20 @@ int mp_dispatch_rows_mxfp8(int R, int N, int H, const void* x, const int32_t* se
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int mp_dispatch_rows_mxfp4(int R, int N, int H, const void* x, const int32_t* send_row,
+                           int64_t recv_capacity, void* recv_x, uint8_t* recv_scales,
+                           mp_stream_t stream) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || H % 32 != 0 || recv_capacity < 0)
+    return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !send_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && (!recv_x || !recv_scales)) return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned4(send_row)) return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch_quant(R, int64_t(R) * N, H, x, recv_x, recv_scales, 2,
+                                           recv_capacity, send_row,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mp_dispatch(int R, int N, int K, int E, int H, int dtype, const void* x, const float* x_scales,
                 const int32_t* topk_idx, const float* topk_weights,
                 const uint32_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
@@ -309,7 +323,7 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t* sizes, const void* in
 }
 
 static int allgatherv_quant(int R, int H, int block, const int64_t* sizes, const void* in,
-                            void* out, void* out_scales, int mx, mp_stream_t stream) {
+                            void* out, void* out_scales, int fmt, mp_stream_t stream) {
   if (R < 1 || R > MP_MAX_RANKS || H <= 0 || H % block != 0 || !sizes) return MP_ERR_INVALID_ARG;
   int64_t S = 0;
   for (int r = 0; r < R; ++r) {
@@ -317,9 +331,9 @@ static int allgatherv_quant(int R, int H, int block, const int64_t* sizes, const
     S += sizes[r];
   }
   if (S > 0 && (!in || !out || !out_scales || !aligned16(in) || !aligned16(out) ||
-                (!mx && !aligned4(out_scales))))
+                (fmt == 0 && !aligned4(out_scales))))
     return MP_ERR_INVALID_ARG;
-  return cuda_status(launch_allgatherv_quant(R, S, H, in, out, out_scales, mx,
+  return cuda_status(launch_allgatherv_quant(R, S, H, in, out, out_scales, fmt,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -331,6 +345,11 @@ int mp_allgatherv_e4m3(int R, int H, const int64_t* sizes, const void* in, void*
 int mp_allgatherv_mxfp8(int R, int H, const int64_t* sizes, const void* in, void* out,
                         uint8_t* out_scales, mp_stream_t stream) {
   return allgatherv_quant(R, H, 32, sizes, in, out, out_scales, 1, stream);
+}
+
+int mp_allgatherv_mxfp4(int R, int H, const int64_t* sizes, const void* in, void* out,
+                        uint8_t* out_scales, mp_stream_t stream) {
+  return allgatherv_quant(R, H, 32, sizes, in, out, out_scales, 2, stream);
 }
 
 int mp_allgatherv_multi(int R, int ntensors, const int64_t* row_bytes, const int64_t* sizes,

@@ -271,35 +271,53 @@ mp_k_dispatch_tma(int R, int64_t tokens, int64_t row_bytes, uint32_t piece_bytes
 }
 
 // ---------------------------------------------------------------------------
-// Row copies with in-kernel FP8 quantisation.
-//
-// [EP] (the FP8 commits of "MSCCLPP EP implementation"): E4M3 payloads with
-// FP32 scales.  Each 128-channel block of a bf16 row gets scale = amax / 448
-// (1 when the block is all zero) and codes e4m3_rn_satfinite(x / scale).
-// MXFP8 (MX = true; the same page's later commits: E4M3 with one UE8M0 scale
-// byte per 32 channels, tiny non-zero blocks kept at code zero): code =
-// clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an all-zero block),
-// X = 2^(code - 127), element codes e4m3(x / X).  Dividing by a power of two
-// and multiplying by its (exactly representable) reciprocal round the same
-// real number once, so MX multiplies by 2^(127 - code).
+// Row copies with in-kernel quantisation.  Formats (FMT):
+//  kQE4M3 -- [EP] (the FP8 commits of "MSCCLPP EP implementation"): E4M3
+//    payloads with FP32 scales.  Each 128-channel block of a bf16 row gets
+//    scale = amax / 448 (1 when the block is all zero) and codes
+//    e4m3_rn_satfinite(x / scale).
+//  kQMXFP8 -- the same page's later commits: E4M3 with one UE8M0 scale byte
+//    per 32 channels, tiny non-zero blocks kept at code zero: code =
+//    clamp(floor(log2 amax) - 8 + 127, 0, 254) (0 for an all-zero block),
+//    X = 2^(code - 127), element codes e4m3(x / X).
+//  kQMXFP4 -- [AGV] (the review note that gathering a list of tensors lets a
+//    caller quantise to fp4 before the all-gather), in the same microscaling
+//    form with E2M1 elements: code = clamp(floor(log2 amax) - 2 + 127, 0,
+//    254), element codes e2m1_rn_satfinite(x / X) (magnitudes 0, 0.5, 1,
+//    1.5, 2, 3, 4, 6; sign kept, also on a zero), two per byte with the
+//    even channel in the low nibble.
+// Dividing by a power of two and multiplying by its (exactly representable)
+// reciprocal round the same real number once, so the microscaling formats
+// multiply by 2^(127 - code).
 //
 // Destinations.  Dispatch (GATHER = false): token `tok`'s destinations are
 // send_row[tok][d] for d < R, skipped when negative or >= `limit` (the receive
 // capacity).  Gather (GATHER = true; [AGV] "Add pynccl all-gatherv and
-// reducescatterv", the note that gathering a list of tensors lets a caller
-// quantise before the all-gather): `limit` = S and logical rank q receives
-// row tok at q * S + tok, so one launch quantises each row once and writes
-// codes and scales R times.
+// reducescatterv"): `limit` = S and logical rank q receives row tok at
+// q * S + tok, so one launch quantises each row once and writes codes and
+// scales R times.
 //
 // A lane holds CPL channels (CPL = 8: one 16-byte load; 16: one 32-byte load)
-// and stores CPL code bytes per destination; kBlock / CPL lanes share a scale.
-// Each row is read once as bf16 and written as 1 byte per channel per
-// destination, roughly half the traffic of a bf16 copy.
+// and stores CPL (FP8) or CPL / 2 (FP4) code bytes per destination;
+// kBlock / CPL lanes share a scale.  Each row is read once as bf16 and written
+// as 1 (FP8) or 1/2 (FP4) byte per channel per destination.
 // ---------------------------------------------------------------------------
+enum QuantFormat { kQE4M3 = 0, kQMXFP8 = 1, kQMXFP4 = 2 };
+
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two E2M1 codes in one byte: `hi` in bits 4-7, `lo` in bits 0-3; each sign
+// bit is set from its input, so a negative value that rounds to zero is -0.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r | ((__float_as_uint(hi) >> 31) << 7) | ((__float_as_uint(lo) >> 31) << 3);
 }
 
 __device__ __forceinline__ int floor_log2_pos(float a) {  // a > 0, finite
@@ -315,25 +333,32 @@ __device__ __forceinline__ void st_codes(unsigned char* p, const uint32_t (&w)[N
     asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3])
                  : "memory");
-  } else {
-    static_assert(NB == 2, "8 or 16 code bytes per lane");
+  } else if constexpr (NB == 2) {
     asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]), "r"(w[1])
                  : "memory");
+  } else {
+    static_assert(NB == 1, "4, 8 or 16 code bytes per lane");
+    asm volatile("st.global.L1::no_allocate.b32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
   }
 }
 
-template <int CPL, int U, bool MX, bool GATHER>
+template <int CPL, int U, int FMT, bool GATHER>
 __global__ void __launch_bounds__(kCopyThreads)
 mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
                 unsigned char* __restrict__ out, void* __restrict__ out_scales, int64_t limit,
                 const int32_t* __restrict__ send_row) {
-  constexpr int kBlock = MX ? 32 : 128;  // channels per scale
-  constexpr int kLanes = kBlock / CPL;   // lanes per scale block
-  constexpr int NW = CPL / 2;            // 32-bit words of bf16 per lane
-  constexpr int NB = CPL / 4;            // 32-bit words of codes per lane
+  constexpr bool MX = FMT != kQE4M3;
+  constexpr bool FP4 = FMT == kQMXFP4;
+  constexpr int kBlock = MX ? 32 : 128;      // channels per scale
+  constexpr int kLanes = kBlock / CPL;       // lanes per scale block
+  constexpr int kEmax = FP4 ? 2 : 8;         // exponent of the element format's largest normal
+  constexpr int NW = CPL / 2;                // 32-bit words of bf16 per lane
+  constexpr int NB = FP4 ? CPL / 8 : CPL / 4;  // 32-bit words of codes per lane
+  constexpr int kCodeBytes = NB * 4;
   static_assert(kLanes >= 1 && kLanes <= 32, "scale block spans whole lanes");
   const int lane = threadIdx.x & 31;
   const int64_t vpr = H / CPL;  // lane vectors per row
+  const int64_t row_bytes = FP4 ? H / 2 : H;
   const int nb = H / kBlock;    // scales per row
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
@@ -378,7 +403,7 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
       for (int o = kLanes / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
       if constexpr (MX) {
         int c = 0;
-        if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - 8 + 127));
+        if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - kEmax + 127));
         sbits[u] = uint32_t(c);
         // 2^(127 - c): biased exponent 254 - c, or the subnormal 2^-127 at c = 254
         const float inv = c < 254 ? __uint_as_float(uint32_t(254 - c) << 23)
@@ -386,10 +411,21 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
         if (valid) {
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
-            const uint32_t lo = cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
-            const uint32_t hi =
-                cvt_e4m3x2(__fmul_rn(f[4 * j + 3], inv), __fmul_rn(f[4 * j + 2], inv));
-            q[u][j] = lo | (hi << 16);
+            if constexpr (FP4) {  // 8 channels -> 4 bytes
+              uint32_t w = 0;
+#pragma unroll
+              for (int b = 0; b < 4; ++b)
+                w |= cvt_e2m1x2(__fmul_rn(f[8 * j + 2 * b + 1], inv),
+                                __fmul_rn(f[8 * j + 2 * b], inv))
+                     << (8 * b);
+              q[u][j] = w;
+            } else {  // 4 channels -> 4 bytes
+              const uint32_t lo =
+                  cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
+              const uint32_t hi =
+                  cvt_e4m3x2(__fmul_rn(f[4 * j + 3], inv), __fmul_rn(f[4 * j + 2], inv));
+              q[u][j] = lo | (hi << 16);
+            }
           }
         }
       } else {
@@ -413,7 +449,7 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
       for (int u = 0; u < U; ++u) {
         const int64_t i = i0 + u * kWarp;
         if (i < vpr) {
-          st_codes<NB>(out + row * H + i * CPL, q[u]);
+          st_codes<NB>(out + row * row_bytes + i * kCodeBytes, q[u]);
           if ((lane & (kLanes - 1)) == 0) {
             if constexpr (MX)
               static_cast<unsigned char*>(out_scales)[row * nb + i / kLanes] = uint8_t(sbits[u]);
@@ -754,62 +790,78 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
 //  - 2 vectors per lane and unit, except 1 for the e4m3 gather (276 vs
 //    285 us);
 //  - one short block per kWarpsPerBlock units (the write-heavy policy above)
-//    for MXFP8 dispatch (260 vs 296 us) and both gathers (276-285 vs 321 us),
-//    but a persistent grid for the e4m3 dispatch, whose fp32 division per
-//    element makes it the most compute-heavy (279 vs 296 us).
-// MP_QUANT_CPL = 8 and MP_QUANT_FULL_MASK (bit (GATHER ? 2 : 0) + (MX ? 1 : 0)
-// set = short blocks) reproduce the other shapes for measurement.
+//    for the microscaling dispatches (MXFP8: 260 vs 296 us) and every gather
+//    (276-285 vs 321 us), but a persistent grid for the e4m3 dispatch, whose
+//    fp32 division per element makes it the most compute-heavy (279 vs
+//    296 us).
+// MP_QUANT_CPL = 8 and MP_QUANT_PERSISTENT_MASK (bit FMT + (GATHER ? 3 : 0)
+// set = persistent grid) reproduce the other shapes for measurement.
 #ifndef MP_QUANT_CPL
 #define MP_QUANT_CPL 16
 #endif
-#ifndef MP_QUANT_FULL_MASK
-#define MP_QUANT_FULL_MASK 14
+#ifndef MP_QUANT_PERSISTENT_MASK
+#define MP_QUANT_PERSISTENT_MASK 1
 #endif
 
-template <int CPL, int U, bool MX, bool GATHER>
+template <int CPL, int U, int FMT, bool GATHER>
 static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void* out,
                               void* out_scales, int64_t limit, const int32_t* send_row,
                               cudaStream_t stream) {
-  auto kernel = mp_k_quant_rows<CPL, U, MX, GATHER>;
+  auto kernel = mp_k_quant_rows<CPL, U, FMT, GATHER>;
   static const int per_sm = resident_blocks(kernel);
   const int64_t vpr = H / CPL;
   const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
-  constexpr bool full = (MP_QUANT_FULL_MASK >> ((GATHER ? 2 : 0) + (MX ? 1 : 0))) & 1;
-  const unsigned grid = full ? grid_full(kWarpsPerBlock, tokens * slabs)
-                             : grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
+  constexpr bool persistent = (MP_QUANT_PERSISTENT_MASK >> (FMT + (GATHER ? 3 : 0))) & 1;
+  const unsigned grid = persistent ? grid_for(per_sm, kWarpsPerBlock, tokens * slabs)
+                                   : grid_full(kWarpsPerBlock, tokens * slabs);
   return launch_kernel(kernel, dim3(grid), dim3(kCopyThreads), 0, stream, R, tokens, H,
                        static_cast<const uint16_t*>(x), static_cast<unsigned char*>(out),
                        out_scales, limit, send_row);
 }
 
-template <bool MX, bool GATHER>
+template <int FMT, bool GATHER>
 static cudaError_t quant_rows_any(int R, int64_t tokens, int H, const void* x, void* out,
                                   void* out_scales, int64_t limit, const int32_t* send_row,
                                   cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  constexpr int U = (GATHER && !MX) ? 1 : 2;  // vectors per lane at 16 channels per lane
+  constexpr int U = (GATHER && FMT == kQE4M3) ? 1 : 2;  // vectors per lane at 16 channels
   if constexpr (MP_QUANT_CPL == 16) {
     if (aligned(x, 32))
-      return quant_rows<16, U, MX, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
-                                           stream);
+      return quant_rows<16, U, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
+                                            stream);
   }
-  return quant_rows<8, 2 * U, MX, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
-                                          stream);
+  return quant_rows<8, 2 * U, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
+                                           stream);
 }
 
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
-                                  void* recv_scales, int mx, int64_t recv_capacity,
+                                  void* recv_scales, int fmt, int64_t recv_capacity,
                                   const int32_t* send_row, cudaStream_t stream) {
-  return mx ? quant_rows_any<true, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
-                                          send_row, stream)
-            : quant_rows_any<false, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
+  switch (fmt) {
+    case kQE4M3:
+      return quant_rows_any<kQE4M3, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
                                            send_row, stream);
+    case kQMXFP8:
+      return quant_rows_any<kQMXFP8, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
+                                            send_row, stream);
+    case kQMXFP4:
+      return quant_rows_any<kQMXFP4, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
+                                            send_row, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_allgatherv_quant(int R, int64_t S, int H, const void* in, void* out,
-                                    void* out_scales, int mx, cudaStream_t stream) {
-  return mx ? quant_rows_any<true, true>(R, S, H, in, out, out_scales, S, nullptr, stream)
-            : quant_rows_any<false, true>(R, S, H, in, out, out_scales, S, nullptr, stream);
+                                    void* out_scales, int fmt, cudaStream_t stream) {
+  switch (fmt) {
+    case kQE4M3:
+      return quant_rows_any<kQE4M3, true>(R, S, H, in, out, out_scales, S, nullptr, stream);
+    case kQMXFP8:
+      return quant_rows_any<kQMXFP8, true>(R, S, H, in, out, out_scales, S, nullptr, stream);
+    case kQMXFP4:
+      return quant_rows_any<kQMXFP4, true>(R, S, H, in, out, out_scales, S, nullptr, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int NW, int U, int RB, bool W>

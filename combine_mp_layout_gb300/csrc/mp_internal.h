@@ -48,11 +48,12 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                  int scales_per_row,
                                  const float* x_scales, float* recv_scales, cudaStream_t stream);
 
-// Quantises bf16 token rows to e4m3 -- one fp32 scale per 128 channels (mx = 0)
-// or one UE8M0 byte per 32 channels (mx = 1) -- and copies them to every
-// receive row listed in send_row.
+// Quantises bf16 token rows -- fmt 0: e4m3 with one fp32 scale per 128
+// channels; 1: MXFP8 (e4m3, one UE8M0 byte per 32 channels); 2: MXFP4 (two
+// e2m1 codes per byte, one UE8M0 byte per 32 channels) -- and copies them to
+// every receive row listed in send_row.
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
-                                  void* recv_scales, int mx, int64_t recv_capacity,
+                                  void* recv_scales, int fmt, int64_t recv_capacity,
                                   const int32_t* send_row, cudaStream_t stream);
 
 cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
@@ -66,7 +67,7 @@ cudaError_t launch_reducescatterv(int R, int64_t S, int H, const void* in, void*
 // launch_dispatch_quant) and writes codes and scales to all R logical ranks'
 // copies: out[q][i] and out_scales[q][i] for q < R.
 cudaError_t launch_allgatherv_quant(int R, int64_t S, int H, const void* in, void* out,
-                                    void* out_scales, int mx, cudaStream_t stream);
+                                    void* out_scales, int fmt, cudaStream_t stream);
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream);
 

@@ -257,6 +257,26 @@ int mp_dispatch_rows_mxfp8(int R, int N, int H, const void *x, const int32_t *se
                            mp_stream_t stream);
 
 /*
+ * mp_dispatch_rows_mxfp4 -- the row copy with in-kernel MXFP4 quantisation
+ * ([AGV] the review note that a list all-gather lets the caller quantise to
+ * fp4 first; the pages name no fp4 format, so the microscaling form of the
+ * MXFP8 scheme above is used with E2M1 elements): per block of 32 channels,
+ * code = clamp(floor(log2 amax) - 2 + 127, 0, 254) (0 for an all-zero
+ * block), X = 2^(code - 127); each element is e2m1(x / X), round-to-nearest-
+ * even over the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (saturating at 6; the
+ * sign bit is kept, also on a zero), bit 3 the sign.
+ *   in   x           bf16 [R][N][H], H % 32 == 0
+ *   out  recv_x      uint8 [recv_capacity][H/2]: byte j of a row holds channel
+ *                    2j in bits 0-3 and channel 2j+1 in bits 4-7
+ *   out  recv_scales uint8 [recv_capacity][H/32]: the UE8M0 codes
+ * Dequantised x is element * 2^(code - 127).  Checks as mp_dispatch_rows_mxfp8.
+ * No device errors.
+ */
+int mp_dispatch_rows_mxfp4(int R, int N, int H, const void *x, const int32_t *send_row,
+                           int64_t recv_capacity, void *recv_x, uint8_t *recv_scales,
+                           mp_stream_t stream);
+
+/*
  * mp_combine -- [EP] intranode_combine, the reverse of dispatch.
  *   in   y        bf16 [y_rows][H]: one row per receive row (for example the
  *                 expert outputs, or recv_x itself)
@@ -341,7 +361,7 @@ int mp_dispatch_noalloc(int R, int N, int K, int E, int H, int dtype, const void
                         int32_t *dev_err, mp_stream_t stream);
 
 /*
- * mp_allgatherv_e4m3 / mp_allgatherv_mxfp8 -- [AGV] all-gatherv with the
+ * mp_allgatherv_e4m3 / _mxfp8 / _mxfp4 -- [AGV] all-gatherv with the
  * quantisation fused in (the page's note that gathering a list of tensors
  * lets a caller quantise before the all-gather; here data and scales leave
  * one launch together).  Each bf16 row of `in` is quantised once, exactly as
@@ -362,6 +382,10 @@ int mp_dispatch_noalloc(int R, int N, int K, int E, int H, int dtype, const void
 int mp_allgatherv_e4m3(int R, int H, const int64_t *sizes, const void *in, void *out,
                        float *out_scales, mp_stream_t stream);
 int mp_allgatherv_mxfp8(int R, int H, const int64_t *sizes, const void *in, void *out,
+                        uint8_t *out_scales, mp_stream_t stream);
+/* The same with MXFP4 (as mp_dispatch_rows_mxfp4): out uint8 [R][S][H/2],
+ * out_scales uint8 [R][S][H/32]. */
+int mp_allgatherv_mxfp4(int R, int H, const int64_t *sizes, const void *in, void *out,
                         uint8_t *out_scales, mp_stream_t stream);
 
 /*

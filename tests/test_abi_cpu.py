@@ -180,6 +180,12 @@ def test_newer_entry_points_reject(L):
     assert L.mp_allgatherv_e4m3(2, 128, sizes, P, P, _p(FAKE + 2), N0) == B.MP_ERR_INVALID_ARG
     assert L.mp_allgatherv_mxfp8(2, 48, sizes, P, P, P, N0) == B.MP_ERR_INVALID_ARG    # H % 32
     assert L.mp_allgatherv_mxfp8(2, 64, sizes, P, N0, P, N0) == B.MP_ERR_INVALID_ARG   # out NULL
+    L.mp_allgatherv_mxfp4.argtypes = L.mp_allgatherv_e4m3.argtypes
+    assert L.mp_allgatherv_mxfp4(2, 80, sizes, P, P, P, N0) == B.MP_ERR_INVALID_ARG    # H % 32
+    assert L.mp_allgatherv_mxfp4(2, 64, sizes, _p(FAKE + 8), P, P, N0) == B.MP_ERR_INVALID_ARG
+    L.mp_dispatch_rows_mxfp4.argtypes = L.mp_dispatch_rows_e4m3.argtypes
+    assert L.mp_dispatch_rows_mxfp4(2, 8, 48, P, P, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # H % 32
+    assert L.mp_dispatch_rows_mxfp4(2, 8, 64, P, N0, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # send_row
     neg = (ctypes.c_int64 * 2)(3, -1)
     assert L.mp_allgatherv_mxfp8(2, 64, neg, P, P, P, N0) == B.MP_ERR_INVALID_ARG      # size < 0
     L.mp_dispatch_noalloc.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + \

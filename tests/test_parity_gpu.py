@@ -301,6 +301,31 @@ def test_dispatch_rows_mxfp8_quantises_like_the_oracle(shape):
     assert np.array_equal(rc[:n].cpu().numpy(), out["recv_x"][:, H:])
 
 
+@pytest.mark.parametrize("shape", [(4, 300, 16, 4, 96), (8, 4096, 256, 8, 7168)],
+                         ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
+def test_dispatch_rows_mxfp4_quantises_like_the_oracle(shape):
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=H + 2)
+    inp.x = _special_blocks(inp.x.reshape(R * N, H), 32).reshape(R, N, H)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    rq = torch.zeros((plan.cap, H // 2), dtype=torch.uint8, device="cuda")
+    rc = torch.zeros((plan.cap, H // 32), dtype=torch.uint8, device="cuda")
+    B.check(B.mp_dispatch_rows_mxfp4(R, N, H, plan.x, plan.send_row, plan.cap, rq, rc))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    q, codes = _oracle_quant("mxfp4", inp.x)
+    payload = np.concatenate([q, codes], axis=-1)
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    out, st2 = oracle.dispatch(payload, inp.topk_idx, inp.topk_weights, mask, E)
+    assert st2 == 0
+    n = out["num_recv"]
+    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"][:, :H // 2])
+    assert np.array_equal(rc[:n].cpu().numpy(), out["recv_x"][:, H // 2:])
+
+
 def test_empty_tokens():
     inp = wl.make_ep(dict(R=4, N=0, E=16, K=2, H=64, routing="uniform", dtype="bf16"))
     plan = run_gpu(inp)
@@ -469,28 +494,43 @@ def _special_blocks(x: torch.Tensor, block: int) -> torch.Tensor:
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+# Quantised formats: scale block, code bytes per row, scale dtype, the gather and
+# dispatch entry points, and the oracle's quantiser (codes, scales, status).
+QFMT = {
+    "e4m3": dict(block=128, qcols=lambda H: H, sdt=torch.float32,
+                 gather="mp_allgatherv_e4m3", disp="mp_dispatch_rows_e4m3", quant="quantize_e4m3"),
+    "mxfp8": dict(block=32, qcols=lambda H: H, sdt=torch.uint8,
+                  gather="mp_allgatherv_mxfp8", disp="mp_dispatch_rows_mxfp8",
+                  quant="quantize_mxfp8"),
+    "mxfp4": dict(block=32, qcols=lambda H: H // 2, sdt=torch.uint8,
+                  gather="mp_allgatherv_mxfp4", disp="mp_dispatch_rows_mxfp4",
+                  quant="quantize_mxfp4"),
+}
+
+
+def _oracle_quant(fmt: str, x: torch.Tensor):
+    """Oracle codes and scales (scales as raw bytes) of bf16 rows."""
+    q, sc, st = getattr(oracle, QFMT[fmt]["quant"])(wl.bf16_bits(x))
+    assert st == 0
+    return q, sc.view(np.uint8)
+
+
+@pytest.mark.parametrize("fmt", sorted(QFMT))
 @pytest.mark.parametrize("R,H,sizes", [(5, 256, [7, 0, 130, 1, 33]), (1, 128, [3]),
                                        (32, 128, [1] * 32), (3, 384, [0, 0, 0])],
                          ids=["R5_ragged", "R1", "R32", "empty"])
 def test_allgatherv_quantised_equals_quantise_then_gather(fmt, R, H, sizes):
+    f = QFMT[fmt]
     S = sum(sizes)
-    blk = 128 if fmt == "e4m3" else 32
     x = wl.random_bf16((max(S, 1), H), seed=R * H)[:S]
     if S:
-        x = _special_blocks(x, blk)
-    out = torch.full((R, S, H), 0x5A, dtype=torch.uint8, device="cuda")
-    if fmt == "e4m3":
-        osc = torch.full((R, S, H // 128), -1.0, dtype=torch.float32, device="cuda")
-        B.check(B.mp_allgatherv_e4m3(R, H, sizes, x.cuda(), out, osc))
-        q, sc, st = oracle.quantize_e4m3(wl.bf16_bits(x))
-        sc = sc.view(np.uint8)
-    else:
-        osc = torch.full((R, S, H // 32), 0x5A, dtype=torch.uint8, device="cuda")
-        B.check(B.mp_allgatherv_mxfp8(R, H, sizes, x.cuda(), out, osc))
-        q, sc, st = oracle.quantize_mxfp8(wl.bf16_bits(x))
+        x = _special_blocks(x, f["block"])
+    out = torch.full((R, S, f["qcols"](H)), 0x5A, dtype=torch.uint8, device="cuda")
+    osc = torch.zeros((R, S, H // f["block"]), dtype=f["sdt"], device="cuda")
+    osc.view(torch.uint8).fill_(0x5A)
+    B.check(getattr(B, f["gather"])(R, H, sizes, x.cuda(), out, osc))
     torch.cuda.synchronize()
-    assert st == 0
+    q, sc = _oracle_quant(fmt, x)
     want_q, st1 = oracle.allgatherv(q, sizes, R)
     want_s, st2 = oracle.allgatherv(sc, sizes, R)
     assert st1 == st2 == 0
@@ -509,72 +549,62 @@ def _offset_16(t: torch.Tensor) -> torch.Tensor:
     return out
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+@pytest.mark.parametrize("fmt", sorted(QFMT))
 def test_quantising_copies_from_a_16_byte_aligned_source(fmt):
     """Sources that are 16- but not 32-byte aligned take the 8-channels-per-lane form."""
+    f = QFMT[fmt]
     R, N, E, K, H = 4, 300, 16, 4, 384
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=77)
-    inp.x = _special_blocks(inp.x.reshape(R * N, H), 128 if fmt == "e4m3" else 32).reshape(R, N, H)
+    inp.x = _special_blocks(inp.x.reshape(R * N, H), f["block"]).reshape(R, N, H)
     plan = EPPlan(R, N, K, E, H)
     plan.load(inp)
     B.check(plan.layout())
     B.check(plan.dispatch_offsets())
     xo = _offset_16(plan.x)
-    nsc = H // 128 if fmt == "e4m3" else H // 32
-    sdt = torch.float32 if fmt == "e4m3" else torch.uint8
-    rq = torch.zeros((plan.cap, H), dtype=torch.uint8, device="cuda")
-    rs = torch.zeros((plan.cap, nsc), dtype=sdt, device="cuda")
-    f = B.mp_dispatch_rows_e4m3 if fmt == "e4m3" else B.mp_dispatch_rows_mxfp8
-    B.check(f(R, N, H, xo, plan.send_row, plan.cap, rq, rs))
+    nsc = H // f["block"]
+    rq = torch.zeros((plan.cap, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    rs = torch.zeros((plan.cap, nsc), dtype=f["sdt"], device="cuda")
+    B.check(getattr(B, f["disp"])(R, N, H, xo, plan.send_row, plan.cap, rq, rs))
     sizes = [5, 0, 17]
     S = sum(sizes)
     sh = _offset_16(plan.x.reshape(R * N, H)[:S])
-    gq = torch.zeros((3, S, H), dtype=torch.uint8, device="cuda")
-    gs = torch.zeros((3, S, nsc), dtype=sdt, device="cuda")
-    g = B.mp_allgatherv_e4m3 if fmt == "e4m3" else B.mp_allgatherv_mxfp8
-    B.check(g(3, H, sizes, sh, gq, gs))
+    gq = torch.zeros((3, S, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((3, S, nsc), dtype=f["sdt"], device="cuda")
+    B.check(getattr(B, f["gather"])(3, H, sizes, sh, gq, gs))
     torch.cuda.synchronize()
-    quant = oracle.quantize_e4m3 if fmt == "e4m3" else oracle.quantize_mxfp8
-    q, sc, st = quant(wl.bf16_bits(inp.x))
-    assert st == 0
-    payload = np.concatenate([q, sc.view(np.uint8)], axis=-1)
+    q, sc = _oracle_quant(fmt, inp.x)
+    payload = np.concatenate([q, sc], axis=-1)
     _, _, mask, _ = oracle.layout(inp.topk_idx, E)
     out, st2 = oracle.dispatch(payload, inp.topk_idx, inp.topk_weights, mask, E)
     assert st2 == 0
     n = out["num_recv"]
-    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"][:, :H])
-    assert np.array_equal(rs[:n].cpu().view(torch.uint8).numpy(), out["recv_x"][:, H:])
-    flat_q, flat_s = q.reshape(R * N, H)[:S], sc.view(np.uint8).reshape(R * N, -1)[:S]
+    qc = f["qcols"](H)
+    assert np.array_equal(rq[:n].cpu().numpy(), out["recv_x"][:, :qc])
+    assert np.array_equal(rs[:n].cpu().view(torch.uint8).numpy(), out["recv_x"][:, qc:])
+    flat_q, flat_s = q.reshape(R * N, -1)[:S], sc.reshape(R * N, -1)[:S]
     for r in range(3):
         assert np.array_equal(gq[r].cpu().numpy(), flat_q)
         assert np.array_equal(gs[r].cpu().view(torch.uint8).numpy(), flat_s)
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8"])
+@pytest.mark.parametrize("fmt", sorted(QFMT))
 def test_allgatherv_quantised_full_size(fmt):
     """The rsv shape (R=8, H=4096, sizes ~ U{0..16384}): every rank's copy equals the
     oracle's quantisation of the gathered rows."""
+    f = QFMT[fmt]
     rsv = wl.CONFIGS["rsv"]
     R, H = rsv["R"], rsv["H"]
     sizes = np.random.default_rng(0).integers(0, rsv["max_rows"] + 1, size=R).tolist()
     S = sum(sizes)
-    blk = 128 if fmt == "e4m3" else 32
-    x = _special_blocks(wl.gathered_bf16(S, H, seed=3), blk)
-    out = torch.zeros((R, S, H), dtype=torch.uint8, device="cuda")
-    if fmt == "e4m3":
-        osc = torch.zeros((R, S, H // 128), dtype=torch.float32, device="cuda")
-        B.check(B.mp_allgatherv_e4m3(R, H, sizes, x.cuda(), out, osc))
-        q, sc, st = oracle.quantize_e4m3(wl.bf16_bits(x))
-        sc = torch.from_numpy(sc.view(np.int32)).cuda()
-        osc = osc.view(torch.int32)
-    else:
-        osc = torch.zeros((R, S, H // 32), dtype=torch.uint8, device="cuda")
-        B.check(B.mp_allgatherv_mxfp8(R, H, sizes, x.cuda(), out, osc))
-        q, sc, st = oracle.quantize_mxfp8(wl.bf16_bits(x))
-        sc = torch.from_numpy(sc).cuda()
+    x = _special_blocks(wl.gathered_bf16(S, H, seed=3), f["block"])
+    out = torch.zeros((R, S, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    osc = torch.zeros((R, S, H // f["block"]), dtype=f["sdt"], device="cuda")
+    B.check(getattr(B, f["gather"])(R, H, sizes, x.cuda(), out, osc))
     torch.cuda.synchronize()
-    assert st == 0
+    q, sc = _oracle_quant(fmt, x)
     q = torch.from_numpy(q).cuda()
+    sc = torch.from_numpy(sc).cuda()
+    osc = osc.view(torch.uint8)
     for r in range(R):
         assert torch.equal(out[r], q), "rank %d codes" % r
         assert torch.equal(osc[r], sc), "rank %d scales" % r
