@@ -790,17 +790,22 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
 //  - 2 vectors per lane and unit, except 1 for the e4m3 gather (276 vs
 //    285 us);
 //  - one short block per kWarpsPerBlock units (the write-heavy policy above)
-//    for the microscaling dispatches (MXFP8: 260 vs 296 us) and every gather
-//    (276-285 vs 321 us), but a persistent grid for the e4m3 dispatch, whose
-//    fp32 division per element makes it the most compute-heavy (279 vs
-//    296 us).
-// MP_QUANT_CPL = 8 and MP_QUANT_PERSISTENT_MASK (bit FMT + (GATHER ? 3 : 0)
-// set = persistent grid) reproduce the other shapes for measurement.
+//    for the MXFP8 dispatch (260 vs 296 us) and every gather (MXFP4 173 vs
+//    199 us, the FP8 ones 276-285 vs 321 us), but a persistent grid for the
+//    e4m3 dispatch, whose fp32 division per element makes it the most
+//    compute-heavy (279 vs 296 us), and for the MXFP4 dispatch, whose reads
+//    are a larger share of its traffic (184 vs 191 us);
+//  - for MXFP4, 2 vectors per lane (190 us) beat 1 (211) and 4 (202).
+// MP_QUANT_CPL = 8, MP_QUANT_U_FP4 and MP_QUANT_PERSISTENT_MASK (bit
+// FMT + (GATHER ? 3 : 0) set = persistent grid) reproduce the other shapes.
 #ifndef MP_QUANT_CPL
 #define MP_QUANT_CPL 16
 #endif
 #ifndef MP_QUANT_PERSISTENT_MASK
-#define MP_QUANT_PERSISTENT_MASK 1
+#define MP_QUANT_PERSISTENT_MASK 5
+#endif
+#ifndef MP_QUANT_U_FP4
+#define MP_QUANT_U_FP4 2
 #endif
 
 template <int CPL, int U, int FMT, bool GATHER>
@@ -824,7 +829,7 @@ static cudaError_t quant_rows_any(int R, int64_t tokens, int H, const void* x, v
                                   void* out_scales, int64_t limit, const int32_t* send_row,
                                   cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  constexpr int U = (GATHER && FMT == kQE4M3) ? 1 : 2;  // vectors per lane at 16 channels
+  constexpr int U = (GATHER && FMT == kQE4M3) ? 1 : (FMT == kQMXFP4 ? MP_QUANT_U_FP4 : 2);
   if constexpr (MP_QUANT_CPL == 16) {
     if (aligned(x, 32))
       return quant_rows<16, U, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
