@@ -442,19 +442,16 @@ def measure_other_rows(steps: int, peak: float):
     yl = torch.randn((cap, H), generator=g, device="cuda").to(torch.bfloat16)
     lo = torch.empty((R, N, H), dtype=torch.bfloat16, device="cuda")
 
-    def ll_step():
-        B.check(plan.layout())
-        B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, plan.num_tokens_per_expert,
-                                         cap, eoff, esoff, src, slot, plan.dev_err))
+    def ll_step():  # the LL offsets count the experts themselves: no layout launch
+        B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff, esoff,
+                                         src, slot, plan.dev_err))
         B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
         B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
 
     ms_ll = timed(ll_step, steps)
     ll_calls = [
-        lambda: B.check(plan.layout()),
-        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx,
-                                                 plan.num_tokens_per_expert, cap, eoff, esoff,
-                                                 src, slot, plan.dev_err)),
+        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff,
+                                                 esoff, src, slot, plan.dev_err)),
         lambda: B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap,
                                               rx, None)),
         lambda: B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo,
@@ -468,7 +465,7 @@ def measure_other_rows(steps: int, peak: float):
             ev[c + 1].record()
     torch.cuda.synchronize()
     ll_phase_us = {name: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / steps * 1e3
-                   for c, name in enumerate(("layout", "ll_offsets", "ll_rows", "combine_ll"))}
+                   for c, name in enumerate(("ll_offsets", "ll_rows", "combine_ll"))}
     s_cap = torch.cuda.Stream()
     s_cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s_cap):
@@ -479,16 +476,15 @@ def measure_other_rows(steps: int, peak: float):
         ll_step()
     ms_llg = timed(graph.replay, steps)
     assert plan.device_error() == 0
-    ll_bytes = (algorithmic_bytes(R, N, K, E, H, 0)["layout"]
-                + R * N * K * 8 + cap * 4 + (E + 1) * 4 + E * R * 4   # LL offsets
+    ll_bytes = (R * N * K * 8 + cap * 4 + (E + 1) * 4 + E * R * 4  # LL offsets
                 + R * N * H * 2 + cap * H * 2 + R * N * K * 4           # LL rows
                 + cap * H * 2 + R * N * K * 8 + R * N * H * 2)          # weighted LL combine
     out["low_latency_step_n128"] = dict(
         row(ms_ll, ll_bytes), us_per_step=ms_ll * 1e3, us_per_step_cuda_graph=ms_llg * 1e3,
         phases_us=ll_phase_us, receive_rows=int(cap),
         GBs_cuda_graph=ll_bytes / (ms_llg / 1e3) / 1e9,
-        workload="R=8, N=128, H=7168 bf16, E=256, top-8: layout + LL offsets + LL rows + "
-                 "weighted LL combine (4 launches)")
+        workload="R=8, N=128, H=7168 bf16, E=256, top-8: LL offsets (counting the experts "
+                 "themselves) + LL rows + weighted LL combine (3 launches)")
     del plan, rx, yl, lo, graph
     torch.cuda.empty_cache()
 

@@ -376,8 +376,7 @@ int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                            int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                            mp_stream_t stream) {
   if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
-  if (!num_tokens_per_expert || !expert_offsets || !expert_src_offsets || !dev_err)
-    return MP_ERR_INVALID_ARG;
+  if (!expert_offsets || !expert_src_offsets || !dev_err) return MP_ERR_INVALID_ARG;
   if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;
   if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
   if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(expert_offsets) ||

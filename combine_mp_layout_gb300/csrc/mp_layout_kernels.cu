@@ -411,7 +411,10 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 //  3. each warp walks its segment 32 entries at a time in order; lanes with
 //     the same expert find each other with __match_any_sync and take
 //     consecutive rows, so the order is deterministic.
-// Shared memory: (nseg + 1) * E int32, nseg = min(32, 16384 / E) (>= 1).
+// num_tokens_per_expert may be NULL: each block then counts every rank's ids
+// itself (R*N*K reads from L2 per block), which saves the layout launch on
+// the small batches this path is for.
+// Shared memory: (nseg + 3) * E int32, nseg = min(32, 16384 / E) (>= 1).
 // ---------------------------------------------------------------------------
 constexpr int kLLThreads = 1024;
 constexpr int kLLHistInts = 16384;
@@ -430,8 +433,10 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   extern __shared__ int32_t ll_smem[];
   __shared__ int64_t warp_sums[kLLThreads / kWarp];
   const int nseg = ll_segments(E);
-  int32_t* hist = ll_smem;             // [nseg][E]: counts, then running offsets
+  int32_t* hist = ll_smem;                // [nseg][E]: counts, then running offsets
   int32_t* rowbase = ll_smem + nseg * E;  // [E]: first row of (expert, this rank)
+  int32_t* tot = rowbase + E;             // [E]: rows of expert e over every source rank
+  int32_t* pre = tot + E;                 // [E]: rows of expert e from source ranks < s
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nk = int64_t(N) * K;
@@ -439,20 +444,48 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   int32_t* slots = slot_row + int64_t(s) * nk;
   const int64_t seg_len = (nk + nseg - 1) / nseg;
   const int64_t g0 = min(nk, int64_t(warp) * seg_len), g1 = min(nk, g0 + seg_len);
-  for (int i = tid; i < nseg * E; i += kLLThreads) hist[i] = 0;
+  for (int i = tid; i < (nseg + 3) * E; i += kLLThreads) ll_smem[i] = 0;
   __syncthreads();
-  // 1. counts per (segment, expert)
+  // 1. counts per (segment, expert) of this rank; the per-expert totals and
+  //    lower-rank prefixes from the layout's num_tokens_per_expert, or, when
+  //    that is NULL, counted here from every rank's ids (ids outside [-1, E)
+  //    are flagged as the layout would)
   if (warp < nseg)
     for (int64_t i = g0 + lane; i < g1; i += kWarp) {
       const int e = __ldg(src + i);
       if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
     }
+  if (num_tokens_per_expert) {
+    for (int e = tid; e < E; e += kLLThreads) {
+      int t = 0, p = 0;
+      for (int q = 0; q < R; ++q) {
+        const int c = __ldg(num_tokens_per_expert + int64_t(q) * E + e);
+        t += c;
+        if (q < s) p += c;
+      }
+      tot[e] = t;
+      pre[e] = p;
+    }
+  } else {
+    bool bad = false;
+    const int64_t all = int64_t(R) * nk;
+    for (int64_t i = tid; i < all; i += kLLThreads) {
+      const int e = __ldg(topk_idx + i);
+      if (e >= 0 && e < E) {
+        atomicAdd(&tot[e], 1);
+        if (i < int64_t(s) * nk) atomicAdd(&pre[e], 1);
+      } else if (e != -1) {
+        bad = true;
+      }
+    }
+    if (bad && s == 0) raise_error(dev_err, MP_ERR_BAD_EXPERT);
+  }
+  __syncthreads();
   // 2a. this thread's experts [e0, e1) and their totals over every source rank
   const int cpt = (E + kLLThreads - 1) / kLLThreads;
   const int e0 = min(E, tid * cpt), e1 = min(E, e0 + cpt);
   int64_t chunk = 0;
-  for (int e = e0; e < e1; ++e)
-    for (int q = 0; q < R; ++q) chunk += __ldg(num_tokens_per_expert + int64_t(q) * E + e);
+  for (int e = e0; e < e1; ++e) chunk += tot[e];
   int64_t inc = chunk;  // block-wide exclusive scan of the chunk totals
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -474,22 +507,16 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   int64_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + inc - chunk;
   // 2b. per expert: outputs, first row of this rank, exclusive prefix over segments
   for (int e = e0; e < e1; ++e) {
-    int64_t tot = 0, pre = 0;
-    for (int q = 0; q < R; ++q) {
-      const int c = __ldg(num_tokens_per_expert + int64_t(q) * E + e);
-      tot += c;
-      if (q < s) pre += c;
-    }
     if (s == 0) expert_offsets[e] = int32_t(base);
-    expert_src_offsets[int64_t(e) * R + s] = int32_t(pre);
-    rowbase[e] = int32_t(base + pre);
+    expert_src_offsets[int64_t(e) * R + s] = pre[e];
+    rowbase[e] = int32_t(base + pre[e]);
     int run = 0;
     for (int g = 0; g < nseg; ++g) {
       const int c = hist[g * E + e];
       hist[g * E + e] = run;
       run += c;
     }
-    base += tot;
+    base += tot[e];
   }
   if (s == 0 && e0 < E && e1 == E) expert_offsets[E] = int32_t(base);
   __syncthreads();
@@ -597,7 +624,7 @@ cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_id
                               int32_t* expert_offsets, int32_t* expert_src_offsets,
                               int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                               cudaStream_t stream) {
-  const size_t smem = sizeof(int32_t) * size_t(ll_segments(E) + 1) * size_t(E);
+  const size_t smem = sizeof(int32_t) * size_t(ll_segments(E) + 3) * size_t(E);
   static thread_local int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);

@@ -417,7 +417,12 @@ int mp_allgatherv_multi(int R, int ntensors, const int64_t *row_bytes, const int
  *
  * mp_dispatch_ll_offsets
  *   in   topk_idx               int32 [R][N][K] (-1 = masked)
- *   in   num_tokens_per_expert  int32 [R][E] from mp_layout (same topk_idx)
+ *   in   num_tokens_per_expert  int32 [R][E] from mp_layout (same topk_idx), or
+ *                               NULL: the call counts the experts itself (each
+ *                               of its R blocks reads all R*N*K ids) and then
+ *                               flags ids outside [-1, E) with
+ *                               MP_ERR_BAD_EXPERT as mp_layout would; this saves
+ *                               the mp_layout launch on small batches
  *   out  expert_offsets         int32 [E+1]: first row of expert e; [E] = total
  *   out  expert_src_offsets     int32 [E][R]: rows of e from source ranks < s
  *   out  recv_src_token         int32 [recv_capacity]: flattened s*N + t

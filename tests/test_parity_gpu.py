@@ -424,7 +424,9 @@ def test_global_ids_and_combined_weights():
                                  dict(R=1, N=40, E=3, K=3, H=64)],
                          ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
                          + ("_cap" if "cap_frac" in c else ""))
-def test_low_latency_layout_matches_oracle(cfg):
+@pytest.mark.parametrize("counts", ["layout", "self"])
+def test_low_latency_layout_matches_oracle(cfg, counts):
+    """counts: expert counts from mp_layout, or counted by the LL offsets call (NULL)."""
     cfg = dict(cfg)
     cap_frac = cfg.pop("cap_frac", None)
     inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=cfg["N"])
@@ -440,7 +442,8 @@ def test_low_latency_layout_matches_oracle(cfg):
     src = torch.full((cap,), -3, dtype=torch.int32, device=dev)
     slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
     rx = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
-    B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, plan.num_tokens_per_expert, cap,
+    ntpe = plan.num_tokens_per_expert if counts == "layout" else None
+    B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, ntpe, cap,
                                      eoff, esoff, src, slot, plan.dev_err))
     B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
     y = wl.random_bf16((cap, H), seed=N).cuda()
@@ -459,6 +462,28 @@ def test_low_latency_layout_matches_oracle(cfg):
     comb, st = oracle.combine_ll(wl.bf16_bits(y), ll["slot_row"], inp.topk_weights)
     assert st == 0
     assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll")
+
+
+def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
+    R, N, E, K = 4, 50, 16, 3
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=64, routing="uniform", dtype="bf16"), seed=9)
+    inp.topk_idx[1, 3, 0] = E + 5
+    inp.topk_idx[2, 7, 2] = -4
+    dev = "cuda"
+    cap = R * N * K
+    topk = torch.from_numpy(inp.topk_idx).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    eoff = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    esoff = torch.zeros((E, R), dtype=torch.int32, device=dev)
+    src = torch.zeros(cap, dtype=torch.int32, device=dev)
+    slot = torch.zeros((R, N, K), dtype=torch.int32, device=dev)
+    B.check(B.mp_dispatch_ll_offsets(R, N, K, E, topk, None, cap, eoff, esoff, src, slot, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == B.MP_ERR_BAD_EXPERT
+    ll, st = oracle.dispatch_ll(np.zeros((R, N, 16), np.uint8), inp.topk_idx, E)
+    assert st == 0
+    assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+    assert np.array_equal(eoff.cpu().numpy(), ll["expert_offsets"])
 
 
 @pytest.mark.parametrize("wide", [False, True], ids=["16B", "32B"])
