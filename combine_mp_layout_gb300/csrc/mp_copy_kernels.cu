@@ -39,6 +39,19 @@
 #ifndef MP_COMBINE_MINB
 #define MP_COMBINE_MINB 3
 #endif
+// The weighted (low-latency) combine's shape; by default the unweighted one's.
+// Measured at R=8, N=128, top-8 (8 rows per token): 16-byte vectors with all 8
+// rows in flight (NW=4, U=1, RB=8) 29.8 us, 6 rows 30.0 us, against 28.5 us for
+// the default; for the dsv3 combine 16-byte vectors cost 491-524 vs 440 us.
+#ifndef MP_COMBINE_W_NW
+#define MP_COMBINE_W_NW MP_COMBINE_NW
+#endif
+#ifndef MP_COMBINE_W_U
+#define MP_COMBINE_W_U MP_COMBINE_U
+#endif
+#ifndef MP_COMBINE_W_RB
+#define MP_COMBINE_W_RB MP_COMBINE_RB
+#endif
 // Small dispatches (fewer warp units at the default shape than the GPU holds
 // warps, e.g. the low-latency batches of 128 tokens per rank) use 1 vector per
 // lane and unit instead, for 4x the units: measured 29 -> 25 us for the rows
@@ -887,11 +900,14 @@ static cudaError_t combine_any(int R, int64_t tokens, int H, const void* y, int6
                                const int32_t* send_row, const float* weights, void* out,
                                int32_t* dev_err, cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  if (MP_COMBINE_NW == 8 && (int64_t(H) * 2) % 32 == 0 && aligned(y, 32) && aligned(out, 32))
-    return combine_nw<MP_COMBINE_NW, MP_COMBINE_U, MP_COMBINE_RB, W>(
-        R, tokens, H, y, y_rows, send_row, weights, out, dev_err, stream);
-  return combine_nw<4, 2 * MP_COMBINE_U, MP_COMBINE_RB, W>(R, tokens, H, y, y_rows, send_row,
-                                                          weights, out, dev_err, stream);
+  constexpr int NW = W ? MP_COMBINE_W_NW : MP_COMBINE_NW;
+  constexpr int U = W ? MP_COMBINE_W_U : MP_COMBINE_U;
+  constexpr int RB = W ? MP_COMBINE_W_RB : MP_COMBINE_RB;
+  if (NW == 8 && (int64_t(H) * 2) % 32 == 0 && aligned(y, 32) && aligned(out, 32))
+    return combine_nw<8, U, RB, W>(R, tokens, H, y, y_rows, send_row, weights, out, dev_err,
+                                   stream);
+  return combine_nw<4, (NW == 8 ? 2 * U : U), RB, W>(R, tokens, H, y, y_rows, send_row, weights,
+                                                     out, dev_err, stream);
 }
 
 cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
