@@ -74,13 +74,14 @@ def lib() -> ctypes.CDLL:
         L.mp_allgatherv_mxfp8.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_allgatherv_mxfp4.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_dispatch_rows_mxfp4.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
+        L.mp_dispatch_rows_bulk.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
                   "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
-                  "mp_dispatch_rows_mxfp4"):
+                  "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -195,6 +196,14 @@ def mp_combine_weights(R, N, K, recv_topk_weights, recv_rows, send_row, combined
                                     int(recv_rows), _dev(send_row, "send_row"),
                                     _dev(combined, "combined_topk_weights"),
                                     _dev(dev_err, "dev_err"), _stream(stream))
+
+
+def mp_dispatch_rows_bulk(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                          recv_scales, dev_err, stream=None) -> int:
+    return lib().mp_dispatch_rows_bulk(R, N, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
+                                       _dev(send_row, "send_row"), int(recv_capacity),
+                                       _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
+                                       _dev(dev_err, "dev_err"), _stream(stream))
 
 
 def mp_dispatch_rows_e4m3(R, N, H, x, send_row, recv_capacity, recv_x, recv_scales,

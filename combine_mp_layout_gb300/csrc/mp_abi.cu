@@ -211,6 +211,20 @@ int mp_dispatch_rows(int R, int N, int H, int dtype, const void* x, const float*
                                  recv_scales, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int mp_dispatch_rows_bulk(int R, int N, int H, int dtype, const void* x, const float* x_scales,
+                          const int32_t* send_row, int64_t recv_capacity, void* recv_x,
+                          float* recv_scales, int32_t* dev_err, mp_stream_t stream) {
+  const int st = check_rows_args(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                                 recv_scales);
+  if (st != MP_OK) return st;
+  if (!dev_err || !aligned4(dev_err)) return MP_ERR_INVALID_ARG;
+  const bool fp8 = dtype == MP_E4M3;
+  return cuda_status(launch_dispatch_bulk(R, int64_t(R) * N, fp8 ? int64_t(H) : int64_t(H) * 2, x,
+                                          recv_x, recv_capacity, send_row,
+                                          fp8 ? H / MP_SCALE_BLOCK : 0, x_scales, recv_scales,
+                                          dev_err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mp_dispatch_rows_e4m3(int R, int N, int H, const void* x, const int32_t* send_row,
                           int64_t recv_capacity, void* recv_x, float* recv_scales,
                           mp_stream_t stream) {

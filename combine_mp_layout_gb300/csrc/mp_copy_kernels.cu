@@ -60,17 +60,6 @@
 #define MP_SMALL_DISPATCH 1
 #endif
 
-#ifndef MP_DISPATCH_TMA
-#define MP_DISPATCH_TMA 0
-#endif
-// 1: one warp unit per (token, slab, destination) instead of (token, slab)
-#ifndef MP_DISPATCH_PER_DEST
-#define MP_DISPATCH_PER_DEST 0
-#endif
-// 1: one unit per (chunk, copy) in all-gatherv instead of (chunk, all copies)
-#ifndef MP_AGV_PER_COPY
-#define MP_AGV_PER_COPY 0
-#endif
 #ifndef MP_TMA_STAGES
 #define MP_TMA_STAGES 6
 #endif
@@ -123,46 +112,6 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ 
         for (int c = lane; c < spr; c += kWarp)
           recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Dispatch copy, one warp unit per (token, slab, destination): the warps that
-// run side by side copy the same slab of one token to its destinations, so
-// the rows being written at any moment form a narrow band (the re-reads of
-// the slab hit L2; DRAM still reads each token row once).
-// ---------------------------------------------------------------------------
-template <int NW, int U>
-__global__ void __launch_bounds__(kCopyThreads)
-mp_k_dispatch_pd(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ x,
-                 Words<NW>* __restrict__ recv_x, int64_t recv_capacity,
-                 const int32_t* __restrict__ send_row, int spr,
-                 const float* __restrict__ x_scales, float* __restrict__ recv_scales) {
-  const int lane = threadIdx.x & 31;
-  const int64_t slab_vec = int64_t(kWarp) * U;
-  const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
-  const int64_t units = tokens * slabs * R;
-  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
-  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
-       unit += nw) {
-    const int64_t ts = unit / R;
-    const int d = int(unit - ts * R);
-    const int64_t tok = ts / slabs;
-    const int64_t slab = ts - tok * slabs;
-    const int64_t row = __ldg(send_row + tok * R + d);
-    if (row < 0 || row >= recv_capacity) continue;
-    const int64_t i0 = slab * slab_vec + lane;
-    Words<NW> v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < vpr) v[u] = ld_shared_l2_w<NW>(x + tok * vpr + i0 + u * kWarp);
-    Words<NW>* dst = recv_x + row * vpr;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < vpr) st_stream_w<NW>(dst + i0 + u * kWarp, v[u]);
-    if (spr > 0 && slab == 0)
-      for (int c = lane; c < spr; c += kWarp)
-        recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
   }
 }
 
@@ -599,31 +548,6 @@ mp_k_agv(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __res
   }
 }
 
-// All-gatherv with one warp unit per (2-vector-per-lane chunk, copy): warps
-// running together write the same chunk to the R copies (chunk re-reads hit L2).
-template <int NW>
-__global__ void __launch_bounds__(kCopyThreads)
-mp_k_agv_pc(int R, int64_t nvec, const Words<NW>* __restrict__ in, Words<NW>* __restrict__ out) {
-  constexpr int U = 2;
-  const int lane = threadIdx.x & 31;
-  const int64_t chunks = (nvec + kWarp * U - 1) / (kWarp * U);
-  const int64_t units = chunks * R;
-  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
-  for (int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); unit < units;
-       unit += nw) {
-    const int64_t c = unit / R;
-    const int q = int(unit - c * R);
-    const int64_t i0 = c * kWarp * U + lane;
-    Words<NW> v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < nvec) v[u] = ld_shared_l2_w<NW>(in + i0 + u * kWarp);
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * kWarp < nvec) st_stream_w<NW>(out + int64_t(q) * nvec + i0 + u * kWarp, v[u]);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Multi-tensor all-gatherv (same page: all-gathering a list of tensors lets
 // quantised data and its scales travel together).  Up to MP_MAX_TENSORS
@@ -705,21 +629,6 @@ static bool aligned(const void* p, int bytes) {
 }
 
 template <int NW, int U>
-static cudaError_t dispatch_copy_pd(int R, int64_t tokens, int64_t row_bytes, const void* x,
-                                    void* recv_x, int64_t recv_capacity, const int32_t* send_row,
-                                    int spr, const float* x_scales, float* recv_scales,
-                                    cudaStream_t stream) {
-  static const int per_sm = resident_blocks(mp_k_dispatch_pd<NW, U>);
-  const int64_t vpr = row_bytes / (4 * NW);
-  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
-  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs * R);
-  return launch_kernel(mp_k_dispatch_pd<NW, U>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
-                       tokens, vpr, static_cast<const Words<NW>*>(x),
-                       static_cast<Words<NW>*>(recv_x), recv_capacity, send_row, spr, x_scales,
-                       recv_scales);
-}
-
-template <int NW, int U>
 static cudaError_t dispatch_copy_nw(int R, int64_t tokens, int64_t row_bytes, const void* x,
                                     void* recv_x, int64_t recv_capacity, const int32_t* send_row,
                                     int spr, const float* x_scales, float* recv_scales,
@@ -767,18 +676,6 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                  int scales_per_row, const float* x_scales, float* recv_scales,
                                  cudaStream_t stream) {
   if (tokens == 0) return cudaSuccess;
-  if (MP_DISPATCH_TMA)
-    return dispatch_copy_tma(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
-                             scales_per_row, x_scales, recv_scales, nullptr, stream);
-  if (MP_DISPATCH_PER_DEST) {
-    if (row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
-      return dispatch_copy_pd<8, MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
-                                                send_row, scales_per_row, x_scales, recv_scales,
-                                                stream);
-    return dispatch_copy_pd<4, 2 * MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
-                                                  send_row, scales_per_row, x_scales,
-                                                  recv_scales, stream);
-  }
   if (MP_SMALL_DISPATCH && MP_DISPATCH_NW == 8 && row_bytes % 32 == 0 && aligned(x, 32) &&
       aligned(recv_x, 32)) {
     const int64_t slabs = (row_bytes / 32 + kWarp * MP_DISPATCH_U - 1) / (kWarp * MP_DISPATCH_U);
@@ -794,6 +691,15 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
   return dispatch_copy_nw<4, 2 * MP_DISPATCH_U>(R, tokens, row_bytes, x, recv_x, recv_capacity,
                                                 send_row, scales_per_row, x_scales, recv_scales,
                                                 stream);
+}
+
+cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                 void* recv_x, int64_t recv_capacity, const int32_t* send_row,
+                                 int scales_per_row, const float* x_scales, float* recv_scales,
+                                 int32_t* dev_err, cudaStream_t stream) {
+  if (tokens == 0) return cudaSuccess;
+  return dispatch_copy_tma(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
+                           scales_per_row, x_scales, recv_scales, dev_err, stream);
 }
 
 // Quantising copies.  Launch shapes measured on GB300 (dsv3 dispatch rows,
@@ -948,25 +854,10 @@ static cudaError_t agv_nw(int R, int64_t bytes, const void* in, void* out, cudaS
                        static_cast<const Words<NW>*>(in), static_cast<Words<NW>*>(out));
 }
 
-template <int NW>
-static cudaError_t agv_pc(int R, int64_t bytes, const void* in, void* out, cudaStream_t stream) {
-  static const int per_sm = resident_blocks(mp_k_agv_pc<NW>);
-  const int64_t nvec = bytes / (4 * NW);
-  const int64_t chunks = (nvec + kWarp * 2 - 1) / (kWarp * 2);
-  const unsigned grid = grid_for(per_sm, kWarpsPerBlock, chunks * R);
-  return launch_kernel(mp_k_agv_pc<NW>, dim3(grid), dim3(kCopyThreads), 0, stream, R, nvec,
-                       static_cast<const Words<NW>*>(in), static_cast<Words<NW>*>(out));
-}
-
 cudaError_t launch_allgatherv(int R, int64_t S, int64_t row_bytes, const void* in, void* out,
                               cudaStream_t stream) {
   const int64_t bytes = S * row_bytes;
   if (bytes == 0) return cudaSuccess;
-  if (MP_AGV_PER_COPY) {
-    if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32))
-      return agv_pc<8>(R, bytes, in, out, stream);
-    return agv_pc<4>(R, bytes, in, out, stream);
-  }
   if (bytes % 32 == 0 && aligned(in, 32) && aligned(out, 32))
     return agv_nw<8, 2>(R, bytes, in, out, stream);
   return agv_nw<4, 4>(R, bytes, in, out, stream);

@@ -48,6 +48,14 @@ cudaError_t launch_dispatch_copy(int R, int64_t tokens, int64_t row_bytes, const
                                  int scales_per_row,
                                  const float* x_scales, float* recv_scales, cudaStream_t stream);
 
+// The same copy as launch_dispatch_copy through the bulk-copy (TMA) engine:
+// cp.async.bulk loads into a shared-memory ring and bulk stores per
+// destination; its bounded mbarrier waits report MP_ERR_TIMEOUT in dev_err.
+cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const void* x,
+                                 void* recv_x, int64_t recv_capacity, const int32_t* send_row,
+                                 int scales_per_row, const float* x_scales, float* recv_scales,
+                                 int32_t* dev_err, cudaStream_t stream);
+
 // Quantises bf16 token rows -- fmt 0: e4m3 with one fp32 scale per 128
 // channels; 1: MXFP8 (e4m3, one UE8M0 byte per 32 channels); 2: MXFP4 (two
 // e2m1 codes per byte, one UE8M0 byte per 32 channels) -- and copies them to

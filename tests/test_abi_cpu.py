@@ -186,6 +186,12 @@ def test_newer_entry_points_reject(L):
     L.mp_dispatch_rows_mxfp4.argtypes = L.mp_dispatch_rows_e4m3.argtypes
     assert L.mp_dispatch_rows_mxfp4(2, 8, 48, P, P, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # H % 32
     assert L.mp_dispatch_rows_mxfp4(2, 8, 64, P, N0, 16, P, P, N0) == B.MP_ERR_INVALID_ARG  # send_row
+    L.mp_dispatch_rows_bulk.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 3 + \
+        [ctypes.c_int64] + [ctypes.c_void_p] * 4
+    assert L.mp_dispatch_rows_bulk(2, 8, 64, B.MP_BF16, P, N0, P, 16, P, N0, N0, N0) == \
+        B.MP_ERR_INVALID_ARG                                                            # dev_err
+    assert L.mp_dispatch_rows_bulk(2, 8, 60, B.MP_BF16, P, N0, P, 16, P, N0, P, N0) == \
+        B.MP_ERR_INVALID_ARG                                                            # H % 8
     neg = (ctypes.c_int64 * 2)(3, -1)
     assert L.mp_allgatherv_mxfp8(2, 64, neg, P, P, P, N0) == B.MP_ERR_INVALID_ARG      # size < 0
     L.mp_dispatch_noalloc.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + \

@@ -326,6 +326,48 @@ def test_dispatch_rows_mxfp4_quantises_like_the_oracle(shape):
     assert np.array_equal(rc[:n].cpu().numpy(), out["recv_x"][:, H // 2:])
 
 
+@pytest.mark.parametrize("dtype,shape,cap_frac", [
+    ("bf16", (4, 300, 16, 4, 384), None), ("e4m3", (3, 129, 12, 2, 256), None),
+    ("bf16", (5, 77, 20, 3, 8200), None), ("bf16", (4, 300, 16, 4, 64), 0.5),
+    ("bf16", (8, 4096, 256, 8, 7168), None)],
+    ids=["bf16", "e4m3_scales", "rows_above_16KB", "capacity", "dsv3"])
+def test_bulk_copy_dispatch_matches_the_oracle(dtype, shape, cap_frac):
+    """mp_dispatch_rows_bulk (cp.async.bulk through shared memory) moves the same bytes
+    as the oracle's dispatch, including rows cut into several 16 KB pieces."""
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype=dtype), seed=H)
+    plan = EPPlan(R, N, K, E, H, dtype)
+    plan.load(inp)
+    B.check(plan.layout())
+    cap = plan.cap
+    if cap_frac is not None:
+        torch.cuda.synchronize()
+        cap = int(plan.num_tokens_per_rank.sum().item() * cap_frac)
+    B.check(B.mp_dispatch_offsets(
+        R, N, K, E, plan.topk_idx, plan.topk_weights, plan.is_token_in_rank,
+        plan.num_tokens_per_rank, plan.num_tokens_per_expert, cap, plan.recv_src_rank,
+        plan.recv_src_idx, plan.recv_topk_idx, plan.recv_topk_weights, plan.dest_offsets,
+        plan.rank_prefix, plan.num_recv_tokens_per_expert, plan.send_row, plan.dev_err,
+        plan.workspace))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.check(B.mp_dispatch_rows_bulk(R, N, H, B.MP_BF16 if dtype == "bf16" else B.MP_E4M3,
+                                    plan.x, plan.x_scales, plan.send_row, cap, plan.recv_x,
+                                    plan.recv_scales, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _, _, mask, _ = oracle.layout(inp.topk_idx, E)
+    xs = inp.x_scales.numpy() if dtype != "bf16" else None
+    out, st = oracle.dispatch(x_host(inp), inp.topk_idx, inp.topk_weights, mask, E,
+                              x_scales=xs, recv_capacity=cap)
+    assert (st == 0) == (cap_frac is None)
+    n = min(out["num_recv"], cap)
+    got = wl.bf16_bits(plan.recv_x[:n]) if dtype == "bf16" else wl.u8_bits(plan.recv_x[:n])
+    assert np.array_equal(got, out["recv_x"][:n])
+    if xs is not None:
+        assert np.array_equal(plan.recv_scales[:n].cpu().numpy().view(np.uint32),
+                              out["recv_scales"][:n].view(np.uint32))
+
+
 def test_empty_tokens():
     inp = wl.make_ep(dict(R=4, N=0, E=16, K=2, H=64, routing="uniform", dtype="bf16"))
     plan = run_gpu(inp)
