@@ -83,6 +83,9 @@ class OracleLib:
         L.oracle_e2m1_to_f32.restype = ctypes.c_float
         L.oracle_dispatch_ll.argtypes = [i32, i32, i32, i32, i64, P, P, i64, P, P, P, P, P]
         L.oracle_dispatch_ll.restype = ctypes.c_int
+        L.oracle_dispatch_ll_rank_major.argtypes = [i32, i32, i32, i32, i64, P, P, i64, P, P, P,
+                                                    P, P]
+        L.oracle_dispatch_ll_rank_major.restype = ctypes.c_int
         L.oracle_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P]
         L.oracle_combine_ll.restype = ctypes.c_int
         for f in ("oracle_layout", "oracle_dispatch", "oracle_combine",
@@ -274,6 +277,29 @@ class OracleLib:
         return dict(recv_x=recv_x[:n], recv_src_token=src[:n], expert_offsets=eoff,
                     expert_src_offsets=esoff, slot_row=slot, num_recv=total), st
 
+    def dispatch_ll_rank_major(self, x: np.ndarray, topk_idx: np.ndarray, E: int,
+                               recv_capacity: int | None = None):
+        """Rank-major low-latency dispatch of x [R][N][...] (bytes copied)."""
+        x = np.ascontiguousarray(x)
+        topk_idx = _c(topk_idx, np.int32)
+        R, N, K = topk_idx.shape
+        row_shape = x.shape[2:]
+        row_bytes = x.itemsize * int(np.prod(row_shape))
+        total = int(((topk_idx >= 0) & (topk_idx < E)).sum())
+        cap = total if recv_capacity is None else int(recv_capacity)
+        n1 = max(cap, 1)
+        recv_x = np.zeros((n1,) + row_shape, x.dtype)
+        src = np.full(n1, -7, np.int32)
+        doff = np.zeros(R + 1, np.int32)
+        dsoff = np.zeros((R, R), np.int32)
+        slot = np.zeros((R, N, K), np.int32)
+        st = self.L.oracle_dispatch_ll_rank_major(R, N, K, E, row_bytes, _p(x), _p(topk_idx), cap,
+                                                  _p(recv_x), _p(src), _p(doff), _p(dsoff),
+                                                  _p(slot))
+        n = min(cap, total)
+        return dict(recv_x=recv_x[:n], recv_src_token=src[:n], dest_offsets=doff,
+                    dest_src_offsets=dsoff, slot_row=slot, num_recv=total), st
+
     def combine_ll(self, y_bits: np.ndarray, slot_row: np.ndarray, topk_weights: np.ndarray):
         y_bits = _c(y_bits, np.uint16)
         slot_row = _c(slot_row, np.int32)
@@ -358,6 +384,10 @@ def combine_weights(recv_topk_weights, send_row):
 
 def dispatch_ll(x, topk_idx, E, recv_capacity=None):
     return default().dispatch_ll(x, topk_idx, E, recv_capacity)
+
+
+def dispatch_ll_rank_major(x, topk_idx, E, recv_capacity=None):
+    return default().dispatch_ll_rank_major(x, topk_idx, E, recv_capacity)
 
 
 def combine_ll(y_bits, slot_row, topk_weights):

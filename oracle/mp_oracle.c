@@ -435,6 +435,55 @@ int oracle_dispatch_ll(int R, int N, int K, int E, int64_t row_bytes, const uint
   return status;
 }
 
+/* ------------------------------------------------------------------ */
+/* Low-latency rank-major layout [EP, the pull request that adds      */
+/* rank-major output to the low-latency path].  The same rows as the  */
+/* expert-major layout (one per token and top-k slot with a valid     */
+/* expert), grouped by the destination rank d = e / (E/R) that owns   */
+/* the expert instead of by expert.  Reading (the pages fix no order  */
+/* inside a group): rows of destination d are contiguous, groups in   */
+/* ascending d; inside a group rows are ordered by source rank, then  */
+/* token, then top-k slot, ascending.                                 */
+/*   dest_offsets[d]      first row of destination d; [R] = total     */
+/*   dest_src_offsets[d][s] rows of d from source ranks < s           */
+/*   recv_src_token, slot_row, recv_x as in the expert-major layout   */
+/* ------------------------------------------------------------------ */
+int oracle_dispatch_ll_rank_major(int R, int N, int K, int E, int64_t row_bytes,
+                                  const uint8_t *x, const int32_t *topk_idx,
+                                  int64_t recv_capacity, uint8_t *recv_x,
+                                  int32_t *recv_src_token, int32_t *dest_offsets,
+                                  int32_t *dest_src_offsets, int32_t *slot_row) {
+  if (R < 1 || N < 0 || K < 1 || E < R || E % R != 0 || row_bytes < 0 || recv_capacity < 0)
+    return ORC_BAD_ARG;
+  const int El = E / R;
+  int status = 0;
+  for (int64_t i = 0; i < (int64_t)R * N * K; ++i) slot_row[i] = -1;
+  int64_t row = 0;
+  for (int d = 0; d < R; ++d) {
+    dest_offsets[d] = (int32_t)row;
+    for (int s = 0; s < R; ++s) {
+      dest_src_offsets[d * R + s] = (int32_t)(row - dest_offsets[d]);
+      for (int t = 0; t < N; ++t) {
+        const int64_t tok = (int64_t)s * N + t;
+        for (int k = 0; k < K; ++k) {
+          const int e = topk_idx[tok * K + k];
+          if (e < d * El || e >= (d + 1) * El) continue;
+          if (row < recv_capacity) {
+            memcpy(recv_x + row * row_bytes, x + tok * row_bytes, (size_t)row_bytes);
+            recv_src_token[row] = (int32_t)tok;
+            slot_row[tok * K + k] = (int32_t)row;
+          } else {
+            status |= ORC_CAPACITY;
+          }
+          row += 1;
+        }
+      }
+    }
+  }
+  dest_offsets[R] = (int32_t)row;
+  return status;
+}
+
 /* Low-latency combine [EP, low-latency combine: the expert outputs of a   */
 /* token are reduced with its top-k weights]: out[s][t] = bf16( sum over   */
 /* k = 0..K-1 ascending with slot_row >= 0 of w[s][t][k] * float(y[row]) ), */

@@ -280,6 +280,45 @@ def pin_low_latency_layout(orc) -> None:
         assert st == 0 and np.array_equal(_f32(comb), exact.astype(np.float32))
 
 
+
+def pin_low_latency_rank_major(orc) -> None:
+    """Rank-major rows against a sorted enumeration of (owner rank, source, token, slot)
+    tuples; the same rows as the expert-major layout, regrouped."""
+    rng = np.random.default_rng(19)
+    for R, N, E, K in [(2, 9, 6, 3), (3, 16, 12, 4), (4, 5, 4, 4), (1, 7, 3, 2)]:
+        idx = wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)
+        idx[rng.random(idx.shape) < 0.2] = -1
+        x = rng.integers(0, 60000, (R, N, 8)).astype(np.uint16)
+        rm, st = orc.dispatch_ll_rank_major(x, idx, E)
+        assert st == 0
+        El = E // R
+        tuples = sorted((int(idx[s, t, k]) // El, s, t, k) for s in range(R) for t in range(N)
+                        for k in range(K) if idx[s, t, k] >= 0)
+        assert rm["num_recv"] == len(tuples) == rm["dest_offsets"][R]
+        for r, (d, s, t, k) in enumerate(tuples):
+            assert rm["slot_row"][s, t, k] == r and rm["recv_src_token"][r] == s * N + t
+            assert rm["dest_offsets"][d] <= r < rm["dest_offsets"][d + 1]
+            assert np.array_equal(rm["recv_x"][r], x[s, t])
+        for d in range(R):
+            for s in range(R):
+                before = sum(1 for tu in tuples if tu[0] == d and tu[1] < s)
+                assert rm["dest_src_offsets"][d, s] == before
+        assert np.all(rm["slot_row"][idx < 0] == -1)
+        # the same (token, slot) rows as the expert-major layout, and per destination the
+        # expert-major blocks of its experts hold exactly as many rows
+        em, st = orc.dispatch_ll(x, idx, E)
+        assert st == 0 and np.array_equal(rm["slot_row"] >= 0, em["slot_row"] >= 0)
+        for d in range(R):
+            assert (rm["dest_offsets"][d + 1] - rm["dest_offsets"][d]
+                    == em["expert_offsets"][(d + 1) * El] - em["expert_offsets"][d * El])
+    # a too-small capacity keeps the first rows and flags the rest
+    idx = wl.topk_uniform(rng, 2 * 6, 4, 2).reshape(2, 6, 2)
+    x = rng.integers(0, 60000, (2, 6, 8)).astype(np.uint16)
+    full, _ = orc.dispatch_ll_rank_major(x, idx, 4)
+    cut, st = orc.dispatch_ll_rank_major(x, idx, 4, recv_capacity=10)
+    assert st == 4 and np.array_equal(cut["recv_src_token"], full["recv_src_token"][:10])
+    assert np.array_equal(cut["slot_row"], np.where(full["slot_row"] < 10, full["slot_row"], -1))
+
 def pin_ep_special_cases(orc) -> None:
     rng = np.random.default_rng(9)
     # R = 1: dispatch is the identity on tokens with an expert; combine gives them back
@@ -579,4 +618,5 @@ def pin_mxfp4_quantisation(orc) -> None:
 ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
             pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
-            pin_low_latency_layout, pin_mxfp8_quantisation, pin_mxfp4_quantisation]
+            pin_low_latency_layout, pin_mxfp8_quantisation, pin_mxfp4_quantisation,
+            pin_low_latency_rank_major]

@@ -27,7 +27,8 @@ MUTANTS = {
                           "for (int t = N - 1; t >= 0; --t) {\n        const int64_t tok = (int64_t)s * N + t;\n        if (!((is_token_in_rank"),
     "global_expert_ids": ("local ? e - d * El : -1", "local ? e : -1"),
     "nonlocal_weight_kept": ("local ? topk_weights[tok * K + k] : 0.0f", "topk_weights[tok * K + k]"),
-    "rank_prefix_absolute": ("(int32_t)(row - dest_offsets[d])", "(int32_t)(row)"),
+    "rank_prefix_absolute": ("rank_prefix[(int64_t)s * R + d] = (int32_t)(row - dest_offsets[d]);",
+                             "rank_prefix[(int64_t)s * R + d] = (int32_t)(row);"),
     "src_idx_off_by_one": ("recv_src_idx[row] = t;", "recv_src_idx[row] = t + 1;"),
     "recv_expert_count_shifted": ("if (e >= 0 && e < E) num_recv_tokens_per_expert[e] += 1;",
                                   "if (e >= 0 && e < E) num_recv_tokens_per_expert[(e + 1) % E] += 1;"),
@@ -73,6 +74,12 @@ MUTANTS = {
     "mxfp4_emax_8": ("code = floor_log2_f32(amax) - 2 + 127;", "code = floor_log2_f32(amax) - 8 + 127;"),
     "mxfp4_nibbles_swapped": ("qb[h / 2] = (uint8_t)(lo | (hi << 4));", "qb[h / 2] = (uint8_t)(hi | (lo << 4));"),
     "e2m1_saturates_to_4": ("if (!(a < 6.0)) return (uint8_t)(sign | 7u);", "if (!(a < 6.0)) return (uint8_t)(sign | 6u);"),
+    "ll_rank_major_by_expert_owner_mod": ("if (e < d * El || e >= (d + 1) * El) continue;",
+                                          "if (e % R != d) continue;"),
+    "ll_rank_major_slot_order_dropped": ("for (int t = 0; t < N; ++t) {\n        const int64_t tok = (int64_t)s * N + t;\n        for (int k = 0; k < K; ++k) {\n          const int e = topk_idx[tok * K + k];",
+                                         "for (int t = N - 1; t >= 0; --t) {\n        const int64_t tok = (int64_t)s * N + t;\n        for (int k = 0; k < K; ++k) {\n          const int e = topk_idx[tok * K + k];"),
+    "ll_rank_major_src_offsets_absolute": ("dest_src_offsets[d * R + s] = (int32_t)(row - dest_offsets[d]);",
+                                           "dest_src_offsets[d * R + s] = (int32_t)(row);"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
 }
