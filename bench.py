@@ -485,6 +485,22 @@ def measure_other_rows(steps: int, peak: float):
         GBs_cuda_graph=ll_bytes / (ms_llg / 1e3) / 1e9,
         workload="R=8, N=128, H=7168 bf16, E=256, top-8: LL offsets (counting the experts "
                  "themselves) + LL rows + weighted LL combine (3 launches)")
+    doff = torch.empty(R + 1, dtype=torch.int32, device="cuda")
+    dsoff = torch.empty((R, R), dtype=torch.int32, device="cuda")
+
+    def ll_rm_step():  # rank-major output: rows grouped by the rank owning the expert
+        B.check(B.mp_dispatch_ll_offsets_rank_major(R, N, K, E, plan.topk_idx, None, cap, doff,
+                                                    dsoff, src, slot, plan.dev_err))
+        B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
+        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
+
+    ms_rm = timed(ll_rm_step, steps)
+    assert plan.device_error() == 0
+    rm_bytes = ll_bytes - (E + 1) * 4 - E * R * 4 + (R + 1) * 4 + R * R * 4
+    out["low_latency_rank_major_step_n128"] = dict(
+        row(ms_rm, rm_bytes), us_per_step=ms_rm * 1e3,
+        workload="as low_latency_step_n128 with rank-major output (rows grouped by the rank "
+                 "owning the expert)")
     del plan, rx, yl, lo, graph
     torch.cuda.empty_cache()
 

@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P]
         L.mp_combine_weights.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
         L.mp_dispatch_ll_offsets.argtypes = [i32, i32, i32, i32, P, P, i64, P, P, P, P, P, P]
+        L.mp_dispatch_ll_offsets_rank_major.argtypes = L.mp_dispatch_ll_offsets.argtypes
         L.mp_dispatch_ll_rows.argtypes = [i32, i32, i32, i32, i32, P, P, P, i64, P, P, P]
         L.mp_combine_ll.argtypes = [i32, i32, i32, i32, P, i64, P, P, P, P, P]
         L.mp_combine.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
@@ -78,7 +79,8 @@ def lib() -> ctypes.CDLL:
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
-                  "mp_dispatch_ll_offsets", "mp_dispatch_ll_rows", "mp_combine_ll",
+                  "mp_dispatch_ll_offsets", "mp_dispatch_ll_offsets_rank_major",
+                  "mp_dispatch_ll_rows", "mp_combine_ll",
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
                   "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk"):
@@ -313,6 +315,16 @@ def mp_dispatch_ll_offsets(R, N, K, E, topk_idx, num_tokens_per_expert, recv_cap
         R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(num_tokens_per_expert, "num_tokens_per_expert"),
         int(recv_capacity), _dev(expert_offsets, "expert_offsets"),
         _dev(expert_src_offsets, "expert_src_offsets"), _dev(recv_src_token, "recv_src_token"),
+        _dev(slot_row, "slot_row"), _dev(dev_err, "dev_err"), _stream(stream))
+
+
+def mp_dispatch_ll_offsets_rank_major(R, N, K, E, topk_idx, num_tokens_per_expert,
+                                      recv_capacity, dest_offsets, dest_src_offsets,
+                                      recv_src_token, slot_row, dev_err, stream=None) -> int:
+    return lib().mp_dispatch_ll_offsets_rank_major(
+        R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(num_tokens_per_expert, "num_tokens_per_expert"),
+        int(recv_capacity), _dev(dest_offsets, "dest_offsets"),
+        _dev(dest_src_offsets, "dest_src_offsets"), _dev(recv_src_token, "recv_src_token"),
         _dev(slot_row, "slot_row"), _dev(dev_err, "dev_err"), _stream(stream))
 
 

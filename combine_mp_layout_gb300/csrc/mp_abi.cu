@@ -384,23 +384,43 @@ int mp_allgatherv_multi(int R, int ntensors, const int64_t* row_bytes, const int
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int ll_offsets_checked(int R, int N, int K, int E, int rank_major,
+                              const int32_t* topk_idx, const int32_t* num_tokens_per_expert,
+                              int64_t recv_capacity, int32_t* bin_offsets,
+                              int32_t* bin_src_offsets, int32_t* recv_src_token,
+                              int32_t* slot_row, int32_t* dev_err, mp_stream_t stream) {
+  if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
+  if (!bin_offsets || !bin_src_offsets || !dev_err) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(bin_offsets) ||
+      !aligned4(bin_src_offsets) || !aligned4(recv_src_token) || !aligned4(slot_row) ||
+      !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  return cuda_status(launch_ll_offsets(R, N, K, E, rank_major, topk_idx, num_tokens_per_expert,
+                                       recv_capacity, bin_offsets, bin_src_offsets,
+                                       recv_src_token, slot_row, dev_err,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                            const int32_t* num_tokens_per_expert, int64_t recv_capacity,
                            int32_t* expert_offsets, int32_t* expert_src_offsets,
                            int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                            mp_stream_t stream) {
-  if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
-  if (!expert_offsets || !expert_src_offsets || !dev_err) return MP_ERR_INVALID_ARG;
-  if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;
-  if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
-  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(expert_offsets) ||
-      !aligned4(expert_src_offsets) || !aligned4(recv_src_token) || !aligned4(slot_row) ||
-      !aligned4(dev_err))
-    return MP_ERR_INVALID_ARG;
-  return cuda_status(launch_ll_offsets(R, N, K, E, topk_idx, num_tokens_per_expert,
-                                       recv_capacity, expert_offsets, expert_src_offsets,
-                                       recv_src_token, slot_row, dev_err,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return ll_offsets_checked(R, N, K, E, 0, topk_idx, num_tokens_per_expert, recv_capacity,
+                            expert_offsets, expert_src_offsets, recv_src_token, slot_row, dev_err,
+                            stream);
+}
+
+int mp_dispatch_ll_offsets_rank_major(int R, int N, int K, int E, const int32_t* topk_idx,
+                                      const int32_t* num_tokens_per_expert,
+                                      int64_t recv_capacity, int32_t* dest_offsets,
+                                      int32_t* dest_src_offsets, int32_t* recv_src_token,
+                                      int32_t* slot_row, int32_t* dev_err, mp_stream_t stream) {
+  return ll_offsets_checked(R, N, K, E, 1, topk_idx, num_tokens_per_expert, recv_capacity,
+                            dest_offsets, dest_src_offsets, recv_src_token, slot_row, dev_err,
+                            stream);
 }
 
 int mp_dispatch_ll_rows(int R, int N, int K, int H, int dtype, const void* x,

@@ -24,12 +24,14 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                         int32_t* send_row, int32_t* dev_err, unsigned char* ws,
                         cudaStream_t stream, int global_ids = 0, int32_t sentinel = -1);
 
-// Low-latency expert-major offsets (one block per source rank).
-cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
-                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
-                              int32_t* expert_offsets, int32_t* expert_src_offsets,
-                              int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
-                              cudaStream_t stream);
+// Low-latency offsets, expert-major (rank_major = 0: bins are experts) or
+// rank-major (1: bins are the ranks owning the experts); one block per source
+// rank.
+cudaError_t launch_ll_offsets(int R, int N, int K, int E, int rank_major,
+                              const int32_t* topk_idx, const int32_t* num_tokens_per_expert,
+                              int64_t recv_capacity, int32_t* bin_offsets,
+                              int32_t* bin_src_offsets, int32_t* recv_src_token,
+                              int32_t* slot_row, int32_t* dev_err, cudaStream_t stream);
 
 // out[t] = bf16( sum over k ascending of weights[t][k] * y[slot_row[t][k]] )
 cudaError_t launch_combine_weighted(int K, int64_t tokens, int H, const void* y, int64_t y_rows,

@@ -424,19 +424,27 @@ __host__ __device__ inline int ll_segments(int E) {
   return n < 1 ? 1 : (n > kLLThreads / kWarp ? kLLThreads / kWarp : n);
 }
 
+// RANK_MAJOR (the same page's rank-major output for the LL path): the rows
+// are grouped by the rank d = e / (E/R) that owns the expert instead of by
+// expert; inside a group by source rank, token and top-k slot.  The kernel is
+// the same counting sort over nbins = R bins instead of E.
+template <bool RANK_MAJOR>
 __global__ void __launch_bounds__(kLLThreads)
 mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx,
                 const int32_t* __restrict__ num_tokens_per_expert, int64_t recv_capacity,
-                int32_t* __restrict__ expert_offsets, int32_t* __restrict__ expert_src_offsets,
+                int32_t* __restrict__ bin_offsets, int32_t* __restrict__ bin_src_offsets,
                 int32_t* __restrict__ recv_src_token, int32_t* __restrict__ slot_row,
                 int32_t* __restrict__ dev_err) {
   extern __shared__ int32_t ll_smem[];
   __shared__ int64_t warp_sums[kLLThreads / kWarp];
-  const int nseg = ll_segments(E);
-  int32_t* hist = ll_smem;                // [nseg][E]: counts, then running offsets
-  int32_t* rowbase = ll_smem + nseg * E;  // [E]: first row of (expert, this rank)
-  int32_t* tot = rowbase + E;             // [E]: rows of expert e over every source rank
-  int32_t* pre = tot + E;                 // [E]: rows of expert e from source ranks < s
+  const int nbins = RANK_MAJOR ? R : E;
+  const int El = E / R;
+  auto bin_of = [&](int e) { return RANK_MAJOR ? e / El : e; };
+  const int nseg = ll_segments(nbins);
+  int32_t* hist = ll_smem;                    // [nseg][nbins]: counts, then running offsets
+  int32_t* rowbase = ll_smem + nseg * nbins;  // [nbins]: first row of (bin, this rank)
+  int32_t* tot = rowbase + nbins;             // [nbins]: rows of the bin over every rank
+  int32_t* pre = tot + nbins;                 // [nbins]: rows of the bin from ranks < s
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nk = int64_t(N) * K;
@@ -444,16 +452,16 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   int32_t* slots = slot_row + int64_t(s) * nk;
   const int64_t seg_len = (nk + nseg - 1) / nseg;
   const int64_t g0 = min(nk, int64_t(warp) * seg_len), g1 = min(nk, g0 + seg_len);
-  for (int i = tid; i < (nseg + 3) * E; i += kLLThreads) ll_smem[i] = 0;
+  for (int i = tid; i < (nseg + 3) * nbins; i += kLLThreads) ll_smem[i] = 0;
   __syncthreads();
-  // 1. counts per (segment, expert) of this rank; the per-expert totals and
+  // 1. counts per (segment, bin) of this rank; the per-bin totals and
   //    lower-rank prefixes from the layout's num_tokens_per_expert, or, when
   //    that is NULL, counted here from every rank's ids (ids outside [-1, E)
   //    are flagged as the layout would)
   if (warp < nseg)
     for (int64_t i = g0 + lane; i < g1; i += kWarp) {
       const int e = __ldg(src + i);
-      if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+      if (e >= 0 && e < E) atomicAdd(&hist[warp * nbins + bin_of(e)], 1);
     }
   if (num_tokens_per_expert) {
     for (int e = tid; e < E; e += kLLThreads) {
@@ -463,8 +471,13 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
         t += c;
         if (q < s) p += c;
       }
-      tot[e] = t;
-      pre[e] = p;
+      if (RANK_MAJOR) {
+        atomicAdd(&tot[bin_of(e)], t);
+        atomicAdd(&pre[bin_of(e)], p);
+      } else {
+        tot[e] = t;
+        pre[e] = p;
+      }
     }
   } else {
     bool bad = false;
@@ -472,8 +485,8 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
     for (int64_t i = tid; i < all; i += kLLThreads) {
       const int e = __ldg(topk_idx + i);
       if (e >= 0 && e < E) {
-        atomicAdd(&tot[e], 1);
-        if (i < int64_t(s) * nk) atomicAdd(&pre[e], 1);
+        atomicAdd(&tot[bin_of(e)], 1);
+        if (i < int64_t(s) * nk) atomicAdd(&pre[bin_of(e)], 1);
       } else if (e != -1) {
         bad = true;
       }
@@ -481,11 +494,11 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
     if (bad && s == 0) raise_error(dev_err, MP_ERR_BAD_EXPERT);
   }
   __syncthreads();
-  // 2a. this thread's experts [e0, e1) and their totals over every source rank
-  const int cpt = (E + kLLThreads - 1) / kLLThreads;
-  const int e0 = min(E, tid * cpt), e1 = min(E, e0 + cpt);
+  // 2a. this thread's bins [b0, b1) and their totals over every source rank
+  const int cpt = (nbins + kLLThreads - 1) / kLLThreads;
+  const int b0 = min(nbins, tid * cpt), b1 = min(nbins, b0 + cpt);
   int64_t chunk = 0;
-  for (int e = e0; e < e1; ++e) chunk += tot[e];
+  for (int b = b0; b < b1; ++b) chunk += tot[b];
   int64_t inc = chunk;  // block-wide exclusive scan of the chunk totals
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -505,20 +518,20 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   }
   __syncthreads();
   int64_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + inc - chunk;
-  // 2b. per expert: outputs, first row of this rank, exclusive prefix over segments
-  for (int e = e0; e < e1; ++e) {
-    if (s == 0) expert_offsets[e] = int32_t(base);
-    expert_src_offsets[int64_t(e) * R + s] = pre[e];
-    rowbase[e] = int32_t(base + pre[e]);
+  // 2b. per bin: outputs, first row of this rank, exclusive prefix over segments
+  for (int b = b0; b < b1; ++b) {
+    if (s == 0) bin_offsets[b] = int32_t(base);
+    bin_src_offsets[int64_t(b) * R + s] = pre[b];
+    rowbase[b] = int32_t(base + pre[b]);
     int run = 0;
     for (int g = 0; g < nseg; ++g) {
-      const int c = hist[g * E + e];
-      hist[g * E + e] = run;
+      const int c = hist[g * nbins + b];
+      hist[g * nbins + b] = run;
       run += c;
     }
-    base += tot[e];
+    base += tot[b];
   }
-  if (s == 0 && e0 < E && e1 == E) expert_offsets[E] = int32_t(base);
+  if (s == 0 && b0 < nbins && b1 == nbins) bin_offsets[nbins] = int32_t(base);
   __syncthreads();
   // 3. rows, segment by segment in entry order
   bool overflow = false;
@@ -527,11 +540,12 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
       const int64_t i = i0 + lane;
       const int e = i < g1 ? __ldg(src + i) : -1;
       const bool ok = e >= 0 && e < E;
-      const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
-      const int run = ok ? hist[warp * E + e] : 0;
+      const int b = ok ? bin_of(e) : -1;
+      const unsigned peers = __match_any_sync(kFull, b);
+      const int run = ok ? hist[warp * nbins + b] : 0;
       __syncwarp();
       if (ok) {
-        const int64_t row = int64_t(rowbase[e]) + run + __popc(peers & lanemask_lt());
+        const int64_t row = int64_t(rowbase[b]) + run + __popc(peers & lanemask_lt());
         if (row < recv_capacity) {
           slots[i] = int32_t(row);
           recv_src_token[row] = int32_t(int64_t(s) * N + i / K);
@@ -539,7 +553,7 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
           slots[i] = -1;
           overflow = true;
         }
-        if ((peers >> lane) == 1u) hist[warp * E + e] = run + __popc(peers);  // highest peer
+        if ((peers >> lane) == 1u) hist[warp * nbins + b] = run + __popc(peers);  // highest peer
       } else if (i < g1) {
         slots[i] = -1;  // masked or invalid: no row
       }
@@ -619,25 +633,41 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
 
 namespace mp {
 
-cudaError_t launch_ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+template <bool RANK_MAJOR>
+static cudaError_t ll_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                               const int32_t* num_tokens_per_expert, int64_t recv_capacity,
-                              int32_t* expert_offsets, int32_t* expert_src_offsets,
+                              int32_t* bin_offsets, int32_t* bin_src_offsets,
                               int32_t* recv_src_token, int32_t* slot_row, int32_t* dev_err,
                               cudaStream_t stream) {
-  const size_t smem = sizeof(int32_t) * size_t(ll_segments(E) + 3) * size_t(E);
+  const int nbins = RANK_MAJOR ? R : E;
+  const size_t smem = sizeof(int32_t) * size_t(ll_segments(nbins) + 3) * size_t(nbins);
   static thread_local int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > 48 * 1024 && configured[dev] < int(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(mp_k_ll_offsets,
+    cudaError_t e = cudaFuncSetAttribute(mp_k_ll_offsets<RANK_MAJOR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  return launch_kernel(mp_k_ll_offsets, dim3(unsigned(R)), dim3(kLLThreads), smem, stream, R, N, K,
-                       E, topk_idx, num_tokens_per_expert, recv_capacity, expert_offsets,
-                       expert_src_offsets, recv_src_token, slot_row, dev_err);
+  return launch_kernel(mp_k_ll_offsets<RANK_MAJOR>, dim3(unsigned(R)), dim3(kLLThreads), smem,
+                       stream, R, N, K, E, topk_idx, num_tokens_per_expert, recv_capacity,
+                       bin_offsets, bin_src_offsets, recv_src_token, slot_row, dev_err);
+}
+
+cudaError_t launch_ll_offsets(int R, int N, int K, int E, int rank_major,
+                              const int32_t* topk_idx, const int32_t* num_tokens_per_expert,
+                              int64_t recv_capacity, int32_t* bin_offsets,
+                              int32_t* bin_src_offsets, int32_t* recv_src_token,
+                              int32_t* slot_row, int32_t* dev_err, cudaStream_t stream) {
+  return rank_major
+             ? ll_offsets<true>(R, N, K, E, topk_idx, num_tokens_per_expert, recv_capacity,
+                                bin_offsets, bin_src_offsets, recv_src_token, slot_row, dev_err,
+                                stream)
+             : ll_offsets<false>(R, N, K, E, topk_idx, num_tokens_per_expert, recv_capacity,
+                                 bin_offsets, bin_src_offsets, recv_src_token, slot_row, dev_err,
+                                 stream);
 }
 
 }  // namespace mp

@@ -461,6 +461,24 @@ int mp_dispatch_ll_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
                            int32_t *expert_offsets, int32_t *expert_src_offsets,
                            int32_t *recv_src_token, int32_t *slot_row, int32_t *dev_err,
                            mp_stream_t stream);
+/*
+ * mp_dispatch_ll_offsets_rank_major -- the low-latency layout with rank-major
+ * output ([EP] the pull request adding rank-major output to the LL path).
+ * The same rows as mp_dispatch_ll_offsets (one per token and top-k slot with
+ * a valid expert), grouped by the rank d = e / (E/R) that owns the expert;
+ * reading (the pages fix no order inside a group): groups in ascending d,
+ * inside a group rows ordered by source rank, then token, then top-k slot.
+ *   out  dest_offsets      int32 [R+1]: first row of destination d; [R] = total
+ *   out  dest_src_offsets  int32 [R][R]: rows of d from source ranks < s
+ *   other arguments, checks and device errors as mp_dispatch_ll_offsets
+ *   (num_tokens_per_expert may be NULL in the same way).  mp_dispatch_ll_rows
+ *   and mp_combine_ll take this slot_row unchanged.
+ */
+int mp_dispatch_ll_offsets_rank_major(int R, int N, int K, int E, const int32_t *topk_idx,
+                                      const int32_t *num_tokens_per_expert,
+                                      int64_t recv_capacity, int32_t *dest_offsets,
+                                      int32_t *dest_src_offsets, int32_t *recv_src_token,
+                                      int32_t *slot_row, int32_t *dev_err, mp_stream_t stream);
 int mp_dispatch_ll_rows(int R, int N, int K, int H, int dtype, const void *x,
                         const float *x_scales, const int32_t *slot_row, int64_t recv_capacity,
                         void *recv_x, float *recv_scales, mp_stream_t stream);

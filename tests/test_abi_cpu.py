@@ -164,6 +164,11 @@ def test_newer_entry_points_reject(L):
     assert L.mp_dispatch_ll_offsets(2, 8, 2, 7, P, P, 16, P, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG
     assert L.mp_dispatch_ll_offsets(2, 8, 33, 8, P, P, 16, P, P, P, P, P, N0) == \
         B.MP_ERR_INVALID_ARG  # K > MP_MAX_TOPK
+    L.mp_dispatch_ll_offsets_rank_major.argtypes = L.mp_dispatch_ll_offsets.argtypes
+    assert L.mp_dispatch_ll_offsets_rank_major(2, 8, 2, 7, P, P, 16, P, P, P, P, P, N0) == \
+        B.MP_ERR_INVALID_ARG  # E % R
+    assert L.mp_dispatch_ll_offsets_rank_major(2, 8, 2, 8, P, P, 16, P, P, P, P, N0, N0) == \
+        B.MP_ERR_INVALID_ARG  # dev_err
     L.mp_combine_ll.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_int64] + \
         [ctypes.c_void_p] * 5
     assert L.mp_combine_ll(2, 8, 2, 60, P, 4, P, P, P, P, N0) == B.MP_ERR_INVALID_ARG   # H % 8

@@ -506,6 +506,52 @@ def test_low_latency_layout_matches_oracle(cfg, counts):
     assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll")
 
 
+@pytest.mark.parametrize("cfg", [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
+                                 dict(R=5, N=77, E=20, K=6, H=264), dict(R=4, N=3000, E=64, K=6, H=64),
+                                 dict(R=32, N=40, E=64, K=4, H=64),
+                                 dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5),
+                                 dict(R=1, N=40, E=3, K=3, H=64)],
+                         ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
+                         + ("_cap" if "cap_frac" in c else ""))
+@pytest.mark.parametrize("counts", ["layout", "self"])
+def test_low_latency_rank_major_matches_oracle(cfg, counts):
+    cfg = dict(cfg)
+    cap_frac = cfg.pop("cap_frac", None)
+    inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=cfg["N"] + 1)
+    R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
+    inp.topk_idx[:, ::5, 0] = -1
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    B.check(plan.layout())
+    cap = R * N * K if cap_frac is None else int(R * N * K * cap_frac)
+    dev = "cuda"
+    doff = torch.full((R + 1,), -3, dtype=torch.int32, device=dev)
+    dsoff = torch.full((R, R), -3, dtype=torch.int32, device=dev)
+    src = torch.full((cap,), -3, dtype=torch.int32, device=dev)
+    slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+    ntpe = plan.num_tokens_per_expert if counts == "layout" else None
+    B.check(B.mp_dispatch_ll_offsets_rank_major(R, N, K, E, plan.topk_idx, ntpe, cap, doff, dsoff,
+                                                src, slot, plan.dev_err))
+    B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
+    y = wl.random_bf16((cap, H), seed=N + 1).cuda()
+    out = torch.zeros((R, N, H), dtype=torch.bfloat16, device=dev)
+    B.check(B.mp_combine_ll(R, N, K, H, y, cap, slot, plan.topk_weights, out, plan.dev_err))
+    torch.cuda.synchronize()
+    rm, st = oracle.dispatch_ll_rank_major(wl.bf16_bits(inp.x), inp.topk_idx, E, recv_capacity=cap)
+    assert plan.device_error() == st
+    assert (st == 0) == (cap_frac is None)
+    n = min(rm["num_recv"], cap)
+    assert np.array_equal(doff.cpu().numpy(), rm["dest_offsets"])
+    assert np.array_equal(dsoff.cpu().numpy(), rm["dest_src_offsets"])
+    assert np.array_equal(slot.cpu().numpy(), rm["slot_row"])
+    assert np.array_equal(src[:n].cpu().numpy(), rm["recv_src_token"])
+    assert np.array_equal(wl.bf16_bits(rx[:n]), rm["recv_x"])
+    comb, st = oracle.combine_ll(wl.bf16_bits(y), rm["slot_row"], inp.topk_weights)
+    assert st == 0
+    assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll rank-major")
+
+
 def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
     R, N, E, K = 4, 50, 16, 3
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=64, routing="uniform", dtype="bf16"), seed=9)
