@@ -59,6 +59,12 @@
 #ifndef MP_SMALL_DISPATCH
 #define MP_SMALL_DISPATCH 1
 #endif
+// 1: the e4m3 quantiser divides by the block scale with a reciprocal and two
+// FMA corrections instead of a division per element (see mp_k_quant_rows);
+// 0: one correctly rounded division per element.
+#ifndef MP_QUANT_FAST_DIV
+#define MP_QUANT_FAST_DIV 1
+#endif
 
 #ifndef MP_TMA_STAGES
 #define MP_TMA_STAGES 6
@@ -394,11 +400,39 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
         const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         sbits[u] = __float_as_uint(sc);
         if (valid) {
+          if (MP_QUANT_FAST_DIV && sc >= 0x1p-60f) {
+            // x / sc correctly rounded without a division per element (Markstein,
+            // "IA-64 and Elementary Functions", the division theorem: with y the
+            // correctly rounded 1/sc and q within one ulp of x / sc, the exact
+            // remainder r = x - sc*q (one FMA) gives RN(q + r*y) = RN(x / sc)).
+            // q0 = x*y is within 1.5 ulp; one correction brings it within one
+            // ulp, the second rounds it correctly.  sc >= 2^-60 keeps every
+            // remainder that matters for an e4m3 code exactly representable.
+            // The corrections turn -0 into +0 (0 - 0 = +0), so the sign of x,
+            // which x / sc always has, is put back.
+            const float y = __frcp_rn(sc);
 #pragma unroll
-          for (int j = 0; j < NB; ++j) {
-            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(f[4 * j + 1], sc), __fdiv_rn(f[4 * j], sc));
-            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(f[4 * j + 3], sc), __fdiv_rn(f[4 * j + 2], sc));
-            q[u][j] = lo | (hi << 16);
+            for (int j = 0; j < CPL; ++j) {
+              const float a = f[j];
+              float qv = __fmul_rn(a, y);
+              qv = __fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv);
+              f[j] = copysignf(__fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv), a);
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const uint32_t lo = cvt_e4m3x2(f[4 * j + 1], f[4 * j]);
+              const uint32_t hi = cvt_e4m3x2(f[4 * j + 3], f[4 * j + 2]);
+              q[u][j] = lo | (hi << 16);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const uint32_t lo =
+                  cvt_e4m3x2(__fdiv_rn(f[4 * j + 1], sc), __fdiv_rn(f[4 * j], sc));
+              const uint32_t hi =
+                  cvt_e4m3x2(__fdiv_rn(f[4 * j + 3], sc), __fdiv_rn(f[4 * j + 2], sc));
+              q[u][j] = lo | (hi << 16);
+            }
           }
         }
       }
@@ -709,11 +743,13 @@ cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const
 //  - 2 vectors per lane and unit, except 1 for the e4m3 gather (276 vs
 //    285 us);
 //  - one short block per kWarpsPerBlock units (the write-heavy policy above)
-//    for the MXFP8 dispatch (260 vs 296 us) and every gather (MXFP4 173 vs
-//    199 us, the FP8 ones 276-285 vs 321 us), but a persistent grid for the
-//    e4m3 dispatch, whose fp32 division per element makes it the most
-//    compute-heavy (279 vs 296 us), and for the MXFP4 dispatch, whose reads
-//    are a larger share of its traffic (184 vs 191 us);
+//    for the FP8 dispatches (MXFP8 260 vs 296 us; e4m3 269 vs 290 us) and
+//    every gather (MXFP4 173 vs 199 us, the FP8 ones 276-285 vs 321 us), but a
+//    persistent grid for the MXFP4 dispatch, whose reads are a larger share of
+//    its traffic (184 vs 191 us);
+//  - the e4m3 quantiser's reciprocal-and-two-FMA division (MP_QUANT_FAST_DIV)
+//    against a division per element: 269 vs 278 us for the dispatch (the best
+//    launch shape of each);
 //  - for MXFP4, 2 vectors per lane (190 us) beat 1 (211) and 4 (202).
 // MP_QUANT_CPL = 8, MP_QUANT_U_FP4 and MP_QUANT_PERSISTENT_MASK (bit
 // FMT + (GATHER ? 3 : 0) set = persistent grid) reproduce the other shapes.
@@ -721,11 +757,12 @@ cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const
 #define MP_QUANT_CPL 16
 #endif
 #ifndef MP_QUANT_PERSISTENT_MASK
-#define MP_QUANT_PERSISTENT_MASK 5
+#define MP_QUANT_PERSISTENT_MASK 4
 #endif
 #ifndef MP_QUANT_U_FP4
 #define MP_QUANT_U_FP4 2
 #endif
+
 
 template <int CPL, int U, int FMT, bool GATHER>
 static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void* out,

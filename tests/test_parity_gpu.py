@@ -701,6 +701,31 @@ def test_quantising_copies_from_a_16_byte_aligned_source(fmt):
 
 
 @pytest.mark.parametrize("fmt", sorted(QFMT))
+def test_quantisers_on_random_bit_patterns(fmt):
+    """67 M elements: random finite bf16 bit patterns, each scale block shifted by a random
+    power of two so that scales span most of the fp32 range; every code and scale must
+    equal the oracle's (R=1 gather = plain quantisation)."""
+    f = QFMT[fmt]
+    S, H = 16384, 4096
+    rng = np.random.default_rng(61)
+    bits = rng.integers(0, 1 << 16, (S, H), dtype=np.uint32).astype(np.uint16)
+    bits &= np.uint16(0x807F) | np.uint16(0x3F80)      # exponent field below 0x7F8: finite
+    shift = rng.integers(-110, 120, (S, H // f["block"]), dtype=np.int64).repeat(f["block"], 1)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() * torch.exp2(
+        torch.from_numpy(shift).float())
+    x = torch.nan_to_num(x, posinf=3.0e38, neginf=-3.0e38).to(torch.bfloat16)
+    out = torch.zeros((1, S, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    osc = torch.zeros((1, S, H // f["block"]), dtype=f["sdt"], device="cuda")
+    B.check(getattr(B, f["gather"])(1, H, [S], x.cuda(), out, osc))
+    torch.cuda.synchronize()
+    q, sc = _oracle_quant(fmt, x)
+    assert np.array_equal(osc[0].cpu().view(torch.uint8).numpy(), sc)
+    got = out[0].cpu().numpy()
+    bad = np.argwhere(got != q)
+    assert bad.size == 0, "first mismatches at %s" % bad[:5].tolist()
+
+
+@pytest.mark.parametrize("fmt", sorted(QFMT))
 def test_allgatherv_quantised_full_size(fmt):
     """The rsv shape (R=8, H=4096, sizes ~ U{0..16384}): every rank's copy equals the
     oracle's quantisation of the gathered rows."""
