@@ -517,9 +517,7 @@ def measure_other_rows(steps: int, peak: float):
     y = torch.randn((T, H), generator=g, device="cuda").to(torch.bfloat16)
 
     def skew_step():
-        B.check(plan.layout())
-        B.check(plan.dispatch())
-        B.check(plan.combine(y))
+        plan.step(y)
 
     ms_sk = timed(skew_step, steps)
     assert plan.device_error() == 0
@@ -583,11 +581,14 @@ def main():
     torch.cuda.synchronize()
     assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
     T = plan.num_recv()
-    nb = algorithmic_bytes(R, N, K, E, H, T, elt=2 if inp.dtype == "bf16" else 1,
+    ab = algorithmic_bytes(R, N, K, E, H, T, elt=2 if inp.dtype == "bf16" else 1,
                            scales_per_row=0 if inp.dtype == "bf16" else H // 128)
+    nb = {"layout_offsets": ab["layout"] + ab["offsets"], "rows": ab["rows"],
+          "combine": ab["combine"]}
+    nb["dispatch"] = nb["layout_offsets"] + nb["rows"]
 
     # timed region: K steps, per-phase CUDA events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -598,33 +599,30 @@ def main():
     for i in range(args.steps):
         e = ev[i]
         e[0].record(stream)
-        B.check(plan.layout())
+        B.check(plan.layout_and_offsets())
         e[1].record(stream)
-        B.check(plan.dispatch_offsets())
-        e[2].record(stream)
         B.check(plan.dispatch_rows())
-        e[3].record(stream)
+        e[2].record(stream)
         B.check(plan.combine(y))
-        e[4].record(stream)
+        e[3].record(stream)
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    ph = {"layout": 0.0, "offsets": 0.0, "rows": 0.0, "combine": 0.0}
+    ph = {"layout_offsets": 0.0, "rows": 0.0, "combine": 0.0}
     for e in ev:
-        ph["layout"] += e[0].elapsed_time(e[1])
-        ph["offsets"] += e[1].elapsed_time(e[2])
-        ph["rows"] += e[2].elapsed_time(e[3])
-        ph["combine"] += e[3].elapsed_time(e[4])
+        ph["layout_offsets"] += e[0].elapsed_time(e[1])
+        ph["rows"] += e[1].elapsed_time(e[2])
+        ph["combine"] += e[2].elapsed_time(e[3])
     ph = {k: v / args.steps for k, v in ph.items()}
-    ph["dispatch"] = ph["offsets"] + ph["rows"]
+    ph["dispatch"] = ph["layout_offsets"] + ph["rows"]
     assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
 
     total_ms = max_over_ranks(total_ms, world, device="cuda")
     ms_step = total_ms / args.steps
     tokens = R * N * world
     value = replica_throughput(R * N, args.steps, world, total_ms)
-    step_bytes = nb["layout"] + nb["offsets"] + nb["rows"] + nb["combine"]
+    step_bytes = nb["layout_offsets"] + nb["rows"] + nb["combine"]
     eff_gbs = step_bytes * world / (ms_step / 1e3) / 1e9
 
     # End to end through the public API with host buffers (pinned): every step
@@ -728,7 +726,7 @@ def main():
             "frac_of_measured_copy_peak": eff_gbs / world / peak,
             "receive_rows": T, "phases_ms": ph,
             "roofline": roofline, "other_rows": other, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps if N > 0 else 0, "clocks": clk,
+            "gpu_launches": 3 * args.steps if N > 0 else 0, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

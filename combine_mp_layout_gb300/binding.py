@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
         L.mp_allgatherv_mxfp4.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_dispatch_rows_mxfp4.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
         L.mp_dispatch_rows_bulk.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P]
+        L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
@@ -83,7 +84,8 @@ def lib() -> ctypes.CDLL:
                   "mp_dispatch_ll_rows", "mp_combine_ll",
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
-                  "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk"):
+                  "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk",
+                  "mp_layout_and_offsets"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -172,6 +174,24 @@ def mp_dispatch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_
                                   _dev(send_row, "send_row"), int(recv_capacity),
                                   _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
                                   _stream(stream))
+
+
+def mp_layout_and_offsets(R, N, K, E, topk_idx, topk_weights, recv_capacity,
+                          num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                          recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                          dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                          dev_err, workspace, stream=None) -> int:
+    return lib().mp_layout_and_offsets(
+        R, N, K, E, _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"),
+        int(recv_capacity), _dev(num_tokens_per_rank, "num_tokens_per_rank"),
+        _dev(num_tokens_per_expert, "num_tokens_per_expert"),
+        _dev(is_token_in_rank, "is_token_in_rank"), _dev(recv_src_rank, "recv_src_rank"),
+        _dev(recv_src_idx, "recv_src_idx"), _dev(recv_topk_idx, "recv_topk_idx"),
+        _dev(recv_topk_weights, "recv_topk_weights"), _dev(dest_offsets, "dest_offsets"),
+        _dev(rank_prefix, "rank_prefix"),
+        _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
+        _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _dev(workspace, "workspace"),
+        _stream(stream))
 
 
 def mp_dispatch_offsets_global(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,

@@ -33,6 +33,21 @@ static bool ep_shape_ok(int R, int N, int K, int E) {
   return true;
 }
 
+static int check_layout_args(int R, int N, int K, int E, const int32_t* topk_idx,
+                             const int32_t* num_tokens_per_rank,
+                             const int32_t* num_tokens_per_expert,
+                             const uint32_t* is_token_in_rank, const int32_t* dev_err,
+                             const void* workspace) {
+  if (!ep_shape_ok(R, N, K, E)) return MP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !dev_err || !workspace)
+    return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !is_token_in_rank)) return MP_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_rank) || !aligned4(num_tokens_per_expert) ||
+      !aligned4(is_token_in_rank) || !aligned4(dev_err) || !aligned16(workspace))
+    return MP_ERR_INVALID_ARG;
+  return MP_OK;
+}
+
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MP_OK : MP_ERR_CUDA; }
 
 }  // namespace mp
@@ -59,13 +74,9 @@ size_t mp_workspace_size(int R, int N, int E) {
 int mp_layout(int R, int N, int K, int E, const int32_t* topk_idx, int32_t* num_tokens_per_rank,
               int32_t* num_tokens_per_expert, uint32_t* is_token_in_rank, int32_t* dev_err,
               void* workspace, mp_stream_t stream) {
-  if (!ep_shape_ok(R, N, K, E)) return MP_ERR_INVALID_ARG;
-  if (!num_tokens_per_rank || !num_tokens_per_expert || !dev_err || !workspace)
-    return MP_ERR_INVALID_ARG;
-  if (N > 0 && (!topk_idx || !is_token_in_rank)) return MP_ERR_INVALID_ARG;
-  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_rank) || !aligned4(num_tokens_per_expert) ||
-      !aligned4(is_token_in_rank) || !aligned4(dev_err) || !aligned16(workspace))
-    return MP_ERR_INVALID_ARG;
+  const int st = check_layout_args(R, N, K, E, topk_idx, num_tokens_per_rank,
+                                   num_tokens_per_expert, is_token_in_rank, dev_err, workspace);
+  if (st != MP_OK) return st;
   return cuda_status(launch_layout(R, N, K, E, topk_idx, num_tokens_per_rank,
                                    num_tokens_per_expert, is_token_in_rank, dev_err,
                                    static_cast<unsigned char*>(workspace),
@@ -199,6 +210,42 @@ int mp_combine_weights(int R, int N, int K, const float* recv_topk_weights, int6
   return cuda_status(launch_combine_weights(R, int64_t(R) * N, K, recv_topk_weights, recv_rows,
                                             send_row, combined_topk_weights, dev_err,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
+                          const float* topk_weights, int64_t recv_capacity,
+                          int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                          uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+                          int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                          float* recv_topk_weights, int32_t* dest_offsets, int32_t* rank_prefix,
+                          int32_t* num_recv_tokens_per_expert, int32_t* send_row,
+                          int32_t* dev_err, void* workspace, mp_stream_t stream) {
+  int st = check_layout_args(R, N, K, E, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                             is_token_in_rank, dev_err, workspace);
+  if (st == MP_OK)
+    st = check_offsets_args(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                            num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                            recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                            dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                            dev_err, workspace);
+  if (st != MP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const cudaError_t e = launch_layout_scan(
+      R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
+      num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
+      recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
+      ws, cs);
+  if (e == cudaSuccess) return MP_OK;
+  if (e != cudaErrorNotSupported) return MP_ERR_CUDA;
+  if (launch_layout(R, N, K, E, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                    is_token_in_rank, dev_err, ws, cs) != cudaSuccess)
+    return MP_ERR_CUDA;
+  return cuda_status(launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                                 num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                                 recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                                 dest_offsets, rank_prefix, num_recv_tokens_per_expert,
+                                 send_row, dev_err, ws, cs));
 }
 
 int mp_dispatch_rows(int R, int N, int H, int dtype, const void* x, const float* x_scales,

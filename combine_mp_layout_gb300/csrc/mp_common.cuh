@@ -27,6 +27,8 @@ struct Control {
   uint32_t scan_epoch;         // tags tile records of the current scan launch
   uint32_t copy_unit_counter;  // reserved for dynamically scheduled copies
   uint32_t layout_done[MP_MAX_RANKS];  // layout blocks finished, per source rank
+  uint32_t bar_count;          // grid barrier of the fused layout + scan: arrivals
+  uint32_t bar_gen;            // ... and its generation
 };
 static_assert(sizeof(Control) <= 512, "control block");
 
@@ -67,14 +69,6 @@ inline __host__ __device__ int64_t ws_total_bytes(int R, int N, int E) {
 // ---------------------------------------------------------------------------
 // Memory-order helpers (PTX ISA memory consistency model, gpu scope).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -89,45 +83,14 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Streaming 16-byte accesses: payload rows are touched once, so keep them
-// out of L1.
-__device__ __forceinline__ int4 ld_stream(const int4* p) {
-  int4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ void st_stream(int4* p, const int4& v) {
-  asm volatile("st.global.L1::no_allocate.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// Vectors of NW 32-bit words (NW = 4: 16 bytes; NW = 8: 32 bytes, the
-// 256-bit global accesses sm_100-class GPUs provide).
+// Streaming vector accesses: payload rows are touched once, so they bypass
+// L1 (and loads are marked evict-first in L2).  Vectors of NW 32-bit words
+// (NW = 4: 16 bytes; NW = 8: 32 bytes, the 256-bit global accesses
+// sm_100-class GPUs provide).
 template <int NW>
 struct alignas(NW * 4) Words {
   uint32_t w[NW];
 };
-
-// Like ld_stream_w, but leaves the line in L2 with normal priority (for data
-// that other warps re-read shortly after).
-template <int NW>
-__device__ __forceinline__ Words<NW> ld_shared_l2_w(const Words<NW>* p) {
-  Words<NW> v;
-  if constexpr (NW == 8) {
-    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
-                   "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
-                 : "l"(p));
-  } else {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                 : "l"(p));
-  }
-  return v;
-}
 
 template <int NW>
 __device__ __forceinline__ Words<NW> ld_stream_w(const Words<NW>* p) {

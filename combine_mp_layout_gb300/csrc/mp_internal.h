@@ -24,6 +24,18 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                         int32_t* send_row, int32_t* dev_err, unsigned char* ws,
                         cudaStream_t stream, int global_ids = 0, int32_t sentinel = -1);
 
+// mp_k_layout + mp_k_scan as one cooperative launch; cudaErrorNotSupported
+// (nothing launched) when the problem does not fit one resident grid.
+cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_idx,
+                               const float* topk_weights, int64_t recv_capacity,
+                               int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                               uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+                               int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                               float* recv_topk_weights, int32_t* dest_offsets,
+                               int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                               int32_t* send_row, int32_t* dev_err, unsigned char* ws,
+                               cudaStream_t stream);
+
 // Low-latency offsets, expert-major (rank_major = 0: bins are experts) or
 // rank-major (1: bins are the ranks owning the experts); one block per source
 // rank.

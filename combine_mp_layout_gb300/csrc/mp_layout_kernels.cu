@@ -157,6 +157,155 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
   return v;
 }
 
+// Warp 0 of a scan tile: the tile's count per destination and per-warp
+// offsets from the ballots, then its record (aggregate, or inclusive for a
+// rank's first tile) and the decoupled lookback over the rank's earlier
+// tiles.  Returns, in lane d, the rows of destination d in this rank's
+// earlier tiles; tcount[d] ends as the inclusive prefix through this tile.
+__device__ __forceinline__ uint32_t tile_publish_lookback(
+    int R, int64_t tile, int c, int src_rank, int C, uint32_t epoch,
+    const uint32_t (*wball)[MP_MAX_RANKS], int32_t (*woff)[MP_MAX_RANKS], uint32_t* tcount,
+    uint32_t* tcnt, uint32_t* flags, uint32_t* agg, uint32_t* incl, int32_t* dev_err) {
+  const int lane = threadIdx.x & 31;
+  // lane d: the tile's count for destination d and the per-warp offsets
+  uint32_t cnt = 0;
+  if (lane < R) {
+    for (int w = 0; w < kScanWarps; ++w) {
+      woff[w][lane] = int32_t(cnt);
+      cnt += __popc(wball[w][lane]);
+    }
+    tcount[lane] = cnt;
+    tcnt[lane] = cnt;
+  }
+  __syncwarp();
+  const int64_t rec = int64_t(tile) * R;
+  uint32_t excl = 0;  // lane d: rows of destination d in this rank's earlier tiles
+  if (c == 0) {
+    if (lane == 0) {
+      for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
+      st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
+    }
+  } else {
+    if (lane == 0) {
+      for (int d = 0; d < R; ++d) agg[rec + d] = tcount[d];
+      st_release_u32(&flags[tile], make_flag(epoch, kStatusAggregate));
+    }
+    // Look back over up to 32 earlier tiles of this rank at a time (lane j
+    // looks at tile base - j), stopping at the nearest one whose inclusive
+    // prefix is out.  Every wait is bounded (MP_ERR_TIMEOUT).
+    const int64_t first = int64_t(src_rank) * C;
+    bool timed_out = false;
+    for (int64_t base = int64_t(tile) - 1; base >= first; base -= 32) {
+      const int64_t p = base - lane;
+      uint32_t status = 0;
+      if (p >= first) {
+        uint32_t f = ld_acquire_u32(&flags[p]);
+        uint32_t spins = 0, nap = 32;
+        while ((f >> 2) != epoch || (f & 3u) == 0) {
+          if (++spins > kSpinLimit) { timed_out = true; break; }
+          __nanosleep(nap);
+          if (nap < 1024) nap <<= 1;
+          f = ld_acquire_u32(&flags[p]);
+        }
+        status = timed_out ? kStatusInclusive : (f & 3u);
+      }
+      const unsigned inclusive = __ballot_sync(kFull, p >= first && status == kStatusInclusive);
+      const int stop = inclusive ? __ffs(inclusive) - 1 : 31;
+      const bool use = p >= first && lane <= stop && !timed_out;
+      const uint32_t* src = status == kStatusInclusive ? incl : agg;
+      uint32_t v[MP_MAX_RANKS];
+#pragma unroll
+      for (int d = 0; d < MP_MAX_RANKS; ++d)
+        v[d] = (use && d < R) ? __ldcg(src + p * R + d) : 0u;
+#pragma unroll
+      for (int d = 0; d < MP_MAX_RANKS; ++d) {
+        if (d < R) {
+          const uint32_t sum = warp_sum(v[d]);
+          if (lane == d) excl += sum;
+        }
+      }
+      if (__any_sync(kFull, timed_out) || inclusive) break;
+    }
+    if (__any_sync(kFull, timed_out) && lane == 0) raise_error(dev_err, MP_ERR_TIMEOUT);
+    if (lane < R) tcount[lane] += excl;  // inclusive prefix through this tile
+    __syncwarp();
+    if (lane == 0) {
+      for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
+      st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
+    }
+  }
+  return excl;
+}
+
+// The rows of one scan tile: each token's row at each destination is staged
+// in shared memory (send_row) and as a per-destination token list, so that
+// the stores run along contiguous rows (a tile's rows for one destination are
+// consecutive).  Called by all threads of the block; needs the tile's masks
+// (one per token thread), the per-warp ballots and offsets, the tile's first
+// row and row count per destination, and its top-k ids and weights staged in
+// shared memory.
+__device__ __forceinline__ void write_tile_rows(
+    const ScanArgs& a, uint32_t mask, int ntok, int t0, int64_t g0, int src_rank,
+    const uint32_t (*wball)[MP_MAX_RANKS], const int32_t (*woff)[MP_MAX_RANKS],
+    const int64_t* row_base, const uint32_t* tcnt, const int32_t* idx_s, const float* w_s,
+    int32_t* sr_s, uint8_t (*tok_of)[kScanTokens]) {
+  const int R = a.R, K = a.K, E = a.E;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // Each token's row at each destination: staged in shared memory (send_row)
+  // and as a per-destination token list, so that the stores below run along
+  // contiguous rows (a tile's rows for one destination are consecutive).
+  if (tid < ntok) {
+    for (int d = 0; d < R; ++d) {
+      int32_t out = -1;
+      if ((mask >> d) & 1u) {
+        const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
+        tok_of[d][rank] = uint8_t(tid);
+        const int64_t row = row_base[d] + rank;
+        if (row < a.recv_capacity) out = int32_t(row);
+      }
+      sr_s[tid * R + d] = out;
+    }
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sr_s[i];
+  {
+    const int El = E / R;
+    const int step_r = kScanThreads / K, step_k = kScanThreads - step_r * K;
+    bool overflow = false;
+    for (int d = 0; d < R; ++d) {
+      const int64_t base = row_base[d];
+      const int cnt = int(tcnt[d]);
+      const int64_t room = a.recv_capacity - base;
+      const int n_ok = room <= 0 ? 0 : (room < cnt ? int(room) : cnt);
+      overflow |= n_ok < cnt;
+#pragma unroll 4
+      for (int i = tid; i < n_ok; i += kScanThreads) {
+        a.recv_src_rank[base + i] = src_rank;
+        a.recv_src_idx[base + i] = t0 + tok_of[d][i];
+      }
+      const int lo = d * El, hi = lo + El;
+      // element i = r*K + k of this destination's rows; (r, k) advance by
+      // (kScanThreads / K, kScanThreads % K) per step, avoiding a division
+      int r = tid / K, k = tid - (tid / K) * K;
+#pragma unroll 4
+      for (int i = tid; i < n_ok * K; i += kScanThreads) {
+        const int tk = tok_of[d][r];
+        const int e = idx_s[tk * K + k];
+        const bool local = e >= lo && e < hi;
+        a.recv_topk_idx[base * K + i] =
+            a.global_ids ? (local ? e : a.sentinel) : (local ? e - lo : -1);
+        a.recv_topk_weights[base * K + i] = local ? w_s[tk * K + k] : 0.0f;
+        r += step_r;
+        k += step_k;
+        if (k >= K) { k -= K; ++r; }
+      }
+    }
+    if (overflow && tid == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
+  }
+
+}
+
 __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   extern __shared__ int32_t sm_scan[];
   int32_t* idx_s = sm_scan;                                             // [kScanTokens * K]
@@ -216,73 +365,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   __syncthreads();
 
   if (warp == 0) {
-    // lane d: the tile's count for destination d and the per-warp offsets
-    uint32_t cnt = 0;
-    if (lane < R) {
-      for (int w = 0; w < kScanWarps; ++w) {
-        woff[w][lane] = int32_t(cnt);
-        cnt += __popc(wball[w][lane]);
-      }
-      tcount[lane] = cnt;
-      tcnt[lane] = cnt;
-    }
-    __syncwarp();
-    const int64_t rec = int64_t(tile) * R;
-    uint32_t excl = 0;  // lane d: rows of destination d in this rank's earlier tiles
-    if (c == 0) {
-      if (lane == 0) {
-        for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
-        st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
-      }
-    } else {
-      if (lane == 0) {
-        for (int d = 0; d < R; ++d) agg[rec + d] = tcount[d];
-        st_release_u32(&flags[tile], make_flag(epoch, kStatusAggregate));
-      }
-      // Look back over up to 32 earlier tiles of this rank at a time (lane j
-      // looks at tile base - j), stopping at the nearest one whose inclusive
-      // prefix is out.  Every wait is bounded (MP_ERR_TIMEOUT).
-      const int64_t first = int64_t(src_rank) * C;
-      bool timed_out = false;
-      for (int64_t base = int64_t(tile) - 1; base >= first; base -= 32) {
-        const int64_t p = base - lane;
-        uint32_t status = 0;
-        if (p >= first) {
-          uint32_t f = ld_acquire_u32(&flags[p]);
-          uint32_t spins = 0, nap = 32;
-          while ((f >> 2) != epoch || (f & 3u) == 0) {
-            if (++spins > kSpinLimit) { timed_out = true; break; }
-            __nanosleep(nap);
-            if (nap < 1024) nap <<= 1;
-            f = ld_acquire_u32(&flags[p]);
-          }
-          status = timed_out ? kStatusInclusive : (f & 3u);
-        }
-        const unsigned inclusive = __ballot_sync(kFull, p >= first && status == kStatusInclusive);
-        const int stop = inclusive ? __ffs(inclusive) - 1 : 31;
-        const bool use = p >= first && lane <= stop && !timed_out;
-        const uint32_t* src = status == kStatusInclusive ? incl : agg;
-        uint32_t v[MP_MAX_RANKS];
-#pragma unroll
-        for (int d = 0; d < MP_MAX_RANKS; ++d)
-          v[d] = (use && d < R) ? __ldcg(src + p * R + d) : 0u;
-#pragma unroll
-        for (int d = 0; d < MP_MAX_RANKS; ++d) {
-          if (d < R) {
-            const uint32_t sum = warp_sum(v[d]);
-            if (lane == d) excl += sum;
-          }
-        }
-        if (__any_sync(kFull, timed_out) || inclusive) break;
-      }
-      if (__any_sync(kFull, timed_out) && lane == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
-      if (lane < R) tcount[lane] += excl;  // inclusive prefix through this tile
-      __syncwarp();
-      if (lane == 0) {
-        for (int d = 0; d < R; ++d) incl[rec + d] = tcount[d];
-        st_release_u32(&flags[tile], make_flag(epoch, kStatusInclusive));
-      }
-    }
+    const uint32_t excl = tile_publish_lookback(R, tile, c, src_rank, C, epoch, wball, woff,
+                                                tcount, tcnt, flags, agg, incl, a.dev_err);
     // first row of this tile at d: rows of destinations < d (an exclusive
     // warp scan of the per-destination totals), rows of d from source ranks
     // < src_rank, rows of d from this rank's earlier tiles
@@ -325,58 +409,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   }
   __syncthreads();
 
-  // Each token's row at each destination: staged in shared memory (send_row)
-  // and as a per-destination token list, so that the stores below run along
-  // contiguous rows (a tile's rows for one destination are consecutive).
-  if (tid < ntok) {
-    for (int d = 0; d < R; ++d) {
-      int32_t out = -1;
-      if ((mask >> d) & 1u) {
-        const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
-        tok_of[d][rank] = uint8_t(tid);
-        const int64_t row = row_base[d] + rank;
-        if (row < a.recv_capacity) out = int32_t(row);
-      }
-      sr_s[tid * R + d] = out;
-    }
-  }
-  __syncthreads();
-#pragma unroll 4
-  for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sr_s[i];
-  {
-    const int El = E / R;
-    const int step_r = kScanThreads / K, step_k = kScanThreads - step_r * K;
-    bool overflow = false;
-    for (int d = 0; d < R; ++d) {
-      const int64_t base = row_base[d];
-      const int cnt = int(tcnt[d]);
-      const int64_t room = a.recv_capacity - base;
-      const int n_ok = room <= 0 ? 0 : (room < cnt ? int(room) : cnt);
-      overflow |= n_ok < cnt;
-#pragma unroll 4
-      for (int i = tid; i < n_ok; i += kScanThreads) {
-        a.recv_src_rank[base + i] = src_rank;
-        a.recv_src_idx[base + i] = t0 + tok_of[d][i];
-      }
-      const int lo = d * El, hi = lo + El;
-      // element i = r*K + k of this destination's rows; (r, k) advance by
-      // (kScanThreads / K, kScanThreads % K) per step, avoiding a division
-      int r = tid / K, k = tid - (tid / K) * K;
-#pragma unroll 4
-      for (int i = tid; i < n_ok * K; i += kScanThreads) {
-        const int tk = tok_of[d][r];
-        const int e = idx_s[tk * K + k];
-        const bool local = e >= lo && e < hi;
-        a.recv_topk_idx[base * K + i] =
-            a.global_ids ? (local ? e : a.sentinel) : (local ? e - lo : -1);
-        a.recv_topk_weights[base * K + i] = local ? w_s[tk * K + k] : 0.0f;
-        r += step_r;
-        k += step_k;
-        if (k >= K) { k -= K; ++r; }
-      }
-    }
-    if (overflow && tid == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
-  }
+  write_tile_rows(a, mask, ntok, t0, g0, src_rank, wball, woff, row_base, tcnt, idx_s, w_s, sr_s,
+                  tok_of);
 
   // the last block out resets the counters and moves to the next epoch
   __syncthreads();
@@ -391,6 +425,239 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
     ctl->copy_unit_counter = 0;
     __threadfence();
     atomicAdd(&ctl->scan_epoch, 1u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Layout and receive offsets in one cooperative launch (the work of mp_k_layout
+// followed by mp_k_scan, for callers of mp_layout_and_offsets).  Every block
+// is resident at once, so blocks own tiles statically (tile = blockIdx.x +
+// i * gridDim.x, in increasing order, which keeps each lookback's
+// predecessors running or done) and may meet at one grid barrier:
+//  1. per tile: the top-k ids give each token's rank mask (is_token_in_rank)
+//     and the tile's expert counts (added into the rank's accumulator); the
+//     tile publishes its per-destination counts and looks back over its
+//     rank's earlier tiles (the segmented decoupled lookback of mp_k_scan);
+//  2. grid barrier (bounded);
+//  3. each rank's last tile holds num_tokens_per_rank; from it every block
+//     forms rank_prefix and the destination bases, the accumulators give
+//     num_tokens_per_expert and num_recv_tokens_per_expert (and are zeroed),
+//     and each tile writes its send_row entries and receive metadata.
+// ---------------------------------------------------------------------------
+constexpr int kFusedMaxTiles = 16;  // tiles one block may own (tiles <= 16 * grid)
+
+struct FusedArgs {
+  ScanArgs a;                      // receive-side outputs (its layout inputs unused)
+  uint32_t* is_token_in_rank;      // [R][N] out
+  int32_t* num_tokens_per_rank;    // [R][R] out
+  int32_t* num_tokens_per_expert;  // [R][E] out
+};
+
+// Grid barrier for a cooperative launch: thread 0 of each block reads the
+// generation, arrives, and waits (bounded) for the last arrival to advance
+// it.  Returns false when the wait gave up.
+__device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, int* ok_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t gen = ld_acquire_u32(&ctl->bar_gen);
+    __threadfence();
+    if (atomicAdd(&ctl->bar_count, 1u) == nblocks - 1) {
+      atomicExch(&ctl->bar_count, 0u);
+      __threadfence();
+      st_release_u32(&ctl->bar_gen, gen + 1u);
+    } else {
+      uint32_t spins = 0;
+      while (ld_acquire_u32(&ctl->bar_gen) == gen) {
+        if (++spins > kSpinLimit) { ok = 0; break; }
+        __nanosleep(32);
+      }
+    }
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+__global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
+  const ScanArgs& a = f.a;
+  extern __shared__ int32_t sm_scan[];
+  int32_t* idx_s = sm_scan;                                             // [kScanTokens * K]
+  float* w_s = reinterpret_cast<float*>(sm_scan + kScanTokens * a.K);  // [kScanTokens * K]
+  int32_t* sr_s = sm_scan + 2 * kScanTokens * a.K;                      // [kScanTokens * R]
+  int32_t* hist = sr_s + kScanTokens * a.R;                             // [E]
+  __shared__ int32_t ntpr_s[MP_MAX_RANKS * MP_MAX_RANKS];  // num_tokens_per_rank
+  __shared__ uint32_t wball[kScanWarps][MP_MAX_RANKS];
+  __shared__ int32_t woff[kScanWarps][MP_MAX_RANKS];
+  __shared__ uint32_t tcount[MP_MAX_RANKS];
+  __shared__ uint32_t tcnt[MP_MAX_RANKS];
+  __shared__ int64_t row_base[MP_MAX_RANKS];
+  __shared__ int64_t dest_base[MP_MAX_RANKS];
+  __shared__ uint8_t tok_of[MP_MAX_RANKS][kScanTokens];
+  __shared__ uint32_t tile_excl[kFusedMaxTiles][MP_MAX_RANKS];
+  __shared__ uint32_t sh_epoch;
+  __shared__ int sh_bad, sh_ok;
+
+  const int R = a.R, N = a.N, K = a.K, E = a.E, El = E / R;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Control* ctl = reinterpret_cast<Control*>(a.ws);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(a.ws + ws_flags_offset(R, E));
+  uint32_t* agg = reinterpret_cast<uint32_t*>(a.ws + ws_agg_offset(R, N, E));
+  uint32_t* incl = reinterpret_cast<uint32_t*>(a.ws + ws_incl_offset(R, N, E));
+  int32_t* acc = reinterpret_cast<int32_t*>(a.ws + ws_acc_offset());  // [R][E + R]
+  const int C = int(scan_tiles_per_rank(N));
+  const int T = R * C;
+  if (tid == 0) {
+    sh_epoch = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
+    sh_bad = 0;
+  }
+  __syncthreads();
+  const uint32_t epoch = sh_epoch;
+  // A block that owns a single tile keeps that tile's ids, weights, ballots
+  // and offsets in shared memory across the barrier instead of reloading them.
+  const bool single = T <= int(gridDim.x);
+
+  // 1. layout work and the per-rank lookback, tile by tile
+  int it = 0;
+  for (int tile = blockIdx.x; tile < T; tile += gridDim.x, ++it) {
+    const int s = tile / C, c = tile - s * C;
+    const int t0 = c * kScanTokens, ntok = min(kScanTokens, N - t0);
+    const int64_t g0 = int64_t(s) * N + t0;
+    for (int i = tid; i < E; i += kScanThreads) hist[i] = 0;
+    {
+      const int n = ntok * K;
+      const int32_t* gi = a.topk_idx + g0 * K;
+      const float* gw = a.topk_weights + g0 * K;
+#pragma unroll 4
+      for (int i = tid; i < n; i += kScanThreads) {
+        idx_s[i] = __ldg(gi + i);
+        if (single) w_s[i] = __ldg(gw + i);
+      }
+    }
+    __syncthreads();
+    uint32_t mask = 0;
+    if (tid < ntok) {
+      bool bad = false;
+      for (int k = 0; k < K; ++k) {
+        const int e = idx_s[tid * K + k];
+        if (e == -1) continue;
+        if (e < -1 || e >= E) { bad = true; continue; }
+        atomicAdd(&hist[e], 1);
+        mask |= 1u << (e / El);
+      }
+      f.is_token_in_rank[g0 + tid] = mask;
+      if (bad) sh_bad = 1;
+    }
+    for (int d = 0; d < R; ++d) {
+      const unsigned b = __ballot_sync(kFull, (mask >> d) & 1u);
+      if (lane == 0) wball[warp][d] = b;
+    }
+    __syncthreads();
+    int32_t* acc_s = acc + int64_t(s) * (E + R);
+    for (int i = tid; i < E; i += kScanThreads)
+      if (hist[i]) atomicAdd(&acc_s[i], hist[i]);
+    if (warp == 0) {
+      const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, epoch, wball, woff, tcount,
+                                                  tcnt, flags, agg, incl, a.dev_err);
+      if (lane < R) tile_excl[it][lane] = excl;
+    }
+    __syncthreads();  // hist, idx_s and the ballots are reused by the next tile
+  }
+  if (tid == 0 && sh_bad) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
+  __threadfence();
+
+  // 2. every tile is published and every expert count added
+  if (!grid_barrier(ctl, gridDim.x, &sh_ok)) {
+    if (tid == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
+    return;
+  }
+
+  // 3. totals, tables, rows
+  for (int i = tid; i < R * R; i += kScanThreads) {  // rank s's last tile: its totals
+    const int s = i / R, d = i - s * R;
+    ntpr_s[i] = int32_t(__ldcg(incl + (int64_t(s) * C + C - 1) * R + d));
+  }
+  __syncthreads();
+  if (warp == 0) {  // first receive row of each destination
+    int64_t tot = 0;
+    if (lane < R)
+      for (int s = 0; s < R; ++s) tot += ntpr_s[s * R + lane];
+    int64_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane < R) dest_base[lane] = inc - tot;
+    if (blockIdx.x == 0 && lane < R) {
+      a.dest_offsets[lane] = int32_t(inc - tot);
+      if (lane == R - 1) a.dest_offsets[R] = int32_t(inc);
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < R * R; i += kScanThreads) {
+      const int s = i / R, d = i - s * R;
+      int pre = 0;
+      for (int q = 0; q < s; ++q) pre += ntpr_s[q * R + d];
+      f.num_tokens_per_rank[i] = ntpr_s[i];
+      a.rank_prefix[i] = pre;
+    }
+    if (tid == 0) atomicAdd(&ctl->scan_epoch, 1u);  // every lookback of this launch is done
+  }
+  // (the last blocks of the grid, so that block 0's tables do not add up)
+  for (int64_t e = int64_t(gridDim.x - 1 - blockIdx.x) * kScanThreads + tid; e < E;
+       e += int64_t(gridDim.x) * kScanThreads) {
+    int sum = 0;
+    for (int s = 0; s < R; ++s) {
+      int32_t* p = acc + int64_t(s) * (E + R) + e;
+      const int v = __ldcg(p);
+      *p = 0;
+      f.num_tokens_per_expert[int64_t(s) * E + e] = v;
+      sum += v;
+    }
+    a.num_recv_tokens_per_expert[e] = sum;
+  }
+  __syncthreads();
+  it = 0;
+  for (int tile = blockIdx.x; tile < T; tile += gridDim.x, ++it) {
+    const int s = tile / C, c = tile - s * C;
+    const int t0 = c * kScanTokens, ntok = min(kScanTokens, N - t0);
+    const int64_t g0 = int64_t(s) * N + t0;
+    const uint32_t mask = tid < ntok ? __ldcg(f.is_token_in_rank + g0 + tid) : 0u;
+    if (!single) {  // ids, weights, ballots and offsets of this tile
+      {
+        const int n = ntok * K;
+        const int32_t* gi = a.topk_idx + g0 * K;
+        const float* gw = a.topk_weights + g0 * K;
+#pragma unroll 4
+        for (int i = tid; i < n; i += kScanThreads) {
+          idx_s[i] = __ldg(gi + i);
+          w_s[i] = __ldg(gw + i);
+        }
+      }
+      for (int d = 0; d < R; ++d) {
+        const unsigned b = __ballot_sync(kFull, (mask >> d) & 1u);
+        if (lane == 0) wball[warp][d] = b;
+      }
+      __syncthreads();
+      if (warp == 0 && lane < R) {
+        uint32_t cnt = 0;
+        for (int w = 0; w < kScanWarps; ++w) {
+          woff[w][lane] = int32_t(cnt);
+          cnt += __popc(wball[w][lane]);
+        }
+        tcnt[lane] = cnt;
+      }
+    }
+    if (warp == 0 && lane < R) {
+      int64_t pre = 0;
+      for (int q = 0; q < s; ++q) pre += ntpr_s[q * R + lane];
+      row_base[lane] = dest_base[lane] + pre + tile_excl[it][lane];
+    }
+    __syncthreads();
+    write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s, sr_s,
+                    tok_of);
+    __syncthreads();
   }
 }
 
@@ -629,6 +896,57 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                        stream, a);
 }
 
+
+// Returns cudaErrorNotSupported (nothing launched) when the problem does not
+// fit one cooperative grid; the caller then runs mp_k_layout and mp_k_scan.
+cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_idx,
+                               const float* topk_weights, int64_t recv_capacity,
+                               int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                               uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+                               int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                               float* recv_topk_weights, int32_t* dest_offsets,
+                               int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                               int32_t* send_row, int32_t* dev_err, unsigned char* ws,
+                               cudaStream_t stream) {
+  if (N == 0) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+  static thread_local int coop[64] = {0};  // 0 unknown, 1 supported, -1 not
+  if (coop[dev] == 0) {
+    int v = 0;
+    coop[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
+                 v) ? 1 : -1;
+  }
+  if (coop[dev] < 0) return cudaErrorNotSupported;
+  const size_t smem =
+      sizeof(int32_t) * (size_t(kScanTokens) * (2 * size_t(K) + size_t(R)) + size_t(E));
+  static thread_local int configured[64] = {0};
+  if (smem > 48 * 1024 && configured[dev] < int(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(mp_k_layout_scan,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cudaErrorNotSupported;
+    configured[dev] = int(smem);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mp_k_layout_scan, kScanThreads,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    return cudaErrorNotSupported;
+  const int64_t tiles = scan_tiles(R, N);
+  const int64_t cap = int64_t(per_sm) * sm_count();
+  const int64_t grid = tiles < cap ? tiles : cap;
+  if (tiles > grid * kFusedMaxTiles) return cudaErrorNotSupported;
+  FusedArgs f{ScanArgs{R, N, K, E, topk_idx, topk_weights, is_token_in_rank, num_tokens_per_rank,
+                       num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx,
+                       recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
+                       num_recv_tokens_per_expert, send_row, dev_err, ws, 0, -1},
+              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert};
+  void* args[] = {&f};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mp_k_layout_scan),
+                                     dim3(unsigned(grid)), dim3(kScanThreads), args, smem,
+                                     stream);
+}
 }  // namespace mp
 
 namespace mp {

@@ -80,6 +80,16 @@ class EPPlan:
             self.dest_offsets, self.rank_prefix, self.num_recv_tokens_per_expert, self.send_row,
             self.dev_err, self.workspace, stream)
 
+    def layout_and_offsets(self, stream=None) -> int:
+        """mp_layout + mp_dispatch_offsets in one call (one cooperative launch when the
+        problem fits one resident grid)."""
+        return B.mp_layout_and_offsets(
+            self.R, self.N, self.K, self.E, self.topk_idx, self.topk_weights, self.cap,
+            self.num_tokens_per_rank, self.num_tokens_per_expert, self.is_token_in_rank,
+            self.recv_src_rank, self.recv_src_idx, self.recv_topk_idx, self.recv_topk_weights,
+            self.dest_offsets, self.rank_prefix, self.num_recv_tokens_per_expert, self.send_row,
+            self.dev_err, self.workspace, stream)
+
     def dispatch_offsets(self, stream=None) -> int:
         return B.mp_dispatch_offsets(
             self.R, self.N, self.K, self.E, self.topk_idx, self.topk_weights,
@@ -105,9 +115,10 @@ class EPPlan:
                             self.dev_err, stream)
 
     def step(self, y: torch.Tensor | None = None, stream=None) -> None:
-        """One pass of the hot path: layout -> dispatch -> combine."""
-        B.check(self.layout(stream), "mp_layout")
-        B.check(self.dispatch(stream), "mp_dispatch")
+        """One pass of the hot path: layout -> dispatch -> combine (layout and receive
+        offsets in one call, then the row copy, then combine)."""
+        B.check(self.layout_and_offsets(stream), "mp_layout_and_offsets")
+        B.check(self.dispatch_rows(stream=stream), "mp_dispatch_rows")
         B.check(self.combine(y, stream), "mp_combine")
 
     def num_recv(self) -> int:

@@ -186,6 +186,31 @@ int mp_dispatch_rows(int R, int N, int H, int dtype, const void *x, const float 
                      float *recv_scales, mp_stream_t stream);
 
 /*
+ * mp_layout_and_offsets -- mp_layout followed by mp_dispatch_offsets in one
+ * call (no counterpart in the pages: the same two steps, fused).  Where the
+ * problem fits one resident grid (R * ceil(N / 128) tiles of 128 tokens, at
+ * most 16 per block of the grid the GPU holds at once) the two steps run as
+ * one cooperative launch: each tile computes its tokens' rank masks and
+ * expert counts, publishes its per-destination counts and looks back over
+ * its rank's earlier tiles; after one grid barrier every tile writes its
+ * rows.  Otherwise the two launches of mp_layout and mp_dispatch_offsets run.
+ *   Arguments: those of mp_layout (outputs num_tokens_per_rank,
+ *   num_tokens_per_expert, is_token_in_rank) and of mp_dispatch_offsets
+ *   (its receive-side outputs); the results are identical to the two calls.
+ *   Checks and device errors as the two calls, plus MP_ERR_TIMEOUT when the
+ *   grid barrier's bounded (~1 s) wait gives up (the workspace must then be
+ *   zero-filled again).
+ */
+int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
+                          const float *topk_weights, int64_t recv_capacity,
+                          int32_t *num_tokens_per_rank, int32_t *num_tokens_per_expert,
+                          uint32_t *is_token_in_rank, int32_t *recv_src_rank,
+                          int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                          float *recv_topk_weights, int32_t *dest_offsets, int32_t *rank_prefix,
+                          int32_t *num_recv_tokens_per_expert, int32_t *send_row,
+                          int32_t *dev_err, void *workspace, mp_stream_t stream);
+
+/*
  * mp_dispatch_offsets_global -- mp_dispatch_offsets with the receive rows'
  * expert ids in global numbering ([EP] the later variant that returns
  * global token-major expert ids with a configurable invalid-expert

@@ -197,6 +197,12 @@ def test_newer_entry_points_reject(L):
         B.MP_ERR_INVALID_ARG                                                            # dev_err
     assert L.mp_dispatch_rows_bulk(2, 8, 60, B.MP_BF16, P, N0, P, 16, P, N0, P, N0) == \
         B.MP_ERR_INVALID_ARG                                                            # H % 8
+    L.mp_layout_and_offsets.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int64] + [ctypes.c_void_p] * 14
+    assert L.mp_layout_and_offsets(2, 8, 2, 7, P, P, 16, *([P] * 13), N0) == \
+        B.MP_ERR_INVALID_ARG  # E % R
+    assert L.mp_layout_and_offsets(2, 8, 2, 8, P, P, 16, *([P] * 12), N0, N0) == \
+        B.MP_ERR_INVALID_ARG  # workspace
     neg = (ctypes.c_int64 * 2)(3, -1)
     assert L.mp_allgatherv_mxfp8(2, 64, neg, P, P, P, N0) == B.MP_ERR_INVALID_ARG      # size < 0
     L.mp_dispatch_noalloc.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + \

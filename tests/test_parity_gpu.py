@@ -89,6 +89,20 @@ def compare_ep(inp: wl.EPInputs, plan: EPPlan, recv_capacity=None, y_bits=None,
     return out
 
 
+def run_gpu_fused(inp: wl.EPInputs, recv_capacity=None, y: torch.Tensor | None = None,
+                  repeat: int = 1) -> EPPlan:
+    """As run_gpu, with mp_layout_and_offsets in place of mp_layout + mp_dispatch_offsets."""
+    plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H, inp.dtype, recv_capacity)
+    plan.load(inp)
+    for _ in range(repeat):
+        plan.dev_err.zero_()
+        B.check(plan.layout_and_offsets(), "mp_layout_and_offsets")
+        B.check(plan.dispatch_rows(), "mp_dispatch_rows")
+        B.check(plan.combine(y), "mp_combine")
+    torch.cuda.synchronize()
+    return plan
+
+
 # ---------------------------------------------------------------------------
 # small and fuzzed shapes
 # ---------------------------------------------------------------------------
@@ -366,6 +380,50 @@ def test_bulk_copy_dispatch_matches_the_oracle(dtype, shape, cap_frac):
     if xs is not None:
         assert np.array_equal(plan.recv_scales[:n].cpu().numpy().view(np.uint32),
                               out["recv_scales"][:n].view(np.uint32))
+
+
+FUSED = [(1, 100, 4, 2, 64), (3, 300, 12, 3, 264), (8, 1000, 64, 8, 520), (16, 130, 32, 3, 96),
+         (32, 40, 64, 8, 16), (7, 777, 28, 28, 24), (2, 9000, 8, 3, 16),
+         (8, 20000, 32, 4, 16)]  # the last: more tiles than blocks, so blocks own several
+
+
+@pytest.mark.parametrize("shape", FUSED, ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
+def test_fused_layout_and_offsets(shape):
+    """One cooperative launch for layout + offsets: the oracle's results, repeatedly
+    (the workspace's barrier words, epochs and accumulators are reused)."""
+    R, N, E, K, H = shape
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"),
+                     seed=R * 1000 + N + 1)
+    if K < E:
+        idx = inp.topk_idx.copy()
+        idx[np.random.default_rng(N).random(idx.shape) < 0.1] = -1
+        idx[:, ::13, :] = -1
+        inp.topk_idx = idx
+    y = wl.random_bf16((R * N * min(R, K), H), seed=N + 1)
+    plan = run_gpu_fused(inp, y=y.cuda(), repeat=3)
+    compare_ep(inp, plan, y_bits=wl.bf16_bits(y))
+
+
+@pytest.mark.parametrize("name", ["dsv3", "skew"])
+def test_fused_layout_and_offsets_full_size(name):
+    inp = wl.make_ep(name, seed=0)
+    plan = run_gpu_fused(inp, repeat=2)
+    compare_ep(inp, plan)
+
+
+def test_fused_layout_and_offsets_capacity_and_bad_ids():
+    inp = wl.make_ep(dict(R=4, N=300, E=16, K=4, H=64, routing="uniform", dtype="bf16"), seed=4)
+    inp.topk_idx[2, 5, 1] = 99
+    plan = run_gpu_fused(inp, recv_capacity=700)
+    compare_ep(inp, plan, recv_capacity=700, expect_err=B.MP_ERR_CAPACITY | B.MP_ERR_BAD_EXPERT)
+
+
+def test_fused_layout_and_offsets_falls_back_beyond_one_grid():
+    """R=32 x 40,000 tokens is 10,016 tiles, more than 16 per block of a resident grid:
+    the call runs the two kernels instead, with the same results."""
+    inp = wl.make_ep(dict(R=32, N=40000, E=64, K=2, H=8, routing="uniform", dtype="bf16"), seed=5)
+    plan = run_gpu_fused(inp)
+    compare_ep(inp, plan)
 
 
 def test_empty_tokens():
