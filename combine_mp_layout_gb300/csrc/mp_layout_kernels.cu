@@ -19,6 +19,7 @@
 // metadata.  Tiles are handed out in launch order through an atomic
 // counter, so every tile a block waits on belongs to a block that is
 // already running.
+#include <cstddef>
 #include <cstdint>
 
 #include "mp_common.cuh"
@@ -445,6 +446,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 //     and each tile writes its send_row entries and receive metadata.
 // ---------------------------------------------------------------------------
 constexpr int kFusedMaxTiles = 16;  // tiles one block may own (tiles <= 16 * grid)
+// (the failure-detection test sets the barrier's arrival count at this offset)
+static_assert(offsetof(Control, bar_count) == 144, "grid barrier words of the control block");
 
 struct FusedArgs {
   ScanArgs a;                      // receive-side outputs (its layout inputs unused)

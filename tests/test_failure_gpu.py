@@ -1,4 +1,5 @@
-"""Failure detection without a GPU fault: the scan's bounded lookback wait.
+"""Failure detection without a GPU fault: the bounded waits of the scan's
+lookback and of the fused layout + offsets kernel's grid barrier.
 
 The workspace's tile counter is set to 1 from the host before a call, so
 the block that should take tile 0 is handed an out-of-range tile instead
@@ -48,5 +49,34 @@ def test_lookback_wait_times_out_and_context_survives():
     _, _, mask, _ = oracle.layout(inp.topk_idx, inp.E)
     out, st = oracle.dispatch(wl.bf16_bits(inp.x), inp.topk_idx, inp.topk_weights, mask, inp.E)
     assert st == 0
+    assert np.array_equal(plan.send_row.cpu().numpy(), out["send_row"])
+    assert np.array_equal(wl.bf16_bits(plan.recv_x[:out["num_recv"]]), out["recv_x"])
+
+
+def test_grid_barrier_wait_times_out_and_context_survives():
+    """The fused kernel's grid barrier: its arrival count is preset from the host to a
+    value no arrival can complete, so every block's bounded wait runs out and the call
+    reports MP_ERR_TIMEOUT; a normal call on a re-zeroed workspace is then exact."""
+    inp = wl.make_ep(dict(R=4, N=2048, E=16, K=4, H=64, routing="uniform", dtype="bf16"), seed=2)
+    plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H)
+    plan.load(inp)
+    torch.cuda.synchronize()
+    plan.workspace[144:148].copy_(torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8))  # 2^30
+    plan.dev_err.zero_()
+    t0 = time.time()
+    B.check(plan.layout_and_offsets())
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert plan.device_error() & B.MP_ERR_TIMEOUT, plan.device_error()
+    assert elapsed < 30.0
+    plan.workspace.zero_()
+    plan.dev_err.zero_()
+    plan.step()
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    ntpr, _, mask, _ = oracle.layout(inp.topk_idx, inp.E)
+    out, st = oracle.dispatch(wl.bf16_bits(inp.x), inp.topk_idx, inp.topk_weights, mask, inp.E)
+    assert st == 0
+    assert np.array_equal(plan.num_tokens_per_rank.cpu().numpy(), ntpr)
     assert np.array_equal(plan.send_row.cpu().numpy(), out["send_row"])
     assert np.array_equal(wl.bf16_bits(plan.recv_x[:out["num_recv"]]), out["recv_x"])
