@@ -615,6 +615,8 @@ def main():
         ph["rows"] += e[1].elapsed_time(e[2])
         ph["combine"] += e[2].elapsed_time(e[3])
     ph = {k: v / args.steps for k, v in ph.items()}
+    step_ms = sorted(e[0].elapsed_time(e[3]) for e in ev)  # each step, launch to launch
+    step_stats = {"median": step_ms[len(step_ms) // 2], "min": step_ms[0], "max": step_ms[-1]}
     ph["dispatch"] = ph["layout_offsets"] + ph["rows"]
     assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
 
@@ -724,7 +726,7 @@ def main():
             "config": config_block(args.config, inp),
             "effective_hbm_gbs": eff_gbs, "frac_of_8tbs": eff_gbs / world / NOMINAL_HBM_GBS,
             "frac_of_measured_copy_peak": eff_gbs / world / peak,
-            "receive_rows": T, "phases_ms": ph,
+            "receive_rows": T, "phases_ms": ph, "step_ms": step_stats,
             "roofline": roofline, "other_rows": other, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 3 * args.steps if N > 0 else 0, "clocks": clk,
         }
