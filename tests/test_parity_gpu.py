@@ -384,7 +384,8 @@ def test_bulk_copy_dispatch_matches_the_oracle(dtype, shape, cap_frac):
 
 FUSED = [(1, 100, 4, 2, 64), (3, 300, 12, 3, 264), (8, 1000, 64, 8, 520), (16, 130, 32, 3, 96),
          (32, 40, 64, 8, 16), (7, 777, 28, 28, 24), (2, 9000, 8, 3, 16),
-         (8, 20000, 32, 4, 16)]  # the last: more tiles than blocks, so blocks own several
+         (32, 300, 8192, 8, 16),  # the largest expert count: 32 KB of histogram per block
+         (8, 20000, 32, 4, 16)]  # more tiles than blocks, so blocks own several
 
 
 @pytest.mark.parametrize("shape", FUSED, ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
