@@ -456,14 +456,16 @@ struct FusedArgs {
   int32_t* num_tokens_per_expert;  // [R][E] out
 };
 
-// Grid barrier for a cooperative launch: thread 0 of each block reads the
-// generation, arrives, and waits (bounded) for the last arrival to advance
-// it.  Returns false when the wait gave up.
-__device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, int* ok_s) {
+// Grid barrier for a cooperative launch: thread 0 of each block arrives and
+// waits (bounded) for the last arrival to advance the generation.  Returns
+// false when the wait gave up.
+// `gen` is the generation read when the kernel started: a launch meets the
+// barrier once, and no other launch on the same workspace runs meanwhile.
+__device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, uint32_t gen,
+                                             int* ok_s) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const uint32_t gen = ld_acquire_u32(&ctl->bar_gen);
     __threadfence();
     if (atomicAdd(&ctl->bar_count, 1u) == nblocks - 1) {
       atomicExch(&ctl->bar_count, 0u);
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   __shared__ int64_t dest_base[MP_MAX_RANKS];
   __shared__ uint8_t tok_of[MP_MAX_RANKS][kScanTokens];
   __shared__ uint32_t tile_excl[kFusedMaxTiles][MP_MAX_RANKS];
-  __shared__ uint32_t sh_epoch;
+  __shared__ uint32_t sh_epoch, sh_gen;
   __shared__ int sh_bad, sh_ok;
 
   const int R = a.R, N = a.N, K = a.K, E = a.E, El = E / R;
@@ -512,6 +514,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   const int T = R * C;
   if (tid == 0) {
     sh_epoch = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
+    sh_gen = ld_relaxed_u32(&ctl->bar_gen);
     sh_bad = 0;
   }
   __syncthreads();
@@ -570,7 +573,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   __threadfence();
 
   // 2. every tile is published and every expert count added
-  if (!grid_barrier(ctl, gridDim.x, &sh_ok)) {
+  if (!grid_barrier(ctl, gridDim.x, sh_gen, &sh_ok)) {
     if (tid == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
     return;
   }
@@ -611,12 +614,19 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   for (int64_t e = int64_t(gridDim.x - 1 - blockIdx.x) * kScanThreads + tid; e < E;
        e += int64_t(gridDim.x) * kScanThreads) {
     int sum = 0;
-    for (int s = 0; s < R; ++s) {
-      int32_t* p = acc + int64_t(s) * (E + R) + e;
-      const int v = __ldcg(p);
-      *p = 0;
-      f.num_tokens_per_expert[int64_t(s) * E + e] = v;
-      sum += v;
+    for (int s0 = 0; s0 < R; s0 += 8) {  // 8 loads in flight before their stores
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = s0 + j < R ? __ldcg(acc + int64_t(s0 + j) * (E + R) + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < R) {
+          acc[int64_t(s0 + j) * (E + R) + e] = 0;
+          f.num_tokens_per_expert[int64_t(s0 + j) * E + e] = v[j];
+          sum += v[j];
+        }
+      }
     }
     a.num_recv_tokens_per_expert[e] = sum;
   }
