@@ -1,0 +1,159 @@
+/*
+ * c_abi_smoke.c -- the C ABI used from plain C (no Python, no torch): one
+ * layout -> dispatch -> combine pass on a small problem, with device memory
+ * from the CUDA runtime, checked on the host against properties that hold by
+ * definition:
+ *   - sum of num_tokens_per_rank == dest_offsets[R] (every receive row is
+ *     some token's row at some destination);
+ *   - a token's send_row has one entry >= 0 per distinct rank owning one of
+ *     its experts (expert e lives on rank e / (E/R));
+ *   - combining the un-modified dispatch gives c * x, c = that rank count
+ *     (exact here: x holds small integers, so every fp32 sum is exact).
+ * Prints "c abi smoke ok" and returns 0 on success.
+ */
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime_api.h>
+
+#include "mp_layout.h"
+
+#define R 4
+#define N 300
+#define K 3
+#define E 16
+#define H 64
+
+static int fail(const char *what) {
+  fprintf(stderr, "c abi smoke FAILED: %s\n", what);
+  return 1;
+}
+
+#define CUDA(call)                                  \
+  do {                                              \
+    if ((call) != cudaSuccess) return fail(#call);  \
+  } while (0)
+
+#define MP(call)                                                  \
+  do {                                                            \
+    int st_ = (call);                                             \
+    if (st_ != MP_OK) {                                           \
+      fprintf(stderr, "%s: %s\n", #call, mp_status_string(st_));  \
+      return 1;                                                   \
+    }                                                             \
+  } while (0)
+
+static uint16_t bf16_of_small_int(int v) { /* exact: |v| < 256 */
+  float f = (float)v;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+static float f32_of_bf16(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+int main(void) {
+  const int El = E / R;
+  const int64_t cap = (int64_t)R * N * (R < K ? R : K);
+  static int32_t topk[R * N * K];
+  static float w[R * N * K];
+  static uint16_t x[R * N * H];
+  static int32_t send_row[R * N * R];
+  static uint16_t out[R * N * H];
+  int32_t ntpr[R * R], dest_offsets[R + 1], err = 0;
+
+  /* K distinct experts per token from a fixed LCG; every 11th token masked */
+  uint32_t lcg = 12345u;
+  for (int tok = 0; tok < R * N; ++tok) {
+    for (int k = 0; k < K; ++k) {
+      int e, dup;
+      do {
+        lcg = lcg * 1664525u + 1013904223u;
+        e = (int)((lcg >> 8) % E);
+        dup = 0;
+        for (int j = 0; j < k; ++j) dup |= topk[tok * K + j] == e;
+      } while (dup);
+      topk[tok * K + k] = e;
+      w[tok * K + k] = 1.0f / K;
+    }
+    if (tok % 11 == 0)
+      for (int k = 0; k < K; ++k) topk[tok * K + k] = -1;
+    for (int h = 0; h < H; ++h) x[tok * H + h] = bf16_of_small_int((tok + h) % 7 - 3);
+  }
+
+  void *d_topk, *d_w, *d_x, *d_ntpr, *d_ntpe, *d_mask, *d_err, *d_ws, *d_recv_x, *d_rsr, *d_rsi,
+      *d_rti, *d_rtw, *d_doff, *d_rp, *d_nrtpe, *d_send, *d_out;
+  const size_t ws = mp_workspace_size(R, N, E);
+  if (ws == 0) return fail("mp_workspace_size");
+  CUDA(cudaMalloc(&d_topk, sizeof topk));
+  CUDA(cudaMalloc(&d_w, sizeof w));
+  CUDA(cudaMalloc(&d_x, sizeof x));
+  CUDA(cudaMalloc(&d_ntpr, sizeof(int32_t) * R * R));
+  CUDA(cudaMalloc(&d_ntpe, sizeof(int32_t) * R * E));
+  CUDA(cudaMalloc(&d_mask, sizeof(uint32_t) * R * N));
+  CUDA(cudaMalloc(&d_err, sizeof(int32_t)));
+  CUDA(cudaMalloc(&d_ws, ws));
+  CUDA(cudaMalloc(&d_recv_x, sizeof(uint16_t) * (size_t)cap * H));
+  CUDA(cudaMalloc(&d_rsr, sizeof(int32_t) * (size_t)cap));
+  CUDA(cudaMalloc(&d_rsi, sizeof(int32_t) * (size_t)cap));
+  CUDA(cudaMalloc(&d_rti, sizeof(int32_t) * (size_t)cap * K));
+  CUDA(cudaMalloc(&d_rtw, sizeof(float) * (size_t)cap * K));
+  CUDA(cudaMalloc(&d_doff, sizeof(int32_t) * (R + 1)));
+  CUDA(cudaMalloc(&d_rp, sizeof(int32_t) * R * R));
+  CUDA(cudaMalloc(&d_nrtpe, sizeof(int32_t) * E));
+  CUDA(cudaMalloc(&d_send, sizeof send_row));
+  CUDA(cudaMalloc(&d_out, sizeof out));
+  CUDA(cudaMemset(d_ws, 0, ws));
+  CUDA(cudaMemset(d_err, 0, sizeof(int32_t)));
+  CUDA(cudaMemcpy(d_topk, topk, sizeof topk, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(d_w, w, sizeof w, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(d_x, x, sizeof x, cudaMemcpyHostToDevice));
+
+  MP(mp_layout(R, N, K, E, d_topk, d_ntpr, d_ntpe, d_mask, d_err, d_ws, NULL));
+  MP(mp_dispatch(R, N, K, E, H, MP_BF16, d_x, NULL, d_topk, d_w, d_mask, d_ntpr, d_ntpe, cap,
+                 d_recv_x, NULL, d_rsr, d_rsi, d_rti, d_rtw, d_doff, d_rp, d_nrtpe, d_send,
+                 d_err, d_ws, NULL));
+  MP(mp_combine(R, N, H, d_recv_x, cap, d_send, d_out, d_err, NULL));
+  CUDA(cudaDeviceSynchronize());
+
+  CUDA(cudaMemcpy(&err, d_err, sizeof err, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(ntpr, d_ntpr, sizeof ntpr, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(dest_offsets, d_doff, sizeof dest_offsets, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(send_row, d_send, sizeof send_row, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(out, d_out, sizeof out, cudaMemcpyDeviceToHost));
+  if (err != 0) {
+    fprintf(stderr, "device error: %s\n", mp_status_string(err));
+    return 1;
+  }
+
+  int64_t total = 0;
+  for (int i = 0; i < R * R; ++i) total += ntpr[i];
+  if (total != dest_offsets[R]) return fail("sum of num_tokens_per_rank != dest_offsets[R]");
+  for (int tok = 0; tok < R * N; ++tok) {
+    int owners = 0, rows = 0;
+    for (int d = 0; d < R; ++d) {
+      int owns = 0;
+      for (int k = 0; k < K; ++k) {
+        const int e = topk[tok * K + k];
+        owns |= e >= d * El && e < (d + 1) * El;
+      }
+      owners += owns;
+      if (owns != (send_row[tok * R + d] >= 0)) return fail("send_row entry vs owning rank");
+      rows += send_row[tok * R + d] >= 0;
+    }
+    if (rows != owners) return fail("destination count");
+    for (int h = 0; h < H; ++h) {
+      const float want = (float)owners * f32_of_bf16(x[tok * H + h]);
+      if (f32_of_bf16(out[tok * H + h]) != want) return fail("combine != c * x");
+    }
+  }
+  printf("c abi smoke ok: %d receive rows\n", dest_offsets[R]);
+  return 0;
+}
