@@ -695,7 +695,7 @@ def main():
     peak, peak_kind = peaks()
     dom = "rows" if ph["rows"] >= ph["combine"] else "combine"
     achieved = nb[dom] / (ph[dom] / 1e3) / 1e9
-    kname = {"rows": "mp_k_dispatch<8,4>", "combine": "mp_k_combine<8,1,4,0>"}[dom]
+    kname = {"rows": "mp_k_dispatch<8,4>", "combine": "mp_k_combine<8,1,3,0>"}[dom]
     traffic = recorded_traffic(kname) if (args.config == "dsv3" and args.tokens == 0) else None
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
