@@ -419,6 +419,29 @@ def test_fused_layout_and_offsets_capacity_and_bad_ids():
     compare_ep(inp, plan, recv_capacity=700, expect_err=B.MP_ERR_CAPACITY | B.MP_ERR_BAD_EXPERT)
 
 
+def test_step_replays_as_a_cuda_graph():
+    """The three-launch step (cooperative layout + offsets, rows, combine) captured in a
+    CUDA graph and replayed: the oracle's results, replay after replay."""
+    inp = wl.make_ep(dict(R=4, N=700, E=16, K=4, H=128, routing="uniform", dtype="bf16"), seed=8)
+    plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H)
+    plan.load(inp)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan.step()  # first calls (one-time launch setup) outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        plan.step()
+    for _ in range(3):
+        plan.out.zero_()
+        plan.recv_x.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    compare_ep(inp, plan)
+
+
 def test_fused_layout_and_offsets_falls_back_beyond_one_grid():
     """R=32 x 40,000 tokens is 10,016 tiles, more than 16 per block of a resident grid:
     the call runs the two kernels instead, with the same results."""
