@@ -324,6 +324,16 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_mx, R * N * H * 2 + T * (H + H // 32) + R * N * R * 4),
         workload="dsv3 rows quantised in-kernel: bf16 in, MXFP8 (e4m3 + UE8M0 byte per 32 "
                  "channels) out")
+    # the same row copy through the bulk-copy (TMA) engine
+    rxb = torch.empty((plan.cap, H), dtype=torch.bfloat16, device="cuda")
+    ms_bulk = timed(lambda: B.check(B.mp_dispatch_rows_bulk(R, N, H, B.MP_BF16, plan.x, None,
+                                                            plan.send_row, plan.cap, rxb, None,
+                                                            plan.dev_err)), steps)
+    assert plan.device_error() == 0
+    out["dispatch_rows_bulk_copy"] = dict(
+        row(ms_bulk, algorithmic_bytes(R, N, K, E, H, T)["rows"]),
+        workload="dsv3 rows, bf16, copied by cp.async.bulk through shared memory")
+    del rxb
     rq4 = torch.empty((plan.cap, H // 2), dtype=torch.uint8, device="cuda")
     ms_m4 = timed(lambda: B.check(B.mp_dispatch_rows_mxfp4(R, N, H, plan.x, plan.send_row,
                                                            plan.cap, rq4, rc)), steps)

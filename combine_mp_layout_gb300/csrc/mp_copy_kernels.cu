@@ -63,18 +63,31 @@
 #ifndef MP_SMALL_DISPATCH
 #define MP_SMALL_DISPATCH 1
 #endif
+
+// Shapes of the other copies.
 // 1: the e4m3 quantiser divides by the block scale with a reciprocal and two
 // FMA corrections instead of a division per element (see mp_k_quant_rows);
 // 0: one correctly rounded division per element.
 #ifndef MP_QUANT_FAST_DIV
 #define MP_QUANT_FAST_DIV 1
 #endif
-
+// Bulk-copy (TMA) dispatch: shared-memory stages per block, tokens per chunk,
+// bytes per bulk copy, and one short block per chunk (1) or a persistent grid
+// (0).  Measured on the dsv3 rows: a persistent grid stays near 500 us for
+// every stage / chunk / piece shape tried (3-8 stages, 2-16 tokens, 4-16 KB);
+// one block per chunk gives 444 us, and 3 stages of 8 KB with 2-token chunks
+// 442 us.
 #ifndef MP_TMA_STAGES
-#define MP_TMA_STAGES 6
+#define MP_TMA_STAGES 3
 #endif
 #ifndef MP_TMA_CHUNK
-#define MP_TMA_CHUNK 8
+#define MP_TMA_CHUNK 2
+#endif
+#ifndef MP_TMA_PIECE
+#define MP_TMA_PIECE 8192
+#endif
+#ifndef MP_TMA_GRID_FULL
+#define MP_TMA_GRID_FULL 1
 #endif
 
 namespace mp {
@@ -131,13 +144,14 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ 
 // a global->shared bulk load per row piece (completing on the stage's
 // mbarrier), then one contiguous shared->global bulk store per destination.
 // A stage is refilled once the stores issued LAG items earlier have finished
-// reading it.  Blocks take chunks of kTmaChunk tokens round-robin; the
-// chunk's send_row entries are staged in shared memory by the whole warp.
+// reading it.  Blocks take chunks of kTmaChunk tokens round-robin (one chunk
+// per block on the default short-block grid); the chunk's send_row entries are
+// staged in shared memory by the whole warp.
 // ---------------------------------------------------------------------------
 constexpr int kTmaStages = MP_TMA_STAGES;
 constexpr int kTmaLag = 2;
 constexpr int kTmaChunk = MP_TMA_CHUNK;
-constexpr uint32_t kTmaPiece = 16384;  // bytes per bulk copy (rows are cut into pieces)
+constexpr uint32_t kTmaPiece = MP_TMA_PIECE;  // bytes per bulk copy (rows are cut into pieces)
 static_assert(kTmaLag < kTmaStages, "lag below the stage count");
 
 __host__ __device__ inline size_t tma_smem_bytes(uint32_t piece_bytes) {
@@ -702,7 +716,7 @@ static cudaError_t dispatch_copy_tma(int R, int64_t tokens, int64_t row_bytes, c
       per_sm < 1)
     per_sm = 1;
   const int64_t chunks = (tokens + kTmaChunk - 1) / kTmaChunk;
-  const unsigned grid = grid_for(per_sm, 1, chunks);
+  const unsigned grid = MP_TMA_GRID_FULL ? grid_full(1, chunks) : grid_for(per_sm, 1, chunks);
   return launch_kernel(mp_k_dispatch_tma, dim3(grid), dim3(kWarp), smem, stream, R, tokens,
                        row_bytes, piece, pieces, static_cast<const unsigned char*>(x),
                        static_cast<unsigned char*>(recv_x), recv_capacity, send_row, spr, x_scales,
