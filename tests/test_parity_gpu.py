@@ -744,9 +744,12 @@ def _offset_16(t: torch.Tensor) -> torch.Tensor:
     return out
 
 
+@pytest.mark.parametrize("which", ["source", "output"])
 @pytest.mark.parametrize("fmt", sorted(QFMT))
-def test_quantising_copies_from_a_16_byte_aligned_source(fmt):
-    """Sources that are 16- but not 32-byte aligned take the 8-channels-per-lane form."""
+def test_quantising_copies_with_16_byte_aligned_buffers(fmt, which):
+    """A source that is 16- but not 32-byte aligned takes the 8-channels-per-lane form;
+    an FP8 output of that alignment the 16-channel one (32 channels per lane store 32
+    code bytes at once)."""
     f = QFMT[fmt]
     R, N, E, K, H = 4, 300, 16, 4, 384
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=77)
@@ -755,15 +758,20 @@ def test_quantising_copies_from_a_16_byte_aligned_source(fmt):
     plan.load(inp)
     B.check(plan.layout())
     B.check(plan.dispatch_offsets())
-    xo = _offset_16(plan.x)
+    xo = _offset_16(plan.x) if which == "source" else plan.x
     nsc = H // f["block"]
     rq = torch.zeros((plan.cap, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    if which == "output":
+        rq = _offset_16(rq)
     rs = torch.zeros((plan.cap, nsc), dtype=f["sdt"], device="cuda")
     B.check(getattr(B, f["disp"])(R, N, H, xo, plan.send_row, plan.cap, rq, rs))
     sizes = [5, 0, 17]
     S = sum(sizes)
-    sh = _offset_16(plan.x.reshape(R * N, H)[:S])
+    sh = plan.x.reshape(R * N, H)[:S]
+    sh = _offset_16(sh) if which == "source" else sh.contiguous()
     gq = torch.zeros((3, S, f["qcols"](H)), dtype=torch.uint8, device="cuda")
+    if which == "output":
+        gq = _offset_16(gq)
     gs = torch.zeros((3, S, nsc), dtype=f["sdt"], device="cuda")
     B.check(getattr(B, f["gather"])(3, H, sizes, sh, gq, gs))
     torch.cuda.synchronize()
