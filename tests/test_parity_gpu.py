@@ -634,6 +634,34 @@ def test_low_latency_rank_major_matches_oracle(cfg, counts):
     assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll rank-major")
 
 
+def test_low_latency_rows_e4m3_with_scales():
+    """The LL row copy of an e4m3 payload moves each row's scales with it."""
+    R, N, E, K, H = 4, 200, 32, 4, 256
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="e4m3"), seed=31)
+    plan = EPPlan(R, N, K, E, H, "e4m3")
+    plan.load(inp)
+    cap = R * N * K
+    dev = "cuda"
+    eoff = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    esoff = torch.zeros((E, R), dtype=torch.int32, device=dev)
+    src = torch.zeros(cap, dtype=torch.int32, device=dev)
+    slot = torch.zeros((R, N, K), dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.uint8, device=dev)
+    rs = torch.zeros((cap, H // 128), dtype=torch.float32, device=dev)
+    B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff, esoff, src, slot,
+                                     plan.dev_err))
+    B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_E4M3, plan.x, plan.x_scales, slot, cap, rx, rs))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    payload = np.concatenate([wl.u8_bits(inp.x), inp.x_scales.numpy().view(np.uint8)], axis=-1)
+    ll, st = oracle.dispatch_ll(payload, inp.topk_idx, E)
+    assert st == 0
+    n = ll["num_recv"]
+    assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+    assert np.array_equal(rx[:n].cpu().numpy(), ll["recv_x"][:, :H])
+    assert np.array_equal(rs[:n].cpu().numpy().view(np.uint8), ll["recv_x"][:, H:])
+
+
 def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
     R, N, E, K = 4, 50, 16, 3
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=64, routing="uniform", dtype="bf16"), seed=9)
