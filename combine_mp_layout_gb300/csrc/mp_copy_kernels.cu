@@ -1,8 +1,10 @@
-// mp_copy_kernels.cu -- the HBM-bound payload kernels: dispatch row copy,
-// combine (gather + fp32 sum), reduce-scatterv (fp32 sum of R inputs) and
-// all-gatherv (one read, R writes).
+// mp_copy_kernels.cu -- the HBM-bound payload kernels: dispatch row copy
+// (SM vectors, or the bulk-copy engine), quantising row copies (dispatch or
+// gather destinations), combine (gather + fp32 sum, plain or top-k
+// weighted), combined top-k weights, reduce-scatterv (fp32 sum of R inputs)
+// and all-gatherv (one read, R writes; one tensor or a list).
 //
-// All four are streaming kernels: nothing is reused, so they are bound by
+// All are streaming kernels: nothing is reused, so they are bound by
 // HBM bandwidth and the design goal is bytes in flight with few
 // instructions.  The work is split into small units handed out to warps:
 //   dispatch / combine : (token, slab) with a slab of 32 lanes x U vectors of

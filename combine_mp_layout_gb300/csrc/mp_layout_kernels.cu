@@ -19,6 +19,12 @@
 // metadata.  Tiles are handed out in launch order through an atomic
 // counter, so every tile a block waits on belongs to a block that is
 // already running.
+//
+// Layout + scan fused (mp_k_layout_scan): the same tiles, in one cooperative
+// launch with one grid barrier between the lookback and the rows.
+//
+// Low-latency offsets (mp_k_ll_offsets): one row per (token, top-k slot),
+// grouped by expert or by the rank owning it, by a per-rank counting sort.
 #include <cstddef>
 #include <cstdint>
 
