@@ -384,6 +384,8 @@ def test_bulk_copy_dispatch_matches_the_oracle(dtype, shape, cap_frac):
 
 FUSED = [(1, 100, 4, 2, 64), (3, 300, 12, 3, 264), (8, 1000, 64, 8, 520), (16, 130, 32, 3, 96),
          (32, 40, 64, 8, 16), (7, 777, 28, 28, 24), (2, 9000, 8, 3, 16),
+         (4, 257, 4, 2, 64),     # one expert per rank
+         (3, 1, 6, 2, 64),       # a single token per rank
          (32, 300, 8192, 8, 16),  # the largest expert count: 32 KB of histogram per block
          (8, 20000, 32, 4, 16)]  # more tiles than blocks, so blocks own several
 
