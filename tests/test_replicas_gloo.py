@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 def test_max_over_ranks_and_whole_job_throughput():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of a threaded process
         out = mgr.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
