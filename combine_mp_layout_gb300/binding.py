@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.mp_dispatch_rows_mxfp4.argtypes = [i32, i32, i32, P, P, i64, P, P, P]
         L.mp_dispatch_rows_bulk.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P]
         L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
+        L.mp_dispatch_noalloc.argtypes = [i32] * 6 + [P] * 7 + [i64] + [P] * 12
+        L.mp_allgatherv_multi.argtypes = [i32, i32, P, P, P, P, P]
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
@@ -85,7 +87,7 @@ def lib() -> ctypes.CDLL:
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
                   "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk",
-                  "mp_layout_and_offsets"):
+                  "mp_layout_and_offsets", "mp_dispatch_noalloc", "mp_allgatherv_multi"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -291,13 +293,7 @@ def mp_dispatch_noalloc(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weight
                         num_recv_tokens_per_expert, send_row, dev_err, stream=None) -> int:
     """mp_dispatch without a workspace, for callers that cannot allocate device memory
     (the scan's scratch is a fixed array inside the library; see the C header)."""
-    L = lib()
-    f = L.mp_dispatch_noalloc
-    if f.argtypes is None:
-        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-        f.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i64,
-                      P, P, P, P, P, P, P, P, P, P, P, P]
-        f.restype = ctypes.c_int
+    f = lib().mp_dispatch_noalloc
     return f(R, N, K, E, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
              _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"),
              _dev(is_token_in_rank, "is_token_in_rank"),
@@ -313,12 +309,7 @@ def mp_dispatch_noalloc(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weight
 
 def mp_allgatherv_multi(R, row_bytes, sizes, inputs, outputs, stream=None) -> int:
     """All-gatherv of several tensors with the same per-rank row counts, one launch."""
-    L = lib()
-    f = L.mp_allgatherv_multi
-    if f.argtypes is None:
-        P = ctypes.c_void_p
-        f.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
-        f.restype = ctypes.c_int
+    f = lib().mp_allgatherv_multi
     n = len(inputs)
     if len(outputs) != n or len(row_bytes) != n:
         raise ValueError("one row size and one output per input")
