@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
         L.mp_dispatch_noalloc.argtypes = [i32] * 6 + [P] * 7 + [i64] + [P] * 12
         L.mp_allgatherv_multi.argtypes = [i32, i32, P, P, P, P, P]
+        L.mp_dispatch_ll.argtypes = [i32] * 7 + [P] * 4 + [i64] + [P] * 9
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
@@ -87,7 +88,8 @@ def lib() -> ctypes.CDLL:
                   "mp_combine", "mp_reducescatterv", "mp_allgatherv",
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
                   "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk",
-                  "mp_layout_and_offsets", "mp_dispatch_noalloc", "mp_allgatherv_multi"):
+                  "mp_layout_and_offsets", "mp_dispatch_noalloc", "mp_allgatherv_multi",
+                  "mp_dispatch_ll"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -345,6 +347,19 @@ def mp_dispatch_ll_rows(R, N, K, H, dtype, x, x_scales, slot_row, recv_capacity,
                                      _dev(slot_row, "slot_row"), int(recv_capacity),
                                      _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
                                      _stream(stream))
+
+
+def mp_dispatch_ll(R, N, K, E, H, dtype, rank_major, x, x_scales, topk_idx,
+                   num_tokens_per_expert, recv_capacity, bin_offsets, bin_src_offsets,
+                   recv_src_token, slot_row, recv_x, recv_scales, dev_err, workspace,
+                   stream=None) -> int:
+    return lib().mp_dispatch_ll(
+        R, N, K, E, H, dtype, int(rank_major), _dev(x, "x"), _dev(x_scales, "x_scales"),
+        _dev(topk_idx, "topk_idx"), _dev(num_tokens_per_expert, "num_tokens_per_expert"),
+        int(recv_capacity), _dev(bin_offsets, "bin_offsets"),
+        _dev(bin_src_offsets, "bin_src_offsets"), _dev(recv_src_token, "recv_src_token"),
+        _dev(slot_row, "slot_row"), _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
+        _dev(dev_err, "dev_err"), _dev(workspace, "workspace"), _stream(stream))
 
 
 def mp_combine_ll(R, N, K, H, y, y_rows, slot_row, topk_weights, out, dev_err, stream=None) -> int:

@@ -664,6 +664,89 @@ def test_low_latency_rows_e4m3_with_scales():
     assert np.array_equal(rs[:n].cpu().numpy().view(np.uint8), ll["recv_x"][:, H:])
 
 
+LL_ONE_LAUNCH = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
+                 dict(R=5, N=77, E=20, K=6, H=264), dict(R=3, N=300, E=9, K=9, H=64),
+                 dict(R=4, N=40, E=16, K=4, H=20480), dict(R=32, N=40, E=64, K=4, H=64),
+                 dict(R=8, N=64, E=8192, K=8, H=64), dict(R=4, N=3000, E=64, K=6, H=64),
+                 dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5), dict(R=1, N=40, E=3, K=3, H=64),
+                 dict(R=4, N=0, E=16, K=4, H=64)]
+
+
+@pytest.mark.parametrize("cfg", LL_ONE_LAUNCH, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
+                         + ("_cap" if "cap_frac" in c else ""))
+@pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
+@pytest.mark.parametrize("counts", ["layout", "self"])
+def test_low_latency_one_launch_dispatch_matches_oracle(cfg, rank_major, counts):
+    """mp_dispatch_ll (sort and row copy in one launch; the two launches when E is too
+    large for one block's counters) against the oracle's LL layout and rows, three calls
+    on one workspace (each launch must start from the ticket and epoch the last left).
+    H=264 takes 16-byte vectors, H=20480 rows longer than the part loaded before the wait."""
+    cfg = dict(cfg)
+    cap_frac = cfg.pop("cap_frac", None)
+    R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
+    inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=N + 7)
+    inp.topk_idx[:, ::6, K - 1] = -1
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    if counts == "layout":
+        B.check(plan.layout())
+    cap = R * N * K if cap_frac is None else int(R * N * K * cap_frac)
+    nb = R if rank_major else E
+    dev = "cuda"
+    want, st = (oracle.dispatch_ll_rank_major if rank_major else oracle.dispatch_ll)(
+        wl.bf16_bits(inp.x), inp.topk_idx, E, recv_capacity=cap)
+    n = min(want["num_recv"], cap)
+    keys = ("dest_offsets", "dest_src_offsets") if rank_major else ("expert_offsets",
+                                                                    "expert_src_offsets")
+    for rep in range(3):
+        boff = torch.full((nb + 1,), -3, dtype=torch.int32, device=dev)
+        bsoff = torch.full((nb, R), -3, dtype=torch.int32, device=dev)
+        src = torch.full((max(cap, 1),), -3, dtype=torch.int32, device=dev)
+        slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
+        rx = torch.zeros((max(cap, 1), H), dtype=torch.bfloat16, device=dev)
+        plan.dev_err.zero_()
+        ntpe = plan.num_tokens_per_expert if counts == "layout" else None
+        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, rank_major, plan.x, None, plan.topk_idx,
+                                 ntpe, cap, boff, bsoff, src, slot, rx, None, plan.dev_err,
+                                 plan.workspace))
+        torch.cuda.synchronize()
+        assert plan.device_error() == st, rep
+        assert np.array_equal(boff.cpu().numpy(), want[keys[0]]), rep
+        assert np.array_equal(bsoff.cpu().numpy(), want[keys[1]]), rep
+        assert np.array_equal(slot.cpu().numpy(), want["slot_row"]), rep
+        assert np.array_equal(src[:n].cpu().numpy(), want["recv_src_token"]), rep
+        assert np.array_equal(wl.bf16_bits(rx[:n]), want["recv_x"]), rep
+    assert (st == 0) == (cap_frac is None)
+
+
+def test_low_latency_one_launch_dispatch_e4m3_with_scales():
+    R, N, E, K, H = 4, 200, 32, 4, 384
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="e4m3"), seed=32)
+    plan = EPPlan(R, N, K, E, H, "e4m3")
+    plan.load(inp)
+    cap = R * N * K
+    dev = "cuda"
+    eoff = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    esoff = torch.zeros((E, R), dtype=torch.int32, device=dev)
+    src = torch.zeros(cap, dtype=torch.int32, device=dev)
+    slot = torch.zeros((R, N, K), dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.uint8, device=dev)
+    rs = torch.zeros((cap, H // 128), dtype=torch.float32, device=dev)
+    B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_E4M3, 0, plan.x, plan.x_scales, plan.topk_idx,
+                             None, cap, eoff, esoff, src, slot, rx, rs, plan.dev_err,
+                             plan.workspace))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    payload = np.concatenate([wl.u8_bits(inp.x), inp.x_scales.numpy().view(np.uint8)], axis=-1)
+    ll, st = oracle.dispatch_ll(payload, inp.topk_idx, E)
+    assert st == 0
+    n = ll["num_recv"]
+    assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+    assert np.array_equal(src[:n].cpu().numpy(), ll["recv_src_token"])
+    assert np.array_equal(rx[:n].cpu().numpy(), ll["recv_x"][:, :H])
+    assert np.array_equal(rs[:n].cpu().numpy().view(np.uint8), ll["recv_x"][:, H:])
+
+
 def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
     R, N, E, K = 4, 50, 16, 3
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=64, routing="uniform", dtype="bf16"), seed=9)
