@@ -511,7 +511,29 @@ def measure_other_rows(steps: int, peak: float):
         row(ms_rm, rm_bytes), us_per_step=ms_rm * 1e3,
         workload="as low_latency_step_n128 with rank-major output (rows grouped by the rank "
                  "owning the expert)")
-    del plan, rx, yl, lo, graph
+
+    def ll_one_step():  # sort and row copy in one launch, then the weighted combine
+        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None, plan.topk_idx,
+                                 None, cap, eoff, esoff, src, slot, rx, None, plan.dev_err,
+                                 plan.workspace))
+        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
+
+    ms_one = timed(ll_one_step, steps)
+    s_cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_cap):
+        ll_one_step()
+    torch.cuda.current_stream().wait_stream(s_cap)
+    graph1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph1):
+        ll_one_step()
+    ms_oneg = timed(graph1.replay, steps)
+    assert plan.device_error() == 0
+    out["low_latency_one_launch_step_n128"] = dict(
+        row(ms_one, ll_bytes), us_per_step=ms_one * 1e3, us_per_step_cuda_graph=ms_oneg * 1e3,
+        GBs_cuda_graph=ll_bytes / (ms_oneg / 1e3) / 1e9,
+        workload="as low_latency_step_n128 with mp_dispatch_ll (LL offsets and rows in one "
+                 "launch) + weighted LL combine (2 launches)")
+    del plan, rx, yl, lo, graph, graph1
     torch.cuda.empty_cache()
 
     # the skewed workload: Zipf(1.2) routing, rank 0 hot

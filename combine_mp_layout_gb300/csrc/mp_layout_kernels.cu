@@ -707,7 +707,12 @@ constexpr int kLLHistInts = 16384;
 #ifndef MP_LL_BATCH
 #define MP_LL_BATCH 8
 #endif
-constexpr int kLLBatch = MP_LL_BATCH;  // id loads in flight per thread (counts and the walk)
+constexpr int kLLBatch = MP_LL_BATCH;  // id loads in flight per lane in the in-order walk
+#ifndef MP_LL_IDS
+#define MP_LL_IDS 16
+#endif
+constexpr int kLLIds = MP_LL_IDS;  // ids per thread and batch while counting (a multiple of 4)
+static_assert(kLLIds % 4 == 0, "counting batches are whole 16-byte loads");
 
 // segments of a rank's entries (one warp each) for NT threads and a budget of
 // hist_ints shared-memory counters
@@ -746,28 +751,71 @@ __device__ __forceinline__ void ll_offsets_block(
   int32_t* slots = slot_row + int64_t(s) * nk;
   const int64_t seg_len = (nk + nseg - 1) / nseg;
   const int64_t g0 = min(nk, int64_t(warp) * seg_len), g1 = min(nk, g0 + seg_len);
-  for (int i = tid; i < (nseg + 3) * nbins; i += NT) ll_smem[i] = 0;
-  __syncthreads();
-  // 1. counts per (segment, bin) of this rank; the per-bin totals and
-  //    lower-rank prefixes from the layout's num_tokens_per_expert, or, when
-  //    that is NULL, counted here from every rank's ids (ids outside [-1, E)
-  //    are flagged as the layout would)
-  // (the loads of a batch are issued before its atomics: kLLBatch reads in
-  // flight per thread instead of one round trip to memory per entry)
-  if (warp < nseg)
-    for (int64_t i0 = g0; i0 < g1; i0 += int64_t(kLLBatch) * kWarp) {
-      int v[kLLBatch];
+  // 1. one pass over the ids: per (segment, bin) counts of this rank's
+  //    entries and, when num_tokens_per_expert is NULL, every rank's per-bin
+  //    totals and the lower-rank prefixes (ids outside [-1, E) then flagged as
+  //    the layout would); else the totals and prefixes from the layout's
+  //    counts.  Each thread loads kLLIds ids per batch (16-byte loads where
+  //    aligned) before its shared-memory adds, and the first batch's loads are
+  //    issued before the counters are cleared.
+  const bool self_count = num_tokens_per_expert == nullptr;
+  const int64_t mine = int64_t(s) * nk;
+  const int64_t lo = self_count ? 0 : mine, hi = self_count ? int64_t(R) * nk : mine + nk;
+  const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15u) == 0 && lo % 4 == 0 &&
+                   hi % 4 == 0;
+  const int64_t per_batch = int64_t(kLLIds) * NT;
+  int ids[kLLIds];
+  auto id_index = [&](int64_t b0, int j) -> int64_t {
+    return vec ? b0 + (int64_t(j / 4) * NT + tid) * 4 + (j & 3) : b0 + int64_t(j) * NT + tid;
+  };
+  auto load_batch = [&](int64_t b0) {
+    if (vec) {
 #pragma unroll
-      for (int j = 0; j < kLLBatch; ++j) {
-        const int64_t i = i0 + int64_t(j) * kWarp + lane;
-        v[j] = i < g1 ? __ldg(src + i) : -1;
+      for (int j = 0; j < kLLIds / 4; ++j) {
+        const int64_t i = b0 + (int64_t(j) * NT + tid) * 4;
+        const int4 q = i < hi ? __ldg(reinterpret_cast<const int4*>(topk_idx + i))
+                              : make_int4(-1, -1, -1, -1);
+        ids[4 * j] = q.x;
+        ids[4 * j + 1] = q.y;
+        ids[4 * j + 2] = q.z;
+        ids[4 * j + 3] = q.w;
       }
+    } else {
 #pragma unroll
-      for (int j = 0; j < kLLBatch; ++j) {
-        if (v[j] >= 0 && v[j] < E) atomicAdd(&hist[warp * nbins + bin_of(v[j])], 1);
+      for (int j = 0; j < kLLIds; ++j) {
+        const int64_t i = b0 + int64_t(j) * NT + tid;
+        ids[j] = i < hi ? __ldg(topk_idx + i) : -1;
       }
     }
-  if (num_tokens_per_expert) {
+  };
+  bool bad = false;
+  auto count_batch = [&](int64_t b0) {
+#pragma unroll
+    for (int j = 0; j < kLLIds; ++j) {
+      const int e = ids[j];
+      if (e < 0 || e >= E) {
+        bad |= e != -1;
+        continue;
+      }
+      const int64_t i = id_index(b0, j);
+      const int b = bin_of(e);
+      if (i >= mine && i < mine + nk)
+        atomicAdd(&hist[int(i - mine) / int(seg_len) * nbins + b], 1);
+      if (self_count) {
+        atomicAdd(&tot[b], 1);
+        if (i < mine) atomicAdd(&pre[b], 1);
+      }
+    }
+  };
+  if (lo < hi) load_batch(lo);
+  for (int i = tid; i < (nseg + 3) * nbins; i += NT) ll_smem[i] = 0;
+  __syncthreads();
+  if (lo < hi) count_batch(lo);
+  for (int64_t b0 = lo + per_batch; b0 < hi; b0 += per_batch) {
+    load_batch(b0);
+    count_batch(b0);
+  }
+  if (!self_count) {
     for (int e = tid; e < E; e += NT) {
       int t = 0, p = 0;
       for (int q = 0; q < R; ++q) {
@@ -783,27 +831,8 @@ __device__ __forceinline__ void ll_offsets_block(
         pre[e] = p;
       }
     }
-  } else {
-    bool bad = false;
-    const int64_t all = int64_t(R) * nk, mine = int64_t(s) * nk;
-    for (int64_t i0 = 0; i0 < all; i0 += int64_t(kLLBatch) * NT) {
-      int v[kLLBatch];
-#pragma unroll
-      for (int j = 0; j < kLLBatch; ++j) {
-        const int64_t i = i0 + int64_t(j) * NT + tid;
-        v[j] = i < all ? __ldg(topk_idx + i) : -1;
-      }
-#pragma unroll
-      for (int j = 0; j < kLLBatch; ++j) {
-        const int e = v[j];
-        const int b = e >= 0 && e < E ? bin_of(e) : -1;
-        const int bp = i0 + int64_t(j) * NT + tid < mine ? b : -1;
-        bad |= b < 0 && e != -1;
-        if (b >= 0) atomicAdd(&tot[b], 1);
-        if (bp >= 0) atomicAdd(&pre[bp], 1);
-      }
-    }
-    if (bad && s == 0) raise_error(dev_err, MP_ERR_BAD_EXPERT);
+  } else if (bad && s == 0) {
+    raise_error(dev_err, MP_ERR_BAD_EXPERT);
   }
   __syncthreads();
   // 2a. this thread's bins [b0, b1) and their totals over every source rank
@@ -857,6 +886,7 @@ __device__ __forceinline__ void ll_offsets_block(
       }
 #pragma unroll
       for (int j = 0; j < kLLBatch; ++j) {
+        if (i00 + int64_t(j) * kWarp >= g1) break;  // (the same for the whole warp)
         const int64_t i = i00 + int64_t(j) * kWarp + lane;
         const int e = v[j];
         const bool ok = e >= 0 && e < E;
