@@ -723,6 +723,29 @@ def main():
                "pipelining": "two buffer sets; H2D, kernels and D2H on separate streams"}
         del plans[1]
 
+    # The same step captured once as a CUDA graph and replayed: the device-side time of
+    # the three launches without the host's launch cost (beside `value`, not instead).
+    s_cap = torch.cuda.Stream()
+    s_cap.wait_stream(stream)
+    with torch.cuda.stream(s_cap):
+        plan.step(y)
+    stream.wait_stream(s_cap)
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph):
+        plan.step(y)
+    for _ in range(3):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record(stream)
+    for _ in range(args.steps):
+        step_graph.replay()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
+    ms_graph = ga.elapsed_time(gb) / args.steps
+    del step_graph
+
     # roofline of the dominant kernel (the larger of the row copy and combine)
     peak, peak_kind = peaks()
     dom = "rows" if ph["rows"] >= ph["combine"] else "combine"
@@ -759,6 +782,7 @@ def main():
             "effective_hbm_gbs": eff_gbs, "frac_of_8tbs": eff_gbs / world / NOMINAL_HBM_GBS,
             "frac_of_measured_copy_peak": eff_gbs / world / peak,
             "receive_rows": T, "phases_ms": ph, "step_ms": step_stats,
+            "ms_per_step_cuda_graph": ms_graph,
             "roofline": roofline, "other_rows": other, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 3 * args.steps if N > 0 else 0, "clocks": clk,
         }

@@ -168,6 +168,8 @@ FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
     (32, 40, 64, 8, 16),
     (7, 777, 28, 28, 24),   # K = E: every token to every rank
     (2, 9000, 8, 3, 16),    # more than 8192 tokens per rank: multi-block layout
+    (4, 300, 64, 32, 16),   # the largest top-k
+    (32, 50, 64, 32, 16),   # the largest rank count and top-k: 49 KB of scan staging
 ]
 
 
@@ -387,7 +389,8 @@ FUSED = [(1, 100, 4, 2, 64), (3, 300, 12, 3, 264), (8, 1000, 64, 8, 520), (16, 1
          (4, 257, 4, 2, 64),     # one expert per rank
          (3, 1, 6, 2, 64),       # a single token per rank
          (32, 300, 8192, 8, 16),  # the largest expert count: 32 KB of histogram per block
-         (8, 20000, 32, 4, 16)]  # more tiles than blocks, so blocks own several
+         (8, 20000, 32, 4, 16),  # more tiles than blocks, so blocks own several
+         (32, 50, 64, 32, 16)]   # the largest rank count and top-k
 
 
 @pytest.mark.parametrize("shape", FUSED, ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s)
@@ -669,7 +672,7 @@ LL_ONE_LAUNCH = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, 
                  dict(R=4, N=40, E=16, K=4, H=20480), dict(R=32, N=40, E=64, K=4, H=64),
                  dict(R=8, N=64, E=8192, K=8, H=64), dict(R=4, N=3000, E=64, K=6, H=64),
                  dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5), dict(R=1, N=40, E=3, K=3, H=64),
-                 dict(R=4, N=0, E=16, K=4, H=64)]
+                 dict(R=4, N=0, E=16, K=4, H=64), dict(R=2, N=50, E=64, K=32, H=64)]
 
 
 @pytest.mark.parametrize("cfg", LL_ONE_LAUNCH, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
