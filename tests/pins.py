@@ -62,8 +62,12 @@ def pin_bf16_rounding(orc) -> None:
     want = _bits(allv)
     bad = np.nonzero(got != want)[0]
     assert bad.size == 0, "bf16 narrowing differs from torch at %r" % (allv[bad[:5]],)
-    # NaN stays NaN
-    nan_bits = orc.f32_to_bf16_array(np.array([np.nan, -np.nan], np.float32))
+    # NaN stays NaN, whatever its payload (IEEE-754: a NaN operand gives a NaN), also
+    # when the payload sits only in the 16 bits that narrowing drops
+    nans = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF800001, 0x7F80FFFF, 0x7FBF0000],
+                    np.uint32).view(np.float32)
+    nan_bits = orc.f32_to_bf16_array(np.concatenate([np.array([np.nan, -np.nan], np.float32),
+                                                     nans]))
     assert all(((int(b) & 0x7f80) == 0x7f80 and (int(b) & 0x7f) != 0) for b in nan_bits)
     # widening is exact: compare with torch's bf16 -> fp32
     b = rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint16)
@@ -457,6 +461,53 @@ def pin_rsv_agv(orc) -> None:
     assert st == 0 and rs.shape == (0, 8)
 
 
+NONFINITE_CASES = [  # (addends in ascending rank order, expected bf16 bits; None = a NaN)
+    ([np.inf, 1.0], 0x7F80), ([1.0, -np.inf], 0xFF80), ([np.inf, np.inf], 0x7F80),
+    ([np.inf, -np.inf], None), ([np.nan, 1.0], None), ([1.0, 2.0, np.nan], None),
+    ([3.3895314e38, 3.3895314e38], 0x7F80),      # binary32 overflow: +Inf
+    ([-3.3895314e38, -3.3895314e38], 0xFF80),
+    ([3.3895314e38, 2.0**118], 0x7F7F),          # 0x7F7F4000: below the midpoint
+    ([3.3895314e38, 2.0**118, 2.0**117], 0x7F7F),  # 0x7F7F6000: still below
+    ([3.3895314e38, 2.0**118, 2.0**118], 0x7F80),  # 0x7F7F8000: a tie, odd kept half: up
+    ([-0.0, -0.0], 0x0000),                      # +0.0 start: (+0) + (-0) = +0
+    ([-0.0], 0x0000),
+    ([2.0**-126, -(2.0**-126)], 0x0000),         # exact cancellation to +0
+]
+
+
+def is_bf16_nan(bits) -> bool:
+    b = int(bits)
+    return (b & 0x7F80) == 0x7F80 and (b & 0x7F) != 0
+
+
+def pin_nonfinite_sums(orc) -> None:
+    """IEEE-754 closed forms for the combine's and the reduce-scatterv's sums: binary32
+    adds from +0.0 in rank order, then one round-to-nearest-even to bf16.  An infinity
+    survives, Inf + -Inf and NaN give NaN, a binary32 overflow gives Inf, and a sum
+    above bf16's largest finite value (0x7F7F = (2 - 2^-7) * 2^127, its ulp 2^120)
+    rounds up only from the midpoint 0x7F7F8000 on."""
+    H = 8
+    for addends, want in NONFINITE_CASES:
+        n = len(addends)
+        rows = _bits(np.repeat(np.array(addends, np.float32)[:, None], H, axis=1))
+        a32 = np.array(addends, np.float32)
+        fin = ~np.isnan(a32)  # every addend is a bf16 value (NaNs: any NaN)
+        assert np.array_equal(_f32(rows)[fin, 0].view(np.uint32), a32[fin].view(np.uint32))
+        assert np.isnan(_f32(rows)[~fin, 0]).all(), addends
+        send_row = np.full((n, 1, n), -1, np.int32)
+        send_row[0, 0] = np.arange(n)
+        comb, st = orc.combine(rows, send_row)
+        sizes = [0] * n
+        sizes[n - 1] = 1
+        rs, st2 = orc.reducescatterv(rows.reshape(n, 1, H), sizes)
+        assert st == 0 and st2 == 0
+        for got in (comb[0, 0], rs[0]):
+            if want is None:
+                assert all(is_bf16_nan(b) for b in got), (addends, got)
+            else:
+                assert all(int(b) == want for b in got), (addends, [hex(int(b)) for b in got])
+
+
 # --------------------------------------------------------------------------
 # FP8 E4M3 narrowing and per-128-channel block quantisation
 # --------------------------------------------------------------------------
@@ -615,7 +666,7 @@ def pin_mxfp4_quantisation(orc) -> None:
     assert np.all(np.signbit(deq) == np.signbit(xf))
 
 
-ALL_PINS = [pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
+ALL_PINS = [pin_nonfinite_sums, pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
             pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
             pin_low_latency_layout, pin_mxfp8_quantisation, pin_mxfp4_quantisation,

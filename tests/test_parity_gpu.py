@@ -157,6 +157,95 @@ def test_sum_order_fixture_on_gpu():
     assert int(err.item()) == 0
 
 
+def assert_bits_or_both_nan(got_bits, want_bits, what):
+    """Bit-exact where the oracle's result is a number (infinities included); a NaN
+    where it is a NaN (NaN payloads are not compared)."""
+    g = np.asarray(got_bits).astype(np.uint32)
+    w = np.asarray(want_bits).astype(np.uint32)
+    gn = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    wn = ((w & 0x7F80) == 0x7F80) & ((w & 0x7F) != 0)
+    assert np.array_equal(gn, wn), "%s: NaN positions differ (%d vs %d)" % (
+        what, int(gn.sum()), int(wn.sum()))
+    bad = np.nonzero(g[~wn] != w[~wn])[0]
+    assert bad.size == 0, "%s: %d results differ, first %s vs %s" % (
+        what, bad.size, hex(int(g[~wn][bad[0]])), hex(int(w[~wn][bad[0]])))
+
+
+def _tb(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def test_nonfinite_sums_match_oracle():
+    """Infinities, NaNs, signed zeros and sums past bf16's or binary32's largest value,
+    through the combine and the reduce-scatterv: the IEEE closed forms the oracle is
+    pinned to, then random rows with such values sprinkled in."""
+    H = 8
+    for addends, _ in pins.NONFINITE_CASES:
+        n = len(addends)
+        rows = pins._bits(np.repeat(np.array(addends, np.float32)[:, None], H, axis=1))
+        send_row = np.full((n, 1, n), -1, np.int32)
+        send_row[0, 0] = np.arange(n)
+        want, st = oracle.combine(rows, send_row)
+        out = torch.zeros((n, 1, H), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.check(B.mp_combine(n, 1, H, _tb(rows), n, torch.from_numpy(send_row).cuda(), out, err))
+        sizes = [0] * n
+        sizes[n - 1] = 1
+        want_rs, st2 = oracle.reducescatterv(rows.reshape(n, 1, H), sizes)
+        rs = torch.zeros((1, H), dtype=torch.bfloat16, device="cuda")
+        B.check(B.mp_reducescatterv(n, H, sizes, _tb(rows.reshape(n, 1, H)), rs))
+        torch.cuda.synchronize()
+        assert st == st2 == 0 and int(err.item()) == 0
+        assert_bits_or_both_nan(wl.bf16_bits(out), want, "combine %r" % (addends,))
+        assert_bits_or_both_nan(wl.bf16_bits(rs), want_rs, "reduce-scatterv %r" % (addends,))
+    # random rows, 1% each of +Inf, -Inf, NaN, +-bf16 max and -0.0 among N(0,1) values
+    inp = wl.make_ep(dict(R=4, N=300, E=16, K=4, H=136, routing="uniform", dtype="bf16"), seed=77)
+    plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H)
+    plan.load(inp)
+    B.check(plan.layout())
+    B.check(plan.dispatch_offsets())
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(78)
+
+    def sprinkle(shape):
+        v = rng.standard_normal(shape).astype(np.float32)
+        u = rng.random(shape)
+        special = [np.inf, -np.inf, np.nan, 3.3895314e38, -3.3895314e38, -0.0]
+        for i, val in enumerate(special):
+            v[(u >= i * 0.01) & (u < (i + 1) * 0.01)] = val
+        return pins._bits(v)
+
+    y = sprinkle((plan.cap, inp.H))
+    B.check(plan.combine(_tb(y)))
+    torch.cuda.synchronize()
+    want, st = oracle.combine(y, plan.send_row.cpu().numpy())
+    assert st == 0 and plan.device_error() == 0
+    assert_bits_or_both_nan(wl.bf16_bits(plan.out), want, "combine, sprinkled")
+    sizes = [7, 0, 130, 1, 64]
+    x = sprinkle((5, sum(sizes), 136))
+    rs = torch.zeros((sum(sizes), 136), dtype=torch.bfloat16, device="cuda")
+    B.check(B.mp_reducescatterv(5, 136, sizes, _tb(x), rs))
+    torch.cuda.synchronize()
+    want_rs, st = oracle.reducescatterv(x, sizes)
+    assert st == 0
+    assert_bits_or_both_nan(wl.bf16_bits(rs), want_rs, "reduce-scatterv, sprinkled")
+    # the weighted low-latency combine: products and sums in binary32 (0 * Inf = NaN)
+    ll, st = oracle.dispatch_ll(np.zeros((inp.R, inp.N, 8), np.uint16), inp.topk_idx, inp.E)
+    assert st == 0
+    yl = sprinkle((ll["num_recv"], 136))
+    w = inp.topk_weights.copy()
+    w[:, ::9, 0] = 0.0
+    want_ll, st = oracle.combine_ll(yl, ll["slot_row"], w)
+    out = torch.zeros((inp.R, inp.N, 136), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.check(B.mp_combine_ll(inp.R, inp.N, inp.K, 136, _tb(yl), ll["num_recv"],
+                            torch.from_numpy(ll["slot_row"]).cuda(), torch.from_numpy(w).cuda(),
+                            out, err))
+    torch.cuda.synchronize()
+    assert st == 0 and int(err.item()) == 0
+    assert_bits_or_both_nan(wl.bf16_bits(out), want_ll, "weighted LL combine, sprinkled")
+
+
 FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
     (1, 100, 4, 2, 64),
     (2, 257, 8, 2, 136),
