@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true",
                     help="skip timing the e4m3 dispatch and reduce-scatterv / all-gatherv rows")
+    ap.add_argument("--other-rows-scale", type=int, default=1,
+                    help="divide the other rows' token counts by this (a cut-down run for "
+                         "profiling; >1 also runs them beside --tokens)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -266,7 +269,7 @@ def config_block(name, inp):
 # ---------------------------------------------------------------------------
 # the other rows of the path on their own workloads (device-timed)
 # ---------------------------------------------------------------------------
-def measure_other_rows(steps: int, peak: float):
+def measure_other_rows(steps: int, peak: float, scale: int = 1):
     """The rows besides the dsv3 step: in-kernel quantise-dispatch (e4m3, MXFP8, MXFP4) of
     the dsv3 rows; e4m3 dispatch (R=8, N=8192, H=7168, per-128-channel fp32 scales,
     top-8 of 256) with its bf16 combine; reduce-scatterv / all-gatherv (R=8, H=4096,
@@ -299,7 +302,7 @@ def measure_other_rows(steps: int, peak: float):
     out = {}
     # in-kernel e4m3 quantisation on dispatch, on the dsv3 workload
     cfg = wl.CONFIGS["dsv3"]
-    R, N, H, E, K = cfg["R"], cfg["N"], cfg["H"], cfg["E"], cfg["K"]
+    R, N, H, E, K = cfg["R"], cfg["N"] // scale, cfg["H"], cfg["E"], cfg["K"]
     rng = np.random.default_rng(0)
     g = torch.Generator(device="cuda").manual_seed(0)
     plan = EPPlan(R, N, K, E, H, "bf16")
@@ -362,7 +365,7 @@ def measure_other_rows(steps: int, peak: float):
     torch.cuda.empty_cache()
 
     cfg = wl.CONFIGS["fp8"]
-    R, N, H, E, K = cfg["R"], cfg["N"], cfg["H"], cfg["E"], cfg["K"]
+    R, N, H, E, K = cfg["R"], cfg["N"] // scale, cfg["H"], cfg["E"], cfg["K"]
     rng = np.random.default_rng(0)
     plan = EPPlan(R, N, K, E, H, "e4m3")
     plan.topk_idx.copy_(torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)))
@@ -387,7 +390,7 @@ def measure_other_rows(steps: int, peak: float):
     torch.cuda.empty_cache()
 
     cfg = wl.CONFIGS["rsv"]
-    sizes = np.random.default_rng(0).integers(0, cfg["max_rows"] + 1, cfg["R"]).tolist()
+    sizes = np.random.default_rng(0).integers(0, cfg["max_rows"] // scale + 1, cfg["R"]).tolist()
     rp = RSVPlan(cfg["R"], cfg["H"], sizes)
     rp.x.normal_(generator=g)
     rp.shards.normal_(generator=g)
@@ -537,7 +540,7 @@ def measure_other_rows(steps: int, peak: float):
     torch.cuda.empty_cache()
 
     # the skewed workload: Zipf(1.2) routing, rank 0 hot
-    inp = wl.make_ep("skew", seed=0)
+    inp = wl.make_ep("skew", seed=0, N=wl.CONFIGS["skew"]["N"] // scale)
     R, N, H, E, K = inp.R, inp.N, inp.H, inp.E, inp.K
     plan = EPPlan(R, N, K, E, H, "bf16")
     plan.load(inp)
@@ -762,8 +765,14 @@ def main():
                                    "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in nb}}
 
     other = None
-    if not args.no_other_rows and args.config == "dsv3" and args.tokens == 0:
-        other = measure_other_rows(max(10, min(args.steps, 100)), peaks()[0])
+    if not args.no_other_rows and args.config == "dsv3" and (args.tokens == 0 or
+                                                            args.other_rows_scale > 1):
+        if args.other_rows_scale > 1:  # a cut-down run (for profiling): token counts / scale
+            other = measure_other_rows(max(1, min(args.steps, 100)), peaks()[0],
+                                       args.other_rows_scale)
+            other["token_counts_divided_by"] = args.other_rows_scale
+        else:
+            other = measure_other_rows(max(10, min(args.steps, 100)), peaks()[0])
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
