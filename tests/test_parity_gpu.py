@@ -811,6 +811,54 @@ def test_low_latency_one_launch_dispatch_matches_oracle(cfg, rank_major, counts)
     assert (st == 0) == (cap_frac is None)
 
 
+def test_low_latency_one_launch_dispatch_replays_as_a_cuda_graph():
+    """mp_dispatch_ll + mp_combine_ll captured once and replayed: the ticket and epoch
+    live in the workspace, so every replay starts where the last one left them."""
+    R, N, E, K, H = 4, 96, 32, 4, 136
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=33)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    cap = R * N * K
+    dev = "cuda"
+    eoff = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    esoff = torch.zeros((E, R), dtype=torch.int32, device=dev)
+    src = torch.zeros(cap, dtype=torch.int32, device=dev)
+    slot = torch.zeros((R, N, K), dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+    out = torch.zeros((R, N, H), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None, plan.topk_idx, None,
+                                 cap, eoff, esoff, src, slot, rx, None, plan.dev_err,
+                                 plan.workspace))
+        B.check(B.mp_combine_ll(R, N, K, H, rx, cap, slot, plan.topk_weights, out,
+                                plan.dev_err))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    ll, st = oracle.dispatch_ll(wl.bf16_bits(inp.x), inp.topk_idx, E)
+    comb, st2 = oracle.combine_ll(ll["recv_x"], ll["slot_row"], inp.topk_weights)
+    assert st == st2 == 0
+    n = ll["num_recv"]
+    for _ in range(3):
+        rx.zero_()
+        out.zero_()
+        slot.fill_(-3)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_error() == 0
+        assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+        assert np.array_equal(wl.bf16_bits(rx[:n]), ll["recv_x"])
+        assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll after replay")
+
+
 def test_low_latency_one_launch_dispatch_e4m3_with_scales():
     R, N, E, K, H = 4, 200, 32, 4, 384
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="e4m3"), seed=32)
