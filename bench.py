@@ -792,6 +792,13 @@ def main():
             "frac_of_measured_copy_peak": eff_gbs / world / peak,
             "receive_rows": T, "phases_ms": ph, "step_ms": step_stats,
             "ms_per_step_cuda_graph": ms_graph,
+            # the pages' bench convention, for comparison only: tokens x hidden bytes per
+            # dispatch / combine (no count of the expanded receive rows)
+            "send_side_convention": {
+                "bytes": R * N * H * (2 if inp.dtype == "bf16" else 1),
+                "dispatch_GBs": R * N * H * (2 if inp.dtype == "bf16" else 1)
+                                / (ph["dispatch"] / 1e3) / 1e9,
+                "combine_GBs": R * N * H * 2 / (ph["combine"] / 1e3) / 1e9},
             "roofline": roofline, "other_rows": other, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 3 * args.steps if N > 0 else 0, "clocks": clk,
         }
