@@ -31,6 +31,20 @@
 #include "mp_common.cuh"
 #include "mp_internal.h"
 
+// Longest back-off (ns) between polls of a predecessor tile's flag (the
+// back-off starts at 32 ns and doubles up to this).  Measured on the fused
+// layout + offsets (dsv3, 256 tiles): 1024 ns 24.4 us, 128 ns 22.9-23.3 us,
+// 32 ns (no doubling) 22.5 us per call.
+#ifndef MP_LOOKBACK_MAX_NAP
+#define MP_LOOKBACK_MAX_NAP 32
+#endif
+// The fused layout + offsets kernel issues its first id loads before it
+// publishes the epoch it read (1) or after (0): 24.5 -> 24.4 us (dsv3),
+// 28.0/26.7 -> 26.7 us (skew), 23.5 -> 22.4 us (dsv3 at N = 128).
+#ifndef MP_FUSED_EARLY_LOADS
+#define MP_FUSED_EARLY_LOADS 1
+#endif
+
 namespace mp {
 
 // ---------------------------------------------------------------------------
@@ -211,7 +225,7 @@ __device__ __forceinline__ uint32_t tile_publish_lookback(
         while ((f >> 2) != epoch || (f & 3u) == 0) {
           if (++spins > kSpinLimit) { timed_out = true; break; }
           __nanosleep(nap);
-          if (nap < 1024) nap <<= 1;
+          if (nap < MP_LOOKBACK_MAX_NAP) nap <<= 1;
           f = ld_acquire_u32(&flags[p]);
         }
         status = timed_out ? kStatusInclusive : (f & 3u);
@@ -518,13 +532,22 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   int32_t* acc = reinterpret_cast<int32_t*>(a.ws + ws_acc_offset());  // [R][E + R]
   const int C = int(scan_tiles_per_rank(N));
   const int T = R * C;
+  // The epoch and barrier generation are read first; thread 0 keeps them in
+  // registers until the first tile's id loads are issued, so those loads do
+  // not wait for them (the first tile's barrier publishes them).
+  uint32_t epoch0 = 0, gen0 = 0;
   if (tid == 0) {
-    sh_epoch = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
-    sh_gen = ld_relaxed_u32(&ctl->bar_gen);
+    epoch0 = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
+    gen0 = ld_relaxed_u32(&ctl->bar_gen);
+  }
+#if !MP_FUSED_EARLY_LOADS
+  if (tid == 0) {
+    sh_epoch = epoch0;
+    sh_gen = gen0;
     sh_bad = 0;
   }
   __syncthreads();
-  const uint32_t epoch = sh_epoch;
+#endif
   // A block that owns a single tile keeps that tile's ids, weights, ballots
   // and offsets in shared memory across the barrier instead of reloading them.
   const bool single = T <= int(gridDim.x);
@@ -546,6 +569,13 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
         if (single) w_s[i] = __ldg(gw + i);
       }
     }
+#if MP_FUSED_EARLY_LOADS
+    if (it == 0 && tid == 0) {
+      sh_epoch = epoch0;
+      sh_gen = gen0;
+      sh_bad = 0;
+    }
+#endif
     __syncthreads();
     uint32_t mask = 0;
     if (tid < ntok) {
@@ -569,7 +599,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     for (int i = tid; i < E; i += kScanThreads)
       if (hist[i]) atomicAdd(&acc_s[i], hist[i]);
     if (warp == 0) {
-      const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, epoch, wball, woff, tcount,
+      const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, sh_epoch, wball, woff, tcount,
                                                   tcnt, flags, agg, incl, a.dev_err);
       if (lane < R) tile_excl[it][lane] = excl;
     }
