@@ -24,7 +24,8 @@
 // launch with one grid barrier between the lookback and the rows.
 //
 // Low-latency offsets (mp_k_ll_offsets): one row per (token, top-k slot),
-// grouped by expert or by the rank owning it, by a per-rank counting sort.
+// grouped by expert or by the rank owning it, by a per-rank counting sort;
+// mp_k_ll_dispatch runs that sort and the row copy in one launch.
 #include <cstddef>
 #include <cstdint>
 
@@ -718,8 +719,9 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
 // token, then top-k slot.
 //
 // One block per source rank s, a stable counting sort of its N*K entries:
-//  1. the rank's entries are cut into nseg contiguous segments, one per warp,
-//     and each warp counts its segment's entries per expert in shared memory;
+//  1. the rank's entries are cut into nseg contiguous segments (one per warp
+//     in step 3); one pass of the whole block over the ids counts the
+//     entries of each (segment, expert) in shared memory;
 //  2. every expert's first row (a block-wide scan of the per-expert totals
 //     over all source ranks, from the layout's num_tokens_per_expert, plus
 //     the rows of e from ranks < s) and, per expert, the exclusive prefix of
@@ -727,9 +729,10 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
 //  3. each warp walks its segment 32 entries at a time in order; lanes with
 //     the same expert find each other with __match_any_sync and take
 //     consecutive rows, so the order is deterministic.
-// num_tokens_per_expert may be NULL: each block then counts every rank's ids
-// itself (R*N*K reads from L2 per block), which saves the layout launch on
-// the small batches this path is for.
+// num_tokens_per_expert may be NULL: the pass of step 1 then reads every
+// rank's ids (R*N*K reads from L2 per block) and counts the totals and
+// lower-rank prefixes too, which saves the layout launch on the small batches
+// this path is for.
 // Shared memory: (nseg + 3) * E int32, nseg = min(32, 16384 / E) (>= 1).
 // ---------------------------------------------------------------------------
 constexpr int kLLThreads = 1024;
