@@ -259,6 +259,8 @@ FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
     (2, 9000, 8, 3, 16),    # more than 8192 tokens per rank: multi-block layout
     (4, 300, 64, 32, 16),   # the largest top-k
     (32, 50, 64, 32, 16),   # the largest rank count and top-k: 49 KB of scan staging
+    (2, 40, 8, 2, 32776),   # 64 KB rows, 16-byte vectors
+    (3, 30, 6, 2, 30720),   # 60 KB rows, 32-byte vectors
 ]
 
 
@@ -549,6 +551,18 @@ def test_empty_tokens():
     plan = run_gpu(inp)
     assert plan.num_tokens_per_rank.abs().sum().item() == 0
     assert plan.dest_offsets.abs().sum().item() == 0
+    # the one-call layout + offsets and the whole step: every count and offset table is
+    # written (zeros), whatever the buffers held before
+    for t in (plan.num_tokens_per_rank, plan.num_tokens_per_expert, plan.dest_offsets,
+              plan.rank_prefix, plan.num_recv_tokens_per_expert):
+        t.fill_(-3)
+    B.check(plan.layout_and_offsets())
+    plan.step()
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    for t in (plan.num_tokens_per_rank, plan.num_tokens_per_expert, plan.dest_offsets,
+              plan.rank_prefix, plan.num_recv_tokens_per_expert):
+        assert not t.any().item()
 
 
 def test_all_masked():
