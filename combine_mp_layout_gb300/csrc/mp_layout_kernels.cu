@@ -259,73 +259,98 @@ __device__ __forceinline__ uint32_t tile_publish_lookback(
   return excl;
 }
 
-// The rows of one scan tile: each token's row at each destination is staged
-// in shared memory (send_row) and as a per-destination token list, so that
-// the stores run along contiguous rows (a tile's rows for one destination are
-// consecutive).  Called by all threads of the block; needs the tile's masks
-// (one per token thread), the per-warp ballots and offsets, the tile's first
-// row and row count per destination, and its top-k ids and weights staged in
-// shared memory.
+// The rows of one scan tile.  A tile's rows for one destination are
+// consecutive, so the tile's rows are numbered destination-major (j =
+// dstart[d] + rank within d) and two shared-memory tables give each j its
+// token and destination; the metadata stores then run over all of the tile's
+// rows (and rows x top-k slots) at once, contiguous within each destination.
+// Each token's row at each destination is staged in shared memory (send_row).
+// Called by all threads of the block; needs the tile's masks (one per token
+// thread), the per-warp ballots and offsets, the tile's first row and row
+// count per destination, and its top-k ids and weights staged in shared memory.
+struct TileRowsSmem {
+  int32_t* sr_s;     // [kScanTokens][R]: send_row entries of the tile's tokens
+  uint8_t* row_tok;  // [kScanTokens * MP_MAX_RANKS]: token of tile row j
+  uint8_t* row_d;    // [kScanTokens * MP_MAX_RANKS]: destination of tile row j
+  int32_t* dstart;   // [MP_MAX_RANKS + 1]: first tile row of destination d
+  int32_t* nok;      // [MP_MAX_RANKS]: rows of d within the receive capacity
+};
+
 __device__ __forceinline__ void write_tile_rows(
     const ScanArgs& a, uint32_t mask, int ntok, int t0, int64_t g0, int src_rank,
     const uint32_t (*wball)[MP_MAX_RANKS], const int32_t (*woff)[MP_MAX_RANKS],
     const int64_t* row_base, const uint32_t* tcnt, const int32_t* idx_s, const float* w_s,
-    int32_t* sr_s, uint8_t (*tok_of)[kScanTokens]) {
+    const TileRowsSmem& sm) {
   const int R = a.R, K = a.K, E = a.E;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  // Each token's row at each destination: staged in shared memory (send_row)
-  // and as a per-destination token list, so that the stores below run along
-  // contiguous rows (a tile's rows for one destination are consecutive).
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (warp == 0) {  // destination-major numbering of the tile's rows; the capacity clamp
+    const int c = lane < R ? int(tcnt[lane]) : 0;
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += v;
+    }
+    int ok = c;
+    if (lane < R) {
+      sm.dstart[lane] = inc - c;
+      const int64_t room = a.recv_capacity - row_base[lane];
+      ok = room <= 0 ? 0 : (room < c ? int(room) : c);
+      sm.nok[lane] = ok;
+    }
+    if (lane == 31) sm.dstart[R] = inc;
+    if (__any_sync(kFull, ok < c) && lane == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
+  }
+  if (tid < ntok)
+    for (int d = 0; d < R; ++d) sm.sr_s[tid * R + d] = -1;
+  __syncthreads();
   if (tid < ntok) {
-    for (int d = 0; d < R; ++d) {
-      int32_t out = -1;
-      if ((mask >> d) & 1u) {
-        const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
-        tok_of[d][rank] = uint8_t(tid);
-        const int64_t row = row_base[d] + rank;
-        if (row < a.recv_capacity) out = int32_t(row);
-      }
-      sr_s[tid * R + d] = out;
+    for (uint32_t m = mask; m; m &= m - 1u) {
+      const int d = __ffs(m) - 1;
+      const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
+      const int j = sm.dstart[d] + rank;
+      sm.row_tok[j] = uint8_t(tid);
+      sm.row_d[j] = uint8_t(d);
+      if (rank < sm.nok[d]) sm.sr_s[tid * R + d] = int32_t(row_base[d] + rank);
     }
   }
   __syncthreads();
 #pragma unroll 4
-  for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sr_s[i];
-  {
-    const int El = E / R;
-    const int step_r = kScanThreads / K, step_k = kScanThreads - step_r * K;
-    bool overflow = false;
-    for (int d = 0; d < R; ++d) {
-      const int64_t base = row_base[d];
-      const int cnt = int(tcnt[d]);
-      const int64_t room = a.recv_capacity - base;
-      const int n_ok = room <= 0 ? 0 : (room < cnt ? int(room) : cnt);
-      overflow |= n_ok < cnt;
+  for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sm.sr_s[i];
+  const int total = sm.dstart[R];
 #pragma unroll 4
-      for (int i = tid; i < n_ok; i += kScanThreads) {
-        a.recv_src_rank[base + i] = src_rank;
-        a.recv_src_idx[base + i] = t0 + tok_of[d][i];
-      }
-      const int lo = d * El, hi = lo + El;
-      // element i = r*K + k of this destination's rows; (r, k) advance by
-      // (kScanThreads / K, kScanThreads % K) per step, avoiding a division
-      int r = tid / K, k = tid - (tid / K) * K;
-#pragma unroll 4
-      for (int i = tid; i < n_ok * K; i += kScanThreads) {
-        const int tk = tok_of[d][r];
-        const int e = idx_s[tk * K + k];
-        const bool local = e >= lo && e < hi;
-        a.recv_topk_idx[base * K + i] =
-            a.global_ids ? (local ? e : a.sentinel) : (local ? e - lo : -1);
-        a.recv_topk_weights[base * K + i] = local ? w_s[tk * K + k] : 0.0f;
-        r += step_r;
-        k += step_k;
-        if (k >= K) { k -= K; ++r; }
-      }
+  for (int j = tid; j < total; j += kScanThreads) {
+    const int d = sm.row_d[j], r = j - sm.dstart[d];
+    if (r < sm.nok[d]) {
+      const int64_t row = row_base[d] + r;
+      a.recv_src_rank[row] = src_rank;
+      a.recv_src_idx[row] = t0 + sm.row_tok[j];
     }
-    if (overflow && tid == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
   }
-
+  // element i = j*K + k of the tile's (row, slot) pairs; (j, k) advance by
+  // (kScanThreads / K, kScanThreads % K) per step, avoiding a division
+  const int El = E / R;
+  const int step_j = kScanThreads / K, step_k = kScanThreads - step_j * K;
+  int j = tid / K, k = tid - (tid / K) * K;
+#pragma unroll 4
+  for (int i = tid; i < total * K; i += kScanThreads) {
+    const int d = sm.row_d[j], r = j - sm.dstart[d];
+    if (r < sm.nok[d]) {
+      const int tk = sm.row_tok[j];
+      const int e = idx_s[tk * K + k];
+      const int lo = d * El;
+      const bool local = e >= lo && e < lo + El;
+      const int64_t o = (row_base[d] + r) * K + k;
+      a.recv_topk_idx[o] = a.global_ids ? (local ? e : a.sentinel) : (local ? e - lo : -1);
+      a.recv_topk_weights[o] = local ? w_s[tk * K + k] : 0.0f;
+    }
+    j += step_j;
+    k += step_k;
+    if (k >= K) {
+      k -= K;
+      ++j;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
@@ -339,7 +364,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   __shared__ uint32_t tcount[MP_MAX_RANKS];                // tile counts, then inclusive prefix
   __shared__ uint32_t tcnt[MP_MAX_RANKS];                  // tile counts
   __shared__ int64_t row_base[MP_MAX_RANKS];               // first receive row of the tile at d
-  __shared__ uint8_t tok_of[MP_MAX_RANKS][kScanTokens];    // [d][rank within d] -> token
+  __shared__ uint8_t row_tok[kScanTokens * MP_MAX_RANKS], row_d[kScanTokens * MP_MAX_RANKS];
+  __shared__ int32_t dstart[MP_MAX_RANKS + 1], nok[MP_MAX_RANKS];
   __shared__ uint32_t sh_tile, sh_epoch;
   __shared__ int sh_last;
 
@@ -431,8 +457,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   }
   __syncthreads();
 
-  write_tile_rows(a, mask, ntok, t0, g0, src_rank, wball, woff, row_base, tcnt, idx_s, w_s, sr_s,
-                  tok_of);
+  write_tile_rows(a, mask, ntok, t0, g0, src_rank, wball, woff, row_base, tcnt, idx_s, w_s,
+                  TileRowsSmem{sr_s, row_tok, row_d, dstart, nok});
 
   // the last block out resets the counters and moves to the next epoch
   __syncthreads();
@@ -519,7 +545,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   __shared__ uint32_t tcnt[MP_MAX_RANKS];
   __shared__ int64_t row_base[MP_MAX_RANKS];
   __shared__ int64_t dest_base[MP_MAX_RANKS];
-  __shared__ uint8_t tok_of[MP_MAX_RANKS][kScanTokens];
+  __shared__ uint8_t row_tok[kScanTokens * MP_MAX_RANKS], row_d[kScanTokens * MP_MAX_RANKS];
+  __shared__ int32_t dstart[MP_MAX_RANKS + 1], nok[MP_MAX_RANKS];
   __shared__ uint32_t tile_excl[kFusedMaxTiles][MP_MAX_RANKS];
   __shared__ uint32_t sh_epoch, sh_gen;
   __shared__ int sh_bad, sh_ok;
@@ -705,8 +732,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       row_base[lane] = dest_base[lane] + pre + tile_excl[it][lane];
     }
     __syncthreads();
-    write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s, sr_s,
-                    tok_of);
+    write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s,
+                    TileRowsSmem{sr_s, row_tok, row_d, dstart, nok});
     __syncthreads();
   }
 }
