@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override N (tokens per rank), e.g. for small profiler captures")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true",
                     help="skip timing the e4m3 dispatch and reduce-scatterv / all-gatherv rows")
