@@ -1,16 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the MoE layout -> dispatch -> combine hot path on one GB300.
 
-One step = mp_layout + mp_dispatch (scan + row copy) + mp_combine on the
-DeepSeek-V3-shaped workload (R=8 logical ranks x N=4096 tokens, H=7168 bf16,
-E=256 experts, top-8 uniform routing), the combine input being the
-dispatched rows themselves (identity experts).  Inputs are synthetic and
+One step = mp_layout_and_offsets (layout + receive offsets, one launch) +
+mp_dispatch_rows (row copy) + mp_combine on the DeepSeek-V3-shaped workload
+(R=8 logical ranks x N=4096 tokens, H=7168 bf16, E=256 experts, top-8 uniform
+routing), the combine input being the dispatched rows themselves (identity
+experts).  Inputs are synthetic and
 seeded, resident in HBM for the device-timed value; the e2e value adds the
 host->device copy of the step's inputs and the device->host copy of its
 result, from/to pinned host memory.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead
-(the reference arm of this build: a plain single-threaded C program).
+(a plain single-threaded C program that defines every step).
 
 Multi-GPU: the path has no exchange between GPUs (all R logical ranks live in
 one GPU's memory), so N GPUs run N independent replicas (weak scaling); the
