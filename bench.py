@@ -439,8 +439,8 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
     torch.cuda.empty_cache()
 
     # low-latency expert-major layout at the pages' small-batch shape (R=8, N=128,
-    # H=7168, top-8 of 256): layout -> LL offsets -> LL rows -> weighted LL combine,
-    # launched one by one and replayed as one CUDA graph
+    # H=7168, top-8 of 256): LL offsets + LL rows -> weighted LL combine, launched one
+    # by one and replayed as one CUDA graph
     R, N, H, E, K = 8, 128, 7168, 256, 8
     rng = np.random.default_rng(1)
     plan = EPPlan(R, N, K, E, H, "bf16")
@@ -456,56 +456,88 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
     yl = torch.randn((cap, H), generator=g, device="cuda").to(torch.bfloat16)
     lo = torch.empty((R, N, H), dtype=torch.bfloat16, device="cuda")
 
-    def ll_step():  # the LL offsets count the experts themselves: no layout launch
-        B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff, esoff,
-                                         src, slot, plan.dev_err))
-        B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
-        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
-
-    ms_ll = timed(ll_step, steps)
-    ll_calls = [
-        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff,
-                                                 esoff, src, slot, plan.dev_err)),
-        lambda: B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap,
-                                              rx, None)),
-        lambda: B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo,
-                                        plan.dev_err))]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ll_calls) + 1)]
-           for _ in range(steps)]
-    for ev in evs:
-        ev[0].record()
-        for c, call in enumerate(ll_calls):
-            call()
-            ev[c + 1].record()
-    torch.cuda.synchronize()
-    ll_phase_us = {name: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / steps * 1e3
-                   for c, name in enumerate(("ll_offsets", "ll_rows", "combine_ll"))}
     s_cap = torch.cuda.Stream()
-    s_cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s_cap):
-        ll_step()
-    torch.cuda.current_stream().wait_stream(s_cap)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        ll_step()
-    ms_llg = timed(graph.replay, steps)
-    assert plan.device_error() == 0
+
+    def as_graph(fn):  # fn captured once as a CUDA graph (after one call outside)
+        s_cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_cap):
+            fn()
+        torch.cuda.current_stream().wait_stream(s_cap)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        return gr
+
+    def phases(calls, names):  # per-call CUDA-event times, us
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+               for _ in range(steps)]
+        for ev in evs:
+            ev[0].record()
+            for c, call in enumerate(calls):
+                call()
+                ev[c + 1].record()
+        torch.cuda.synchronize()
+        return {nm: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / steps * 1e3
+                for c, nm in enumerate(names)}
+
     ll_bytes = (R * N * K * 8 + cap * 4 + (E + 1) * 4 + E * R * 4  # LL offsets
                 + R * N * H * 2 + cap * H * 2 + R * N * K * 4           # LL rows
                 + cap * H * 2 + R * N * K * 8 + R * N * H * 2)          # weighted LL combine
+
+    # one call for the LL offsets and rows (the sort, then the row copy as its
+    # programmatic dependent), then the weighted combine
+    ll_calls = [
+        lambda: B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None,
+                                         plan.topk_idx, None, cap, eoff, esoff, src, slot, rx,
+                                         None, plan.dev_err)),
+        lambda: B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo,
+                                        plan.dev_err))]
+
+    def ll_step():
+        for c in ll_calls:
+            c()
+
+    ms_ll = timed(ll_step, steps)
+    ll_phase_us = phases(ll_calls, ("dispatch_ll", "combine_ll"))
+    graph = as_graph(ll_step)
+    ms_llg = timed(graph.replay, steps)
+    assert plan.device_error() == 0
     out["low_latency_step_n128"] = dict(
         row(ms_ll, ll_bytes), us_per_step=ms_ll * 1e3, us_per_step_cuda_graph=ms_llg * 1e3,
         phases_us=ll_phase_us, receive_rows=int(cap),
         GBs_cuda_graph=ll_bytes / (ms_llg / 1e3) / 1e9,
-        workload="R=8, N=128, H=7168 bf16, E=256, top-8: LL offsets (counting the experts "
-                 "themselves) + LL rows + weighted LL combine (3 launches)")
+        workload="R=8, N=128, H=7168 bf16, E=256, top-8: mp_dispatch_ll (LL offsets counting "
+                 "the experts themselves, then the LL rows as a programmatic dependent) + "
+                 "weighted LL combine")
+
+    # the same step as three calls: LL offsets, LL rows, weighted combine
+    ll3_calls = [
+        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff,
+                                                 esoff, src, slot, plan.dev_err)),
+        lambda: B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap,
+                                              rx, None)),
+        ll_calls[1]]
+
+    def ll3_step():
+        for c in ll3_calls:
+            c()
+
+    ms_ll3 = timed(ll3_step, steps)
+    ll3_phase_us = phases(ll3_calls, ("ll_offsets", "ll_rows", "combine_ll"))
+    graph3 = as_graph(ll3_step)
+    ms_ll3g = timed(graph3.replay, steps)
+    assert plan.device_error() == 0
+    out["low_latency_three_calls_step_n128"] = dict(
+        row(ms_ll3, ll_bytes), us_per_step=ms_ll3 * 1e3, us_per_step_cuda_graph=ms_ll3g * 1e3,
+        phases_us=ll3_phase_us, GBs_cuda_graph=ll_bytes / (ms_ll3g / 1e3) / 1e9,
+        workload="as low_latency_step_n128 with the LL offsets and the LL rows as two calls "
+                 "(3 launches, no overlap)")
     doff = torch.empty(R + 1, dtype=torch.int32, device="cuda")
     dsoff = torch.empty((R, R), dtype=torch.int32, device="cuda")
 
     def ll_rm_step():  # rank-major output: rows grouped by the rank owning the expert
-        B.check(B.mp_dispatch_ll_offsets_rank_major(R, N, K, E, plan.topk_idx, None, cap, doff,
-                                                    dsoff, src, slot, plan.dev_err))
-        B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap, rx, None))
+        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 1, plan.x, None, plan.topk_idx,
+                                 None, cap, doff, dsoff, src, slot, rx, None, plan.dev_err))
         B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
 
     ms_rm = timed(ll_rm_step, steps)
@@ -515,29 +547,7 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
         row(ms_rm, rm_bytes), us_per_step=ms_rm * 1e3,
         workload="as low_latency_step_n128 with rank-major output (rows grouped by the rank "
                  "owning the expert)")
-
-    def ll_one_step():  # sort and row copy in one launch, then the weighted combine
-        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None, plan.topk_idx,
-                                 None, cap, eoff, esoff, src, slot, rx, None, plan.dev_err,
-                                 plan.workspace))
-        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
-
-    ms_one = timed(ll_one_step, steps)
-    s_cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s_cap):
-        ll_one_step()
-    torch.cuda.current_stream().wait_stream(s_cap)
-    graph1 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph1):
-        ll_one_step()
-    ms_oneg = timed(graph1.replay, steps)
-    assert plan.device_error() == 0
-    out["low_latency_one_launch_step_n128"] = dict(
-        row(ms_one, ll_bytes), us_per_step=ms_one * 1e3, us_per_step_cuda_graph=ms_oneg * 1e3,
-        GBs_cuda_graph=ll_bytes / (ms_oneg / 1e3) / 1e9,
-        workload="as low_latency_step_n128 with mp_dispatch_ll (LL offsets and rows in one "
-                 "launch) + weighted LL combine (2 launches)")
-    del plan, rx, yl, lo, graph, graph1
+    del plan, rx, yl, lo, graph, graph3
     torch.cuda.empty_cache()
 
     # the skewed workload: Zipf(1.2) routing, rank 0 hot

@@ -79,7 +79,7 @@ def lib() -> ctypes.CDLL:
         L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
         L.mp_dispatch_noalloc.argtypes = [i32] * 6 + [P] * 7 + [i64] + [P] * 12
         L.mp_allgatherv_multi.argtypes = [i32, i32, P, P, P, P, P]
-        L.mp_dispatch_ll.argtypes = [i32] * 7 + [P] * 4 + [i64] + [P] * 9
+        L.mp_dispatch_ll.argtypes = [i32] * 7 + [P] * 4 + [i64] + [P] * 8
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
                   "mp_dispatch_rows_e4m3", "mp_dispatch_rows_mxfp8", "mp_dispatch_offsets_global",
                   "mp_combine_weights",
@@ -351,7 +351,7 @@ def mp_dispatch_ll_rows(R, N, K, H, dtype, x, x_scales, slot_row, recv_capacity,
 
 def mp_dispatch_ll(R, N, K, E, H, dtype, rank_major, x, x_scales, topk_idx,
                    num_tokens_per_expert, recv_capacity, bin_offsets, bin_src_offsets,
-                   recv_src_token, slot_row, recv_x, recv_scales, dev_err, workspace,
+                   recv_src_token, slot_row, recv_x, recv_scales, dev_err,
                    stream=None) -> int:
     return lib().mp_dispatch_ll(
         R, N, K, E, H, dtype, int(rank_major), _dev(x, "x"), _dev(x_scales, "x_scales"),
@@ -359,7 +359,7 @@ def mp_dispatch_ll(R, N, K, E, H, dtype, rank_major, x, x_scales, topk_idx,
         int(recv_capacity), _dev(bin_offsets, "bin_offsets"),
         _dev(bin_src_offsets, "bin_src_offsets"), _dev(recv_src_token, "recv_src_token"),
         _dev(slot_row, "slot_row"), _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"),
-        _dev(dev_err, "dev_err"), _dev(workspace, "workspace"), _stream(stream))
+        _dev(dev_err, "dev_err"), _stream(stream))
 
 
 def mp_combine_ll(R, N, K, H, y, y_rows, slot_row, topk_weights, out, dev_err, stream=None) -> int:

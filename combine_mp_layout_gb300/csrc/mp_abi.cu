@@ -491,15 +491,15 @@ int mp_dispatch_ll(int R, int N, int K, int E, int H, int dtype, int rank_major,
                    const int32_t* num_tokens_per_expert, int64_t recv_capacity,
                    int32_t* bin_offsets, int32_t* bin_src_offsets, int32_t* recv_src_token,
                    int32_t* slot_row, void* recv_x, float* recv_scales, int32_t* dev_err,
-                   void* workspace, mp_stream_t stream) {
+                   mp_stream_t stream) {
   if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0 || (rank_major != 0 && rank_major != 1))
     return MP_ERR_INVALID_ARG;
-  if (!bin_offsets || !bin_src_offsets || !dev_err || !workspace) return MP_ERR_INVALID_ARG;
+  if (!bin_offsets || !bin_src_offsets || !dev_err) return MP_ERR_INVALID_ARG;
   if (N > 0 && (!topk_idx || !slot_row)) return MP_ERR_INVALID_ARG;
   if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
   if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(bin_offsets) ||
       !aligned4(bin_src_offsets) || !aligned4(recv_src_token) || !aligned4(slot_row) ||
-      !aligned4(dev_err) || !aligned16(workspace))
+      !aligned4(dev_err))
     return MP_ERR_INVALID_ARG;
   const int st = check_rows_args(1, N, H, dtype, x, x_scales, slot_row, recv_capacity, recv_x,
                                  recv_scales);
@@ -509,7 +509,7 @@ int mp_dispatch_ll(int R, int N, int K, int E, int H, int dtype, int rank_major,
       R, N, K, E, rank_major, fp8 ? int64_t(H) : int64_t(H) * 2, topk_idx, num_tokens_per_expert,
       recv_capacity, bin_offsets, bin_src_offsets, recv_src_token, slot_row, x,
       fp8 ? H / MP_SCALE_BLOCK : 0, x_scales, recv_x, recv_scales, dev_err,
-      static_cast<unsigned char*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int mp_combine_ll(int R, int N, int K, int H, const void* y, int64_t y_rows,

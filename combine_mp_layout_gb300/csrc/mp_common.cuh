@@ -29,11 +29,6 @@ struct Control {
   uint32_t layout_done[MP_MAX_RANKS];  // layout blocks finished, per source rank
   uint32_t bar_count;          // grid barrier of the fused layout + scan: arrivals
   uint32_t bar_gen;            // ... and its generation
-  uint32_t ll_ticket;          // one-launch LL dispatch: next block ticket
-  uint32_t ll_done;            // ... blocks finished
-  uint32_t ll_epoch;           // ... tags the ready flags of the current launch
-  uint32_t ll_reserved;
-  uint32_t ll_ready[MP_MAX_RANKS];  // ... source rank s's slot rows are written
 };
 static_assert(sizeof(Control) <= 512, "control block");
 

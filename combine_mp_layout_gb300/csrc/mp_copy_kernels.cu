@@ -1025,3 +1025,89 @@ cudaError_t launch_combine_weights(int R, int64_t tokens, int K, const float* re
 }
 
 }  // namespace mp
+
+namespace mp {
+
+// ---------------------------------------------------------------------------
+// Low-latency row copy as a programmatic dependent of the LL sort (the second
+// kernel of mp_dispatch_ll).  It is launched with programmatic stream
+// serialization, so its blocks may start while the sort still runs: each warp
+// loads its first slab of a token row (x is an input of the sort's caller,
+// complete before the sort started), then waits for the sort grid to finish
+// and its writes to be visible (griddepcontrol.wait), then reads the token's
+// slot rows and stores.  One 32-byte vector per lane and unit, one short
+// block per kWarpsPerBlock units (the small-dispatch shape).
+// ---------------------------------------------------------------------------
+template <int NW>
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_ll_rows_after_sort(int K, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ x,
+                        Words<NW>* __restrict__ recv_x, int64_t recv_capacity,
+                        const int32_t* slot_row, int spr, const float* __restrict__ x_scales,
+                        float* __restrict__ recv_scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t slabs = (vpr + kWarp - 1) / kWarp;
+  const int64_t units = tokens * slabs;
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  Words<NW> v;
+  if (unit < units) {  // the first unit's vector, before the wait
+    const int64_t tok = unit / slabs, i = (unit - tok * slabs) * kWarp + lane;
+    if (i < vpr) v = ld_stream_w<NW>(x + tok * vpr + i);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (bool first = true; unit < units; unit += nw, first = false) {
+    const int64_t tok = unit / slabs;
+    const int64_t slab = unit - tok * slabs;
+    const int64_t i = slab * kWarp + lane;
+    if (!first && i < vpr) v = ld_stream_w<NW>(x + tok * vpr + i);
+    // slot_row was written by the sort grid: read through L2, not the read-only path
+    const int my = lane < K ? __ldcg(slot_row + tok * K + lane) : -1;
+    unsigned vm = __ballot_sync(kFull, my >= 0 && int64_t(my) < recv_capacity);
+    while (vm) {
+      const int d = __ffs(vm) - 1;
+      vm &= vm - 1;
+      const int64_t row = __shfl_sync(kFull, my, d);
+      if (i < vpr) st_stream_w<NW>(recv_x + row * vpr + i, v);
+      if (spr > 0 && slab == 0)
+        for (int c = lane; c < spr; c += kWarp)
+          recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
+    }
+  }
+}
+
+template <int NW>
+static cudaError_t ll_rows_after_sort_nw(int K, int64_t tokens, int64_t row_bytes, const void* x,
+                                         void* recv_x, int64_t recv_capacity,
+                                         const int32_t* slot_row, int spr, const float* x_scales,
+                                         float* recv_scales, cudaStream_t stream) {
+  const int64_t vpr = row_bytes / (4 * NW);
+  const int64_t slabs = (vpr + kWarp - 1) / kWarp;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_full(kWarpsPerBlock, tokens * slabs));
+  cfg.blockDim = dim3(kCopyThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mp_k_ll_rows_after_sort<NW>, K, tokens, vpr,
+                            static_cast<const Words<NW>*>(x), static_cast<Words<NW>*>(recv_x),
+                            recv_capacity, slot_row, spr, x_scales, recv_scales);
+}
+
+cudaError_t launch_ll_rows_after_sort(int K, int64_t tokens, int64_t row_bytes, const void* x,
+                                      void* recv_x, int64_t recv_capacity,
+                                      const int32_t* slot_row, int scales_per_row,
+                                      const float* x_scales, float* recv_scales,
+                                      cudaStream_t stream) {
+  if (tokens == 0) return cudaSuccess;
+  if (row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32))
+    return ll_rows_after_sort_nw<8>(K, tokens, row_bytes, x, recv_x, recv_capacity, slot_row,
+                                    scales_per_row, x_scales, recv_scales, stream);
+  return ll_rows_after_sort_nw<4>(K, tokens, row_bytes, x, recv_x, recv_capacity, slot_row,
+                                  scales_per_row, x_scales, recv_scales, stream);
+}
+
+}  // namespace mp

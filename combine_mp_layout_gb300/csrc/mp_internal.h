@@ -46,16 +46,23 @@ cudaError_t launch_ll_offsets(int R, int N, int K, int E, int rank_major,
                               int32_t* slot_row, int32_t* dev_err, cudaStream_t stream);
 
 // launch_ll_offsets followed by the row copy of each (token, top-k slot) to
-// its slot row, in one launch (mp_k_ll_dispatch) when the sort's counters fit
-// 48 KB of shared memory, else as the two launches.  ws: the control block of
-// the workspace (ticket, epoch and per-rank ready flags).
+// its slot row, launched as the sort's programmatic dependent.
 cudaError_t launch_ll_dispatch(int R, int N, int K, int E, int rank_major, int64_t row_bytes,
                                const int32_t* topk_idx, const int32_t* num_tokens_per_expert,
                                int64_t recv_capacity, int32_t* bin_offsets,
                                int32_t* bin_src_offsets, int32_t* recv_src_token,
                                int32_t* slot_row, const void* x, int scales_per_row,
                                const float* x_scales, void* recv_x, float* recv_scales,
-                               int32_t* dev_err, unsigned char* ws, cudaStream_t stream);
+                               int32_t* dev_err, cudaStream_t stream);
+
+// The low-latency row copy launched as a programmatic dependent of the kernel
+// before it on the stream (the LL sort): its row loads overlap that kernel,
+// its slot_row reads wait for it.  Only for use right after the sort.
+cudaError_t launch_ll_rows_after_sort(int K, int64_t tokens, int64_t row_bytes, const void* x,
+                                      void* recv_x, int64_t recv_capacity,
+                                      const int32_t* slot_row, int scales_per_row,
+                                      const float* x_scales, float* recv_scales,
+                                      cudaStream_t stream);
 
 // out[t] = bf16( sum over k ascending of weights[t][k] * y[slot_row[t][k]] )
 cudaError_t launch_combine_weighted(int K, int64_t tokens, int H, const void* y, int64_t y_rows,

@@ -507,27 +507,22 @@ int mp_dispatch_ll_offsets_rank_major(int R, int N, int K, int E, const int32_t 
 /*
  * mp_dispatch_ll -- the low-latency dispatch in one call: the results of
  * mp_dispatch_ll_offsets (rank_major = 0) or mp_dispatch_ll_offsets_rank_major
- * (rank_major = 1) followed by mp_dispatch_ll_rows, bit for bit, from one
- * kernel launch ("MSCCLPP EP implementation", the low-latency dispatch, whose
- * one kernel both places and sends the tokens).  Blocks of the launch sort
- * each source rank's entries while the others load token rows; a row is
- * stored once its rank's slot rows are published (a bounded wait:
- * MP_ERR_TIMEOUT in dev_err if it gives up, the row then not copied).  When
- * the sort's counters do not fit one block's shared memory (E above ~3000
- * for the expert-major form) the call runs the two launches instead.
+ * (rank_major = 1) followed by mp_dispatch_ll_rows, bit for bit ("MSCCLPP EP
+ * implementation", the low-latency dispatch, one call that both places and
+ * sends the tokens).  The row copy is launched as a programmatic dependent of
+ * the sort, so its row loads overlap the sort; x must therefore be complete
+ * when the call is enqueued (as for every call, by stream order).
  *   bin_offsets / bin_src_offsets: expert_offsets / expert_src_offsets, or
  *   dest_offsets / dest_src_offsets for rank_major = 1; every other argument
  *   as in those calls (dtype MP_BF16 or MP_E4M3 with its scales).
- *   workspace  mp_workspace_size(R, N, E) bytes, zeroed once before first
- *              use, 16-byte aligned; no other call may use it meanwhile.
- *   Device errors: as mp_dispatch_ll_offsets, plus MP_ERR_TIMEOUT.
+ *   Device errors: as mp_dispatch_ll_offsets.
  */
 int mp_dispatch_ll(int R, int N, int K, int E, int H, int dtype, int rank_major, const void *x,
                    const float *x_scales, const int32_t *topk_idx,
                    const int32_t *num_tokens_per_expert, int64_t recv_capacity,
                    int32_t *bin_offsets, int32_t *bin_src_offsets, int32_t *recv_src_token,
                    int32_t *slot_row, void *recv_x, float *recv_scales, int32_t *dev_err,
-                   void *workspace, mp_stream_t stream);
+                   mp_stream_t stream);
 int mp_dispatch_ll_rows(int R, int N, int K, int H, int dtype, const void *x,
                         const float *x_scales, const int32_t *slot_row, int64_t recv_capacity,
                         void *recv_x, float *recv_scales, mp_stream_t stream);

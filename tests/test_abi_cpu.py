@@ -205,8 +205,8 @@ def test_newer_entry_points_reject(L):
     assert L.mp_layout_and_offsets(2, 8, 2, 8, P, P, 16, *([P] * 12), N0, N0) == \
         B.MP_ERR_INVALID_ARG  # workspace
     L.mp_dispatch_ll.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + [ctypes.c_int64] + \
-        [ctypes.c_void_p] * 9
-    ok = (2, 8, 2, 8, 64, B.MP_BF16, 0, P, N0, P, N0, 16, P, P, P, P, P, N0, P, P, N0)
+        [ctypes.c_void_p] * 8
+    ok = (2, 8, 2, 8, 64, B.MP_BF16, 0, P, N0, P, N0, 16, P, P, P, P, P, N0, P, N0)
 
     def ll(**kw):
         a = list(ok)
@@ -214,8 +214,8 @@ def test_newer_entry_points_reject(L):
             a[int(i[1:])] = v
         return L.mp_dispatch_ll(*a)
     assert ll(a6=2) == B.MP_ERR_INVALID_ARG                                             # rank_major
-    assert ll(a19=N0) == B.MP_ERR_INVALID_ARG                                           # workspace
-    assert ll(a19=_p(FAKE + 8)) == B.MP_ERR_INVALID_ARG                                 # ws alignment
+    assert ll(a15=_p(FAKE + 2)) == B.MP_ERR_INVALID_ARG                                 # slot_row align
+    assert ll(a16=_p(FAKE + 8)) == B.MP_ERR_INVALID_ARG                                 # recv_x align
     assert ll(a4=60) == B.MP_ERR_INVALID_ARG                                            # H % 8
     assert ll(a3=7) == B.MP_ERR_INVALID_ARG                                             # E % R
     assert ll(a5=B.MP_E4M3, a4=128) == B.MP_ERR_INVALID_ARG                             # no scales

@@ -181,9 +181,9 @@ def test_low_latency_path_writes_only_its_buffers(rank_major):
 
 
 @pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
-def test_one_launch_low_latency_dispatch_writes_only_its_buffers(rank_major):
-    """mp_dispatch_ll (sort and copy in one launch) with a too-small capacity; the
-    workspace is guarded too (only its control block and counters are written)."""
+def test_one_call_low_latency_dispatch_writes_only_its_buffers(rank_major):
+    """mp_dispatch_ll (the sort, then the row copy as its programmatic dependent) with a
+    too-small capacity."""
     R, N, E, K, H = 4, 77, 16, 3, 72
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=10)
     inp.topk_idx[:, ::5, 1] = -1
@@ -198,14 +198,13 @@ def test_one_launch_low_latency_dispatch_writes_only_its_buffers(rank_major):
     slot = Guarded((R, N, K), torch.int32)
     rx = Guarded((cap, H), torch.bfloat16)
     err = Guarded((1,), torch.int32, 0)
-    ws = Guarded((B.mp_workspace_size(R, N, E),), torch.uint8, 0)
     for _ in range(2):
         B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, rank_major, x, None, topk, None, cap,
-                                 off.t, soff.t, src.t, slot.t, rx.t, None, err.t, ws.t))
+                                 off.t, soff.t, src.t, slot.t, rx.t, None, err.t))
     torch.cuda.synchronize()
     assert int(err.t.item()) == B.MP_ERR_CAPACITY
     for name, gb in (("offsets", off), ("source offsets", soff), ("source tokens", src),
-                     ("slots", slot), ("rows", rx), ("error word", err), ("workspace", ws)):
+                     ("slots", slot), ("rows", rx), ("error word", err)):
         assert gb.intact(), "guard bytes overwritten next to the " + name
 
 

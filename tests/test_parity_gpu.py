@@ -770,7 +770,7 @@ def test_low_latency_rows_e4m3_with_scales():
     assert np.array_equal(rs[:n].cpu().numpy().view(np.uint8), ll["recv_x"][:, H:])
 
 
-LL_ONE_LAUNCH = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
+LL_ONE_CALL = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=7168),
                  dict(R=5, N=77, E=20, K=6, H=264), dict(R=3, N=300, E=9, K=9, H=64),
                  dict(R=4, N=40, E=16, K=4, H=20480), dict(R=32, N=40, E=64, K=4, H=64),
                  dict(R=8, N=64, E=8192, K=8, H=64), dict(R=4, N=3000, E=64, K=6, H=64),
@@ -778,15 +778,14 @@ LL_ONE_LAUNCH = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, 
                  dict(R=4, N=0, E=16, K=4, H=64), dict(R=2, N=50, E=64, K=32, H=64)]
 
 
-@pytest.mark.parametrize("cfg", LL_ONE_LAUNCH, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
+@pytest.mark.parametrize("cfg", LL_ONE_CALL, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
                          + ("_cap" if "cap_frac" in c else ""))
 @pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
 @pytest.mark.parametrize("counts", ["layout", "self"])
-def test_low_latency_one_launch_dispatch_matches_oracle(cfg, rank_major, counts):
-    """mp_dispatch_ll (sort and row copy in one launch; the two launches when E is too
-    large for one block's counters) against the oracle's LL layout and rows, three calls
-    on one workspace (each launch must start from the ticket and epoch the last left).
-    H=264 takes 16-byte vectors, H=20480 rows longer than the part loaded before the wait."""
+def test_low_latency_one_call_dispatch_matches_oracle(cfg, rank_major, counts):
+    """mp_dispatch_ll (the sort, then the row copy as its programmatic dependent, which
+    loads rows before waiting for the sort) against the oracle's LL layout and rows, three
+    calls in a row.  H=264 takes 16-byte vectors, H=20480 rows of several slabs."""
     cfg = dict(cfg)
     cap_frac = cfg.pop("cap_frac", None)
     R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
@@ -813,8 +812,7 @@ def test_low_latency_one_launch_dispatch_matches_oracle(cfg, rank_major, counts)
         plan.dev_err.zero_()
         ntpe = plan.num_tokens_per_expert if counts == "layout" else None
         B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, rank_major, plan.x, None, plan.topk_idx,
-                                 ntpe, cap, boff, bsoff, src, slot, rx, None, plan.dev_err,
-                                 plan.workspace))
+                                 ntpe, cap, boff, bsoff, src, slot, rx, None, plan.dev_err))
         torch.cuda.synchronize()
         assert plan.device_error() == st, rep
         assert np.array_equal(boff.cpu().numpy(), want[keys[0]]), rep
@@ -825,9 +823,9 @@ def test_low_latency_one_launch_dispatch_matches_oracle(cfg, rank_major, counts)
     assert (st == 0) == (cap_frac is None)
 
 
-def test_low_latency_one_launch_dispatch_replays_as_a_cuda_graph():
-    """mp_dispatch_ll + mp_combine_ll captured once and replayed: the ticket and epoch
-    live in the workspace, so every replay starts where the last one left them."""
+def test_low_latency_one_call_dispatch_replays_as_a_cuda_graph():
+    """mp_dispatch_ll + mp_combine_ll captured once and replayed (the programmatic
+    dependency between the sort and the row copy is captured with them)."""
     R, N, E, K, H = 4, 96, 32, 4, 136
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=33)
     plan = EPPlan(R, N, K, E, H)
@@ -843,8 +841,7 @@ def test_low_latency_one_launch_dispatch_replays_as_a_cuda_graph():
 
     def step():
         B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None, plan.topk_idx, None,
-                                 cap, eoff, esoff, src, slot, rx, None, plan.dev_err,
-                                 plan.workspace))
+                                 cap, eoff, esoff, src, slot, rx, None, plan.dev_err))
         B.check(B.mp_combine_ll(R, N, K, H, rx, cap, slot, plan.topk_weights, out,
                                 plan.dev_err))
 
@@ -873,7 +870,7 @@ def test_low_latency_one_launch_dispatch_replays_as_a_cuda_graph():
         assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll after replay")
 
 
-def test_low_latency_one_launch_dispatch_e4m3_with_scales():
+def test_low_latency_one_call_dispatch_e4m3_with_scales():
     R, N, E, K, H = 4, 200, 32, 4, 384
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="e4m3"), seed=32)
     plan = EPPlan(R, N, K, E, H, "e4m3")
@@ -887,8 +884,7 @@ def test_low_latency_one_launch_dispatch_e4m3_with_scales():
     rx = torch.zeros((cap, H), dtype=torch.uint8, device=dev)
     rs = torch.zeros((cap, H // 128), dtype=torch.float32, device=dev)
     B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_E4M3, 0, plan.x, plan.x_scales, plan.topk_idx,
-                             None, cap, eoff, esoff, src, slot, rx, rs, plan.dev_err,
-                             plan.workspace))
+                             None, cap, eoff, esoff, src, slot, rx, rs, plan.dev_err))
     torch.cuda.synchronize()
     assert plan.device_error() == 0
     payload = np.concatenate([wl.u8_bits(inp.x), inp.x_scales.numpy().view(np.uint8)], axis=-1)
