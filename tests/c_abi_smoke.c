@@ -8,7 +8,10 @@
  *   - a token's send_row has one entry >= 0 per distinct rank owning one of
  *     its experts (expert e lives on rank e / (E/R));
  *   - combining the un-modified dispatch gives c * x, c = that rank count
- *     (exact here: x holds small integers, so every fp32 sum is exact).
+ *     (exact here: x holds small integers, so every fp32 sum is exact);
+ *   - the low-latency dispatch in one call gives every routed (token, slot) a row,
+ *     and its weighted combine with unit weights gives K' * x, K' = the token's
+ *     routed slots.
  * Prints "c abi smoke ok" and returns 0 on success.
  */
 #include <stdint.h>
@@ -152,6 +155,46 @@ int main(void) {
     for (int h = 0; h < H; ++h) {
       const float want = (float)owners * f32_of_bf16(x[tok * H + h]);
       if (f32_of_bf16(out[tok * H + h]) != want) return fail("combine != c * x");
+    }
+  }
+  /* the low-latency path in one call: one row per valid (token, slot), then the
+   * weighted combine with unit weights, which gives K * x for a routed token */
+  {
+    const int64_t lcap = (int64_t)R * N * K;
+    static int32_t slot[R * N * K];
+    static float ones[R * N * K];
+    for (int i = 0; i < R * N * K; ++i) ones[i] = 1.0f;
+    void *d_boff, *d_bsoff, *d_src, *d_slot, *d_lrx, *d_ones, *d_lout;
+    CUDA(cudaMalloc(&d_boff, sizeof(int32_t) * (E + 1)));
+    CUDA(cudaMalloc(&d_bsoff, sizeof(int32_t) * E * R));
+    CUDA(cudaMalloc(&d_src, sizeof(int32_t) * (size_t)lcap));
+    CUDA(cudaMalloc(&d_slot, sizeof slot));
+    CUDA(cudaMalloc(&d_lrx, sizeof(uint16_t) * (size_t)lcap * H));
+    CUDA(cudaMalloc(&d_ones, sizeof ones));
+    CUDA(cudaMalloc(&d_lout, sizeof out));
+    CUDA(cudaMemcpy(d_ones, ones, sizeof ones, cudaMemcpyHostToDevice));
+    MP(mp_dispatch_ll(R, N, K, E, H, MP_BF16, 0, d_x, NULL, d_topk, NULL, lcap, d_boff, d_bsoff,
+                      d_src, d_slot, d_lrx, NULL, d_err, NULL));
+    MP(mp_combine_ll(R, N, K, H, d_lrx, lcap, d_slot, d_ones, d_lout, d_err, NULL));
+    CUDA(cudaDeviceSynchronize());
+    CUDA(cudaMemcpy(&err, d_err, sizeof err, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(slot, d_slot, sizeof slot, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(out, d_lout, sizeof out, cudaMemcpyDeviceToHost));
+    if (err != 0) {
+      fprintf(stderr, "device error (low-latency): %s\n", mp_status_string(err));
+      return 1;
+    }
+    for (int tok = 0; tok < R * N; ++tok) {
+      int valid = 0;
+      for (int k = 0; k < K; ++k) {
+        const int routed = topk[tok * K + k] >= 0;
+        if (routed != (slot[tok * K + k] >= 0)) return fail("slot_row vs routed slot");
+        valid += routed;
+      }
+      for (int h = 0; h < H; ++h) {
+        const float want = (float)valid * f32_of_bf16(x[tok * H + h]);
+        if (f32_of_bf16(out[tok * H + h]) != want) return fail("low-latency combine != c * x");
+      }
     }
   }
   printf("c abi smoke ok: %d receive rows\n", dest_offsets[R]);
