@@ -384,6 +384,28 @@ def pin_sum_order_fixture(orc) -> None:
     assert st == 0 and np.array_equal(out[0], want)
 
 
+def pin_low_latency_combine_closed_forms(orc) -> None:
+    """The weighted low-latency combine.  With unit weights every product is exact, so it
+    is the plain sum of the hand-worked sum-order fixture, slots taken in ascending k (a
+    masked slot contributes nothing).  Each product is rounded to binary32 before it is
+    added: w*y with w = 1 + 2^-20 and y = 1 + 2^-7 is 1 + 2^-7 + 2^-20 + 2^-27, which
+    rounds to 1 + 2^-7 + 2^-20, so adding the product of -w and y cancels it to +0,
+    where a fused multiply-add would leave -2^-27."""
+    g = load("sum_order_r3.json")
+    rows = _bits(g["rows_in_rank_order"])          # [3][8]
+    want = np.array([int(h, 16) for h in g["expect_bf16_bits"]], np.uint16)
+    out, st = orc.combine_ll(rows, np.array([[[0, 1, 2]]], np.int32),
+                             np.ones((1, 1, 3), np.float32))
+    assert st == 0 and np.array_equal(out[0, 0], want), out[0, 0]
+    out, st = orc.combine_ll(rows, np.array([[[0, -1, 1, 2]]], np.int32),
+                             np.ones((1, 1, 4), np.float32))
+    assert st == 0 and np.array_equal(out[0, 0], want), out[0, 0]
+    y = _bits(np.full((2, 8), 1.0 + 2.0**-7, np.float32))
+    w = np.array([[[1.0 + 2.0**-20, -(1.0 + 2.0**-20)]]], np.float32)
+    out, st = orc.combine_ll(y, np.array([[[0, 1]]], np.int32), w)
+    assert st == 0 and not out.any(), [hex(int(b)) for b in out[0, 0]]
+
+
 def pin_combine_closed_forms(orc) -> None:
     rng = np.random.default_rng(21)
     inp = wl.make_ep("dsv3", seed=2, N=48, H=64)
@@ -666,7 +688,7 @@ def pin_mxfp4_quantisation(orc) -> None:
     assert np.all(np.signbit(deq) == np.signbit(xf))
 
 
-ALL_PINS = [pin_nonfinite_sums, pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
+ALL_PINS = [pin_nonfinite_sums, pin_low_latency_combine_closed_forms, pin_bf16_rounding, pin_ep_hand_fixture, pin_ep_brute_force, pin_ep_invariants,
             pin_ep_special_cases, pin_sum_order_fixture, pin_combine_closed_forms, pin_rsv_agv,
             pin_e4m3_conversions, pin_block_quantisation, pin_global_ids_and_combined_weights,
             pin_low_latency_layout, pin_mxfp8_quantisation, pin_mxfp4_quantisation,

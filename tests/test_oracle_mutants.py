@@ -82,6 +82,10 @@ MUTANTS = {
                                            "dest_src_offsets[d * R + s] = (int32_t)(row);"),
     "agv_shard_shift": ("memcpy(out + ((int64_t)q * S + i) * row_bytes, in + i * row_bytes",
                         "memcpy(out + ((int64_t)q * S + i) * row_bytes, in + (i - off) * row_bytes"),
+    "ll_combine_descending": ("    for (int k = 0; k < K; ++k) {\n      const int32_t r = slot_row[tok * K + k];",
+                              "    for (int k = K - 1; k >= 0; --k) {\n      const int32_t r = slot_row[tok * K + k];"),
+    "ll_combine_fused_multiply_add": ("        acc[h] = acc[h] + p;",
+                                      "        acc[h] = fmaf(w, oracle_bf16_to_f32(y[(int64_t)r * H + h]), acc[h]);"),
     "rsv_negative_zero_start": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
                                 "        float acc = -0.0f;\n        for (int q = 0; q < R; ++q)"),
     "bf16_nan_quiet_bit_dropped": ("return (uint16_t)((u >> 16) | 0x0040u);",

@@ -246,6 +246,34 @@ def test_nonfinite_sums_match_oracle():
     assert_bits_or_both_nan(wl.bf16_bits(out), want_ll, "weighted LL combine, sprinkled")
 
 
+def test_weighted_combine_closed_forms_on_gpu():
+    """The weighted LL combine on the closed forms its oracle is pinned to: the
+    sum-order fixture with unit weights (slots in ascending k, a masked slot skipped),
+    and a product rounded before it is added (w = 1 + 2^-20, y = 1 + 2^-7, then -w:
+    +0, not the -2^-27 a fused multiply-add would leave)."""
+    g = pins.load("sum_order_r3.json")
+    rows = pins._bits(g["rows_in_rank_order"])
+    want = [int(h, 16) for h in g["expect_bf16_bits"]]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for slots in ([0, 1, 2], [0, -1, 1, 2]):
+        k = len(slots)
+        out = torch.full((1, 1, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+        B.check(B.mp_combine_ll(1, 1, k, 8, _tb(rows), 3,
+                                torch.tensor([[slots]], dtype=torch.int32, device="cuda"),
+                                torch.ones((1, 1, k), dtype=torch.float32, device="cuda"), out, err))
+        torch.cuda.synchronize()
+        assert wl.bf16_bits(out[0, 0]).tolist() == want, slots
+    y = pins._bits(np.full((2, 8), 1.0 + 2.0**-7, np.float32))
+    w = torch.tensor([[[1.0 + 2.0**-20, -(1.0 + 2.0**-20)]]], dtype=torch.float32, device="cuda")
+    out = torch.full((1, 1, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    B.check(B.mp_combine_ll(1, 1, 2, 8, _tb(y), 2,
+                            torch.tensor([[[0, 1]]], dtype=torch.int32, device="cuda"), w, out,
+                            err))
+    torch.cuda.synchronize()
+    assert not wl.bf16_bits(out).any(), wl.bf16_bits(out)
+    assert int(err.item()) == 0
+
+
 FUZZ = [  # R, N, E, K, H  (N not a multiple of 256, H not a multiple of a slab)
     (1, 100, 4, 2, 64),
     (2, 257, 8, 2, 136),
