@@ -214,6 +214,11 @@ def pin_ep_invariants(orc) -> None:
         trip = list(zip(dest.tolist(), *zip(*keys))) if T else []
         assert trip == sorted(trip) and len(set(trip)) == T
         assert np.array_equal(out["recv_x"], x[out["recv_src_rank"], out["recv_src_idx"]])
+        # scales travel with their row: every token's scales distinct
+        xs = np.arange(R * N * 3, dtype=np.float32).reshape(R, N, 3) + 0.5
+        outs, st = orc.dispatch(x, idx, inp.topk_weights, mask, E, x_scales=xs)
+        assert st == 0 and np.array_equal(outs["recv_scales"][:T],
+                                          xs[out["recv_src_rank"], out["recv_src_idx"]])
         El = E // R
         assert out["num_recv_tokens_per_expert"].sum() == int(ntpe.sum())
         assert np.array_equal(out["num_recv_tokens_per_expert"].reshape(-1), ntpe.sum(axis=0))
@@ -364,6 +369,22 @@ def pin_ep_special_cases(orc) -> None:
     out, st = orc.dispatch(x, idx, np.ones(idx.shape, np.float32), mask, 2, recv_capacity=4)
     assert st & 4 and out["num_recv"] == 6
     assert int((out["send_row"] >= 0).sum()) == 4 and out["send_row"].max() == 3
+    # ... the capacity only truncates: the offset tables still describe every row (the
+    # exact need is dest_offsets[R]), rows below it are those of an unlimited run
+    full, st = orc.dispatch(x, idx, np.ones(idx.shape, np.float32), mask, 2)
+    assert st == 0 and full["dest_offsets"].tolist() == [0, 3, 6]
+    assert np.array_equal(out["dest_offsets"], full["dest_offsets"])
+    assert np.array_equal(out["rank_prefix"], full["rank_prefix"])
+    assert np.array_equal(out["send_row"], np.where(full["send_row"] < 4, full["send_row"], -1))
+    assert np.array_equal(out["recv_x"][:4], full["recv_x"][:4])
+    # combine: a send_row entry past the rows given is flagged and skipped
+    y = _bits(np.arange(1, 7, dtype=np.float32)[:, None].repeat(8, axis=1))
+    comb, st = orc.combine(y[:4], full["send_row"])
+    assert st & 4
+    got = _f32(comb)[..., 0]
+    for s_, t_ in itertools.product(range(2), range(3)):
+        r = [v for v in full["send_row"][s_, t_] if 0 <= v < 4]
+        assert got[s_, t_] == sum(float(r_ + 1) for r_ in r)
 
 
 # --------------------------------------------------------------------------

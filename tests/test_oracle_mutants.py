@@ -86,6 +86,12 @@ MUTANTS = {
                               "    for (int k = K - 1; k >= 0; --k) {\n      const int32_t r = slot_row[tok * K + k];"),
     "ll_combine_fused_multiply_add": ("        acc[h] = acc[h] + p;",
                                       "        acc[h] = fmaf(w, oracle_bf16_to_f32(y[(int64_t)r * H + h]), acc[h]);"),
+    "capacity_row_not_advanced": ("if (row >= recv_capacity) { status |= ORC_CAPACITY; row += 1; continue; }",
+                                  "if (row >= recv_capacity) { status |= ORC_CAPACITY; continue; }"),
+    "scales_from_first_token": ("          recv_scales[row * scales_per_row + c] = x_scales[tok * scales_per_row + c];",
+                                "          recv_scales[row * scales_per_row + c] = x_scales[c];"),
+    "combine_capacity_not_flagged": ("        if ((int64_t)r >= y_rows) { status |= ORC_CAPACITY; continue; }\n        const uint16_t *src = y",
+                                     "        if ((int64_t)r >= y_rows) { continue; }\n        const uint16_t *src = y"),
     "rsv_negative_zero_start": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
                                 "        float acc = -0.0f;\n        for (int q = 0; q < R; ++q)"),
     "bf16_nan_quiet_bit_dropped": ("return (uint16_t)((u >> 16) | 0x0040u);",
