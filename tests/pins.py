@@ -250,6 +250,23 @@ def pin_global_ids_and_combined_weights(orc) -> None:
     valid = (idx >= 0) & (idx < E)
     assert np.array_equal(cw.view(np.uint32),
                           np.where(valid, inp.topk_weights, np.float32(0)).view(np.uint32))
+    # order and rounding of the sum over destinations, binary32 from +0 in ascending d:
+    # the sum-order fixture's columns as the weights three destinations hold for one
+    # token (slot k = column); exact binary32 results, derived by hand:
+    #   (2^24 + 1) rounds to 2^24 (tie to even), minus 2^24: 0  -- both orders of col 0/1
+    #   -2^24 + 2^24 + 1 = 1;  1+1+1 = 3;  0.5+0.25+0.125 = 0.875;  (+0)+(-0)+(-0) = +0;
+    #   1 + 2^-8 + 0 = 1.00390625;  1 + 2^-8 + 2^-16 (exact in binary32)
+    g = load("sum_order_r3.json")
+    w3 = np.array(g["rows_in_rank_order"], np.float32)            # [d][k]
+    send3 = np.full((3, 1, 3), -1, np.int32)
+    send3[0, 0] = [0, 1, 2]
+    cw, st = orc.combine_weights(w3, send3)
+    want = np.array([0.0, 0.0, 1.0, 3.0, 0.875, 0.0, 1.00390625, 1.0 + 2.0**-8 + 2.0**-16],
+                    np.float32)
+    assert st == 0 and np.array_equal(cw[0, 0].view(np.uint32), want.view(np.uint32)), cw[0, 0]
+    # a row past the rows given is flagged and skipped
+    cw, st = orc.combine_weights(w3[:2], send3)
+    assert st & 4 and cw[0, 0, 3] == 2.0
 
 
 def pin_low_latency_layout(orc) -> None:
@@ -287,7 +304,18 @@ def pin_low_latency_layout(orc) -> None:
                     if r >= 0:
                         exact[s, t] += float(wts[s, t, k]) * y[r]
         assert st == 0 and np.array_equal(_f32(comb), exact.astype(np.float32))
-
+    # receive capacity: rows are numbered as without it (the offsets count every row),
+    # rows at or past it are not written, their slot_row is -1, and the call flags it
+    idx = wl.topk_uniform(rng, 3 * 10, 6, 2).reshape(3, 10, 2)
+    x = rng.integers(0, 60000, (3, 10, 8)).astype(np.uint16)
+    full, st = orc.dispatch_ll(x, idx, 6)
+    assert st == 0 and full["num_recv"] == 60
+    cut, st = orc.dispatch_ll(x, idx, 6, recv_capacity=25)
+    assert st & 4
+    assert np.array_equal(cut["expert_offsets"], full["expert_offsets"])
+    assert np.array_equal(cut["expert_src_offsets"], full["expert_src_offsets"])
+    assert np.array_equal(cut["slot_row"], np.where(full["slot_row"] < 25, full["slot_row"], -1))
+    assert np.array_equal(cut["recv_x"][:25], full["recv_x"][:25])
 
 
 def pin_low_latency_rank_major(orc) -> None:

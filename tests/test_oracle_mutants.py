@@ -92,6 +92,14 @@ MUTANTS = {
                                 "          recv_scales[row * scales_per_row + c] = x_scales[c];"),
     "combine_capacity_not_flagged": ("        if ((int64_t)r >= y_rows) { status |= ORC_CAPACITY; continue; }\n        const uint16_t *src = y",
                                      "        if ((int64_t)r >= y_rows) { continue; }\n        const uint16_t *src = y"),
+    "combined_weights_capacity_not_flagged": ("        if ((int64_t)r >= recv_rows) { status |= ORC_CAPACITY; continue; }\n        acc = acc + recv_topk_weights",
+                                              "        if ((int64_t)r >= recv_rows) { continue; }\n        acc = acc + recv_topk_weights"),
+    "combined_weights_descending": ("      for (int d = 0; d < R; ++d) {\n        const int32_t r = send_row[tok * R + d];\n        if (r < 0) continue;\n        if ((int64_t)r >= recv_rows)",
+                                    "      for (int d = R - 1; d >= 0; --d) {\n        const int32_t r = send_row[tok * R + d];\n        if (r < 0) continue;\n        if ((int64_t)r >= recv_rows)"),
+    "ll_capacity_not_flagged": ("          } else {\n            status |= ORC_CAPACITY;\n          }\n          row += 1;\n        }\n      }\n    }\n  }\n  expert_offsets[E]",
+                                "          } else {\n          }\n          row += 1;\n        }\n      }\n    }\n  }\n  expert_offsets[E]"),
+    "ll_capacity_row_not_advanced": ("          } else {\n            status |= ORC_CAPACITY;\n          }\n          row += 1;\n        }\n      }\n    }\n  }\n  expert_offsets[E]",
+                                     "          } else {\n            status |= ORC_CAPACITY; row -= 1;\n          }\n          row += 1;\n        }\n      }\n    }\n  }\n  expert_offsets[E]"),
     "rsv_negative_zero_start": ("        float acc = 0.0f;\n        for (int q = 0; q < R; ++q)",
                                 "        float acc = -0.0f;\n        for (int q = 0; q < R; ++q)"),
     "bf16_nan_quiet_bit_dropped": ("return (uint16_t)((u >> 16) | 0x0040u);",
