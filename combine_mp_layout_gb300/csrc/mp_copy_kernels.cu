@@ -1,8 +1,9 @@
 // mp_copy_kernels.cu -- the HBM-bound payload kernels: dispatch row copy
 // (SM vectors, or the bulk-copy engine), quantising row copies (dispatch or
 // gather destinations), combine (gather + fp32 sum, plain or top-k
-// weighted), combined top-k weights, reduce-scatterv (fp32 sum of R inputs)
-// and all-gatherv (one read, R writes; one tensor or a list).
+// weighted), combined top-k weights, reduce-scatterv (fp32 sum of R inputs),
+// all-gatherv (one read, R writes; one tensor or a list), and the
+// low-latency row copy launched as a programmatic dependent of the LL sort.
 //
 // All are streaming kernels: nothing is reused, so they are bound by
 // HBM bandwidth and the design goal is bytes in flight with few
