@@ -93,7 +93,8 @@ const char *mp_status_string(int status);
 size_t mp_workspace_size(int R, int N, int E);
 
 /*
- * mp_layout -- [EP] get_dispatch_layout ("counts + token-in-rank").
+ * mp_layout -- [EP] get_dispatch_layout: the per-rank and per-expert
+ * counts and the token-in-rank masks.
  *   in   topk_idx              int32 [R][N][K]; -1 marks a masked entry
  *   out  num_tokens_per_rank   int32 [R][R]  [s][d] = #tokens of s sent to d
  *   out  num_tokens_per_expert int32 [R][E]  [s][e] = #(t,k) of s with expert e

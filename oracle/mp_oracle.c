@@ -79,7 +79,8 @@ uint16_t oracle_f32_to_bf16(float f) {
 }
 
 /* ------------------------------------------------------------------ */
-/* Layout [EP, get_dispatch_layout: "counts + token-in-rank"].          */
+/* Layout [EP, get_dispatch_layout: the counts and the token-in-rank   */
+/* masks].                                                            */
 /*   num_tokens_per_expert[s][e] = #(t,k) with topk_idx[s][t][k] == e   */
 /*   is_token_in_rank[s][t]      = bit d set iff some k has its expert  */
 /*                                 on rank d                            */
