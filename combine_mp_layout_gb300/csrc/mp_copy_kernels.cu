@@ -505,8 +505,8 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
 }
 
 // ---------------------------------------------------------------------------
-// Combine (same page: intranode_combine runs in the reverse direction of
-// dispatch).  out[s][t] = bf16_rn( sum_{d ascending} float(y[send_row[s][t][d]]) )
+// Combine (same page: intranode_combine takes the dispatched rows back to
+// their tokens).  out[s][t] = bf16_rn( sum_{d ascending} float(y[send_row[s][t][d]]) )
 // from +0.0f.  Up to RB source rows are loaded at once (memory-level
 // parallelism) and then added strictly in ascending d.
 // ---------------------------------------------------------------------------

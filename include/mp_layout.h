@@ -35,8 +35,8 @@
  *  [EP]  "MSCCLPP EP implementation", microsoft/mscclpp pull request #852:
  *        port scope (get_dispatch_layout, intranode_dispatch,
  *        intranode_combine), the intranode multirank validation note, the
- *        internode combine note (combine runs in the reverse direction of
- *        dispatch), the bench byte-accounting notes (one receive row per
+ *        internode combine note (combine takes the dispatched rows back to
+ *        their tokens), the bench byte-accounting notes (one receive row per
  *        (token, source rank) pair; combine moves as many bytes as
  *        dispatch) and the FP8 E4M3 payload with FP32 scales.
  *  [AGV] "Add pynccl all-gatherv and reducescatterv", vllm-project/vllm pull

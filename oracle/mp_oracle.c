@@ -15,7 +15,7 @@
  *        token-in-rank; intranode_dispatch / intranode_combine), the
  *        commit note on the bench byte accounting (the receive buffer holds
  *        one row per (token, source rank) pair) and the commit note that
- *        combine runs in the reverse direction of dispatch.
+ *        combine takes the dispatched rows back to their source tokens.
  *  [AGV] "Add pynccl all-gatherv and reducescatterv" (vllm-project/vllm pull
  *        request #20154): the all_gather / reduce_scatter code under review
  *        (per-root split along dim 0, offsets are running sums of sizes).
