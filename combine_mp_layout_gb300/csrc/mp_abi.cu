@@ -87,26 +87,27 @@ int mp_layout(int R, int N, int K, int E, const int32_t* topk_idx, int32_t* num_
 
 namespace mp {
 
-// Checks shared by mp_dispatch and mp_dispatch_offsets.
-static int check_offsets_args(int R, int N, int K, int E, const int32_t* topk_idx,
-                              const float* topk_weights, const uint32_t* is_token_in_rank,
-                              const int32_t* num_tokens_per_rank,
-                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
-                              const int32_t* recv_src_rank, const int32_t* recv_src_idx,
-                              const int32_t* recv_topk_idx, const float* recv_topk_weights,
-                              const int32_t* dest_offsets, const int32_t* rank_prefix,
-                              const int32_t* num_recv_tokens_per_expert, const int32_t* send_row,
-                              const int32_t* dev_err, const void* workspace) {
+// Checks shared by mp_dispatch, mp_dispatch_offsets and mp_dispatch_noalloc:
+// every argument of the receive-offset scan except its workspace.
+int check_offsets_buffers(int R, int N, int K, int E, const int32_t* topk_idx,
+                          const float* topk_weights, const uint32_t* is_token_in_rank,
+                          const int32_t* num_tokens_per_rank,
+                          const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                          const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                          const int32_t* recv_topk_idx, const float* recv_topk_weights,
+                          const int32_t* dest_offsets, const int32_t* rank_prefix,
+                          const int32_t* num_recv_tokens_per_expert, const int32_t* send_row,
+                          const int32_t* dev_err) {
   if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0) return MP_ERR_INVALID_ARG;
   if (!num_tokens_per_rank || !num_tokens_per_expert || !dest_offsets || !rank_prefix ||
-      !num_recv_tokens_per_expert || !dev_err || !workspace)
+      !num_recv_tokens_per_expert || !dev_err)
     return MP_ERR_INVALID_ARG;
   if (N > 0 && (!topk_idx || !topk_weights || !is_token_in_rank || !send_row))
     return MP_ERR_INVALID_ARG;
   if (recv_capacity > 0 &&
       (!recv_src_rank || !recv_src_idx || !recv_topk_idx || !recv_topk_weights))
     return MP_ERR_INVALID_ARG;
-  if (!aligned16(workspace) || !aligned4(topk_idx) || !aligned4(topk_weights) ||
+  if (!aligned4(topk_idx) || !aligned4(topk_weights) ||
       !aligned4(is_token_in_rank) || !aligned4(send_row) || !aligned4(recv_src_rank) ||
       !aligned4(recv_src_idx) || !aligned4(recv_topk_idx) || !aligned4(recv_topk_weights) ||
       !aligned4(num_tokens_per_rank) || !aligned4(num_tokens_per_expert) ||
@@ -116,10 +117,28 @@ static int check_offsets_args(int R, int N, int K, int E, const int32_t* topk_id
   return MP_OK;
 }
 
-// Checks shared by mp_dispatch and mp_dispatch_rows.
-static int check_rows_args(int R, int N, int H, int dtype, const void* x, const float* x_scales,
-                           const int32_t* send_row, int64_t recv_capacity, const void* recv_x,
-                           const float* recv_scales) {
+// The same with the caller's workspace (non-NULL, 16-byte aligned).
+static int check_offsets_args(int R, int N, int K, int E, const int32_t* topk_idx,
+                              const float* topk_weights, const uint32_t* is_token_in_rank,
+                              const int32_t* num_tokens_per_rank,
+                              const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                              const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                              const int32_t* recv_topk_idx, const float* recv_topk_weights,
+                              const int32_t* dest_offsets, const int32_t* rank_prefix,
+                              const int32_t* num_recv_tokens_per_expert, const int32_t* send_row,
+                              const int32_t* dev_err, const void* workspace) {
+  if (!workspace || !aligned16(workspace)) return MP_ERR_INVALID_ARG;
+  return check_offsets_buffers(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                               num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                               recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                               dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                               dev_err);
+}
+
+// Checks shared by mp_dispatch, mp_dispatch_rows and mp_dispatch_noalloc.
+int check_rows_args(int R, int N, int H, int dtype, const void* x, const float* x_scales,
+                    const int32_t* send_row, int64_t recv_capacity, const void* recv_x,
+                    const float* recv_scales) {
   if (R < 1 || R > MP_MAX_RANKS || N < 0 || H <= 0 || recv_capacity < 0)
     return MP_ERR_INVALID_ARG;
   if (int64_t(R) * N * R >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;

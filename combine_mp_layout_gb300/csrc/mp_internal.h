@@ -10,6 +10,22 @@ namespace mp {
 // SM count of the current device (cached per device).
 int sm_count();
 
+// Host-side argument checks of mp_dispatch (MP_OK or MP_ERR_INVALID_ARG):
+// the receive-offset scan's arguments without its workspace, and the row
+// copy's.
+int check_offsets_buffers(int R, int N, int K, int E, const int32_t* topk_idx,
+                          const float* topk_weights, const uint32_t* is_token_in_rank,
+                          const int32_t* num_tokens_per_rank,
+                          const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                          const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                          const int32_t* recv_topk_idx, const float* recv_topk_weights,
+                          const int32_t* dest_offsets, const int32_t* rank_prefix,
+                          const int32_t* num_recv_tokens_per_expert, const int32_t* send_row,
+                          const int32_t* dev_err);
+int check_rows_args(int R, int N, int H, int dtype, const void* x, const float* x_scales,
+                    const int32_t* send_row, int64_t recv_capacity, const void* recv_x,
+                    const float* recv_scales);
+
 cudaError_t launch_layout(int R, int N, int K, int E, const int32_t* topk_idx,
                           int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
                           uint32_t* is_token_in_rank, int32_t* dev_err, unsigned char* ws,

@@ -379,14 +379,22 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const void *in
  * The scan's scratch lives instead in a fixed array of
  * MP_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
  * GPU that loads the library holds until the process exits.
+ *  - Scope: only the dispatch step goes without a workspace.  Its inputs
+ *    num_tokens_per_rank, num_tokens_per_expert and is_token_in_rank come
+ *    from mp_layout, which still takes a caller-allocated workspace (a caller
+ *    may also compute them by other means).
  *  - Limit: problems whose mp_workspace_size(R, N, E) exceeds
  *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with E=256 that allows up to 244,608
  *    tokens per rank at R=8 and 15,488 at R=32) are rejected with
  *    MP_ERR_INVALID_ARG before anything is launched; use mp_dispatch with a
- *    workspace for those.
- *  - Set-up: the first call on each device (with that device current) finds
- *    the array's device address and zero-fills it with a synchronous
- *    cudaMemset.  Make that first call before any stream capture.
+ *    workspace for those.  Every other argument is checked as by mp_dispatch,
+ *    also before anything is put on the stream.
+ *  - Set-up: the first call on each device (with that device current), and
+ *    the first call after that device's context was reset, finds the array's
+ *    device address, zero-fills it on `stream` and waits for that stream
+ *    (cudaStreamSynchronize), so the fill is complete before this or any
+ *    later call uses the array.  Make that first call before any stream
+ *    capture.
  *  - Every call on a device shares the one array and starts by clearing its
  *    counters on `stream`, so calls whose work overlaps on the GPU (other
  *    streams, other host threads) race and give wrong results: order them on

@@ -642,6 +642,35 @@ def pin_block_quantisation(orc) -> None:
     tol = np.maximum(np.abs(xf) * 2.0**-4, np.repeat(sc, 128, axis=1) * 2.0**-10) * 1.0001
     assert np.all(np.abs(deq - xf) <= tol)
     assert np.all((deq == 0) | (np.sign(deq) == np.sign(xf)))
+    # every code exactly: the binary32 quotient x / scale correctly rounded (numpy's
+    # float32 division is IEEE-754's), narrowed by torch's e4m3 cast with the
+    # satfinite clamp at +-448 of the reading
+    x32 = _f32(xb).reshape(40, 4, 128)
+    quo = np.clip(x32 / sc[..., None], np.float32(-448), np.float32(448))
+    assert np.array_equal(q, _torch_e4m3(quo.reshape(40, 512)))
+    # blocks whose elements sit where x * RN(1 / scale) and RN(x / scale) narrow to
+    # different codes: they pin the division itself (a reciprocal taken first moves
+    # these across an e4m3 rounding boundary)
+    bf16_pos = (np.arange(1, 0x7f80, dtype=np.uint32) << 16).view(np.float32)
+    rows = []
+    for a_bits in (0x4118, 0x3fd0, 0x4944, 0x4b44, 0x4c52, 0x42d2):
+        amax_b = np.float32((np.uint32(a_bits) << 16).view(np.float32))
+        scale = np.float32(amax_b / np.float32(448))
+        cand = bf16_pos[bf16_pos < amax_b]
+        by_div = _torch_e4m3(np.clip(cand / scale, 0, 448))
+        by_rcp = _torch_e4m3(np.clip(cand * (np.float32(1) / scale), 0, 448))
+        hard = cand[by_div != by_rcp][:63]
+        assert hard.size > 0
+        blk = np.zeros(128, np.float32)
+        blk[0] = amax_b
+        blk[1:1 + hard.size] = hard
+        blk[64:64 + hard.size] = -hard
+        rows.append(blk)
+    xh = _bits(np.stack(rows))
+    qh, sch, st = orc.quantize_e4m3(xh)
+    assert st == 0
+    quo = np.clip(_f32(xh) / sch, np.float32(-448), np.float32(448))
+    assert np.array_equal(qh, _torch_e4m3(quo))
 
 
 def pin_mxfp8_quantisation(orc) -> None:

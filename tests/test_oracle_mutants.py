@@ -52,6 +52,8 @@ MUTANTS = {
     "quant_divisor_240": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
     "quant_multiplies": ("oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / scale)",
                          "oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) * scale)"),
+    "quant_reciprocal_first": ("oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) / scale)",
+                               "oracle_f32_to_e4m3(oracle_bf16_to_f32(xb[h]) * (1.0f / scale))"),
     "quant_zero_scale": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 448.0f : 0.0f"),
     "global_ids_sentinel_ignored": ("(e >= d * El && e < (d + 1) * El) ? e : sentinel;",
                                     "(e >= d * El && e < (d + 1) * El) ? e : -1;"),
