@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the MoE layout -> dispatch -> combine hot path on one GB300.
 
-One step = mp_layout_and_offsets (layout + receive offsets, one launch) +
-mp_dispatch_rows (row copy) + mp_combine on the DeepSeek-V3-shaped workload
+One step = mp_layout_dispatch (layout + receive offsets in one cooperative
+launch, then the row copy launched as its programmatic dependent) + mp_combine
+(launched as the copy's programmatic dependent) on the DeepSeek-V3-shaped workload
 (R=8 logical ranks x N=4096 tokens, H=7168 bf16, E=256 experts, top-8 uniform
 routing), the combine input being the dispatched rows themselves (identity
 experts).  Inputs are synthetic and
@@ -246,8 +247,8 @@ def reference_arm(args):
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(args.config, inp),
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1,
+                         "host_cores": os.cpu_count(), "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -550,6 +551,34 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
     del plan, rx, yl, lo, graph, graph3
     torch.cuda.empty_cache()
 
+    # the DeepSeek-V3 shape at small batches (the pages' EP bench defaults to 128 tokens
+    # per rank): the step as timed above (one-call dispatch + combine, launched one by
+    # one), as three calls, and replayed as a CUDA graph
+    for nb_tok in (128, 512, 1024):
+        inp = wl.make_ep("dsv3", seed=0, N=nb_tok)
+        R, N, H, E, K = inp.R, inp.N, inp.H, inp.E, inp.K
+        plan = EPPlan(R, N, K, E, H, "bf16")
+        plan.load(inp)
+        del inp
+        plan.step()
+        torch.cuda.synchronize()
+        T = plan.num_recv()
+        ms1 = timed(plan.step, steps)
+        ms3 = timed(plan.step_three_calls, steps)
+        graph = as_graph(plan.step)
+        msg = timed(graph.replay, steps)
+        assert plan.device_error() == 0
+        ab = algorithmic_bytes(R, N, K, E, H, T)
+        nbytes = ab["layout"] + ab["dispatch"] + ab["combine"]
+        out["dsv3_small_batch_n%d" % nb_tok] = dict(
+            row(ms1, nbytes), us_per_step=ms1 * 1e3, tokens_per_s=R * N / (ms1 / 1e3),
+            us_per_step_three_calls=ms3 * 1e3, us_per_step_cuda_graph=msg * 1e3,
+            GBs_cuda_graph=nbytes / (msg / 1e3) / 1e9, receive_rows=T,
+            workload="dsv3 shape at N=%d tokens per rank: mp_layout_dispatch + mp_combine "
+                     "(identity experts), eager" % N)
+        del plan, graph
+    torch.cuda.empty_cache()
+
     # the skewed workload: Zipf(1.2) routing, rank 0 hot
     inp = wl.make_ep("skew", seed=0, N=wl.CONFIGS["skew"]["N"] // scale)
     R, N, H, E, K = inp.R, inp.N, inp.H, inp.E, inp.K
@@ -634,7 +663,7 @@ def main():
     nb["dispatch"] = nb["layout_offsets"] + nb["rows"]
 
     # timed region: K steps, per-phase CUDA events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -645,32 +674,53 @@ def main():
     for i in range(args.steps):
         e = ev[i]
         e[0].record(stream)
-        B.check(plan.layout_and_offsets())
+        B.check(plan.layout_dispatch(), "mp_layout_dispatch")
         e[1].record(stream)
-        B.check(plan.dispatch_rows())
+        B.check(plan.combine(y), "mp_combine")
         e[2].record(stream)
-        B.check(plan.combine(y))
-        e[3].record(stream)
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    ph = {"layout_offsets": 0.0, "rows": 0.0, "combine": 0.0}
+    ph = {"dispatch": 0.0, "combine": 0.0}
     for e in ev:
-        ph["layout_offsets"] += e[0].elapsed_time(e[1])
-        ph["rows"] += e[1].elapsed_time(e[2])
-        ph["combine"] += e[2].elapsed_time(e[3])
+        ph["dispatch"] += e[0].elapsed_time(e[1])
+        ph["combine"] += e[1].elapsed_time(e[2])
     ph = {k: v / args.steps for k, v in ph.items()}
-    step_ms = sorted(e[0].elapsed_time(e[3]) for e in ev)  # each step, launch to launch
+    step_ms = sorted(e[0].elapsed_time(e[2]) for e in ev)  # each step, launch to launch
     step_stats = {"median": step_ms[len(step_ms) // 2], "min": step_ms[0], "max": step_ms[-1]}
-    ph["dispatch"] = ph["layout_offsets"] + ph["rows"]
     assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
+
+    # The same step as three calls (layout + offsets, rows, combine), timed per call
+    # outside the timed region: the split of the dispatch and the gain of the one call.
+    three = None
+    if N > 0:
+        ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(min(args.steps, 50))]
+        for _ in range(3):
+            plan.step_three_calls(y)
+        torch.cuda.synchronize()
+        for e in ev3:
+            e[0].record(stream)
+            B.check(plan.layout_and_offsets())
+            e[1].record(stream)
+            B.check(plan.dispatch_rows())
+            e[2].record(stream)
+            B.check(plan.combine(y))
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        assert plan.device_error() == 0, B.mp_status_string(plan.device_error())
+        n3 = len(ev3)
+        three = {"layout_offsets": sum(e[0].elapsed_time(e[1]) for e in ev3) / n3,
+                 "rows": sum(e[1].elapsed_time(e[2]) for e in ev3) / n3,
+                 "combine": sum(e[2].elapsed_time(e[3]) for e in ev3) / n3,
+                 "step": sum(e[0].elapsed_time(e[3]) for e in ev3) / n3}
 
     total_ms = max_over_ranks(total_ms, world, device="cuda")
     ms_step = total_ms / args.steps
     tokens = R * N * world
     value = replica_throughput(R * N, args.steps, world, total_ms)
-    step_bytes = nb["layout_offsets"] + nb["rows"] + nb["combine"]
+    step_bytes = nb["dispatch"] + nb["combine"]
     eff_gbs = step_bytes * world / (ms_step / 1e3) / 1e9
 
     # End to end through the public API with host buffers (pinned): every step
@@ -760,11 +810,12 @@ def main():
     ms_graph = ga.elapsed_time(gb) / args.steps
     del step_graph
 
-    # roofline of the dominant kernel (the larger of the row copy and combine)
+    # roofline of the dominant kernel: the combine, the step's largest single kernel (the
+    # dispatch phase is two kernels, the cooperative layout + offsets and the row copy)
     peak, peak_kind = peaks()
-    dom = "rows" if ph["rows"] >= ph["combine"] else "combine"
+    dom = "combine"
     achieved = nb[dom] / (ph[dom] / 1e3) / 1e9
-    kname = {"rows": "mp_k_dispatch<8,4>", "combine": "mp_k_combine<8,1,3,0>"}[dom]
+    kname = "mp_k_combine<8,1,3,0>"
     traffic = recorded_traffic(kname) if (args.config == "dsv3" and args.tokens == 0) else None
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
@@ -773,7 +824,11 @@ def main():
                                 "N=1536 capture summarised under profiles/; null if the "
                                 "kernel source changed since",
                 "all_phases": {k: {"ms": ph[k], "algorithmic_bytes": nb[k],
-                                   "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in nb}}
+                                   "GB/s": nb[k] / (ph[k] / 1e3) / 1e9} for k in ph},
+                "three_calls_ms": three,
+                "three_calls_GBs": None if three is None else {
+                    k: nb[k] / (three[k] / 1e3) / 1e9
+                    for k in ("layout_offsets", "rows", "combine")}}
 
     other = None
     if not args.no_other_rows and args.config == "dsv3" and (args.tokens == 0 or
@@ -788,9 +843,11 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = time_oracle(inp, args.cpu_budget_s)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+               "kind": "oracle",
                "sample": "first %d of %d tokens per rank, %d ranks, one layout + dispatch + "
-                         "combine pass (%.1f s)" % (n, N, R, dt)}
+                         "combine pass (%.1f s; single-threaded, 1 of the host's %s cores)"
+                         % (n, N, R, dt, os.cpu_count())}
 
     if rank == 0:
         line = {

@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.mp_dispatch_rows_bulk.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P]
         L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
         L.mp_dispatch_noalloc.argtypes = [i32] * 6 + [P] * 7 + [i64] + [P] * 12
+        L.mp_layout_dispatch.argtypes = [i32] * 6 + [P] * 4 + [i64] + [P] * 16
         L.mp_allgatherv_multi.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_dispatch_ll.argtypes = [i32] * 7 + [P] * 4 + [i64] + [P] * 8
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
@@ -89,7 +90,7 @@ def lib() -> ctypes.CDLL:
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
                   "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk",
                   "mp_layout_and_offsets", "mp_dispatch_noalloc", "mp_allgatherv_multi",
-                  "mp_dispatch_ll"):
+                  "mp_dispatch_ll", "mp_layout_dispatch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -190,6 +191,26 @@ def mp_layout_and_offsets(R, N, K, E, topk_idx, topk_weights, recv_capacity,
         int(recv_capacity), _dev(num_tokens_per_rank, "num_tokens_per_rank"),
         _dev(num_tokens_per_expert, "num_tokens_per_expert"),
         _dev(is_token_in_rank, "is_token_in_rank"), _dev(recv_src_rank, "recv_src_rank"),
+        _dev(recv_src_idx, "recv_src_idx"), _dev(recv_topk_idx, "recv_topk_idx"),
+        _dev(recv_topk_weights, "recv_topk_weights"), _dev(dest_offsets, "dest_offsets"),
+        _dev(rank_prefix, "rank_prefix"),
+        _dev(num_recv_tokens_per_expert, "num_recv_tokens_per_expert"),
+        _dev(send_row, "send_row"), _dev(dev_err, "dev_err"), _dev(workspace, "workspace"),
+        _stream(stream))
+
+
+def mp_layout_dispatch(R, N, K, E, H, dtype, x, x_scales, topk_idx, topk_weights, recv_capacity,
+                       num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank, recv_x,
+                       recv_scales, recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                       dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
+                       workspace, stream=None) -> int:
+    return lib().mp_layout_dispatch(
+        R, N, K, E, H, dtype, _dev(x, "x"), _dev(x_scales, "x_scales"),
+        _dev(topk_idx, "topk_idx"), _dev(topk_weights, "topk_weights"), int(recv_capacity),
+        _dev(num_tokens_per_rank, "num_tokens_per_rank"),
+        _dev(num_tokens_per_expert, "num_tokens_per_expert"),
+        _dev(is_token_in_rank, "is_token_in_rank"), _dev(recv_x, "recv_x"),
+        _dev(recv_scales, "recv_scales"), _dev(recv_src_rank, "recv_src_rank"),
         _dev(recv_src_idx, "recv_src_idx"), _dev(recv_topk_idx, "recv_topk_idx"),
         _dev(recv_topk_weights, "recv_topk_weights"), _dev(dest_offsets, "dest_offsets"),
         _dev(rank_prefix, "rank_prefix"),

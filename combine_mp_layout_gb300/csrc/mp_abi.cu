@@ -267,6 +267,57 @@ int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
                                  send_row, dev_err, ws, cs));
 }
 
+int mp_layout_dispatch(int R, int N, int K, int E, int H, int dtype, const void* x,
+                       const float* x_scales, const int32_t* topk_idx,
+                       const float* topk_weights, int64_t recv_capacity,
+                       int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                       uint32_t* is_token_in_rank, void* recv_x, float* recv_scales,
+                       int32_t* recv_src_rank, int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                       float* recv_topk_weights, int32_t* dest_offsets, int32_t* rank_prefix,
+                       int32_t* num_recv_tokens_per_expert, int32_t* send_row, int32_t* dev_err,
+                       void* workspace, mp_stream_t stream) {
+  int st = check_layout_args(R, N, K, E, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                             is_token_in_rank, dev_err, workspace);
+  if (st == MP_OK)
+    st = check_offsets_args(R, N, K, E, topk_idx, topk_weights, is_token_in_rank,
+                            num_tokens_per_rank, num_tokens_per_expert, recv_capacity,
+                            recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                            dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+                            dev_err, workspace);
+  if (st == MP_OK)
+    st = check_rows_args(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                         recv_scales);
+  if (st != MP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const bool fp8 = dtype == MP_E4M3;
+  const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
+  const int spr = fp8 ? H / MP_SCALE_BLOCK : 0;
+  // one cooperative launch for layout + offsets (receive metadata left out),
+  // then the row copy, which writes the metadata, as its programmatic dependent
+  const cudaError_t e = launch_layout_scan(
+      R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
+      num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
+      recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
+      ws, cs, /*meta=*/0);
+  if (e == cudaSuccess)
+    return cuda_status(launch_dispatch_after_offsets(
+        R, N, K, E, row_bytes, x, recv_x, recv_capacity, send_row, spr, x_scales, recv_scales,
+        topk_idx, topk_weights, recv_src_rank, recv_src_idx, recv_topk_idx, recv_topk_weights,
+        cs));
+  if (e != cudaErrorNotSupported) return MP_ERR_CUDA;
+  // beyond one resident grid (or no tokens): layout, offsets and rows as three launches
+  if (launch_layout(R, N, K, E, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                    is_token_in_rank, dev_err, ws, cs) != cudaSuccess ||
+      launch_scan(R, N, K, E, topk_idx, topk_weights, is_token_in_rank, num_tokens_per_rank,
+                  num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx,
+                  recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
+                  num_recv_tokens_per_expert, send_row, dev_err, ws, cs) != cudaSuccess)
+    return MP_ERR_CUDA;
+  return cuda_status(launch_rows(R, N, H, dtype, x, x_scales, send_row, recv_capacity, recv_x,
+                                 recv_scales, cs));
+}
+
 int mp_dispatch_rows(int R, int N, int H, int dtype, const void* x, const float* x_scales,
                      const int32_t* send_row, int64_t recv_capacity, void* recv_x,
                      float* recv_scales, mp_stream_t stream) {

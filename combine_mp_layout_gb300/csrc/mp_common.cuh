@@ -27,8 +27,8 @@ struct Control {
   uint32_t scan_epoch;         // tags tile records of the current scan launch
   uint32_t copy_unit_counter;  // reserved for dynamically scheduled copies
   uint32_t layout_done[MP_MAX_RANKS];  // layout blocks finished, per source rank
-  uint32_t bar_count;          // grid barrier of the fused layout + scan: arrivals
-  uint32_t bar_gen;            // ... and its generation
+  uint32_t bar_count;          // grid barrier of the fused layout + scan: arrivals (never reset)
+  uint32_t bar_base;           // ... and their count when the current launch began
 };
 static_assert(sizeof(Control) <= 512, "control block");
 
@@ -81,6 +81,24 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 }
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Atomic add with acquire-release semantics at gpu scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Programmatic dependent launch (sm_90+): let the grid launched after this one
+// on the stream (with programmatic stream serialization) start its blocks now,
+// and, in such a dependent grid, wait until the grid before it has finished
+// and its writes are visible.  Both are no-ops without such a neighbour.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Streaming vector accesses: payload rows are touched once, so they bypass

@@ -118,6 +118,7 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ 
               Words<NW>* __restrict__ recv_x, int64_t recv_capacity,
               const int32_t* __restrict__ send_row, int spr, const float* __restrict__ x_scales,
               float* __restrict__ recv_scales) {
+  pdl_launch_dependents();  // a combine launched as a dependent may stage its blocks
   const int lane = threadIdx.x & 31;
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
@@ -146,6 +147,85 @@ mp_k_dispatch(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ 
       if (spr > 0 && slab == 0)
         for (int c = lane; c < spr; c += kWarp)
           recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The row copy of mp_layout_dispatch: mp_k_dispatch launched as the
+// programmatic dependent of the fused layout + offsets kernel, which also
+// writes the receive metadata the fused kernel leaves out.  Its blocks may
+// start while that kernel runs: each warp loads its first unit's row vectors
+// (and, for a token's first slab, the token's top-k ids and weights) -- inputs
+// of the call, complete before it began -- then waits for the offsets grid to
+// finish (griddepcontrol.wait) and only then reads send_row.  For every
+// receive row of a token the warp of its first slab writes recv_src_rank,
+// recv_src_idx and the K local top-k ids and weights (e - d*E/R and the weight
+// for an expert on the row's destination d, else -1 and 0).
+// ---------------------------------------------------------------------------
+template <int NW, int U>
+__global__ void __launch_bounds__(kCopyThreads)
+mp_k_dispatch_after_offsets(int R, int N, int K, int El, int64_t tokens, int64_t vpr,
+                            const Words<NW>* __restrict__ x, Words<NW>* __restrict__ recv_x,
+                            int64_t recv_capacity, const int32_t* send_row, int spr,
+                            const float* __restrict__ x_scales, float* __restrict__ recv_scales,
+                            const int32_t* __restrict__ topk_idx,
+                            const float* __restrict__ topk_weights,
+                            int32_t* __restrict__ recv_src_rank, int32_t* __restrict__ recv_src_idx,
+                            int32_t* __restrict__ recv_topk_idx,
+                            float* __restrict__ recv_topk_weights) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t slab_vec = int64_t(kWarp) * U;
+  const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
+  const int64_t units = tokens * slabs;
+  const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
+  int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  Words<NW> v[U];
+  int my_e = -1;
+  float my_w = 0.0f;
+  auto load_unit = [&](int64_t u0) {
+    const int64_t tok = u0 / slabs, i0 = (u0 - tok * slabs) * slab_vec + lane;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * kWarp < vpr) v[u] = ld_stream_w<NW>(x + tok * vpr + i0 + u * kWarp);
+    if (i0 < kWarp && lane < K) {  // the token's first slab: its top-k ids and weights
+      my_e = __ldg(topk_idx + tok * K + lane);
+      my_w = __ldg(topk_weights + tok * K + lane);
+    }
+  };
+  if (unit < units) load_unit(unit);
+  pdl_wait_prior_grid();
+  for (bool first = true; unit < units; unit += nw, first = false) {
+    if (!first) load_unit(unit);
+    const int64_t tok = unit / slabs;
+    const int64_t slab = unit - tok * slabs;
+    const int64_t i0 = slab * slab_vec + lane;
+    // send_row was written by the offsets grid: read through L2, not the read-only path
+    const int my = lane < R ? __ldcg(send_row + tok * R + lane) : -1;
+    unsigned vm = __ballot_sync(kFull, my >= 0 && int64_t(my) < recv_capacity);
+    while (vm) {
+      const int d = __ffs(vm) - 1;
+      vm &= vm - 1;
+      const int64_t row = __shfl_sync(kFull, my, d);
+      Words<NW>* dst = recv_x + row * vpr;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i0 + u * kWarp < vpr) st_stream_w<NW>(dst + i0 + u * kWarp, v[u]);
+      if (slab == 0) {
+        if (spr > 0)
+          for (int c = lane; c < spr; c += kWarp)
+            recv_scales[row * spr + c] = __ldg(x_scales + tok * spr + c);
+        const int src = int(tok / N);
+        if (lane == 0) recv_src_rank[row] = src;
+        if (lane == 1) recv_src_idx[row] = int(tok - int64_t(src) * N);
+        if (lane < K) {
+          const int lo = d * El;
+          const bool local = my_e >= lo && my_e < lo + El;
+          recv_topk_idx[row * K + lane] = local ? my_e - lo : -1;
+          recv_topk_weights[row * K + lane] = local ? my_w : 0.0f;
+        }
+      }
     }
   }
 }
@@ -517,6 +597,9 @@ __global__ void __launch_bounds__(kCopyThreads, MP_COMBINE_MINB)
 mp_k_combine(int R, int64_t tokens, int64_t vpr, const Words<NW>* __restrict__ y, int64_t y_rows,
              const int32_t* __restrict__ send_row, const float* __restrict__ weights,
              Words<NW>* __restrict__ out, int32_t* __restrict__ dev_err) {
+  // launched with programmatic stream serialization: the blocks may be staged
+  // while the kernel before it (e.g. the row copy producing y) finishes
+  pdl_wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int64_t slab_vec = int64_t(kWarp) * U;
   const int64_t slabs = (vpr + slab_vec - 1) / slab_vec;
@@ -681,6 +764,26 @@ mp_k_agv_multi(int R, int64_t total, AgvList l) {
 // Launchers: a persistent grid of (SMs x resident blocks) blocks, trimmed to
 // the work available; 32-byte vectors when sizes and pointers allow.
 // ---------------------------------------------------------------------------
+// Launch with programmatic stream serialization: the kernel's blocks may start
+// before the kernel ahead of it on the stream has finished, once that kernel's
+// blocks have all triggered (pdl_launch_dependents) or exited; the kernel
+// itself must call pdl_wait_prior_grid before it touches that kernel's output.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, cudaStream_t stream,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kCopyThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename Kernel>
 static int resident_blocks(Kernel k) {
   int n = 0;
@@ -780,6 +883,58 @@ cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const
   if (tokens == 0) return cudaSuccess;
   return dispatch_copy_tma(R, tokens, row_bytes, x, recv_x, recv_capacity, send_row,
                            scales_per_row, x_scales, recv_scales, dev_err, stream);
+}
+
+template <int NW, int U>
+static cudaError_t dispatch_after_offsets_nw(int R, int N, int K, int El, int64_t row_bytes,
+                                             const void* x, void* recv_x, int64_t recv_capacity,
+                                             const int32_t* send_row, int spr,
+                                             const float* x_scales, float* recv_scales,
+                                             const int32_t* topk_idx, const float* topk_weights,
+                                             int32_t* recv_src_rank, int32_t* recv_src_idx,
+                                             int32_t* recv_topk_idx, float* recv_topk_weights,
+                                             cudaStream_t stream) {
+  const int64_t tokens = int64_t(R) * N;
+  const int64_t vpr = row_bytes / (4 * NW);
+  const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
+  return launch_dependent(mp_k_dispatch_after_offsets<NW, U>,
+                          dim3(grid_full(kWarpsPerBlock, tokens * slabs)), stream, R, N, K, El,
+                          tokens, vpr, static_cast<const Words<NW>*>(x),
+                          static_cast<Words<NW>*>(recv_x), recv_capacity, send_row, spr, x_scales,
+                          recv_scales, topk_idx, topk_weights, recv_src_rank, recv_src_idx,
+                          recv_topk_idx, recv_topk_weights);
+}
+
+cudaError_t launch_dispatch_after_offsets(int R, int N, int K, int E, int64_t row_bytes,
+                                          const void* x, void* recv_x, int64_t recv_capacity,
+                                          const int32_t* send_row, int scales_per_row,
+                                          const float* x_scales, float* recv_scales,
+                                          const int32_t* topk_idx, const float* topk_weights,
+                                          int32_t* recv_src_rank, int32_t* recv_src_idx,
+                                          int32_t* recv_topk_idx, float* recv_topk_weights,
+                                          cudaStream_t stream) {
+  const int64_t tokens = int64_t(R) * N;
+  if (tokens == 0) return cudaSuccess;
+  const int El = E / R;
+  // the shapes of launch_dispatch_copy: 1 vector per lane and unit for small
+  // problems (more units in flight), 4 otherwise; 16-byte vectors when the row
+  // size or the pointers do not allow 32
+  if (row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32)) {
+    const int64_t slabs = (row_bytes / 32 + kWarp * MP_DISPATCH_U - 1) / (kWarp * MP_DISPATCH_U);
+    if (MP_SMALL_DISPATCH && tokens * slabs < int64_t(sm_count()) * (2048 / kWarp))
+      return dispatch_after_offsets_nw<8, 1>(R, N, K, El, row_bytes, x, recv_x, recv_capacity,
+                                             send_row, scales_per_row, x_scales, recv_scales,
+                                             topk_idx, topk_weights, recv_src_rank, recv_src_idx,
+                                             recv_topk_idx, recv_topk_weights, stream);
+    return dispatch_after_offsets_nw<8, MP_DISPATCH_U>(
+        R, N, K, El, row_bytes, x, recv_x, recv_capacity, send_row, scales_per_row, x_scales,
+        recv_scales, topk_idx, topk_weights, recv_src_rank, recv_src_idx, recv_topk_idx,
+        recv_topk_weights, stream);
+  }
+  return dispatch_after_offsets_nw<4, 2 * MP_DISPATCH_U>(
+      R, N, K, El, row_bytes, x, recv_x, recv_capacity, send_row, scales_per_row, x_scales,
+      recv_scales, topk_idx, topk_weights, recv_src_rank, recv_src_idx, recv_topk_idx,
+      recv_topk_weights, stream);
 }
 
 // Quantising copies.  Launch shapes measured on GB300 (dsv3 dispatch rows,
@@ -885,9 +1040,9 @@ static cudaError_t combine_nw(int R, int64_t tokens, int H, const void* y, int64
   const int64_t vpr = int64_t(H) * 2 / (4 * NW);
   const int64_t slabs = (vpr + kWarp * U - 1) / (kWarp * U);
   const unsigned grid = grid_for(per_sm, kWarpsPerBlock, tokens * slabs);
-  return launch_kernel(mp_k_combine<NW, U, RB, W>, dim3(grid), dim3(kCopyThreads), 0, stream, R,
-                       tokens, vpr, static_cast<const Words<NW>*>(y), y_rows, send_row, weights,
-                       static_cast<Words<NW>*>(out), dev_err);
+  return launch_dependent(mp_k_combine<NW, U, RB, W>, dim3(grid), stream, R, tokens, vpr,
+                          static_cast<const Words<NW>*>(y), y_rows, send_row, weights,
+                          static_cast<Words<NW>*>(out), dev_err);
 }
 
 template <bool W>
@@ -1050,12 +1205,13 @@ mp_k_ll_rows_after_sort(int K, int64_t tokens, int64_t vpr, const Words<NW>* __r
   const int64_t units = tokens * slabs;
   const int64_t nw = int64_t(gridDim.x) * kWarpsPerBlock;
   int64_t unit = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  pdl_launch_dependents();  // the weighted combine after it may stage its blocks
   Words<NW> v;
   if (unit < units) {  // the first unit's vector, before the wait
     const int64_t tok = unit / slabs, i = (unit - tok * slabs) * kWarp + lane;
     if (i < vpr) v = ld_stream_w<NW>(x + tok * vpr + i);
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait_prior_grid();
   for (bool first = true; unit < units; unit += nw, first = false) {
     const int64_t tok = unit / slabs;
     const int64_t slab = unit - tok * slabs;

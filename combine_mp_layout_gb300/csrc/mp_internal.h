@@ -41,7 +41,9 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                         cudaStream_t stream, int global_ids = 0, int32_t sentinel = -1);
 
 // mp_k_layout + mp_k_scan as one cooperative launch; cudaErrorNotSupported
-// (nothing launched) when the problem does not fit one resident grid.
+// (nothing launched) when the problem does not fit one resident grid.  With
+// meta = 0 the receive metadata (recv_src_rank, recv_src_idx, recv_topk_idx,
+// recv_topk_weights) is not written: launch_dispatch_after_offsets writes it.
 cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_idx,
                                const float* topk_weights, int64_t recv_capacity,
                                int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
@@ -50,7 +52,22 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                                float* recv_topk_weights, int32_t* dest_offsets,
                                int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
                                int32_t* send_row, int32_t* dev_err, unsigned char* ws,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int meta = 1);
+
+// The row copy of mp_layout_dispatch, launched as the programmatic dependent of
+// the fused layout + offsets kernel right before it on the stream: its first
+// row loads (and the tokens' top-k ids and weights) overlap that kernel, its
+// send_row reads wait for it.  Besides the rows (and e4m3 scales) it writes the
+// receive metadata: recv_src_rank / recv_src_idx and the local top-k ids and
+// weights of every receive row.
+cudaError_t launch_dispatch_after_offsets(int R, int N, int K, int E, int64_t row_bytes,
+                                          const void* x, void* recv_x, int64_t recv_capacity,
+                                          const int32_t* send_row, int scales_per_row,
+                                          const float* x_scales, float* recv_scales,
+                                          const int32_t* topk_idx, const float* topk_weights,
+                                          int32_t* recv_src_rank, int32_t* recv_src_idx,
+                                          int32_t* recv_topk_idx, float* recv_topk_weights,
+                                          cudaStream_t stream);
 
 // Low-latency offsets, expert-major (rank_major = 0: bins are experts) or
 // rank-major (1: bins are the ranks owning the experts); one block per source

@@ -267,6 +267,8 @@ __device__ __forceinline__ uint32_t tile_publish_lookback(
 // Called by all threads of the block; needs the tile's masks (one per token
 // thread), the per-warp ballots and offsets, the tile's first row and row
 // count per destination, and its top-k ids and weights staged in shared memory.
+// With META false only send_row is written (the receive metadata is then left
+// to the row copy that follows, mp_k_dispatch_after_offsets).
 struct TileRowsSmem {
   int32_t* sr_s;     // [kScanTokens][R]: send_row entries of the tile's tokens
   uint8_t* row_tok;  // [kScanTokens * MP_MAX_RANKS]: token of tile row j
@@ -279,7 +281,7 @@ __device__ __forceinline__ void write_tile_rows(
     const ScanArgs& a, uint32_t mask, int ntok, int t0, int64_t g0, int src_rank,
     const uint32_t (*wball)[MP_MAX_RANKS], const int32_t (*woff)[MP_MAX_RANKS],
     const int64_t* row_base, const uint32_t* tcnt, const int32_t* idx_s, const float* w_s,
-    const TileRowsSmem& sm) {
+    const TileRowsSmem& sm, bool meta = true) {
   const int R = a.R, K = a.K, E = a.E;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (warp == 0) {  // destination-major numbering of the tile's rows; the capacity clamp
@@ -307,15 +309,18 @@ __device__ __forceinline__ void write_tile_rows(
     for (uint32_t m = mask; m; m &= m - 1u) {
       const int d = __ffs(m) - 1;
       const int rank = woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
-      const int j = sm.dstart[d] + rank;
-      sm.row_tok[j] = uint8_t(tid);
-      sm.row_d[j] = uint8_t(d);
+      if (meta) {
+        const int j = sm.dstart[d] + rank;
+        sm.row_tok[j] = uint8_t(tid);
+        sm.row_d[j] = uint8_t(d);
+      }
       if (rank < sm.nok[d]) sm.sr_s[tid * R + d] = int32_t(row_base[d] + rank);
     }
   }
   __syncthreads();
 #pragma unroll 4
   for (int i = tid; i < ntok * R; i += kScanThreads) a.send_row[g0 * R + i] = sm.sr_s[i];
+  if (!meta) return;
   const int total = sm.dstart[R];
 #pragma unroll 4
   for (int j = tid; j < total; j += kScanThreads) {
@@ -477,10 +482,11 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 
 // ---------------------------------------------------------------------------
 // Layout and receive offsets in one cooperative launch (the work of mp_k_layout
-// followed by mp_k_scan, for callers of mp_layout_and_offsets).  Every block
-// is resident at once, so blocks own tiles statically (tile = blockIdx.x +
-// i * gridDim.x, in increasing order, which keeps each lookback's
-// predecessors running or done) and may meet at one grid barrier:
+// followed by mp_k_scan, for callers of mp_layout_and_offsets and
+// mp_layout_dispatch).  Every block is resident at once, so blocks own tiles
+// statically (tile = blockIdx.x + i * gridDim.x, in increasing order, which
+// keeps each lookback's predecessors running or done) and may meet at one
+// grid barrier:
 //  1. per tile: the top-k ids give each token's rank mask (is_token_in_rank)
 //     and the tile's expert counts (added into the rank's accumulator); the
 //     tile publishes its per-destination counts and looks back over its
@@ -489,40 +495,43 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 //  3. each rank's last tile holds num_tokens_per_rank; from it every block
 //     forms rank_prefix and the destination bases, the accumulators give
 //     num_tokens_per_expert and num_recv_tokens_per_expert (and are zeroed),
-//     and each tile writes its send_row entries and receive metadata.
+//     and each tile writes its send_row entries and (with meta) the receive
+//     metadata.
+// The kernel lets its programmatic dependent (the row copy of
+// mp_layout_dispatch) launch as soon as it starts.
 // ---------------------------------------------------------------------------
 constexpr int kFusedMaxTiles = 16;  // tiles one block may own (tiles <= 16 * grid)
-// (the failure-detection test sets the barrier's arrival count at this offset)
-static_assert(offsetof(Control, bar_count) == 144, "grid barrier words of the control block");
+// (the failure-detection test presets the barrier's base word at this offset)
+static_assert(offsetof(Control, bar_count) == 144 && offsetof(Control, bar_base) == 148,
+              "grid barrier words of the control block");
 
 struct FusedArgs {
   ScanArgs a;                      // receive-side outputs (its layout inputs unused)
   uint32_t* is_token_in_rank;      // [R][N] out
   int32_t* num_tokens_per_rank;    // [R][R] out
   int32_t* num_tokens_per_expert;  // [R][E] out
+  int meta;                        // 1: write the receive metadata too; 0: send_row only
 };
 
-// Grid barrier for a cooperative launch: thread 0 of each block arrives and
-// waits (bounded) for the last arrival to advance the generation.  Returns
-// false when the wait gave up.
-// `gen` is the generation read when the kernel started: a launch meets the
-// barrier once, and no other launch on the same workspace runs meanwhile.
-__device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, uint32_t gen,
+// Grid barrier for a cooperative launch.  bar_count counts arrivals and is
+// never reset; bar_base is its value when this launch began (every block reads
+// it before arriving, and block 0 moves it on by the grid size once past the
+// barrier, for the next launch).  Thread 0 of each block adds its arrival with
+// acquire-release semantics -- which also publishes the block's earlier writes,
+// ordered before it by the CTA barrier -- and polls (bounded) until every
+// block's arrival is in: one atomic and one poll, with no reset on the way.
+// Returns false when the wait gave up.
+__device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, uint32_t base,
                                              int* ok_s) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    __threadfence();
-    if (atomicAdd(&ctl->bar_count, 1u) == nblocks - 1) {
-      atomicExch(&ctl->bar_count, 0u);
-      __threadfence();
-      st_release_u32(&ctl->bar_gen, gen + 1u);
-    } else {
-      uint32_t spins = 0;
-      while (ld_acquire_u32(&ctl->bar_gen) == gen) {
-        if (++spins > kSpinLimit) { ok = 0; break; }
-        __nanosleep(32);
-      }
+    uint32_t seen = atom_add_acq_rel_u32(&ctl->bar_count, 1u) + 1u;
+    uint32_t spins = 0;
+    while (int32_t(seen - base) < int32_t(nblocks)) {
+      if (++spins > kSpinLimit) { ok = 0; break; }
+      __nanosleep(32);
+      seen = ld_acquire_u32(&ctl->bar_count);
     }
     *ok_s = ok;
   }
@@ -559,13 +568,14 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   int32_t* acc = reinterpret_cast<int32_t*>(a.ws + ws_acc_offset());  // [R][E + R]
   const int C = int(scan_tiles_per_rank(N));
   const int T = R * C;
-  // The epoch and barrier generation are read first; thread 0 keeps them in
+  pdl_launch_dependents();
+  // The epoch and barrier base are read first; thread 0 keeps them in
   // registers until the first tile's id loads are issued, so those loads do
   // not wait for them (the first tile's barrier publishes them).
   uint32_t epoch0 = 0, gen0 = 0;
   if (tid == 0) {
     epoch0 = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
-    gen0 = ld_relaxed_u32(&ctl->bar_gen);
+    gen0 = ld_relaxed_u32(&ctl->bar_base);
   }
 #if !MP_FUSED_EARLY_LOADS
   if (tid == 0) {
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
 #pragma unroll 4
       for (int i = tid; i < n; i += kScanThreads) {
         idx_s[i] = __ldg(gi + i);
-        if (single) w_s[i] = __ldg(gw + i);
+        if (single && f.meta) w_s[i] = __ldg(gw + i);
       }
     }
 #if MP_FUSED_EARLY_LOADS
@@ -633,7 +643,6 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     __syncthreads();  // hist, idx_s and the ballots are reused by the next tile
   }
   if (tid == 0 && sh_bad) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
-  __threadfence();
 
   // 2. every tile is published and every expert count added
   if (!grid_barrier(ctl, gridDim.x, sh_gen, &sh_ok)) {
@@ -671,7 +680,10 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       f.num_tokens_per_rank[i] = ntpr_s[i];
       a.rank_prefix[i] = pre;
     }
-    if (tid == 0) atomicAdd(&ctl->scan_epoch, 1u);  // every lookback of this launch is done
+    if (tid == 0) {
+      atomicAdd(&ctl->scan_epoch, 1u);  // every lookback of this launch is done
+      ctl->bar_base = sh_gen + gridDim.x;  // every arrival of this launch is in
+    }
   }
   // (the last blocks of the grid, so that block 0's tables do not add up)
   for (int64_t e = int64_t(gridDim.x - 1 - blockIdx.x) * kScanThreads + tid; e < E;
@@ -701,7 +713,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     const int64_t g0 = int64_t(s) * N + t0;
     const uint32_t mask = tid < ntok ? __ldcg(f.is_token_in_rank + g0 + tid) : 0u;
     if (!single) {  // ids, weights, ballots and offsets of this tile
-      {
+      if (f.meta) {
         const int n = ntok * K;
         const int32_t* gi = a.topk_idx + g0 * K;
         const float* gw = a.topk_weights + g0 * K;
@@ -732,7 +744,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     }
     __syncthreads();
     write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s,
-                    TileRowsSmem{sr_s, row_tok, row_d, dstart, nok});
+                    TileRowsSmem{sr_s, row_tok, row_d, dstart, nok}, f.meta != 0);
     __syncthreads();
   }
 }
@@ -982,7 +994,7 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
                 int32_t* __restrict__ dev_err) {
   // a row copy launched as this grid's programmatic dependent may start now:
   // it reads slot_row only after this grid has finished
-  asm volatile("griddepcontrol.launch_dependents;");
+  pdl_launch_dependents();
   extern __shared__ int32_t ll_smem[];
   __shared__ int64_t warp_sums[kLLThreads / kWarp];
   ll_offsets_block<RANK_MAJOR, kLLThreads, kLLHistInts>(
@@ -1067,7 +1079,7 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                                float* recv_topk_weights, int32_t* dest_offsets,
                                int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
                                int32_t* send_row, int32_t* dev_err, unsigned char* ws,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int meta) {
   if (N == 0) return cudaErrorNotSupported;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1101,7 +1113,7 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                        num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx,
                        recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
                        num_recv_tokens_per_expert, send_row, dev_err, ws, 0, -1},
-              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert};
+              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert, meta};
   void* args[] = {&f};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mp_k_layout_scan),
                                      dim3(unsigned(grid)), dim3(kScanThreads), args, smem,

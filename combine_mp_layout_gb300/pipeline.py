@@ -90,6 +90,18 @@ class EPPlan:
             self.dest_offsets, self.rank_prefix, self.num_recv_tokens_per_expert, self.send_row,
             self.dev_err, self.workspace, stream)
 
+    def layout_dispatch(self, stream=None) -> int:
+        """The whole dispatch in one call (mp_layout_dispatch): layout, receive offsets
+        and row copy, the copy launched as a programmatic dependent of the offsets."""
+        return B.mp_layout_dispatch(
+            self.R, self.N, self.K, self.E, self.H,
+            B.MP_BF16 if self.dtype == "bf16" else B.MP_E4M3, self.x, self.x_scales,
+            self.topk_idx, self.topk_weights, self.cap, self.num_tokens_per_rank,
+            self.num_tokens_per_expert, self.is_token_in_rank, self.recv_x, self.recv_scales,
+            self.recv_src_rank, self.recv_src_idx, self.recv_topk_idx, self.recv_topk_weights,
+            self.dest_offsets, self.rank_prefix, self.num_recv_tokens_per_expert, self.send_row,
+            self.dev_err, self.workspace, stream)
+
     def dispatch_offsets(self, stream=None) -> int:
         return B.mp_dispatch_offsets(
             self.R, self.N, self.K, self.E, self.topk_idx, self.topk_weights,
@@ -111,12 +123,20 @@ class EPPlan:
     def combine(self, y: torch.Tensor | None = None, stream=None) -> int:
         """Combine y (default: recv_x, i.e. identity experts) back into self.out."""
         y = self.recv_x if y is None else y
+        if y.dtype != torch.bfloat16 or y.dim() != 2 or y.shape[1] != self.H:
+            raise ValueError("combine takes bf16 rows [rows][H] (an e4m3 plan needs its "
+                             "expert outputs as y)")
         return B.mp_combine(self.R, self.N, self.H, y, y.shape[0], self.send_row, self.out,
                             self.dev_err, stream)
 
     def step(self, y: torch.Tensor | None = None, stream=None) -> None:
-        """One pass of the hot path: layout -> dispatch -> combine (layout and receive
-        offsets in one call, then the row copy, then combine)."""
+        """One pass of the hot path: layout -> dispatch -> combine as two calls (the whole
+        dispatch in one call, then combine)."""
+        B.check(self.layout_dispatch(stream), "mp_layout_dispatch")
+        B.check(self.combine(y, stream), "mp_combine")
+
+    def step_three_calls(self, y: torch.Tensor | None = None, stream=None) -> None:
+        """The same pass as three calls: layout and receive offsets, row copy, combine."""
         B.check(self.layout_and_offsets(stream), "mp_layout_and_offsets")
         B.check(self.dispatch_rows(stream=stream), "mp_dispatch_rows")
         B.check(self.combine(y, stream), "mp_combine")

@@ -162,6 +162,18 @@ def make_rsv(name_or_cfg="rsv", seed: int = 0, **overrides) -> RSVInputs:
     return RSVInputs(R, H, sizes, x, shards)
 
 
+def random_bf16_rows(rows: int, H: int, seed: int, chunk: int = 32768) -> torch.Tensor:
+    """[rows][H] standard-normal bf16 (CPU), every row drawn independently; made in
+    chunks of rows (each with its own seed) so that full-size expert outputs need no
+    full-size fp32 temporary."""
+    out = torch.empty((rows, H), dtype=torch.bfloat16)
+    for c, r0 in enumerate(range(0, rows, chunk)):
+        r1 = min(rows, r0 + chunk)
+        out[r0:r1] = torch.randn((r1 - r0, H), generator=_torch_gen(seed * 100003 + c + 1),
+                                 dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
 def gathered_bf16(rows: int, H: int, seed: int, table_rows: int = 1024) -> torch.Tensor:
     """[rows][H] bf16 synthetic expert outputs made cheaply at large sizes: each row is
     a row of a standard-normal table picked uniformly at random (CPU)."""

@@ -212,6 +212,34 @@ int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
                           int32_t *dev_err, void *workspace, mp_stream_t stream);
 
 /*
+ * mp_layout_dispatch -- the whole dispatch in one call: mp_layout, then
+ * mp_dispatch (receive offsets and row copy), from the routing and the token
+ * rows ([EP] get_dispatch_layout followed by intranode_dispatch; fusing them
+ * has no counterpart in the pages).  Where the problem fits one resident grid
+ * (as for mp_layout_and_offsets), layout and offsets run as one cooperative
+ * launch that writes send_row and the tables, and the row copy -- which also
+ * writes the receive metadata -- is launched as its programmatic dependent:
+ * its blocks start while the offsets are computed, load their first token
+ * rows, and wait for the offsets before they store.  Otherwise the launches of
+ * mp_layout and mp_dispatch run.
+ *   Arguments: the layout outputs of mp_layout and every argument of
+ *   mp_dispatch (same meaning, layout and ownership); the results are
+ *   identical to those two calls.
+ *   Checks and device errors: those of mp_layout and mp_dispatch, plus
+ *   MP_ERR_TIMEOUT when the grid barrier's bounded (~1 s) wait gives up (the
+ *   workspace must then be zero-filled again).
+ */
+int mp_layout_dispatch(int R, int N, int K, int E, int H, int dtype, const void *x,
+                       const float *x_scales, const int32_t *topk_idx,
+                       const float *topk_weights, int64_t recv_capacity,
+                       int32_t *num_tokens_per_rank, int32_t *num_tokens_per_expert,
+                       uint32_t *is_token_in_rank, void *recv_x, float *recv_scales,
+                       int32_t *recv_src_rank, int32_t *recv_src_idx, int32_t *recv_topk_idx,
+                       float *recv_topk_weights, int32_t *dest_offsets, int32_t *rank_prefix,
+                       int32_t *num_recv_tokens_per_expert, int32_t *send_row, int32_t *dev_err,
+                       void *workspace, mp_stream_t stream);
+
+/*
  * mp_dispatch_offsets_global -- mp_dispatch_offsets with the receive rows'
  * expert ids in global numbering ([EP] the later variant that returns
  * global token-major expert ids with a configurable invalid-expert

@@ -53,18 +53,21 @@ def test_lookback_wait_times_out_and_context_survives():
     assert np.array_equal(wl.bf16_bits(plan.recv_x[:out["num_recv"]]), out["recv_x"])
 
 
-def test_grid_barrier_wait_times_out_and_context_survives():
-    """The fused kernel's grid barrier: its arrival count is preset from the host to a
-    value no arrival can complete, so every block's bounded wait runs out and the call
-    reports MP_ERR_TIMEOUT; a normal call on a re-zeroed workspace is then exact."""
+@pytest.mark.parametrize("call", ["layout_and_offsets", "layout_dispatch"])
+def test_grid_barrier_wait_times_out_and_context_survives(call):
+    """The fused kernel's grid barrier: the arrival count it waits to reach is moved out
+    of reach from the host (the barrier's base word preset to 2^30 above the count), so
+    every block's bounded wait runs out and the call reports MP_ERR_TIMEOUT; a normal call
+    on a re-zeroed workspace is then exact.  Through mp_layout_dispatch the row copy that
+    follows the timed-out kernel still runs and stays inside its buffers."""
     inp = wl.make_ep(dict(R=4, N=2048, E=16, K=4, H=64, routing="uniform", dtype="bf16"), seed=2)
     plan = EPPlan(inp.R, inp.N, inp.K, inp.E, inp.H)
     plan.load(inp)
     torch.cuda.synchronize()
-    plan.workspace[144:148].copy_(torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8))  # 2^30
+    plan.workspace[148:152].copy_(torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8))  # 2^30
     plan.dev_err.zero_()
     t0 = time.time()
-    B.check(plan.layout_and_offsets())
+    B.check(getattr(plan, call)())
     torch.cuda.synchronize()
     elapsed = time.time() - t0
     assert plan.device_error() & B.MP_ERR_TIMEOUT, plan.device_error()

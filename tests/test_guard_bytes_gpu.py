@@ -62,7 +62,7 @@ def ep_buffers(R, N, K, E, H, cap, x_dtype=torch.bfloat16):
 EP_SHAPES = [(3, 333, 12, 3, 72, None), (4, 300, 16, 4, 1024, None), (2, 129, 8, 2, 256, 0.5)]
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
+@pytest.mark.parametrize("fused", ["fused", "two_calls", "one_call"])
 @pytest.mark.parametrize("shape", EP_SHAPES, ids=lambda s: "R%d_N%d_E%d_K%d_H%d" % s[:5]
                          + ("_cap" if s[5] else ""))
 def test_ep_path_writes_only_its_buffers(shape, fused):
@@ -76,7 +76,12 @@ def test_ep_path_writes_only_its_buffers(shape, fused):
     cap = R * N * min(R, K) if cap_frac is None else int(T * cap_frac)
     g = ep_buffers(R, N, K, E, H, cap)
     t = {k: v.t for k, v in g.items()}
-    if fused:
+    if fused == "one_call":
+        B.check(B.mp_layout_dispatch(
+            R, N, K, E, H, B.MP_BF16, x, None, topk, w, cap, t["ntpr"], t["ntpe"], t["mask"],
+            t["recv_x"], None, t["rsr"], t["rsi"], t["rti"], t["rtw"], t["doff"], t["rp"],
+            t["nrtpe"], t["send"], t["err"], t["ws"]))
+    elif fused == "fused":
         B.check(B.mp_layout_and_offsets(
             R, N, K, E, topk, w, cap, t["ntpr"], t["ntpe"], t["mask"], t["rsr"], t["rsi"],
             t["rti"], t["rtw"], t["doff"], t["rp"], t["nrtpe"], t["send"], t["err"], t["ws"]))
