@@ -18,14 +18,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // Workspace layout (bytes).  A 512-byte control block of counters, then the
 // layout kernel's per-rank count accumulators, then the scan's tile records
 // (a flag word per tile, then the tiles' aggregate counts, then their
-// inclusive prefixes, R words each).  Every region starts on a 256-byte
-// boundary.
+// inclusive prefixes, R words each), then the fused kernel's two rank-totals
+// buffers.  Every region starts on a 256-byte boundary.
 // ---------------------------------------------------------------------------
 struct Control {
   uint32_t scan_tile_counter;  // next scan tile to hand out
   uint32_t scan_done;          // scan blocks finished
   uint32_t scan_epoch;         // tags tile records of the current scan launch
-  uint32_t copy_unit_counter;  // reserved for dynamically scheduled copies
+  uint32_t fused_gen;          // fused layout + scan launches: picks the rank-totals buffer
   uint32_t layout_done[MP_MAX_RANKS];  // layout blocks finished, per source rank
   uint32_t bar_count;          // grid barrier of the fused layout + scan: arrivals (never reset)
   uint32_t bar_base;           // ... and their count when the current launch began
@@ -62,8 +62,15 @@ inline __host__ __device__ int64_t ws_agg_offset(int R, int N, int E) {
 inline __host__ __device__ int64_t ws_incl_offset(int R, int N, int E) {
   return ws_agg_offset(R, N, E) + align256(scan_tiles(R, N) * R * 4);
 }
-inline __host__ __device__ int64_t ws_total_bytes(int R, int N, int E) {
+// rank totals of the fused layout + scan: two buffers of int32
+// [MP_MAX_RANKS][MP_MAX_RANKS], used by alternate launches (a launch adds into
+// one and zeroes the other for the next)
+constexpr int64_t kTotBufInts = int64_t(MP_MAX_RANKS) * MP_MAX_RANKS;
+inline __host__ __device__ int64_t ws_tot_offset(int R, int N, int E) {
   return ws_incl_offset(R, N, E) + align256(scan_tiles(R, N) * R * 4);
+}
+inline __host__ __device__ int64_t ws_total_bytes(int R, int N, int E) {
+  return ws_tot_offset(R, N, E) + 2 * kTotBufInts * 4;
 }
 
 // ---------------------------------------------------------------------------

@@ -474,7 +474,6 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
   if (sh_last && tid == 0) {
     ctl->scan_tile_counter = 0;
     ctl->scan_done = 0;
-    ctl->copy_unit_counter = 0;
     __threadfence();
     atomicAdd(&ctl->scan_epoch, 1u);
   }
@@ -501,6 +500,17 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_scan(ScanArgs a) {
 // mp_layout_dispatch) launch as soon as it starts.
 // ---------------------------------------------------------------------------
 constexpr int kFusedMaxTiles = 16;  // tiles one block may own (tiles <= 16 * grid)
+// Up to this many tiles per source rank, the tiles publish plain aggregate
+// counts before the barrier (and add them into their rank's totals), and after
+// it each tile sums the aggregates of its rank's earlier tiles; beyond it (the
+// C^2 / 2 reads per rank grow) the tiles run the decoupled lookback before the
+// barrier.  Measured (globaltimer, dsv3 shape): with the lookback and its
+// release fences the phase before the barrier took 3.5 us at N = 128 (one tile
+// per rank) and 8-10 us at N = 4096; with aggregates 3.3 and 4.3 us.
+#ifndef MP_FUSED_AGG_MAX_TILES
+#define MP_FUSED_AGG_MAX_TILES 32
+#endif
+constexpr int kFusedAggMaxTiles = MP_FUSED_AGG_MAX_TILES;
 // (the failure-detection test presets the barrier's base word at this offset)
 static_assert(offsetof(Control, bar_count) == 144 && offsetof(Control, bar_base) == 148,
               "grid barrier words of the control block");
@@ -511,6 +521,8 @@ struct FusedArgs {
   int32_t* num_tokens_per_rank;    // [R][R] out
   int32_t* num_tokens_per_expert;  // [R][E] out
   int meta;                        // 1: write the receive metadata too; 0: send_row only
+  int lookback;                    // 1: decoupled lookback before the barrier; 0: aggregates
+                                   // (then rank totals in the accumulators' last R words)
 };
 
 // Grid barrier for a cooperative launch.  bar_count counts arrivals and is
@@ -556,7 +568,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   __shared__ uint8_t row_tok[kScanTokens * MP_MAX_RANKS], row_d[kScanTokens * MP_MAX_RANKS];
   __shared__ int32_t dstart[MP_MAX_RANKS + 1], nok[MP_MAX_RANKS];
   __shared__ uint32_t tile_excl[kFusedMaxTiles][MP_MAX_RANKS];
-  __shared__ uint32_t sh_epoch, sh_gen;
+  __shared__ uint32_t sh_epoch, sh_gen, sh_fgen;
   __shared__ int sh_bad, sh_ok;
 
   const int R = a.R, N = a.N, K = a.K, E = a.E, El = E / R;
@@ -566,31 +578,40 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   uint32_t* agg = reinterpret_cast<uint32_t*>(a.ws + ws_agg_offset(R, N, E));
   uint32_t* incl = reinterpret_cast<uint32_t*>(a.ws + ws_incl_offset(R, N, E));
   int32_t* acc = reinterpret_cast<int32_t*>(a.ws + ws_acc_offset());  // [R][E + R]
+  int32_t* tot = reinterpret_cast<int32_t*>(a.ws + ws_tot_offset(R, N, E));  // [2][32][32]
   const int C = int(scan_tiles_per_rank(N));
   const int T = R * C;
   pdl_launch_dependents();
   // The epoch and barrier base are read first; thread 0 keeps them in
   // registers until the first tile's id loads are issued, so those loads do
   // not wait for them (the first tile's barrier publishes them).
-  uint32_t epoch0 = 0, gen0 = 0;
+  uint32_t epoch0 = 0, gen0 = 0, fgen0 = 0;
   if (tid == 0) {
     epoch0 = ld_relaxed_u32(&ctl->scan_epoch) & 0x3fffffffu;
     gen0 = ld_relaxed_u32(&ctl->bar_base);
+    fgen0 = ld_relaxed_u32(&ctl->fused_gen);
   }
 #if !MP_FUSED_EARLY_LOADS
   if (tid == 0) {
     sh_epoch = epoch0;
     sh_gen = gen0;
+    sh_fgen = fgen0;
     sh_bad = 0;
   }
   __syncthreads();
 #endif
-  // A block that owns a single tile keeps that tile's ids, weights, ballots
-  // and offsets in shared memory across the barrier instead of reloading them.
+  // A block that owns a single tile keeps that tile's ids, weights, ballots,
+  // offsets and masks across the barrier instead of reloading them.
   const bool single = T <= int(gridDim.x);
+  if (!f.lookback)  // summed from the earlier tiles' aggregates after the barrier
+    for (int i = tid; i < kFusedMaxTiles * MP_MAX_RANKS; i += kScanThreads)
+      (&tile_excl[0][0])[i] = 0u;
 
-  // 1. layout work and the per-rank lookback, tile by tile
+  // 1. layout work, and per tile its per-destination counts: published as
+  //    plain aggregates (the barrier publishes them), or with the decoupled
+  //    lookback over the rank's earlier tiles
   int it = 0;
+  uint32_t mask_kept = 0;
   for (int tile = blockIdx.x; tile < T; tile += gridDim.x, ++it) {
     const int s = tile / C, c = tile - s * C;
     const int t0 = c * kScanTokens, ntok = min(kScanTokens, N - t0);
@@ -610,6 +631,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     if (it == 0 && tid == 0) {
       sh_epoch = epoch0;
       sh_gen = gen0;
+      sh_fgen = fgen0;
       sh_bad = 0;
     }
 #endif
@@ -627,6 +649,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       f.is_token_in_rank[g0 + tid] = mask;
       if (bad) sh_bad = 1;
     }
+    mask_kept = mask;
     for (int d = 0; d < R; ++d) {
       const unsigned b = __ballot_sync(kFull, (mask >> d) & 1u);
       if (lane == 0) wball[warp][d] = b;
@@ -636,12 +659,26 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     for (int i = tid; i < E; i += kScanThreads)
       if (hist[i]) atomicAdd(&acc_s[i], hist[i]);
     if (warp == 0) {
-      const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, sh_epoch, wball, woff, tcount,
-                                                  tcnt, flags, agg, incl, a.dev_err);
-      if (lane < R) tile_excl[it][lane] = excl;
+      if (f.lookback) {
+        const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, sh_epoch, wball, woff,
+                                                    tcount, tcnt, flags, agg, incl, a.dev_err);
+        if (lane < R) tile_excl[it][lane] = excl;
+      } else if (lane < R) {  // the tile's count per destination and per-warp offsets
+        uint32_t cnt = 0;
+        for (int w = 0; w < kScanWarps; ++w) {
+          woff[w][lane] = int32_t(cnt);
+          cnt += __popc(wball[w][lane]);
+        }
+        tcnt[lane] = cnt;
+        agg[int64_t(tile) * R + lane] = cnt;
+        // the rank's totals (one tile per rank: the aggregate itself)
+        if (C > 1 && cnt)
+          atomicAdd(&tot[(sh_fgen & 1u) * kTotBufInts + s * MP_MAX_RANKS + lane], int32_t(cnt));
+      }
     }
     __syncthreads();  // hist, idx_s and the ballots are reused by the next tile
   }
+  const int nown = it;  // tiles this block owns
   if (tid == 0 && sh_bad) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
 
   // 2. every tile is published and every expert count added
@@ -650,10 +687,85 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     return;
   }
 
-  // 3. totals, tables, rows
-  for (int i = tid; i < R * R; i += kScanThreads) {  // rank s's last tile: its totals
-    const int s = i / R, d = i - s * R;
-    ntpr_s[i] = int32_t(__ldcg(incl + (int64_t(s) * C + C - 1) * R + d));
+  // 3. totals, tables, rows.  The lower half of the block gathers the
+  //    per-destination counts, the upper half (in the last blocks of the grid,
+  //    so that block 0's tables do not add up) the expert counts: both start
+  //    their loads at once.
+  constexpr int kHalf = kScanThreads / 2;
+  if (tid < kHalf) {
+    if (f.lookback) {
+      for (int i = tid; i < R * R; i += kHalf) {  // rank s's last tile: its totals
+        const int s = i / R, d = i - s * R;
+        ntpr_s[i] = int32_t(__ldcg(incl + (int64_t(s) * C + C - 1) * R + d));
+      }
+    } else {
+      // the rank totals (from this launch's totals buffer, or with one tile
+      // per rank its aggregate), and for each of this block's tiles the
+      // per-destination counts of its rank's earlier tiles, summed in shared
+      // memory (integer adds: their order does not matter).  Items [0, R*R)
+      // are the totals, then each own tile's c*R earlier counts; 16 loads are
+      // in flight before they are added.
+      int n_items = R * R;
+      for (int q = 0; q < nown; ++q) n_items += ((int(blockIdx.x) + q * int(gridDim.x)) % C) * R;
+      constexpr int kB = 16;
+      for (int i0 = tid; i0 < n_items; i0 += kHalf * kB) {
+        uint32_t v[kB];
+        int dst[kB];  // < R*R: ntpr_s index; R*R + k: tile_excl entry k; -1: none
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = i0 + j * kHalf;
+          v[j] = 0u;
+          dst[j] = -1;
+          if (i >= n_items) continue;
+          if (i < R * R) {
+            const int s = i / R, d = i - s * R;
+            v[j] = C == 1 ? __ldcg(agg + i)
+                          : uint32_t(__ldcg(tot + (sh_fgen & 1u) * kTotBufInts +
+                                            s * MP_MAX_RANKS + d));
+            dst[j] = i;
+          } else {
+            int r = i - R * R;
+            for (int q = 0; q < nown; ++q) {  // the own tile this item belongs to
+              const int own = int(blockIdx.x) + q * int(gridDim.x);
+              const int span = (own % C) * R;
+              if (r < span) {
+                const int c = r / R, d = r - c * R;
+                v[j] = __ldcg(agg + (int64_t(own - own % C) + c) * R + d);
+                dst[j] = R * R + q * MP_MAX_RANKS + d;
+                break;
+              }
+              r -= span;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          if (dst[j] < 0) continue;
+          if (dst[j] < R * R) ntpr_s[dst[j]] = int32_t(v[j]);
+          else if (v[j]) atomicAdd(&tile_excl[0][0] + (dst[j] - R * R), v[j]);
+        }
+      }
+    }
+  } else {
+    for (int64_t e = int64_t(gridDim.x - 1 - blockIdx.x) * kHalf + (tid - kHalf); e < E;
+         e += int64_t(gridDim.x) * kHalf) {
+      int sum = 0;
+      for (int s0 = 0; s0 < R; s0 += 8) {  // 8 loads in flight before their stores
+        int v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v[j] = s0 + j < R ? __ldcg(acc + int64_t(s0 + j) * (E + R) + e) : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (s0 + j < R) {
+            acc[int64_t(s0 + j) * (E + R) + e] = 0;
+            f.num_tokens_per_expert[int64_t(s0 + j) * E + e] = v[j];
+            sum += v[j];
+          }
+        }
+      }
+      a.num_recv_tokens_per_expert[e] = sum;
+    }
   }
   __syncthreads();
   if (warp == 0) {  // first receive row of each destination
@@ -680,30 +792,14 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       f.num_tokens_per_rank[i] = ntpr_s[i];
       a.rank_prefix[i] = pre;
     }
+    // the other totals buffer, zero for the next launch (nothing uses it in this one)
+    int32_t* next = tot + ((sh_fgen + 1u) & 1u) * kTotBufInts;
+    for (int i = tid; i < int(kTotBufInts); i += kScanThreads) next[i] = 0;
     if (tid == 0) {
       atomicAdd(&ctl->scan_epoch, 1u);  // every lookback of this launch is done
       ctl->bar_base = sh_gen + gridDim.x;  // every arrival of this launch is in
+      ctl->fused_gen = sh_fgen + 1u;
     }
-  }
-  // (the last blocks of the grid, so that block 0's tables do not add up)
-  for (int64_t e = int64_t(gridDim.x - 1 - blockIdx.x) * kScanThreads + tid; e < E;
-       e += int64_t(gridDim.x) * kScanThreads) {
-    int sum = 0;
-    for (int s0 = 0; s0 < R; s0 += 8) {  // 8 loads in flight before their stores
-      int v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = s0 + j < R ? __ldcg(acc + int64_t(s0 + j) * (E + R) + e) : 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (s0 + j < R) {
-          acc[int64_t(s0 + j) * (E + R) + e] = 0;
-          f.num_tokens_per_expert[int64_t(s0 + j) * E + e] = v[j];
-          sum += v[j];
-        }
-      }
-    }
-    a.num_recv_tokens_per_expert[e] = sum;
   }
   __syncthreads();
   it = 0;
@@ -711,7 +807,8 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     const int s = tile / C, c = tile - s * C;
     const int t0 = c * kScanTokens, ntok = min(kScanTokens, N - t0);
     const int64_t g0 = int64_t(s) * N + t0;
-    const uint32_t mask = tid < ntok ? __ldcg(f.is_token_in_rank + g0 + tid) : 0u;
+    const uint32_t mask =
+        single ? mask_kept : (tid < ntok ? __ldcg(f.is_token_in_rank + g0 + tid) : 0u);
     if (!single) {  // ids, weights, ballots and offsets of this tile
       if (f.meta) {
         const int n = ntok * K;
@@ -743,8 +840,28 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       row_base[lane] = dest_base[lane] + pre + tile_excl[it][lane];
     }
     __syncthreads();
-    write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s,
-                    TileRowsSmem{sr_s, row_tok, row_d, dstart, nok}, f.meta != 0);
+    if (f.meta) {
+      write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s,
+                      TileRowsSmem{sr_s, row_tok, row_d, dstart, nok});
+    } else {
+      // send_row only: each token's thread writes its R entries (the receive
+      // metadata is written by the row copy)
+      bool over = false;
+      if (tid < ntok) {
+        int32_t* dst = a.send_row + (g0 + tid) * R;
+        for (int d = 0; d < R; ++d) {
+          int32_t v = -1;
+          if ((mask >> d) & 1u) {
+            const int64_t row =
+                row_base[d] + woff[warp][d] + __popc(wball[warp][d] & lanemask_lt());
+            if (row < a.recv_capacity) v = int32_t(row);
+            else over = true;
+          }
+          dst[d] = v;
+        }
+      }
+      if (__any_sync(kFull, over) && lane == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
+    }
     __syncthreads();
   }
 }
@@ -1113,7 +1230,8 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                        num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx,
                        recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
                        num_recv_tokens_per_expert, send_row, dev_err, ws, 0, -1},
-              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert, meta};
+              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert, meta,
+              scan_tiles_per_rank(N) > kFusedAggMaxTiles ? 1 : 0};
   void* args[] = {&f};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mp_k_layout_scan),
                                      dim3(unsigned(grid)), dim3(kScanThreads), args, smem,

@@ -412,8 +412,8 @@ int mp_allgatherv(int R, int64_t row_bytes, const int64_t *sizes, const void *in
  *    from mp_layout, which still takes a caller-allocated workspace (a caller
  *    may also compute them by other means).
  *  - Limit: problems whose mp_workspace_size(R, N, E) exceeds
- *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with E=256 that allows up to 244,608
- *    tokens per rank at R=8 and 15,488 at R=32) are rejected with
+ *    MP_NOALLOC_SCRATCH_BYTES (1 MiB; with E=256 that allows up to 242,688
+ *    tokens per rank at R=8 and 15,360 at R=32) are rejected with
  *    MP_ERR_INVALID_ARG before anything is launched; use mp_dispatch with a
  *    workspace for those.  Every other argument is checked as by mp_dispatch,
  *    also before anything is put on the stream.
