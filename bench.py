@@ -5,8 +5,8 @@ One step = mp_layout_dispatch (layout + receive offsets in one cooperative
 launch, then the row copy launched as its programmatic dependent) + mp_combine
 (launched as the copy's programmatic dependent) on the DeepSeek-V3-shaped workload
 (R=8 logical ranks x N=4096 tokens, H=7168 bf16, E=256 experts, top-8 uniform
-routing), the combine input being the dispatched rows themselves (identity
-experts).  Inputs are synthetic and
+routing), the combine input being synthetic expert outputs, one bf16 row per
+receive row, in a buffer of their own.  Inputs are synthetic and
 seeded, resident in HBM for the device-timed value; the e2e value adds the
 host->device copy of the step's inputs and the device->host copy of its
 result, from/to pinned host memory.
@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
@@ -257,12 +258,13 @@ def reference_arm(args):
 
 def config_block(name, inp):
     return {"workload": "%s: R=%d logical ranks x N=%d tokens, H=%d %s, E=%d experts, top-%d %s "
-                        "routing; layout -> dispatch -> combine of the dispatched rows"
+                        "routing; layout -> dispatch -> combine of synthetic expert outputs"
                         % (name, inp.R, inp.N, inp.H, inp.dtype, inp.E, inp.K,
                            inp.meta.get("routing", "uniform")),
             "R": inp.R, "N": inp.N, "H": inp.H, "E": inp.E, "K": inp.K,
             "global_batch": inp.R * inp.N,
-            "l2": "inputs larger than L2 (x %.0f MB, receive rows ~%.0f MB vs 129 MB L2)"
+            "l2": "inputs larger than L2 (x %.0f MB, receive rows and expert outputs ~%.0f MB "
+                  "each vs 129 MB L2)"
                   % (inp.R * inp.N * inp.row_bytes / 1e6,
                      inp.R * inp.N * inp.row_bytes * 5.3 / 1e6),
             "parallelism": "replicas"}
@@ -439,23 +441,13 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
     del rp, qx, qd, qs, qso
     torch.cuda.empty_cache()
 
-    # low-latency expert-major layout at the pages' small-batch shape (R=8, N=128,
-    # H=7168, top-8 of 256): LL offsets + LL rows -> weighted LL combine, launched one
-    # by one and replayed as one CUDA graph
-    R, N, H, E, K = 8, 128, 7168, 256, 8
-    rng = np.random.default_rng(1)
-    plan = EPPlan(R, N, K, E, H, "bf16")
-    plan.topk_idx.copy_(torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K)))
-    plan.topk_weights.copy_(torch.from_numpy(wl.softmax_weights(rng, R, N, K)))
-    plan.x.copy_(torch.randn((R, N, H), generator=g, device="cuda").to(torch.bfloat16))
-    cap = R * N * K
-    eoff = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-    esoff = torch.empty((E, R), dtype=torch.int32, device="cuda")
-    src = torch.empty(cap, dtype=torch.int32, device="cuda")
-    slot = torch.empty((R, N, K), dtype=torch.int32, device="cuda")
-    rx = torch.empty((cap, H), dtype=torch.bfloat16, device="cuda")
-    yl = torch.randn((cap, H), generator=g, device="cuda").to(torch.bfloat16)
-    lo = torch.empty((R, N, H), dtype=torch.bfloat16, device="cuda")
+    # Small problems fit in L2 (129 MB), so they rotate through P buffer sets whose
+    # combined size is several times L2: a set's inputs and expert outputs have been
+    # evicted by the time it is used again, and each kernel reads from HBM.
+    L2_BYTES = 129e6
+
+    def n_sets(bytes_per_set):
+        return max(2, 1 + int(math.ceil(3 * L2_BYTES / bytes_per_set)))
 
     s_cap = torch.cuda.Stream()
 
@@ -469,114 +461,167 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
             fn()
         return gr
 
-    def phases(calls, names):  # per-call CUDA-event times, us
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-               for _ in range(steps)]
-        for ev in evs:
+    def phases(sets, calls, names, n):  # per-call CUDA-event times, us
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+               for _ in range(n)]
+        for i, ev in enumerate(evs):
+            st = sets[i % len(sets)]
             ev[0].record()
             for c, call in enumerate(calls):
-                call()
+                call(st)
                 ev[c + 1].record()
         torch.cuda.synchronize()
-        return {nm: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / steps * 1e3
+        return {nm: sum(ev[c].elapsed_time(ev[c + 1]) for ev in evs) / n * 1e3
                 for c, nm in enumerate(names)}
+
+    # low-latency expert-major layout at the pages' small-batch shape (R=8, N=128,
+    # H=7168, top-8 of 256): LL offsets + LL rows -> weighted LL combine, launched one
+    # by one and replayed as one CUDA graph
+    R, N, H, E, K = 8, 128, 7168, 256, 8
+    cap = R * N * K
+    rng = np.random.default_rng(1)
+    topk_ll = torch.from_numpy(wl.topk_uniform(rng, R * N, E, K).reshape(R, N, K))
+    w_ll = torch.from_numpy(wl.softmax_weights(rng, R, N, K))
+    ll_set_bytes = R * N * H * 2 * 2 + cap * H * 2 * 2
+    ll_sets = []
+    for _ in range(n_sets(ll_set_bytes)):
+        plan = EPPlan(R, N, K, E, H, "bf16")
+        plan.topk_idx.copy_(topk_ll)
+        plan.topk_weights.copy_(w_ll)
+        plan.x.normal_(generator=g)
+        ll_sets.append(dict(
+            plan=plan, eoff=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+            esoff=torch.empty((E, R), dtype=torch.int32, device="cuda"),
+            doff=torch.empty(R + 1, dtype=torch.int32, device="cuda"),
+            dsoff=torch.empty((R, R), dtype=torch.int32, device="cuda"),
+            src=torch.empty(cap, dtype=torch.int32, device="cuda"),
+            slot=torch.empty((R, N, K), dtype=torch.int32, device="cuda"),
+            rx=torch.empty((cap, H), dtype=torch.bfloat16, device="cuda"),
+            yl=torch.randn((cap, H), generator=g, device="cuda").to(torch.bfloat16),
+            lo=torch.empty((R, N, H), dtype=torch.bfloat16, device="cuda")))
 
     ll_bytes = (R * N * K * 8 + cap * 4 + (E + 1) * 4 + E * R * 4  # LL offsets
                 + R * N * H * 2 + cap * H * 2 + R * N * K * 4           # LL rows
                 + cap * H * 2 + R * N * K * 8 + R * N * H * 2)          # weighted LL combine
 
+    def ll_dispatch(st, rank_major=0):
+        p = st["plan"]
+        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, rank_major, p.x, None, p.topk_idx,
+                                 None, cap, st["doff"] if rank_major else st["eoff"],
+                                 st["dsoff"] if rank_major else st["esoff"], st["src"],
+                                 st["slot"], st["rx"], None, p.dev_err))
+
+    def ll_combine(st):
+        p = st["plan"]
+        B.check(B.mp_combine_ll(R, N, K, H, st["yl"], cap, st["slot"], p.topk_weights, st["lo"],
+                                p.dev_err))
+
+    def ll_offsets(st):
+        p = st["plan"]
+        B.check(B.mp_dispatch_ll_offsets(R, N, K, E, p.topk_idx, None, cap, st["eoff"],
+                                         st["esoff"], st["src"], st["slot"], p.dev_err))
+
+    def ll_rows(st):
+        p = st["plan"]
+        B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, p.x, None, st["slot"], cap,
+                                      st["rx"], None))
+
+    def over_sets(sets, *calls):
+        def run():
+            for st in sets:
+                for c in calls:
+                    c(st)
+        return run
+
+    def ll_errors():
+        return sum(st["plan"].device_error() for st in ll_sets)
+
+    P = len(ll_sets)
     # one call for the LL offsets and rows (the sort, then the row copy as its
-    # programmatic dependent), then the weighted combine
-    ll_calls = [
-        lambda: B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None,
-                                         plan.topk_idx, None, cap, eoff, esoff, src, slot, rx,
-                                         None, plan.dev_err)),
-        lambda: B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo,
-                                        plan.dev_err))]
-
-    def ll_step():
-        for c in ll_calls:
-            c()
-
-    ms_ll = timed(ll_step, steps)
-    ll_phase_us = phases(ll_calls, ("dispatch_ll", "combine_ll"))
-    graph = as_graph(ll_step)
-    ms_llg = timed(graph.replay, steps)
-    assert plan.device_error() == 0
+    # programmatic dependent), then the weighted combine (the copy's dependent)
+    ms_ll = timed(over_sets(ll_sets, ll_dispatch, ll_combine), max(1, steps // P)) / P
+    ll_phase_us = phases(ll_sets, [ll_dispatch, ll_combine], ("dispatch_ll", "combine_ll"), steps)
+    graph = as_graph(over_sets(ll_sets, ll_dispatch, ll_combine))
+    ms_llg = timed(graph.replay, max(1, steps // P)) / P
+    assert ll_errors() == 0
     out["low_latency_step_n128"] = dict(
         row(ms_ll, ll_bytes), us_per_step=ms_ll * 1e3, us_per_step_cuda_graph=ms_llg * 1e3,
-        phases_us=ll_phase_us, receive_rows=int(cap),
+        phases_us=ll_phase_us, receive_rows=int(cap), buffer_sets=P,
         GBs_cuda_graph=ll_bytes / (ms_llg / 1e3) / 1e9,
         workload="R=8, N=128, H=7168 bf16, E=256, top-8: mp_dispatch_ll (LL offsets counting "
                  "the experts themselves, then the LL rows as a programmatic dependent) + "
-                 "weighted LL combine")
+                 "weighted LL combine of synthetic expert outputs; %d buffer sets in turn "
+                 "(L2 never holds a set's inputs)" % P)
 
     # the same step as three calls: LL offsets, LL rows, weighted combine
-    ll3_calls = [
-        lambda: B.check(B.mp_dispatch_ll_offsets(R, N, K, E, plan.topk_idx, None, cap, eoff,
-                                                 esoff, src, slot, plan.dev_err)),
-        lambda: B.check(B.mp_dispatch_ll_rows(R, N, K, H, B.MP_BF16, plan.x, None, slot, cap,
-                                              rx, None)),
-        ll_calls[1]]
-
-    def ll3_step():
-        for c in ll3_calls:
-            c()
-
-    ms_ll3 = timed(ll3_step, steps)
-    ll3_phase_us = phases(ll3_calls, ("ll_offsets", "ll_rows", "combine_ll"))
-    graph3 = as_graph(ll3_step)
-    ms_ll3g = timed(graph3.replay, steps)
-    assert plan.device_error() == 0
+    ms_ll3 = timed(over_sets(ll_sets, ll_offsets, ll_rows, ll_combine), max(1, steps // P)) / P
+    ll3_phase_us = phases(ll_sets, [ll_offsets, ll_rows, ll_combine],
+                          ("ll_offsets", "ll_rows", "combine_ll"), steps)
+    graph3 = as_graph(over_sets(ll_sets, ll_offsets, ll_rows, ll_combine))
+    ms_ll3g = timed(graph3.replay, max(1, steps // P)) / P
+    assert ll_errors() == 0
     out["low_latency_three_calls_step_n128"] = dict(
         row(ms_ll3, ll_bytes), us_per_step=ms_ll3 * 1e3, us_per_step_cuda_graph=ms_ll3g * 1e3,
         phases_us=ll3_phase_us, GBs_cuda_graph=ll_bytes / (ms_ll3g / 1e3) / 1e9,
         workload="as low_latency_step_n128 with the LL offsets and the LL rows as two calls "
-                 "(3 launches, no overlap)")
-    doff = torch.empty(R + 1, dtype=torch.int32, device="cuda")
-    dsoff = torch.empty((R, R), dtype=torch.int32, device="cuda")
+                 "(3 launches)")
 
-    def ll_rm_step():  # rank-major output: rows grouped by the rank owning the expert
-        B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 1, plan.x, None, plan.topk_idx,
-                                 None, cap, doff, dsoff, src, slot, rx, None, plan.dev_err))
-        B.check(B.mp_combine_ll(R, N, K, H, yl, cap, slot, plan.topk_weights, lo, plan.dev_err))
+    def ll_dispatch_rm(st):
+        ll_dispatch(st, rank_major=1)
 
-    ms_rm = timed(ll_rm_step, steps)
-    assert plan.device_error() == 0
+    ms_rm = timed(over_sets(ll_sets, ll_dispatch_rm, ll_combine), max(1, steps // P)) / P
+    assert ll_errors() == 0
     rm_bytes = ll_bytes - (E + 1) * 4 - E * R * 4 + (R + 1) * 4 + R * R * 4
     out["low_latency_rank_major_step_n128"] = dict(
         row(ms_rm, rm_bytes), us_per_step=ms_rm * 1e3,
         workload="as low_latency_step_n128 with rank-major output (rows grouped by the rank "
                  "owning the expert)")
-    del plan, rx, yl, lo, graph, graph3
+    del ll_sets, graph, graph3
     torch.cuda.empty_cache()
 
     # the DeepSeek-V3 shape at small batches (the pages' EP bench defaults to 128 tokens
-    # per rank): the step as timed above (one-call dispatch + combine, launched one by
-    # one), as three calls, and replayed as a CUDA graph
+    # per rank): the step as timed above (one-call dispatch + combine of synthetic expert
+    # outputs, launched one by one), as three calls, and replayed as a CUDA graph
     for nb_tok in (128, 512, 1024):
         inp = wl.make_ep("dsv3", seed=0, N=nb_tok)
         R, N, H, E, K = inp.R, inp.N, inp.H, inp.E, inp.K
-        plan = EPPlan(R, N, K, E, H, "bf16")
-        plan.load(inp)
-        del inp
-        plan.step()
+        sets = []
+        probe = EPPlan(R, N, K, E, H, "bf16")
+        probe.load(inp)
+        B.check(probe.layout_dispatch())
         torch.cuda.synchronize()
-        T = plan.num_recv()
-        ms1 = timed(plan.step, steps)
-        ms3 = timed(plan.step_three_calls, steps)
-        graph = as_graph(plan.step)
-        msg = timed(graph.replay, steps)
-        assert plan.device_error() == 0
+        T = probe.num_recv()
+        del probe
+        nsets = n_sets(R * N * H * 2 * 2 + T * H * 2 * 2)
+        for _ in range(nsets):
+            plan = EPPlan(R, N, K, E, H, "bf16")
+            plan.load(inp)
+            sets.append(dict(plan=plan, y=torch.randn((T, H), generator=g, device="cuda")
+                             .to(torch.bfloat16)))
+        del inp
+
+        def one(st):
+            st["plan"].step(st["y"])
+
+        def three(st):
+            st["plan"].step_three_calls(st["y"])
+
+        P = len(sets)
+        ms1 = timed(over_sets(sets, one), max(1, steps // P)) / P
+        ms3 = timed(over_sets(sets, three), max(1, steps // P)) / P
+        graph = as_graph(over_sets(sets, one))
+        msg = timed(graph.replay, max(1, steps // P)) / P
+        assert sum(st["plan"].device_error() for st in sets) == 0
         ab = algorithmic_bytes(R, N, K, E, H, T)
         nbytes = ab["layout"] + ab["dispatch"] + ab["combine"]
         out["dsv3_small_batch_n%d" % nb_tok] = dict(
             row(ms1, nbytes), us_per_step=ms1 * 1e3, tokens_per_s=R * N / (ms1 / 1e3),
             us_per_step_three_calls=ms3 * 1e3, us_per_step_cuda_graph=msg * 1e3,
-            GBs_cuda_graph=nbytes / (msg / 1e3) / 1e9, receive_rows=T,
-            workload="dsv3 shape at N=%d tokens per rank: mp_layout_dispatch + mp_combine "
-                     "(identity experts), eager" % N)
-        del plan, graph
+            GBs_cuda_graph=nbytes / (msg / 1e3) / 1e9, receive_rows=T, buffer_sets=P,
+            workload="dsv3 shape at N=%d tokens per rank: mp_layout_dispatch + mp_combine of "
+                     "synthetic expert outputs, eager; %d buffer sets in turn (L2 never holds "
+                     "a set's inputs)" % (N, P))
+        del sets, graph
     torch.cuda.empty_cache()
 
     # the skewed workload: Zipf(1.2) routing, rank 0 hot
@@ -642,12 +687,16 @@ def main():
     plan = EPPlan(R, N, K, E, H, inp.dtype)
     plan.load(inp)
     torch.cuda.synchronize()
-    y = None
-    if inp.dtype != "bf16":  # e4m3 dispatch, bf16 combine of synthetic expert outputs
-        B.check(plan.layout())
-        B.check(plan.dispatch())
-        torch.cuda.synchronize()
-        y = wl.gathered_bf16(plan.num_recv(), H, seed=args.seed + 1).cuda()
+    # the combine's input: synthetic expert outputs (bf16, one per receive row) in a
+    # buffer of their own, so that the combine reads HBM rather than the rows the
+    # dispatch has just written (some of which would still be in L2)
+    B.check(plan.layout_dispatch())
+    torch.cuda.synchronize()
+    y = torch.empty((max(plan.num_recv(), 1), H), dtype=torch.bfloat16, device="cuda")
+    gy = torch.Generator(device="cuda").manual_seed(args.seed + 1)
+    for r0 in range(0, y.shape[0], 16384):  # in slices: no full-size fp32 temporary
+        y[r0:r0 + 16384].copy_(torch.randn((min(16384, y.shape[0] - r0), H), generator=gy,
+                                           device="cuda"))
     stream = torch.cuda.current_stream()
 
     # warm-up (also checks the run is error-free)

@@ -250,7 +250,15 @@ int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t* topk_idx,
   if (st != MP_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  const cudaError_t e = launch_layout_scan(
+  // small batches: one thread-block cluster; else one cooperative grid; else two launches
+  cudaError_t e = launch_layout_cluster(
+      R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
+      num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
+      recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
+      cs, /*meta=*/1);
+  if (e == cudaSuccess) return MP_OK;
+  if (e != cudaErrorNotSupported) return MP_ERR_CUDA;
+  e = launch_layout_scan(
       R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
       num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
       recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
@@ -293,13 +301,20 @@ int mp_layout_dispatch(int R, int N, int K, int E, int H, int dtype, const void*
   const bool fp8 = dtype == MP_E4M3;
   const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
   const int spr = fp8 ? H / MP_SCALE_BLOCK : 0;
-  // one cooperative launch for layout + offsets (receive metadata left out),
-  // then the row copy, which writes the metadata, as its programmatic dependent
-  const cudaError_t e = launch_layout_scan(
+  // one launch for layout + offsets (receive metadata left out: a thread-block
+  // cluster for small batches, else a cooperative grid), then the row copy,
+  // which writes the metadata, as its programmatic dependent
+  cudaError_t e = launch_layout_cluster(
       R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
       num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
       recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,
-      ws, cs, /*meta=*/0);
+      cs, /*meta=*/0);
+  if (e == cudaErrorNotSupported)
+    e = launch_layout_scan(
+        R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
+        num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
+        recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row,
+        dev_err, ws, cs, /*meta=*/0);
   if (e == cudaSuccess)
     return cuda_status(launch_dispatch_after_offsets(
         R, N, K, E, row_bytes, x, recv_x, recv_capacity, send_row, spr, x_scales, recv_scales,

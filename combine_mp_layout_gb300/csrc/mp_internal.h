@@ -54,6 +54,20 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                                int32_t* send_row, int32_t* dev_err, unsigned char* ws,
                                cudaStream_t stream, int meta = 1);
 
+// Layout + offsets for small batches (R <= 16, N <= MP_CLUSTER_MAX_TOKENS) in
+// one thread-block cluster, one CTA per source rank, exchanging counts through
+// distributed shared memory (no workspace); cudaErrorNotSupported (nothing
+// launched) when the shape or the device does not suit it.  meta as above.
+cudaError_t launch_layout_cluster(int R, int N, int K, int E, const int32_t* topk_idx,
+                                  const float* topk_weights, int64_t recv_capacity,
+                                  int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                  uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+                                  int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                                  float* recv_topk_weights, int32_t* dest_offsets,
+                                  int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                                  int32_t* send_row, int32_t* dev_err, cudaStream_t stream,
+                                  int meta);
+
 // The row copy of mp_layout_dispatch, launched as the programmatic dependent of
 // the fused layout + offsets kernel right before it on the stream: its first
 // row loads (and the tokens' top-k ids and weights) overlap that kernel, its

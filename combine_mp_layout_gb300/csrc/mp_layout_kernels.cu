@@ -520,9 +520,6 @@ struct FusedArgs {
   uint32_t* is_token_in_rank;      // [R][N] out
   int32_t* num_tokens_per_rank;    // [R][R] out
   int32_t* num_tokens_per_expert;  // [R][E] out
-  int meta;                        // 1: write the receive metadata too; 0: send_row only
-  int lookback;                    // 1: decoupled lookback before the barrier; 0: aggregates
-                                   // (then rank totals in the accumulators' last R words)
 };
 
 // Grid barrier for a cooperative launch.  bar_count counts arrivals and is
@@ -551,6 +548,13 @@ __device__ __forceinline__ bool grid_barrier(Control* ctl, uint32_t nblocks, uin
   return *ok_s != 0;
 }
 
+// META: also write the receive metadata (else send_row only: the row copy of
+// mp_layout_dispatch writes the metadata).  LOOKBACK: the decoupled lookback
+// before the barrier (more than kFusedAggMaxTiles tiles per rank), else plain
+// aggregates and rank totals.  Both are compile-time so that each launched
+// instance holds only its own code: the kernel runs once per block, and its
+// instructions are fetched cold.
+template <bool META, bool LOOKBACK>
 __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   const ScanArgs& a = f.a;
   extern __shared__ int32_t sm_scan[];
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   // A block that owns a single tile keeps that tile's ids, weights, ballots,
   // offsets and masks across the barrier instead of reloading them.
   const bool single = T <= int(gridDim.x);
-  if (!f.lookback)  // summed from the earlier tiles' aggregates after the barrier
+  if (!LOOKBACK)  // summed from the earlier tiles' aggregates after the barrier
     for (int i = tid; i < kFusedMaxTiles * MP_MAX_RANKS; i += kScanThreads)
       (&tile_excl[0][0])[i] = 0u;
 
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
 #pragma unroll 4
       for (int i = tid; i < n; i += kScanThreads) {
         idx_s[i] = __ldg(gi + i);
-        if (single && f.meta) w_s[i] = __ldg(gw + i);
+        if (META && single) w_s[i] = __ldg(gw + i);
       }
     }
 #if MP_FUSED_EARLY_LOADS
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     for (int i = tid; i < E; i += kScanThreads)
       if (hist[i]) atomicAdd(&acc_s[i], hist[i]);
     if (warp == 0) {
-      if (f.lookback) {
+      if constexpr (LOOKBACK) {
         const uint32_t excl = tile_publish_lookback(R, tile, c, s, C, sh_epoch, wball, woff,
                                                     tcount, tcnt, flags, agg, incl, a.dev_err);
         if (lane < R) tile_excl[it][lane] = excl;
@@ -693,7 +697,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
   //    their loads at once.
   constexpr int kHalf = kScanThreads / 2;
   if (tid < kHalf) {
-    if (f.lookback) {
+    if constexpr (LOOKBACK) {
       for (int i = tid; i < R * R; i += kHalf) {  // rank s's last tile: its totals
         const int s = i / R, d = i - s * R;
         ntpr_s[i] = int32_t(__ldcg(incl + (int64_t(s) * C + C - 1) * R + d));
@@ -810,7 +814,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
     const uint32_t mask =
         single ? mask_kept : (tid < ntok ? __ldcg(f.is_token_in_rank + g0 + tid) : 0u);
     if (!single) {  // ids, weights, ballots and offsets of this tile
-      if (f.meta) {
+      if constexpr (META) {
         const int n = ntok * K;
         const int32_t* gi = a.topk_idx + g0 * K;
         const float* gw = a.topk_weights + g0 * K;
@@ -840,7 +844,7 @@ __global__ void __launch_bounds__(kScanThreads) mp_k_layout_scan(FusedArgs f) {
       row_base[lane] = dest_base[lane] + pre + tile_excl[it][lane];
     }
     __syncthreads();
-    if (f.meta) {
+    if constexpr (META) {
       write_tile_rows(a, mask, ntok, t0, g0, s, wball, woff, row_base, tcnt, idx_s, w_s,
                       TileRowsSmem{sr_s, row_tok, row_d, dstart, nok});
     } else {
@@ -1119,6 +1123,244 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
       bin_src_offsets, recv_src_token, slot_row, dev_err, ll_smem, warp_sums);
 }
 
+
+// ---------------------------------------------------------------------------
+// Layout and receive offsets for small batches in one thread-block cluster
+// (mp_layout_and_offsets / mp_layout_dispatch when R <= 16 and N is at most
+// MP_CLUSTER_MAX_TOKENS): CTA s of an R-CTA cluster takes source rank s whole.
+//  1. in rounds of 1024 tokens: each token's rank mask (is_token_in_rank), the
+//     rank's expert histogram in shared memory and, per (round, warp), a ballot
+//     per destination; one warp per destination scans the ballots' counts,
+//     which places every token among the rank's rows for that destination and
+//     gives the rank's total per destination;
+//  2. cluster barrier; each CTA reads the other ranks' totals, and for the
+//     experts its rank owns their counts, from those CTAs' shared memory
+//     (distributed shared memory): no global round trip, no workspace;
+//  3. the tables, send_row (and with META the receive metadata);
+//  4. a second cluster barrier keeps every CTA's shared memory alive until the
+//     others have read it.
+// Every thread reaches both cluster barriers (there is no early exit).
+// ---------------------------------------------------------------------------
+constexpr int kClThreads = 1024;
+constexpr int kClWarps = kClThreads / kWarp;
+constexpr int kClMaxRounds = 4;  // tokens per rank <= 4096
+constexpr int kClMaxRanks = 16;  // a cluster of at most 16 CTAs
+
+struct ClusterArgs {
+  int R, N, K, E;
+  const int32_t* topk_idx;
+  const float* topk_weights;
+  int64_t recv_capacity;
+  uint32_t* is_token_in_rank;
+  int32_t* num_tokens_per_rank;
+  int32_t* num_tokens_per_expert;
+  int32_t* recv_src_rank;
+  int32_t* recv_src_idx;
+  int32_t* recv_topk_idx;
+  float* recv_topk_weights;
+  int32_t* dest_offsets;
+  int32_t* rank_prefix;
+  int32_t* num_recv_tokens_per_expert;
+  int32_t* send_row;
+  int32_t* dev_err;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: writes before it (shared and
+// global) are visible to the cluster's threads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The 32-bit word at shared-memory address `p` of CTA `rank` of the cluster.
+__device__ __forceinline__ int32_t ld_peer_smem(const void* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  int32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <bool META>
+__global__ void __launch_bounds__(kClThreads, 1) mp_k_layout_cluster(ClusterArgs a) {
+  extern __shared__ int32_t cl_hist[];  // [E]: this rank's expert counts (read by peers)
+  __shared__ uint32_t ball[kClMaxRounds][kClWarps][kClMaxRanks];
+  __shared__ int32_t woff[kClMaxRounds][kClWarps][kClMaxRanks];
+  __shared__ int32_t tot[kClMaxRanks];  // this rank's rows per destination (read by peers)
+  __shared__ int32_t ntpr[kClMaxRanks * kClMaxRanks];
+  __shared__ int64_t row_base[kClMaxRanks];
+  __shared__ int sh_bad;
+  const int R = a.R, N = a.N, K = a.K, E = a.E, El = E / R;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = int(cluster_ctarank());
+  pdl_launch_dependents();
+  const int rounds = (N + kClThreads - 1) / kClThreads;
+
+  // 1. the ids of every round first (8 per token and round in flight), then
+  //    the counting
+  int ids[kClMaxRounds][8];
+#pragma unroll
+  for (int r = 0; r < kClMaxRounds; ++r) {
+    const int t = r * kClThreads + tid;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      ids[r][j] = (r < rounds && t < N && j < K) ? __ldg(a.topk_idx + (int64_t(s) * N + t) * K + j)
+                                                 : -1;
+  }
+  for (int e = tid; e < E; e += kClThreads) cl_hist[e] = 0;
+  if (tid == 0) sh_bad = 0;
+  __syncthreads();
+  bool bad = false;
+  uint32_t masks[kClMaxRounds];
+#pragma unroll
+  for (int r = 0; r < kClMaxRounds; ++r) {
+    masks[r] = 0u;
+    if (r >= rounds) continue;
+    const int t = r * kClThreads + tid;
+    if (t < N) {
+      uint32_t m = 0u;
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        int e8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          e8[j] = k0 == 0 ? ids[r][j]
+                          : (k0 + j < K ? __ldg(a.topk_idx + (int64_t(s) * N + t) * K + k0 + j)
+                                        : -1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e = e8[j];
+          if (k0 + j >= K || e == -1) continue;
+          if (e < -1 || e >= E) { bad = true; continue; }
+          atomicAdd(&cl_hist[e], 1);
+          m |= 1u << (e / El);
+        }
+      }
+      masks[r] = m;
+      a.is_token_in_rank[int64_t(s) * N + t] = m;
+    }
+    for (int d = 0; d < R; ++d) {
+      const unsigned b = __ballot_sync(kFull, (masks[r] >> d) & 1u);
+      if (lane == 0) ball[r][warp][d] = b;
+    }
+  }
+  if (bad) sh_bad = 1;
+  __syncthreads();
+  if (warp < R) {  // destination d = warp: the counts of every (round, warp), in order
+    const int d = warp, n = rounds * kClWarps;  // n <= 128: 4 entries per lane
+    int v[4], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane * 4 + q;
+      v[q] = j < n ? __popc(ball[j / kClWarps][j % kClWarps][d]) : 0;
+      sum += v[q];
+    }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += x;
+    }
+    int run = inc - sum;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane * 4 + q;
+      if (j < n) woff[j / kClWarps][j % kClWarps][d] = run;
+      run += v[q];
+    }
+    if (lane == 31) tot[d] = inc;
+  }
+  for (int e = tid; e < E; e += kClThreads) a.num_tokens_per_expert[int64_t(s) * E + e] = cl_hist[e];
+  if (tid == 0 && sh_bad) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
+
+  // 2. every rank's totals and histogram are final
+  cluster_sync_all();
+  if (tid < R * R) {
+    const int q = tid / R, d = tid - q * R;
+    ntpr[tid] = q == s ? tot[d] : ld_peer_smem(&tot[d], uint32_t(q));
+  }
+  for (int j = tid; j < El; j += kClThreads) {  // the experts destination s owns
+    const int e = s * El + j;
+    int sum = 0;
+    for (int q0 = 0; q0 < R; q0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        c[i] = q0 + i >= R ? 0 : (q0 + i == s ? cl_hist[e] : ld_peer_smem(&cl_hist[e], uint32_t(q0 + i)));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += c[i];
+    }
+    a.num_recv_tokens_per_expert[e] = sum;
+  }
+  __syncthreads();
+
+  // 3. tables and rows
+  if (warp == 0) {
+    int64_t col = 0, pre = 0;
+    if (lane < R)
+      for (int q = 0; q < R; ++q) {
+        const int v = ntpr[q * R + lane];
+        col += v;
+        if (q < s) pre += v;
+      }
+    int64_t inc = col;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t x = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += x;
+    }
+    if (lane < R) {
+      row_base[lane] = inc - col + pre;
+      a.num_tokens_per_rank[s * R + lane] = tot[lane];
+      a.rank_prefix[s * R + lane] = int32_t(pre);
+      if (s == 0) {
+        a.dest_offsets[lane] = int32_t(inc - col);
+        if (lane == R - 1) a.dest_offsets[R] = int32_t(inc);
+      }
+    }
+  }
+  __syncthreads();
+  bool over = false;
+#pragma unroll
+  for (int r = 0; r < kClMaxRounds; ++r) {
+    const int t = r * kClThreads + tid;
+    if (r >= rounds || t >= N) continue;
+    const int64_t tok = int64_t(s) * N + t;
+    int32_t* dst = a.send_row + tok * R;
+    for (int d = 0; d < R; ++d) {
+      int32_t v = -1;
+      if ((masks[r] >> d) & 1u) {
+        const int64_t row = row_base[d] + woff[r][warp][d] + __popc(ball[r][warp][d] & lanemask_lt());
+        if (row < a.recv_capacity) {
+          v = int32_t(row);
+          if constexpr (META) {
+            a.recv_src_rank[row] = s;
+            a.recv_src_idx[row] = t;
+            const int lo = d * El;
+            for (int k = 0; k < K; ++k) {
+              const int e = __ldg(a.topk_idx + tok * K + k);
+              const bool local = e >= lo && e < lo + El;
+              a.recv_topk_idx[row * K + k] = local ? e - lo : -1;
+              a.recv_topk_weights[row * K + k] = local ? __ldg(a.topk_weights + tok * K + k) : 0.0f;
+            }
+          }
+        } else {
+          over = true;
+        }
+      }
+      dst[d] = v;
+    }
+  }
+  if (__any_sync(kFull, over) && lane == 0) raise_error(a.dev_err, MP_ERR_CAPACITY);
+
+  // 4. the peers have read this CTA's shared memory
+  cluster_sync_all();
+}
+
 }  // namespace mp
 
 // ---------------------------------------------------------------------------
@@ -1186,6 +1428,85 @@ cudaError_t launch_scan(int R, int N, int K, int E, const int32_t* topk_idx,
 }
 
 
+
+// Token count up to which layout + offsets run in one thread-block cluster.
+// Measured (globaltimer, dsv3 shape R=8, one-call dispatch): the row copy's wait
+// returned 1.3 us earlier than after the cooperative kernel at N=128, at the
+// same time at N=512, and 3.5 us later at N=1024 (one CTA per rank then writes
+// too many rows).
+#ifndef MP_CLUSTER_MAX_TOKENS
+#define MP_CLUSTER_MAX_TOKENS 256
+#endif
+
+// Layout + offsets in one thread-block cluster (one CTA per source rank);
+// cudaErrorNotSupported (nothing launched) when the shape does not suit it.
+cudaError_t launch_layout_cluster(int R, int N, int K, int E, const int32_t* topk_idx,
+                                  const float* topk_weights, int64_t recv_capacity,
+                                  int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                  uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+                                  int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                                  float* recv_topk_weights, int32_t* dest_offsets,
+                                  int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+                                  int32_t* send_row, int32_t* dev_err, cudaStream_t stream,
+                                  int meta) {
+  if (N < 1 || N > MP_CLUSTER_MAX_TOKENS || N > kClMaxRounds * kClThreads || R > kClMaxRanks)
+    return cudaErrorNotSupported;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
+  // per device and instance: 0 unknown, -1 unusable, else the largest cluster size that
+  // could be scheduled when it was set up
+  static thread_local int ready[64][2] = {};
+  static thread_local int configured_smem[64][2] = {};
+  void (*kernel)(ClusterArgs) = meta ? mp_k_layout_cluster<true> : mp_k_layout_cluster<false>;
+  const int v = meta ? 1 : 0;
+  const size_t smem = sizeof(int32_t) * size_t(E);
+  if (ready[dev][v] == 0) {
+    int ok = 0;
+    if (cudaDeviceGetAttribute(&ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess || !ok ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+      ready[dev][v] = -1;
+      return cudaErrorNotSupported;
+    }
+    ready[dev][v] = 1;
+  }
+  if (ready[dev][v] < 0) return cudaErrorNotSupported;
+  if (smem > 48 * 1024 && configured_smem[dev][v] < int(smem)) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+      return cudaErrorNotSupported;
+    configured_smem[dev][v] = int(smem);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(R));
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(R);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // can a cluster of R such CTAs be scheduled at all (cached per size and memory)?
+  static thread_local int checked[64][2][kClMaxRanks + 1] = {};
+  if (checked[dev][v][R] != int(smem) + 1) {
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kernel, &cfg) != cudaSuccess ||
+        nclusters < 1) {
+      cudaGetLastError();  // clear a refused query
+      return cudaErrorNotSupported;
+    }
+    checked[dev][v][R] = int(smem) + 1;
+  }
+  ClusterArgs args{R, N, K, E, topk_idx, topk_weights, recv_capacity, is_token_in_rank,
+                   num_tokens_per_rank, num_tokens_per_expert, recv_src_rank, recv_src_idx,
+                   recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
+                   num_recv_tokens_per_expert, send_row, dev_err};
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 // Returns cudaErrorNotSupported (nothing launched) when the problem does not
 // fit one cooperative grid; the caller then runs mp_k_layout and mp_k_scan.
 cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_idx,
@@ -1210,18 +1531,30 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
   if (coop[dev] < 0) return cudaErrorNotSupported;
   const size_t smem =
       sizeof(int32_t) * (size_t(kScanTokens) * (2 * size_t(K) + size_t(R)) + size_t(E));
-  static thread_local int configured[64] = {0};
-  if (smem > 48 * 1024 && configured[dev] < int(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(mp_k_layout_scan,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  const int lookback = scan_tiles_per_rank(N) > kFusedAggMaxTiles ? 1 : 0;
+  void (*kernel)(FusedArgs) =
+      meta ? (lookback ? mp_k_layout_scan<true, true> : mp_k_layout_scan<true, false>)
+           : (lookback ? mp_k_layout_scan<false, true> : mp_k_layout_scan<false, false>);
+  const int variant = (meta ? 2 : 0) + lookback;
+  static thread_local int configured[64][4] = {};
+  if (smem > 48 * 1024 && configured[dev][variant] < int(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
     if (e != cudaSuccess) return cudaErrorNotSupported;
-    configured[dev] = int(smem);
+    configured[dev][variant] = int(smem);
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mp_k_layout_scan, kScanThreads,
-                                                    smem) != cudaSuccess ||
-      per_sm < 1)
-    return cudaErrorNotSupported;
+  // resident blocks per SM, cached per device, instance and shared-memory size
+  static thread_local int occ_smem[64][4] = {}, occ_per_sm[64][4] = {};
+  if (occ_per_sm[dev][variant] < 1 || occ_smem[dev][variant] != int(smem)) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScanThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      return cudaErrorNotSupported;
+    occ_smem[dev][variant] = int(smem);
+    occ_per_sm[dev][variant] = per_sm;
+  }
+  const int per_sm = occ_per_sm[dev][variant];
   const int64_t tiles = scan_tiles(R, N);
   const int64_t cap = int64_t(per_sm) * sm_count();
   const int64_t grid = tiles < cap ? tiles : cap;
@@ -1230,12 +1563,10 @@ cudaError_t launch_layout_scan(int R, int N, int K, int E, const int32_t* topk_i
                        num_tokens_per_expert, recv_capacity, recv_src_rank, recv_src_idx,
                        recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
                        num_recv_tokens_per_expert, send_row, dev_err, ws, 0, -1},
-              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert, meta,
-              scan_tiles_per_rank(N) > kFusedAggMaxTiles ? 1 : 0};
+              is_token_in_rank, num_tokens_per_rank, num_tokens_per_expert};
   void* args[] = {&f};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mp_k_layout_scan),
-                                     dim3(unsigned(grid)), dim3(kScanThreads), args, smem,
-                                     stream);
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(unsigned(grid)),
+                                     dim3(kScanThreads), args, smem, stream);
 }
 }  // namespace mp
 
