@@ -576,6 +576,33 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
         row(ms_rm, rm_bytes), us_per_step=ms_rm * 1e3,
         workload="as low_latency_step_n128 with rank-major output (rows grouped by the rank "
                  "owning the expert)")
+    # the low-latency dispatch with the quantisation in the row copy (e4m3 with an fp32
+    # scale per 128 channels, and MXFP8), then the weighted combine of bf16 expert outputs
+    for fmt, qcode, sbytes in (("e4m3", B.MP_Q_E4M3, H // 128 * 4), ("mxfp8", B.MP_Q_MXFP8,
+                                                                      H // 32)):
+        for st in ll_sets:
+            st["rq"] = torch.empty((cap, H), dtype=torch.uint8, device="cuda")
+            st["rs"] = torch.empty((cap, sbytes), dtype=torch.uint8, device="cuda")
+
+        def ll_quant(st, qcode=qcode):
+            p = st["plan"]
+            B.check(B.mp_dispatch_ll_quant(R, N, K, E, H, qcode, 0, p.x, p.topk_idx, None, cap,
+                                           st["eoff"], st["esoff"], st["src"], st["slot"],
+                                           st["rq"], st["rs"], p.dev_err))
+
+        ms_q = timed(over_sets(ll_sets, ll_quant, ll_combine), max(1, steps // P)) / P
+        q_phase_us = phases(ll_sets, [ll_quant, ll_combine], ("dispatch_ll_quant", "combine_ll"),
+                            steps)
+        assert ll_errors() == 0
+        q_bytes = ll_bytes - cap * H * 2 + cap * (H + sbytes)
+        out["low_latency_quantised_%s_step_n128" % fmt] = dict(
+            row(ms_q, q_bytes), us_per_step=ms_q * 1e3, phases_us=q_phase_us,
+            workload="as low_latency_step_n128 with mp_dispatch_ll_quant: bf16 rows quantised "
+                     "in the row copy to %s (%s), then the weighted combine of bf16 expert "
+                     "outputs" % (fmt, "fp32 scale per 128 channels" if fmt == "e4m3"
+                                  else "UE8M0 scale per 32 channels"))
+        for st in ll_sets:
+            del st["rq"], st["rs"]
     del ll_sets, graph, graph3
     torch.cuda.empty_cache()
 

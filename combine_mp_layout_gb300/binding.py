@@ -24,6 +24,10 @@ MP_ERR_TIMEOUT = 16
 MP_BF16 = 0
 MP_E4M3 = 1
 SCALE_BLOCK = 128
+# formats of the low-latency dispatch's in-kernel quantisation
+MP_Q_E4M3 = 0
+MP_Q_MXFP8 = 1
+MP_Q_MXFP4 = 2
 
 _lib = None
 
@@ -79,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.mp_layout_and_offsets.argtypes = [i32, i32, i32, i32, P, P, i64] + [P] * 14
         L.mp_dispatch_noalloc.argtypes = [i32] * 6 + [P] * 7 + [i64] + [P] * 12
         L.mp_layout_dispatch.argtypes = [i32] * 6 + [P] * 4 + [i64] + [P] * 16
+        L.mp_dispatch_ll_rows_quant.argtypes = [i32] * 5 + [P, P, i64, P, P, P]
+        L.mp_dispatch_ll_quant.argtypes = [i32] * 7 + [P] * 3 + [i64] + [P] * 8
         L.mp_allgatherv_multi.argtypes = [i32, i32, P, P, P, P, P]
         L.mp_dispatch_ll.argtypes = [i32] * 7 + [P] * 4 + [i64] + [P] * 8
         for f in ("mp_layout", "mp_dispatch", "mp_dispatch_offsets", "mp_dispatch_rows",
@@ -90,7 +96,8 @@ def lib() -> ctypes.CDLL:
                   "mp_allgatherv_e4m3", "mp_allgatherv_mxfp8", "mp_allgatherv_mxfp4",
                   "mp_dispatch_rows_mxfp4", "mp_dispatch_rows_bulk",
                   "mp_layout_and_offsets", "mp_dispatch_noalloc", "mp_allgatherv_multi",
-                  "mp_dispatch_ll", "mp_layout_dispatch"):
+                  "mp_dispatch_ll", "mp_layout_dispatch", "mp_dispatch_ll_rows_quant",
+                  "mp_dispatch_ll_quant"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -387,3 +394,26 @@ def mp_combine_ll(R, N, K, H, y, y_rows, slot_row, topk_weights, out, dev_err, s
     return lib().mp_combine_ll(R, N, K, H, _dev(y, "y"), int(y_rows), _dev(slot_row, "slot_row"),
                                _dev(topk_weights, "topk_weights"), _dev(out, "out"),
                                _dev(dev_err, "dev_err"), _stream(stream))
+
+
+def mp_dispatch_ll_rows_quant(R, N, K, H, qformat, x, slot_row, recv_capacity, recv_x,
+                              recv_scales, stream=None) -> int:
+    """LL row copy with the quantisation in the kernel (qformat MP_Q_E4M3 / _MXFP8 /
+    _MXFP4): bf16 token rows in, codes and scales at every slot row."""
+    return lib().mp_dispatch_ll_rows_quant(R, N, K, H, int(qformat), _dev(x, "x"),
+                                           _dev(slot_row, "slot_row"), int(recv_capacity),
+                                           _dev(recv_x, "recv_x"),
+                                           _dev(recv_scales, "recv_scales"), _stream(stream))
+
+
+def mp_dispatch_ll_quant(R, N, K, E, H, qformat, rank_major, x, topk_idx, num_tokens_per_expert,
+                         recv_capacity, bin_offsets, bin_src_offsets, recv_src_token, slot_row,
+                         recv_x, recv_scales, dev_err, stream=None) -> int:
+    """mp_dispatch_ll with the quantisation in the row copy."""
+    return lib().mp_dispatch_ll_quant(
+        R, N, K, E, H, int(qformat), int(rank_major), _dev(x, "x"), _dev(topk_idx, "topk_idx"),
+        _dev(num_tokens_per_expert, "num_tokens_per_expert"), int(recv_capacity),
+        _dev(bin_offsets, "bin_offsets"), _dev(bin_src_offsets, "bin_src_offsets"),
+        _dev(recv_src_token, "recv_src_token"), _dev(slot_row, "slot_row"),
+        _dev(recv_x, "recv_x"), _dev(recv_scales, "recv_scales"), _dev(dev_err, "dev_err"),
+        _stream(stream))

@@ -597,6 +597,63 @@ int mp_dispatch_ll(int R, int N, int K, int E, int H, int dtype, int rank_major,
       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int ll_quant_rows_checked(int R, int N, int K, int H, int qformat, const void* x,
+                                 const int32_t* slot_row, int64_t recv_capacity,
+                                 const void* recv_x, const void* recv_scales) {
+  if (R < 1 || R > MP_MAX_RANKS || N < 0 || K < 1 || K > MP_MAX_TOPK || H <= 0 ||
+      recv_capacity < 0)
+    return MP_ERR_INVALID_ARG;
+  if (qformat != MP_Q_E4M3 && qformat != MP_Q_MXFP8 && qformat != MP_Q_MXFP4)
+    return MP_ERR_INVALID_ARG;
+  if (H % (qformat == MP_Q_E4M3 ? MP_SCALE_BLOCK : 32) != 0) return MP_ERR_INVALID_ARG;
+  if (int64_t(R) * N * K >= (int64_t(1) << 31)) return MP_ERR_INVALID_ARG;
+  if (N > 0 && (!x || !slot_row)) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && (!recv_x || !recv_scales)) return MP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned4(slot_row) ||
+      (qformat == MP_Q_E4M3 && !aligned4(recv_scales)))
+    return MP_ERR_INVALID_ARG;
+  return MP_OK;
+}
+
+int mp_dispatch_ll_rows_quant(int R, int N, int K, int H, int qformat, const void* x,
+                              const int32_t* slot_row, int64_t recv_capacity, void* recv_x,
+                              void* recv_scales, mp_stream_t stream) {
+  const int st = ll_quant_rows_checked(R, N, K, H, qformat, x, slot_row, recv_capacity, recv_x,
+                                       recv_scales);
+  if (st != MP_OK) return st;
+  // the quantising copy with the K top-k slots of a token in place of its R destinations
+  return cuda_status(launch_dispatch_quant(K, int64_t(R) * N, H, x, recv_x, recv_scales, qformat,
+                                           recv_capacity, slot_row,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mp_dispatch_ll_quant(int R, int N, int K, int E, int H, int qformat, int rank_major,
+                         const void* x, const int32_t* topk_idx,
+                         const int32_t* num_tokens_per_expert, int64_t recv_capacity,
+                         int32_t* bin_offsets, int32_t* bin_src_offsets, int32_t* recv_src_token,
+                         int32_t* slot_row, void* recv_x, void* recv_scales, int32_t* dev_err,
+                         mp_stream_t stream) {
+  if (!ep_shape_ok(R, N, K, E) || recv_capacity < 0 || (rank_major != 0 && rank_major != 1))
+    return MP_ERR_INVALID_ARG;
+  if (!bin_offsets || !bin_src_offsets || !dev_err) return MP_ERR_INVALID_ARG;
+  if (N > 0 && !topk_idx) return MP_ERR_INVALID_ARG;
+  if (recv_capacity > 0 && !recv_src_token) return MP_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(num_tokens_per_expert) || !aligned4(bin_offsets) ||
+      !aligned4(bin_src_offsets) || !aligned4(recv_src_token) || !aligned4(dev_err))
+    return MP_ERR_INVALID_ARG;
+  const int st = ll_quant_rows_checked(R, N, K, H, qformat, x, slot_row, recv_capacity, recv_x,
+                                       recv_scales);
+  if (st != MP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // the sort, then the quantising row copy as its programmatic dependent
+  const cudaError_t e = launch_ll_offsets(R, N, K, E, rank_major, topk_idx,
+                                          num_tokens_per_expert, recv_capacity, bin_offsets,
+                                          bin_src_offsets, recv_src_token, slot_row, dev_err, cs);
+  if (e != cudaSuccess || N == 0) return cuda_status(e);
+  return cuda_status(launch_dispatch_quant(K, int64_t(R) * N, H, x, recv_x, recv_scales, qformat,
+                                           recv_capacity, slot_row, cs, /*dependent=*/true));
+}
+
 int mp_combine_ll(int R, int N, int K, int H, const void* y, int64_t y_rows,
                   const int32_t* slot_row, const float* topk_weights, void* out,
                   int32_t* dev_err, mp_stream_t stream) {

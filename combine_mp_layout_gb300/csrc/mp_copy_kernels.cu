@@ -439,6 +439,9 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
   constexpr int NB = FP4 ? CPL / 8 : CPL / 4;  // 32-bit words of codes per lane
   constexpr int kCodeBytes = NB * 4;
   static_assert(kLanes >= 1 && kLanes <= 32, "scale block spans whole lanes");
+  // launched as the low-latency sort's programmatic dependent, the blocks start
+  // while the sort runs and wait here for its slot rows (a no-op otherwise)
+  pdl_wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int64_t vpr = H / CPL;  // lane vectors per row
   const int64_t row_bytes = FP4 ? H / 2 : H;
@@ -968,7 +971,7 @@ cudaError_t launch_dispatch_after_offsets(int R, int N, int K, int E, int64_t ro
 template <int CPL, int U, int FMT, bool GATHER>
 static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void* out,
                               void* out_scales, int64_t limit, const int32_t* send_row,
-                              cudaStream_t stream) {
+                              bool dependent, cudaStream_t stream) {
   auto kernel = mp_k_quant_rows<CPL, U, FMT, GATHER>;
   static const int per_sm = resident_blocks(kernel);
   const int64_t vpr = H / CPL;
@@ -976,6 +979,10 @@ static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void*
   constexpr bool persistent = (MP_QUANT_PERSISTENT_MASK >> (FMT + (GATHER ? 3 : 0))) & 1;
   const unsigned grid = persistent ? grid_for(per_sm, kWarpsPerBlock, tokens * slabs)
                                    : grid_full(kWarpsPerBlock, tokens * slabs);
+  if (dependent)
+    return launch_dependent(kernel, dim3(grid), stream, R, tokens, H,
+                            static_cast<const uint16_t*>(x), static_cast<unsigned char*>(out),
+                            out_scales, limit, send_row);
   return launch_kernel(kernel, dim3(grid), dim3(kCopyThreads), 0, stream, R, tokens, H,
                        static_cast<const uint16_t*>(x), static_cast<unsigned char*>(out),
                        out_scales, limit, send_row);
@@ -984,37 +991,37 @@ static cudaError_t quant_rows(int R, int64_t tokens, int H, const void* x, void*
 template <int FMT, bool GATHER>
 static cudaError_t quant_rows_any(int R, int64_t tokens, int H, const void* x, void* out,
                                   void* out_scales, int64_t limit, const int32_t* send_row,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool dependent = false) {
   if (tokens == 0) return cudaSuccess;
   constexpr int U = (GATHER && FMT == kQE4M3) ? 1 : (FMT == kQMXFP4 ? MP_QUANT_U_FP4 : 2);
   if constexpr ((MP_QUANT_CPL32_MASK >> (FMT + (GATHER ? 3 : 0))) & 1) {
     // 32 channels per lane: 32-byte FP8 code stores need a 32-byte aligned output
     if (aligned(x, 32) && (FMT == kQMXFP4 || aligned(out, 32)))
       return quant_rows<32, 1, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
-                                            stream);
+                                            dependent, stream);
   }
   if constexpr (MP_QUANT_CPL == 16) {
     if (aligned(x, 32))
       return quant_rows<16, U, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
-                                            stream);
+                                            dependent, stream);
   }
   return quant_rows<8, 2 * U, FMT, GATHER>(R, tokens, H, x, out, out_scales, limit, send_row,
-                                           stream);
+                                           dependent, stream);
 }
 
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
                                   void* recv_scales, int fmt, int64_t recv_capacity,
-                                  const int32_t* send_row, cudaStream_t stream) {
+                                  const int32_t* send_row, cudaStream_t stream, bool dependent) {
   switch (fmt) {
     case kQE4M3:
       return quant_rows_any<kQE4M3, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
-                                           send_row, stream);
+                                           send_row, stream, dependent);
     case kQMXFP8:
       return quant_rows_any<kQMXFP8, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
-                                            send_row, stream);
+                                            send_row, stream, dependent);
     case kQMXFP4:
       return quant_rows_any<kQMXFP4, false>(R, tokens, H, x, recv_x, recv_scales, recv_capacity,
-                                            send_row, stream);
+                                            send_row, stream, dependent);
   }
   return cudaErrorInvalidValue;
 }

@@ -139,10 +139,14 @@ cudaError_t launch_dispatch_bulk(int R, int64_t tokens, int64_t row_bytes, const
 // Quantises bf16 token rows -- fmt 0: e4m3 with one fp32 scale per 128
 // channels; 1: MXFP8 (e4m3, one UE8M0 byte per 32 channels); 2: MXFP4 (two
 // e2m1 codes per byte, one UE8M0 byte per 32 channels) -- and copies them to
-// every receive row listed in send_row.
+// every receive row listed in send_row (R entries per token; the K slot rows
+// of the low-latency layout work the same way).  dependent: launched as the
+// programmatic dependent of the kernel before it (the LL sort writing the
+// destinations), its blocks waiting for that kernel before they read them.
 cudaError_t launch_dispatch_quant(int R, int64_t tokens, int H, const void* x, void* recv_x,
                                   void* recv_scales, int fmt, int64_t recv_capacity,
-                                  const int32_t* send_row, cudaStream_t stream);
+                                  const int32_t* send_row, cudaStream_t stream,
+                                  bool dependent = false);
 
 cudaError_t launch_combine(int R, int64_t tokens, int H, const void* y, int64_t y_rows,
                            const int32_t* send_row, void* out, int32_t* dev_err,

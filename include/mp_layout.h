@@ -567,6 +567,58 @@ int mp_combine_ll(int R, int N, int K, int H, const void *y, int64_t y_rows,
                   const int32_t *slot_row, const float *topk_weights, void *out,
                   int32_t *dev_err, mp_stream_t stream);
 
+/*
+ * Formats of the in-kernel quantisation on low-latency dispatch
+ * (mp_dispatch_ll_quant, mp_dispatch_ll_rows_quant); each is the per-row
+ * quantisation of mp_dispatch_rows_e4m3 / _mxfp8 / _mxfp4.
+ *   MP_Q_E4M3   e4m3 codes [cap][H], one fp32 scale per 128 channels
+ *               (recv_scales fp32 [cap][H/128]): scale = amax / 448 (1 for an
+ *               all-zero block), code = e4m3(x / scale), saturating
+ *   MP_Q_MXFP8  e4m3 codes [cap][H], one UE8M0 byte per 32 channels
+ *               (recv_scales uint8 [cap][H/32])
+ *   MP_Q_MXFP4  two e2m1 codes per byte [cap][H/2] (even channel in the low
+ *               nibble), one UE8M0 byte per 32 channels (uint8 [cap][H/32])
+ */
+#define MP_Q_E4M3 0
+#define MP_Q_MXFP8 1
+#define MP_Q_MXFP4 2
+
+/*
+ * mp_dispatch_ll_rows_quant -- [EP] the low-latency dispatch with the FP8
+ * quantisation done in the dispatch kernel (the page's file table lists FP8
+ * E4M3 quantisation helpers for LL dispatch; its LL kernel list templates the
+ * dispatch on FP8): each bf16 token row is quantised once and its codes and
+ * scales are written to every slot row the LL offsets gave it.
+ *   x            bf16 [R][N][H]
+ *   slot_row     int32 [R][N][K] from mp_dispatch_ll_offsets(_rank_major)
+ *   recv_x       codes and recv_scales scales, per qformat (MP_Q_*); rows at
+ *                or past recv_capacity are not written
+ * Checks: 1 <= R <= 32, 1 <= K <= 32, H a multiple of 128 (MP_Q_E4M3) or 32,
+ *   16-byte aligned x / recv_x, non-NULL buffers where rows exist.
+ * The result equals quantising x (the per-row definition above) and then
+ * copying codes and scales to the slot rows (mp_dispatch_ll_rows).
+ */
+int mp_dispatch_ll_rows_quant(int R, int N, int K, int H, int qformat, const void *x,
+                              const int32_t *slot_row, int64_t recv_capacity, void *recv_x,
+                              void *recv_scales, mp_stream_t stream);
+
+/*
+ * mp_dispatch_ll_quant -- mp_dispatch_ll with the quantisation done in the row
+ * copy: the LL offsets (expert-major, or rank-major with rank_major = 1), then
+ * the quantising row copy of mp_dispatch_ll_rows_quant launched as the sort's
+ * programmatic dependent (its blocks start while the sort runs and wait for
+ * its slot rows).  Arguments: those of mp_dispatch_ll, with qformat and
+ * void *recv_scales in place of dtype, x_scales and the float scales (x is
+ * bf16); checks and device errors as mp_dispatch_ll_offsets and
+ * mp_dispatch_ll_rows_quant.
+ */
+int mp_dispatch_ll_quant(int R, int N, int K, int E, int H, int qformat, int rank_major,
+                         const void *x, const int32_t *topk_idx,
+                         const int32_t *num_tokens_per_expert, int64_t recv_capacity,
+                         int32_t *bin_offsets, int32_t *bin_src_offsets, int32_t *recv_src_token,
+                         int32_t *slot_row, void *recv_x, void *recv_scales, int32_t *dev_err,
+                         mp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -213,6 +213,41 @@ def test_one_call_low_latency_dispatch_writes_only_its_buffers(rank_major):
         assert gb.intact(), "guard bytes overwritten next to the " + name
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
+def test_quantised_low_latency_dispatch_writes_only_its_buffers(fmt, rank_major):
+    """mp_dispatch_ll_quant and mp_dispatch_ll_rows_quant with a too-small capacity."""
+    R, N, E, K, H = 4, 77, 16, 3, 256
+    inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=12)
+    inp.topk_idx[:, ::5, 1] = -1
+    topk = torch.from_numpy(inp.topk_idx).cuda()
+    x = inp.x.cuda()
+    total = int((inp.topk_idx >= 0).sum())
+    cap = total - 10
+    nb = R if rank_major else E
+    qcode = {"e4m3": B.MP_Q_E4M3, "mxfp8": B.MP_Q_MXFP8, "mxfp4": B.MP_Q_MXFP4}[fmt]
+    qcols, blk = (H // 2, 32) if fmt == "mxfp4" else (H, 128 if fmt == "e4m3" else 32)
+    sdt = torch.float32 if fmt == "e4m3" else torch.uint8
+    off = Guarded((nb + 1,), torch.int32)
+    soff = Guarded((nb, R), torch.int32)
+    src = Guarded((cap,), torch.int32)
+    slot = Guarded((R, N, K), torch.int32)
+    rq = Guarded((cap, qcols), torch.uint8)
+    rs = Guarded((cap, H // blk), sdt)
+    rq2 = Guarded((cap, qcols), torch.uint8)
+    rs2 = Guarded((cap, H // blk), sdt)
+    err = Guarded((1,), torch.int32, 0)
+    B.check(B.mp_dispatch_ll_quant(R, N, K, E, H, qcode, rank_major, x, topk, None, cap, off.t,
+                                   soff.t, src.t, slot.t, rq.t, rs.t, err.t))
+    B.check(B.mp_dispatch_ll_rows_quant(R, N, K, H, qcode, x, slot.t, cap, rq2.t, rs2.t))
+    torch.cuda.synchronize()
+    assert int(err.t.item()) == B.MP_ERR_CAPACITY
+    for name, gb in (("offsets", off), ("source offsets", soff), ("source tokens", src),
+                     ("slots", slot), ("codes", rq), ("scales", rs), ("codes (rows call)", rq2),
+                     ("scales (rows call)", rs2), ("error word", err)):
+        assert gb.intact(), "guard bytes overwritten next to the " + name
+
+
 def test_bulk_copy_dispatch_writes_only_its_buffers():
     R, N, E, K, H = 3, 333, 12, 3, 72
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="bf16"), seed=11)

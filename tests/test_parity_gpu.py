@@ -1030,6 +1030,77 @@ def test_low_latency_one_call_dispatch_e4m3_with_scales():
     assert np.array_equal(rs[:n].cpu().numpy().view(np.uint8), ll["recv_x"][:, H:])
 
 
+LL_QUANT = [dict(R=8, N=128, E=256, K=8, H=7168), dict(R=5, N=77, E=20, K=6, H=384),
+            dict(R=3, N=300, E=9, K=9, H=256), dict(R=4, N=500, E=16, K=4, H=128, cap_frac=0.5),
+            dict(R=2, N=50, E=64, K=32, H=128), dict(R=4, N=0, E=16, K=4, H=128)]
+
+
+@pytest.mark.parametrize("cfg", LL_QUANT, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
+                         + ("_cap" if "cap_frac" in c else ""))
+@pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
+@pytest.mark.parametrize("fmt", ["e4m3", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("call", ["one_call", "rows"])
+def test_low_latency_quantised_dispatch_matches_oracle(cfg, rank_major, fmt, call):
+    """The low-latency dispatch with the quantisation in the row copy -- mp_dispatch_ll_quant
+    (the sort, then the quantising copy as its programmatic dependent) or the LL offsets
+    followed by mp_dispatch_ll_rows_quant -- against the oracle's composition: every token
+    row quantised by the oracle (codes and scales), then the oracle's LL layout of those
+    bytes; bit for bit, two calls in a row, with all-zero, tiny and wide-range blocks."""
+    cfg = dict(cfg)
+    cap_frac = cfg.pop("cap_frac", None)
+    R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
+    f = QFMT[fmt]
+    qcode = {"e4m3": B.MP_Q_E4M3, "mxfp8": B.MP_Q_MXFP8, "mxfp4": B.MP_Q_MXFP4}[fmt]
+    inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=N + 11)
+    if N > 0:
+        inp.topk_idx[:, ::5, K - 1] = -1
+        inp.x = _special_blocks(inp.x.reshape(R * N, H), f["block"]).reshape(R, N, H)
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    cap = R * N * K if cap_frac is None else int(R * N * K * cap_frac)
+    q, sc, st = getattr(oracle, f["quant"])(wl.bf16_bits(inp.x))
+    assert st == 0
+    ncode = f["qcols"](H)
+    nsb = (H // f["block"]) * sc.itemsize  # scale bytes per row
+    payload = np.concatenate([q.reshape(R, N, ncode),
+                              np.ascontiguousarray(sc).view(np.uint8).reshape(R, N, nsb)],
+                             axis=-1)
+    want, st = (oracle.dispatch_ll_rank_major if rank_major else oracle.dispatch_ll)(
+        payload, inp.topk_idx, E, recv_capacity=cap)
+    n = min(want["num_recv"], cap)
+    keys = ("dest_offsets", "dest_src_offsets") if rank_major else ("expert_offsets",
+                                                                    "expert_src_offsets")
+    nb = R if rank_major else E
+    dev = "cuda"
+    for rep in range(2):
+        boff = torch.full((nb + 1,), -3, dtype=torch.int32, device=dev)
+        bsoff = torch.full((nb, R), -3, dtype=torch.int32, device=dev)
+        src = torch.full((max(cap, 1),), -3, dtype=torch.int32, device=dev)
+        slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
+        rq = torch.zeros((max(cap, 1), ncode), dtype=torch.uint8, device=dev)
+        rs = torch.zeros((max(cap, 1), H // f["block"]), dtype=f["sdt"], device=dev)
+        plan.dev_err.zero_()
+        if call == "one_call":
+            B.check(B.mp_dispatch_ll_quant(R, N, K, E, H, qcode, rank_major, plan.x, plan.topk_idx,
+                                           None, cap, boff, bsoff, src, slot, rq, rs,
+                                           plan.dev_err))
+        else:
+            off = B.mp_dispatch_ll_offsets_rank_major if rank_major else B.mp_dispatch_ll_offsets
+            B.check(off(R, N, K, E, plan.topk_idx, None, cap, boff, bsoff, src, slot,
+                        plan.dev_err))
+            B.check(B.mp_dispatch_ll_rows_quant(R, N, K, H, qcode, plan.x, slot, cap, rq, rs))
+        torch.cuda.synchronize()
+        assert plan.device_error() == st, rep
+        assert np.array_equal(boff.cpu().numpy(), want[keys[0]]), rep
+        assert np.array_equal(bsoff.cpu().numpy(), want[keys[1]]), rep
+        assert np.array_equal(slot.cpu().numpy(), want["slot_row"]), rep
+        assert np.array_equal(src[:n].cpu().numpy(), want["recv_src_token"]), rep
+        assert np.array_equal(rq[:n].cpu().numpy(), want["recv_x"][:n, :ncode]), rep
+        assert np.array_equal(rs[:n].contiguous().view(torch.uint8).cpu().numpy(),
+                              want["recv_x"][:n, ncode:]), rep
+    assert (st == 0) == (cap_frac is None)
+
+
 def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
     R, N, E, K = 4, 50, 16, 3
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=64, routing="uniform", dtype="bf16"), seed=9)
