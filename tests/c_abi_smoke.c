@@ -9,9 +9,15 @@
  *     its experts (expert e lives on rank e / (E/R));
  *   - combining the un-modified dispatch gives c * x, c = that rank count
  *     (exact here: x holds small integers, so every fp32 sum is exact);
+ *   - the whole dispatch in one call (mp_layout_dispatch) gives the same send_row
+ *     and the same combine;
  *   - the low-latency dispatch in one call gives every routed (token, slot) a row,
  *     and its weighted combine with unit weights gives K' * x, K' = the token's
- *     routed slots.
+ *     routed slots;
+ *   - the low-latency dispatch with MXFP8 quantisation in the row copy gives the
+ *     same slot rows, and every received row decodes back to x exactly (x holds
+ *     small integers, so each 32-channel block's scale 2^(floor(log2 amax) - 8)
+ *     makes every element an exact e4m3 value).
  * Prints "c abi smoke ok" and returns 0 on success.
  */
 #include <stdint.h>
@@ -53,6 +59,13 @@ static uint16_t bf16_of_small_int(int v) { /* exact: |v| < 256 */
   uint32_t u;
   memcpy(&u, &f, sizeof u);
   return (uint16_t)(u >> 16);
+}
+
+/* e4m3 ("fn") code -> value, from the format's definition (finite codes only) */
+static float f32_of_e4m3(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  const float mag = e == 0 ? (float)m / 512.0f : (1.0f + (float)m / 8.0f) * (float)(1 << e) / 128.0f;
+  return (c & 0x80) ? -mag : mag;
 }
 
 static float f32_of_bf16(uint16_t b) {
@@ -157,6 +170,34 @@ int main(void) {
       if (f32_of_bf16(out[tok * H + h]) != want) return fail("combine != c * x");
     }
   }
+  /* the whole dispatch in one call: layout, offsets and rows (the row copy a
+   * programmatic dependent of the offsets kernel, writing the receive metadata) */
+  {
+    static int32_t send_row2[R * N * R];
+    CUDA(cudaMemset(d_send, 0xff, sizeof send_row));
+    CUDA(cudaMemset(d_recv_x, 0, sizeof(uint16_t) * (size_t)cap * H));
+    CUDA(cudaMemset(d_out, 0, sizeof out));
+    MP(mp_layout_dispatch(R, N, K, E, H, MP_BF16, d_x, NULL, d_topk, d_w, cap, d_ntpr, d_ntpe,
+                          d_mask, d_recv_x, NULL, d_rsr, d_rsi, d_rti, d_rtw, d_doff, d_rp,
+                          d_nrtpe, d_send, d_err, d_ws, NULL));
+    MP(mp_combine(R, N, H, d_recv_x, cap, d_send, d_out, d_err, NULL));
+    CUDA(cudaDeviceSynchronize());
+    CUDA(cudaMemcpy(&err, d_err, sizeof err, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(send_row2, d_send, sizeof send_row2, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(out, d_out, sizeof out, cudaMemcpyDeviceToHost));
+    if (err != 0) {
+      fprintf(stderr, "device error (one-call dispatch): %s\n", mp_status_string(err));
+      return 1;
+    }
+    if (memcmp(send_row, send_row2, sizeof send_row) != 0) return fail("one-call send_row");
+    for (int tok = 0; tok < R * N; ++tok) {
+      int owners = 0;
+      for (int d = 0; d < R; ++d) owners += send_row[tok * R + d] >= 0;
+      for (int h = 0; h < H; ++h)
+        if (f32_of_bf16(out[tok * H + h]) != (float)owners * f32_of_bf16(x[tok * H + h]))
+          return fail("one-call combine != c * x");
+    }
+  }
   /* the low-latency path in one call: one row per valid (token, slot), then the
    * weighted combine with unit weights, which gives K * x for a routed token */
   {
@@ -196,6 +237,36 @@ int main(void) {
         if (f32_of_bf16(out[tok * H + h]) != want) return fail("low-latency combine != c * x");
       }
     }
+    /* the same dispatch with MXFP8 quantisation in the row copy */
+    static int32_t slot2[R * N * K];
+    static uint8_t codes[(size_t)R * N * K * H], scales[(size_t)R * N * K * (H / 32)];
+    void *d_q, *d_qs;
+    CUDA(cudaMalloc(&d_q, sizeof codes));
+    CUDA(cudaMalloc(&d_qs, sizeof scales));
+    MP(mp_dispatch_ll_quant(R, N, K, E, H, MP_Q_MXFP8, 0, d_x, d_topk, NULL, lcap, d_boff,
+                            d_bsoff, d_src, d_slot, d_q, d_qs, d_err, NULL));
+    CUDA(cudaDeviceSynchronize());
+    CUDA(cudaMemcpy(&err, d_err, sizeof err, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(slot2, d_slot, sizeof slot2, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(codes, d_q, sizeof codes, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(scales, d_qs, sizeof scales, cudaMemcpyDeviceToHost));
+    if (err != 0) {
+      fprintf(stderr, "device error (quantised low-latency): %s\n", mp_status_string(err));
+      return 1;
+    }
+    if (memcmp(slot, slot2, sizeof slot) != 0) return fail("quantised slot_row");
+    for (int tok = 0; tok < R * N; ++tok)
+      for (int k = 0; k < K; ++k) {
+        const int32_t row = slot2[tok * K + k];
+        if (row < 0) continue;
+        for (int h = 0; h < H; ++h) {
+          const int code = scales[(size_t)row * (H / 32) + h / 32];
+          const float X = code == 0 ? 0.0f : (float)(code >= 127 ? (1u << (code - 127)) : 1u) /
+                                                 (float)(code < 127 ? (1u << (127 - code)) : 1u);
+          if (f32_of_e4m3(codes[(size_t)row * H + h]) * X != f32_of_bf16(x[tok * H + h]))
+            return fail("MXFP8 row does not decode to x");
+        }
+      }
   }
   printf("c abi smoke ok: %d receive rows\n", dest_offsets[R]);
   return 0;

@@ -1,8 +1,9 @@
 """The C ABI from plain C: tests/c_abi_smoke.c is compiled with gcc against
 include/mp_layout.h and the built library (no Python, no torch on its path).
 On the CPU the program is only compiled (the header must be valid C11); on a
-GPU it runs one layout -> dispatch -> combine pass and one low-latency
-dispatch -> weighted combine pass, and checks both."""
+GPU it runs a layout -> dispatch -> combine pass, the same dispatch in one call
+(mp_layout_dispatch), a low-latency dispatch -> weighted combine pass and the
+low-latency dispatch with MXFP8 quantisation in the row copy, and checks them."""
 import os
 import shutil
 import subprocess
