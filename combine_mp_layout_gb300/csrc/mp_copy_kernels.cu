@@ -388,14 +388,31 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   return r;
 }
 
-// Two E2M1 codes in one byte: `hi` in bits 4-7, `lo` in bits 0-3; each sign
-// bit is set from its input, so a negative value that rounds to zero is -0.
+// Two E2M1 codes in one byte: `hi` in bits 4-7, `lo` in bits 0-3, as the
+// conversion gives them (a negative value that rounds to zero comes out +0;
+// e2m1_signs puts the sign bits back).
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
   uint32_t r;
   asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}"
       : "=r"(r)
       : "f"(hi), "f"(lo));
-  return r | ((__float_as_uint(hi) >> 31) << 7) | ((__float_as_uint(lo) >> 31) << 3);
+  return r;
+}
+
+// The sign bits of eight E2M1 codes (one 32-bit word, channel 2b in the low
+// nibble of byte b and channel 2b+1 in its high nibble) from the four bf16
+// words of those channels (channel 2b in bits 0-15 of w[b], 2b+1 in bits
+// 16-31): the bf16 sign bits 15 and 31 of w[b] become bits 3 and 7 of byte b.
+// x / X has the sign of x for every finite x (X > 0), so every code, a zero
+// included, keeps its input's sign.  Byte permutes gather the four words'
+// high and low middle bytes, which hold those sign bits as their bit 7.
+__device__ __forceinline__ uint32_t e2m1_signs(uint32_t w0, uint32_t w1, uint32_t w2,
+                                               uint32_t w3) {
+  const uint32_t hi = __byte_perm(__byte_perm(w0, w1, 0x0073), __byte_perm(w2, w3, 0x0073),
+                                  0x5410);  // byte b = byte 3 of w[b]
+  const uint32_t lo = __byte_perm(__byte_perm(w0, w1, 0x0051), __byte_perm(w2, w3, 0x0051),
+                                  0x5410);  // byte b = byte 1 of w[b]
+  return (hi & 0x80808080u) | ((lo >> 4) & 0x08080808u);
 }
 
 __device__ __forceinline__ int floor_log2_pos(float a) {  // a > 0, finite
@@ -469,6 +486,7 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
     const int64_t i0 = slab * slab_vec + lane;
     uint32_t q[U][NB];
     uint32_t sbits[U];  // fp32 scale bits, or the UE8M0 code
+    uint32_t sgn[U][FP4 ? NB : 1];  // FP4: the codes' sign bits, from the bf16 inputs
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * kWarp;
@@ -493,6 +511,11 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
           f[2 * j] = __uint_as_float(v.w[j] << 16);
           f[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
         }
+        if constexpr (FP4) {
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            sgn[u][j] = e2m1_signs(v.w[4 * j], v.w[4 * j + 1], v.w[4 * j + 2], v.w[4 * j + 3]);
+        }
 #pragma unroll
         for (int j = 0; j < CPL; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
@@ -509,7 +532,7 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
             if constexpr (FP4) {  // 8 channels -> 4 bytes
-              uint32_t w = 0;
+              uint32_t w = sgn[u][j];
 #pragma unroll
               for (int b = 0; b < 4; ++b)
                 w |= cvt_e2m1x2(__fmul_rn(f[8 * j + 2 * b + 1], inv),
