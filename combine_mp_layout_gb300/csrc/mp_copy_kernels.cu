@@ -388,14 +388,21 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   return r;
 }
 
-// Two E2M1 codes in one byte: `hi` in bits 4-7, `lo` in bits 0-3, as the
-// conversion gives them (a negative value that rounds to zero comes out +0;
-// e2m1_signs puts the sign bits back).
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+// Eight E2M1 codes in one 32-bit word, channel c[2b] in the low nibble and
+// c[2b+1] in the high nibble of byte b: four pair conversions packed by one
+// vector move.  A negative value that rounds to zero comes out +0 here;
+// e2m1_signs puts the sign bits back.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float c0, float c1, float c2, float c3, float c4,
+                                               float c5, float c6, float c7) {
   uint32_t r;
-  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}"
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
       : "=r"(r)
-      : "f"(hi), "f"(lo));
+      : "f"(c0), "f"(c1), "f"(c2), "f"(c3), "f"(c4), "f"(c5), "f"(c6), "f"(c7));
   return r;
 }
 
@@ -532,13 +539,12 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
             if constexpr (FP4) {  // 8 channels -> 4 bytes
-              uint32_t w = sgn[u][j];
-#pragma unroll
-              for (int b = 0; b < 4; ++b)
-                w |= cvt_e2m1x2(__fmul_rn(f[8 * j + 2 * b + 1], inv),
-                                __fmul_rn(f[8 * j + 2 * b], inv))
-                     << (8 * b);
-              q[u][j] = w;
+              const float* c = f + 8 * j;
+              q[u][j] = sgn[u][j] |
+                        cvt_e2m1x8(__fmul_rn(c[0], inv), __fmul_rn(c[1], inv),
+                                   __fmul_rn(c[2], inv), __fmul_rn(c[3], inv),
+                                   __fmul_rn(c[4], inv), __fmul_rn(c[5], inv),
+                                   __fmul_rn(c[6], inv), __fmul_rn(c[7], inv));
             } else {  // 4 channels -> 4 bytes
               const uint32_t lo =
                   cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
