@@ -1303,4 +1303,369 @@ cudaError_t launch_ll_rows_after_sort(int K, int64_t tokens, int64_t row_bytes, 
                                   scales_per_row, x_scales, recv_scales, stream);
 }
 
+// ---------------------------------------------------------------------------
+// The low-latency dispatch in one kernel for small batches, no block waiting
+// for another.  The rows of a bin are ordered by source rank, token and top-k
+// slot, which is the entries' flat index i = (s*N + n)*K + k, so entry i goes
+// to the bin's first row plus the number of entries j < i in the same bin.
+// Block b copies the units [V*b/G, V*(b+1)/G) of the token-major row space
+// (V = R*N*vpr units of 16 or 32 bytes); for the tokens those units belong to
+// it finds the rows itself:
+//  1. one pass over all R*N*K ids (they are few: the path is for small
+//     batches): per bin, the entries before the block's first entry (lower)
+//     and the others (upper), counted in shared memory, and the block's own
+//     ids kept;
+//  2. the bins' first rows, an exclusive scan of lower + upper over the bins
+//     (block 0 writes them out as bin_offsets);
+//  3. one warp walks the block's entries in order (lanes of a bin find each
+//     other with __match_any_sync) and continues the counts; for the
+//     tokens whose first unit is the block's it writes slot_row and
+//     recv_src_token, and, at the first entry of a rank s, the counts so far
+//     as bin_src_offsets[., s];
+//  4. the copy, then the owned tokens' scales.
+// The block's part of x is fetched while it counts.  With BULK (rows of at
+// least kLLFBulkMinRow bytes) one thread loads it into shared memory with a
+// bulk copy at the start, and in step 3 each lane of the walking warp stores
+// its entry's piece of the token row with a shared -> global bulk copy.  Else each
+// thread loads its kLLFJ vectors into registers before the counting and
+// stores them to the rows of their token (the register loads in flight slow
+// the shared-memory adds of step 1, which the bulk load does not: measured
+// 5.2 against 3.1 us for step 1 at R=8, N=128, top-8 of 256, H=7168).
+// Every block reads all ids, so the launcher takes this path only up to
+// kLLFMaxIds ids; the sort + dependent copy pair handles the rest.
+// ---------------------------------------------------------------------------
+#ifndef MP_LLF_THREADS
+#define MP_LLF_THREADS 512
+#endif
+#ifndef MP_LLF_BPS
+#define MP_LLF_BPS 2
+#endif
+#ifndef MP_LLF_J
+#define MP_LLF_J 3
+#endif
+#ifndef MP_LLF_MAX_IDS
+#define MP_LLF_MAX_IDS 16384
+#endif
+#ifndef MP_LLF_BULK_MIN_ROW
+#define MP_LLF_BULK_MIN_ROW 2048
+#endif
+constexpr int kLLFThreads = MP_LLF_THREADS;  // threads per block
+constexpr int kLLFBlocksPerSM = MP_LLF_BPS;  // blocks per SM
+constexpr int kLLFJ = MP_LLF_J;              // vectors per thread in flight (register copy)
+constexpr int64_t kLLFMaxIds = MP_LLF_MAX_IDS;
+constexpr int64_t kLLFBulkMinRow = MP_LLF_BULK_MIN_ROW;  // row bytes from which BULK is used
+constexpr int kLLFMaxBins = 2048;
+constexpr size_t kLLFMaxStage = 96 * 1024;  // shared-memory bytes of a block's part of x
+constexpr size_t kLLFMaxTable = 32 * 1024;  // shared-memory bytes of counts and rows
+
+struct LLFusedArgs {
+  int R, N, K, E, vpr, spr;
+  uint32_t stage_bytes;  // BULK: bytes reserved for the block's part of x (multiple of 128)
+  const int32_t* topk_idx;
+  int64_t recv_capacity;
+  int32_t* bin_offsets;
+  int32_t* bin_src_offsets;
+  int32_t* recv_src_token;
+  int32_t* slot_row;
+  const void* x;
+  void* recv_x;
+  const float* x_scales;
+  float* recv_scales;
+  int32_t* dev_err;
+};
+
+template <int NW, bool RANK_MAJOR, bool BULK>
+__global__ void __launch_bounds__(kLLFThreads, kLLFBlocksPerSM)
+mp_k_ll_dispatch_fused(LLFusedArgs a) {
+  pdl_launch_dependents();  // the weighted combine after it may stage its blocks
+  extern __shared__ __align__(128) unsigned char llf_smem[];
+  __shared__ int32_t warp_tot[kLLFThreads / kWarp];
+  constexpr int UB = 4 * NW;                 // bytes per unit
+  unsigned char* stage = llf_smem;           // BULK: the block's units of x
+  uint64_t* bar = reinterpret_cast<uint64_t*>(llf_smem + a.stage_bytes);
+  int32_t* lower = reinterpret_cast<int32_t*>(llf_smem + a.stage_bytes + 16);
+  const int nbins = RANK_MAJOR ? a.R : a.E;
+  const int El = a.E / a.R;
+  const int K = a.K;
+  int32_t* upper = lower + nbins;  // [nbins] the other entries, then the bins' first rows
+  int32_t* rows = upper + nbins;   // [block's entries] their ids, then their rows (-1: none)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = a.R * a.N;
+  const int V = T * a.vpr;  // < 2^30 (launcher)
+  const int vb0 = int(int64_t(V) * blockIdx.x / gridDim.x);
+  const int vb1 = int(int64_t(V) * (blockIdx.x + 1) / gridDim.x);
+  const int tf = vb0 / a.vpr;                             // first token touched
+  const int tl = vb1 > vb0 ? (vb1 - 1) / a.vpr + 1 : tf;  // one past the last
+  const int town = (vb0 + a.vpr - 1) / a.vpr;             // first token whose first unit is here
+  const int e0 = tf * K, e1 = tl * K;                     // the block's entries
+  const unsigned char* xb = static_cast<const unsigned char*>(a.x);
+  if (BULK && tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init_fence();
+    if (vb1 > vb0) {
+      const uint32_t bytes = uint32_t(vb1 - vb0) * UB;
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(stage, xb + int64_t(vb0) * UB, bytes, bar);
+    }
+  }
+  // 1. per-bin counts below and from the block's first entry; the block's own
+  //    ids kept in `rows` for the walk
+  const int nall = T * K;
+  const bool vec4 = (reinterpret_cast<uintptr_t>(a.topk_idx) & 15u) == 0;
+  const int n4 = vec4 ? nall / 4 : 0;
+  const int4* t4 = reinterpret_cast<const int4*>(a.topk_idx);
+  constexpr int L = 4;  // 16-byte id loads in flight per thread
+  int4 p[L];
+  auto load_ids = [&](int q0) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const int q = q0 + l * kLLFThreads;
+      p[l] = q < n4 ? __ldg(t4 + q) : make_int4(-1, -1, -1, -1);
+    }
+  };
+  bool bad = false;
+  auto count = [&](int i, int e) {
+    if (i >= e0 && i < e1) rows[i - e0] = e;
+    if (e < 0 || e >= a.E) {
+      bad |= e != -1;
+      return;
+    }
+    atomicAdd(i < e0 ? &lower[RANK_MAJOR ? e / El : e] : &upper[RANK_MAJOR ? e / El : e], 1);
+  };
+  auto count_ids = [&](int q0) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const int q = q0 + l * kLLFThreads;
+      if (q < n4) {
+        count(4 * q, p[l].x);
+        count(4 * q + 1, p[l].y);
+        count(4 * q + 2, p[l].z);
+        count(4 * q + 3, p[l].w);
+      }
+    }
+  };
+  load_ids(tid);
+  const Words<NW>* x = reinterpret_cast<const Words<NW>*>(xb);
+  Words<NW> v[BULK ? 1 : kLLFJ];
+  if (!BULK) {
+#pragma unroll
+    for (int j = 0; j < kLLFJ; ++j) {
+      const int q = vb0 + tid + j * kLLFThreads;
+      if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
+    }
+  }
+  for (int b = tid; b < 2 * nbins; b += kLLFThreads) lower[b] = 0;
+  __syncthreads();  // (also publishes the mbarrier's initialisation)
+  count_ids(tid);
+  for (int q0 = tid + L * kLLFThreads; q0 < n4; q0 += L * kLLFThreads) {
+    load_ids(q0);
+    count_ids(q0);
+  }
+  for (int i = 4 * n4 + tid; i < nall; i += kLLFThreads) count(i, __ldg(a.topk_idx + i));
+  if (bad && blockIdx.x == 0) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
+  __syncthreads();
+  // 2. the bins' first rows: each thread a run of consecutive bins, a warp
+  //    scan of the runs' totals, then a scan of the warps' totals
+  {
+    const int cpt = (nbins + kLLFThreads - 1) / kLLFThreads;
+    const int b0 = min(nbins, tid * cpt), b1 = min(nbins, b0 + cpt);
+    int chunk = 0;
+    for (int b = b0; b < b1; ++b) chunk += lower[b] + upper[b];
+    int inc = chunk;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < kLLFThreads / kWarp ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, w, o);
+        if (lane >= o) w += t;
+      }
+      if (lane < kLLFThreads / kWarp) warp_tot[lane] = w;
+    }
+    __syncthreads();
+    int base = (warp > 0 ? warp_tot[warp - 1] : 0) + inc - chunk;
+    for (int b = b0; b < b1; ++b) {
+      const int c = lower[b] + upper[b];
+      if (blockIdx.x == 0) a.bin_offsets[b] = base;
+      upper[b] = base;
+      base += c;
+    }
+    if (blockIdx.x == 0 && b0 < nbins && b1 == nbins) a.bin_offsets[nbins] = base;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // with BULK the entries' pieces are stored as the walk places them, once
+    // the block's units are in shared memory (a bounded wait; on a timeout
+    // report it, wait once more so the load is not left writing shared memory,
+    // and store nothing)
+    bool staged = false;
+    if (BULK && vb1 > vb0) {
+      uint32_t spins = 0;
+      staged = true;
+      while (!mbar_try_wait(bar, 0)) {
+        if (++spins > kSpinLimit) {
+          staged = false;
+          break;
+        }
+      }
+      if (!staged) {
+        if (lane == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
+        uint32_t n = 0;
+        while (!mbar_try_wait(bar, 0) && ++n < kSpinLimit) {
+        }
+      }
+    }
+    unsigned char* rxb = static_cast<unsigned char*>(a.recv_x);
+    // 3. the block's entries in order; a batch never crosses the first entry
+    //    of a rank
+    bool overflow = false;
+    const int NK = a.N * K;
+    for (int i0 = e0; i0 < e1;) {
+      const int i1 = min(min(i0 + kWarp, e1), (i0 / NK + 1) * NK);
+      if (i0 % NK == 0 && i0 / K >= town) {  // rank s begins with a token of this block
+        const int s = i0 / NK;
+        for (int b = lane; b < nbins; b += kWarp) a.bin_src_offsets[int64_t(b) * a.R + s] = lower[b];
+        __syncwarp();
+      }
+      const int i = i0 + lane;
+      const int e = i < i1 ? rows[i - e0] : -1;  // the id, replaced by its row below
+      const bool ok = e >= 0 && e < a.E;
+      const int b = ok ? (RANK_MAJOR ? e / El : e) : -1;
+      const unsigned peers = __match_any_sync(kFull, b);
+      const int run = ok ? lower[b] : 0;
+      __syncwarp();
+      int row = -1;
+      if (ok) {
+        const int64_t r = int64_t(upper[b]) + run + __popc(peers & lanemask_lt());
+        if (r < a.recv_capacity) row = int(r);
+        else overflow = true;
+        if ((peers >> lane) == 1u) lower[b] = run + __popc(peers);  // highest peer
+      }
+      if (i < i1) {
+        rows[i - e0] = row;
+        const int t = i / K;
+        if (t >= town) {
+          a.slot_row[i] = row;
+          if (row >= 0) a.recv_src_token[row] = t;
+        }
+        if (BULK && staged && row >= 0) {  // the entry's piece of its token's row
+          const int p0 = max(vb0, t * a.vpr), p1 = min(vb1, (t + 1) * a.vpr);
+          bulk_s2g(rxb + (int64_t(row) * a.vpr + (p0 - t * a.vpr)) * UB, stage + (p0 - vb0) * UB,
+                   uint32_t(p1 - p0) * UB);
+        }
+      }
+      __syncwarp();
+      i0 = i1;
+    }
+    if (overflow) raise_error(a.dev_err, MP_ERR_CAPACITY);
+    if (BULK && staged) {
+      bulk_commit();
+      bulk_wait_all();  // the pieces written (and shared memory no longer read)
+    }
+  }
+  __syncthreads();
+  // 4. the register copy (BULK: stored in step 3)
+  if (!BULK) {
+    Words<NW>* rx = static_cast<Words<NW>*>(a.recv_x);
+    for (int q0 = vb0; q0 < vb1; q0 += kLLFJ * kLLFThreads) {
+      if (q0 != vb0) {
+#pragma unroll
+        for (int j = 0; j < kLLFJ; ++j) {
+          const int q = q0 + tid + j * kLLFThreads;
+          if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kLLFJ; ++j) {
+        const int q = q0 + tid + j * kLLFThreads;
+        if (q < vb1) {
+          const int t = q / a.vpr;
+          const int off = q - t * a.vpr;
+          const int32_t* tr = rows + (t - tf) * K;
+          for (int k = 0; k < K; ++k) {
+            const int r = tr[k];
+            if (r >= 0) st_stream_w<NW>(rx + int64_t(r) * a.vpr + off, v[j]);
+          }
+        }
+      }
+    }
+  }
+  if (a.spr > 0) {
+    const int nown = (tl - town) * K;  // entries of the owned tokens (<= 0: none)
+    for (int idx = tid; idx < nown * a.spr; idx += kLLFThreads) {
+      const int ent = idx / a.spr, c = idx - ent * a.spr;
+      const int i = town * K + ent;
+      const int r = rows[i - e0];
+      if (r >= 0)
+        a.recv_scales[int64_t(r) * a.spr + c] = __ldg(a.x_scales + int64_t(i / K) * a.spr + c);
+    }
+  }
+}
+
+template <int NW, bool RANK_MAJOR, bool BULK>
+static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
+  const int nbins = RANK_MAJOR ? a.R : a.E;
+  const int64_t V = int64_t(a.R) * a.N * a.vpr;
+  int64_t G = int64_t(sm_count()) * kLLFBlocksPerSM;
+  if (G > V) G = V;
+  const int64_t vmax = (V + G - 1) / G;                 // units of one block at most
+  const int64_t tmax = (vmax + a.vpr - 1) / a.vpr + 1;  // tokens one block's units touch
+  const size_t table = sizeof(int32_t) * size_t(2 * nbins + tmax * a.K);
+  const size_t stage = BULK ? (size_t(vmax) * 4 * NW + 127) / 128 * 128 : 0;
+  if (table > kLLFMaxTable || stage > kLLFMaxStage) return cudaErrorNotSupported;
+  a.stage_bytes = uint32_t(stage);
+  const size_t smem = stage + 16 + table;
+  auto kernel = mp_k_ll_dispatch_fused<NW, RANK_MAJOR, BULK>;
+  static int configured[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && configured[dev] < int(smem)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = int(smem);
+  }
+  return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
+}
+
+cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
+                                     int64_t row_bytes, const int32_t* topk_idx,
+                                     int64_t recv_capacity, int32_t* bin_offsets,
+                                     int32_t* bin_src_offsets, int32_t* recv_src_token,
+                                     int32_t* slot_row, const void* x, int scales_per_row,
+                                     const float* x_scales, void* recv_x, float* recv_scales,
+                                     int32_t* dev_err, cudaStream_t stream) {
+  const int nbins = rank_major ? R : E;
+  const int64_t ids = int64_t(R) * N * K;
+  if (N <= 0 || ids > kLLFMaxIds || nbins > kLLFMaxBins || row_bytes % 16 != 0 ||
+      !aligned(x, 16) || !aligned(recv_x, 16))
+    return cudaErrorNotSupported;
+  const bool bulk = row_bytes >= kLLFBulkMinRow;
+  const bool wide = !bulk && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32);
+  const int64_t vpr = row_bytes / (wide ? 32 : 16);
+  if (int64_t(R) * N * vpr >= (int64_t(1) << 30)) return cudaErrorNotSupported;
+  const LLFusedArgs a{R,        N,           K,           E,        int(vpr),
+                      scales_per_row,        0,           topk_idx, recv_capacity,
+                      bin_offsets,           bin_src_offsets,       recv_src_token,
+                      slot_row, x,           recv_x,      x_scales, recv_scales,
+                      dev_err};
+  cudaError_t e;
+  if (bulk) {
+    e = rank_major ? ll_dispatch_fused_nw<4, true, true>(a, stream)
+                   : ll_dispatch_fused_nw<4, false, true>(a, stream);
+    if (e != cudaErrorNotSupported) return e;  // else the register copy (16-byte units)
+  }
+  if (wide)
+    return rank_major ? ll_dispatch_fused_nw<8, true, false>(a, stream)
+                      : ll_dispatch_fused_nw<8, false, false>(a, stream);
+  return rank_major ? ll_dispatch_fused_nw<4, true, false>(a, stream)
+                    : ll_dispatch_fused_nw<4, false, false>(a, stream);
+}
+
 }  // namespace mp

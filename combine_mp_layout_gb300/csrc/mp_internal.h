@@ -102,6 +102,18 @@ cudaError_t launch_ll_dispatch(int R, int N, int K, int E, int rank_major, int64
                                const float* x_scales, void* recv_x, float* recv_scales,
                                int32_t* dev_err, cudaStream_t stream);
 
+// The low-latency dispatch as one kernel whose blocks each count all R*N*K
+// ids (small batches with num_tokens_per_expert NULL): the same outputs as
+// launch_ll_dispatch.  cudaErrorNotSupported, with nothing launched, when the
+// problem is outside its limits.
+cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
+                                     int64_t row_bytes, const int32_t* topk_idx,
+                                     int64_t recv_capacity, int32_t* bin_offsets,
+                                     int32_t* bin_src_offsets, int32_t* recv_src_token,
+                                     int32_t* slot_row, const void* x, int scales_per_row,
+                                     const float* x_scales, void* recv_x, float* recv_scales,
+                                     int32_t* dev_err, cudaStream_t stream);
+
 // The low-latency row copy launched as a programmatic dependent of the kernel
 // before it on the stream (the LL sort): its row loads overlap that kernel,
 // its slot_row reads wait for it.  Only for use right after the sort.

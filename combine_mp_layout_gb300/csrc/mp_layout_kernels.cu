@@ -1606,6 +1606,13 @@ cudaError_t launch_ll_dispatch(int R, int N, int K, int E, int rank_major, int64
                                int32_t* slot_row, const void* x, int scales_per_row,
                                const float* x_scales, void* recv_x, float* recv_scales,
                                int32_t* dev_err, cudaStream_t stream) {
+  if (num_tokens_per_expert == nullptr) {
+    const cudaError_t f = launch_ll_dispatch_fused(
+        R, N, K, E, rank_major, row_bytes, topk_idx, recv_capacity, bin_offsets, bin_src_offsets,
+        recv_src_token, slot_row, x, scales_per_row, x_scales, recv_x, recv_scales, dev_err,
+        stream);
+    if (f != cudaErrorNotSupported) return f;
+  }
   cudaError_t e = launch_ll_offsets(R, N, K, E, rank_major, topk_idx, num_tokens_per_expert,
                                     recv_capacity, bin_offsets, bin_src_offsets, recv_src_token,
                                     slot_row, dev_err, stream);

@@ -908,7 +908,8 @@ LL_ONE_CALL = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=
                  dict(R=4, N=40, E=16, K=4, H=20480), dict(R=32, N=40, E=64, K=4, H=64),
                  dict(R=8, N=64, E=8192, K=8, H=64), dict(R=4, N=3000, E=64, K=6, H=64),
                  dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5), dict(R=1, N=40, E=3, K=3, H=64),
-                 dict(R=4, N=0, E=16, K=4, H=64), dict(R=2, N=50, E=64, K=32, H=64)]
+                 dict(R=4, N=0, E=16, K=4, H=64), dict(R=2, N=50, E=64, K=32, H=64),
+                 dict(R=16, N=1, E=32, K=4, H=64), dict(R=2, N=3, E=8, K=2, H=20480)]
 
 
 @pytest.mark.parametrize("cfg", LL_ONE_CALL, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
@@ -916,9 +917,11 @@ LL_ONE_CALL = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=
 @pytest.mark.parametrize("rank_major", [0, 1], ids=["expert_major", "rank_major"])
 @pytest.mark.parametrize("counts", ["layout", "self"])
 def test_low_latency_one_call_dispatch_matches_oracle(cfg, rank_major, counts):
-    """mp_dispatch_ll (the sort, then the row copy as its programmatic dependent, which
-    loads rows before waiting for the sort) against the oracle's LL layout and rows, three
-    calls in a row.  H=264 takes 16-byte vectors, H=20480 rows of several slabs."""
+    """mp_dispatch_ll against the oracle's LL layout and rows, three calls in a row.  With
+    counts="self" and up to 32,768 ids it is one kernel whose blocks each count every id
+    (N=1: every block's tokens begin ranks; R=2, N=3, H=20480: most blocks copy part of one
+    token and own none), else the sort and the row copy as its programmatic dependent.
+    H=264 takes 16-byte vectors, H=20480 rows of several slabs."""
     cfg = dict(cfg)
     cap_frac = cfg.pop("cap_frac", None)
     R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
@@ -1003,8 +1006,11 @@ def test_low_latency_one_call_dispatch_replays_as_a_cuda_graph():
         assert_bf16_close(wl.bf16_bits(out), comb, "combine_ll after replay")
 
 
-def test_low_latency_one_call_dispatch_e4m3_with_scales():
-    R, N, E, K, H = 4, 200, 32, 4, 384
+@pytest.mark.parametrize("H", [384, 4096], ids=["vector_copy", "bulk_copy"])
+def test_low_latency_one_call_dispatch_e4m3_with_scales(H):
+    """e4m3 rows with their scales through mp_dispatch_ll; rows of 4 KB take the bulk
+    copies of the one-kernel dispatch."""
+    R, N, E, K = 4, 200, 32, 4
     inp = wl.make_ep(dict(R=R, N=N, E=E, K=K, H=H, routing="uniform", dtype="e4m3"), seed=32)
     plan = EPPlan(R, N, K, E, H, "e4m3")
     plan.load(inp)
@@ -1121,6 +1127,41 @@ def test_low_latency_offsets_flag_bad_ids_when_counting_themselves():
     assert st == 0
     assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
     assert np.array_equal(eoff.cpu().numpy(), ll["expert_offsets"])
+
+
+@pytest.mark.parametrize("cfg", [dict(R=4, N=50, E=16, K=3, H=64),      # one kernel
+                                 dict(R=4, N=3000, E=16, K=3, H=64)],  # sort + row copy
+                         ids=["fused", "sort_then_copy"])
+def test_low_latency_one_call_dispatch_flags_bad_ids(cfg):
+    """Ids outside [-1, E) through mp_dispatch_ll counting itself: MP_ERR_BAD_EXPERT, no row
+    for them, every other entry placed as the oracle places it."""
+    R, N, E, K, H = cfg["R"], cfg["N"], cfg["E"], cfg["K"], cfg["H"]
+    inp = wl.make_ep(dict(cfg, routing="uniform", dtype="bf16"), seed=19)
+    inp.topk_idx[1, 3, 0] = E + 5
+    inp.topk_idx[2, 7, 2] = -4
+    inp.topk_idx[0, 0, 1] = -1
+    plan = EPPlan(R, N, K, E, H)
+    plan.load(inp)
+    cap = R * N * K
+    dev = "cuda"
+    eoff = torch.full((E + 1,), -3, dtype=torch.int32, device=dev)
+    esoff = torch.full((E, R), -3, dtype=torch.int32, device=dev)
+    src = torch.full((cap,), -3, dtype=torch.int32, device=dev)
+    slot = torch.full((R, N, K), -3, dtype=torch.int32, device=dev)
+    rx = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+    B.check(B.mp_dispatch_ll(R, N, K, E, H, B.MP_BF16, 0, plan.x, None, plan.topk_idx, None,
+                             cap, eoff, esoff, src, slot, rx, None, plan.dev_err))
+    torch.cuda.synchronize()
+    assert plan.device_error() == B.MP_ERR_BAD_EXPERT
+    ll, st = oracle.dispatch_ll(wl.bf16_bits(inp.x), inp.topk_idx, E)
+    assert st == 0  # the oracle treats ids outside [0, E) as "no row" without a status
+    n = ll["num_recv"]
+    assert slot[1, 3, 0].item() == -1 and slot[2, 7, 2].item() == -1
+    assert np.array_equal(slot.cpu().numpy(), ll["slot_row"])
+    assert np.array_equal(eoff.cpu().numpy(), ll["expert_offsets"])
+    assert np.array_equal(esoff.cpu().numpy(), ll["expert_src_offsets"])
+    assert np.array_equal(src[:n].cpu().numpy(), ll["recv_src_token"])
+    assert np.array_equal(wl.bf16_bits(rx[:n]), ll["recv_x"])
 
 
 @pytest.mark.parametrize("wide", [False, True], ids=["16B", "32B"])
