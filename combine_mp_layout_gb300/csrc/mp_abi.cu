@@ -301,10 +301,17 @@ int mp_layout_dispatch(int R, int N, int K, int E, int H, int dtype, const void*
   const bool fp8 = dtype == MP_E4M3;
   const int64_t row_bytes = fp8 ? int64_t(H) : int64_t(H) * 2;
   const int spr = fp8 ? H / MP_SCALE_BLOCK : 0;
-  // one launch for layout + offsets (receive metadata left out: a thread-block
-  // cluster for small batches, else a cooperative grid), then the row copy,
-  // which writes the metadata, as its programmatic dependent
-  cudaError_t e = launch_layout_cluster(
+  // small batches: one kernel whose blocks each count every token
+  cudaError_t e = launch_layout_dispatch_fused(
+      R, N, K, E, row_bytes, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
+      num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
+      recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, x, spr,
+      x_scales, recv_x, recv_scales, dev_err, cs);
+  if (e != cudaErrorNotSupported) return cuda_status(e);
+  // else one launch for layout + offsets (receive metadata left out: a
+  // thread-block cluster for small batches, else a cooperative grid), then the
+  // row copy, which writes the metadata, as its programmatic dependent
+  e = launch_layout_cluster(
       R, N, K, E, topk_idx, topk_weights, recv_capacity, num_tokens_per_rank,
       num_tokens_per_expert, is_token_in_rank, recv_src_rank, recv_src_idx, recv_topk_idx,
       recv_topk_weights, dest_offsets, rank_prefix, num_recv_tokens_per_expert, send_row, dev_err,

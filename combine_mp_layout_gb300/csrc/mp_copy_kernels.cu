@@ -1358,6 +1358,48 @@ constexpr int kLLFMaxBins = 2048;
 constexpr size_t kLLFMaxStage = 96 * 1024;  // shared-memory bytes of a block's part of x
 constexpr size_t kLLFMaxTable = 32 * 1024;  // shared-memory bytes of counts and rows
 
+// BULK staging of a block's units [vb0, vb1) of x: one bulk load into shared
+// memory completing on one mbarrier (issued by one thread).  Loading each
+// token's part on its own mbarrier, so that stores could start after the first
+// part, measured slower (R=8, N=128, top-8 of 256, H=7168: low-latency step
+// 48.6 vs 47.9 us, dsv3 step 41.2 vs 40.4 us).
+template <int UB>
+__device__ __forceinline__ void stage_units(unsigned char* stage, uint64_t* bar,
+                                            const unsigned char* xb, int vb0, int vb1) {
+  mbar_init(bar, 1);
+  mbar_init_fence();
+  if (vb1 > vb0) {
+    const uint32_t bytes = uint32_t(vb1 - vb0) * UB;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(stage, xb + int64_t(vb0) * UB, bytes, bar);
+  }
+}
+
+// A bounded wait for the staged units: false (after raising MP_ERR_TIMEOUT) if
+// it gave up.
+__device__ __forceinline__ bool wait_staged(uint64_t* bar, int32_t* dev_err) {
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, 0)) {
+    if (++spins > kSpinLimit) {
+      raise_error(dev_err, MP_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Before the block exits (warp 0): the staged load has landed (a bounded wait,
+// at once when it was waited for already), and every bulk store of this
+// thread has been performed.
+__device__ __forceinline__ void drain_stage(uint64_t* bar, bool staged_any, int lane) {
+  if (lane == 0 && staged_any) {
+    uint32_t n = 0;
+    while (!mbar_try_wait(bar, 0) && ++n < kSpinLimit) {
+    }
+  }
+  bulk_wait_all();
+}
+
 struct LLFusedArgs {
   int R, N, K, E, vpr, spr;
   uint32_t stage_bytes;  // BULK: bytes reserved for the block's part of x (multiple of 128)
@@ -1399,15 +1441,7 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
   const int town = (vb0 + a.vpr - 1) / a.vpr;             // first token whose first unit is here
   const int e0 = tf * K, e1 = tl * K;                     // the block's entries
   const unsigned char* xb = static_cast<const unsigned char*>(a.x);
-  if (BULK && tid == 0) {
-    mbar_init(bar, 1);
-    mbar_init_fence();
-    if (vb1 > vb0) {
-      const uint32_t bytes = uint32_t(vb1 - vb0) * UB;
-      mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(stage, xb + int64_t(vb0) * UB, bytes, bar);
-    }
-  }
+  if (BULK && tid == 0) stage_units<UB>(stage, bar, xb, vb0, vb1);
   // 1. per-bin counts below and from the block's first entry; the block's own
   //    ids kept in `rows` for the walk
   const int nall = T * K;
@@ -1500,27 +1534,10 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
   }
   __syncthreads();
   if (warp == 0) {
-    // with BULK the entries' pieces are stored as the walk places them, once
-    // the block's units are in shared memory (a bounded wait; on a timeout
-    // report it, wait once more so the load is not left writing shared memory,
-    // and store nothing)
-    bool staged = false;
-    if (BULK && vb1 > vb0) {
-      uint32_t spins = 0;
-      staged = true;
-      while (!mbar_try_wait(bar, 0)) {
-        if (++spins > kSpinLimit) {
-          staged = false;
-          break;
-        }
-      }
-      if (!staged) {
-        if (lane == 0) raise_error(a.dev_err, MP_ERR_TIMEOUT);
-        uint32_t n = 0;
-        while (!mbar_try_wait(bar, 0) && ++n < kSpinLimit) {
-        }
-      }
-    }
+    // with BULK each entry's piece is stored as the walk places it, once the
+    // block's units are in shared memory (a bounded wait; a lane that gives up
+    // stores nothing)
+    bool staged = true;
     unsigned char* rxb = static_cast<unsigned char*>(a.recv_x);
     // 3. the block's entries in order; a batch never crosses the first entry
     //    of a rank
@@ -1554,7 +1571,7 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
           a.slot_row[i] = row;
           if (row >= 0) a.recv_src_token[row] = t;
         }
-        if (BULK && staged && row >= 0) {  // the entry's piece of its token's row
+        if (BULK && row >= 0 && staged && (staged = wait_staged(bar, a.dev_err))) {
           const int p0 = max(vb0, t * a.vpr), p1 = min(vb1, (t + 1) * a.vpr);
           bulk_s2g(rxb + (int64_t(row) * a.vpr + (p0 - t * a.vpr)) * UB, stage + (p0 - vb0) * UB,
                    uint32_t(p1 - p0) * UB);
@@ -1564,9 +1581,9 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
       i0 = i1;
     }
     if (overflow) raise_error(a.dev_err, MP_ERR_CAPACITY);
-    if (BULK && staged) {
+    if (BULK) {
       bulk_commit();
-      bulk_wait_all();  // the pieces written (and shared memory no longer read)
+      drain_stage(bar, vb1 > vb0, lane);  // the load landed, the pieces written
     }
   }
   __syncthreads();
@@ -1634,6 +1651,406 @@ static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
   return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
 }
 
+// ---------------------------------------------------------------------------
+// The whole high-throughput dispatch in one kernel for small batches (layout,
+// receive offsets, receive metadata and row copy), no block waiting for
+// another.  The rows of destination d are ordered by source rank and token,
+// which is the flat token index t = s*N + n, so token t's row on d is
+// dest_offsets[d] + P(t, d), P(t, d) = the number of tokens t' < t that go to
+// d.  Block b copies the units [V*b/G, V*(b+1)/G) of the token-major row
+// space, like the low-latency kernel above:
+//  1. one pass over all tokens: each token's destination mask from its K ids;
+//     per destination, the tokens before the block's first (lower = P(tf, .)),
+//     the others (upper), and the tokens before the end of the last rank whose
+//     first token the block owns (rend);
+//  2. warp 0: dest_offsets (a scan of lower + upper; block 0 writes it), then
+//     it walks the block's tokens in order, 32 at a time, placing each token
+//     on each of its destinations with a ballot, and stores (BULK) each row's
+//     piece as it is placed; for the tokens whose first unit is the block's it
+//     writes is_token_in_rank and send_row, and keeps P(s*N, .) for each rank
+//     s that begins with one of them;
+//  3. all threads: rank_prefix[s] = P(s*N, .) and num_tokens_per_rank[s] (the
+//     difference to the next rank's P) for those ranks, the receive metadata of
+//     the owned tokens' rows, the register copy (without BULK) and the scales;
+//  4. one job per block while the bulk copies run: job j < R counts source
+//     rank j's ids per expert (num_tokens_per_expert[j]), job R every id
+//     (num_recv_tokens_per_expert).
+// The pass of step 1 keeps its counts in registers (four 8-bit fields per
+// word; a lane leads at most 8 tokens within the id limit) and reduces them
+// over the warp once at the end, and issues its first id loads before the
+// block's x: a warp reduction per destination and group of tokens, or the ids
+// queued behind x, cost several microseconds at R=8, N=128 (every block reads
+// every id).
+// ---------------------------------------------------------------------------
+struct HTFusedArgs {
+  int R, N, K, E, vpr, spr;
+  uint32_t stage_bytes;  // BULK: bytes reserved for the block's part of x (multiple of 128)
+  int tmax;              // tokens one block's units touch, at most
+  const int32_t* topk_idx;
+  const float* topk_weights;
+  int64_t recv_capacity;
+  int32_t* num_tokens_per_rank;
+  int32_t* num_tokens_per_expert;
+  uint32_t* is_token_in_rank;
+  int32_t* recv_src_rank;
+  int32_t* recv_src_idx;
+  int32_t* recv_topk_idx;
+  float* recv_topk_weights;
+  int32_t* dest_offsets;
+  int32_t* rank_prefix;
+  int32_t* num_recv_tokens_per_expert;
+  int32_t* send_row;
+  const void* x;
+  void* recv_x;
+  const float* x_scales;
+  float* recv_scales;
+  int32_t* dev_err;
+};
+
+// shared-memory int32 words of the fused dispatch's tables
+__host__ __device__ inline int htf_table_words(int R, int E, int tmax) {
+  return 3 * R + E + 2 * tmax * R + tmax;
+}
+
+template <int NW, bool BULK>
+__global__ void __launch_bounds__(kLLFThreads, kLLFBlocksPerSM)
+mp_k_layout_dispatch_fused(HTFusedArgs a) {
+  pdl_launch_dependents();  // the combine after it may stage its blocks
+  extern __shared__ __align__(128) unsigned char htf_smem[];
+  constexpr int UB = 4 * NW;  // bytes per unit
+  constexpr int L = 4;        // 16-byte id loads in flight per thread
+  const int R = a.R, N = a.N, K = a.K, E = a.E, El = E / R;
+  unsigned char* stage = htf_smem;  // BULK: the block's units of x
+  uint64_t* bar = reinterpret_cast<uint64_t*>(htf_smem + a.stage_bytes);
+  int32_t* lower = reinterpret_cast<int32_t*>(htf_smem + a.stage_bytes + 16);  // [R]
+  int32_t* upper = lower + R;                      // [R]
+  int32_t* rend = upper + R;                       // [R]
+  int32_t* hist = rend + R;                        // [E] expert counts (step 4)
+  int32_t* rows = hist + E;                        // [tmax][R] the block's tokens' rows
+  int32_t* pref = rows + a.tmax * R;               // [tmax][R] P(s*N, .) of its ranks
+  uint32_t* masks = reinterpret_cast<uint32_t*>(pref + a.tmax * R);  // [tmax]
+  __shared__ int sh_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = R * N;
+  const int V = T * a.vpr;  // < 2^30 (launcher)
+  const int vb0 = int(int64_t(V) * blockIdx.x / gridDim.x);
+  const int vb1 = int(int64_t(V) * (blockIdx.x + 1) / gridDim.x);
+  const int tf = vb0 / a.vpr;                             // first token touched
+  const int tl = vb1 > vb0 ? (vb1 - 1) / a.vpr + 1 : tf;  // one past the last
+  const int town = (vb0 + a.vpr - 1) / a.vpr;             // first token whose first unit is here
+  // the ranks s whose first token s*N is owned: [s_lo, s_lo + nranks)
+  const int s_lo = (town + N - 1) / N;
+  const int nranks = max(0, (tl - 1) / N - s_lo + 1);
+  const int split2 = nranks > 0 ? (s_lo + nranks) * N : -1;  // rend counts the tokens below
+  const unsigned char* xb = static_cast<const unsigned char*>(a.x);
+  const Words<NW>* x = reinterpret_cast<const Words<NW>*>(xb);
+  // e / El as a multiply-high (exact for every e, El < 8192 above 1)
+  const uint32_t el_magic = El > 1 ? 0xFFFFFFFFu / uint32_t(El) + 1u : 0u;
+  auto dest_of = [&](int e) { return El > 1 ? int(__umulhi(uint32_t(e), el_magic)) : e; };
+  bool bad = false;
+  auto add_mask = [&](uint32_t& m, int e) {
+    if (e == -1) return;
+    if (e < -1 || e >= E) {
+      bad = true;
+      return;
+    }
+    m |= 1u << dest_of(e);
+  };
+  const int G4 = K / 4;  // 16-byte id vectors per token
+  const bool vec = K % 4 == 0 && (kWarp % G4) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.topk_idx) & 15u) == 0;
+  const int4* t4 = reinterpret_cast<const int4*>(a.topk_idx);
+  int4 p[L];
+  auto load_ids = [&](int base, int q1) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const int q = base + l * kLLFThreads + tid;
+      p[l] = q < q1 ? __ldg(t4 + q) : make_int4(-1, -1, -1, -1);
+    }
+  };
+  // 1. every token's destinations.  The first id loads go out first, then the
+  //    block's x with BULK (x and the ids are inputs of the call, complete at
+  //    launch; without BULK the row vectors are loaded after this pass).
+  if (vec) load_ids(0, T * G4);
+  for (int i = tid; i < 3 * R; i += kLLFThreads) lower[i] = 0;  // lower, upper, rend
+  if (tid == 0) sh_bad = 0;
+  __syncthreads();
+  // (the stage's mbarrier is first waited on after the next block barrier)
+  if (BULK && tid == 0) stage_units<UB>(stage, bar, xb, vb0, vb1);
+  {
+    const int nw = (R + 3) / 4;  // count words (4 destinations each)
+    uint32_t ca[8], cb[8], cc[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) ca[w] = cb[w] = cc[w] = 0u;
+    auto tally = [&](int t, uint32_t m) {
+      if (t >= tf && t < tl) masks[t - tf] = m;
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (w < nw) {
+          const uint32_t u = m >> (4 * w);  // bits 0..3 to the low bit of bytes 0..3
+          const uint32_t sp = (u & 1u) | ((u & 2u) << 7) | ((u & 4u) << 14) | ((u & 8u) << 21);
+          if (t < tf) ca[w] += sp;
+          else cb[w] += sp;
+          if (t < split2) cc[w] += sp;
+        }
+    };
+    if (vec) {  // a token's K/4 vectors on neighbouring lanes, masks OR-ed by shuffles
+      const int q1 = T * G4;
+      for (int base = 0; base < q1; base += L * kLLFThreads) {
+        if (base != 0) load_ids(base, q1);
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const int q = base + l * kLLFThreads + tid;
+          uint32_t m = 0u;
+          add_mask(m, p[l].x);
+          add_mask(m, p[l].y);
+          add_mask(m, p[l].z);
+          add_mask(m, p[l].w);
+          for (int o = 1; o < G4; o <<= 1) m |= __shfl_xor_sync(kFull, m, o);
+          if (q < q1 && (lane & (G4 - 1)) == 0) tally(q / G4, m);
+        }
+      }
+    } else {  // one token per thread
+      for (int t = tid; t < T; t += kLLFThreads) {
+        uint32_t m = 0u;
+        for (int k = 0; k < K; ++k) add_mask(m, __ldg(a.topk_idx + int64_t(t) * K + k));
+        tally(t, m);
+      }
+    }
+    // one warp reduction per destination and count, then one shared add
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int d = 4 * w + j;
+        if (d < R) {
+          const int sa = __reduce_add_sync(kFull, (ca[w] >> (8 * j)) & 0xffu);
+          const int sb = __reduce_add_sync(kFull, (cb[w] >> (8 * j)) & 0xffu);
+          const int sc = split2 >= 0 ? __reduce_add_sync(kFull, (cc[w] >> (8 * j)) & 0xffu) : 0;
+          if (lane == 0) {
+            if (sa) atomicAdd(&lower[d], sa);
+            if (sb) atomicAdd(&upper[d], sb);
+            if (sc) atomicAdd(&rend[d], sc);
+          }
+        }
+      }
+  }
+  if (bad) sh_bad = 1;
+  __syncthreads();
+  if (sh_bad && blockIdx.x == 0 && tid == 0) raise_error(a.dev_err, MP_ERR_BAD_EXPERT);
+  Words<NW> v[BULK ? 1 : kLLFJ];  // the register copy's first vectors, in flight during the walk
+  if (!BULK) {
+#pragma unroll
+    for (int j = 0; j < kLLFJ; ++j) {
+      const int q = vb0 + tid + j * kLLFThreads;
+      if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
+    }
+  }
+  // 2. (warp 0) dest_offsets, then the walk
+  if (warp == 0) {
+    const int col = lane < R ? lower[lane] + upper[lane] : 0;  // lane d: tokens to d
+    int inc = col;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const int base = inc - col;  // lane d: dest_offsets[d]
+    if (blockIdx.x == 0 && lane < R) {
+      a.dest_offsets[lane] = base;
+      if (lane == R - 1) a.dest_offsets[R] = inc;
+    }
+    int low = lane < R ? lower[lane] : 0;  // lane d: P(next token of the walk, d)
+    bool staged = true;  // BULK: the block's units arrived (a bounded wait)
+    unsigned char* rxb = static_cast<unsigned char*>(a.recv_x);
+    bool overflow = false;
+    for (int t0 = tf; t0 < tl; t0 += kWarp) {
+      const int t = t0 + lane;
+      const bool valid = t < tl;
+      const uint32_t m = valid ? masks[t - tf] : 0u;
+      const bool rank_start = valid && t >= town && t % N == 0;
+      int p0 = 0, p1 = 0;
+      if (valid) p0 = max(vb0, t * a.vpr), p1 = min(vb1, (t + 1) * a.vpr);
+      for (int d = 0; d < R; ++d) {
+        const bool hit = (m >> d) & 1u;
+        const unsigned b = __ballot_sync(kFull, hit);
+        const int ld = __shfl_sync(kFull, low, d), bd = __shfl_sync(kFull, base, d);
+        if (lane == d) low += __popc(b);
+        const int before = ld + __popc(b & lanemask_lt());  // P(t, d)
+        if (rank_start) pref[(t / N - s_lo) * R + d] = before;
+        int row = -1;
+        if (hit) {
+          const int64_t r = int64_t(bd) + before;
+          if (r < a.recv_capacity) row = int(r);
+          else overflow = true;
+        }
+        if (valid) {
+          rows[(t - tf) * R + d] = row;
+          if (t >= town) a.send_row[int64_t(t) * R + d] = row;
+          if (BULK && row >= 0 && staged && (staged = wait_staged(bar, a.dev_err)))
+            bulk_s2g(rxb + (int64_t(row) * a.vpr + (p0 - t * a.vpr)) * UB,
+                     stage + (p0 - vb0) * UB, uint32_t(p1 - p0) * UB);
+        }
+      }
+      if (valid && t >= town) a.is_token_in_rank[t] = m;
+    }
+    if (overflow) raise_error(a.dev_err, MP_ERR_CAPACITY);
+    if (BULK) bulk_commit();
+  }
+  __syncthreads();
+  // 3. the tables of the ranks beginning here, the metadata of the owned
+  //    tokens' rows, the register copy, the scales
+  for (int idx = tid; idx < nranks * R; idx += kLLFThreads) {
+    const int i = idx / R, d = idx - i * R, s = s_lo + i;
+    const int here = pref[i * R + d];
+    const int next = i + 1 < nranks ? pref[(i + 1) * R + d] : rend[d];
+    a.rank_prefix[s * R + d] = here;
+    a.num_tokens_per_rank[s * R + d] = next - here;
+  }
+  const int nown = tl - town;  // (<= 0: none)
+  for (int idx = tid; idx < nown * R * K; idx += kLLFThreads) {
+    const int j = idx / (R * K), rem = idx - j * R * K, d = rem / K, k = rem - d * K;
+    const int t = town + j;
+    const int r = rows[(t - tf) * R + d];
+    if (r < 0) continue;
+    const int e = __ldg(a.topk_idx + int64_t(t) * K + k);
+    const int lo = d * El;
+    const bool local = e >= lo && e < lo + El;
+    a.recv_topk_idx[int64_t(r) * K + k] = local ? e - lo : -1;
+    a.recv_topk_weights[int64_t(r) * K + k] = local ? __ldg(a.topk_weights + int64_t(t) * K + k) : 0.0f;
+    if (k == 0) {
+      a.recv_src_rank[r] = t / N;
+      a.recv_src_idx[r] = t - (t / N) * N;
+    }
+  }
+  if (!BULK) {
+    Words<NW>* rx = static_cast<Words<NW>*>(a.recv_x);
+    for (int q0 = vb0; q0 < vb1; q0 += kLLFJ * kLLFThreads) {
+      if (q0 != vb0) {
+#pragma unroll
+        for (int j = 0; j < kLLFJ; ++j) {
+          const int q = q0 + tid + j * kLLFThreads;
+          if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kLLFJ; ++j) {
+        const int q = q0 + tid + j * kLLFThreads;
+        if (q < vb1) {
+          const int t = q / a.vpr;
+          const int off = q - t * a.vpr;
+          const int32_t* tr = rows + (t - tf) * R;
+          for (int d = 0; d < R; ++d) {
+            const int r = tr[d];
+            if (r >= 0) st_stream_w<NW>(rx + int64_t(r) * a.vpr + off, v[j]);
+          }
+        }
+      }
+    }
+  }
+  if (a.spr > 0) {
+    for (int idx = tid; idx < nown * R * a.spr; idx += kLLFThreads) {
+      const int j = idx / (R * a.spr), rem = idx - j * R * a.spr, d = rem / a.spr,
+                c = rem - d * a.spr;
+      const int t = town + j;
+      const int r = rows[(t - tf) * R + d];
+      if (r >= 0)
+        a.recv_scales[int64_t(r) * a.spr + c] = __ldg(a.x_scales + int64_t(t) * a.spr + c);
+    }
+  }
+  // 4. job j < R: source rank j's expert counts; job R: every id's expert
+  for (int job = blockIdx.x; job <= R; job += gridDim.x) {
+    for (int i = tid; i < E; i += kLLFThreads) hist[i] = 0;
+    __syncthreads();
+    const int i0 = job < R ? job * N * K : 0;
+    const int i1 = job < R ? i0 + N * K : T * K;
+    int i4 = i0;  // 16-byte loads, L in flight per thread, where the range allows
+    if ((reinterpret_cast<uintptr_t>(a.topk_idx) & 15u) == 0 && i0 % 4 == 0) {
+      const int q1 = i1 / 4;
+      for (int q0 = i0 / 4; q0 < q1; q0 += L * kLLFThreads) {
+        load_ids(q0, q1);
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const int e4[4] = {p[l].x, p[l].y, p[l].z, p[l].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (e4[j] >= 0 && e4[j] < E) atomicAdd(&hist[e4[j]], 1);
+        }
+      }
+      i4 = 4 * q1;
+    }
+    for (int i = i4 + tid; i < i1; i += kLLFThreads) {
+      const int e = __ldg(a.topk_idx + i);
+      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    int32_t* out = job < R ? a.num_tokens_per_expert + int64_t(job) * E : a.num_recv_tokens_per_expert;
+    for (int e = tid; e < E; e += kLLFThreads) out[e] = hist[e];
+    __syncthreads();
+  }
+  if (BULK && warp == 0) drain_stage(bar, vb1 > vb0, lane);  // the load landed, pieces written
+}
+
+template <int NW, bool BULK>
+static cudaError_t layout_dispatch_fused_nw(HTFusedArgs a, cudaStream_t stream) {
+  const int64_t V = int64_t(a.R) * a.N * a.vpr;
+  int64_t G = int64_t(sm_count()) * kLLFBlocksPerSM;
+  if (G > V) G = V;
+  const int64_t vmax = (V + G - 1) / G;
+  const int64_t tmax = (vmax + a.vpr - 1) / a.vpr + 1;
+  const size_t table = sizeof(int32_t) * size_t(htf_table_words(a.R, a.E, int(tmax)));
+  const size_t stage = BULK ? (size_t(vmax) * 4 * NW + 127) / 128 * 128 : 0;
+  if (table > kLLFMaxTable || stage > kLLFMaxStage) return cudaErrorNotSupported;
+  a.stage_bytes = uint32_t(stage);
+  a.tmax = int(tmax);
+  const size_t smem = stage + 16 + table;
+  auto kernel = mp_k_layout_dispatch_fused<NW, BULK>;
+  static int configured[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && configured[dev] < int(smem)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = int(smem);
+  }
+  return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
+}
+
+cudaError_t launch_layout_dispatch_fused(
+    int R, int N, int K, int E, int64_t row_bytes, const int32_t* topk_idx,
+    const float* topk_weights, int64_t recv_capacity, int32_t* num_tokens_per_rank,
+    int32_t* num_tokens_per_expert, uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+    int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+    int32_t* dest_offsets, int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+    int32_t* send_row, const void* x, int scales_per_row, const float* x_scales, void* recv_x,
+    float* recv_scales, int32_t* dev_err, cudaStream_t stream) {
+  const int64_t ids = int64_t(R) * N * K;
+  if (N <= 0 || ids > kLLFMaxIds || R > 32 || row_bytes % 16 != 0 || !aligned(x, 16) ||
+      !aligned(recv_x, 16))
+    return cudaErrorNotSupported;
+  const bool bulk = row_bytes >= kLLFBulkMinRow;
+  const bool wide = !bulk && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32);
+  const int64_t vpr = row_bytes / (wide ? 32 : 16);
+  if (int64_t(R) * N * vpr >= (int64_t(1) << 30)) return cudaErrorNotSupported;
+  HTFusedArgs a{};
+  a.R = R, a.N = N, a.K = K, a.E = E, a.vpr = int(vpr), a.spr = scales_per_row;
+  a.topk_idx = topk_idx, a.topk_weights = topk_weights, a.recv_capacity = recv_capacity;
+  a.num_tokens_per_rank = num_tokens_per_rank, a.num_tokens_per_expert = num_tokens_per_expert;
+  a.is_token_in_rank = is_token_in_rank, a.recv_src_rank = recv_src_rank;
+  a.recv_src_idx = recv_src_idx, a.recv_topk_idx = recv_topk_idx;
+  a.recv_topk_weights = recv_topk_weights, a.dest_offsets = dest_offsets;
+  a.rank_prefix = rank_prefix, a.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
+  a.send_row = send_row, a.x = x, a.recv_x = recv_x, a.x_scales = x_scales;
+  a.recv_scales = recv_scales, a.dev_err = dev_err;
+  if (bulk) {
+    const cudaError_t e = layout_dispatch_fused_nw<4, true>(a, stream);
+    if (e != cudaErrorNotSupported) return e;  // else the register copy (16-byte units)
+  }
+  if (wide) return layout_dispatch_fused_nw<8, false>(a, stream);
+  return layout_dispatch_fused_nw<4, false>(a, stream);
+}
+
 cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
                                      int64_t row_bytes, const int32_t* topk_idx,
                                      int64_t recv_capacity, int32_t* bin_offsets,
@@ -1650,11 +2067,12 @@ cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
   const bool wide = !bulk && row_bytes % 32 == 0 && aligned(x, 32) && aligned(recv_x, 32);
   const int64_t vpr = row_bytes / (wide ? 32 : 16);
   if (int64_t(R) * N * vpr >= (int64_t(1) << 30)) return cudaErrorNotSupported;
-  const LLFusedArgs a{R,        N,           K,           E,        int(vpr),
-                      scales_per_row,        0,           topk_idx, recv_capacity,
-                      bin_offsets,           bin_src_offsets,       recv_src_token,
-                      slot_row, x,           recv_x,      x_scales, recv_scales,
-                      dev_err};
+  LLFusedArgs a{};
+  a.R = R, a.N = N, a.K = K, a.E = E, a.vpr = int(vpr), a.spr = scales_per_row;
+  a.topk_idx = topk_idx, a.recv_capacity = recv_capacity, a.bin_offsets = bin_offsets;
+  a.bin_src_offsets = bin_src_offsets, a.recv_src_token = recv_src_token, a.slot_row = slot_row;
+  a.x = x, a.recv_x = recv_x, a.x_scales = x_scales, a.recv_scales = recv_scales;
+  a.dev_err = dev_err;
   cudaError_t e;
   if (bulk) {
     e = rank_major ? ll_dispatch_fused_nw<4, true, true>(a, stream)

@@ -114,6 +114,18 @@ cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
                                      const float* x_scales, void* recv_x, float* recv_scales,
                                      int32_t* dev_err, cudaStream_t stream);
 
+// The whole high-throughput dispatch (mp_layout_dispatch's outputs) as one
+// kernel whose blocks each count every token, for small batches.
+// cudaErrorNotSupported, with nothing launched, outside its limits.
+cudaError_t launch_layout_dispatch_fused(
+    int R, int N, int K, int E, int64_t row_bytes, const int32_t* topk_idx,
+    const float* topk_weights, int64_t recv_capacity, int32_t* num_tokens_per_rank,
+    int32_t* num_tokens_per_expert, uint32_t* is_token_in_rank, int32_t* recv_src_rank,
+    int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+    int32_t* dest_offsets, int32_t* rank_prefix, int32_t* num_recv_tokens_per_expert,
+    int32_t* send_row, const void* x, int scales_per_row, const float* x_scales, void* recv_x,
+    float* recv_scales, int32_t* dev_err, cudaStream_t stream);
+
 // The low-latency row copy launched as a programmatic dependent of the kernel
 // before it on the stream (the LL sort): its row loads overlap that kernel,
 // its slot_row reads wait for it.  Only for use right after the sort.

@@ -620,6 +620,29 @@ def test_one_call_dispatch_capacity_and_bad_ids():
     compare_ep(inp, plan, recv_capacity=700, expect_err=B.MP_ERR_CAPACITY | B.MP_ERR_BAD_EXPERT)
 
 
+@pytest.mark.parametrize("cfg", [dict(R=5, N=77, E=20, K=6, H=2056, dtype="bf16"),
+                                 dict(R=4, N=150, E=32, K=4, H=4096, dtype="e4m3"),
+                                 dict(R=8, N=60, E=64, K=8, H=1024, dtype="bf16", cap=900),
+                                 dict(R=2, N=3, E=8, K=2, H=20480, dtype="bf16"),
+                                 dict(R=16, N=1, E=32, K=4, H=7168, dtype="bf16")],
+                         ids=["ragged", "e4m3_scales", "capacity", "blocks_inside_a_token",
+                              "one_token_per_rank"])
+def test_one_call_dispatch_bulk_copies(cfg):
+    """mp_layout_dispatch at small batches with rows of 2 KB or more: one kernel whose
+    blocks count every token, bulk-load their part of x and bulk-store each row piece."""
+    cfg = dict(cfg)
+    cap = cfg.pop("cap", None)
+    inp = wl.make_ep(dict(cfg, routing="uniform"), seed=cfg["N"] + cfg["H"])
+    idx = inp.topk_idx.copy()
+    idx[:, ::5, 0] = -1
+    inp.topk_idx = idx
+    y = wl.random_bf16((inp.R * inp.N * min(inp.R, inp.K), inp.H), seed=3)
+    plan = run_gpu_one_call(inp, recv_capacity=cap, y=y.cuda(), repeat=2)
+    compare_ep(inp, plan, recv_capacity=cap, y_bits=wl.bf16_bits(y),
+               expect_err=B.MP_ERR_CAPACITY if cap is not None else 0,
+               what="one-kernel dispatch combine(y)")
+
+
 def test_one_call_dispatch_falls_back_beyond_one_grid():
     """Beyond one resident grid the one-call dispatch runs the layout, scan and row-copy
     kernels one after another, with the same results."""
