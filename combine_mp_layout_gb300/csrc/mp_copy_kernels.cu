@@ -1712,8 +1712,17 @@ __host__ __device__ inline int htf_table_words(int R, int E, int tmax) {
   return 3 * R + E + 2 * tmax * R + tmax;
 }
 
-template <int NW, bool BULK>
-__global__ void __launch_bounds__(kLLFThreads, kLLFBlocksPerSM)
+// The one-kernel high-throughput dispatch's launch shape: one block per SM.
+// Its counting pass costs every block the same whatever its share, so fewer,
+// larger blocks count less in all (dsv3 N=256 step 70.2 -> 66.8 us against two
+// blocks of 512 threads per SM); 512 threads up to kHTFSmallIds ids (N=128 step
+// 37.9 us, against 39.3 with 1,024), 1,024 above.
+constexpr int64_t kHTFSmallIds = 8192;
+// a block's stage of x: what the SM's shared memory leaves beside the tables
+constexpr size_t kHTFMaxStage = 192 * 1024;
+
+template <int NW, bool BULK, int NT>
+__global__ void __launch_bounds__(NT, 1)
 mp_k_layout_dispatch_fused(HTFusedArgs a) {
   pdl_launch_dependents();  // the combine after it may stage its blocks
   extern __shared__ __align__(128) unsigned char htf_smem[];
@@ -1764,7 +1773,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   auto load_ids = [&](int base, int q1) {
 #pragma unroll
     for (int l = 0; l < L; ++l) {
-      const int q = base + l * kLLFThreads + tid;
+      const int q = base + l * NT + tid;
       p[l] = q < q1 ? __ldg(t4 + q) : make_int4(-1, -1, -1, -1);
     }
   };
@@ -1772,7 +1781,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   //    block's x with BULK (x and the ids are inputs of the call, complete at
   //    launch; without BULK the row vectors are loaded after this pass).
   if (vec) load_ids(0, T * G4);
-  for (int i = tid; i < 3 * R; i += kLLFThreads) lower[i] = 0;  // lower, upper, rend
+  for (int i = tid; i < 3 * R; i += NT) lower[i] = 0;  // lower, upper, rend
   if (tid == 0) sh_bad = 0;
   __syncthreads();
   // (the stage's mbarrier is first waited on after the next block barrier)
@@ -1796,11 +1805,11 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
     };
     if (vec) {  // a token's K/4 vectors on neighbouring lanes, masks OR-ed by shuffles
       const int q1 = T * G4;
-      for (int base = 0; base < q1; base += L * kLLFThreads) {
+      for (int base = 0; base < q1; base += L * NT) {
         if (base != 0) load_ids(base, q1);
 #pragma unroll
         for (int l = 0; l < L; ++l) {
-          const int q = base + l * kLLFThreads + tid;
+          const int q = base + l * NT + tid;
           uint32_t m = 0u;
           add_mask(m, p[l].x);
           add_mask(m, p[l].y);
@@ -1811,7 +1820,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
         }
       }
     } else {  // one token per thread
-      for (int t = tid; t < T; t += kLLFThreads) {
+      for (int t = tid; t < T; t += NT) {
         uint32_t m = 0u;
         for (int k = 0; k < K; ++k) add_mask(m, __ldg(a.topk_idx + int64_t(t) * K + k));
         tally(t, m);
@@ -1842,7 +1851,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   if (!BULK) {
 #pragma unroll
     for (int j = 0; j < kLLFJ; ++j) {
-      const int q = vb0 + tid + j * kLLFThreads;
+      const int q = vb0 + tid + j * NT;
       if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
     }
   }
@@ -1900,7 +1909,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   __syncthreads();
   // 3. the tables of the ranks beginning here, the metadata of the owned
   //    tokens' rows, the register copy, the scales
-  for (int idx = tid; idx < nranks * R; idx += kLLFThreads) {
+  for (int idx = tid; idx < nranks * R; idx += NT) {
     const int i = idx / R, d = idx - i * R, s = s_lo + i;
     const int here = pref[i * R + d];
     const int next = i + 1 < nranks ? pref[(i + 1) * R + d] : rend[d];
@@ -1908,7 +1917,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
     a.num_tokens_per_rank[s * R + d] = next - here;
   }
   const int nown = tl - town;  // (<= 0: none)
-  for (int idx = tid; idx < nown * R * K; idx += kLLFThreads) {
+  for (int idx = tid; idx < nown * R * K; idx += NT) {
     const int j = idx / (R * K), rem = idx - j * R * K, d = rem / K, k = rem - d * K;
     const int t = town + j;
     const int r = rows[(t - tf) * R + d];
@@ -1925,17 +1934,17 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   }
   if (!BULK) {
     Words<NW>* rx = static_cast<Words<NW>*>(a.recv_x);
-    for (int q0 = vb0; q0 < vb1; q0 += kLLFJ * kLLFThreads) {
+    for (int q0 = vb0; q0 < vb1; q0 += kLLFJ * NT) {
       if (q0 != vb0) {
 #pragma unroll
         for (int j = 0; j < kLLFJ; ++j) {
-          const int q = q0 + tid + j * kLLFThreads;
+          const int q = q0 + tid + j * NT;
           if (q < vb1) v[j] = ld_stream_w<NW>(x + q);
         }
       }
 #pragma unroll
       for (int j = 0; j < kLLFJ; ++j) {
-        const int q = q0 + tid + j * kLLFThreads;
+        const int q = q0 + tid + j * NT;
         if (q < vb1) {
           const int t = q / a.vpr;
           const int off = q - t * a.vpr;
@@ -1949,7 +1958,7 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
     }
   }
   if (a.spr > 0) {
-    for (int idx = tid; idx < nown * R * a.spr; idx += kLLFThreads) {
+    for (int idx = tid; idx < nown * R * a.spr; idx += NT) {
       const int j = idx / (R * a.spr), rem = idx - j * R * a.spr, d = rem / a.spr,
                 c = rem - d * a.spr;
       const int t = town + j;
@@ -1960,14 +1969,14 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
   }
   // 4. job j < R: source rank j's expert counts; job R: every id's expert
   for (int job = blockIdx.x; job <= R; job += gridDim.x) {
-    for (int i = tid; i < E; i += kLLFThreads) hist[i] = 0;
+    for (int i = tid; i < E; i += NT) hist[i] = 0;
     __syncthreads();
     const int i0 = job < R ? job * N * K : 0;
     const int i1 = job < R ? i0 + N * K : T * K;
     int i4 = i0;  // 16-byte loads, L in flight per thread, where the range allows
     if ((reinterpret_cast<uintptr_t>(a.topk_idx) & 15u) == 0 && i0 % 4 == 0) {
       const int q1 = i1 / 4;
-      for (int q0 = i0 / 4; q0 < q1; q0 += L * kLLFThreads) {
+      for (int q0 = i0 / 4; q0 < q1; q0 += L * NT) {
         load_ids(q0, q1);
 #pragma unroll
         for (int l = 0; l < L; ++l) {
@@ -1979,32 +1988,32 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
       }
       i4 = 4 * q1;
     }
-    for (int i = i4 + tid; i < i1; i += kLLFThreads) {
+    for (int i = i4 + tid; i < i1; i += NT) {
       const int e = __ldg(a.topk_idx + i);
       if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
     int32_t* out = job < R ? a.num_tokens_per_expert + int64_t(job) * E : a.num_recv_tokens_per_expert;
-    for (int e = tid; e < E; e += kLLFThreads) out[e] = hist[e];
+    for (int e = tid; e < E; e += NT) out[e] = hist[e];
     __syncthreads();
   }
   if (BULK && warp == 0) drain_stage(bar, vb1 > vb0, lane);  // the load landed, pieces written
 }
 
-template <int NW, bool BULK>
+template <int NW, bool BULK, int NT>
 static cudaError_t layout_dispatch_fused_nw(HTFusedArgs a, cudaStream_t stream) {
   const int64_t V = int64_t(a.R) * a.N * a.vpr;
-  int64_t G = int64_t(sm_count()) * kLLFBlocksPerSM;
+  int64_t G = int64_t(sm_count());
   if (G > V) G = V;
   const int64_t vmax = (V + G - 1) / G;
   const int64_t tmax = (vmax + a.vpr - 1) / a.vpr + 1;
   const size_t table = sizeof(int32_t) * size_t(htf_table_words(a.R, a.E, int(tmax)));
   const size_t stage = BULK ? (size_t(vmax) * 4 * NW + 127) / 128 * 128 : 0;
-  if (table > kLLFMaxTable || stage > kLLFMaxStage) return cudaErrorNotSupported;
+  if (table > kLLFMaxTable || stage > kHTFMaxStage) return cudaErrorNotSupported;
   a.stage_bytes = uint32_t(stage);
   a.tmax = int(tmax);
   const size_t smem = stage + 16 + table;
-  auto kernel = mp_k_layout_dispatch_fused<NW, BULK>;
+  auto kernel = mp_k_layout_dispatch_fused<NW, BULK, NT>;
   static int configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -2014,7 +2023,7 @@ static cudaError_t layout_dispatch_fused_nw(HTFusedArgs a, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
+  return launch_kernel(kernel, dim3(unsigned(G)), dim3(NT), smem, stream, a);
 }
 
 cudaError_t launch_layout_dispatch_fused(
@@ -2043,12 +2052,17 @@ cudaError_t launch_layout_dispatch_fused(
   a.rank_prefix = rank_prefix, a.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
   a.send_row = send_row, a.x = x, a.recv_x = recv_x, a.x_scales = x_scales;
   a.recv_scales = recv_scales, a.dev_err = dev_err;
+  const bool small = ids <= kHTFSmallIds;
   if (bulk) {
-    const cudaError_t e = layout_dispatch_fused_nw<4, true>(a, stream);
+    const cudaError_t e = small ? layout_dispatch_fused_nw<4, true, 512>(a, stream)
+                                : layout_dispatch_fused_nw<4, true, 1024>(a, stream);
     if (e != cudaErrorNotSupported) return e;  // else the register copy (16-byte units)
   }
-  if (wide) return layout_dispatch_fused_nw<8, false>(a, stream);
-  return layout_dispatch_fused_nw<4, false>(a, stream);
+  if (wide)
+    return small ? layout_dispatch_fused_nw<8, false, 512>(a, stream)
+                 : layout_dispatch_fused_nw<8, false, 1024>(a, stream);
+  return small ? layout_dispatch_fused_nw<4, false, 512>(a, stream)
+               : layout_dispatch_fused_nw<4, false, 1024>(a, stream);
 }
 
 cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,

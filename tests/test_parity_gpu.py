@@ -582,10 +582,11 @@ def test_one_call_dispatch(shape):
     compare_ep(inp, plan, y_bits=wl.bf16_bits(y), what="one-call step combine(y)")
 
 
-@pytest.mark.parametrize("N", [128, 512, 1024])
+@pytest.mark.parametrize("N", [128, 256, 512, 1024])
 def test_one_call_dispatch_small_batches(N):
     """The DeepSeek-V3 shape at the small batches the benchmark also times (N tokens per
-    rank): one-call dispatch, then the combine of random rows."""
+    rank): one-call dispatch (one kernel of 512-thread blocks at N=128, of 1,024-thread
+    blocks at N=256, two launches above), then the combine of random rows."""
     inp = wl.make_ep("dsv3", seed=N, N=N)
     _, _, mask, _ = oracle.layout(inp.topk_idx, inp.E)
     rows = int(np.unpackbits(mask.view(np.uint8)).sum())
