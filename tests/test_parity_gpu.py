@@ -625,12 +625,18 @@ def test_one_call_dispatch_capacity_and_bad_ids():
                                  dict(R=4, N=150, E=32, K=4, H=4096, dtype="e4m3"),
                                  dict(R=8, N=60, E=64, K=8, H=1024, dtype="bf16", cap=900),
                                  dict(R=2, N=3, E=8, K=2, H=20480, dtype="bf16"),
-                                 dict(R=16, N=1, E=32, K=4, H=7168, dtype="bf16")],
+                                 dict(R=16, N=1, E=32, K=4, H=7168, dtype="bf16"),
+                                 dict(R=4, N=256, E=16, K=4, H=16384, dtype="bf16"),
+                                 dict(R=4, N=256, E=16, K=4, H=32768, dtype="e4m3"),
+                                 dict(R=4, N=256, E=16, K=4, H=16384, dtype="bf16", cap=2000)],
                          ids=["ragged", "e4m3_scales", "capacity", "blocks_inside_a_token",
-                              "one_token_per_rank"])
+                              "one_token_per_rank", "large_part", "large_part_e4m3_scales",
+                              "large_part_capacity"])
 def test_one_call_dispatch_bulk_copies(cfg):
     """mp_layout_dispatch at small batches with rows of 2 KB or more: one kernel whose
-    blocks count every token, bulk-load their part of x and bulk-store each row piece."""
+    blocks count every token, bulk-load their part of x and bulk-store each row piece.
+    "large_part": 32 KB rows, so a block's part of x (over 192 KB) does not fit shared
+    memory and the kernel copies through registers instead."""
     cfg = dict(cfg)
     cap = cfg.pop("cap", None)
     inp = wl.make_ep(dict(cfg, routing="uniform"), seed=cfg["N"] + cfg["H"])
