@@ -652,7 +652,14 @@ int mp_dispatch_ll_quant(int R, int N, int K, int E, int H, int qformat, int ran
                                        recv_scales);
   if (st != MP_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // the sort, then the quantising row copy as its programmatic dependent
+  // small batches counting themselves: one kernel
+  if (num_tokens_per_expert == nullptr) {
+    const cudaError_t f = launch_ll_dispatch_quant_fused(
+        R, N, K, E, rank_major, H, qformat, topk_idx, recv_capacity, bin_offsets,
+        bin_src_offsets, recv_src_token, slot_row, x, recv_x, recv_scales, dev_err, cs);
+    if (f != cudaErrorNotSupported) return cuda_status(f);
+  }
+  // else the sort, then the quantising row copy as its programmatic dependent
   const cudaError_t e = launch_ll_offsets(R, N, K, E, rank_major, topk_idx,
                                           num_tokens_per_expert, recv_capacity, bin_offsets,
                                           bin_src_offsets, recv_src_token, slot_row, dev_err, cs);

@@ -381,6 +381,8 @@ mp_k_dispatch_tma(int R, int64_t tokens, int64_t row_bytes, uint32_t piece_bytes
 // as 1 (FP8) or 1/2 (FP4) byte per channel per destination.
 // ---------------------------------------------------------------------------
 enum QuantFormat { kQE4M3 = 0, kQMXFP8 = 1, kQMXFP4 = 2 };
+static_assert(kQE4M3 == MP_Q_E4M3 && kQMXFP8 == MP_Q_MXFP8 && kQMXFP4 == MP_Q_MXFP4,
+              "the C ABI's format codes are the kernels' format numbers");
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;
@@ -449,6 +451,106 @@ __device__ __forceinline__ void st_codes(unsigned char* p, const uint32_t (&w)[N
   }
 }
 
+// One lane vector of CPL bf16 channels (its NW = CPL/2 words in v) to its
+// codes q[NB] and its scale (sbits: the fp32 scale's bits, or the UE8M0 code),
+// the scale block's kBlock / CPL lanes combining their amax by shuffles: every
+// lane of the warp calls it together (valid or not; whole scale blocks are
+// valid or not).
+template <int CPL, int FMT>
+__device__ __forceinline__ void quant_vector(bool valid, const Words<CPL / 2>& v,
+                                             uint32_t (&q)[FMT == kQMXFP4 ? CPL / 8 : CPL / 4],
+                                             uint32_t& sbits) {
+  constexpr bool MX = FMT != kQE4M3;
+  constexpr bool FP4 = FMT == kQMXFP4;
+  constexpr int kBlock = MX ? 32 : 128;      // channels per scale
+  constexpr int kLanes = kBlock / CPL;       // lanes per scale block
+  constexpr int kEmax = FP4 ? 2 : 8;         // exponent of the element format's largest normal
+  constexpr int NW = CPL / 2;                // 32-bit words of bf16 per lane
+  constexpr int NB = FP4 ? CPL / 8 : CPL / 4;  // 32-bit words of codes per lane
+  static_assert(kLanes >= 1 && kLanes <= 32, "scale block spans whole lanes");
+  float f[CPL];
+  float amax = 0.0f;
+  uint32_t sgn[FP4 ? NB : 1];  // FP4: the codes' sign bits, from the bf16 inputs
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+      f[2 * j] = __uint_as_float(v.w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
+    }
+    if constexpr (FP4) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        sgn[j] = e2m1_signs(v.w[4 * j], v.w[4 * j + 1], v.w[4 * j + 2], v.w[4 * j + 3]);
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  }
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+  if constexpr (MX) {
+    int c = 0;
+    if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - kEmax + 127));
+    sbits = uint32_t(c);
+    // 2^(127 - c): biased exponent 254 - c, or the subnormal 2^-127 at c = 254
+    const float inv = c < 254 ? __uint_as_float(uint32_t(254 - c) << 23)
+                              : __uint_as_float(0x00400000u);
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        if constexpr (FP4) {  // 8 channels -> 4 bytes
+          const float* c8 = f + 8 * j;
+          q[j] = sgn[j] |
+                 cvt_e2m1x8(__fmul_rn(c8[0], inv), __fmul_rn(c8[1], inv), __fmul_rn(c8[2], inv),
+                            __fmul_rn(c8[3], inv), __fmul_rn(c8[4], inv), __fmul_rn(c8[5], inv),
+                            __fmul_rn(c8[6], inv), __fmul_rn(c8[7], inv));
+        } else {  // 4 channels -> 4 bytes
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
+          const uint32_t hi =
+              cvt_e4m3x2(__fmul_rn(f[4 * j + 3], inv), __fmul_rn(f[4 * j + 2], inv));
+          q[j] = lo | (hi << 16);
+        }
+      }
+    }
+  } else {
+    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    sbits = __float_as_uint(sc);
+    if (valid) {
+      if (MP_QUANT_FAST_DIV && sc >= 0x1p-60f) {
+        // x / sc correctly rounded without a division per element (Markstein,
+        // "IA-64 and Elementary Functions", the division theorem: with y the
+        // correctly rounded 1/sc and q within one ulp of x / sc, the exact
+        // remainder r = x - sc*q (one FMA) gives RN(q + r*y) = RN(x / sc)).
+        // q0 = x*y is within 1.5 ulp; one correction brings it within one
+        // ulp, the second rounds it correctly.  sc >= 2^-60 keeps every
+        // remainder that matters for an e4m3 code exactly representable.
+        // The corrections turn -0 into +0 (0 - 0 = +0), so the sign of x,
+        // which x / sc always has, is put back.
+        const float y = __frcp_rn(sc);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const float a = f[j];
+          float qv = __fmul_rn(a, y);
+          qv = __fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv);
+          f[j] = copysignf(__fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv), a);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const uint32_t lo = cvt_e4m3x2(f[4 * j + 1], f[4 * j]);
+          const uint32_t hi = cvt_e4m3x2(f[4 * j + 3], f[4 * j + 2]);
+          q[j] = lo | (hi << 16);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const uint32_t lo = cvt_e4m3x2(__fdiv_rn(f[4 * j + 1], sc), __fdiv_rn(f[4 * j], sc));
+          const uint32_t hi = cvt_e4m3x2(__fdiv_rn(f[4 * j + 3], sc), __fdiv_rn(f[4 * j + 2], sc));
+          q[j] = lo | (hi << 16);
+        }
+      }
+    }
+  }
+}
+
 template <int CPL, int U, int FMT, bool GATHER>
 __global__ void __launch_bounds__(kCopyThreads)
 mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
@@ -458,7 +560,6 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
   constexpr bool FP4 = FMT == kQMXFP4;
   constexpr int kBlock = MX ? 32 : 128;      // channels per scale
   constexpr int kLanes = kBlock / CPL;       // lanes per scale block
-  constexpr int kEmax = FP4 ? 2 : 8;         // exponent of the element format's largest normal
   constexpr int NW = CPL / 2;                // 32-bit words of bf16 per lane
   constexpr int NB = FP4 ? CPL / 8 : CPL / 4;  // 32-bit words of codes per lane
   constexpr int kCodeBytes = NB * 4;
@@ -493,108 +594,27 @@ mp_k_quant_rows(int R, int64_t tokens, int H, const uint16_t* __restrict__ x,
     const int64_t i0 = slab * slab_vec + lane;
     uint32_t q[U][NB];
     uint32_t sbits[U];  // fp32 scale bits, or the UE8M0 code
-    uint32_t sgn[U][FP4 ? NB : 1];  // FP4: the codes' sign bits, from the bf16 inputs
+    Words<NW> v[U];     // every unit's loads first, then the arithmetic
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * kWarp;
-      const bool valid = i < vpr;  // whole scale blocks are valid or not (H % kBlock == 0)
-      float f[CPL];
-      float amax = 0.0f;
-      if (valid) {
-        Words<NW> v;
+      if (i < vpr) {
         if constexpr (NW == 16) {  // 32 channels: two 32-byte loads
           const Words<8>* p8 = reinterpret_cast<const Words<8>*>(x) + 2 * (tok * vpr + i);
           const Words<8> a = ld_stream_w<8>(p8), b = ld_stream_w<8>(p8 + 1);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            v.w[j] = a.w[j];
-            v.w[8 + j] = b.w[j];
+            v[u].w[j] = a.w[j];
+            v[u].w[8 + j] = b.w[j];
           }
         } else {
-          v = ld_stream_w<NW>(xv + tok * vpr + i);
-        }
-#pragma unroll
-        for (int j = 0; j < NW; ++j) {
-          f[2 * j] = __uint_as_float(v.w[j] << 16);
-          f[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
-        }
-        if constexpr (FP4) {
-#pragma unroll
-          for (int j = 0; j < NB; ++j)
-            sgn[u][j] = e2m1_signs(v.w[4 * j], v.w[4 * j + 1], v.w[4 * j + 2], v.w[4 * j + 3]);
-        }
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) amax = fmaxf(amax, fabsf(f[j]));
-      }
-#pragma unroll
-      for (int o = kLanes / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      if constexpr (MX) {
-        int c = 0;
-        if (amax > 0.0f) c = min(254, max(0, floor_log2_pos(amax) - kEmax + 127));
-        sbits[u] = uint32_t(c);
-        // 2^(127 - c): biased exponent 254 - c, or the subnormal 2^-127 at c = 254
-        const float inv = c < 254 ? __uint_as_float(uint32_t(254 - c) << 23)
-                                  : __uint_as_float(0x00400000u);
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < NB; ++j) {
-            if constexpr (FP4) {  // 8 channels -> 4 bytes
-              const float* c = f + 8 * j;
-              q[u][j] = sgn[u][j] |
-                        cvt_e2m1x8(__fmul_rn(c[0], inv), __fmul_rn(c[1], inv),
-                                   __fmul_rn(c[2], inv), __fmul_rn(c[3], inv),
-                                   __fmul_rn(c[4], inv), __fmul_rn(c[5], inv),
-                                   __fmul_rn(c[6], inv), __fmul_rn(c[7], inv));
-            } else {  // 4 channels -> 4 bytes
-              const uint32_t lo =
-                  cvt_e4m3x2(__fmul_rn(f[4 * j + 1], inv), __fmul_rn(f[4 * j], inv));
-              const uint32_t hi =
-                  cvt_e4m3x2(__fmul_rn(f[4 * j + 3], inv), __fmul_rn(f[4 * j + 2], inv));
-              q[u][j] = lo | (hi << 16);
-            }
-          }
-        }
-      } else {
-        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        sbits[u] = __float_as_uint(sc);
-        if (valid) {
-          if (MP_QUANT_FAST_DIV && sc >= 0x1p-60f) {
-            // x / sc correctly rounded without a division per element (Markstein,
-            // "IA-64 and Elementary Functions", the division theorem: with y the
-            // correctly rounded 1/sc and q within one ulp of x / sc, the exact
-            // remainder r = x - sc*q (one FMA) gives RN(q + r*y) = RN(x / sc)).
-            // q0 = x*y is within 1.5 ulp; one correction brings it within one
-            // ulp, the second rounds it correctly.  sc >= 2^-60 keeps every
-            // remainder that matters for an e4m3 code exactly representable.
-            // The corrections turn -0 into +0 (0 - 0 = +0), so the sign of x,
-            // which x / sc always has, is put back.
-            const float y = __frcp_rn(sc);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-              const float a = f[j];
-              float qv = __fmul_rn(a, y);
-              qv = __fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv);
-              f[j] = copysignf(__fmaf_rn(__fmaf_rn(-sc, qv, a), y, qv), a);
-            }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              const uint32_t lo = cvt_e4m3x2(f[4 * j + 1], f[4 * j]);
-              const uint32_t hi = cvt_e4m3x2(f[4 * j + 3], f[4 * j + 2]);
-              q[u][j] = lo | (hi << 16);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              const uint32_t lo =
-                  cvt_e4m3x2(__fdiv_rn(f[4 * j + 1], sc), __fdiv_rn(f[4 * j], sc));
-              const uint32_t hi =
-                  cvt_e4m3x2(__fdiv_rn(f[4 * j + 3], sc), __fdiv_rn(f[4 * j + 2], sc));
-              q[u][j] = lo | (hi << 16);
-            }
-          }
+          v[u] = ld_stream_w<NW>(xv + tok * vpr + i);
         }
       }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)  // (whole scale blocks are valid or not: H % kBlock == 0)
+      quant_vector<CPL, FMT>(i0 + u * kWarp < vpr, v[u], q[u], sbits[u]);
     while (vm) {
       const int d = __ffs(vm) - 1;
       vm &= vm - 1;
@@ -1407,6 +1427,7 @@ __device__ __forceinline__ void drain_stage(uint64_t* bar, bool staged_any, int 
 struct LLFusedArgs {
   int R, N, K, E, vpr, spr;
   uint32_t stage_bytes;  // BULK: bytes reserved for the block's part of x (multiple of 128)
+  void* q_scales;        // quantising mode: the rows' scales (fp32 or UE8M0 bytes)
   const int32_t* topk_idx;
   int64_t recv_capacity;
   int32_t* bin_offsets;
@@ -1420,13 +1441,14 @@ struct LLFusedArgs {
   int32_t* dev_err;
 };
 
-template <int NW, bool RANK_MAJOR, bool BULK>
+template <int NW, bool RANK_MAJOR, bool BULK, int QF>
 __global__ void __launch_bounds__(kLLFThreads, kLLFBlocksPerSM)
 mp_k_ll_dispatch_fused(LLFusedArgs a) {
   pdl_launch_dependents();  // the weighted combine after it may stage its blocks
   extern __shared__ __align__(128) unsigned char llf_smem[];
   __shared__ int32_t warp_tot[kLLFThreads / kWarp];
-  constexpr int UB = 4 * NW;                 // bytes per unit
+  // bytes per unit: 16/32-byte vectors, or in the quantising mode a scale block of bf16
+  constexpr int UB = QF >= 0 ? (QF == kQE4M3 ? 128 : 32) * 2 : 4 * NW;
   unsigned char* stage = llf_smem;           // BULK: the block's units of x
   uint64_t* bar = reinterpret_cast<uint64_t*>(llf_smem + a.stage_bytes);
   int32_t* lower = reinterpret_cast<int32_t*>(llf_smem + a.stage_bytes + 16);
@@ -1445,7 +1467,10 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
   const int town = (vb0 + a.vpr - 1) / a.vpr;             // first token whose first unit is here
   const int e0 = tf * K, e1 = tl * K;                     // the block's entries
   const unsigned char* xb = static_cast<const unsigned char*>(a.x);
-  if (BULK && tid == 0) stage_units<UB>(stage, bar, xb, vb0, vb1);
+  // the block's part of x into shared memory (BULK; and in the quantising mode
+  // when it fits, stage_bytes > 0)
+  const bool stage_x = BULK || (QF >= 0 && a.stage_bytes > 0);
+  if (stage_x && tid == 0) stage_units<UB>(stage, bar, xb, vb0, vb1);
   // 1. per-bin counts below and from the block's first entry; the block's own
   //    ids kept in `rows` for the walk
   const int nall = T * K;
@@ -1485,7 +1510,7 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
   load_ids(tid);
   const Words<NW>* x = reinterpret_cast<const Words<NW>*>(xb);
   Words<NW> v[BULK ? 1 : kLLFJ];
-  if (!BULK) {
+  if (!BULK && QF < 0) {
 #pragma unroll
     for (int j = 0; j < kLLFJ; ++j) {
       const int q = vb0 + tid + j * kLLFThreads;
@@ -1591,8 +1616,64 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
     }
   }
   __syncthreads();
-  // 4. the register copy (BULK: stored in step 3)
-  if (!BULK) {
+  // 4. the register copy (BULK: stored in step 3), or the quantising one
+  if constexpr (QF >= 0) {
+    // units are scale blocks; each lane quantises CPL channels once (the scale
+    // block's lanes combining their amax) and stores the codes to its token's
+    // rows, the block's first lane its scale
+    constexpr int CPL = 16;
+    constexpr bool FP4 = QF == kQMXFP4;
+    constexpr int kLanes = (QF == kQE4M3 ? 128 : 32) / CPL;  // lanes per scale block
+    constexpr int NB = FP4 ? CPL / 8 : CPL / 4;             // 32-bit words of codes per lane
+    const int lvpr = a.vpr * kLanes;                        // lane vectors per row
+    const int lv0 = vb0 * kLanes, lv1 = vb1 * kLanes;
+    const int64_t code_row = int64_t(lvpr) * NB * 4;        // code bytes per row
+    const Words<8>* xw = reinterpret_cast<const Words<8>*>(xb);
+    const Words<8>* sw = reinterpret_cast<const Words<8>*>(stage);  // lane vector lv0 first
+    unsigned char* out = static_cast<unsigned char*>(a.recv_x);
+    // the staged units (a bounded wait; on a timeout report it, wait once more so
+    // the load is not left writing shared memory, and read x from memory instead)
+    bool from_smem = stage_x && lv0 + warp * kWarp < lv1;
+    if (from_smem && !wait_staged(bar, a.dev_err)) {
+      uint32_t n = 0;
+      while (!mbar_try_wait(bar, 0) && ++n < kSpinLimit) {
+      }
+      from_smem = false;
+    }
+    for (int base = lv0 + warp * kWarp; base < lv1; base += kLLFThreads) {
+      const int qv = base + lane;
+      const bool valid = qv < lv1;  // (whole scale blocks: lv1 is a multiple of kLanes)
+      Words<8> w;
+      if (valid) {
+        if (from_smem) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(sw + (qv - lv0));
+          const uint4 lo = s4[0], hi = s4[1];
+          w.w[0] = lo.x, w.w[1] = lo.y, w.w[2] = lo.z, w.w[3] = lo.w;
+          w.w[4] = hi.x, w.w[5] = hi.y, w.w[6] = hi.z, w.w[7] = hi.w;
+        } else {
+          w = ld_stream_w<8>(xw + qv);
+        }
+      }
+      uint32_t q[NB], sbits;
+      quant_vector<CPL, QF>(valid, w, q, sbits);
+      if (valid) {
+        const int t = qv / lvpr, off = qv - t * lvpr;
+        const int32_t* tr = rows + (t - tf) * K;
+        for (int k = 0; k < K; ++k) {
+          const int r = tr[k];
+          if (r < 0) continue;
+          st_codes<NB>(out + int64_t(r) * code_row + off * (NB * 4), q);
+          if ((lane & (kLanes - 1)) == 0) {
+            if constexpr (QF == kQE4M3)
+              static_cast<uint32_t*>(a.q_scales)[int64_t(r) * a.vpr + off / kLanes] = sbits;
+            else
+              static_cast<unsigned char*>(a.q_scales)[int64_t(r) * a.vpr + off / kLanes] =
+                  uint8_t(sbits);
+          }
+        }
+      }
+    }
+  } else if (!BULK) {
     Words<NW>* rx = static_cast<Words<NW>*>(a.recv_x);
     for (int q0 = vb0; q0 < vb1; q0 += kLLFJ * kLLFThreads) {
       if (q0 != vb0) {
@@ -1629,7 +1710,7 @@ mp_k_ll_dispatch_fused(LLFusedArgs a) {
   }
 }
 
-template <int NW, bool RANK_MAJOR, bool BULK>
+template <int NW, bool RANK_MAJOR, bool BULK, int QF = -1>
 static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
   const int nbins = RANK_MAJOR ? a.R : a.E;
   const int64_t V = int64_t(a.R) * a.N * a.vpr;
@@ -1638,11 +1719,18 @@ static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
   const int64_t vmax = (V + G - 1) / G;                 // units of one block at most
   const int64_t tmax = (vmax + a.vpr - 1) / a.vpr + 1;  // tokens one block's units touch
   const size_t table = sizeof(int32_t) * size_t(2 * nbins + tmax * a.K);
-  const size_t stage = BULK ? (size_t(vmax) * 4 * NW + 127) / 128 * 128 : 0;
-  if (table > kLLFMaxTable || stage > kLLFMaxStage) return cudaErrorNotSupported;
+  if (table > kLLFMaxTable) return cudaErrorNotSupported;
+  size_t stage = 0;
+  if (BULK) {
+    stage = (size_t(vmax) * 4 * NW + 127) / 128 * 128;
+    if (stage > kLLFMaxStage) return cudaErrorNotSupported;
+  } else if (QF >= 0) {  // staged when it fits, else read from memory
+    stage = (size_t(vmax) * (QF == kQE4M3 ? 128 : 32) * 2 + 127) / 128 * 128;
+    if (stage > kLLFMaxStage) stage = 0;
+  }
   a.stage_bytes = uint32_t(stage);
   const size_t smem = stage + 16 + table;
-  auto kernel = mp_k_ll_dispatch_fused<NW, RANK_MAJOR, BULK>;
+  auto kernel = mp_k_ll_dispatch_fused<NW, RANK_MAJOR, BULK, QF>;
   static int configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1653,6 +1741,38 @@ static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
     configured[dev] = int(smem);
   }
   return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
+}
+
+template <int QF>
+static cudaError_t ll_quant_fused_q(int rank_major, const LLFusedArgs& a, cudaStream_t stream) {
+  return rank_major ? ll_dispatch_fused_nw<8, true, false, QF>(a, stream)
+                    : ll_dispatch_fused_nw<8, false, false, QF>(a, stream);
+}
+
+cudaError_t launch_ll_dispatch_quant_fused(int R, int N, int K, int E, int rank_major, int H,
+                                           int fmt, const int32_t* topk_idx,
+                                           int64_t recv_capacity, int32_t* bin_offsets,
+                                           int32_t* bin_src_offsets, int32_t* recv_src_token,
+                                           int32_t* slot_row, const void* x, void* recv_x,
+                                           void* recv_scales, int32_t* dev_err,
+                                           cudaStream_t stream) {
+  const int nbins = rank_major ? R : E;
+  const int64_t ids = int64_t(R) * N * K;
+  const int block = fmt == kQE4M3 ? 128 : 32;  // channels per scale (H is a multiple)
+  if (N <= 0 || ids > kLLFMaxIds || nbins > kLLFMaxBins || H % block != 0 || !aligned(x, 32) ||
+      !aligned(recv_x, 16) || int64_t(R) * N * (H / 16) >= (int64_t(1) << 30))
+    return cudaErrorNotSupported;
+  LLFusedArgs a{};
+  a.R = R, a.N = N, a.K = K, a.E = E, a.vpr = H / block, a.spr = 0;
+  a.topk_idx = topk_idx, a.recv_capacity = recv_capacity, a.bin_offsets = bin_offsets;
+  a.bin_src_offsets = bin_src_offsets, a.recv_src_token = recv_src_token, a.slot_row = slot_row;
+  a.x = x, a.recv_x = recv_x, a.q_scales = recv_scales, a.dev_err = dev_err;
+  switch (fmt) {
+    case kQE4M3: return ll_quant_fused_q<kQE4M3>(rank_major, a, stream);
+    case kQMXFP8: return ll_quant_fused_q<kQMXFP8>(rank_major, a, stream);
+    case kQMXFP4: return ll_quant_fused_q<kQMXFP4>(rank_major, a, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------------------

@@ -114,6 +114,17 @@ cudaError_t launch_ll_dispatch_fused(int R, int N, int K, int E, int rank_major,
                                      const float* x_scales, void* recv_x, float* recv_scales,
                                      int32_t* dev_err, cudaStream_t stream);
 
+// mp_dispatch_ll_quant as one kernel (blocks each count every id, then
+// quantise their tokens' rows); fmt is MP_Q_E4M3 / MP_Q_MXFP8 / MP_Q_MXFP4.
+// cudaErrorNotSupported, with nothing launched, outside its limits.
+cudaError_t launch_ll_dispatch_quant_fused(int R, int N, int K, int E, int rank_major, int H,
+                                           int fmt, const int32_t* topk_idx,
+                                           int64_t recv_capacity, int32_t* bin_offsets,
+                                           int32_t* bin_src_offsets, int32_t* recv_src_token,
+                                           int32_t* slot_row, const void* x, void* recv_x,
+                                           void* recv_scales, int32_t* dev_err,
+                                           cudaStream_t stream);
+
 // The whole high-throughput dispatch (mp_layout_dispatch's outputs) as one
 // kernel whose blocks each count every token, for small batches.
 // cudaErrorNotSupported, with nothing launched, outside its limits.

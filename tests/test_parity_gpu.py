@@ -1078,8 +1078,9 @@ LL_QUANT = [dict(R=8, N=128, E=256, K=8, H=7168), dict(R=5, N=77, E=20, K=6, H=3
 @pytest.mark.parametrize("call", ["one_call", "rows"])
 def test_low_latency_quantised_dispatch_matches_oracle(cfg, rank_major, fmt, call):
     """The low-latency dispatch with the quantisation in the row copy -- mp_dispatch_ll_quant
-    (the sort, then the quantising copy as its programmatic dependent) or the LL offsets
-    followed by mp_dispatch_ll_rows_quant -- against the oracle's composition: every token
+    (one kernel that counts, places and quantises up to 16,384 ids, else the sort and then
+    the quantising copy as its programmatic dependent) or the LL offsets followed by
+    mp_dispatch_ll_rows_quant -- against the oracle's composition: every token
     row quantised by the oracle (codes and scales), then the oracle's LL layout of those
     bytes; bit for bit, two calls in a row, with all-zero, tiny and wide-range blocks."""
     cfg = dict(cfg)
