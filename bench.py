@@ -578,10 +578,11 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
                  "owning the expert)")
     # the low-latency dispatch with the quantisation in the row copy (e4m3 with an fp32
     # scale per 128 channels, and MXFP8), then the weighted combine of bf16 expert outputs
-    for fmt, qcode, sbytes in (("e4m3", B.MP_Q_E4M3, H // 128 * 4), ("mxfp8", B.MP_Q_MXFP8,
-                                                                      H // 32)):
+    for fmt, qcode, sbytes, cbytes in (("e4m3", B.MP_Q_E4M3, H // 128 * 4, H),
+                                       ("mxfp8", B.MP_Q_MXFP8, H // 32, H),
+                                       ("mxfp4", B.MP_Q_MXFP4, H // 32, H // 2)):
         for st in ll_sets:
-            st["rq"] = torch.empty((cap, H), dtype=torch.uint8, device="cuda")
+            st["rq"] = torch.empty((cap, cbytes), dtype=torch.uint8, device="cuda")
             st["rs"] = torch.empty((cap, sbytes), dtype=torch.uint8, device="cuda")
 
         def ll_quant(st, qcode=qcode):
@@ -594,7 +595,7 @@ def measure_other_rows(steps: int, peak: float, scale: int = 1):
         q_phase_us = phases(ll_sets, [ll_quant, ll_combine], ("dispatch_ll_quant", "combine_ll"),
                             steps)
         assert ll_errors() == 0
-        q_bytes = ll_bytes - cap * H * 2 + cap * (H + sbytes)
+        q_bytes = ll_bytes - cap * H * 2 + cap * (cbytes + sbytes)
         out["low_latency_quantised_%s_step_n128" % fmt] = dict(
             row(ms_q, q_bytes), us_per_step=ms_q * 1e3, phases_us=q_phase_us,
             workload="as low_latency_step_n128 with mp_dispatch_ll_quant: bf16 rows quantised "
