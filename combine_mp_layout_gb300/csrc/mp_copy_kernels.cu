@@ -1901,10 +1901,22 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
       p[l] = q < q1 ? __ldg(t4 + q) : make_int4(-1, -1, -1, -1);
     }
   };
+  // K = 4 or 8: each thread loads whole tokens (L / G4 of them, tokens
+  // base_t + j*NT + tid), so that every lane tallies and no shuffle is needed
+  const bool whole = vec && G4 <= 2;
+  const int gs = G4 - 1;  // (whole) log2 of the vectors per token
+  auto load_tokens = [&](int base_t) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const int t = base_t + (l >> gs) * NT + tid;
+      p[l] = t < T ? __ldg(t4 + int64_t(t) * G4 + (l & gs)) : make_int4(-1, -1, -1, -1);
+    }
+  };
   // 1. every token's destinations.  The first id loads go out first, then the
   //    block's x with BULK (x and the ids are inputs of the call, complete at
   //    launch; without BULK the row vectors are loaded after this pass).
-  if (vec) load_ids(0, T * G4);
+  if (whole) load_tokens(0);
+  else if (vec) load_ids(0, T * G4);
   for (int i = tid; i < 3 * R; i += NT) lower[i] = 0;  // lower, upper, rend
   if (tid == 0) sh_bad = 0;
   __syncthreads();
@@ -1927,7 +1939,29 @@ mp_k_layout_dispatch_fused(HTFusedArgs a) {
           if (t < split2) cc[w] += sp;
         }
     };
-    if (vec) {  // a token's K/4 vectors on neighbouring lanes, masks OR-ed by shuffles
+    if (whole) {
+      for (int base_t = 0; base_t < T; base_t += (L >> gs) * NT) {
+        if (base_t != 0) load_tokens(base_t);
+        uint32_t mprev = 0u;
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          uint32_t m = 0u;
+          add_mask(m, p[l].x);
+          add_mask(m, p[l].y);
+          add_mask(m, p[l].z);
+          add_mask(m, p[l].w);
+          if (gs == 1) {  // a token's two vectors: l even, then l odd
+            if ((l & 1) == 0) {
+              mprev = m;
+              continue;
+            }
+            m |= mprev;
+          }
+          const int t = base_t + (l >> gs) * NT + tid;
+          if (t < T) tally(t, m);
+        }
+      }
+    } else if (vec) {  // a token's K/4 vectors on neighbouring lanes, masks OR-ed by shuffles
       const int q1 = T * G4;
       for (int base = 0; base < q1; base += L * NT) {
         if (base != 0) load_ids(base, q1);
