@@ -215,19 +215,25 @@ int mp_layout_and_offsets(int R, int N, int K, int E, const int32_t *topk_idx,
  * mp_layout_dispatch -- the whole dispatch in one call: mp_layout, then
  * mp_dispatch (receive offsets and row copy), from the routing and the token
  * rows ([EP] get_dispatch_layout followed by intranode_dispatch; fusing them
- * has no counterpart in the pages).  Where the problem fits one resident grid
- * (as for mp_layout_and_offsets), layout and offsets run as one cooperative
- * launch that writes send_row and the tables, and the row copy -- which also
- * writes the receive metadata -- is launched as its programmatic dependent:
- * its blocks start while the offsets are computed, load their first token
- * rows, and wait for the offsets before they store.  Otherwise the launches of
- * mp_layout and mp_dispatch run.
+ * has no counterpart in the pages).  Up to 16,384 top-k ids (R*N*K) it is one
+ * kernel whose blocks each read every id, place their own share of the tokens
+ * (a token's row on destination d is dest_offsets[d] plus the number of
+ * earlier tokens in source-rank, token order that go to d) and copy their
+ * share of the rows, through shared memory by the bulk-copy engine when it
+ * fits; the workspace is not used then.  Above that, where the problem fits
+ * one resident grid (as for mp_layout_and_offsets), layout and offsets run as
+ * one launch that writes send_row and the tables, and the row copy -- which
+ * also writes the receive metadata -- is launched as its programmatic
+ * dependent: its blocks start while the offsets are computed, load their first
+ * token rows, and wait for the offsets before they store.  Otherwise the
+ * launches of mp_layout and mp_dispatch run.
  *   Arguments: the layout outputs of mp_layout and every argument of
  *   mp_dispatch (same meaning, layout and ownership); the results are
  *   identical to those two calls.
  *   Checks and device errors: those of mp_layout and mp_dispatch, plus
- *   MP_ERR_TIMEOUT when the grid barrier's bounded (~1 s) wait gives up (the
- *   workspace must then be zero-filled again).
+ *   MP_ERR_TIMEOUT when a bounded (~1 s) device wait gives up: the grid
+ *   barrier (the workspace must then be zero-filled again) or, in the
+ *   one-kernel form, a block's wait for its bulk load of x.
  */
 int mp_layout_dispatch(int R, int N, int K, int E, int H, int dtype, const void *x,
                        const float *x_scales, const int32_t *topk_idx,
@@ -546,13 +552,19 @@ int mp_dispatch_ll_offsets_rank_major(int R, int N, int K, int E, const int32_t 
  * mp_dispatch_ll_offsets (rank_major = 0) or mp_dispatch_ll_offsets_rank_major
  * (rank_major = 1) followed by mp_dispatch_ll_rows, bit for bit ("MSCCLPP EP
  * implementation", the low-latency dispatch, one call that both places and
- * sends the tokens).  The row copy is launched as a programmatic dependent of
- * the sort, so its row loads overlap the sort; x must therefore be complete
+ * sends the tokens).  With num_tokens_per_expert NULL and up to 16,384 ids it
+ * is one kernel whose blocks each read every id, place their share of the
+ * entries (an entry's row is its bin's first row plus the number of earlier
+ * entries of that bin in source-rank, token, slot order) and copy their share
+ * of the rows (through shared memory by the bulk-copy engine for rows of 2 KB
+ * or more).  Otherwise the row copy is launched as a programmatic dependent of
+ * the sort, so its row loads overlap the sort.  Either way x must be complete
  * when the call is enqueued (as for every call, by stream order).
  *   bin_offsets / bin_src_offsets: expert_offsets / expert_src_offsets, or
  *   dest_offsets / dest_src_offsets for rank_major = 1; every other argument
  *   as in those calls (dtype MP_BF16 or MP_E4M3 with its scales).
- *   Device errors: as mp_dispatch_ll_offsets.
+ *   Device errors: as mp_dispatch_ll_offsets, plus MP_ERR_TIMEOUT if a
+ *   block's bounded (~1 s) wait for its bulk load of x gives up.
  */
 int mp_dispatch_ll(int R, int N, int K, int E, int H, int dtype, int rank_major, const void *x,
                    const float *x_scales, const int32_t *topk_idx,
@@ -604,13 +616,16 @@ int mp_dispatch_ll_rows_quant(int R, int N, int K, int H, int qformat, const voi
 
 /*
  * mp_dispatch_ll_quant -- mp_dispatch_ll with the quantisation done in the row
- * copy: the LL offsets (expert-major, or rank-major with rank_major = 1), then
- * the quantising row copy of mp_dispatch_ll_rows_quant launched as the sort's
+ * copy: the LL offsets (expert-major, or rank-major with rank_major = 1) and
+ * the quantising row copy of mp_dispatch_ll_rows_quant, bit for bit.  With
+ * num_tokens_per_expert NULL and up to 16,384 ids (and x 32-byte aligned) one
+ * kernel counts, places and quantises (as mp_dispatch_ll); otherwise the
+ * quantising copy is launched as the sort's
  * programmatic dependent (its blocks start while the sort runs and wait for
  * its slot rows).  Arguments: those of mp_dispatch_ll, with qformat and
  * void *recv_scales in place of dtype, x_scales and the float scales (x is
  * bf16); checks and device errors as mp_dispatch_ll_offsets and
- * mp_dispatch_ll_rows_quant.
+ * mp_dispatch_ll_rows_quant, plus MP_ERR_TIMEOUT as mp_dispatch_ll.
  */
 int mp_dispatch_ll_quant(int R, int N, int K, int E, int H, int qformat, int rank_major,
                          const void *x, const int32_t *topk_idx,
