@@ -1841,7 +1841,10 @@ __host__ __device__ inline int htf_table_words(int R, int E, int tmax) {
 // larger blocks count less in all (dsv3 N=256 step 70.2 -> 66.8 us against two
 // blocks of 512 threads per SM); 512 threads up to kHTFSmallIds ids (N=128 step
 // 37.9 us, against 39.3 with 1,024), 1,024 above.
-constexpr int64_t kHTFSmallIds = 8192;
+#ifndef MP_HTF_SMALL_IDS
+#define MP_HTF_SMALL_IDS 8192
+#endif
+constexpr int64_t kHTFSmallIds = MP_HTF_SMALL_IDS;
 // a block's stage of x: what the SM's shared memory leaves beside the tables
 constexpr size_t kHTFMaxStage = 192 * 1024;
 
