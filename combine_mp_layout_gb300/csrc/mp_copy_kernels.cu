@@ -836,6 +836,25 @@ static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, cudaStr
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Any kernel launched with programmatic stream serialization (block size and
+// shared memory given): it may start before the kernel ahead of it ends, so it
+// must call pdl_wait_prior_grid() before touching memory that kernel writes.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename Kernel>
 static int resident_blocks(Kernel k) {
   int n = 0;
@@ -1445,6 +1464,10 @@ template <int NW, bool RANK_MAJOR, bool BULK, int QF>
 __global__ void __launch_bounds__(kLLFThreads, kLLFBlocksPerSM)
 mp_k_ll_dispatch_fused(LLFusedArgs a) {
   pdl_launch_dependents();  // the weighted combine after it may stage its blocks
+  // launched as a programmatic dependent of the kernel before it on the stream:
+  // the blocks are placed while that kernel ends, and wait for it here, before
+  // any global memory access (every input is then complete and visible)
+  pdl_wait_prior_grid();
   extern __shared__ __align__(128) unsigned char llf_smem[];
   __shared__ int32_t warp_tot[kLLFThreads / kWarp];
   // bytes per unit: 16/32-byte vectors, or in the quantising mode a scale block of bf16
@@ -1740,7 +1763,7 @@ static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  return launch_kernel(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
+  return launch_pdl(kernel, dim3(unsigned(G)), dim3(kLLFThreads), smem, stream, a);
 }
 
 template <int QF>
@@ -1852,6 +1875,10 @@ template <int NW, bool BULK, int NT>
 __global__ void __launch_bounds__(NT, 1)
 mp_k_layout_dispatch_fused(HTFusedArgs a) {
   pdl_launch_dependents();  // the combine after it may stage its blocks
+  // launched as a programmatic dependent of the kernel before it on the stream:
+  // the blocks are placed while that kernel ends, and wait for it here, before
+  // any global memory access (every input is then complete and visible)
+  pdl_wait_prior_grid();
   extern __shared__ __align__(128) unsigned char htf_smem[];
   constexpr int UB = 4 * NW;  // bytes per unit
   constexpr int L = 4;        // 16-byte id loads in flight per thread
@@ -2184,7 +2211,7 @@ static cudaError_t layout_dispatch_fused_nw(HTFusedArgs a, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  return launch_kernel(kernel, dim3(unsigned(G)), dim3(NT), smem, stream, a);
+  return launch_pdl(kernel, dim3(unsigned(G)), dim3(NT), smem, stream, a);
 }
 
 cudaError_t launch_layout_dispatch_fused(
