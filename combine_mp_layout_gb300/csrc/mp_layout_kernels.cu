@@ -1116,6 +1116,9 @@ mp_k_ll_offsets(int R, int N, int K, int E, const int32_t* __restrict__ topk_idx
   // a row copy launched as this grid's programmatic dependent may start now:
   // it reads slot_row only after this grid has finished
   pdl_launch_dependents();
+  // launched as a programmatic dependent of the kernel before it on the stream:
+  // wait for it before any global memory access
+  pdl_wait_prior_grid();
   extern __shared__ int32_t ll_smem[];
   __shared__ int64_t warp_sums[kLLThreads / kWarp];
   ll_offsets_block<RANK_MAJOR, kLLThreads, kLLHistInts>(
@@ -1199,6 +1202,9 @@ __global__ void __launch_bounds__(kClThreads, 1) mp_k_layout_cluster(ClusterArgs
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = int(cluster_ctarank());
   pdl_launch_dependents();
+  // launched as a programmatic dependent of the kernel before it on the stream:
+  // wait for it before any global memory access
+  pdl_wait_prior_grid();
   const int rounds = (N + kClThreads - 1) / kClThreads;
 
   // 1. the ids of every round first (8 per token and round in flight), then
@@ -1504,6 +1510,12 @@ cudaError_t launch_layout_cluster(int R, int N, int K, int E, const int32_t* top
                    num_tokens_per_rank, num_tokens_per_expert, recv_src_rank, recv_src_idx,
                    recv_topk_idx, recv_topk_weights, dest_offsets, rank_prefix,
                    num_recv_tokens_per_expert, send_row, dev_err};
+  // launched as a programmatic dependent of the kernel before it (it waits first)
+  cudaLaunchAttribute attr2[2] = {attr[0], {}};
+  attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr2[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr2;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
@@ -1590,9 +1602,20 @@ static cudaError_t ll_offsets(int R, int N, int K, int E, const int32_t* topk_id
     if (e != cudaSuccess) return e;
     configured[dev] = int(smem);
   }
-  return launch_kernel(mp_k_ll_offsets<RANK_MAJOR>, dim3(unsigned(R)), dim3(kLLThreads), smem,
-                       stream, R, N, K, E, topk_idx, num_tokens_per_expert, recv_capacity,
-                       bin_offsets, bin_src_offsets, recv_src_token, slot_row, dev_err);
+  // launched as a programmatic dependent of the kernel before it (it waits first)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(R));
+  cfg.blockDim = dim3(kLLThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mp_k_ll_offsets<RANK_MAJOR>, R, N, K, E, topk_idx,
+                            num_tokens_per_expert, recv_capacity, bin_offsets, bin_src_offsets,
+                            recv_src_token, slot_row, dev_err);
 }
 
 // The low-latency dispatch: the sort, then the row copy launched as its
