@@ -1348,8 +1348,9 @@ cudaError_t launch_ll_rows_after_sort(int K, int64_t tokens, int64_t row_bytes, 
 // slot, which is the entries' flat index i = (s*N + n)*K + k, so entry i goes
 // to the bin's first row plus the number of entries j < i in the same bin.
 // Block b copies the units [V*b/G, V*(b+1)/G) of the token-major row space
-// (V = R*N*vpr units of 16 or 32 bytes); for the tokens those units belong to
-// it finds the rows itself:
+// (V = R*N*vpr units of 16 or 32 bytes; in the quantising mode, QF >= 0, whole
+// scale blocks, so that no block shares a scale block with another); for the
+// tokens those units belong to it finds the rows itself:
 //  1. one pass over all R*N*K ids (they are few: the path is for small
 //     batches): per bin, the entries before the block's first entry (lower)
 //     and the others (upper), counted in shared memory, and the block's own
@@ -1361,11 +1362,17 @@ cudaError_t launch_ll_rows_after_sort(int K, int64_t tokens, int64_t row_bytes, 
 //     tokens whose first unit is the block's it writes slot_row and
 //     recv_src_token, and, at the first entry of a rank s, the counts so far
 //     as bin_src_offsets[., s];
-//  4. the copy, then the owned tokens' scales.
+//  4. the copy (quantising mode: each lane quantises 16 channels once, with
+//     the same device function as the quantising copies, and stores the codes
+//     to its token's rows, the scale block's first lane its scale), then the
+//     owned tokens' scales.
+// The kernel is launched as a programmatic dependent of the kernel before it
+// on the stream and waits for that kernel before any memory access.
 // The block's part of x is fetched while it counts.  With BULK (rows of at
 // least kLLFBulkMinRow bytes) one thread loads it into shared memory with a
 // bulk copy at the start, and in step 3 each lane of the walking warp stores
-// its entry's piece of the token row with a shared -> global bulk copy.  Else each
+// its entry's piece of the token row with a shared -> global bulk copy (the
+// quantising mode stages x the same way when it fits).  Else each
 // thread loads its kLLFJ vectors into registers before the counting and
 // stores them to the rows of their token (the register loads in flight slow
 // the shared-memory adds of step 1, which the bulk load does not: measured
@@ -1823,11 +1830,14 @@ cudaError_t launch_ll_dispatch_quant_fused(int R, int N, int K, int E, int rank_
 //     rank j's ids per expert (num_tokens_per_expert[j]), job R every id
 //     (num_recv_tokens_per_expert).
 // The pass of step 1 keeps its counts in registers (four 8-bit fields per
-// word; a lane leads at most 8 tokens within the id limit) and reduces them
-// over the warp once at the end, and issues its first id loads before the
-// block's x: a warp reduction per destination and group of tokens, or the ids
-// queued behind x, cost several microseconds at R=8, N=128 (every block reads
-// every id).
+// word; within the id limit a thread tallies at most 32 tokens) and reduces
+// them over the warp once at the end; for K = 4 or 8 each thread loads whole
+// tokens, else a token's 16-byte id vectors sit on neighbouring lanes; its
+// first id loads go out before the block's x.  A warp reduction per
+// destination and group of tokens, or the ids queued behind x, cost several
+// microseconds at R=8, N=128 (every block reads every id).
+// The kernel is launched as a programmatic dependent of the kernel before it
+// on the stream and waits for that kernel before any memory access.
 // ---------------------------------------------------------------------------
 struct HTFusedArgs {
   int R, N, K, E, vpr, spr;
