@@ -628,10 +628,11 @@ def test_one_call_dispatch_capacity_and_bad_ids():
                                  dict(R=16, N=1, E=32, K=4, H=7168, dtype="bf16"),
                                  dict(R=4, N=256, E=16, K=4, H=16384, dtype="bf16"),
                                  dict(R=4, N=256, E=16, K=4, H=32768, dtype="e4m3"),
-                                 dict(R=4, N=256, E=16, K=4, H=16384, dtype="bf16", cap=2000)],
+                                 dict(R=4, N=256, E=16, K=4, H=16384, dtype="bf16", cap=2000),
+                                 dict(R=32, N=16, E=64, K=8, H=2048, dtype="bf16")],
                          ids=["ragged", "e4m3_scales", "capacity", "blocks_inside_a_token",
                               "one_token_per_rank", "large_part", "large_part_e4m3_scales",
-                              "large_part_capacity"])
+                              "large_part_capacity", "32_ranks"])
 def test_one_call_dispatch_bulk_copies(cfg):
     """mp_layout_dispatch at small batches with rows of 2 KB or more: one kernel whose
     blocks count every token, bulk-load their part of x and bulk-store each row piece.
@@ -939,7 +940,8 @@ LL_ONE_CALL = [dict(R=2, N=64, E=8, K=2, H=128), dict(R=8, N=128, E=256, K=8, H=
                  dict(R=8, N=64, E=8192, K=8, H=64), dict(R=4, N=3000, E=64, K=6, H=64),
                  dict(R=4, N=500, E=16, K=4, H=64, cap_frac=0.5), dict(R=1, N=40, E=3, K=3, H=64),
                  dict(R=4, N=0, E=16, K=4, H=64), dict(R=2, N=50, E=64, K=32, H=64),
-                 dict(R=16, N=1, E=32, K=4, H=64), dict(R=2, N=3, E=8, K=2, H=20480)]
+                 dict(R=16, N=1, E=32, K=4, H=64), dict(R=2, N=3, E=8, K=2, H=20480),
+                 dict(R=4, N=100, E=2048, K=8, H=1024)]  # the one kernel's largest bin count
 
 
 @pytest.mark.parametrize("cfg", LL_ONE_CALL, ids=lambda c: "R%(R)d_N%(N)d_E%(E)d_K%(K)d_H%(H)d" % c
