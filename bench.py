@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark of the MoE layout -> dispatch -> combine hot path on one GB300.
 
-One step = mp_layout_dispatch (layout + receive offsets in one cooperative
-launch, then the row copy launched as its programmatic dependent) + mp_combine
-(launched as the copy's programmatic dependent) on the DeepSeek-V3-shaped workload
+One step = mp_layout_dispatch (at this size layout + receive offsets in one
+cooperative launch, then the row copy launched as its programmatic dependent; at
+up to 16,384 top-k ids, as in the small-batch rows, one kernel) + mp_combine
+(launched as the dispatch's programmatic dependent) on the DeepSeek-V3-shaped workload
 (R=8 logical ranks x N=4096 tokens, H=7168 bf16, E=256 experts, top-8 uniform
 routing), the combine input being synthetic expert outputs, one bf16 row per
 receive row, in a buffer of their own.  Inputs are synthetic and
