@@ -518,6 +518,7 @@ FUSED = [(1, 100, 4, 2, 64), (3, 300, 12, 3, 264), (8, 1000, 64, 8, 520), (16, 1
          (4, 257, 4, 2, 64),     # one expert per rank
          (3, 1, 6, 2, 64),       # a single token per rank
          (32, 300, 8192, 8, 16),  # the largest expert count: 32 KB of histogram per block
+         (8, 64, 8192, 8, 64),    # few ids, but too many experts for the one-kernel form's tables
          (8, 20000, 32, 4, 16),  # more tiles than blocks, so blocks own several
          (32, 50, 64, 32, 16)]   # the largest rank count and top-k
 
