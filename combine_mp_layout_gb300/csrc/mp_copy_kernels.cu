@@ -1761,7 +1761,7 @@ static cudaError_t ll_dispatch_fused_nw(LLFusedArgs a, cudaStream_t stream) {
   a.stage_bytes = uint32_t(stage);
   const size_t smem = stage + 16 + table;
   auto kernel = mp_k_ll_dispatch_fused<NW, RANK_MAJOR, BULK, QF>;
-  static int configured[64] = {0};
+  static thread_local int configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > 48 * 1024 && configured[dev] < int(smem)) {
@@ -2212,7 +2212,7 @@ static cudaError_t layout_dispatch_fused_nw(HTFusedArgs a, cudaStream_t stream) 
   a.tmax = int(tmax);
   const size_t smem = stage + 16 + table;
   auto kernel = mp_k_layout_dispatch_fused<NW, BULK, NT>;
-  static int configured[64] = {0};
+  static thread_local int configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > 48 * 1024 && configured[dev] < int(smem)) {
